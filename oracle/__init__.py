@@ -1,0 +1,132 @@
+"""CPU oracle for the gated delta-rule scan -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It wraps ``gdn_ref.c`` (plain sequential
+float64 C, built with gcc into ``oracle/_build/``) through ctypes.  It does not
+import, link or share anything with the CUDA library.
+
+Pins: every function here is checked in ``tests/test_oracle.py`` against facts
+fixed independently of it -- a worked example printed on the onnxruntime-ep-mlx
+ssm.rs page (``tests/golden/``), closed forms, invariants and a brute-force
+product of transition matrices.  None is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdn_ref.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libgdn_ref.so")
+
+RULES = {"gated_delta": 0, "delta": 1, "gated": 2, "linear": 3}
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math, no FMA contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or \
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+                        "-pthread", _SRC, "-o", tmp, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        D = ctypes.POINTER(ctypes.c_double)
+        I64 = ctypes.POINTER(ctypes.c_int64)
+        lib.gdn_ref_scan.restype = ctypes.c_int
+        lib.gdn_ref_scan.argtypes = [
+            ctypes.c_int64, I64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+            ctypes.c_int32, D, D, D, D, D, D, D, D, D, D, ctypes.c_double,
+            ctypes.c_int32, I64, ctypes.c_int64, ctypes.c_int32, D, D]
+        for name in ("gdn_ref_softplus", "gdn_ref_sigmoid"):
+            getattr(lib, name).restype = ctypes.c_double
+            getattr(lib, name).argtypes = [ctypes.c_double]
+        lib.gdn_ref_decay.restype = ctypes.c_double
+        lib.gdn_ref_decay.argtypes = [ctypes.c_double] * 3
+        _lib = lib
+    return _lib
+
+
+def _ptr(x: Optional[np.ndarray], ctype=ctypes.c_double):
+    if x is None:
+        return None
+    return x.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _f64(x) -> Optional[np.ndarray]:
+    if x is None:
+        return None
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64).reshape(-1))
+
+
+def softplus(x: float) -> float:
+    return _load().gdn_ref_softplus(float(x))
+
+
+def sigmoid(x: float) -> float:
+    return _load().gdn_ref_sigmoid(float(x))
+
+
+def decay(a: float, A_log: float, dt_bias: float) -> float:
+    """g = -exp(A_log) * softplus(a + dt_bias)."""
+    return _load().gdn_ref_decay(float(a), float(A_log), float(dt_bias))
+
+
+def scan(cu_seqlens: Sequence[int], h_qk: int, h_v: int, d_k: int, d_v: int,
+         q, k, v, a=None, b=None, A_log=None, dt_bias=None, g=None, beta=None,
+         state_in=None, scale: Optional[float] = None, rule: str = "gated_delta",
+         units: Optional[Sequence[int]] = None, threads: int = 1):
+    """Run the recurrence over packed tokens.
+
+    q, k: [T_total, h_qk, d_k]; v: [T_total, h_v, d_v]; a, b, g, beta: [T_total, h_v];
+    A_log, dt_bias: [h_v]; state_in: [n_seq, h_v, d_k, d_v] or None.
+    If ``a`` is None the gates are ``g`` (log-space, None = 0) and ``beta``
+    (None = 1).  ``scale`` None means 1/sqrt(d_k).  ``units`` restricts the run
+    to the listed (n * h_v + h) units; other rows of the outputs stay zero.
+    Returns (o [T_total, h_v, d_v], state_out [n_seq, h_v, d_k, d_v]) in float64.
+    """
+    lib = _load()
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
+    n_seq = len(cu) - 1
+    total = int(cu[-1]) if n_seq >= 0 and len(cu) else 0
+    if scale is None or scale == 0.0:
+        scale = 1.0 / np.sqrt(d_k)
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    a, b, A_log, dt_bias = _f64(a), _f64(b), _f64(A_log), _f64(dt_bias)
+    g, beta, state_in = _f64(g), _f64(beta), _f64(state_in)
+    assert q.size == total * h_qk * d_k and k.size == q.size
+    assert v.size == total * h_v * d_v
+    o = np.zeros(total * h_v * d_v, dtype=np.float64)
+    s_out = np.zeros(max(n_seq, 0) * h_v * d_k * d_v, dtype=np.float64)
+    ulist = None if units is None else np.ascontiguousarray(np.asarray(units, dtype=np.int64))
+    rc = lib.gdn_ref_scan(
+        n_seq, _ptr(cu, ctypes.c_int64), h_qk, h_v, d_k, d_v, _ptr(q), _ptr(k), _ptr(v),
+        _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(g), _ptr(beta), _ptr(state_in),
+        float(scale), RULES[rule], _ptr(ulist, ctypes.c_int64),
+        0 if ulist is None else len(ulist), int(threads), _ptr(o), _ptr(s_out))
+    if rc != 0:
+        raise ValueError(f"gdn_ref_scan failed with code {rc}")
+    return o.reshape(total, h_v, d_v), s_out.reshape(max(n_seq, 0), h_v, d_k, d_v)
+
+
+def scan_inputs(inp, units=None, threads: int = 1):
+    """Run the oracle on a drawn ``workloads.Inputs`` (the float64 copies)."""
+    s = inp.spec
+    f = inp.f64
+    return scan(inp.cu_seqlens, s.h_qk, s.h_v, s.d_k, s.d_v, f["q"], f["k"], f["v"],
+                a=f["a"], b=f["b"], A_log=f["A_log"], dt_bias=f["dt_bias"],
+                state_in=f["state_in"], scale=inp.scale, units=units, threads=threads)

@@ -1,0 +1,324 @@
+"""Pins for the CPU oracle: each test checks it against something other than itself.
+
+CPU only (no GPU marker).  The pins come from the pages and from mathematics:
+the worked example printed on the onnxruntime-ep-mlx ssm.rs page, closed forms
+for special gates and rules, a retrieval invariant of the delta rule, a
+brute-force product of per-token transition matrices, library routines for the
+gate functions, and the float64 chunked re-association the GPU prefill uses.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import workloads
+from chunked_ref import chunked_unit
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand_unit(rng, T, H, d):
+    x = rng.standard_normal((T, H, d))
+    return x / np.linalg.norm(x, axis=-1, keepdims=True)
+
+
+def _rel(a, b):
+    a, b = np.asarray(a), np.asarray(b)
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300))
+
+
+# ---------------------------------------------------------------- worked example
+
+def test_worked_example_from_page(oracle_mod):
+    """onnxruntime-ep-mlx ssm.rs unit test: linear rule, q = k = e0, v = 1/256."""
+    import torch
+    with open(os.path.join(GOLDEN, "linear_worked_example.json")) as f:
+        fx = json.load(f)
+    stored = fx["printed"]["state_bf16_after_T_steps"]
+    for case in fx["cases"]:
+        dk, T = case["d_k"], case["T"]
+        q = np.zeros((T, 1, dk)); q[:, 0, 0] = 1.0
+        v = np.full((T, 1, 1), 1.0 / 256.0)
+        s0 = np.zeros((1, 1, dk, 1)); s0[0, 0, 0, 0] = 1.0
+        o, s = oracle_mod.scan([0, T], 1, 1, dk, 1, q, q, v, state_in=s0, scale=1.0,
+                               rule="linear")
+        assert o.reshape(-1).tolist() == case["o"]              # exact, as printed
+        # The page stores its state in bf16: round ours the same way.
+        s_bf16 = torch.tensor(s.reshape(-1)).to(torch.bfloat16).to(torch.float64).numpy()
+        assert s_bf16[0] == stored[str(T)]
+        assert np.all(s_bf16[1:] == 0.0)
+        assert s.reshape(-1)[0] == 1.0 + T / 256.0              # wide working state
+
+
+# ---------------------------------------------------------------- gates
+
+def test_gate_functions_against_library(oracle_mod):
+    from scipy.special import expit
+    xs = [-800.0, -50.0, -30.0, -3.5, -1.0, -1e-9, 0.0, 1e-9, 0.7, 2.0, 30.0, 50.0, 800.0]
+    for x in xs:
+        assert oracle_mod.sigmoid(x) == pytest.approx(float(expit(x)), rel=1e-15, abs=1e-300)
+        assert oracle_mod.softplus(x) == pytest.approx(float(np.logaddexp(0.0, x)), rel=1e-15)
+        # Identities: softplus(x) - softplus(-x) = x; sigmoid(x) + sigmoid(-x) = 1.
+        assert oracle_mod.softplus(x) - oracle_mod.softplus(-x) == pytest.approx(x, abs=1e-12)
+        assert oracle_mod.sigmoid(x) + oracle_mod.sigmoid(-x) == pytest.approx(1.0, abs=1e-15)
+    assert oracle_mod.softplus(0.0) == math.log(2.0)
+    assert oracle_mod.sigmoid(0.0) == 0.5
+    assert oracle_mod.sigmoid(-math.inf) == 0.0 and oracle_mod.sigmoid(math.inf) == 1.0
+    # g = -exp(A_log) softplus(a + dt_bias)
+    assert oracle_mod.decay(0.0, 0.0, 0.0) == -math.log(2.0)
+    assert oracle_mod.decay(0.25, math.log(3.0), -0.25) == pytest.approx(-3 * math.log(2.0), rel=1e-15)
+    assert oracle_mod.decay(5.0, -math.inf, 1.0) == 0.0
+    assert oracle_mod.decay(-60.0, 0.0, 0.0) == pytest.approx(-math.exp(-60.0), rel=1e-12)
+
+
+def test_gates_end_to_end_half_decay_and_half_beta(oracle_mod):
+    """A_log = 0, a + dt_bias = 0 gives alpha = 1/2; b = 0 gives beta = 1/2."""
+    rng = np.random.default_rng(1)
+    dk, dv = 8, 5
+    q = _rand_unit(rng, 1, 1, dk)
+    s0 = rng.standard_normal((1, 1, dk, dv))
+    # k = 0: nothing is written, so S1 = alpha S0 and o = scale alpha S0^T q.
+    o, s = oracle_mod.scan([0, 1], 1, 1, dk, dv, q, np.zeros((1, 1, dk)),
+                           rng.standard_normal((1, 1, dv)), a=[0.3], b=[0.0], A_log=[0.0],
+                           dt_bias=[-0.3], state_in=s0, scale=1.0)
+    assert _rel(s, 0.5 * s0) < 1e-15
+    assert _rel(o[0, 0], 0.5 * (s0[0, 0].T @ q[0, 0])) < 1e-14
+    # From zero state with alpha irrelevant: S = beta k v^T, o = beta (q.k) v.
+    k = _rand_unit(rng, 1, 1, dk)
+    v = rng.standard_normal((1, 1, dv))
+    o, s = oracle_mod.scan([0, 1], 1, 1, dk, dv, q, k, v, a=[0.0], b=[0.0], A_log=[0.0],
+                           dt_bias=[0.0], scale=1.0)
+    assert _rel(s[0, 0], 0.5 * np.outer(k[0, 0], v[0, 0])) < 1e-15
+    assert _rel(o[0, 0], 0.5 * (q[0, 0] @ k[0, 0]) * v[0, 0]) < 1e-14
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_invariant_a_no_gate_no_write(oracle_mod):
+    """beta = 0 and g = 0 (b = -inf, A_log = -inf): from a zero state o = 0 and S = 0;
+    from any state, S is unchanged and o_t = scale S0^T q_t."""
+    rng = np.random.default_rng(2)
+    T, H, dk, dv = 6, 2, 16, 12
+    q, k = _rand_unit(rng, T, H, dk), _rand_unit(rng, T, H, dk)
+    v = rng.standard_normal((T, H, dv))
+    a = rng.standard_normal((T, H))
+    b = np.full((T, H), -np.inf)
+    A_log = np.full(H, -np.inf)
+    dt = rng.normal(0, 0.1, H)
+    o, s = oracle_mod.scan([0, T], H, H, dk, dv, q, k, v, a=a, b=b, A_log=A_log, dt_bias=dt)
+    assert np.all(o == 0.0) and np.all(s == 0.0)
+    s0 = rng.standard_normal((1, H, dk, dv))
+    o, s = oracle_mod.scan([0, T], H, H, dk, dv, q, k, v, a=a, b=b, A_log=A_log, dt_bias=dt,
+                           state_in=s0, scale=0.5)
+    assert np.array_equal(s, s0)
+    for t in range(T):
+        for h in range(H):
+            assert _rel(o[t, h], 0.5 * s0[0, h].T @ q[t, h]) < 1e-14
+
+
+def test_invariant_b_linear_rule_is_causal_linear_attention(oracle_mod):
+    """Rule linear with g = 0: o_t = scale sum_{s<=t} (q_t.k_s) v_s (direct O(T^2) sum)."""
+    rng = np.random.default_rng(3)
+    T, H, dk, dv = 40, 2, 16, 24
+    q, k = rng.standard_normal((T, H, dk)), rng.standard_normal((T, H, dk))
+    v = rng.standard_normal((T, H, dv))
+    o, s = oracle_mod.scan([0, T], H, H, dk, dv, q, k, v, scale=0.3, rule="linear")
+    for h in range(H):
+        for t in range(T):
+            ref = 0.3 * sum((q[t, h] @ k[s_, h]) * v[s_, h] for s_ in range(t + 1))
+            assert _rel(o[t, h], ref) < 1e-12
+        assert _rel(s[0, h], sum(np.outer(k[s_, h], v[s_, h]) for s_ in range(T))) < 1e-12
+
+
+def test_gated_rule_is_decayed_linear_attention(oracle_mod):
+    """Rule gated: o_t = scale (e^{G_t} S0^T q_t + sum_{s<=t} e^{G_t-G_s} (q_t.k_s) v_s)."""
+    rng = np.random.default_rng(4)
+    T, dk, dv = 30, 8, 6
+    q, k = rng.standard_normal((T, 1, dk)), rng.standard_normal((T, 1, dk))
+    v = rng.standard_normal((T, 1, dv))
+    g = -rng.uniform(0, 0.5, (T, 1))
+    s0 = rng.standard_normal((1, 1, dk, dv))
+    o, _ = oracle_mod.scan([0, T], 1, 1, dk, dv, q, k, v, g=g, state_in=s0, scale=1.0,
+                           rule="gated")
+    G = np.cumsum(g[:, 0])
+    for t in range(T):
+        ref = np.exp(G[t]) * s0[0, 0].T @ q[t, 0]
+        ref = ref + sum(np.exp(G[t] - G[s_]) * (q[t, 0] @ k[s_, 0]) * v[s_, 0]
+                        for s_ in range(t + 1))
+        assert _rel(o[t, 0], ref) < 1e-12
+
+
+def test_invariant_c_delta_rule_retrieval(oracle_mod):
+    """beta = 1, unit keys, g = 0: after writing (k1,v1), (k2 _|_ k1, v2), (k1,v3),
+    reading with k1 returns v3 and reading with k2 returns v2."""
+    rng = np.random.default_rng(5)
+    dk, dv = 16, 10
+    k1 = rng.standard_normal(dk); k1 /= np.linalg.norm(k1)
+    k2 = rng.standard_normal(dk); k2 -= (k2 @ k1) * k1; k2 /= np.linalg.norm(k2)
+    v1, v2, v3 = rng.standard_normal((3, dv))
+    ks = np.stack([k1, k2, k1, k1, k2])[:, None, :]
+    vs = np.stack([v1, v2, v3, np.zeros(dv), np.zeros(dv)])[:, None, :]
+    # Tokens 4 and 5 read with q = k1, k2; beta = 0 there so they write nothing.
+    qs = ks.copy()
+    b = np.array([np.inf, np.inf, np.inf, -np.inf, -np.inf])[:, None]
+    o, s = oracle_mod.scan([0, 5], 1, 1, dk, dv, qs, ks, vs, a=np.zeros((5, 1)), b=b,
+                           A_log=[-np.inf], dt_bias=[0.0], scale=1.0)
+    assert np.max(np.abs(o[3, 0] - v3)) < 1e-14
+    assert np.max(np.abs(o[4, 0] - v2)) < 1e-14
+    assert np.max(np.abs(o[2, 0] - v3)) < 1e-14     # readout uses the updated state
+    assert np.max(np.abs(s[0, 0].T @ k1 - v3)) < 1e-14
+
+
+def _transition_bruteforce(q, k, v, g, beta, S0, scale):
+    """S_t = A_t ... A_1 S0 + sum_s A_t ... A_{s+1} beta_s k_s v_s^T with
+    A_t = e^{g_t} (I - beta_t k_t k_t^T); o_t = scale S_t^T q_t."""
+    T, dk = k.shape
+    A = [np.exp(g[t]) * (np.eye(dk) - beta[t] * np.outer(k[t], k[t])) for t in range(T)]
+
+    def phi(t, s):          # A_t A_{t-1} ... A_{s+1}  (0-based t, s exclusive)
+        M = np.eye(dk)
+        for r in range(s + 1, t + 1):
+            M = A[r] @ M
+        return M
+
+    o = []
+    S = None
+    for t in range(T):
+        S = phi(t, -1) @ S0
+        for s in range(t + 1):
+            S = S + phi(t, s) @ (beta[s] * np.outer(k[s], v[s]))
+        o.append(scale * S.T @ q[t])
+    return np.array(o), S
+
+
+@pytest.mark.parametrize("T", [1, 2, 5, 8])
+def test_invariant_d_bruteforce(oracle_mod, T):
+    """Random gates, GQA (2 value heads per q/k head), d_k != d_v, a nonzero state."""
+    rng = np.random.default_rng(10 + T)
+    h_qk, h_v, dk, dv = 2, 4, 6, 5
+    q, k = _rand_unit(rng, T, h_qk, dk), _rand_unit(rng, T, h_qk, dk)
+    v = rng.standard_normal((T, h_v, dv))
+    g = -rng.uniform(0.0, 1.5, (T, h_v))
+    beta = rng.uniform(0.0, 1.0, (T, h_v))
+    s0 = rng.standard_normal((1, h_v, dk, dv))
+    o, s = oracle_mod.scan([0, T], h_qk, h_v, dk, dv, q, k, v, g=g, beta=beta, state_in=s0,
+                           scale=0.7)
+    for h in range(h_v):
+        hq = h // (h_v // h_qk)
+        ob, sb = _transition_bruteforce(q[:, hq], k[:, hq], v[:, h], g[:, h], beta[:, h],
+                                        s0[0, h], 0.7)
+        assert _rel(o[:, h], ob) < 1e-12
+        assert _rel(s[0, h], sb) < 1e-12
+
+
+def test_delta_rule_equals_gated_delta_with_zero_decay(oracle_mod):
+    rng = np.random.default_rng(6)
+    T, dk, dv = 12, 8, 8
+    q, k = _rand_unit(rng, T, 1, dk), _rand_unit(rng, T, 1, dk)
+    v = rng.standard_normal((T, 1, dv))
+    beta = rng.uniform(0, 1, (T, 1))
+    o1, s1 = oracle_mod.scan([0, T], 1, 1, dk, dv, q, k, v, beta=beta, rule="delta",
+                             g=-np.ones((T, 1)))
+    o2, s2 = oracle_mod.scan([0, T], 1, 1, dk, dv, q, k, v, beta=beta, g=np.zeros((T, 1)))
+    assert np.array_equal(o1, o2) and np.array_equal(s1, s2)
+
+
+# ---------------------------------------------------------------- composition, edges
+
+def test_composition_chaining_varlen_and_gqa(oracle_mod):
+    spec = workloads.small_spec(io="bf16", lengths=[37, 0, 64, 101], h_qk=2, h_v=4, d_k=16,
+                                d_v=8, seed=21, state_std=0.05)
+    inp = workloads.draw(spec)
+    o, s = oracle_mod.scan_inputs(inp)
+    f = inp.f64
+    cu = inp.cu_seqlens
+    hq, hv, dk, dv = spec.h_qk, spec.h_v, spec.d_k, spec.d_v
+    q, k = f["q"].reshape(-1, hq, dk), f["k"].reshape(-1, hq, dk)
+    v = f["v"].reshape(-1, hv, dv)
+    a, b = f["a"].reshape(-1, hv), f["b"].reshape(-1, hv)
+    s0 = f["state_in"].reshape(-1, hv, dk, dv)
+    kw = dict(A_log=f["A_log"], dt_bias=f["dt_bias"], scale=inp.scale)
+    for n in range(len(cu) - 1):
+        t0, t1 = cu[n], cu[n + 1]
+        sl = slice(t0, t1)
+        # varlen == one call per sequence (bit-identical)
+        o1, s1 = oracle_mod.scan([0, t1 - t0], hq, hv, dk, dv, q[sl], k[sl], v[sl], a=a[sl],
+                                 b=b[sl], state_in=s0[n:n + 1], **kw)
+        assert np.array_equal(o1, o[sl]) and np.array_equal(s1[0], s[n])
+        # chaining: run the first part, then the rest from its state
+        m = t0 + (t1 - t0) // 3
+        oa, sa = oracle_mod.scan([0, m - t0], hq, hv, dk, dv, q[t0:m], k[t0:m], v[t0:m],
+                                 a=a[t0:m], b=b[t0:m], state_in=s0[n:n + 1], **kw)
+        ob, sb = oracle_mod.scan([0, t1 - m], hq, hv, dk, dv, q[m:t1], k[m:t1], v[m:t1],
+                                 a=a[m:t1], b=b[m:t1], state_in=sa, **kw)
+        assert np.array_equal(np.concatenate([oa, ob]), o[sl]) and np.array_equal(sb[0], s[n])
+    # GQA == the same call with each q/k head repeated for its value heads
+    rep = hv // hq
+    o2, s2 = oracle_mod.scan(cu, hv, hv, dk, dv, np.repeat(q, rep, axis=1),
+                             np.repeat(k, rep, axis=1), v, a=a, b=b, state_in=s0, **kw)
+    assert np.array_equal(o2, o) and np.array_equal(s2, s)
+    # A unit subset computes exactly those units
+    units = [1, 6, 13]
+    o3, s3 = oracle_mod.scan_inputs(inp, units=units)
+    for u in units:
+        n, h = divmod(u, hv)
+        assert np.array_equal(s3[n, h], s[n, h])
+        assert np.array_equal(o3[cu[n]:cu[n + 1], h], o[cu[n]:cu[n + 1], h])
+
+
+def test_empty_time_axis_keeps_state(oracle_mod):
+    rng = np.random.default_rng(8)
+    s0 = rng.standard_normal((2, 3, 4, 5))
+    e = np.zeros((0,))
+    o, s = oracle_mod.scan([0, 0, 0], 3, 3, 4, 5, e, e, e, a=e, b=e, A_log=np.zeros(3),
+                           dt_bias=np.zeros(3), state_in=s0)
+    assert o.shape == (0, 3, 5) and np.array_equal(s, s0)
+    o, s = oracle_mod.scan([0, 0], 3, 3, 4, 5, e, e, e, a=e, b=e, A_log=np.zeros(3),
+                           dt_bias=np.zeros(3))
+    assert np.all(s == 0.0)
+
+
+def test_threads_do_not_change_results(oracle_mod):
+    inp = workloads.draw(workloads.small_spec(lengths=[50, 70, 3], h_qk=2, h_v=2, d_k=16,
+                                              d_v=16, seed=9))
+    o1, s1 = oracle_mod.scan_inputs(inp, threads=1)
+    o2, s2 = oracle_mod.scan_inputs(inp, threads=4)
+    assert np.array_equal(o1, o2) and np.array_equal(s1, s2)
+
+
+# ---------------------------------------------------------------- the chunked algebra
+
+@pytest.mark.parametrize("C,L", [(64, 64), (64, 200), (16, 37), (64, 1), (32, 128)])
+def test_chunked_reassociation_matches_sequential(oracle_mod, C, L):
+    """The WY/UT chunked form the GPU prefill uses equals the recurrence in float64."""
+    spec = workloads.small_spec(io="f32", lengths=[L], h_qk=1, h_v=2, d_k=32, d_v=16,
+                                seed=100 + L, state_std=0.05)
+    inp = workloads.draw(spec)
+    o, s = oracle_mod.scan_inputs(inp)
+    f = inp.f64
+    q, k = f["q"].reshape(L, 1, 32), f["k"].reshape(L, 1, 32)
+    v = f["v"].reshape(L, 2, 16)
+    for h in range(2):
+        g = np.array([oracle_mod.decay(x, f["A_log"][h], f["dt_bias"][h])
+                      for x in f["a"].reshape(L, 2)[:, h]])
+        beta = np.array([oracle_mod.sigmoid(x) for x in f["b"].reshape(L, 2)[:, h]])
+        oc, sc = chunked_unit(q[:, 0], k[:, 0], v[:, h], g, beta,
+                              f["state_in"].reshape(1, 2, 32, 16)[0, h], inp.scale, C)
+        assert _rel(oc, o[:, h]) < 1e-11
+        assert _rel(sc, s[0, h]) < 1e-11
+
+
+def test_workload_recipe():
+    """The measured workloads' shapes and draws (c3's lengths are drawn first)."""
+    w = workloads.WORKLOADS
+    assert set(w) == {"tiny_f32_prefill", "bf16_prefill_t4096", "bf16_decode_b256",
+                      "varlen_bf16_prefill", "gqa_f16_prefill"}
+    rng = np.random.default_rng(1003)
+    lengths = rng.integers(512, 8193, 8)
+    assert np.all((lengths >= 512) & (lengths <= 8192))
+    inp = workloads.draw(workloads.small_spec(io="bf16", lengths=[3, 4], h_qk=1, h_v=1,
+                                              d_k=64, d_v=8))
+    qn = np.linalg.norm(inp.f64["q"].reshape(-1, 64), axis=-1)
+    assert np.all(np.abs(qn - 1.0) < 1e-2)   # unit norm up to the bf16 cast

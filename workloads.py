@@ -1,0 +1,171 @@
+"""Seeded synthetic inputs for the gated delta-rule scan.
+
+This module is shared by the tests, the benchmark and the CPU oracle's callers.
+It holds none of the method's arithmetic: no gates, no decay, no recurrence.
+It only draws random numbers, L2-normalises q and k per (token, head) as the
+input recipe asks, and rounds the draws once to the I/O dtype.  The oracle is
+then handed the widened float64 copies of exactly those rounded values, and
+the GPU path the rounded tensors themselves, so both see the same bits.
+
+Recipe (one numpy ``default_rng(seed)``, float64 draws in this order):
+  (varlen only: the sequence lengths), q, k, v, a, b, A_log, dt_bias, state_in.
+  q, k ~ N(0, 1) then divided by their L2 norm over d_k; v, a, b ~ N(0, 1);
+  A_log ~ U(-1, 1) and dt_bias ~ N(0, 0.1) per value head (fp32);
+  state_in ~ N(0, state_std) fp32 when the workload asks for one (std, not
+  variance), else no draw and a zero state.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+_TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+
+
+@dataclasses.dataclass(frozen=True)
+class Spec:
+    """Shape and distribution of one synthetic workload."""
+    name: str
+    io: str                      # "f32" | "bf16" | "f16": q,k,v,a,b,o dtype
+    h_qk: int
+    h_v: int
+    d_k: int
+    d_v: int
+    seed: int
+    batch: int = 1               # B for batched (non-varlen) input
+    seqlen: int = 0              # T per sequence for batched input
+    lengths: Optional[Sequence[int]] = None   # explicit varlen lengths
+    varlen_range: Optional[tuple] = None      # (lo, hi) inclusive, drawn first
+    n_varlen: int = 0
+    state_std: float = 0.0       # 0 -> zero initial state (state_in = None)
+    decode: bool = False         # one token per sequence, state updated in place
+    qk_scale: float = 1.0        # multiplies q,k after normalisation (tests only)
+
+
+# The five workloads the method is measured on.
+WORKLOADS = {
+    "tiny_f32_prefill": Spec(
+        "tiny_f32_prefill", io="f32", batch=1, seqlen=64, h_qk=2, h_v=2,
+        d_k=32, d_v=32, seed=1000),
+    "bf16_prefill_t4096": Spec(
+        "bf16_prefill_t4096", io="bf16", batch=1, seqlen=4096, h_qk=16, h_v=16,
+        d_k=128, d_v=128, seed=1001),
+    "bf16_decode_b256": Spec(
+        "bf16_decode_b256", io="bf16", batch=256, seqlen=1, h_qk=32, h_v=32,
+        d_k=128, d_v=128, seed=1002, state_std=0.05, decode=True),
+    "varlen_bf16_prefill": Spec(
+        "varlen_bf16_prefill", io="bf16", h_qk=16, h_v=16, d_k=128, d_v=128,
+        seed=1003, varlen_range=(512, 8192), n_varlen=8, state_std=0.05),
+    "gqa_f16_prefill": Spec(
+        "gqa_f16_prefill", io="f16", batch=2, seqlen=8192, h_qk=16, h_v=32,
+        d_k=128, d_v=128, seed=1004),
+}
+
+
+@dataclasses.dataclass
+class Inputs:
+    """One drawn workload.  Torch tensors live on the CPU in their final dtype;
+    ``f64`` holds float64 copies (widened from those exact values) for the oracle."""
+    spec: Spec
+    cu_seqlens: np.ndarray        # int64 [n_seq+1] token offsets into the packed axis
+    q: torch.Tensor               # [B, T, h_qk, d_k] (varlen: B=1, T=total)
+    k: torch.Tensor
+    v: torch.Tensor               # [B, T, h_v, d_v]
+    a: torch.Tensor               # [B, T, h_v]
+    b: torch.Tensor
+    A_log: torch.Tensor           # [h_v] fp32
+    dt_bias: torch.Tensor         # [h_v] fp32
+    state_in: Optional[torch.Tensor]   # [n_seq, h_v, d_k, d_v] fp32 or None
+    scale: float
+    f64: dict
+
+    @property
+    def n_seq(self) -> int:
+        return len(self.cu_seqlens) - 1
+
+    @property
+    def total_tokens(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+    @property
+    def varlen(self) -> bool:
+        return self.spec.lengths is not None or self.spec.varlen_range is not None
+
+    def lengths(self) -> np.ndarray:
+        return np.diff(self.cu_seqlens)
+
+
+def _round(x: np.ndarray, io: str) -> torch.Tensor:
+    """Round float64 draws once, to nearest even, into the given dtype."""
+    return torch.from_numpy(np.ascontiguousarray(x)).to(_TORCH_DTYPE[io])
+
+
+def _widen(t: torch.Tensor) -> np.ndarray:
+    return t.to(torch.float64).numpy().reshape(-1)
+
+
+def _l2_normalise(x: np.ndarray) -> np.ndarray:
+    n = np.sqrt(np.sum(x * x, axis=-1, keepdims=True))
+    return x / np.where(n == 0.0, 1.0, n)
+
+
+def draw(spec: Spec) -> Inputs:
+    """Draw the inputs of ``spec`` with its seed, in the recipe's order."""
+    rng = np.random.default_rng(spec.seed)
+    if spec.varlen_range is not None:
+        lo, hi = spec.varlen_range
+        lengths = rng.integers(lo, hi + 1, spec.n_varlen)
+    elif spec.lengths is not None:
+        lengths = np.asarray(spec.lengths, dtype=np.int64)
+    else:
+        lengths = None
+    if lengths is not None:
+        B, T = 1, int(np.sum(lengths))
+        cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    else:
+        B, T = spec.batch, spec.seqlen
+        cu = np.arange(B + 1, dtype=np.int64) * T
+    n_seq = len(cu) - 1
+
+    q = _l2_normalise(rng.standard_normal((B, T, spec.h_qk, spec.d_k))) * spec.qk_scale
+    k = _l2_normalise(rng.standard_normal((B, T, spec.h_qk, spec.d_k))) * spec.qk_scale
+    v = rng.standard_normal((B, T, spec.h_v, spec.d_v))
+    a = rng.standard_normal((B, T, spec.h_v))
+    b = rng.standard_normal((B, T, spec.h_v))
+    A_log = rng.uniform(-1.0, 1.0, spec.h_v)
+    dt_bias = rng.normal(0.0, 0.1, spec.h_v)
+    state = None
+    if spec.state_std > 0.0:
+        state = rng.normal(0.0, spec.state_std, (n_seq, spec.h_v, spec.d_k, spec.d_v))
+
+    tq, tk, tv = _round(q, spec.io), _round(k, spec.io), _round(v, spec.io)
+    ta, tb = _round(a, spec.io), _round(b, spec.io)
+    tA, tdt = _round(A_log, "f32"), _round(dt_bias, "f32")
+    ts = None if state is None else _round(state, "f32")
+    f64 = {
+        "q": _widen(tq), "k": _widen(tk), "v": _widen(tv),
+        "a": _widen(ta), "b": _widen(tb),
+        "A_log": _widen(tA), "dt_bias": _widen(tdt),
+        "state_in": None if ts is None else _widen(ts),
+    }
+    return Inputs(spec=spec, cu_seqlens=cu, q=tq, k=tk, v=tv, a=ta, b=tb,
+                  A_log=tA, dt_bias=tdt, state_in=ts,
+                  scale=1.0 / math.sqrt(spec.d_k), f64=f64)
+
+
+def workload(name: str) -> Inputs:
+    return draw(WORKLOADS[name])
+
+
+def small_spec(name="small", io="bf16", batch=1, seqlen=0, lengths=None, h_qk=2,
+               h_v=2, d_k=128, d_v=128, seed=7, state_std=0.0, decode=False,
+               qk_scale=1.0) -> Spec:
+    """A test-sized workload with the same distributions as the measured ones."""
+    return Spec(name=name, io=io, batch=batch, seqlen=seqlen,
+                lengths=None if lengths is None else tuple(int(x) for x in lengths),
+                h_qk=h_qk, h_v=h_v, d_k=d_k, d_v=d_v, seed=seed,
+                state_std=state_std, decode=decode, qk_scale=qk_scale)
