@@ -1,0 +1,443 @@
+#!/usr/bin/env python
+"""Benchmark of the gated delta-rule scan on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one gdn_prefill call over one batch of the named synthetic workload
+(default: bf16 prefill, B=1, H=16, d_k=d_v=128, T=4096), inputs resident in
+HBM, L2 flushed (256 MiB write) before every step and outside its timing.
+Each GPU (torchrun rank) runs its own full copy of the workload: the units
+(sequence, head) are independent, so there is no collective on the data path
+and scaling is weak.  `--impl reference` times the CPU oracle on host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "gated-delta-rule tokens/s (prefill) & state GB/s (decode), % of roofline"
+DEFAULT_WORKLOAD = "bf16_prefill_t4096"
+CHUNK = 64                         # tokens per chunk of the tensor-core prefill
+FLUSH_BYTES = 256 << 20            # > 129 MB L2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------- accounting
+
+def io_bytes(inp) -> dict:
+    s = inp.spec
+    es = 4 if s.io == "f32" else 2
+    T = inp.total_tokens
+    n = inp.n_seq
+    st = n * s.h_v * s.d_k * s.d_v * 4
+    return {
+        "q": T * s.h_qk * s.d_k * es, "k": T * s.h_qk * s.d_k * es, "v": T * s.h_v * s.d_v * es,
+        "a": T * s.h_v * es, "b": T * s.h_v * es, "params": 2 * s.h_v * 4,
+        "state_in": st if inp.state_in is not None else 0,
+        "o": T * s.h_v * s.d_v * es, "state_out": st,
+    }
+
+
+def algorithmic_bytes(inp) -> int:
+    """Minimum HBM traffic of one call: every input read once, every output written once."""
+    return int(sum(io_bytes(inp).values()))
+
+
+def algorithmic_flops(inp) -> float:
+    """Chunked prefill, C = 64, per (token, value head): 10*C*d + 6*d^2, with the
+    q.k and k.k chunk products (4*C*d) counted once per q/k head.  Decode: 8*d_k*d_v."""
+    s = inp.spec
+    T = inp.total_tokens
+    if s.decode:
+        return 8.0 * T * s.h_v * s.d_k * s.d_v
+    d = s.d_k
+    return T * s.h_v * (6.0 * CHUNK * d + 6.0 * d * s.d_v) + T * s.h_qk * 4.0 * CHUNK * d
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return {k: float(m[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "recurrent_state_scan_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
+    or None when there is none or the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.startswith("- "):
+                k, v = line[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha256") != source_digest():
+        return None
+    try:
+        return int(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.strip()]
+        os.unlink(self.out.name)
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                mx = float(r[1])
+                for name, val in zip(names, r[3:7]):
+                    if val.strip().lower() == "active":
+                        reasons.add(name)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def time_oracle(inp, budget_s: float, min_reps: int = 1):
+    """Run the oracle over the whole workload repeatedly for about budget_s seconds."""
+    import oracle
+    threads = cpu_threads()
+    oracle.build()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.scan_inputs(inp, threads=threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if reps >= min_reps and el >= budget_s:
+            break
+        if el > 0 and reps >= min_reps and el / reps * (reps + 1) > 3 * budget_s:
+            break
+    return el / reps, reps, threads
+
+
+def units_per_step(inp):
+    return inp.total_tokens
+
+
+def cpu_baseline_line(inp, budget_s=10.0):
+    per, reps, threads = time_oracle(inp, budget_s)
+    s = inp.spec
+    if s.decode:
+        val, unit = algorithmic_bytes(inp) / per / 1e9, "GB/s"
+    else:
+        val, unit = units_per_step(inp) / per, "tokens/s"
+    return {"value": val, "unit": unit, "cores": threads, "kind": "oracle",
+            "sample": f"the whole {s.name} workload x{reps} through the float64 C oracle "
+                      f"({threads} threads over (sequence, head) units), {per * reps:.1f} s"}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local):
+    from recurrent_state_scan_gb300 import gdn_decode_step, gdn_prefill, load
+    load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = workloads.workload(args.workload)
+    s = inp.spec
+    t = {n: getattr(inp, n).to(dev) for n in ("q", "k", "v", "a", "b", "A_log", "dt_bias")}
+    state0 = None if inp.state_in is None else inp.state_in.to(dev)
+    cu = torch.tensor(inp.cu_seqlens, dtype=torch.int32, device=dev) if inp.varlen else None
+    o = torch.empty(t["v"].shape, dtype=t["v"].dtype, device=dev)
+    n_state = (inp.n_seq, s.h_v, s.d_k, s.d_v)
+    state_out = torch.empty(n_state, dtype=torch.float32, device=dev)
+    work_state = None if state0 is None else state0.clone()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        if s.decode:
+            gdn_decode_step(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"], t["dt_bias"],
+                            work_state, inp.scale, o=o, stream=stream)
+        else:
+            gdn_prefill(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"], t["dt_bias"],
+                        state0, cu, inp.scale, o=o, state_out=state_out, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    times_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms = max_over_ranks(float(np.mean(times_ms)), world)
+
+    # End to end through the public API: pinned host inputs -> device -> call -> host.
+    e2e = None
+    if not args.no_e2e:
+        host = {n: v.pin_memory() for n, v in
+                [("q", inp.q), ("k", inp.k), ("v", inp.v), ("a", inp.a), ("b", inp.b),
+                 ("A_log", inp.A_log), ("dt_bias", inp.dt_bias)] +
+                ([("state", inp.state_in)] if inp.state_in is not None else [])}
+        o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        s_host = torch.empty(n_state, dtype=torch.float32).pin_memory()
+        dbuf = {n: torch.empty_like(v, device=dev) for n, v in host.items()}
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = o_host.numel() * o_host.element_size() + s_host.numel() * 4
+
+        def e2e_step():
+            for n, v in host.items():
+                dbuf[n].copy_(v, non_blocking=True)
+            if s.decode:
+                gdn_decode_step(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["a"], dbuf["b"],
+                                dbuf["A_log"], dbuf["dt_bias"], dbuf["state"], inp.scale, o=o,
+                                stream=stream)
+                s_host.copy_(dbuf["state"], non_blocking=True)
+            else:
+                gdn_prefill(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["a"], dbuf["b"], dbuf["A_log"],
+                            dbuf["dt_bias"], dbuf.get("state"), cu, inp.scale, o=o,
+                            state_out=state_out, stream=stream)
+                s_host.copy_(state_out, non_blocking=True)
+            o_host.copy_(o, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier(world)
+        for i in range(args.steps):
+            flush.zero_()
+            es[i].record(stream)
+            e2e_step()
+            ee[i].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        ems = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in zip(es, ee)])), world)
+        e2e = {"ms_per_step": ems, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    return inp, ms, times_ms, clocks, e2e
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_init()
+    inp_name = args.workload
+    if args.impl == "reference":
+        # The reference arm is the CPU oracle, timed as it stands, on rank 0 only.
+        if rank != 0:
+            return
+        inp = workloads.workload(inp_name)
+        s = inp.spec
+        for _ in range(args.warmup):
+            time_oracle(inp, 0.0)
+        per, reps, threads = time_oracle(inp, 0.0, min_reps=args.steps)
+        if s.decode:
+            value, unit = algorithmic_bytes(inp) / per / 1e9, "GB/s"
+        else:
+            value, unit = inp.total_tokens / per, "tokens/s"
+        line = {
+            "impl": "reference", "metric": METRIC, "value": value, "unit": unit,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(inp, world),
+            "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
+                             "sample": f"the whole {s.name} workload per step, {reps} steps"},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line), flush=True)
+        return
+
+    inp, ms, times_ms, clocks, e2e = run_ours(args, rank, world, local)
+    s = inp.spec
+    pk, pk_kind = peaks()
+    nbytes = algorithmic_bytes(inp)
+    flops = algorithmic_flops(inp)
+    sec = ms / 1e3
+    if s.decode:
+        value, unit = world * nbytes / sec / 1e9, "GB/s"
+    else:
+        value, unit = world * inp.total_tokens / sec, "tokens/s"
+    # Roofline of the dominant kernel (one launch per call: the call's device time).
+    gbs = nbytes / sec / 1e9
+    tfs = flops / sec / 1e12
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+    t_tc = flops / (pk["bf16_tflops"] * 1e12)
+    roof = {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": gbs / pk["hbm_gbs"], "traffic": profiled_traffic(inp_name),
+            "peak_source": f"{pk_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+            if pk_kind == "measured" else "fallback 6.8 TB/s"}
+    if not s.decode:
+        roof["tensor_tflops"] = tfs
+        roof["tensor_frac_of_bf16_peak"] = tfs / pk["bf16_tflops"]
+        roof["roofline_time_us"] = max(t_hbm, t_tc) * 1e6
+        roof["frac_of_roofline"] = max(t_hbm, t_tc) / sec
+    line = {
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": dtype_of(inp), "data": "synthetic",
+        "config": config_of(inp, world), "roofline": roof,
+        "gpu_launches": args.steps * launches_per_call(inp),
+    }
+    if e2e is not None:
+        esec = e2e["ms_per_step"] / 1e3
+        ev = world * (nbytes / esec / 1e9 if s.decode else inp.total_tokens / esec)
+        line["e2e"] = {"value": ev, "unit": unit, "ms_per_step": e2e["ms_per_step"],
+                       "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+                       "d2h_bytes_per_step": e2e["d2h_bytes_per_step"]}
+    if clocks is not None:
+        line["clocks"] = clocks
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_line(inp)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def dtype_of(inp) -> str:
+    from recurrent_state_scan_gb300 import gdn
+    return gdn.path_dtype(inp.spec, inp.n_seq, inp.total_tokens)
+
+
+def launches_per_call(inp) -> int:
+    from recurrent_state_scan_gb300 import gdn
+    return gdn.launches_per_call(inp.spec, inp.n_seq, inp.total_tokens)
+
+
+def config_of(inp, world):
+    s = inp.spec
+    c = {"workload": s.name, "io_dtype": s.io, "state_dtype": "f32", "num_seqs": inp.n_seq,
+         "total_tokens": inp.total_tokens, "h_qk": s.h_qk, "h_v": s.h_v, "d_k": s.d_k,
+         "d_v": s.d_v, "initial_state": "N(0,%g)" % s.state_std if s.state_std else "zero",
+         "l2": "flushed before every step (256 MiB write, untimed)",
+         "parallelism": f"replicas: the full workload on each of {world} GPU(s), no collective"}
+    if inp.varlen:
+        c["lengths"] = [int(x) for x in inp.lengths()]
+    else:
+        c["batch"], c["seq_len"] = s.batch, s.seqlen
+    return c
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,138 @@
+/*
+ * gdn.h -- C ABI of libgdn: the gated delta-rule recurrent state scan
+ * (Gated DeltaNet linear attention) on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (onnx-runtime-ep-cuda 0.1.0-dev.6, src/kernels/linear_attention.rs,
+ * `linear_attention_core`, Steps 1-4, and its fused gate chain): for every
+ * sequence n and value head h there is a state S[d_k][d_v] in fp32.  For each
+ * token t of the sequence, in order,
+ *     g_t    = -exp(A_log[h]) * softplus(a[t,h] + dt_bias[h])      (log-space decay)
+ *     beta_t = sigmoid(b[t,h])
+ *     S      = exp(g_t) * S                                        (Step 1, decay)
+ *     r      = S^T k_t                                             (Step 2, retrieval)
+ *     S      = S + k_t (x) beta_t (v_t - r)                        (Step 3, delta update)
+ *     o_t    = scale * S^T q_t      (with the updated S)           (Step 4, readout)
+ * Value head h reads query/key head h / (h_v / h_qk): consecutive value heads
+ * share one q/k head (the GQA mapping of the same page and of nuvec-core 0.6.1,
+ * src/fast/imp.rs, `gated_delta_graph`).
+ *
+ * Conventions for every call below:
+ *  - All tensor pointers are DEVICE pointers to contiguous row-major arrays,
+ *    owned by the caller; the library never allocates, frees or keeps them.
+ *  - Layouts (T = tokens per sequence, or the packed total for varlen):
+ *        q, k   [B, T, h_qk, d_k]   io dtype
+ *        v, o   [B, T, h_v,  d_v]   io dtype
+ *        a, b   [B, T, h_v]         io dtype (raw gate logits)
+ *        A_log, dt_bias [h_v]       fp32
+ *        state  [N, h_v, d_k, d_v]  fp32 (N = number of sequences)
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Calls are asynchronous on that stream; nothing synchronises.
+ *  - Errors found on the host return a status and launch nothing.  Errors only
+ *    the device can see (a malformed device cu_seqlens) set a device check word,
+ *    skip the affected work without faulting, and are reported by
+ *    gdn_last_device_status().
+ *  - gdn_last_error_message() gives a human-readable detail of the last
+ *    non-OK status returned on the calling thread.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,   /* bad shape, null or misaligned pointer, bad size  */
+    GDN_ERR_UNSUPPORTED = 2,   /* valid arguments, geometry not built (d_k > 256)   */
+    GDN_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed              */
+    GDN_ERR_DEVICE_CHECK = 4,  /* the device found malformed cu_seqlens             */
+    GDN_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up                */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1, GDN_F16 = 2 } gdn_dtype;
+
+/* Problem geometry shared by every entry point. */
+typedef struct gdn_shape {
+    int32_t io_dtype;   /* gdn_dtype of q, k, v, a, b and o                          */
+    int32_t batch;      /* B; must be 1 when cu_seqlens is given                       */
+    int64_t seqlen;     /* T per sequence, or the packed token total with cu_seqlens   */
+    int32_t num_seqs;   /* N: equals batch, or len(cu_seqlens) - 1 with cu_seqlens     */
+    int32_t h_qk;       /* query/key heads; h_v % h_qk == 0                            */
+    int32_t h_v;        /* value heads (one state per value head)                      */
+    int32_t d_k;        /* key dim, 1..256 (the tensor-core prefill needs 128)         */
+    int32_t d_v;        /* value dim, 1..256, a multiple of 4                          */
+} gdn_shape;
+
+/*
+ * gdn_prefill -- run the recurrence over whole sequences.
+ *
+ *   q, k, v, a, b  inputs in the layouts above.
+ *   A_log, dt_bias per-value-head gate parameters (fp32 [h_v]).
+ *   state_in       initial states [N, h_v, d_k, d_v] fp32, or NULL for zeros.
+ *   cu_seqlens     NULL for B sequences of length shape->seqlen; else a DEVICE
+ *                  int32 array [N+1] of token offsets into the packed axis
+ *                  (cu[0] = 0, non-decreasing, cu[N] = shape->seqlen).  A
+ *                  sequence whose entries break these rules is skipped and the
+ *                  device check word is set.  Empty sequences are allowed.
+ *   scale          readout scale; 0 means 1/sqrt(d_k).
+ *   o              output [B, T, h_v, d_v] io dtype, written for every token.
+ *   state_out      final states [N, h_v, d_k, d_v] fp32; may alias state_in.
+ *                  A sequence with no tokens gets state_in (zeros if NULL),
+ *                  as the onnxruntime-ep-mlx ssm.rs page does for an empty
+ *                  time axis.
+ *   workspace      device scratch of at least gdn_prefill_workspace_bytes(shape)
+ *                  bytes (may be NULL when that is 0); its contents need no
+ *                  initialisation and are not preserved.
+ *
+ * bf16/f16 I/O with d_k = d_v = 128 runs the chunked tensor-core path; other
+ * shapes and fp32 I/O run the sequential SIMT path.  State math is fp32 always.
+ */
+size_t gdn_prefill_workspace_bytes(const gdn_shape *shape);
+
+gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                       const void *a, const void *b, const float *A_log, const float *dt_bias,
+                       const float *state_in, const int32_t *cu_seqlens, float scale, void *o,
+                       float *state_out, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * gdn_decode_step -- one token per sequence (shape->seqlen must be 1 and
+ * cu_seqlens is not taken): B = shape->batch = shape->num_seqs.  `state`
+ * [B, h_v, d_k, d_v] fp32 is read and overwritten in place with the updated
+ * state.  o [B, 1, h_v, d_v] receives the readout.  Same gates and scale as
+ * gdn_prefill; the result equals gdn_prefill on T = 1.
+ */
+gdn_status gdn_decode_step(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                           const void *a, const void *b, const float *A_log,
+                           const float *dt_bias, float *state, float scale, void *o,
+                           void *stream);
+
+/*
+ * gdn_last_device_status -- synchronise `stream`, read the device check word
+ * set by any earlier call on the current device, clear it, and return GDN_OK or
+ * GDN_ERR_DEVICE_CHECK / GDN_ERR_TIMEOUT.
+ */
+gdn_status gdn_last_device_status(void *stream);
+
+/*
+ * gdn_prefill_plan -- report, without launching anything, which kernel path
+ * gdn_prefill takes for `shape` (*path: 1 = token-sequential SIMT scan,
+ * 2 = chunked tensor-core scan) and how many kernels one call launches
+ * (*launches).  Returns the same status gdn_prefill's shape checks would.
+ */
+gdn_status gdn_prefill_plan(const gdn_shape *shape, int32_t *path, int32_t *launches);
+
+/* Static name of a status code. */
+const char *gdn_status_string(gdn_status status);
+
+/* Detail of the last non-OK status returned on the calling host thread. */
+const char *gdn_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

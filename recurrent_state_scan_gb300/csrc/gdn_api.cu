@@ -1,0 +1,227 @@
+// gdn_api.cu -- the C ABI of libgdn: argument checks, status codes, dispatch.
+//
+// The checks mirror the host validation of onnx-runtime-ep-cuda 0.1.0-dev.6,
+// src/kernels/linear_attention.rs (`LinearAttentionKernel::execute`): shapes,
+// head divisibility, d_k <= 256, pointer presence; bad arguments return
+// GDN_ERR_INVALID_ARG and unbuilt geometry GDN_ERR_UNSUPPORTED, and in both
+// cases nothing is launched.  Unlike that page the calls never synchronise.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "gdn_internal.cuh"
+
+namespace gdn {
+
+// Device check word: kernels OR error bits into it instead of trapping.
+__device__ int g_device_status = 0;
+
+namespace {
+
+thread_local char g_message[512] = "";
+
+gdn_status fail(gdn_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_message, sizeof(g_message), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+gdn_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(GDN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Address of the check word on the current device (looked up once per device).
+gdn_status status_word(int **out) {
+    static int *cache[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(GDN_ERR_UNSUPPORTED, "device ordinal %d >= 64", dev);
+    if (cache[dev] == nullptr) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_device_status);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(check word)");
+        cache[dev] = static_cast<int *>(ptr);
+    }
+    *out = cache[dev];
+    return GDN_OK;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t io_size(int32_t io) { return io == GDN_F32 ? 4 : 2; }
+
+// Shape rules common to both calls.
+gdn_status check_shape(const gdn_shape *s, bool varlen) {
+    if (s == nullptr) return fail(GDN_ERR_INVALID_ARG, "shape is NULL");
+    if (s->io_dtype != GDN_F32 && s->io_dtype != GDN_BF16 && s->io_dtype != GDN_F16)
+        return fail(GDN_ERR_INVALID_ARG, "io_dtype %d is not F32/BF16/F16", s->io_dtype);
+    if (s->seqlen < 0) return fail(GDN_ERR_INVALID_ARG, "seqlen %lld < 0", (long long)s->seqlen);
+    if (s->num_seqs < 0) return fail(GDN_ERR_INVALID_ARG, "num_seqs %d < 0", s->num_seqs);
+    if (varlen) {
+        if (s->batch != 1)
+            return fail(GDN_ERR_INVALID_ARG, "batch must be 1 with cu_seqlens (got %d)", s->batch);
+    } else if (s->batch != s->num_seqs) {
+        return fail(GDN_ERR_INVALID_ARG, "num_seqs (%d) must equal batch (%d)", s->num_seqs,
+                    s->batch);
+    }
+    if (s->h_qk <= 0 || s->h_v <= 0)
+        return fail(GDN_ERR_INVALID_ARG, "head counts must be positive (h_qk %d, h_v %d)",
+                    s->h_qk, s->h_v);
+    if (s->h_v % s->h_qk != 0)
+        return fail(GDN_ERR_INVALID_ARG, "h_v (%d) must be a multiple of h_qk (%d)", s->h_v,
+                    s->h_qk);
+    if (s->d_k <= 0 || s->d_v <= 0)
+        return fail(GDN_ERR_INVALID_ARG, "d_k (%d) and d_v (%d) must be positive", s->d_k, s->d_v);
+    if (s->d_k > 256 || s->d_v > 256)
+        return fail(GDN_ERR_UNSUPPORTED, "d_k (%d) and d_v (%d) above 256 are not built", s->d_k,
+                    s->d_v);
+    if (s->d_v % 4 != 0)
+        return fail(GDN_ERR_UNSUPPORTED, "d_v (%d) must be a multiple of 4", s->d_v);
+    return GDN_OK;
+}
+
+gdn_status check_inputs(const gdn_shape *s, int64_t tokens, const void *q, const void *k,
+                        const void *v, const void *a, const void *b, const float *A_log,
+                        const float *dt_bias, const void *o) {
+    if (tokens > 0) {
+        const void *ptrs[] = {q, k, v, a, b, A_log, dt_bias, o};
+        const char *names[] = {"q", "k", "v", "a", "b", "A_log", "dt_bias", "o"};
+        for (int i = 0; i < 8; ++i)
+            if (ptrs[i] == nullptr) return fail(GDN_ERR_INVALID_ARG, "%s is NULL", names[i]);
+        const size_t es = io_size(s->io_dtype);
+        const void *io_ptrs[] = {q, k, v, a, b, o};
+        for (int i = 0; i < 6; ++i)
+            if (!aligned(io_ptrs[i], es))
+                return fail(GDN_ERR_INVALID_ARG, "pointer is not %zu-byte aligned", es);
+        if (!aligned(A_log, 4) || !aligned(dt_bias, 4))
+            return fail(GDN_ERR_INVALID_ARG, "A_log/dt_bias must be 4-byte aligned");
+    }
+    return GDN_OK;
+}
+
+}  // namespace
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+const char *gdn_status_string(gdn_status st) {
+    switch (st) {
+        case GDN_OK: return "GDN_OK";
+        case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+        case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+        case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+        case GDN_ERR_DEVICE_CHECK: return "GDN_ERR_DEVICE_CHECK";
+        case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
+    }
+    return "GDN_ERR_UNKNOWN";
+}
+
+const char *gdn_last_error_message(void) { return g_message; }
+
+gdn_status gdn_prefill_plan(const gdn_shape *shape, int32_t *path, int32_t *launches) {
+    gdn_status st = check_shape(shape, shape != nullptr && shape->batch == 1 &&
+                                           shape->num_seqs != 1);
+    if (st != GDN_OK) return st;
+    if (path) *path = 1;
+    if (launches) *launches = shape->num_seqs > 0 ? 1 : 0;
+    return GDN_OK;
+}
+
+size_t gdn_prefill_workspace_bytes(const gdn_shape *shape) {
+    (void)shape;
+    return 0;
+}
+
+gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                       const void *a, const void *b, const float *A_log, const float *dt_bias,
+                       const float *state_in, const int32_t *cu_seqlens, float scale, void *o,
+                       float *state_out, void *workspace, size_t workspace_bytes, void *stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    gdn_status st = check_shape(shape, cu_seqlens != nullptr);
+    if (st != GDN_OK) return st;
+    const int64_t tokens = cu_seqlens ? shape->seqlen : shape->seqlen * (int64_t)shape->batch;
+    st = check_inputs(shape, tokens, q, k, v, a, b, A_log, dt_bias, o);
+    if (st != GDN_OK) return st;
+    if (shape->num_seqs == 0) return GDN_OK;
+    if (state_out == nullptr) return fail(GDN_ERR_INVALID_ARG, "state_out is NULL");
+    if (!aligned(state_out, 16) || !aligned(state_in, 16))
+        return fail(GDN_ERR_INVALID_ARG, "state_in/state_out must be 16-byte aligned");
+    if (!(scale == scale) || isinf(scale)) return fail(GDN_ERR_INVALID_ARG, "scale is not finite");
+    int *word = nullptr;
+    st = status_word(&word);
+    if (st != GDN_OK) return st;
+
+    ScanParams p{};
+    p.q = q; p.k = k; p.v = v; p.a = a; p.b = b;
+    p.A_log = A_log; p.dt_bias = dt_bias;
+    p.state_in = state_in; p.state_out = state_out; p.o = o;
+    p.cu_seqlens = cu_seqlens;
+    p.seqlen = shape->seqlen;
+    p.num_seqs = shape->num_seqs;
+    p.h_qk = shape->h_qk; p.h_v = shape->h_v; p.d_k = shape->d_k; p.d_v = shape->d_v;
+    p.scale = scale == 0.0f ? 1.0f / sqrtf((float)shape->d_k) : scale;
+    p.status = word;
+    cudaError_t e = launch_scan_simt(p, (gdn_dtype)shape->io_dtype, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return GDN_OK;
+}
+
+gdn_status gdn_decode_step(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                           const void *a, const void *b, const float *A_log,
+                           const float *dt_bias, float *state, float scale, void *o,
+                           void *stream) {
+    gdn_status st = check_shape(shape, false);
+    if (st != GDN_OK) return st;
+    if (shape->seqlen != 1)
+        return fail(GDN_ERR_INVALID_ARG, "decode takes seqlen 1 (got %lld)", (long long)shape->seqlen);
+    st = check_inputs(shape, shape->batch, q, k, v, a, b, A_log, dt_bias, o);
+    if (st != GDN_OK) return st;
+    if (shape->batch == 0) return GDN_OK;
+    if (state == nullptr) return fail(GDN_ERR_INVALID_ARG, "state is NULL");
+    if (!aligned(state, 16)) return fail(GDN_ERR_INVALID_ARG, "state must be 16-byte aligned");
+    if (!(scale == scale) || isinf(scale)) return fail(GDN_ERR_INVALID_ARG, "scale is not finite");
+    int *word = nullptr;
+    st = status_word(&word);
+    if (st != GDN_OK) return st;
+
+    ScanParams p{};
+    p.q = q; p.k = k; p.v = v; p.a = a; p.b = b;
+    p.A_log = A_log; p.dt_bias = dt_bias;
+    p.state_in = state; p.state_out = state; p.o = o;
+    p.cu_seqlens = nullptr;
+    p.seqlen = 1;
+    p.num_seqs = shape->batch;
+    p.h_qk = shape->h_qk; p.h_v = shape->h_v; p.d_k = shape->d_k; p.d_v = shape->d_v;
+    p.scale = scale == 0.0f ? 1.0f / sqrtf((float)shape->d_k) : scale;
+    p.status = word;
+    cudaError_t e = launch_scan_simt(p, (gdn_dtype)shape->io_dtype, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return GDN_OK;
+}
+
+gdn_status gdn_last_device_status(void *stream) {
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int *word = nullptr;
+    gdn_status st = status_word(&word);
+    if (st != GDN_OK) return st;
+    int value = 0;
+    e = cudaMemcpy(&value, word, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read check word");
+    const int zero = 0;
+    e = cudaMemcpy(word, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "clear check word");
+    if (value & kDevTimeout) return fail(GDN_ERR_TIMEOUT, "a device-side wait timed out");
+    if (value & kDevBadCuSeqlens)
+        return fail(GDN_ERR_DEVICE_CHECK, "cu_seqlens is malformed on the device");
+    return GDN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,86 @@
+// gdn_internal.cuh -- definitions shared by libgdn's translation units.
+//
+// Gate math follows onnx-runtime-ep-cuda 0.1.0-dev.6, src/kernels/linear_attention.rs
+// (`la_softplus`, `la_sigmoid`, the fused decay chain g = -exp(A_log) * softplus(a + dt_bias)),
+// evaluated in fp32 once per token from widened inputs, with no intermediate
+// re-rounding to the I/O dtype (the onnxruntime-ep-mlx ssm.rs gate op computes
+// its gates wide and casts once; here g and beta are never stored at all).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+// Device check word values (OR-ed together by kernels that detect a problem).
+enum : int { kDevOk = 0, kDevBadCuSeqlens = 1, kDevTimeout = 2 };
+
+struct ScanParams {
+    const void *q, *k, *v, *a, *b;
+    const float *A_log, *dt_bias;
+    const float *state_in;   // may be null (zeros); may alias state_out
+    float *state_out;
+    void *o;
+    const int32_t *cu_seqlens;   // device, may be null
+    int64_t seqlen;              // T per sequence, or packed total with cu_seqlens
+    int32_t num_seqs, h_qk, h_v, d_k, d_v;
+    float scale;
+    int *status;                 // device check word
+};
+
+// ------------------------------------------------------------------ I/O types
+template <typename T> struct IoType;
+template <> struct IoType<float> {
+    static __device__ __forceinline__ float ld(const float *p) { return *p; }
+    static __device__ __forceinline__ void st(float *p, float x) { *p = x; }
+};
+template <> struct IoType<__nv_bfloat16> {
+    static __device__ __forceinline__ float ld(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+    static __device__ __forceinline__ void st(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+};
+template <> struct IoType<__half> {
+    static __device__ __forceinline__ float ld(const __half *p) { return __half2float(*p); }
+    static __device__ __forceinline__ void st(__half *p, float x) { *p = __float2half_rn(x); }
+};
+
+// ------------------------------------------------------------------ gates
+// softplus(x) = log(1 + e^x) written as max(x,0) + log1p(e^-|x|) (no overflow).
+__device__ __forceinline__ float softplus_f(float x) {
+    return fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x)));
+}
+// sigmoid(x) = 1/(1+e^-x), split on the sign so the exponential never overflows.
+__device__ __forceinline__ float sigmoid_f(float x) {
+    if (x >= 0.0f) return 1.0f / (1.0f + expf(-x));
+    const float e = expf(x);
+    return e / (1.0f + e);
+}
+// Log-space decay g = -exp(A_log) * softplus(a + dt_bias).
+__device__ __forceinline__ float decay_f(float a, float A_log, float dt_bias) {
+    return -expf(A_log) * softplus_f(a + dt_bias);
+}
+
+// Token range [t0, t1) of sequence n; false (and the check word set) if the
+// device-resident cu_seqlens entries for n are malformed.
+__device__ __forceinline__ bool seq_range(const ScanParams &p, int64_t n, int64_t &t0,
+                                          int64_t &t1) {
+    if (p.cu_seqlens == nullptr) {
+        t0 = n * p.seqlen;
+        t1 = t0 + p.seqlen;
+        return true;
+    }
+    t0 = p.cu_seqlens[n];
+    t1 = p.cu_seqlens[n + 1];
+    const bool ok = (t0 >= 0) && (t0 <= t1) && (t1 <= p.seqlen) && (n != 0 || t0 == 0) &&
+                    (n + 1 != p.num_seqs || t1 == p.seqlen);
+    if (!ok) atomicOr(p.status, kDevBadCuSeqlens);
+    return ok;
+}
+
+// Launchers implemented in the kernel translation units.
+cudaError_t launch_scan_simt(const ScanParams &p, gdn_dtype io, cudaStream_t stream);
+
+}  // namespace gdn

@@ -1,0 +1,188 @@
+// scan_simt.cu -- the token-sequential gated delta-rule scan on FP32 ALUs.
+//
+// Serves gdn_decode_step (one token, state updated in place: the decode hot path)
+// and gdn_prefill for fp32 I/O and for shapes the tensor-core chunked path does not
+// take.  It evaluates, per token, Steps 1-4 of `linear_attention_core`
+// (onnx-runtime-ep-cuda 0.1.0-dev.6, src/kernels/linear_attention.rs): decay,
+// retrieval r = S^T k, delta update S += k (x) beta (v - r), readout o = scale S^T q.
+//
+// Design (GB300-first, not the page's one-thread-per-column / one-warp-per-column):
+//  - One CTA of 256 threads owns the full d_k rows of a tile of 4*LPR state columns
+//    of one (sequence, value head).  The page's "Parallelization" note -- columns
+//    evolve independently -- is what lets a CTA own a column tile.
+//  - A warp-row of LPR lanes covers the tile's columns with one float4 each, so a
+//    warp reads/writes whole 512 B rows of S[d_k][d_v]: fully coalesced 128-bit
+//    accesses.  Each thread keeps RPT rows x 4 columns of S in registers for the
+//    whole scan (fp32), so S is read from HBM once and written once.
+//  - Per token the d_k reductions for both Sk and Sq run in ONE pass over the
+//    registers; the readout uses S'^T q = alpha S^T q + (q.k) delta, which is the
+//    updated-state readout re-associated, so no second pass is needed.
+//  - Cross-row partial sums go through shared memory (three barriers per token).
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <typename IO, int DKMAX, int LPR>
+__global__ void __launch_bounds__(kThreads) scan_simt_kernel(const ScanParams p) {
+    constexpr int RPP = kThreads / LPR;   // rows covered per pass
+    constexpr int RPT = DKMAX / RPP;      // rows held per thread
+    constexpr int TILE = 4 * LPR;         // state columns per CTA
+    static_assert(RPT >= 1 && DKMAX % RPP == 0, "bad tiling");
+
+    __shared__ float sq[DKMAX], sk[DKMAX];
+    __shared__ float sv[TILE], sdelta[TILE];
+    __shared__ __align__(16) float red_k[RPP * TILE];
+    __shared__ __align__(16) float red_q[RPP * TILE];
+    __shared__ float s_alpha, s_beta, s_qk;
+
+    const int tid = threadIdx.x;
+    const int lr = tid % LPR, rg = tid / LPR;
+    const int tiles = (p.d_v + TILE - 1) / TILE;
+    int64_t unit = blockIdx.x;
+    const int tile = (int)(unit % tiles);
+    unit /= tiles;
+    const int h = (int)(unit % p.h_v);
+    const int64_t n = unit / p.h_v;
+    const int hq = h / (p.h_v / p.h_qk);
+    const int col0 = tile * TILE + 4 * lr;
+    const bool col_ok = col0 < p.d_v;   // d_v is a multiple of 4
+
+    int64_t t0, t1;
+    if (!seq_range(p, n, t0, t1)) return;
+
+    const size_t sbase = ((size_t)n * p.h_v + h) * (size_t)p.d_k * p.d_v;
+    float4 S[RPT];
+#pragma unroll
+    for (int m = 0; m < RPT; ++m) {
+        const int i = rg + RPP * m;
+        S[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p.state_in != nullptr && col_ok && i < p.d_k)
+            S[m] = __ldcs(reinterpret_cast<const float4 *>(p.state_in + sbase +
+                                                          (size_t)i * p.d_v + col0));
+    }
+
+    const IO *q = static_cast<const IO *>(p.q);
+    const IO *k = static_cast<const IO *>(p.k);
+    const IO *v = static_cast<const IO *>(p.v);
+    const IO *ga = static_cast<const IO *>(p.a);
+    const IO *gb = static_cast<const IO *>(p.b);
+    IO *o = static_cast<IO *>(p.o);
+    const float A_log = p.A_log[h], dt_bias = p.dt_bias[h];
+
+    for (int64_t t = t0; t < t1; ++t) {
+        __syncthreads();   // previous token's shared values are no longer read
+        const size_t qk_off = ((size_t)t * p.h_qk + hq) * p.d_k;
+        for (int i = tid; i < DKMAX; i += kThreads) {
+            sq[i] = i < p.d_k ? IoType<IO>::ld(q + qk_off + i) : 0.f;
+            sk[i] = i < p.d_k ? IoType<IO>::ld(k + qk_off + i) : 0.f;
+        }
+        const size_t v_off = ((size_t)t * p.h_v + h) * p.d_v;
+        for (int j = tid; j < TILE; j += kThreads) {
+            const int c = tile * TILE + j;
+            sv[j] = c < p.d_v ? IoType<IO>::ld(v + v_off + c) : 0.f;
+        }
+        if (tid == 0) {
+            const size_t gi = (size_t)t * p.h_v + h;
+            s_alpha = expf(decay_f(IoType<IO>::ld(ga + gi), A_log, dt_bias));
+            s_beta = sigmoid_f(IoType<IO>::ld(gb + gi));
+        }
+        __syncthreads();
+
+        // Partial retrieval S^T k and readout S^T q over this thread's rows.
+        float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+#pragma unroll
+        for (int m = 0; m < RPT; ++m) {
+            const int i = rg + RPP * m;
+            const float kk = sk[i], qq = sq[i];
+            pk.x = fmaf(S[m].x, kk, pk.x); pk.y = fmaf(S[m].y, kk, pk.y);
+            pk.z = fmaf(S[m].z, kk, pk.z); pk.w = fmaf(S[m].w, kk, pk.w);
+            pq.x = fmaf(S[m].x, qq, pq.x); pq.y = fmaf(S[m].y, qq, pq.y);
+            pq.z = fmaf(S[m].z, qq, pq.z); pq.w = fmaf(S[m].w, qq, pq.w);
+        }
+        *reinterpret_cast<float4 *>(&red_k[rg * TILE + 4 * lr]) = pk;
+        *reinterpret_cast<float4 *>(&red_q[rg * TILE + 4 * lr]) = pq;
+        if (tid < 32) {
+            float acc = 0.f;
+            for (int i = tid; i < DKMAX; i += 32) acc = fmaf(sq[i], sk[i], acc);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (tid == 0) s_qk = acc;
+        }
+        __syncthreads();
+
+        const float alpha = s_alpha;
+        if (tid < TILE) {
+            float rk = 0.f, rq = 0.f;
+#pragma unroll 8
+            for (int r = 0; r < RPP; ++r) {
+                rk += red_k[r * TILE + tid];
+                rq += red_q[r * TILE + tid];
+            }
+            // r = (alpha S)^T k; delta = beta (v - r); o = scale (alpha S + k delta^T)^T q
+            const float delta = s_beta * (sv[tid] - alpha * rk);
+            sdelta[tid] = delta;
+            const int c = tile * TILE + tid;
+            if (c < p.d_v) IoType<IO>::st(o + v_off + c, p.scale * fmaf(s_qk, delta, alpha * rq));
+        }
+        __syncthreads();
+
+        const float4 d4 = *reinterpret_cast<const float4 *>(&sdelta[4 * lr]);
+#pragma unroll
+        for (int m = 0; m < RPT; ++m) {
+            const float kk = sk[rg + RPP * m];
+            S[m].x = fmaf(alpha, S[m].x, kk * d4.x);
+            S[m].y = fmaf(alpha, S[m].y, kk * d4.y);
+            S[m].z = fmaf(alpha, S[m].z, kk * d4.z);
+            S[m].w = fmaf(alpha, S[m].w, kk * d4.w);
+        }
+    }
+
+#pragma unroll
+    for (int m = 0; m < RPT; ++m) {
+        const int i = rg + RPP * m;
+        if (col_ok && i < p.d_k)
+            __stcs(reinterpret_cast<float4 *>(p.state_out + sbase + (size_t)i * p.d_v + col0),
+                   S[m]);
+    }
+}
+
+template <typename IO, int DKMAX>
+cudaError_t launch_dk(const ScanParams &p, cudaStream_t stream) {
+    int lpr = 32;
+    if (p.d_v <= 32) lpr = 8;
+    else if (p.d_v <= 64) lpr = 16;
+    const int tiles = (p.d_v + 4 * lpr - 1) / (4 * lpr);
+    const int64_t blocks = (int64_t)p.num_seqs * p.h_v * tiles;
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)blocks), block(kThreads);
+    switch (lpr) {
+        case 8: scan_simt_kernel<IO, DKMAX, 8><<<grid, block, 0, stream>>>(p); break;
+        case 16: scan_simt_kernel<IO, DKMAX, 16><<<grid, block, 0, stream>>>(p); break;
+        default: scan_simt_kernel<IO, DKMAX, 32><<<grid, block, 0, stream>>>(p); break;
+    }
+    return cudaGetLastError();
+}
+
+template <typename IO>
+cudaError_t launch_io(const ScanParams &p, cudaStream_t stream) {
+    if (p.d_k <= 32) return launch_dk<IO, 32>(p, stream);
+    if (p.d_k <= 64) return launch_dk<IO, 64>(p, stream);
+    if (p.d_k <= 128) return launch_dk<IO, 128>(p, stream);
+    return launch_dk<IO, 256>(p, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_scan_simt(const ScanParams &p, gdn_dtype io, cudaStream_t stream) {
+    switch (io) {
+        case GDN_F32: return launch_io<float>(p, stream);
+        case GDN_BF16: return launch_io<__nv_bfloat16>(p, stream);
+        default: return launch_io<__half>(p, stream);
+    }
+}
+
+}  // namespace gdn

@@ -1,0 +1,249 @@
+"""Thin Python binding of libgdn's C ABI (argument marshalling only).
+
+Every step of the scan runs in libgdn's CUDA kernels; PyTorch only supplies
+device memory and the stream.  The entry points keep the C names:
+``gdn_prefill``, ``gdn_decode_step``, ``gdn_prefill_workspace_bytes``,
+``gdn_last_device_status``, ``gdn_status_string``.  If the library cannot be
+loaded every call raises -- there is no CPU or PyTorch fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+from . import _build
+
+GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED = 0, 1, 2
+GDN_ERR_CUDA, GDN_ERR_DEVICE_CHECK, GDN_ERR_TIMEOUT = 3, 4, 5
+GDN_F32, GDN_BF16, GDN_F16 = 0, 1, 2
+_DTYPE_CODE = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16, torch.float16: GDN_F16}
+
+# Every symbol include/gdn.h declares.
+EXPORTS = ("gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode_step",
+           "gdn_prefill_plan", "gdn_last_device_status", "gdn_status_string",
+           "gdn_last_error_message")
+PATH_SIMT, PATH_TC = 1, 2
+
+
+class GdnShape(ctypes.Structure):
+    _fields_ = [("io_dtype", ctypes.c_int32), ("batch", ctypes.c_int32),
+                ("seqlen", ctypes.c_int64), ("num_seqs", ctypes.c_int32),
+                ("h_qk", ctypes.c_int32), ("h_v", ctypes.c_int32),
+                ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32)]
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{status_name(status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libgdn.so (building it first if allowed).  Raises if unavailable."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB) or (build_if_missing and not _build.up_to_date()):
+        if not build_if_missing:
+            raise GdnError(GDN_ERR_CUDA, f"libgdn is not built ({_build.LIB})")
+        _build.build()
+    lib = ctypes.CDLL(_build.LIB)
+    P = ctypes.c_void_p
+    S = ctypes.POINTER(GdnShape)
+    lib.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
+    lib.gdn_prefill_workspace_bytes.argtypes = [S]
+    lib.gdn_prefill.restype = ctypes.c_int
+    lib.gdn_prefill.argtypes = [S, P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P,
+                                ctypes.c_size_t, P]
+    lib.gdn_decode_step.restype = ctypes.c_int
+    lib.gdn_decode_step.argtypes = [S, P, P, P, P, P, P, P, P, ctypes.c_float, P, P]
+    lib.gdn_prefill_plan.restype = ctypes.c_int
+    lib.gdn_prefill_plan.argtypes = [S, ctypes.POINTER(ctypes.c_int32),
+                                     ctypes.POINTER(ctypes.c_int32)]
+    lib.gdn_last_device_status.restype = ctypes.c_int
+    lib.gdn_last_device_status.argtypes = [P]
+    lib.gdn_status_string.restype = ctypes.c_char_p
+    lib.gdn_status_string.argtypes = [ctypes.c_int]
+    lib.gdn_last_error_message.restype = ctypes.c_char_p
+    lib.gdn_last_error_message.argtypes = []
+    _lib = lib
+    return lib
+
+
+def status_name(status: int) -> str:
+    try:
+        return load().gdn_status_string(int(status)).decode()
+    except Exception:  # the name is only cosmetic
+        return f"status {status}"
+
+
+def _check(status: int):
+    if status != GDN_OK:
+        raise GdnError(status, load().gdn_last_error_message().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _need_cuda(name: str, t: torch.Tensor, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise GdnError(GDN_ERR_INVALID_ARG, f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise GdnError(GDN_ERR_INVALID_ARG, f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise GdnError(GDN_ERR_INVALID_ARG, f"{name} must be {dtype}, got {t.dtype}")
+
+
+def make_shape(io_dtype: int, batch: int, seqlen: int, num_seqs: int, h_qk: int, h_v: int,
+               d_k: int, d_v: int) -> GdnShape:
+    return GdnShape(io_dtype, batch, seqlen, num_seqs, h_qk, h_v, d_k, d_v)
+
+
+def _shape_of(q, v, cu_seqlens) -> GdnShape:
+    if q.dim() != 4 or v.dim() != 4:
+        raise GdnError(GDN_ERR_INVALID_ARG, "q and v must be [B, T, H, D]")
+    B, T, h_qk, d_k = q.shape
+    h_v, d_v = v.shape[2], v.shape[3]
+    if q.dtype not in _DTYPE_CODE:
+        raise GdnError(GDN_ERR_INVALID_ARG, f"unsupported io dtype {q.dtype}")
+    n = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    return make_shape(_DTYPE_CODE[q.dtype], B, T, n, h_qk, h_v, d_k, d_v)
+
+
+def gdn_prefill_workspace_bytes(shape: GdnShape) -> int:
+    return int(load().gdn_prefill_workspace_bytes(ctypes.byref(shape)))
+
+
+def gdn_prefill(q, k, v, a, b, A_log, dt_bias, state_in=None, cu_seqlens=None,
+                scale: float = 0.0, *, o=None, state_out=None, workspace=None, stream=None):
+    """Run the gated delta rule over whole sequences; returns (o, state_out).
+
+    q, k [B,T,h_qk,d_k]; v [B,T,h_v,d_v]; a, b [B,T,h_v] (all one io dtype);
+    A_log, dt_bias [h_v] fp32; state_in [N,h_v,d_k,d_v] fp32 or None;
+    cu_seqlens int32 [N+1] on the device (then B must be 1) or None.
+    """
+    lib = load()
+    shape = _shape_of(q, v, cu_seqlens)
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v), ("a", a), ("b", b)):
+        _need_cuda(name, t, dt)
+    _need_cuda("A_log", A_log, torch.float32)
+    _need_cuda("dt_bias", dt_bias, torch.float32)
+    if tuple(k.shape) != tuple(q.shape) or tuple(a.shape) != tuple(v.shape[:3]) or \
+            tuple(b.shape) != tuple(a.shape):
+        raise GdnError(GDN_ERR_INVALID_ARG, "k must match q, and a, b must be [B, T, h_v]")
+    if tuple(A_log.shape) != (shape.h_v,) or tuple(dt_bias.shape) != (shape.h_v,):
+        raise GdnError(GDN_ERR_INVALID_ARG, "A_log and dt_bias must be [h_v]")
+    st_shape = (shape.num_seqs, shape.h_v, shape.d_k, shape.d_v)
+    if state_in is not None:
+        _need_cuda("state_in", state_in, torch.float32)
+        if tuple(state_in.shape) != st_shape:
+            raise GdnError(GDN_ERR_INVALID_ARG, f"state_in must be {st_shape}")
+    if cu_seqlens is not None:
+        _need_cuda("cu_seqlens", cu_seqlens, torch.int32)
+    if o is None:
+        o = torch.empty(v.shape, dtype=dt, device=v.device)
+    else:
+        _need_cuda("o", o, dt)
+    if state_out is None:
+        state_out = torch.empty(st_shape, dtype=torch.float32, device=v.device)
+    else:
+        _need_cuda("state_out", state_out, torch.float32)
+    need = int(lib.gdn_prefill_workspace_bytes(ctypes.byref(shape)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=v.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.gdn_prefill(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b),
+                           _ptr(A_log), _ptr(dt_bias), _ptr(state_in), _ptr(cu_seqlens),
+                           float(scale), _ptr(o), _ptr(state_out), _ptr(workspace), ws_bytes,
+                           _stream(stream)))
+    return o, state_out
+
+
+def gdn_decode_step(q, k, v, a, b, A_log, dt_bias, state, scale: float = 0.0, *, o=None,
+                    stream=None):
+    """One token per sequence; ``state`` [B,h_v,d_k,d_v] fp32 is updated in place.
+
+    q, k [B,1,h_qk,d_k]; v [B,1,h_v,d_v]; a, b [B,1,h_v].  Returns o [B,1,h_v,d_v].
+    """
+    lib = load()
+    shape = _shape_of(q, v, None)
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v), ("a", a), ("b", b)):
+        _need_cuda(name, t, dt)
+    _need_cuda("A_log", A_log, torch.float32)
+    _need_cuda("dt_bias", dt_bias, torch.float32)
+    _need_cuda("state", state, torch.float32)
+    if tuple(state.shape) != (shape.batch, shape.h_v, shape.d_k, shape.d_v):
+        raise GdnError(GDN_ERR_INVALID_ARG, "state must be [B, h_v, d_k, d_v]")
+    if o is None:
+        o = torch.empty(v.shape, dtype=dt, device=v.device)
+    else:
+        _need_cuda("o", o, dt)
+    _check(lib.gdn_decode_step(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a),
+                               _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(state), float(scale),
+                               _ptr(o), _stream(stream)))
+    return o
+
+
+def gdn_prefill_plan(shape: GdnShape):
+    """(path, launches per call) that gdn_prefill takes for ``shape``."""
+    path, launches = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(load().gdn_prefill_plan(ctypes.byref(shape), ctypes.byref(path),
+                                   ctypes.byref(launches)))
+    return path.value, launches.value
+
+
+def shape_of_spec(spec, n_seq: int, total_tokens: int) -> GdnShape:
+    io = {"f32": GDN_F32, "bf16": GDN_BF16, "f16": GDN_F16}[spec.io]
+    if spec.lengths is not None or spec.varlen_range is not None:
+        return make_shape(io, 1, total_tokens, n_seq, spec.h_qk, spec.h_v, spec.d_k, spec.d_v)
+    return make_shape(io, spec.batch, spec.seqlen, spec.batch, spec.h_qk, spec.h_v, spec.d_k,
+                      spec.d_v)
+
+
+def launches_per_call(spec, n_seq: int = 0, total_tokens: int = 0) -> int:
+    if spec.decode:
+        return 1
+    return gdn_prefill_plan(shape_of_spec(spec, n_seq, total_tokens))[1]
+
+
+def path_dtype(spec, n_seq: int = 0, total_tokens: int = 0) -> str:
+    """Arithmetic type of the path: MMA operand type on the tensor-core path, else f32."""
+    if spec.decode:
+        return "f32"
+    path = gdn_prefill_plan(shape_of_spec(spec, n_seq, total_tokens))[0]
+    return spec.io if path == PATH_TC else "f32"
+
+
+def gdn_last_device_status(stream=None) -> int:
+    """Synchronise, read and clear the device check word; returns the status code."""
+    return int(load().gdn_last_device_status(_stream(stream)))
+
+
+def gdn_status_string(status: int) -> str:
+    return load().gdn_status_string(int(status)).decode()
+
+
+def default_scale(d_k: int) -> float:
+    return 1.0 / math.sqrt(d_k)

@@ -1,0 +1,210 @@
+"""GPU parity: libgdn (through its C ABI) against the float64 CPU oracle.
+
+Tolerance (max|gpu - ref| / max|ref|, separately for o and the final state):
+1e-4 for fp32 I/O, 2e-2 for bf16/f16 I/O; the state is fp32 on both sides.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from gpu_util import TOL, check, rel_err, run_prefill, to_device
+
+pytestmark = pytest.mark.gpu
+
+needs_cuda = pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from recurrent_state_scan_gb300 import load
+    load()
+
+
+def _decode(inp, state=None):
+    from recurrent_state_scan_gb300 import gdn_decode_step
+    d = to_device(inp)
+    st = d["state_in"].clone() if state is None else state
+    o = gdn_decode_step(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], st,
+                        inp.scale)
+    torch.cuda.synchronize()
+    return o.float().cpu().numpy().reshape(-1, inp.spec.h_v, inp.spec.d_v), st.cpu().numpy()
+
+
+# ---------------------------------------------------------------- measured workloads
+
+def test_tiny_f32_prefill_full():
+    inp = workloads.workload("tiny_f32_prefill")
+    o_ref, s_ref = oracle.scan_inputs(inp)
+    o, s = run_prefill(inp)
+    check(inp, o, s, o_ref, s_ref, what="tiny fp32 prefill")
+
+
+def test_decode_b256_full():
+    inp = workloads.workload("bf16_decode_b256")
+    o_ref, s_ref = oracle.scan_inputs(inp, threads=8)
+    o, s = _decode(inp)
+    check(inp, o, s, o_ref, s_ref, what="decode B=256")
+
+
+SAMPLED = {
+    # (workload, sampled (sequence * h_v + head) units)
+    "bf16_prefill_t4096": [0, 7, 15],
+    "varlen_bf16_prefill": [0 * 16 + 3, 1 * 16 + 0, 6 * 16 + 15, 7 * 16 + 9],
+    "gqa_f16_prefill": [0, 1, 31, 32 + 14, 32 + 15],
+}
+
+
+@pytest.mark.parametrize("name", sorted(SAMPLED))
+def test_prefill_workloads_sampled_units(name):
+    """Full-size run in the benchmark's launch configuration; the oracle computes
+    a sample of (sequence, head) units in full (every token, the final state)."""
+    inp = workloads.workload(name)
+    o, s = run_prefill(inp)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(s))
+    units = SAMPLED[name]
+    o_ref, s_ref = oracle.scan_inputs(inp, units=units, threads=len(units))
+    check(inp, o, s, o_ref, s_ref, units=units, what=name)
+
+
+# ---------------------------------------------------------------- small shapes, edges
+
+@pytest.mark.parametrize("io", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("dims", [(2, 4, 128, 128), (1, 1, 64, 32), (2, 2, 256, 256),
+                                  (3, 3, 100, 36), (1, 2, 32, 4)])
+def test_decode_small(io, dims):
+    h_qk, h_v, d_k, d_v = dims
+    inp = workloads.draw(workloads.small_spec(io=io, batch=5, seqlen=1, h_qk=h_qk, h_v=h_v,
+                                              d_k=d_k, d_v=d_v, seed=31, state_std=0.05,
+                                              decode=True))
+    o_ref, s_ref = oracle.scan_inputs(inp)
+    o, s = _decode(inp)
+    check(inp, o, s, o_ref, s_ref, what=f"decode {io} {dims}")
+
+
+PREFILL_CASES = [
+    # (io, lengths, h_qk, h_v, d_k, d_v, state_std)
+    ("bf16", [64], 1, 1, 128, 128, 0.0),
+    ("bf16", [1, 63, 65, 130, 0, 200], 2, 2, 128, 128, 0.05),   # ragged chunks, empty seq
+    ("f16", [129, 64, 7], 2, 4, 128, 128, 0.05),                # GQA
+    ("bf16", [300], 1, 1, 128, 128, 0.0),
+    ("f32", [64, 33], 2, 2, 32, 32, 0.0),
+    ("f32", [100], 1, 2, 128, 128, 0.05),
+    ("bf16", [50, 20], 1, 1, 64, 64, 0.05),
+    ("f16", [40], 2, 2, 256, 128, 0.05),
+    ("bf16", [17, 0, 0, 5], 1, 1, 96, 12, 0.05),
+]
+
+
+@pytest.mark.parametrize("case", PREFILL_CASES, ids=lambda c: f"{c[0]}-{len(c[1])}seq-d{c[4]}x{c[5]}")
+def test_prefill_small(case):
+    io, lengths, h_qk, h_v, d_k, d_v, sstd = case
+    inp = workloads.draw(workloads.small_spec(io=io, lengths=lengths, h_qk=h_qk, h_v=h_v,
+                                              d_k=d_k, d_v=d_v, seed=41 + len(lengths),
+                                              state_std=sstd))
+    o_ref, s_ref = oracle.scan_inputs(inp)
+    o, s = run_prefill(inp)
+    check(inp, o, s, o_ref, s_ref, what=f"prefill {case}")
+
+
+def test_prefill_batched_equals_varlen():
+    """B sequences of one length through the batched layout and through cu_seqlens."""
+    spec = workloads.small_spec(io="bf16", batch=3, seqlen=150, h_qk=2, h_v=2, seed=51,
+                                state_std=0.05)
+    inp = workloads.draw(spec)
+    o_ref, s_ref = oracle.scan_inputs(inp)
+    o, s = run_prefill(inp)
+    check(inp, o, s, o_ref, s_ref, what="batched")
+    from recurrent_state_scan_gb300 import gdn_prefill
+    d = to_device(inp)
+    cu = torch.tensor(inp.cu_seqlens, dtype=torch.int32, device="cuda")
+    flat = {n: d[n].reshape(1, -1, *d[n].shape[2:]) for n in ("q", "k", "v", "a", "b")}
+    o2, s2 = gdn_prefill(flat["q"], flat["k"], flat["v"], flat["a"], flat["b"], d["A_log"],
+                         d["dt_bias"], d["state_in"], cu, inp.scale)
+    o2 = o2.float().cpu().numpy().reshape(o.shape)
+    assert rel_err(o2, o_ref) <= TOL["bf16"] and rel_err(s2.cpu().numpy(), s_ref) <= TOL["bf16"]
+
+
+def test_chaining_and_decode_steps():
+    """prefill(T1) then prefill(T2) from its state, and T decode steps, all equal
+    one prefill over T1+T2 (each within tolerance of the oracle)."""
+    from recurrent_state_scan_gb300 import gdn_decode_step, gdn_prefill
+    spec = workloads.small_spec(io="bf16", batch=2, seqlen=96, h_qk=1, h_v=2, seed=61,
+                                state_std=0.05)
+    inp = workloads.draw(spec)
+    o_ref, s_ref = oracle.scan_inputs(inp)
+    d = to_device(inp)
+    T1 = 40
+    sl = lambda x, a, b: x[:, a:b].contiguous()
+    oa, sa = gdn_prefill(*(sl(d[n], 0, T1) for n in ("q", "k", "v", "a", "b")), d["A_log"],
+                         d["dt_bias"], d["state_in"], None, inp.scale)
+    ob, sb = gdn_prefill(*(sl(d[n], T1, 96) for n in ("q", "k", "v", "a", "b")), d["A_log"],
+                         d["dt_bias"], sa, None, inp.scale)
+    o = torch.cat([oa, ob], dim=1).float().cpu().numpy().reshape(-1, 2, 128)
+    assert rel_err(o, o_ref) <= TOL["bf16"]
+    assert rel_err(sb.cpu().numpy(), s_ref) <= TOL["bf16"]
+    st = d["state_in"].clone()
+    outs = []
+    for t in range(96):
+        outs.append(gdn_decode_step(*(sl(d[n], t, t + 1) for n in ("q", "k", "v", "a", "b")),
+                                    d["A_log"], d["dt_bias"], st, inp.scale))
+    o = torch.cat(outs, dim=1).float().cpu().numpy().reshape(-1, 2, 128)
+    assert rel_err(o, o_ref) <= TOL["bf16"]
+    assert rel_err(st.cpu().numpy(), s_ref) <= TOL["bf16"]
+
+
+def test_state_in_place_and_null_state():
+    from recurrent_state_scan_gb300 import gdn_prefill
+    inp = workloads.draw(workloads.small_spec(io="bf16", lengths=[70, 0, 9], seed=71,
+                                              state_std=0.05))
+    o_ref, s_ref = oracle.scan_inputs(inp)
+    d = to_device(inp)
+    st = d["state_in"].clone()
+    o, s = gdn_prefill(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], st,
+                       d["cu_seqlens"], inp.scale, state_out=st)
+    assert s.data_ptr() == st.data_ptr()
+    assert rel_err(st.cpu().numpy(), s_ref) <= TOL["bf16"]
+    # The empty sequence keeps its state exactly.
+    assert np.array_equal(st.cpu().numpy()[1], inp.state_in.numpy()[1])
+    # NULL state_in means zeros.
+    o0, s0 = gdn_prefill(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], None,
+                         d["cu_seqlens"], inp.scale)
+    f = inp.f64
+    o_ref0, s_ref0 = oracle.scan(inp.cu_seqlens, 2, 2, 128, 128, f["q"], f["k"], f["v"],
+                                 a=f["a"], b=f["b"], A_log=f["A_log"], dt_bias=f["dt_bias"],
+                                 scale=inp.scale)
+    assert rel_err(s0.cpu().numpy(), s_ref0) <= TOL["bf16"]
+    assert np.all(s0.cpu().numpy()[1] == 0.0)
+
+
+def test_zero_gates_invariant_on_gpu():
+    """b = -inf (beta = 0) and A_log = -inf (g = 0): o = 0 and S = 0 from a zero state."""
+    from recurrent_state_scan_gb300 import gdn_prefill
+    inp = workloads.draw(workloads.small_spec(io="bf16", lengths=[130], seed=81))
+    d = to_device(inp)
+    d["b"].fill_(float("-inf"))
+    A_log = torch.full_like(d["A_log"], float("-inf"))
+    o, s = gdn_prefill(d["q"], d["k"], d["v"], d["a"], d["b"], A_log, d["dt_bias"], None,
+                       d["cu_seqlens"], inp.scale)
+    torch.cuda.synchronize()
+    assert torch.all(o == 0) and torch.all(s == 0)
+
+
+def test_bad_device_cu_seqlens_sets_check_word():
+    """A malformed device cu_seqlens is skipped and reported, without a fault."""
+    from recurrent_state_scan_gb300 import gdn_last_device_status, gdn_prefill
+    from recurrent_state_scan_gb300.gdn import GDN_ERR_DEVICE_CHECK, GDN_OK
+    inp = workloads.draw(workloads.small_spec(io="bf16", lengths=[10, 20], seed=91))
+    d = to_device(inp)
+    assert gdn_last_device_status() == GDN_OK
+    bad = torch.tensor([0, 25, 20], dtype=torch.int32, device="cuda")   # decreasing
+    gdn_prefill(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], None, bad,
+                inp.scale)
+    assert gdn_last_device_status() == GDN_ERR_DEVICE_CHECK
+    assert gdn_last_device_status() == GDN_OK          # read-and-clear
+    o, s = run_prefill(inp)                            # the context is still usable
+    o_ref, s_ref = oracle.scan_inputs(inp)
+    check(inp, o, s, o_ref, s_ref, what="after device check")
