@@ -88,8 +88,9 @@ typedef struct gdn_shape {
  *                  bytes (may be NULL when that is 0); its contents need no
  *                  initialisation and are not preserved.
  *
- * bf16/f16 I/O with d_k = d_v = 128 runs the chunked tensor-core path; other
- * shapes and fp32 I/O run the sequential SIMT path.  State math is fp32 always.
+ * bf16/f16 I/O with d_k = d_v = 128 runs the chunked tensor-core path (q, k, v
+ * and o must then be 16-byte aligned, else the SIMT path runs); other shapes and
+ * fp32 I/O run the token-sequential SIMT path.  State math is fp32 always.
  */
 size_t gdn_prefill_workspace_bytes(const gdn_shape *shape);
 

@@ -128,7 +128,12 @@ gdn_status gdn_prefill_plan(const gdn_shape *shape, int32_t *path, int32_t *laun
     gdn_status st = check_shape(shape, shape != nullptr && shape->batch == 1 &&
                                            shape->num_seqs != 1);
     if (st != GDN_OK) return st;
-    if (path) *path = 1;
+    const bool varlen = shape->batch == 1 && shape->num_seqs != 1;
+    const int64_t tokens = varlen ? shape->seqlen : shape->seqlen * (int64_t)shape->batch;
+    const bool tc = (shape->io_dtype == GDN_BF16 || shape->io_dtype == GDN_F16) &&
+                    shape->d_k == 128 && shape->d_v == 128 && tokens > 0 &&
+                    tokens <= 0x7fffff00LL;
+    if (path) *path = tc ? 2 : 1;
     if (launches) *launches = shape->num_seqs > 0 ? 1 : 0;
     return GDN_OK;
 }
@@ -168,8 +173,15 @@ gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, con
     p.h_qk = shape->h_qk; p.h_v = shape->h_v; p.d_k = shape->d_k; p.d_v = shape->d_v;
     p.scale = scale == 0.0f ? 1.0f / sqrtf((float)shape->d_k) : scale;
     p.status = word;
-    cudaError_t e = launch_scan_simt(p, (gdn_dtype)shape->io_dtype, (cudaStream_t)stream);
-    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    const gdn_dtype io = (gdn_dtype)shape->io_dtype;
+    cudaError_t e;
+    if (prefill_tc_supported(p, io, tokens)) {
+        e = launch_prefill_tc(p, io, tokens, prefill_tc_columns(p), (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");
+    } else {
+        e = launch_scan_simt(p, io, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    }
     return GDN_OK;
 }
 

@@ -65,22 +65,35 @@ __device__ __forceinline__ float decay_f(float a, float A_log, float dt_bias) {
 
 // Token range [t0, t1) of sequence n; false (and the check word set) if the
 // device-resident cu_seqlens entries for n are malformed.
-__device__ __forceinline__ bool seq_range(const ScanParams &p, int64_t n, int64_t &t0,
+__device__ __forceinline__ bool seq_range(const int32_t *cu_seqlens, int64_t seqlen,
+                                          int32_t num_seqs, int *status, int64_t n, int64_t &t0,
                                           int64_t &t1) {
-    if (p.cu_seqlens == nullptr) {
-        t0 = n * p.seqlen;
-        t1 = t0 + p.seqlen;
+    if (cu_seqlens == nullptr) {
+        t0 = n * seqlen;
+        t1 = t0 + seqlen;
         return true;
     }
-    t0 = p.cu_seqlens[n];
-    t1 = p.cu_seqlens[n + 1];
-    const bool ok = (t0 >= 0) && (t0 <= t1) && (t1 <= p.seqlen) && (n != 0 || t0 == 0) &&
-                    (n + 1 != p.num_seqs || t1 == p.seqlen);
-    if (!ok) atomicOr(p.status, kDevBadCuSeqlens);
+    t0 = cu_seqlens[n];
+    t1 = cu_seqlens[n + 1];
+    const bool ok = (t0 >= 0) && (t0 <= t1) && (t1 <= seqlen) && (n != 0 || t0 == 0) &&
+                    (n + 1 != num_seqs || t1 == seqlen);
+    if (!ok) atomicOr(status, kDevBadCuSeqlens);
     return ok;
+}
+__device__ __forceinline__ bool seq_range(const ScanParams &p, int64_t n, int64_t &t0,
+                                          int64_t &t1) {
+    return seq_range(p.cu_seqlens, p.seqlen, p.num_seqs, p.status, n, t0, t1);
 }
 
 // Launchers implemented in the kernel translation units.
 cudaError_t launch_scan_simt(const ScanParams &p, gdn_dtype io, cudaStream_t stream);
+
+// Chunked tensor-core prefill (bf16/f16 I/O, d_k = d_v = 128).  `nv` is the number
+// of state columns per CTA (64 or 128).  Returns cudaErrorNotSupported if the
+// driver entry point for tensor-map encoding is unavailable.
+bool prefill_tc_supported(const ScanParams &p, gdn_dtype io, int64_t total_tokens);
+int prefill_tc_columns(const ScanParams &p);
+cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_tokens, int nv,
+                              cudaStream_t stream);
 
 }  // namespace gdn

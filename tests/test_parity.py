@@ -96,6 +96,8 @@ PREFILL_CASES = [
     ("bf16", [50, 20], 1, 1, 64, 64, 0.05),
     ("f16", [40], 2, 2, 256, 128, 0.05),
     ("bf16", [17, 0, 0, 5], 1, 1, 96, 12, 0.05),
+    ("bf16", [70, 1, 130, 64], 16, 32, 128, 128, 0.05),        # >= 120 units: 128-column CTAs
+    ("f16", [200, 3], 8, 64, 128, 128, 0.0),
 ]
 
 
@@ -108,6 +110,14 @@ def test_prefill_small(case):
     o_ref, s_ref = oracle.scan_inputs(inp)
     o, s = run_prefill(inp)
     check(inp, o, s, o_ref, s_ref, what=f"prefill {case}")
+
+
+def test_plan_takes_the_tensor_core_path_for_16bit_d128():
+    from recurrent_state_scan_gb300 import gdn
+    for io in (gdn.GDN_BF16, gdn.GDN_F16):
+        assert gdn.gdn_prefill_plan(gdn.make_shape(io, 1, 4096, 1, 16, 16, 128, 128))[0] == gdn.PATH_TC
+    assert gdn.gdn_prefill_plan(gdn.make_shape(gdn.GDN_F32, 1, 64, 1, 2, 2, 32, 32))[0] == gdn.PATH_SIMT
+    assert gdn.gdn_prefill_plan(gdn.make_shape(gdn.GDN_BF16, 1, 64, 1, 2, 2, 64, 64))[0] == gdn.PATH_SIMT
 
 
 def test_prefill_batched_equals_varlen():
