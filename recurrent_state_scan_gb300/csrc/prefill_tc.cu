@@ -7,28 +7,30 @@
 //   A_ij = beta_i e^{G_i-G_j} k_i.k_j (j < i),  T = (I + A)^-1
 //   W = T diag(beta gamma) K,   U = T diag(beta) V,   Delta = U - W S0
 //   o_i = scale gamma_i q_i^T S0 + sum_{j<=i} scale e^{G_i-G_j} (q_i.k_j) Delta_j
-//   S  = gamma_C S0 + (diag(e^{G_C-G}) K)^T Delta
-// Every product above runs on tcgen05 (bf16/f16 operands, fp32 accumulation in
-// TMEM); T is formed in fp32 on the SIMT cores; the state S stays in TMEM in fp32
-// for the whole sequence.  The pages run the recurrence one token at a time; this
-// chunked form is a re-association, exact up to rounding.
+//   S  = gamma_C S0 + K^T diag(e^{G_C-G}) Delta
+// The pages run the recurrence one token at a time; this chunked form is a
+// re-association of the same sums, exact up to rounding.
 //
-// One CTA (256 threads) owns one (sequence, value head, slice of NV state columns).
-// Columns of S evolve independently (the page's "Parallelization" note), so a slice
-// needs only its columns of V, U, Delta and o; the q/k-only chunk work (k.k, q.k, T,
-// W) is recomputed by each slice.
-//
-// All MMAs use M = 128 so every accumulator row lives in TMEM lane = row:
-//   D1  = [K ; Q] K^T       (K-major A and B)      lanes 0-63 K K^T, 64-127 Q K^T
-//   D2  = [T'; T''] K       (B = K tile MN-major)  lanes 0-63 W
-//   D3  = [T'; T''] V       (B = V tile MN-major)  lanes 64-127 U
-//   D4  = [Q ; W] S         (B = S bf16 MN-major)  lanes 0-63 Q S, 64-127 W S
-//   D5  = [P ; 0] Delta     (B = Delta MN-major)   lanes 0-63 P Delta
-//   DS += Ktil^T Delta      (A = Ktil MN-major)    lanes = d_k rows of S
-// with T' = T diag(beta gamma), T'' = T diag(beta), P_ij = scale e^{G_i-G_j} q_i.k_j.
+// One CTA owns one (sequence, value head, half of the 128 state columns) and walks the
+// sequence's chunks in order.  Columns of S evolve independently (the page's
+// "Parallelization" note), so a half needs only its columns of V, U, Delta and o.
+// Its 12 warps split into two roles that run one chunk apart:
+//   prep  (warps 0-7)  chunk c+1: gates and their prefix sums, D1 = [K; Q] K^T (tcgen05),
+//                      A and P, T = (I + A)^-1 (fp32 diagonal blocks + tf32 warp-MMA
+//                      merges), [T'; T''] = [T diag(beta gamma); T diag(beta)],
+//                      D2 = [T'; T''] K -> W,  D3 = [T'; T''] V -> U (tcgen05).
+//   chain (warps 8-11) chunk c: D4 = [Q; W] S0 (tcgen05), Delta = U - W S0,
+//                      D5 = [P; 0] Delta, DS = K^T diag(e^{G_C-G}) Delta (tcgen05),
+//                      S = gamma_C S0 + DS with S in fp32 registers, o to HBM.
+// K, Q and V arrive by TMA into two stages; the chain refills a stage as soon as its
+// last reader is done.  All MMAs use M = 128, so accumulator row r is TMEM lane r:
+//   D1 lanes 0-63 K K^T, 64-127 Q K^T;  D2 lanes 0-63 W;  D3 lanes 64-127 U;
+//   D4 lanes 0-63 Q S0, 64-127 W S0;  D5 lanes 0-63 P Delta;  DS lanes = d_k rows.
 // Rows past the end of a sequence get g = 0 and beta = 0, which makes their T row the
 // unit row and their W, U and Delta rows exactly zero, so they change nothing.
 #include <cudaTypedefs.h>
+
+#include <type_traits>
 
 #include "gdn_internal.cuh"
 #include "tc_ptx.cuh"
@@ -38,13 +40,18 @@ namespace {
 
 using namespace tc;
 
-constexpr int kC = 64;             // tokens per chunk
-constexpr int kDK = 128;           // d_k (and full d_v) of this path
-constexpr int kThreads = 256;
+constexpr int kC = 64;                 // tokens per chunk
+constexpr int kDK = 128;               // d_k = d_v of this path
+constexpr int kNV = 64;                // state columns per CTA
+constexpr int kPrepThreads = 256, kChainThreads = 128;
+constexpr int kThreads = kPrepThreads + kChainThreads;
+constexpr uint32_t kBarPrep = 1, kBarChain = 2;
 constexpr long long kWaitBudget = 4000000000LL;   // cycles (~2 s) before a wait gives up
 
 struct TcParams {
     CUtensorMap tm_q, tm_k, tm_v;
+    CUtensorMap tm_a, tm_b;        // gate logits [tokens][h_v], used when gate_tma != 0
+    int32_t gate_tma;
     const void *a, *b;
     const float *A_log, *dt_bias;
     const float *state_in;
@@ -58,22 +65,30 @@ struct TcParams {
 };
 
 // Shared-memory plan (byte offsets from a 1024-aligned base).
-template <int NV>
-struct Plan {
-    static constexpr int kRegion = 24576;                    // 192 rows x 128 B: K | Q | W
-    static constexpr int KQW = 0;                            // 2 regions (d_k 0-63, 64-127)
-    static constexpr int V = KQW + 2 * kRegion;              // NV/64 regions of 64 x 128 B
-    static constexpr int KT = V + (NV / 64) * 8192;          // Ktil, 2 regions 64 x 128 B
-    static constexpr int TT = KT + 2 * 8192;                 // [T'; T''] 128 x 128 B
-    static constexpr int PZ = TT + 16384;                    // [P; 0]    128 x 128 B
-    static constexpr int SB = PZ + 16384;                    // S bf16, NV/64 regions 128 x 128 B
-    static constexpr int DB = SB + (NV / 64) * 16384;        // Delta,  NV/64 regions 64 x 128 B
-    static constexpr int AS = DB + (NV / 64) * 8192;         // A fp32 [64][65]
-    static constexpr int TS = AS + 17408;                    // T fp32 [64][65]
-    static constexpr int kBytes = TS + 17408;
-    static constexpr int kAlloc = kBytes + 1024;             // slack for the 1024 alignment
-    // TMEM columns
-    static constexpr uint32_t tD1 = 0, tD24 = 64, tD35 = 192, tDS = 192 + NV;
+constexpr int kRegion = 24576;                 // 192 rows x 128 B: K | Q | W for 64 d_k
+constexpr int kGates = 2 * kRegion + 8192;     // gate logit tiles a, b: 64 tokens x 8 heads
+constexpr int kStage = kGates + 2048;          // + V (64 tokens x 64 columns) + gate tiles
+constexpr int OFF_STAGE = 0;                   // two stages
+constexpr int OFF_PZ = 2 * kStage;             // two [P; 0] tiles, 128 x 128 B each
+constexpr int OFF_TT = OFF_PZ + 2 * 16384;     // [T'; T''], 128 x 128 B
+constexpr int OFF_SB = OFF_TT + 16384;         // S0 in the I/O type, MN-major (d_k rows)
+constexpr int OFF_DB0 = OFF_SB + 16384;        // Delta, MN-major (token rows)
+constexpr int OFF_DB1 = OFF_DB0 + 8192;        // diag(e^{G_C - G}) Delta
+constexpr int OFF_AS = OFF_DB1 + 8192;         // A, then T, fp32 [64][68]
+constexpr int kAs = 68;                        // row stride (floats) of A / T
+constexpr int kSmemBytes = OFF_AS + 64 * kAs * 4;
+constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for the 1024-byte alignment
+
+// TMEM columns.
+constexpr uint32_t TM_D1 = 0, TM_D2 = 64, TM_D3 = 192, TM_D4 = 320, TM_D5 = 384, TM_DS = 448;
+
+struct Ctl {
+    uint64_t full[2], prep_done[2], chain_done[2], d1, d23, d4, d5;
+    uint32_t tmem;
+    int abort;
+    float G[kC], beta[kC], E[kC], F[kC], wsum[2];
+    float gam[2][kC], kf[2][kC], gC[2];
+    float X[3][16][20];                        // warp scratch of the T merges
 };
 
 template <typename IO> struct Pack;
@@ -82,466 +97,541 @@ template <> struct Pack<__nv_bfloat16> {
         __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
         return *reinterpret_cast<uint32_t *>(&v);
     }
-    static __device__ __forceinline__ float2 unpack(uint32_t u) {
-        return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&u));
-    }
 };
 template <> struct Pack<__half> {
     static __device__ __forceinline__ uint32_t two(float a, float b) {
         __half2 v = __floats2half2_rn(a, b);
         return *reinterpret_cast<uint32_t *>(&v);
     }
-    static __device__ __forceinline__ float2 unpack(uint32_t u) {
-        return __half22float2(*reinterpret_cast<__half2 *>(&u));
-    }
 };
-
 template <typename IO>
 __device__ __forceinline__ uint4 pack8(const float *x) {
     return make_uint4(Pack<IO>::two(x[0], x[1]), Pack<IO>::two(x[2], x[3]),
                       Pack<IO>::two(x[4], x[5]), Pack<IO>::two(x[6], x[7]));
 }
 
-// T = (I + A)^-1 for a 64 x 64 strictly-lower A (row stride 65 floats), in fp32.
-// Diagonal 16x16 blocks by forward substitution, then block forward substitution
-// T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj for the blocks below the diagonal.
-// Entries above the diagonal of T are left unwritten.
-__device__ void invert_unit_lower_64(const float *As, float *Ts, float (*sX)[16][17], int tid) {
-    if (tid < 64) {
-        const int blk = tid >> 4, j = tid & 15, o = blk * 16;
+// OR-reduction of `pred` over the `count` threads of named barrier `id`.
+__device__ __forceinline__ bool bar_any(uint32_t id, uint32_t count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+// Store T[r][c] (scaled by f1 and f2) into [T diag(beta gamma); T diag(beta)].
+template <typename IO>
+__device__ __forceinline__ void tt_put(uint8_t *tt, int r, int c, float x, float f1, float f2) {
+    const uint32_t off = sw128_offset(r, c >> 3) + (c & 7) * 2;
+    IoType<IO>::st(reinterpret_cast<IO *>(tt + off), x * f1);
+    IoType<IO>::st(reinterpret_cast<IO *>(tt + 8192 + off), x * f2);   // row r + 64
+}
+template <typename IO>
+__device__ __forceinline__ void tt_put2(uint8_t *tt, int r, int c, float x0, float x1,
+                                        const float *beta, const float *gam) {
+    const uint32_t off = sw128_offset(r, c >> 3) + (c & 7) * 2;
+    const float b0 = beta[c], b1 = beta[c + 1];
+    *reinterpret_cast<uint32_t *>(tt + off) = Pack<IO>::two(x0 * b0 * gam[c], x1 * b1 * gam[c + 1]);
+    *reinterpret_cast<uint32_t *>(tt + 8192 + off) = Pack<IO>::two(x0 * b0, x1 * b1);
+}
+
+// T = (I + A)^-1 for the strictly-lower 64 x 64 A in As (prep threads only), written
+// straight into the K-major operand tile [T diag(beta gamma); T diag(beta)].
+// The diagonal 16x16 blocks are solved by forward substitution in fp32, one thread per
+// column, and kept (unscaled) in place in As.  Warp w < 3 then owns column block w and
+// forms the blocks below the diagonal, T_ij = -T_ii (sum_{k=j}^{i-1} A_ik T_kj), with
+// tf32 warp MMAs; each finished block is also kept transposed in the unused upper block
+// (j, i) of As, so A below the diagonal is never overwritten while other warps read it.
+template <typename IO>
+__device__ void invert_chunk(float *As, float (*X)[16][20], uint8_t *tt, const float *beta,
+                             const float *gam, int pt) {
+    if (pt < 64) {
+        const int o = (pt >> 4) * 16, j = pt & 15, cj = o + j;
         float x[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            if (i < j) {
-                x[i] = 0.f;
-            } else if (i == j) {
-                x[i] = 1.f;
-            } else {
-                float acc = 0.f;
+            float acc = 0.f;
 #pragma unroll
-                for (int l = 0; l < i; ++l)
-                    if (l >= j) acc = fmaf(As[(o + i) * 65 + o + l], x[l], acc);
-                x[i] = -acc;
-            }
+            for (int l = 0; l < i; ++l) acc = fmaf(As[(o + i) * kAs + o + l], x[l], acc);
+            x[i] = (i < j) ? 0.f : ((i == j) ? 1.f : -acc);
         }
+        __syncwarp();
+        const float f2 = beta[cj], f1 = f2 * gam[cj];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            if (i >= j) Ts[(o + i) * 65 + o + j] = x[i];
+        for (int i = 0; i < 16; ++i) {
+            As[(o + i) * kAs + cj] = x[i];
+            tt_put<IO>(tt, o + i, cj, x[i], f1, f2);
+        }
     }
-    __syncthreads();
-    for (int bi = 1; bi < 4; ++bi) {
-        for (int e = tid; e < bi * 256; e += kThreads) {
-            const int bj = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-            float acc = 0.f;
+    named_bar(kBarPrep, kPrepThreads);
+    const int w = pt >> 5, lane = pt & 31, g = lane >> 2, t = lane & 3;
+    if (w < 3) {
+        const int bj = w;
+        float *Xw = &X[w][0][0];
+        for (int bi = bj + 1; bi < 4; ++bi) {
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             for (int k = bj; k < bi; ++k) {
+                const bool diag = (k == bj);
 #pragma unroll
-                for (int l = 0; l < 16; ++l)
-                    acc = fmaf(As[(bi * 16 + r) * 65 + k * 16 + l], Ts[(k * 16 + l) * 65 + bj * 16 + cc],
-                               acc);
+                for (int kh = 0; kh < 2; ++kh) {
+                    const float *Ab = As + (16 * bi) * kAs + 16 * k + 8 * kh;
+                    const uint32_t a[4] = {to_tf32(Ab[g * kAs + t]), to_tf32(Ab[(g + 8) * kAs + t]),
+                                           to_tf32(Ab[g * kAs + t + 4]),
+                                           to_tf32(Ab[(g + 8) * kAs + t + 4])};
+#pragma unroll
+                    for (int nh = 0; nh < 2; ++nh) {
+                        const int r0 = 16 * k + 8 * kh + t, c0 = 16 * bj + 8 * nh + g;
+                        const uint32_t bb[2] = {
+                            to_tf32(diag ? As[r0 * kAs + c0] : As[c0 * kAs + r0]),
+                            to_tf32(diag ? As[(r0 + 4) * kAs + c0] : As[c0 * kAs + r0 + 4])};
+                        mma_tf32_16x8x8(acc[nh], a, bb);
+                    }
+                }
             }
-            sX[bj][r][cc] = acc;
-        }
-        __syncthreads();
-        for (int e = tid; e < bi * 256; e += kThreads) {
-            const int bj = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-            float acc = 0.f;
 #pragma unroll
-            for (int l = 0; l < 16; ++l)
-                if (l <= r) acc = fmaf(Ts[(bi * 16 + r) * 65 + bi * 16 + l], sX[bj][l][cc], acc);
-            Ts[(bi * 16 + r) * 65 + bj * 16 + cc] = -acc;
+            for (int nh = 0; nh < 2; ++nh) {
+                Xw[g * 20 + 8 * nh + 2 * t] = acc[nh][0];
+                Xw[g * 20 + 8 * nh + 2 * t + 1] = acc[nh][1];
+                Xw[(g + 8) * 20 + 8 * nh + 2 * t] = acc[nh][2];
+                Xw[(g + 8) * 20 + 8 * nh + 2 * t + 1] = acc[nh][3];
+            }
+            __syncwarp();
+            float res[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int kh = 0; kh < 2; ++kh) {
+                const float *Tb = As + (16 * bi) * kAs + 16 * bi + 8 * kh;
+                const uint32_t a[4] = {to_tf32(Tb[g * kAs + t]), to_tf32(Tb[(g + 8) * kAs + t]),
+                                       to_tf32(Tb[g * kAs + t + 4]),
+                                       to_tf32(Tb[(g + 8) * kAs + t + 4])};
+#pragma unroll
+                for (int nh = 0; nh < 2; ++nh) {
+                    const uint32_t bb[2] = {to_tf32(Xw[(8 * kh + t) * 20 + 8 * nh + g]),
+                                            to_tf32(Xw[(8 * kh + t + 4) * 20 + 8 * nh + g])};
+                    mma_tf32_16x8x8(res[nh], a, bb);
+                }
+            }
+            // T_{bi,bj}[r][c] -> As[16 bj + c][16 bi + r] and the operand tile.
+#pragma unroll
+            for (int nh = 0; nh < 2; ++nh) {
+                const int c = 16 * bj + 8 * nh + 2 * t, r = 16 * bi + g;
+                As[c * kAs + r] = -res[nh][0];
+                As[(c + 1) * kAs + r] = -res[nh][1];
+                As[c * kAs + r + 8] = -res[nh][2];
+                As[(c + 1) * kAs + r + 8] = -res[nh][3];
+                tt_put2<IO>(tt, r, c, -res[nh][0], -res[nh][1], beta, gam);
+                tt_put2<IO>(tt, r + 8, c, -res[nh][2], -res[nh][3], beta, gam);
+            }
+            __syncwarp();
         }
-        __syncthreads();
     }
 }
 
-template <typename IO, int NV>
+template <typename IO>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
-    using PL = Plan<NV>;
     constexpr bool kBf16 = std::is_same<IO, __nv_bfloat16>::value;
-    constexpr int NSL = kDK / NV;                 // column slices per head
-    constexpr int HALF = NV / 2;                  // columns per thread in 2-warp splits
     constexpr uint32_t kIdD1 = idesc_f16(kBf16, 128, 64, false, false);
     constexpr uint32_t kIdD2 = idesc_f16(kBf16, 128, 128, false, true);
-    constexpr uint32_t kIdNV = idesc_f16(kBf16, 128, NV, false, true);
-    constexpr uint32_t kIdDS = idesc_f16(kBf16, 128, NV, true, true);
+    constexpr uint32_t kIdNV = idesc_f16(kBf16, 128, kNV, false, true);
+    constexpr uint32_t kIdDS = idesc_f16(kBf16, 128, kNV, true, true);
+    const uint32_t kStageTx = 2 * 2 * 8192 + 8192 + (p.gate_tma ? 2048 : 0);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-    __shared__ uint64_t bar_load, bar_mma;
-    __shared__ uint32_t s_tmem;
-    __shared__ float sG[kC], sBeta[kC], sGam[kC], sKf[kC];
-    __shared__ float s_wsum[2];
-    __shared__ float sX[3][16][17];
+    __shared__ Ctl ctl;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;
-    const int slice = blockIdx.x % NSL;
-    const int h = (blockIdx.x / NSL) % p.h_v;
-    const int64_t n = (int64_t)(blockIdx.x / NSL) / p.h_v;
+    const int slice = blockIdx.x & 1;
+    const int h = (blockIdx.x >> 1) % p.h_v;
+    const int64_t n = (int64_t)(blockIdx.x >> 1) / p.h_v;
     const int hq = h / (p.h_v / p.h_qk);
-    const int v0 = slice * NV;
+    const int v0 = slice * kNV;
 
     int64_t t0, t1;
     if (!seq_range(p.cu_seqlens, p.seqlen, p.num_seqs, p.status, n, t0, t1)) return;
+    const int64_t L = t1 - t0;
+    const int nchunks = (int)((L + kC - 1) / kC);
 
-    uint8_t *const sKQW = sm + PL::KQW, *const sV = sm + PL::V, *const sKT = sm + PL::KT;
-    uint8_t *const sTT = sm + PL::TT, *const sPZ = sm + PL::PZ, *const sSB = sm + PL::SB;
-    uint8_t *const sDB = sm + PL::DB;
-    float *const As = reinterpret_cast<float *>(sm + PL::AS);
-    float *const Ts = reinterpret_cast<float *>(sm + PL::TS);
+    float *const As = reinterpret_cast<float *>(sm + OFF_AS);
+    const uint32_t aStage = smem_u32(sm + OFF_STAGE), aPZ = smem_u32(sm + OFF_PZ);
+    const uint32_t aTT = smem_u32(sm + OFF_TT), aSB = smem_u32(sm + OFF_SB);
+    const uint32_t aDB0 = smem_u32(sm + OFF_DB0), aDB1 = smem_u32(sm + OFF_DB1);
 
     if (warp == 0) {
-        tmem_alloc(&s_tmem, 512);
+        tmem_alloc(&ctl.tmem, 512);
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&bar_load, 1);
-        mbar_init(&bar_mma, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ctl.full[i], 1);
+            mbar_init(&ctl.prep_done[i], 1);
+            mbar_init(&ctl.chain_done[i], 1);
+        }
+        mbar_init(&ctl.d1, 1);
+        mbar_init(&ctl.d23, 1);
+        mbar_init(&ctl.d4, 1);
+        mbar_init(&ctl.d5, 1);
+        ctl.abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&p.tm_q);
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_v);
     }
-    // Zero rows 64-127 of [P; 0] once.
-    for (int e = tid; e < 8192 / 16; e += kThreads)
-        *reinterpret_cast<uint4 *>(sPZ + 8192 + 16 * e) = make_uint4(0, 0, 0, 0);
+    // Rows 64-127 of both [P; 0] tiles stay zero, and so do the blocks of [T'; T'']
+    // above the diagonal (the inverse writes only the blocks on and below it).
+    for (int e = tid; e < 2 * 8192 / 16; e += kThreads)
+        *reinterpret_cast<uint4 *>(sm + OFF_PZ + (e >> 9) * 16384 + 8192 + 16 * (e & 511)) =
+            make_uint4(0, 0, 0, 0);
+    for (int e = tid; e < 16384 / 16; e += kThreads)
+        *reinterpret_cast<uint4 *>(sm + OFF_TT + 16 * e) = make_uint4(0, 0, 0, 0);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-
-    const uint32_t tmem = s_tmem;
-    const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
-    const int row = 32 * quarter + lane;           // this thread's TMEM lane
-    const IO *ga = static_cast<const IO *>(p.a);
-    const IO *gb = static_cast<const IO *>(p.b);
-    IO *go = static_cast<IO *>(p.o);
-    const float A_log = p.A_log[h], dt_bias = p.dt_bias[h];
+    const uint32_t tmem = ctl.tmem;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const size_t sbase = ((size_t)n * p.h_v + h) * kDK * kDK;
 
-    // Initial state -> DS (thread: row `row`, columns [half*HALF, +HALF)).
+    auto issue_stage = [&](int c) {   // TMA of chunk c into stage c & 1 (one thread)
+        const int s = c & 1;
+        uint8_t *st = sm + OFF_STAGE + s * kStage;
+        const int tok = (int)(t0 + (int64_t)c * kC);
+        mbar_arrive_expect_tx(&ctl.full[s], kStageTx);
 #pragma unroll
-    for (int c0 = 0; c0 < HALF; c0 += 32) {
-        const int col = half * HALF + c0;
-        uint32_t r[32];
-        if (p.state_in != nullptr) {
-            const float4 *src =
-                reinterpret_cast<const float4 *>(p.state_in + sbase + (size_t)row * kDK + v0 + col);
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-                const float4 f = src[q4];
-                r[4 * q4 + 0] = __float_as_uint(f.x);
-                r[4 * q4 + 1] = __float_as_uint(f.y);
-                r[4 * q4 + 2] = __float_as_uint(f.z);
-                r[4 * q4 + 3] = __float_as_uint(f.w);
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = 0u;
+        for (int r = 0; r < 2; ++r) {
+            tma_load_3d(st + r * kRegion, &p.tm_k, r * 64, hq, tok, &ctl.full[s]);
+            tma_load_3d(st + r * kRegion + 8192, &p.tm_q, r * 64, hq, tok, &ctl.full[s]);
         }
-        tmem_st32(tmem + lane_base + PL::tDS + col, r);
-    }
-    tmem_st_wait();
+        tma_load_3d(st + 2 * kRegion, &p.tm_v, v0, h, tok, &ctl.full[s]);
+        if (p.gate_tma) {
+            tma_load_2d(st + kGates, &p.tm_a, h & ~7, tok, &ctl.full[s]);
+            tma_load_2d(st + kGates + 1024, &p.tm_b, h & ~7, tok, &ctl.full[s]);
+        }
+    };
 
-    uint32_t ph_load = 0, ph_mma = 0;
-    bool failed = false;
-    const int64_t L = t1 - t0;
-    const int64_t nchunks = (L + kC - 1) / kC;
-    const uint32_t aKQW = smem_u32(sKQW), aV = smem_u32(sV), aKT = smem_u32(sKT);
-    const uint32_t aTT = smem_u32(sTT), aPZ = smem_u32(sPZ), aSB = smem_u32(sSB);
-    const uint32_t aDB = smem_u32(sDB);
+    if (tid < kPrepThreads) {
+        // ============================================================== prep role
+        const int pt = tid;
+        const int q = warp & 3, hf = warp >> 2;    // TMEM lane quarter, column half
+        const IO *ga = static_cast<const IO *>(p.a);
+        const IO *gb = static_cast<const IO *>(p.b);
+        const float A_log = p.A_log[h], dt_bias = p.dt_bias[h];
+        float ra = 0.f, rb = 0.f;                  // this thread's gate logits, next chunk
+        if (!p.gate_tma && pt < kC && pt < L) {
+            ra = IoType<IO>::ld(ga + (size_t)(t0 + pt) * p.h_v + h);
+            rb = IoType<IO>::ld(gb + (size_t)(t0 + pt) * p.h_v + h);
+        }
+        bool failed = false;
+        for (int c = 0; c < nchunks; ++c) {
+            const int b = c & 1, s = c & 1;
+            const int64_t tc0 = t0 + (int64_t)c * kC;
+            const int Lc = (int)((L - (int64_t)c * kC) < kC ? (L - (int64_t)c * kC) : kC);
+            bool ok = true;
+            if (c >= 2) ok = mbar_wait(&ctl.chain_done[b], ((c >> 1) - 1) & 1, kWaitBudget);
+            if (ok) ok = mbar_wait(&ctl.full[s], (c >> 1) & 1, kWaitBudget);
+            if (bar_any(kBarPrep, kPrepThreads, !ok || *(volatile int *)&ctl.abort)) { failed = true; break; }
 
-    for (int64_t c = 0; c < nchunks && !failed; ++c) {
-        const int64_t tc0 = t0 + c * kC;
-        const int Lc = (int)((L - c * kC) < kC ? (L - c * kC) : kC);
-
-        // (1) TMA: K and Q of the q/k head, V columns of this slice.
-        if (tid == 0) {
-            mbar_arrive_expect_tx(&bar_load, 2 * 2 * 8192 + (NV / 64) * 8192);
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                tma_load_3d(sKQW + r * PL::kRegion, &p.tm_k, r * 64, hq, (int)tc0, &bar_load);
-                tma_load_3d(sKQW + r * PL::kRegion + 8192, &p.tm_q, r * 64, hq, (int)tc0, &bar_load);
-            }
-#pragma unroll
-            for (int r = 0; r < NV / 64; ++r)
-                tma_load_3d(sV + r * 8192, &p.tm_v, v0 + r * 64, h, (int)tc0, &bar_load);
-        }
-        // (2) Gates and their within-chunk prefix sum (threads 0-63 = tokens).
-        float gsum = 0.f;
-        if (tid < kC) {
-            float g = 0.f, be = 0.f;
-            if (tid < Lc) {
-                const size_t gi = (size_t)(tc0 + tid) * p.h_v + h;
-                g = decay_f(IoType<IO>::ld(ga + gi), A_log, dt_bias);
-                be = sigmoid_f(IoType<IO>::ld(gb + gi));
-            }
-            gsum = g;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, gsum, off);
-                if (lane >= off) gsum += y;
-            }
-            if (lane == 31) s_wsum[warp] = gsum;
-            sBeta[tid] = be;
-        }
-        __syncthreads();
-        if (tid < kC) sG[tid] = gsum + (warp == 1 ? s_wsum[0] : 0.f);
-        __syncthreads();
-        const float GC = sG[kC - 1];
-        if (tid < kC) {
-            sGam[tid] = expf(sG[tid]);
-            sKf[tid] = expf(GC - sG[tid]);
-        }
-        const bool ok_load = mbar_wait(&bar_load, ph_load, kWaitBudget);
-        ph_load ^= 1;
-        if (__syncthreads_or(!ok_load)) { failed = true; break; }
-
-        // (3) D1 = [K; Q] K^T.
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t off = (s >> 2) * PL::kRegion + (s & 3) * 32;
-                mma_f16(tmem + PL::tD1, sw128_desc(aKQW + off, 16, 1024),
-                        sw128_desc(aKQW + off, 16, 1024), kIdD1, s > 0);
-            }
-            mma_commit(&bar_mma);
-        }
-        // Meanwhile: Ktil = diag(e^{G_C - G_j}) K, same swizzled layout as the K tile.
-        for (int e = tid; e < 1024; e += kThreads) {
-            const int r = e >> 9, j = (e >> 3) & 63, ch = e & 7;
-            const uint32_t off = sw128_offset(j, ch);
-            const uint4 u = *reinterpret_cast<const uint4 *>(sKQW + r * PL::kRegion + off);
-            const float f = sKf[j];
-            float x[8];
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float2 t = Pack<IO>::unpack(w[q]);
-                x[2 * q] = t.x * f;
-                x[2 * q + 1] = t.y * f;
-            }
-            *reinterpret_cast<uint4 *>(sKT + r * 8192 + off) = pack8<IO>(x);
-        }
-        fence_async_smem();
-        bool ok = mbar_wait(&bar_mma, ph_mma, kWaitBudget);
-        ph_mma ^= 1;
-        tc_fence_after();
-
-        // (4) A from k.k (lanes 0-63), P from q.k (lanes 64-127); each half-warp group
-        //     takes 32 of the 64 columns.
-        {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_base + PL::tD1 + 32 * half, r);
-            tmem_ld_wait();
-            if (quarter < 2) {
-                const int i = row;
-                const float Gi = sG[i], bi = sBeta[i];
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int j = 32 * half + jj;
-                    As[i * 65 + j] = (j < i) ? bi * __expf(Gi - sG[j]) * __uint_as_float(r[jj]) : 0.f;
+            // Gates and prefix sums (threads 0-63 = tokens of the chunk).
+            float gsum = 0.f, be = 0.f;
+            if (pt < kC) {
+                if (p.gate_tma) {
+                    const IO *gt = reinterpret_cast<const IO *>(sm + OFF_STAGE + s * kStage + kGates);
+                    ra = IoType<IO>::ld(gt + pt * 8 + (h & 7));
+                    rb = IoType<IO>::ld(gt + 512 + pt * 8 + (h & 7));
                 }
-            } else {
-                const int i = row - 64;
-                const float Gi = sG[i];
+                if (pt < Lc) {
+                    gsum = decay_f(ra, A_log, dt_bias);
+                    be = sigmoid_f(rb);
+                }
 #pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
-                    float x[8];
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, gsum, off);
+                    if (lane >= off) gsum += y;
+                }
+                if (lane == 31) ctl.wsum[warp] = gsum;
+                // Without gate TMA, prefetch the next chunk's gate logits.
+                const int64_t tn = tc0 + kC + pt;
+                ra = rb = 0.f;
+                if (!p.gate_tma && tn < t1) {
+                    ra = IoType<IO>::ld(ga + (size_t)tn * p.h_v + h);
+                    rb = IoType<IO>::ld(gb + (size_t)tn * p.h_v + h);
+                }
+            }
+            named_bar(kBarPrep, kPrepThreads);
+            if (pt < kC) {
+                ctl.G[pt] = gsum + (warp == 1 ? ctl.wsum[0] : 0.f);
+                ctl.beta[pt] = be;
+            }
+            named_bar(kBarPrep, kPrepThreads);
+            const float GC = ctl.G[kC - 1], Gm = ctl.G[31];
+            const bool safe = (ctl.G[0] - GC) <= 80.f;   // e^{G_i - G_m} e^{G_m - G_j} cannot overflow
+            if (pt < kC) {
+                const float G = ctl.G[pt];
+                ctl.gam[b][pt] = expf(G);
+                ctl.kf[b][pt] = expf(GC - G);
+                ctl.E[pt] = expf(G - Gm);
+                ctl.F[pt] = expf(Gm - G);
+                if (pt == 0) ctl.gC[b] = expf(GC);
+            }
+            named_bar(kBarPrep, kPrepThreads);   // E, F, gamma visible to every prep warp
+
+            // D1 = [K; Q] K^T once the stage has landed.
+            if (pt == 0) {
+                tc_fence_after();
+                const uint32_t st = aStage + s * kStage;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int j = 32 * half + 8 * q8 + e;
-                        x[e] = (j <= i) ? p.scale * __expf(Gi - sG[j]) * __uint_as_float(r[8 * q8 + e])
-                                        : 0.f;
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t off = (k >> 2) * kRegion + (k & 3) * 32;
+                    mma_f16(tmem + TM_D1, sw128_desc(st + off, 16, 1024),
+                            sw128_desc(st + off, 16, 1024), kIdD1, k > 0);
+                }
+                mma_commit(&ctl.d1);
+            }
+            ok = mbar_wait(&ctl.d1, c & 1, kWaitBudget);
+            tc_fence_after();
+
+            // A rows (lanes 0-63, fp32) and P rows (lanes 64-127, I/O type); each column
+            // half of the prep warps takes 32 of the 64 columns.
+            {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + TM_D1 + 32 * hf, r);
+                tmem_ld_wait();
+                const int i = (32 * q + lane) & 63;
+                const float Ei = ctl.E[i], Gi = ctl.G[i];
+                if (q < 2) {
+                    const float bi = ctl.beta[i];
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        float x[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = 32 * hf + 4 * j4 + e;
+                            const float d = safe ? Ei * ctl.F[j] : __expf(Gi - ctl.G[j]);
+                            x[e] = (j < i) ? bi * d * __uint_as_float(r[4 * j4 + e]) : 0.f;
+                        }
+                        *reinterpret_cast<float4 *>(As + i * kAs + 32 * hf + 4 * j4) =
+                            make_float4(x[0], x[1], x[2], x[3]);
                     }
-                    *reinterpret_cast<uint4 *>(sPZ + sw128_offset(i, 4 * half + q8)) = pack8<IO>(x);
+                } else {
+                    uint8_t *pz = sm + OFF_PZ + b * 16384;
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        float x[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int j = 32 * hf + 8 * q8 + e;
+                            const float d = safe ? Ei * ctl.F[j] : __expf(Gi - ctl.G[j]);
+                            x[e] = (j <= i) ? p.scale * d * __uint_as_float(r[8 * q8 + e]) : 0.f;
+                        }
+                        *reinterpret_cast<uint4 *>(pz + sw128_offset(i, 4 * hf + q8)) = pack8<IO>(x);
+                    }
                 }
             }
-        }
-        fence_async_smem();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
+            fence_async_smem();
+            if (bar_any(kBarPrep, kPrepThreads, !ok)) { failed = true; break; }
 
-        // (5) T = (I + A)^-1, then [T'; T''] in the I/O type, K-major.
-        invert_unit_lower_64(As, Ts, sX, tid);
-        for (int e = tid; e < 128 * 8; e += kThreads) {
-            const int R = e >> 3, ch = e & 7, i = R & 63;
-            float x[8];
+            // T = (I + A)^-1, written as [T diag(beta gamma); T diag(beta)] (K-major).
+            invert_chunk<IO>(As, ctl.X, sm + OFF_TT, ctl.beta, ctl.gam[b], pt);
+            fence_async_smem();
+            tc_fence_before();
+            named_bar(kBarPrep, kPrepThreads);
+
+            // D2 = [T'; T''] K and D3 = [T'; T''] V (B operands MN-major from the stage).
+            if (pt == 0) {
+                tc_fence_after();
+                const uint32_t st = aStage + s * kStage;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int j = 8 * ch + q;
-                const float f = (R < 64) ? sBeta[j] * sGam[j] : sBeta[j];
-                x[q] = (j <= i) ? Ts[i * 65 + j] * f : 0.f;
+                for (int k = 0; k < 4; ++k) {
+                    const uint64_t da = sw128_desc(aTT + k * 32, 16, 1024);
+                    mma_f16(tmem + TM_D2, da, sw128_desc(st + k * 2048, kRegion, 1024), kIdD2, k > 0);
+                    mma_f16(tmem + TM_D3 + 64 * b, da, sw128_desc(st + 2 * kRegion + k * 2048, 8192, 1024),
+                            kIdNV, k > 0);
+                }
+                mma_commit(&ctl.d23);
             }
-            *reinterpret_cast<uint4 *>(sTT + sw128_offset(R, ch)) = pack8<IO>(x);
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // (6) D2 = [T'; T''] K, D3 = [T'; T''] V (B operands MN-major from the TMA tiles).
-        if (tid == 0) {
+            ok = mbar_wait(&ctl.d23, c & 1, kWaitBudget);
             tc_fence_after();
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t da = sw128_desc(aTT + s * 32, 16, 1024);
-                mma_f16(tmem + PL::tD24, da, sw128_desc(aKQW + s * 2048, PL::kRegion, 1024), kIdD2,
-                        s > 0);
-                mma_f16(tmem + PL::tD35, da, sw128_desc(aV + s * 2048, 8192, 1024), kIdNV, s > 0);
-            }
-            mma_commit(&bar_mma);
-        }
-        // Meanwhile: S0 (TMEM) -> bf16 B operand (MN-major: row = d_k index), then
-        // DS <- gamma_C * S0, to which the chunk's K^T Delta is added below.
-        {
-            const float gC = expf(GC);
-#pragma unroll
-            for (int c0 = 0; c0 < HALF; c0 += 32) {
-                const int col = half * HALF + c0;           // within the slice
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_base + PL::tDS + col, r);
-                tmem_ld_wait();
-                float x[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
-                uint8_t *dst = sSB + (col >> 6) * 16384;
-#pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8)
-                    *reinterpret_cast<uint4 *>(dst + sw128_offset(row, ((col & 63) >> 3) + q8)) =
-                        pack8<IO>(x + 8 * q8);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[j] * gC);
-                tmem_st32(tmem + lane_base + PL::tDS + col, r);
-            }
-            tmem_st_wait();
-        }
-        fence_async_smem();
-        ok = mbar_wait(&bar_mma, ph_mma, kWaitBudget);
-        ph_mma ^= 1;
-        tc_fence_after();
 
-        // (7) W (lanes 0-63 of D2) -> rows 128-191 of the K|Q|W regions.
-        if (quarter < 2) {
+            // W (lanes 0-63 of D2) -> rows 128-191 of the stage's K|Q|W regions.
+            if (q < 2) {
+                const int i = 32 * q + lane;
+                uint8_t *reg = sm + OFF_STAGE + s * kStage + hf * kRegion;
 #pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_base + PL::tD24 + 64 * half + c0, r);
-                tmem_ld_wait();
-                float x[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
-#pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8)
-                    *reinterpret_cast<uint4 *>(sKQW + half * PL::kRegion +
-                                               sw128_offset(128 + row, (c0 >> 3) + q8)) =
-                        pack8<IO>(x + 8 * q8);
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-
-        // (8) D4 = [Q; W] S0.
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t off = (s >> 2) * PL::kRegion + 8192 + (s & 3) * 32;
-                mma_f16(tmem + PL::tD24, sw128_desc(aKQW + off, 16, 1024),
-                        sw128_desc(aSB + s * 2048, 16384, 1024), kIdNV, s > 0);
-            }
-            mma_commit(&bar_mma);
-        }
-        ok = mbar_wait(&bar_mma, ph_mma, kWaitBudget);
-        ph_mma ^= 1;
-        tc_fence_after();
-
-        // (9) Delta = U - W S0 (lanes 64-127), written MN-major (row = token).
-        if (quarter >= 2) {
-            const int j = row - 64;
-#pragma unroll
-            for (int c0 = 0; c0 < HALF; c0 += 32) {
-                const int col = half * HALF + c0;
-                uint32_t ws[32], u[32];
-                tmem_ld32(tmem + lane_base + PL::tD24 + col, ws);
-                tmem_ld32(tmem + lane_base + PL::tD35 + col, u);
-                tmem_ld_wait();
-                float x[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(u[e]) - __uint_as_float(ws[e]);
-                uint8_t *dst = sDB + (col >> 6) * 8192;
-#pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8)
-                    *reinterpret_cast<uint4 *>(dst + sw128_offset(j, ((col & 63) >> 3) + q8)) =
-                        pack8<IO>(x + 8 * q8);
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-
-        // (10) D5 = [P; 0] Delta;  DS += Ktil^T Delta.
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t db = sw128_desc(aDB + s * 2048, 8192, 1024);
-                mma_f16(tmem + PL::tD35, sw128_desc(aPZ + s * 32, 16, 1024), db, kIdNV, s > 0);
-                mma_f16(tmem + PL::tDS, sw128_desc(aKT + s * 2048, 8192, 1024), db, kIdDS, 1u);
-            }
-            mma_commit(&bar_mma);
-        }
-        ok = mbar_wait(&bar_mma, ph_mma, kWaitBudget);
-        ph_mma ^= 1;
-        tc_fence_after();
-
-        // (11) o_i = scale gamma_i (Q S0)_i + (P Delta)_i for the chunk's valid rows.
-        if (quarter < 2) {
-            const int i = row;
-            const float f = p.scale * sGam[i];
-#pragma unroll
-            for (int c0 = 0; c0 < HALF; c0 += 32) {
-                const int col = half * HALF + c0;
-                uint32_t qs[32], pd[32];
-                tmem_ld32(tmem + lane_base + PL::tD24 + col, qs);
-                tmem_ld32(tmem + lane_base + PL::tD35 + col, pd);
-                tmem_ld_wait();
-                if (i < Lc) {
+                for (int c0 = 0; c0 < 64; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_base + TM_D2 + 64 * hf + c0, r);
+                    tmem_ld_wait();
                     float x[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        x[e] = fmaf(f, __uint_as_float(qs[e]), __uint_as_float(pd[e]));
-                    uint4 *dst = reinterpret_cast<uint4 *>(
-                        go + ((size_t)(tc0 + i) * p.h_v + h) * kDK + v0 + col);
+                    for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
 #pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8) dst[q8] = pack8<IO>(x + 8 * q8);
+                    for (int q8 = 0; q8 < 4; ++q8)
+                        *reinterpret_cast<uint4 *>(reg + sw128_offset(128 + i, (c0 >> 3) + q8)) =
+                            pack8<IO>(x + 8 * q8);
                 }
             }
+            fence_async_smem();
+            tc_fence_before();
+            if (bar_any(kBarPrep, kPrepThreads, !ok)) { failed = true; break; }
+            if (pt == 0) mbar_arrive(&ctl.prep_done[b]);
         }
-        tc_fence_before();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
+        if (failed && pt == 0) {
+            ctl.abort = 1;
+            atomicOr(p.status, kDevTimeout);
+        }
+    } else {
+        // ============================================================== chain role
+        const int ct = tid - kPrepThreads;         // = TMEM lane = d_k row of S
+        const int cw = ct >> 5;
+        IO *go = static_cast<IO *>(p.o);
+        float S[kNV];
+        {
+            const float4 *src = reinterpret_cast<const float4 *>(p.state_in + sbase +
+                                                                 (size_t)ct * kDK + v0);
+#pragma unroll
+            for (int q4 = 0; q4 < kNV / 4; ++q4) {
+                const float4 f = p.state_in ? src[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
+                S[4 * q4] = f.x; S[4 * q4 + 1] = f.y; S[4 * q4 + 2] = f.z; S[4 * q4 + 3] = f.w;
+            }
+        }
+        auto write_sb = [&]() {   // S (fp32 registers) -> MN-major operand tile, row = ct
+#pragma unroll
+            for (int q8 = 0; q8 < 8; ++q8)
+                *reinterpret_cast<uint4 *>(sm + OFF_SB + sw128_offset(ct, q8)) = pack8<IO>(S + 8 * q8);
+        };
+        write_sb();
+        fence_async_smem();
+        if (ct == 0) {
+            if (nchunks > 0) issue_stage(0);
+            if (nchunks > 1) issue_stage(1);
+        }
+        named_bar(kBarChain, kChainThreads);
+        bool failed = false;
+        for (int c = 0; c < nchunks; ++c) {
+            const int b = c & 1, s = c & 1;
+            const int64_t tc0 = t0 + (int64_t)c * kC;
+            const int Lc = (int)((L - (int64_t)c * kC) < kC ? (L - (int64_t)c * kC) : kC);
+            bool ok = mbar_wait(&ctl.prep_done[b], (c >> 1) & 1, kWaitBudget);
+            if (bar_any(kBarChain, kChainThreads, !ok || *(volatile int *)&ctl.abort)) { failed = true; break; }
+            tc_fence_after();
+            const uint32_t st = aStage + s * kStage;
+
+            // D4 = [Q; W] S0.
+            if (ct == 0) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t off = (k >> 2) * kRegion + 8192 + (k & 3) * 32;
+                    mma_f16(tmem + TM_D4, sw128_desc(st + off, 16, 1024),
+                            sw128_desc(aSB + k * 2048, 16384, 1024), kIdNV, k > 0);
+                }
+                mma_commit(&ctl.d4);
+            }
+            ok = mbar_wait(&ctl.d4, c & 1, kWaitBudget);
+            tc_fence_after();
+
+            // Delta = U - W S0 on lanes 64-127 (token rows), in two versions.
+            if (cw >= 2) {
+                const int j = ct - 64;
+                const float kfj = ctl.kf[b][j];
+#pragma unroll
+                for (int c0 = 0; c0 < kNV; c0 += 32) {
+                    uint32_t ws[32], u[32];
+                    tmem_ld32(tmem + lane_base + TM_D4 + c0, ws);
+                    tmem_ld32(tmem + lane_base + TM_D3 + 64 * b + c0, u);
+                    tmem_ld_wait();
+                    float x[32], y[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        x[e] = __uint_as_float(u[e]) - __uint_as_float(ws[e]);
+                        y[e] = kfj * x[e];
+                    }
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        const uint32_t off = sw128_offset(j, (c0 >> 3) + q8);
+                        *reinterpret_cast<uint4 *>(sm + OFF_DB0 + off) = pack8<IO>(x + 8 * q8);
+                        *reinterpret_cast<uint4 *>(sm + OFF_DB1 + off) = pack8<IO>(y + 8 * q8);
+                    }
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            if (bar_any(kBarChain, kChainThreads, !ok)) { failed = true; break; }
+
+            // D5 = [P; 0] Delta;  DS = K^T diag(e^{G_C - G}) Delta.
+            if (ct == 0) {
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    mma_f16(tmem + TM_D5, sw128_desc(aPZ + b * 16384 + k * 32, 16, 1024),
+                            sw128_desc(aDB0 + k * 2048, 8192, 1024), kIdNV, k > 0);
+                    mma_f16(tmem + TM_DS, sw128_desc(st + k * 2048, kRegion, 1024),
+                            sw128_desc(aDB1 + k * 2048, 8192, 1024), kIdDS, k > 0);
+                }
+                mma_commit(&ctl.d5);
+            }
+            ok = mbar_wait(&ctl.d5, c & 1, kWaitBudget);
+            tc_fence_after();
+            // The stage's last readers are done: refill it with chunk c + 2.
+            if (ct == 0 && ok && c + 2 < nchunks) issue_stage(c + 2);
+
+            // S = gamma_C S0 + DS (fp32 registers), then the next chunk's operand tile.
+            {
+                const float gC = ctl.gC[b];
+#pragma unroll
+                for (int c0 = 0; c0 < kNV; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_base + TM_DS + c0, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) S[c0 + e] = fmaf(gC, S[c0 + e], __uint_as_float(r[e]));
+                }
+                write_sb();
+            }
+            // o_i = scale gamma_i (Q S0)_i + (P Delta)_i on lanes 0-63.
+            if (cw < 2) {
+                const int i = ct;
+                const float f = p.scale * ctl.gam[b][i];
+#pragma unroll
+                for (int c0 = 0; c0 < kNV; c0 += 32) {
+                    uint32_t qs[32], pd[32];
+                    tmem_ld32(tmem + lane_base + TM_D4 + c0, qs);
+                    tmem_ld32(tmem + lane_base + TM_D5 + c0, pd);
+                    tmem_ld_wait();
+                    if (i < Lc) {
+                        float x[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            x[e] = fmaf(f, __uint_as_float(qs[e]), __uint_as_float(pd[e]));
+                        uint4 *dst = reinterpret_cast<uint4 *>(
+                            go + ((size_t)(tc0 + i) * p.h_v + h) * kDK + v0 + c0);
+#pragma unroll
+                        for (int q8 = 0; q8 < 4; ++q8) dst[q8] = pack8<IO>(x + 8 * q8);
+                    }
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            if (bar_any(kBarChain, kChainThreads, !ok)) { failed = true; break; }
+            if (ct == 0) mbar_arrive(&ctl.chain_done[b]);
+        }
+        if (failed) {
+            if (ct == 0) {
+                ctl.abort = 1;
+                atomicOr(p.status, kDevTimeout);
+            }
+        } else {
+            float4 *dst = reinterpret_cast<float4 *>(p.state_out + sbase + (size_t)ct * kDK + v0);
+#pragma unroll
+            for (int q4 = 0; q4 < kNV / 4; ++q4)
+                dst[q4] = make_float4(S[4 * q4], S[4 * q4 + 1], S[4 * q4 + 2], S[4 * q4 + 3]);
+        }
     }
 
-    if (failed) {
-        if (tid == 0) atomicOr(p.status, kDevTimeout);
-        // Let any MMA still in flight drain (bounded) before TMEM is released.
-        mbar_wait(&bar_mma, ph_mma, kWaitBudget);
-    } else {
-        // Final state: DS -> state_out (fp32).
-#pragma unroll
-        for (int c0 = 0; c0 < HALF; c0 += 32) {
-            const int col = half * HALF + c0;
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_base + PL::tDS + col, r);
-            tmem_ld_wait();
-            float4 *dst = reinterpret_cast<float4 *>(p.state_out + sbase + (size_t)row * kDK + v0 + col);
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-                dst[q4] = make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]),
-                                      __uint_as_float(r[4 * q4 + 2]), __uint_as_float(r[4 * q4 + 3]));
-        }
-    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -582,18 +672,32 @@ bool make_map(CUtensorMap *m, const void *base, gdn_dtype io, int heads, int64_t
     return r == CUDA_SUCCESS;
 }
 
-template <typename IO, int NV>
+// 2-D map over the [tokens][h_v] gate logits with 8-head x 64-token boxes.
+bool make_gate_map(CUtensorMap *m, const void *base, gdn_dtype io, int h_v, int64_t tokens) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)h_v, (cuuint64_t)tokens};
+    const cuuint64_t strides[1] = {(cuuint64_t)h_v * 2};
+    const cuuint32_t box[2] = {8, (cuuint32_t)kC};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, io == GDN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <typename IO>
 cudaError_t launch_typed(const TcParams &tp, int64_t units, cudaStream_t stream) {
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<IO, NV>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Plan<NV>::kAlloc);
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<IO>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const int64_t blocks = units * (kDK / NV);
-    prefill_tc_kernel<IO, NV><<<(unsigned)blocks, kThreads, Plan<NV>::kAlloc, stream>>>(tp);
+    const int64_t blocks = units * (kDK / kNV);
+    prefill_tc_kernel<IO><<<(unsigned)blocks, kThreads, kSmemAlloc, stream>>>(tp);
     return cudaGetLastError();
 }
 
@@ -610,29 +714,30 @@ bool prefill_tc_supported(const ScanParams &p, gdn_dtype io, int64_t total_token
     return encode_fn() != nullptr;
 }
 
-int prefill_tc_columns(const ScanParams &p) {
-    // Few (sequence, head) units: split the columns to put more CTAs on the SMs.
-    return ((int64_t)p.num_seqs * p.h_v >= 120) ? 128 : 64;
-}
+int prefill_tc_columns(const ScanParams &) { return kNV; }
 
 cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_tokens, int nv,
                               cudaStream_t stream) {
+    if (nv != kNV) return cudaErrorInvalidValue;
     TcParams tp;
     memset(&tp, 0, sizeof(tp));
     if (!make_map(&tp.tm_q, p.q, io, p.h_qk, total_tokens) ||
         !make_map(&tp.tm_k, p.k, io, p.h_qk, total_tokens) ||
         !make_map(&tp.tm_v, p.v, io, p.h_v, total_tokens))
         return cudaErrorInvalidValue;
+    // Gate logits ride along with each stage's TMA when their rows are 16-byte multiples.
+    tp.gate_tma = (p.h_v % 8 == 0 && reinterpret_cast<uintptr_t>(p.a) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(p.b) % 16 == 0 &&
+                   make_gate_map(&tp.tm_a, p.a, io, p.h_v, total_tokens) &&
+                   make_gate_map(&tp.tm_b, p.b, io, p.h_v, total_tokens))
+                      ? 1 : 0;
     tp.a = p.a; tp.b = p.b; tp.A_log = p.A_log; tp.dt_bias = p.dt_bias;
     tp.state_in = p.state_in; tp.state_out = p.state_out; tp.o = p.o;
     tp.cu_seqlens = p.cu_seqlens; tp.seqlen = p.seqlen; tp.num_seqs = p.num_seqs;
     tp.h_qk = p.h_qk; tp.h_v = p.h_v; tp.scale = p.scale; tp.status = p.status;
     const int64_t units = (int64_t)p.num_seqs * p.h_v;
-    if (io == GDN_BF16)
-        return nv == 64 ? launch_typed<__nv_bfloat16, 64>(tp, units, stream)
-                        : launch_typed<__nv_bfloat16, 128>(tp, units, stream);
-    return nv == 64 ? launch_typed<__half, 64>(tp, units, stream)
-                    : launch_typed<__half, 128>(tp, units, stream);
+    if (io == GDN_BF16) return launch_typed<__nv_bfloat16>(tp, units, stream);
+    return launch_typed<__half>(tp, units, stream);
 }
 
 }  // namespace gdn
