@@ -49,7 +49,7 @@ constexpr uint32_t kBarPrep = 1, kBarChain = 2;
 constexpr long long kWaitBudget = 4000000000LL;   // cycles (~2 s) before a wait gives up
 
 struct TcParams {
-    CUtensorMap tm_q, tm_k, tm_v;
+    CUtensorMap tm_q, tm_k, tm_v, tm_o;
     CUtensorMap tm_a, tm_b;        // gate logits [tokens][h_v], used when gate_tma != 0
     int32_t gate_tma;
     const void *a, *b;
@@ -69,9 +69,10 @@ constexpr int kRegion = 24576;                 // 192 rows x 128 B: K | Q | W fo
 constexpr int kGates = 2 * kRegion + 8192;     // gate logit tiles a, b: 64 tokens x 8 heads
 constexpr int kStage = kGates + 2048;          // + V (64 tokens x 64 columns) + gate tiles
 constexpr int OFF_STAGE = 0;                   // two stages
-constexpr int OFF_PZ = 2 * kStage;             // two [P; 0] tiles, 128 x 128 B each
-constexpr int OFF_TT = OFF_PZ + 2 * 16384;     // [T'; T''], 128 x 128 B
-constexpr int OFF_SB = OFF_TT + 16384;         // S0 in the I/O type, MN-major (d_k rows)
+constexpr int OFF_PZ = 2 * kStage;             // two P tiles, 64 x 128 B each
+constexpr int OFF_TT = OFF_PZ + 2 * 8192;      // [T'; T''], 128 x 128 B
+constexpr int OFF_TTR = OFF_TT + 16384;        // [0; T''] received from the peer CTA
+constexpr int OFF_SB = OFF_TTR + 16384;        // S0 in the I/O type, MN-major (d_k rows)
 constexpr int OFF_DB0 = OFF_SB + 16384;        // Delta, MN-major (token rows)
 constexpr int OFF_DB1 = OFF_DB0 + 8192;        // diag(e^{G_C - G}) Delta
 constexpr int OFF_AS = OFF_DB1 + 8192;         // A, then T, fp32 [64][68]
@@ -80,16 +81,25 @@ constexpr int kSmemBytes = OFF_AS + 64 * kAs * 4;
 constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for the 1024-byte alignment
 
 // TMEM columns.
-constexpr uint32_t TM_D1 = 0, TM_D2 = 64, TM_D3 = 192, TM_D4 = 320, TM_D5 = 384, TM_DS = 448;
+constexpr uint32_t TM_D1 = 0, TM_D2 = 64, TM_D3 = 192, TM_D4 = 320, TM_DS = 384;
+
+// Per-chunk gate values the chain needs; sent whole to the peer CTA (16-byte multiple).
+struct __align__(16) GateBuf {
+    float gam[kC];      // e^{G_i}
+    float kf[kC];       // e^{G_C - G_i}
+    float gC, pad[3];   // e^{G_C}
+};
 
 struct Ctl {
     uint64_t full[2], prep_done[2], chain_done[2], d1, d23, d4, d5;
+    uint64_t recv[2], recvd[2], peer_free[2];  // cluster hand-off of the shared chunk prep
     uint32_t tmem;
     int abort;
     float G[kC], beta[kC], E[kC], F[kC], wsum[2];
-    float gam[2][kC], kf[2][kC], gC[2];
-    float X[3][16][20];                        // warp scratch of the T merges
+    GateBuf gb[2];
+    float X[4][16][20];                        // warp scratch of the T merges
 };
+constexpr uint32_t kPeerBytes = 2 * 8192 + 8192 + 8192 + sizeof(GateBuf);
 
 template <typename IO> struct Pack;
 template <> struct Pack<__nv_bfloat16> {
@@ -97,11 +107,17 @@ template <> struct Pack<__nv_bfloat16> {
         __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
         return *reinterpret_cast<uint32_t *>(&v);
     }
+    static __device__ __forceinline__ float2 unpack(uint32_t u) {
+        return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&u));
+    }
 };
 template <> struct Pack<__half> {
     static __device__ __forceinline__ uint32_t two(float a, float b) {
         __half2 v = __floats2half2_rn(a, b);
         return *reinterpret_cast<uint32_t *>(&v);
+    }
+    static __device__ __forceinline__ float2 unpack(uint32_t u) {
+        return __half22float2(*reinterpret_cast<__half2 *>(&u));
     }
 };
 template <typename IO>
@@ -140,13 +156,51 @@ __device__ __forceinline__ void tt_put2(uint8_t *tt, int r, int c, float x0, flo
     *reinterpret_cast<uint32_t *>(tt + 8192 + off) = Pack<IO>::two(x0 * b0, x1 * b1);
 }
 
+// A 16x16 block of a matrix in shared memory: element (r, c) at p[r * rs + c * cs].
+struct Blk {
+    float *p;
+    int rs, cs;
+    __device__ __forceinline__ float at(int r, int c) const { return p[r * rs + c * cs]; }
+};
+
+// acc (16x16 fp32, as two 16x8 halves) += X * Y for 16x16 blocks, with tf32 warp MMAs.
+__device__ __forceinline__ void block_mma(float (&acc)[2][4], const Blk &x, const Blk &y, int g,
+                                          int t) {
+#pragma unroll
+    for (int kh = 0; kh < 2; ++kh) {
+        const uint32_t a[4] = {to_tf32(x.at(g, 8 * kh + t)), to_tf32(x.at(g + 8, 8 * kh + t)),
+                               to_tf32(x.at(g, 8 * kh + t + 4)), to_tf32(x.at(g + 8, 8 * kh + t + 4))};
+#pragma unroll
+        for (int nh = 0; nh < 2; ++nh) {
+            const uint32_t bb[2] = {to_tf32(y.at(8 * kh + t, 8 * nh + g)),
+                                    to_tf32(y.at(8 * kh + t + 4, 8 * nh + g))};
+            mma_tf32_16x8x8(acc[nh], a, bb);
+        }
+    }
+}
+
+__device__ __forceinline__ void block_store(const Blk &d, const float (&acc)[2][4], float sgn, int g,
+                                            int t) {
+#pragma unroll
+    for (int nh = 0; nh < 2; ++nh) {
+        const int c = 8 * nh + 2 * t;
+        d.p[g * d.rs + c * d.cs] = sgn * acc[nh][0];
+        d.p[g * d.rs + (c + 1) * d.cs] = sgn * acc[nh][1];
+        d.p[(g + 8) * d.rs + c * d.cs] = sgn * acc[nh][2];
+        d.p[(g + 8) * d.rs + (c + 1) * d.cs] = sgn * acc[nh][3];
+    }
+}
+
 // T = (I + A)^-1 for the strictly-lower 64 x 64 A in As (prep threads only), written
 // straight into the K-major operand tile [T diag(beta gamma); T diag(beta)].
-// The diagonal 16x16 blocks are solved by forward substitution in fp32, one thread per
-// column, and kept (unscaled) in place in As.  Warp w < 3 then owns column block w and
-// forms the blocks below the diagonal, T_ij = -T_ii (sum_{k=j}^{i-1} A_ik T_kj), with
-// tf32 warp MMAs; each finished block is also kept transposed in the unused upper block
-// (j, i) of As, so A below the diagonal is never overwritten while other warps read it.
+//  1. The diagonal 16x16 blocks T_bb = (I + A_bb)^-1 by forward substitution in fp32,
+//     one thread per column, kept in place in As.
+//  2. 16 -> 32: T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22 (one warp each).
+//  3. 32 -> 64: Y = A_[23][01] T_[01][01], then T_[23][01] = -T_[23][23] Y, one 16x16
+//     block per warp.
+// Blocks below the diagonal use tf32 warp MMAs; each is also kept transposed in the
+// unused upper block of As (T_ij at As[16 j + c][16 i + r]), so A below the diagonal
+// is never overwritten while it is still read.
 template <typename IO>
 __device__ void invert_chunk(float *As, float (*X)[16][20], uint8_t *tt, const float *beta,
                              const float *gam, int pt) {
@@ -170,75 +224,62 @@ __device__ void invert_chunk(float *As, float (*X)[16][20], uint8_t *tt, const f
     }
     named_bar(kBarPrep, kPrepThreads);
     const int w = pt >> 5, lane = pt & 31, g = lane >> 2, t = lane & 3;
-    if (w < 3) {
-        const int bj = w;
-        float *Xw = &X[w][0][0];
-        for (int bi = bj + 1; bi < 4; ++bi) {
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            for (int k = bj; k < bi; ++k) {
-                const bool diag = (k == bj);
+    auto diag = [&](int b) { return Blk{As + 16 * b * kAs + 16 * b, kAs, 1}; };
+    auto low = [&](int i, int j) { return Blk{As + 16 * i * kAs + 16 * j, kAs, 1}; };  // A_ij
+    auto tlo = [&](int i, int j) { return Blk{As + 16 * j * kAs + 16 * i, 1, kAs}; };  // T_ij
+    auto scratch = [&](int k) { return Blk{&X[k][0][0], 20, 1}; };
+    auto emit = [&](int i, int j, const float (&acc)[2][4]) {   // T_ij = -acc
+        block_store(tlo(i, j), acc, -1.f, g, t);
 #pragma unroll
-                for (int kh = 0; kh < 2; ++kh) {
-                    const float *Ab = As + (16 * bi) * kAs + 16 * k + 8 * kh;
-                    const uint32_t a[4] = {to_tf32(Ab[g * kAs + t]), to_tf32(Ab[(g + 8) * kAs + t]),
-                                           to_tf32(Ab[g * kAs + t + 4]),
-                                           to_tf32(Ab[(g + 8) * kAs + t + 4])};
-#pragma unroll
-                    for (int nh = 0; nh < 2; ++nh) {
-                        const int r0 = 16 * k + 8 * kh + t, c0 = 16 * bj + 8 * nh + g;
-                        const uint32_t bb[2] = {
-                            to_tf32(diag ? As[r0 * kAs + c0] : As[c0 * kAs + r0]),
-                            to_tf32(diag ? As[(r0 + 4) * kAs + c0] : As[c0 * kAs + r0 + 4])};
-                        mma_tf32_16x8x8(acc[nh], a, bb);
-                    }
-                }
-            }
-#pragma unroll
-            for (int nh = 0; nh < 2; ++nh) {
-                Xw[g * 20 + 8 * nh + 2 * t] = acc[nh][0];
-                Xw[g * 20 + 8 * nh + 2 * t + 1] = acc[nh][1];
-                Xw[(g + 8) * 20 + 8 * nh + 2 * t] = acc[nh][2];
-                Xw[(g + 8) * 20 + 8 * nh + 2 * t + 1] = acc[nh][3];
-            }
-            __syncwarp();
-            float res[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-            for (int kh = 0; kh < 2; ++kh) {
-                const float *Tb = As + (16 * bi) * kAs + 16 * bi + 8 * kh;
-                const uint32_t a[4] = {to_tf32(Tb[g * kAs + t]), to_tf32(Tb[(g + 8) * kAs + t]),
-                                       to_tf32(Tb[g * kAs + t + 4]),
-                                       to_tf32(Tb[(g + 8) * kAs + t + 4])};
-#pragma unroll
-                for (int nh = 0; nh < 2; ++nh) {
-                    const uint32_t bb[2] = {to_tf32(Xw[(8 * kh + t) * 20 + 8 * nh + g]),
-                                            to_tf32(Xw[(8 * kh + t + 4) * 20 + 8 * nh + g])};
-                    mma_tf32_16x8x8(res[nh], a, bb);
-                }
-            }
-            // T_{bi,bj}[r][c] -> As[16 bj + c][16 bi + r] and the operand tile.
-#pragma unroll
-            for (int nh = 0; nh < 2; ++nh) {
-                const int c = 16 * bj + 8 * nh + 2 * t, r = 16 * bi + g;
-                As[c * kAs + r] = -res[nh][0];
-                As[(c + 1) * kAs + r] = -res[nh][1];
-                As[c * kAs + r + 8] = -res[nh][2];
-                As[(c + 1) * kAs + r + 8] = -res[nh][3];
-                tt_put2<IO>(tt, r, c, -res[nh][0], -res[nh][1], beta, gam);
-                tt_put2<IO>(tt, r + 8, c, -res[nh][2], -res[nh][3], beta, gam);
-            }
-            __syncwarp();
+        for (int nh = 0; nh < 2; ++nh) {
+            const int c = 16 * j + 8 * nh + 2 * t, r = 16 * i + g;
+            tt_put2<IO>(tt, r, c, -acc[nh][0], -acc[nh][1], beta, gam);
+            tt_put2<IO>(tt, r + 8, c, -acc[nh][2], -acc[nh][3], beta, gam);
         }
+    };
+    if (w < 2) {                                    // 16 -> 32
+        const int hi = 2 * w + 1, lo = 2 * w;       // (1, 0) or (3, 2)
+        float acc[2][4] = {};
+        block_mma(acc, low(hi, lo), diag(lo), g, t);
+        block_store(scratch(w), acc, 1.f, g, t);
+        __syncwarp();
+        float res[2][4] = {};
+        block_mma(res, diag(hi), scratch(w), g, t);
+        emit(hi, lo, res);
+    }
+    named_bar(kBarPrep, kPrepThreads);
+    const int bi = 2 + (w >> 1), bj = w & 1;        // this warp's block of T_[23][01]
+    if (w < 4) {                                    // Y = A_[23][01] T_[01][01]
+        float acc[2][4] = {};
+        if (bj == 0) {
+            block_mma(acc, low(bi, 0), diag(0), g, t);
+            block_mma(acc, low(bi, 1), tlo(1, 0), g, t);
+        } else {
+            block_mma(acc, low(bi, 1), diag(1), g, t);
+        }
+        block_store(scratch(w), acc, 1.f, g, t);
+    }
+    named_bar(kBarPrep, kPrepThreads);
+    if (w < 4) {                                    // T_[23][01] = -T_[23][23] Y
+        float res[2][4] = {};
+        if (bi == 2) {
+            block_mma(res, diag(2), scratch(bj), g, t);
+        } else {
+            block_mma(res, tlo(3, 2), scratch(bj), g, t);
+            block_mma(res, diag(3), scratch(2 + bj), g, t);
+        }
+        emit(bi, bj, res);
     }
 }
 
 template <typename IO>
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ TcParams p) {
     constexpr bool kBf16 = std::is_same<IO, __nv_bfloat16>::value;
     constexpr uint32_t kIdD1 = idesc_f16(kBf16, 128, 64, false, false);
     constexpr uint32_t kIdD2 = idesc_f16(kBf16, 128, 128, false, true);
     constexpr uint32_t kIdNV = idesc_f16(kBf16, 128, kNV, false, true);
     constexpr uint32_t kIdDS = idesc_f16(kBf16, 128, kNV, true, true);
-    const uint32_t kStageTx = 2 * 2 * 8192 + 8192 + (p.gate_tma ? 2048 : 0);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -246,12 +287,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     __shared__ Ctl ctl;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int slice = blockIdx.x & 1;
+    const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;   // rank = column half
     const int h = (blockIdx.x >> 1) % p.h_v;
     const int64_t n = (int64_t)(blockIdx.x >> 1) / p.h_v;
     const int hq = h / (p.h_v / p.h_qk);
-    const int v0 = slice * kNV;
+    const int v0 = (int)rank * kNV;
 
+    // Both CTAs of a cluster share (n, h), so they leave here together.
     int64_t t0, t1;
     if (!seq_range(p.cu_seqlens, p.seqlen, p.num_seqs, p.status, n, t0, t1)) return;
     const int64_t L = t1 - t0;
@@ -259,7 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 
     float *const As = reinterpret_cast<float *>(sm + OFF_AS);
     const uint32_t aStage = smem_u32(sm + OFF_STAGE), aPZ = smem_u32(sm + OFF_PZ);
-    const uint32_t aTT = smem_u32(sm + OFF_TT), aSB = smem_u32(sm + OFF_SB);
+    const uint32_t aTT = smem_u32(sm + OFF_TT), aTTR = smem_u32(sm + OFF_TTR);
+    const uint32_t aSB = smem_u32(sm + OFF_SB);
     const uint32_t aDB0 = smem_u32(sm + OFF_DB0), aDB1 = smem_u32(sm + OFF_DB1);
 
     if (warp == 0) {
@@ -271,6 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             mbar_init(&ctl.full[i], 1);
             mbar_init(&ctl.prep_done[i], 1);
             mbar_init(&ctl.chain_done[i], 1);
+            mbar_init(&ctl.recv[i], 1);
+            mbar_init(&ctl.recvd[i], 1);
+            mbar_init(&ctl.peer_free[i], 1);
         }
         mbar_init(&ctl.d1, 1);
         mbar_init(&ctl.d23, 1);
@@ -282,33 +328,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_v);
     }
-    // Rows 64-127 of both [P; 0] tiles stay zero, and so do the blocks of [T'; T'']
-    // above the diagonal (the inverse writes only the blocks on and below it).
-    for (int e = tid; e < 2 * 8192 / 16; e += kThreads)
-        *reinterpret_cast<uint4 *>(sm + OFF_PZ + (e >> 9) * 16384 + 8192 + 16 * (e & 511)) =
-            make_uint4(0, 0, 0, 0);
-    for (int e = tid; e < 16384 / 16; e += kThreads)
-        *reinterpret_cast<uint4 *>(sm + OFF_TT + 16 * e) = make_uint4(0, 0, 0, 0);
+    // Zero the P tiles, [T'; T''] (its blocks above the diagonal stay zero) and the
+    // receive tile [0; T''], so every operand row an MMA reads is finite.
+    for (int e = tid; e < (2 * 8192 + 2 * 16384) / 16; e += kThreads)
+        *reinterpret_cast<uint4 *>(sm + OFF_PZ + 16 * e) = make_uint4(0, 0, 0, 0);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    cluster_sync();   // the peer's barriers exist before any remote arrive or copy
     const uint32_t tmem = ctl.tmem;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const size_t sbase = ((size_t)n * p.h_v + h) * kDK * kDK;
+    auto owns = [&](int c) { return (uint32_t)(c & 1) == rank; };
 
-    auto issue_stage = [&](int c) {   // TMA of chunk c into stage c & 1 (one thread)
+    // TMA of chunk c into stage c & 1: K, Q and V always; the gate logits only for the
+    // chunks this CTA preps.
+    auto issue_stage = [&](int c) {
         const int s = c & 1;
+        const bool own = owns(c);
         uint8_t *st = sm + OFF_STAGE + s * kStage;
         const int tok = (int)(t0 + (int64_t)c * kC);
-        mbar_arrive_expect_tx(&ctl.full[s], kStageTx);
+        const uint32_t tx = 2 * 2 * 8192 + 8192 + ((own && p.gate_tma) ? 2048 : 0);
+        mbar_arrive_expect_tx(&ctl.full[s], tx);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             tma_load_3d(st + r * kRegion, &p.tm_k, r * 64, hq, tok, &ctl.full[s]);
             tma_load_3d(st + r * kRegion + 8192, &p.tm_q, r * 64, hq, tok, &ctl.full[s]);
         }
         tma_load_3d(st + 2 * kRegion, &p.tm_v, v0, h, tok, &ctl.full[s]);
-        if (p.gate_tma) {
+        if (own && p.gate_tma) {
             tma_load_2d(st + kGates, &p.tm_a, h & ~7, tok, &ctl.full[s]);
             tma_load_2d(st + kGates + 1024, &p.tm_b, h & ~7, tok, &ctl.full[s]);
         }
@@ -316,71 +365,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 
     if (tid < kPrepThreads) {
         // ============================================================== prep role
+        // Preps the chunks c with c % 2 == rank, for this CTA's chain and the peer's.
         const int pt = tid;
         const int q = warp & 3, hf = warp >> 2;    // TMEM lane quarter, column half
         const IO *ga = static_cast<const IO *>(p.a);
         const IO *gb = static_cast<const IO *>(p.b);
         const float A_log = p.A_log[h], dt_bias = p.dt_bias[h];
-        float ra = 0.f, rb = 0.f;                  // this thread's gate logits, next chunk
-        if (!p.gate_tma && pt < kC && pt < L) {
-            ra = IoType<IO>::ld(ga + (size_t)(t0 + pt) * p.h_v + h);
-            rb = IoType<IO>::ld(gb + (size_t)(t0 + pt) * p.h_v + h);
-        }
         bool failed = false;
-        for (int c = 0; c < nchunks; ++c) {
+        for (int c = (int)rank; c < nchunks; c += 2) {
             const int b = c & 1, s = c & 1;
             const int64_t tc0 = t0 + (int64_t)c * kC;
             const int Lc = (int)((L - (int64_t)c * kC) < kC ? (L - (int64_t)c * kC) : kC);
+            GateBuf &gbuf = ctl.gb[b];
             bool ok = true;
-            if (c >= 2) ok = mbar_wait(&ctl.chain_done[b], ((c >> 1) - 1) & 1, kWaitBudget);
+            if (c >= 2) {
+                ok = mbar_wait(&ctl.chain_done[b], ((c >> 1) - 1) & 1, kWaitBudget);
+                if (ok) ok = mbar_wait(&ctl.recvd[b], ((c >> 1) - 1) & 1, kWaitBudget);
+            }
             if (ok) ok = mbar_wait(&ctl.full[s], (c >> 1) & 1, kWaitBudget);
             if (bar_any(kBarPrep, kPrepThreads, !ok || *(volatile int *)&ctl.abort)) { failed = true; break; }
 
-            // Gates and prefix sums (threads 0-63 = tokens of the chunk).
-            float gsum = 0.f, be = 0.f;
-            if (pt < kC) {
-                if (p.gate_tma) {
-                    const IO *gt = reinterpret_cast<const IO *>(sm + OFF_STAGE + s * kStage + kGates);
-                    ra = IoType<IO>::ld(gt + pt * 8 + (h & 7));
-                    rb = IoType<IO>::ld(gt + 512 + pt * 8 + (h & 7));
-                }
-                if (pt < Lc) {
-                    gsum = decay_f(ra, A_log, dt_bias);
-                    be = sigmoid_f(rb);
-                }
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, gsum, off);
-                    if (lane >= off) gsum += y;
-                }
-                if (lane == 31) ctl.wsum[warp] = gsum;
-                // Without gate TMA, prefetch the next chunk's gate logits.
-                const int64_t tn = tc0 + kC + pt;
-                ra = rb = 0.f;
-                if (!p.gate_tma && tn < t1) {
-                    ra = IoType<IO>::ld(ga + (size_t)tn * p.h_v + h);
-                    rb = IoType<IO>::ld(gb + (size_t)tn * p.h_v + h);
-                }
-            }
-            named_bar(kBarPrep, kPrepThreads);
-            if (pt < kC) {
-                ctl.G[pt] = gsum + (warp == 1 ? ctl.wsum[0] : 0.f);
-                ctl.beta[pt] = be;
-            }
-            named_bar(kBarPrep, kPrepThreads);
-            const float GC = ctl.G[kC - 1], Gm = ctl.G[31];
-            const bool safe = (ctl.G[0] - GC) <= 80.f;   // e^{G_i - G_m} e^{G_m - G_j} cannot overflow
-            if (pt < kC) {
-                const float G = ctl.G[pt];
-                ctl.gam[b][pt] = expf(G);
-                ctl.kf[b][pt] = expf(GC - G);
-                ctl.E[pt] = expf(G - Gm);
-                ctl.F[pt] = expf(Gm - G);
-                if (pt == 0) ctl.gC[b] = expf(GC);
-            }
-            named_bar(kBarPrep, kPrepThreads);   // E, F, gamma visible to every prep warp
-
-            // D1 = [K; Q] K^T once the stage has landed.
+            // D1 = [K; Q] K^T (the stage has landed); the gates are computed meanwhile.
             if (pt == 0) {
                 tc_fence_after();
                 const uint32_t st = aStage + s * kStage;
@@ -392,7 +397,48 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 }
                 mma_commit(&ctl.d1);
             }
-            ok = mbar_wait(&ctl.d1, c & 1, kWaitBudget);
+
+            // Gates and prefix sums (threads 0-63 = tokens of the chunk).
+            float gsum = 0.f, be = 0.f;
+            if (pt < kC) {
+                float ra = 0.f, rb = 0.f;
+                if (p.gate_tma) {
+                    const IO *gt = reinterpret_cast<const IO *>(sm + OFF_STAGE + s * kStage + kGates);
+                    ra = IoType<IO>::ld(gt + pt * 8 + (h & 7));
+                    rb = IoType<IO>::ld(gt + 512 + pt * 8 + (h & 7));
+                } else if (pt < Lc) {
+                    ra = IoType<IO>::ld(ga + (size_t)(tc0 + pt) * p.h_v + h);
+                    rb = IoType<IO>::ld(gb + (size_t)(tc0 + pt) * p.h_v + h);
+                }
+                if (pt < Lc) {
+                    gsum = decay_f(ra, A_log, dt_bias);
+                    be = sigmoid_f(rb);
+                }
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, gsum, off);
+                    if (lane >= off) gsum += y;
+                }
+                if (lane == 31) ctl.wsum[warp] = gsum;
+            }
+            named_bar(kBarPrep, kPrepThreads);
+            if (pt < kC) {
+                ctl.G[pt] = gsum + (warp == 1 ? ctl.wsum[0] : 0.f);
+                ctl.beta[pt] = be;
+            }
+            named_bar(kBarPrep, kPrepThreads);
+            const float GC = ctl.G[kC - 1], Gm = ctl.G[31];
+            const bool safe = (ctl.G[0] - GC) <= 80.f;   // e^{G_i - G_m} e^{G_m - G_j} cannot overflow
+            if (pt < kC) {
+                const float G = ctl.G[pt];
+                gbuf.gam[pt] = __expf(G);
+                gbuf.kf[pt] = __expf(GC - G);
+                ctl.E[pt] = __expf(G - Gm);
+                ctl.F[pt] = __expf(Gm - G);
+                if (pt == 0) gbuf.gC = __expf(GC);
+            }
+            named_bar(kBarPrep, kPrepThreads);   // E, F, gamma visible to every prep warp
+            ok = mbar_wait(&ctl.d1, (c >> 1) & 1, kWaitBudget);
             tc_fence_after();
 
             // A rows (lanes 0-63, fp32) and P rows (lanes 64-127, I/O type); each column
@@ -418,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                             make_float4(x[0], x[1], x[2], x[3]);
                     }
                 } else {
-                    uint8_t *pz = sm + OFF_PZ + b * 16384;
+                    uint8_t *pz = sm + OFF_PZ + b * 8192;
 #pragma unroll
                     for (int q8 = 0; q8 < 4; ++q8) {
                         float x[8];
@@ -432,11 +478,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                     }
                 }
             }
+            // D1 has read Q: scale the stage's Q rows in place, Q~ = diag(scale gamma) Q,
+            // so that [Q~; W] S0 yields the inter-chunk output term directly.
+            for (int e = pt; e < 1024; e += kPrepThreads) {
+                const int r = e >> 9, row = (e >> 3) & 63, ch = e & 7;
+                uint8_t *ptr = sm + OFF_STAGE + s * kStage + r * kRegion + 8192 + sw128_offset(row, ch);
+                const uint4 u = *reinterpret_cast<const uint4 *>(ptr);
+                const float f = p.scale * gbuf.gam[row];
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                float x[8];
+#pragma unroll
+                for (int k2 = 0; k2 < 4; ++k2) {
+                    const float2 t2 = Pack<IO>::unpack(w[k2]);
+                    x[2 * k2] = t2.x * f;
+                    x[2 * k2 + 1] = t2.y * f;
+                }
+                *reinterpret_cast<uint4 *>(ptr) = pack8<IO>(x);
+            }
             fence_async_smem();
             if (bar_any(kBarPrep, kPrepThreads, !ok)) { failed = true; break; }
 
             // T = (I + A)^-1, written as [T diag(beta gamma); T diag(beta)] (K-major).
-            invert_chunk<IO>(As, ctl.X, sm + OFF_TT, ctl.beta, ctl.gam[b], pt);
+            invert_chunk<IO>(As, ctl.X, sm + OFF_TT, ctl.beta, gbuf.gam, pt);
             fence_async_smem();
             tc_fence_before();
             named_bar(kBarPrep, kPrepThreads);
@@ -454,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 }
                 mma_commit(&ctl.d23);
             }
-            ok = mbar_wait(&ctl.d23, c & 1, kWaitBudget);
+            ok = mbar_wait(&ctl.d23, (c >> 1) & 1, kWaitBudget);
             tc_fence_after();
 
             // W (lanes 0-63 of D2) -> rows 128-191 of the stage's K|Q|W regions.
@@ -478,7 +541,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             fence_async_smem();
             tc_fence_before();
             if (bar_any(kBarPrep, kPrepThreads, !ok)) { failed = true; break; }
-            if (pt == 0) mbar_arrive(&ctl.prep_done[b]);
+            if (pt == 0) {
+                mbar_arrive(&ctl.prep_done[b]);
+                // Hand the chunk to the peer once it has released the previous one:
+                // the W rows of both d_k halves, P, T'' and the gate values.
+                ok = (c < 2) || mbar_wait(&ctl.peer_free[b], ((c >> 1) - 1) & 1, kWaitBudget);
+                if (ok) {
+                    const uint32_t rb = mapa_shared(smem_u32(&ctl.recv[b]), peer);
+                    uint8_t *st = sm + OFF_STAGE + s * kStage;
+#pragma unroll
+                    for (int r = 0; r < 2; ++r)
+                        bulk_copy_to_cluster(mapa_shared(smem_u32(st + r * kRegion + 16384), peer),
+                                             st + r * kRegion + 16384, 8192, rb);
+                    bulk_copy_to_cluster(mapa_shared(aPZ + b * 8192, peer), sm + OFF_PZ + b * 8192, 8192, rb);
+                    bulk_copy_to_cluster(mapa_shared(aTTR + 8192, peer), sm + OFF_TT + 8192, 8192, rb);
+                    bulk_copy_to_cluster(mapa_shared(smem_u32(&gbuf), peer), &gbuf, sizeof(GateBuf), rb);
+                }
+            }
+            if (bar_any(kBarPrep, kPrepThreads, !ok)) { failed = true; break; }
         }
         if (failed && pt == 0) {
             ctl.abort = 1;
@@ -514,15 +594,50 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         bool failed = false;
         for (int c = 0; c < nchunks; ++c) {
             const int b = c & 1, s = c & 1;
+            const bool own = owns(c);
             const int64_t tc0 = t0 + (int64_t)c * kC;
             const int Lc = (int)((L - (int64_t)c * kC) < kC ? (L - (int64_t)c * kC) : kC);
-            bool ok = mbar_wait(&ctl.prep_done[b], (c >> 1) & 1, kWaitBudget);
+            bool ok;
+            if (own) {
+                ok = mbar_wait(&ctl.prep_done[b], (c >> 1) & 1, kWaitBudget);
+            } else {
+                if (ct == 0) mbar_arrive_expect_tx(&ctl.recv[b], kPeerBytes);
+                ok = mbar_wait(&ctl.recv[b], (c >> 1) & 1, kWaitBudget);
+                if (ok) ok = mbar_wait(&ctl.full[s], (c >> 1) & 1, kWaitBudget);
+                if (ok && ct == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl.recvd[b]), peer));
+                if (ok) {   // Q~ = diag(scale gamma) Q in place, as the owner did for its copy
+                    for (int e = ct; e < 1024; e += kChainThreads) {
+                        const int r = e >> 9, row = (e >> 3) & 63, ch = e & 7;
+                        uint8_t *ptr = sm + OFF_STAGE + s * kStage + r * kRegion + 8192 +
+                                       sw128_offset(row, ch);
+                        const uint4 u = *reinterpret_cast<const uint4 *>(ptr);
+                        const float f = p.scale * ctl.gb[b].gam[row];
+                        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                        float x[8];
+#pragma unroll
+                        for (int k2 = 0; k2 < 4; ++k2) {
+                            const float2 t2 = Pack<IO>::unpack(w[k2]);
+                            x[2 * k2] = t2.x * f;
+                            x[2 * k2 + 1] = t2.y * f;
+                        }
+                        *reinterpret_cast<uint4 *>(ptr) = pack8<IO>(x);
+                    }
+                    fence_async_smem();
+                }
+            }
+            if (ct == 0) bulk_wait_read();   // the previous output tile (in DB0) has been read
             if (bar_any(kBarChain, kChainThreads, !ok || *(volatile int *)&ctl.abort)) { failed = true; break; }
             tc_fence_after();
             const uint32_t st = aStage + s * kStage;
 
-            // D4 = [Q; W] S0.
+            // (Received chunks: U = T'' V of this half.)  D4 = [Q~; W] S0.
             if (ct == 0) {
+                if (!own) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_f16(tmem + TM_D3 + 64 * b, sw128_desc(aTTR + k * 32, 16, 1024),
+                                sw128_desc(st + 2 * kRegion + k * 2048, 8192, 1024), kIdNV, k > 0);
+                }
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t off = (k >> 2) * kRegion + 8192 + (k & 3) * 32;
@@ -537,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             // Delta = U - W S0 on lanes 64-127 (token rows), in two versions.
             if (cw >= 2) {
                 const int j = ct - 64;
-                const float kfj = ctl.kf[b][j];
+                const float kfj = ctl.gb[b].kf[j];
 #pragma unroll
                 for (int c0 = 0; c0 < kNV; c0 += 32) {
                     uint32_t ws[32], u[32];
@@ -562,13 +677,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             tc_fence_before();
             if (bar_any(kBarChain, kChainThreads, !ok)) { failed = true; break; }
 
-            // D5 = [P; 0] Delta;  DS = K^T diag(e^{G_C - G}) Delta.
+            // D4[0:64] += P Delta (the A rows past P land in the spent W S0 lanes);
+            // DS = K^T diag(e^{G_C - G}) Delta.
             if (ct == 0) {
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    mma_f16(tmem + TM_D5, sw128_desc(aPZ + b * 16384 + k * 32, 16, 1024),
-                            sw128_desc(aDB0 + k * 2048, 8192, 1024), kIdNV, k > 0);
+                    mma_f16(tmem + TM_D4, sw128_desc(aPZ + b * 8192 + k * 32, 16, 1024),
+                            sw128_desc(aDB0 + k * 2048, 8192, 1024), kIdNV, 1u);
                     mma_f16(tmem + TM_DS, sw128_desc(st + k * 2048, kRegion, 1024),
                             sw128_desc(aDB1 + k * 2048, 8192, 1024), kIdDS, k > 0);
                 }
@@ -581,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 
             // S = gamma_C S0 + DS (fp32 registers), then the next chunk's operand tile.
             {
-                const float gC = ctl.gC[b];
+                const float gC = ctl.gb[b].gC;
 #pragma unroll
                 for (int c0 = 0; c0 < kNV; c0 += 32) {
                     uint32_t r[32];
@@ -592,21 +708,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 }
                 write_sb();
             }
-            // o_i = scale gamma_i (Q S0)_i + (P Delta)_i on lanes 0-63.
+            // o_i = (Q~ S0 + P Delta)_i on lanes 0-63.  A full chunk goes out as one TMA
+            // store of a 64 x 64 tile staged in DB0 (free once D4 and DS have read it); a
+            // sequence's ragged last chunk is stored row by row so that no row of the next
+            // sequence is touched.
+            const bool tile_store = (Lc == kC);
             if (cw < 2) {
                 const int i = ct;
-                const float f = p.scale * ctl.gam[b][i];
 #pragma unroll
                 for (int c0 = 0; c0 < kNV; c0 += 32) {
-                    uint32_t qs[32], pd[32];
-                    tmem_ld32(tmem + lane_base + TM_D4 + c0, qs);
-                    tmem_ld32(tmem + lane_base + TM_D5 + c0, pd);
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_base + TM_D4 + c0, r);
                     tmem_ld_wait();
-                    if (i < Lc) {
-                        float x[32];
+                    float x[32];
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            x[e] = fmaf(f, __uint_as_float(qs[e]), __uint_as_float(pd[e]));
+                    for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
+                    if (tile_store) {
+#pragma unroll
+                        for (int q8 = 0; q8 < 4; ++q8)
+                            *reinterpret_cast<uint4 *>(sm + OFF_DB0 + sw128_offset(i, (c0 >> 3) + q8)) =
+                                pack8<IO>(x + 8 * q8);
+                    } else if (i < Lc) {
                         uint4 *dst = reinterpret_cast<uint4 *>(
                             go + ((size_t)(tc0 + i) * p.h_v + h) * kDK + v0 + c0);
 #pragma unroll
@@ -617,8 +739,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             fence_async_smem();
             tc_fence_before();
             if (bar_any(kBarChain, kChainThreads, !ok)) { failed = true; break; }
-            if (ct == 0) mbar_arrive(&ctl.chain_done[b]);
+            if (ct == 0 && tile_store) {
+                tma_store_3d(&p.tm_o, sm + OFF_DB0, v0, h, (int)tc0);
+                bulk_commit();
+            }
+            if (ct == 0) {
+                if (own) mbar_arrive(&ctl.chain_done[b]);
+                else mbar_arrive_cluster(mapa_shared(smem_u32(&ctl.peer_free[b]), peer));
+            }
         }
+        if (ct == 0) bulk_wait_all();   // the output tiles have reached global memory
         if (failed) {
             if (ct == 0) {
                 ctl.abort = 1;
@@ -634,6 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 
     tc_fence_before();
     __syncthreads();
+    cluster_sync();   // no remote copy or arrive may target a CTA that has exited
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -723,7 +854,8 @@ cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_t
     memset(&tp, 0, sizeof(tp));
     if (!make_map(&tp.tm_q, p.q, io, p.h_qk, total_tokens) ||
         !make_map(&tp.tm_k, p.k, io, p.h_qk, total_tokens) ||
-        !make_map(&tp.tm_v, p.v, io, p.h_v, total_tokens))
+        !make_map(&tp.tm_v, p.v, io, p.h_v, total_tokens) ||
+        !make_map(&tp.tm_o, p.o, io, p.h_v, total_tokens))
         return cudaErrorInvalidValue;
     // Gate logits ride along with each stage's TMA when their rows are 16-byte multiples.
     tp.gate_tma = (p.h_v % 8 == 0 && reinterpret_cast<uintptr_t>(p.a) % 16 == 0 &&

@@ -34,6 +34,8 @@ def run_prefill(inp, device="cuda", **kw):
     o, s = gdn_prefill(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
                        d["state_in"], d["cu_seqlens"], inp.scale, **kw)
     torch.cuda.synchronize()
+    from recurrent_state_scan_gb300 import gdn_last_device_status
+    assert gdn_last_device_status() == 0, "the device check word is set (a bounded wait gave up)"
     spec = inp.spec
     o = o.float().cpu().numpy().reshape(-1, spec.h_v, spec.d_v)
     s = s.cpu().numpy()
