@@ -257,6 +257,10 @@ def run_ours(args, rank, world, local):
     n_state = (inp.n_seq, s.h_v, s.d_k, s.d_v)
     state_out = torch.empty(n_state, dtype=torch.float32, device=dev)
     work_state = None if state0 is None else state0.clone()
+    from recurrent_state_scan_gb300 import gdn
+    ws_need = 0 if s.decode else gdn.gdn_prefill_workspace_bytes(
+        gdn.shape_of_spec(s, inp.n_seq, inp.total_tokens))
+    ws = torch.empty(ws_need, dtype=torch.uint8, device=dev) if ws_need else None
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -266,7 +270,8 @@ def run_ours(args, rank, world, local):
                             work_state, inp.scale, o=o, stream=stream)
         else:
             gdn_prefill(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"], t["dt_bias"],
-                        state0, cu, inp.scale, o=o, state_out=state_out, stream=stream)
+                        state0, cu, inp.scale, o=o, state_out=state_out, workspace=ws,
+                        stream=stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -313,7 +318,7 @@ def run_ours(args, rank, world, local):
             else:
                 gdn_prefill(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["a"], dbuf["b"], dbuf["A_log"],
                             dbuf["dt_bias"], dbuf.get("state"), cu, inp.scale, o=o,
-                            state_out=state_out, stream=stream)
+                            state_out=state_out, workspace=ws, stream=stream)
                 s_host.copy_(state_out, non_blocking=True)
             o_host.copy_(o, non_blocking=True)
 

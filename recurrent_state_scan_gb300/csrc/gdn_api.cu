@@ -130,25 +130,28 @@ gdn_status gdn_prefill_plan(const gdn_shape *shape, int32_t *path, int32_t *laun
     if (st != GDN_OK) return st;
     const bool varlen = shape->batch == 1 && shape->num_seqs != 1;
     const int64_t tokens = varlen ? shape->seqlen : shape->seqlen * (int64_t)shape->batch;
-    const bool tc = (shape->io_dtype == GDN_BF16 || shape->io_dtype == GDN_F16) &&
-                    shape->d_k == 128 && shape->d_v == 128 && tokens > 0 &&
-                    tokens <= 0x7fffff00LL;
+    const bool tc = prefill_tc_shape_ok((gdn_dtype)shape->io_dtype, shape->d_k, shape->d_v, tokens);
     if (path) *path = tc ? 2 : 1;
-    if (launches) *launches = shape->num_seqs > 0 ? 1 : 0;
+    if (launches) *launches = shape->num_seqs > 0 ? (tc ? 2 : 1) : 0;
     return GDN_OK;
 }
 
+// Packed sequences come with batch == 1; a single batch-1 sequence is sized as packed too,
+// which covers both readings.
 size_t gdn_prefill_workspace_bytes(const gdn_shape *shape) {
-    (void)shape;
-    return 0;
+    if (shape == nullptr || shape->seqlen < 0 || shape->batch < 0 || shape->num_seqs < 0 ||
+        shape->h_v <= 0)
+        return 0;
+    const bool packed = shape->batch == 1;
+    const int64_t tokens = packed ? shape->seqlen : shape->seqlen * (int64_t)shape->batch;
+    if (!prefill_tc_shape_ok((gdn_dtype)shape->io_dtype, shape->d_k, shape->d_v, tokens)) return 0;
+    return prefill_tc_workspace(packed, shape->seqlen, shape->batch, shape->num_seqs, shape->h_v);
 }
 
 gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, const void *v,
                        const void *a, const void *b, const float *A_log, const float *dt_bias,
                        const float *state_in, const int32_t *cu_seqlens, float scale, void *o,
                        float *state_out, void *workspace, size_t workspace_bytes, void *stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     gdn_status st = check_shape(shape, cu_seqlens != nullptr);
     if (st != GDN_OK) return st;
     const int64_t tokens = cu_seqlens ? shape->seqlen : shape->seqlen * (int64_t)shape->batch;
@@ -176,7 +179,13 @@ gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, con
     const gdn_dtype io = (gdn_dtype)shape->io_dtype;
     cudaError_t e;
     if (prefill_tc_supported(p, io, tokens)) {
-        e = launch_prefill_tc(p, io, tokens, prefill_tc_columns(p), (cudaStream_t)stream);
+        const size_t need = prefill_tc_workspace(cu_seqlens != nullptr, shape->seqlen, shape->batch,
+                                                 shape->num_seqs, shape->h_v);
+        if (workspace == nullptr || workspace_bytes < need)
+            return fail(GDN_ERR_INVALID_ARG, "workspace of %zu bytes is below the %zu this call needs",
+                        workspace == nullptr ? (size_t)0 : workspace_bytes, need);
+        if (!aligned(workspace, 16)) return fail(GDN_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+        e = launch_prefill_tc(p, io, tokens, workspace, (cudaStream_t)stream);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");
     } else {
         e = launch_scan_simt(p, io, (cudaStream_t)stream);

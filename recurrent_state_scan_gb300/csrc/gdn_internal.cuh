@@ -88,12 +88,15 @@ __device__ __forceinline__ bool seq_range(const ScanParams &p, int64_t n, int64_
 // Launchers implemented in the kernel translation units.
 cudaError_t launch_scan_simt(const ScanParams &p, gdn_dtype io, cudaStream_t stream);
 
-// Chunked tensor-core prefill (bf16/f16 I/O, d_k = d_v = 128).  `nv` is the number
-// of state columns per CTA (64 or 128).  Returns cudaErrorNotSupported if the
-// driver entry point for tensor-map encoding is unavailable.
+// Chunked tensor-core prefill (bf16/f16 I/O, d_k = d_v = 128): a chunk-prep kernel
+// that writes one workspace record per (chunk, value head), then a state-scan kernel.
+// prefill_tc_shape_ok: the shape rules alone (host-only).  prefill_tc_workspace: bytes
+// of records the call needs (packed sequences: an upper bound from the token total).
+// prefill_tc_supported adds the pointer rules and the tensor-map encoder's presence.
+bool prefill_tc_shape_ok(gdn_dtype io, int d_k, int d_v, int64_t total_tokens);
+size_t prefill_tc_workspace(bool varlen, int64_t seqlen, int64_t batch, int64_t num_seqs, int h_v);
 bool prefill_tc_supported(const ScanParams &p, gdn_dtype io, int64_t total_tokens);
-int prefill_tc_columns(const ScanParams &p);
-cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_tokens, int nv,
-                              cudaStream_t stream);
+cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_tokens,
+                              void *workspace, cudaStream_t stream);
 
 }  // namespace gdn

@@ -11,23 +11,22 @@
 // The pages run the recurrence one token at a time; this chunked form is a
 // re-association of the same sums, exact up to rounding.
 //
-// One CTA owns one (sequence, value head, half of the 128 state columns) and walks the
-// sequence's chunks in order.  Columns of S evolve independently (the page's
-// "Parallelization" note), so a half needs only its columns of V, U, Delta and o.
-// Its 12 warps split into two roles that run one chunk apart:
-//   prep  (warps 0-7)  chunk c+1: gates and their prefix sums, D1 = [K; Q] K^T (tcgen05),
-//                      A and P, T = (I + A)^-1 (fp32 diagonal blocks + tf32 warp-MMA
-//                      merges), [T'; T''] = [T diag(beta gamma); T diag(beta)],
-//                      D2 = [T'; T''] K -> W,  D3 = [T'; T''] V -> U (tcgen05).
-//   chain (warps 8-11) chunk c: D4 = [Q; W] S0 (tcgen05), Delta = U - W S0,
-//                      D5 = [P; 0] Delta, DS = K^T diag(e^{G_C-G}) Delta (tcgen05),
-//                      S = gamma_C S0 + DS with S in fp32 registers, o to HBM.
-// K, Q and V arrive by TMA into two stages; the chain refills a stage as soon as its
-// last reader is done.  All MMAs use M = 128, so accumulator row r is TMEM lane r:
-//   D1 lanes 0-63 K K^T, 64-127 Q K^T;  D2 lanes 0-63 W;  D3 lanes 64-127 U;
-//   D4 lanes 0-63 Q S0, 64-127 W S0;  D5 lanes 0-63 P Delta;  DS lanes = d_k rows.
-// Rows past the end of a sequence get g = 0 and beta = 0, which makes their T row the
-// unit row and their W, U and Delta rows exactly zero, so they change nothing.
+// Two kernels, stream-ordered:
+//  * gdn_chunk_prep -- one CTA per (chunk, value head), all in parallel: everything that
+//    does not depend on the state.  Gates and their prefix sums, D1 = [K; Q] K^T
+//    (tcgen05), A and P, T = (I + A)^-1 (fp32 diagonal blocks, tf32 warp-MMA merges),
+//    D2 = [T'; T''] K -> W and D3 = [T'; T''] V -> U (tcgen05), Q~ = diag(scale gamma) Q.
+//    It writes one workspace record per (chunk, head): shared-memory images of [Q~; W],
+//    U, P and the gate values, laid out exactly as the scan loads them.
+//  * gdn_chunk_scan -- one CTA per (sequence, value head, half of the 128 state columns),
+//    walking the sequence's chunks in order: D4 = [Q~; W] S0 (tcgen05),
+//    Delta = U - W S0, DS = K^T diag(e^{G_C-G}) Delta and D4 += [P; .] Delta (tcgen05),
+//    S = gamma_C S0 + DS with S in fp32 registers, o by TMA store.  Records and K arrive
+//    by bulk copy / TMA into two stages, one chunk ahead.
+// Columns of S evolve independently (the page's "Parallelization" note), so a column
+// half needs only its half of U and Delta.  All MMAs use M = 128, so accumulator row r
+// is TMEM lane r.  Rows past the end of a sequence get g = 0 and beta = 0, which makes
+// their T row the unit row and their W, U and Delta rows exactly zero.
 #include <cudaTypedefs.h>
 
 #include <type_traits>
@@ -42,16 +41,28 @@ using namespace tc;
 
 constexpr int kC = 64;                 // tokens per chunk
 constexpr int kDK = 128;               // d_k = d_v of this path
-constexpr int kNV = 64;                // state columns per CTA
-constexpr int kPrepThreads = 256, kChainThreads = 128;
-constexpr int kThreads = kPrepThreads + kChainThreads;
-constexpr uint32_t kBarPrep = 1, kBarChain = 2;
+constexpr int kNV = 64;                // state columns per scan CTA
+constexpr int kPrepThreads = 256, kScanThreads = 256;
+constexpr uint32_t kBarPrep = 1, kBarChain = 1;
 constexpr long long kWaitBudget = 4000000000LL;   // cycles (~2 s) before a wait gives up
+constexpr int kAs = 68;                // row stride (floats) of the fp32 A / T tile
+
+// Workspace record of one (chunk, value head): shared-memory images for the scan.
+constexpr int REC_QW = 0;              // 2 d_k halves x [Q~ rows | W rows], 128 x 128 B each
+constexpr int REC_U = 32768;           // 2 column halves x 64 token rows x 128 B
+constexpr int REC_P = 49152;           // 64 rows x 128 B
+constexpr int REC_G = 57344;           // GateRec
+constexpr int kRecord = 58368;
+
+struct __align__(16) GateRec {
+    float gam[kC];      // e^{G_i}
+    float kf[kC];       // e^{G_C - G_i}
+    float gC, pad[3];   // e^{G_C}
+};
 
 struct TcParams {
-    CUtensorMap tm_q, tm_k, tm_v, tm_o;
-    CUtensorMap tm_a, tm_b;        // gate logits [tokens][h_v], used when gate_tma != 0
-    int32_t gate_tma;
+    CUtensorMap tm_q, tm_k, tm_v, tm_o, tm_a, tm_b;
+    int32_t gate_tma;               // gate logits by TMA (h_v % 8 == 0) or plain loads
     const void *a, *b;
     const float *A_log, *dt_bias;
     const float *state_in;
@@ -60,46 +71,19 @@ struct TcParams {
     const int32_t *cu_seqlens;
     int64_t seqlen;
     int32_t num_seqs, h_qk, h_v;
+    int32_t chunks_per_seq;         // batched input: chunks of every sequence
     float scale;
     int *status;
+    uint8_t *ws;                    // workspace records
 };
 
-// Shared-memory plan (byte offsets from a 1024-aligned base).
-constexpr int kRegion = 24576;                 // 192 rows x 128 B: K | Q | W for 64 d_k
-constexpr int kGates = 2 * kRegion + 8192;     // gate logit tiles a, b: 64 tokens x 8 heads
-constexpr int kStage = kGates + 2048;          // + V (64 tokens x 64 columns) + gate tiles
-constexpr int OFF_STAGE = 0;                   // two stages
-constexpr int OFF_PZ = 2 * kStage;             // two P tiles, 64 x 128 B each
-constexpr int OFF_TT = OFF_PZ + 2 * 8192;      // [T'; T''], 128 x 128 B
-constexpr int OFF_TTR = OFF_TT + 16384;        // [0; T''] received from the peer CTA
-constexpr int OFF_SB = OFF_TTR + 16384;        // S0 in the I/O type, MN-major (d_k rows)
-constexpr int OFF_DB0 = OFF_SB + 16384;        // Delta, MN-major (token rows)
-constexpr int OFF_DB1 = OFF_DB0 + 8192;        // diag(e^{G_C - G}) Delta
-constexpr int OFF_AS = OFF_DB1 + 8192;         // A, then T, fp32 [64][68]
-constexpr int kAs = 68;                        // row stride (floats) of A / T
-constexpr int kSmemBytes = OFF_AS + 64 * kAs * 4;
-constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for the 1024-byte alignment
-
-// TMEM columns.
-constexpr uint32_t TM_D1 = 0, TM_D2 = 64, TM_D3 = 192, TM_D4 = 320, TM_DS = 384;
-
-// Per-chunk gate values the chain needs; sent whole to the peer CTA (16-byte multiple).
-struct __align__(16) GateBuf {
-    float gam[kC];      // e^{G_i}
-    float kf[kC];       // e^{G_C - G_i}
-    float gC, pad[3];   // e^{G_C}
-};
-
-struct Ctl {
-    uint64_t full[2], prep_done[2], chain_done[2], d1, d23, d4, d5;
-    uint64_t recv[2], recvd[2], peer_free[2];  // cluster hand-off of the shared chunk prep
-    uint32_t tmem;
-    int abort;
-    float G[kC], beta[kC], E[kC], F[kC], wsum[2];
-    GateBuf gb[2];
-    float X[4][16][20];                        // warp scratch of the T merges
-};
-constexpr uint32_t kPeerBytes = 2 * 8192 + 8192 + 8192 + sizeof(GateBuf);
+// First workspace slot of sequence n.  Batched: n * chunks_per_seq.  Packed: slot
+// floor(cu[n] / C) + n; consecutive sequences never overlap because a sequence of L
+// tokens starting at cu[n] ends before slot floor((cu[n] + L) / C) + n + 1.
+__device__ __forceinline__ int64_t slot_base(const TcParams &p, int64_t n) {
+    if (p.cu_seqlens == nullptr) return n * p.chunks_per_seq;
+    return (int64_t)(p.cu_seqlens[n] / kC) + n;
+}
 
 template <typename IO> struct Pack;
 template <> struct Pack<__nv_bfloat16> {
@@ -222,6 +206,7 @@ __device__ void invert_chunk(float *As, float (*X)[16][20], uint8_t *tt, const f
             tt_put<IO>(tt, o + i, cj, x[i], f1, f2);
         }
     }
+    if (pt == 0) bulk_wait_read();   // X below reuses the staging tile of the P store
     named_bar(kBarPrep, kPrepThreads);
     const int w = pt >> 5, lane = pt & 31, g = lane >> 2, t = lane & 3;
     auto diag = [&](int b) { return Blk{As + 16 * b * kAs + 16 * b, kAs, 1}; };
@@ -272,502 +257,545 @@ __device__ void invert_chunk(float *As, float (*X)[16][20], uint8_t *tt, const f
     }
 }
 
+// ===================================================================== chunk prep
+// Shared memory (from a 1024-aligned base).
+constexpr int kRegion = 24576;                 // 192 rows x 128 B: K | Q | W for 64 d_k
+constexpr int PP_KQW = 0;                      // two regions
+constexpr int PP_V = 2 * kRegion;              // V, 2 x 64 x 128 B; later the U image
+constexpr int PP_GT = PP_V + 16384;            // gate logit tiles a, b: 64 tokens x 8 heads
+constexpr int PP_PS = PP_GT + 2048;            // P image; later the merges' scratch
+constexpr int PP_TT = PP_PS + 8192;            // [T'; T''], 128 x 128 B
+constexpr int PP_AS = PP_TT + 16384;           // A, then T, fp32 [64][68]
+constexpr int kPrepSmem = PP_AS + 64 * kAs * 4 + 1024;
+
+struct PrepCtl {
+    uint64_t full, d1, d23;
+    uint32_t tmem;
+    float G[kC], beta[kC], E[kC], F[kC], wsum[2];
+    GateRec gr;
+};
+
 template <typename IO>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_constant__ TcParams p) {
     constexpr bool kBf16 = std::is_same<IO, __nv_bfloat16>::value;
     constexpr uint32_t kIdD1 = idesc_f16(kBf16, 128, 64, false, false);
     constexpr uint32_t kIdD2 = idesc_f16(kBf16, 128, 128, false, true);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+    __shared__ PrepCtl ctl;
+    const int pt = threadIdx.x, warp = pt >> 5, lane = pt & 31;
+    const int q = warp & 3, hf = warp >> 2;        // TMEM lane quarter, column half
+    const int64_t slot = blockIdx.x / p.h_v;
+    const int h = blockIdx.x % p.h_v;
+    const int hq = h / (p.h_v / p.h_qk);
+
+    // Which sequence and chunk this slot holds (idle slots leave at once).
+    int64_t n;
+    if (p.cu_seqlens == nullptr) {
+        n = slot / p.chunks_per_seq;
+        if (n >= p.num_seqs) return;
+    } else {
+        int64_t lo = 0, hi = p.num_seqs - 1;       // last n with slot_base(n) <= slot
+        if (slot_base(p, 0) > slot) return;
+        while (lo < hi) {
+            const int64_t mid = (lo + hi + 1) >> 1;
+            if (slot_base(p, mid) <= slot) lo = mid; else hi = mid - 1;
+        }
+        n = lo;
+    }
+    int64_t t0, t1;
+    if (!seq_range(p.cu_seqlens, p.seqlen, p.num_seqs, p.status, n, t0, t1)) return;
+    const int64_t c = slot - slot_base(p, n);
+    if (c * kC >= t1 - t0) return;
+    const int64_t tc0 = t0 + c * kC;
+    const int Lc = (int)((t1 - tc0) < kC ? (t1 - tc0) : kC);
+    uint8_t *rec = p.ws + (size_t)blockIdx.x * kRecord;
+
+    float *const As = reinterpret_cast<float *>(sm + PP_AS);
+    const uint32_t aKQW = smem_u32(sm + PP_KQW), aTT = smem_u32(sm + PP_TT), aV = smem_u32(sm + PP_V);
+    if (warp == 0) {
+        tmem_alloc(&ctl.tmem, 256);
+        tmem_relinquish();
+    }
+    if (pt == 0) {
+        mbar_init(&ctl.full, 1);
+        mbar_init(&ctl.d1, 1);
+        mbar_init(&ctl.d23, 1);
+        fence_mbar_init();
+    }
+    // [T'; T''] blocks above the diagonal are never written: keep them zero.
+    for (int e = pt; e < 16384 / 16; e += kPrepThreads)
+        *reinterpret_cast<uint4 *>(sm + PP_TT + 16 * e) = make_uint4(0, 0, 0, 0);
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl.tmem;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+
+    uint32_t issued = 0;                           // MMA groups issued (thread 0): 2 = D1, 4 = D2/D3
+    if (pt == 0) {
+        const int tok = (int)tc0;
+        mbar_arrive_expect_tx(&ctl.full, 2 * 2 * 8192 + 2 * 8192 + (p.gate_tma ? 2048 : 0));
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            tma_load_3d(sm + PP_KQW + r * kRegion, &p.tm_k, r * 64, hq, tok, &ctl.full);
+            tma_load_3d(sm + PP_KQW + r * kRegion + 8192, &p.tm_q, r * 64, hq, tok, &ctl.full);
+            tma_load_3d(sm + PP_V + r * 8192, &p.tm_v, r * 64, h, tok, &ctl.full);
+        }
+        if (p.gate_tma) {
+            tma_load_2d(sm + PP_GT, &p.tm_a, h & ~7, tok, &ctl.full);
+            tma_load_2d(sm + PP_GT + 1024, &p.tm_b, h & ~7, tok, &ctl.full);
+        }
+    }
+    // Gate logits without TMA: plain loads, issued before the wait.
+    float ra = 0.f, rb = 0.f;
+    if (!p.gate_tma && pt < Lc) {
+        ra = IoType<IO>::ld(static_cast<const IO *>(p.a) + (size_t)(tc0 + pt) * p.h_v + h);
+        rb = IoType<IO>::ld(static_cast<const IO *>(p.b) + (size_t)(tc0 + pt) * p.h_v + h);
+    }
+    bool ok = mbar_wait(&ctl.full, 0, kWaitBudget);
+    bool failed = bar_any(kBarPrep, kPrepThreads, !ok);
+
+    if (!failed) {
+        // D1 = [K; Q] K^T; the gates are computed meanwhile.
+        if (pt == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t off = (k >> 2) * kRegion + (k & 3) * 32;
+                mma_f16(tmem, sw128_desc(aKQW + off, 16, 1024), sw128_desc(aKQW + off, 16, 1024), kIdD1,
+                        k > 0);
+            }
+            mma_commit(&ctl.d1);
+            issued |= 2;
+        }
+        float gsum = 0.f, be = 0.f;
+        if (pt < kC) {
+            if (p.gate_tma) {
+                const IO *gt = reinterpret_cast<const IO *>(sm + PP_GT);
+                ra = IoType<IO>::ld(gt + pt * 8 + (h & 7));
+                rb = IoType<IO>::ld(gt + 512 + pt * 8 + (h & 7));
+            }
+            if (pt < Lc) {
+                gsum = decay_f(ra, p.A_log[h], p.dt_bias[h]);
+                be = sigmoid_f(rb);
+            }
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, gsum, off);
+                if (lane >= off) gsum += y;
+            }
+            if (lane == 31) ctl.wsum[warp] = gsum;
+        }
+        named_bar(kBarPrep, kPrepThreads);
+        if (pt < kC) {
+            ctl.G[pt] = gsum + (warp == 1 ? ctl.wsum[0] : 0.f);
+            ctl.beta[pt] = be;
+        }
+        named_bar(kBarPrep, kPrepThreads);
+        const float GC = ctl.G[kC - 1], Gm = ctl.G[31];
+        if (pt < kC) {
+            const float G = ctl.G[pt];
+            ctl.gr.gam[pt] = __expf(G);
+            ctl.gr.kf[pt] = __expf(GC - G);
+            ctl.E[pt] = __expf(G - Gm);
+            ctl.F[pt] = __expf(Gm - G);
+            if (pt == 0) ctl.gr.gC = __expf(GC);
+        }
+        ok = mbar_wait(&ctl.d1, 0, kWaitBudget);
+        failed = bar_any(kBarPrep, kPrepThreads, !ok);   // also publishes E, F, gamma
+    }
+    if (!failed) {
+        tc_fence_after();
+        // A rows (lanes 0-63, fp32) and P rows (lanes 64-127, I/O type); each column half
+        // of the warps takes 32 of the 64 columns.
+        {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_base + 32 * hf, r);
+            tmem_ld_wait();
+            const int i = (32 * q + lane) & 63;
+            const float Ei = ctl.E[i], Gi = ctl.G[i];
+            // e^{G_i - G_m} e^{G_m - G_j} cannot overflow while G spans at most 80.
+            const bool safe = (ctl.G[0] - ctl.G[kC - 1]) <= 80.f;
+            if (q < 2) {
+                const float bi = ctl.beta[i];
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    float x[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 32 * hf + 4 * j4 + e;
+                        const float d = safe ? Ei * ctl.F[j] : __expf(Gi - ctl.G[j]);
+                        x[e] = (j < i) ? bi * d * __uint_as_float(r[4 * j4 + e]) : 0.f;
+                    }
+                    *reinterpret_cast<float4 *>(As + i * kAs + 32 * hf + 4 * j4) =
+                        make_float4(x[0], x[1], x[2], x[3]);
+                }
+            } else {
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int j = 32 * hf + 8 * q8 + e;
+                        const float d = safe ? Ei * ctl.F[j] : __expf(Gi - ctl.G[j]);
+                        x[e] = (j <= i) ? p.scale * d * __uint_as_float(r[8 * q8 + e]) : 0.f;
+                    }
+                    *reinterpret_cast<uint4 *>(sm + PP_PS + sw128_offset(i, 4 * hf + q8)) = pack8<IO>(x);
+                }
+            }
+        }
+        // D1 has read Q: scale it in place, Q~ = diag(scale gamma) Q.
+        for (int e = pt; e < 1024; e += kPrepThreads) {
+            const int r = e >> 9, row = (e >> 3) & 63, ch = e & 7;
+            uint8_t *ptr = sm + PP_KQW + r * kRegion + 8192 + sw128_offset(row, ch);
+            const uint4 u = *reinterpret_cast<const uint4 *>(ptr);
+            const float f = p.scale * ctl.gr.gam[row];
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            float x[8];
+#pragma unroll
+            for (int k2 = 0; k2 < 4; ++k2) {
+                const float2 t2 = Pack<IO>::unpack(w[k2]);
+                x[2 * k2] = t2.x * f;
+                x[2 * k2 + 1] = t2.y * f;
+            }
+            *reinterpret_cast<uint4 *>(ptr) = pack8<IO>(x);
+        }
+        fence_async_smem();
+        named_bar(kBarPrep, kPrepThreads);
+        if (pt == 0) {
+            bulk_store(rec + REC_P, sm + PP_PS, 8192);
+            bulk_commit();
+        }
+
+        // T = (I + A)^-1, written as [T diag(beta gamma); T diag(beta)] (K-major); its
+        // merges reuse the P staging tile once the store above has read it.
+        invert_chunk<IO>(As, reinterpret_cast<float (*)[16][20]>(sm + PP_PS), sm + PP_TT, ctl.beta,
+                         ctl.gr.gam, pt);
+        fence_async_smem();
+        tc_fence_before();
+        named_bar(kBarPrep, kPrepThreads);
+
+        // D2 = [T'; T''] K -> columns 0-127 (W on lanes 0-63), D3 = [T'; T''] V ->
+        // columns 128-255 (U on lanes 64-127).
+        if (pt == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint64_t da = sw128_desc(aTT + k * 32, 16, 1024);
+                mma_f16(tmem, da, sw128_desc(aKQW + k * 2048, kRegion, 1024), kIdD2, k > 0);
+                mma_f16(tmem + 128, da, sw128_desc(aV + k * 2048, 8192, 1024), kIdD2, k > 0);
+            }
+            mma_commit(&ctl.d23);
+            issued |= 4;
+        }
+        ok = mbar_wait(&ctl.d23, 0, kWaitBudget);
+        failed = bar_any(kBarPrep, kPrepThreads, !ok);
+    }
+    if (!failed) {
+        tc_fence_after();
+        // W rows -> rows 128-191 of the K|Q|W regions; U rows -> the U image (over V).
+        const int row = 32 * q + lane;
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_base + (q < 2 ? 0 : 128) + 64 * hf + c0, r);
+            tmem_ld_wait();
+            float x[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
+            uint8_t *base = (q < 2) ? sm + PP_KQW + hf * kRegion : sm + PP_V + hf * 8192;
+            const int rr = (q < 2) ? 128 + row : row - 64;
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8)
+                *reinterpret_cast<uint4 *>(base + sw128_offset(rr, (c0 >> 3) + q8)) = pack8<IO>(x + 8 * q8);
+        }
+        fence_async_smem();
+        named_bar(kBarPrep, kPrepThreads);
+        if (pt == 0) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+                bulk_store(rec + REC_QW + r * 16384, sm + PP_KQW + r * kRegion + 8192, 16384);
+            bulk_store(rec + REC_U, sm + PP_V, 16384);
+            bulk_store(rec + REC_G, &ctl.gr, sizeof(GateRec));
+            bulk_commit();
+        }
+    }
+    if (failed && pt == 0) {
+        // Let the copies and MMAs already issued land before the CTA leaves (bounded).
+        atomicOr(p.status, kDevTimeout);
+        mbar_wait(&ctl.full, 0, kWaitBudget);
+        if (issued & 2) mbar_wait(&ctl.d1, 0, kWaitBudget);
+        if (issued & 4) mbar_wait(&ctl.d23, 0, kWaitBudget);
+    }
+    if (pt == 0) bulk_wait_all();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+// ===================================================================== state scan
+// Shared memory (from a 1024-aligned base): two stages, then the chain's own tiles.
+constexpr int SS_KQW = 0;                      // K (TMA) | Q~ W (record), two d_k regions
+constexpr int SS_U = 2 * kRegion;              // this column half of U, 64 x 128 B
+constexpr int SS_P = SS_U + 8192;              // P, 64 x 128 B (the MMA reads 64 more rows)
+constexpr int SS_G = SS_P + 8192;              // GateRec
+constexpr int kScanStage = SS_G + 1024;        // 65 KB
+constexpr int SS_SB = 2 * kScanStage;          // S0 in the I/O type, MN-major (d_k rows)
+constexpr int SS_DB0 = SS_SB + 16384;          // Delta, MN-major (token rows)
+constexpr int SS_DB1 = SS_DB0 + 8192;          // diag(e^{G_C - G}) Delta
+constexpr int SS_OUT = SS_DB1 + 8192;          // output tile staging
+constexpr int kScanSmem = SS_OUT + 8192 + 1024;
+constexpr uint32_t kScanTx = 2 * 8192 + 2 * 16384 + 8192 + 8192 + sizeof(GateRec);
+constexpr uint32_t TS_D4 = 0, TS_DS = 64;      // TMEM columns
+
+struct ScanCtl {
+    uint64_t full[2], d4, d5;
+    uint32_t tmem;
+};
+
+template <typename IO>
+__global__ void __launch_bounds__(kScanThreads, 1) gdn_chunk_scan(const __grid_constant__ TcParams p) {
+    constexpr bool kBf16 = std::is_same<IO, __nv_bfloat16>::value;
     constexpr uint32_t kIdNV = idesc_f16(kBf16, 128, kNV, false, true);
     constexpr uint32_t kIdDS = idesc_f16(kBf16, 128, kNV, true, true);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-    __shared__ Ctl ctl;
-
+    __shared__ ScanCtl ctl;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;   // rank = column half
+    const int q = warp & 3, g = warp >> 2;         // TMEM lane quarter, 32-column group
+    const int row = 32 * q + lane;                 // this thread's TMEM lane
+    const int half = blockIdx.x & 1;
     const int h = (blockIdx.x >> 1) % p.h_v;
     const int64_t n = (int64_t)(blockIdx.x >> 1) / p.h_v;
     const int hq = h / (p.h_v / p.h_qk);
-    const int v0 = (int)rank * kNV;
+    const int v0 = half * kNV;
 
-    // Both CTAs of a cluster share (n, h), so they leave here together.
     int64_t t0, t1;
     if (!seq_range(p.cu_seqlens, p.seqlen, p.num_seqs, p.status, n, t0, t1)) return;
     const int64_t L = t1 - t0;
     const int nchunks = (int)((L + kC - 1) / kC);
-
-    float *const As = reinterpret_cast<float *>(sm + OFF_AS);
-    const uint32_t aStage = smem_u32(sm + OFF_STAGE), aPZ = smem_u32(sm + OFF_PZ);
-    const uint32_t aTT = smem_u32(sm + OFF_TT), aTTR = smem_u32(sm + OFF_TTR);
-    const uint32_t aSB = smem_u32(sm + OFF_SB);
-    const uint32_t aDB0 = smem_u32(sm + OFF_DB0), aDB1 = smem_u32(sm + OFF_DB1);
+    const int64_t base_slot = slot_base(p, n);
 
     if (warp == 0) {
-        tmem_alloc(&ctl.tmem, 512);
+        tmem_alloc(&ctl.tmem, 128);
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&ctl.full[i], 1);
-            mbar_init(&ctl.prep_done[i], 1);
-            mbar_init(&ctl.chain_done[i], 1);
-            mbar_init(&ctl.recv[i], 1);
-            mbar_init(&ctl.recvd[i], 1);
-            mbar_init(&ctl.peer_free[i], 1);
-        }
-        mbar_init(&ctl.d1, 1);
-        mbar_init(&ctl.d23, 1);
+        mbar_init(&ctl.full[0], 1);
+        mbar_init(&ctl.full[1], 1);
         mbar_init(&ctl.d4, 1);
         mbar_init(&ctl.d5, 1);
-        ctl.abort = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&p.tm_q);
         tma_prefetch_desc(&p.tm_k);
-        tma_prefetch_desc(&p.tm_v);
+        tma_prefetch_desc(&p.tm_o);
     }
-    // Zero the P tiles, [T'; T''] (its blocks above the diagonal stay zero) and the
-    // receive tile [0; T''], so every operand row an MMA reads is finite.
-    for (int e = tid; e < (2 * 8192 + 2 * 16384) / 16; e += kThreads)
-        *reinterpret_cast<uint4 *>(sm + OFF_PZ + 16 * e) = make_uint4(0, 0, 0, 0);
-    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    cluster_sync();   // the peer's barriers exist before any remote arrive or copy
     const uint32_t tmem = ctl.tmem;
-    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    const uint32_t aSB = smem_u32(sm + SS_SB), aDB0 = smem_u32(sm + SS_DB0), aDB1 = smem_u32(sm + SS_DB1);
     const size_t sbase = ((size_t)n * p.h_v + h) * kDK * kDK;
-    auto owns = [&](int c) { return (uint32_t)(c & 1) == rank; };
+    IO *go = static_cast<IO *>(p.o);
 
-    // TMA of chunk c into stage c & 1: K, Q and V always; the gate logits only for the
-    // chunks this CTA preps.
+    // Chunk c into stage c & 1: K by TMA, the record's [Q~; W], U half, P and gates by
+    // bulk copy.  One thread.
     auto issue_stage = [&](int c) {
         const int s = c & 1;
-        const bool own = owns(c);
-        uint8_t *st = sm + OFF_STAGE + s * kStage;
-        const int tok = (int)(t0 + (int64_t)c * kC);
-        const uint32_t tx = 2 * 2 * 8192 + 8192 + ((own && p.gate_tma) ? 2048 : 0);
-        mbar_arrive_expect_tx(&ctl.full[s], tx);
+        uint8_t *st = sm + s * kScanStage;
+        const uint8_t *rec = p.ws + (size_t)((base_slot + c) * p.h_v + h) * kRecord;
+        mbar_arrive_expect_tx(&ctl.full[s], kScanTx);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-            tma_load_3d(st + r * kRegion, &p.tm_k, r * 64, hq, tok, &ctl.full[s]);
-            tma_load_3d(st + r * kRegion + 8192, &p.tm_q, r * 64, hq, tok, &ctl.full[s]);
+            tma_load_3d(st + SS_KQW + r * kRegion, &p.tm_k, r * 64, hq, (int)(t0 + (int64_t)c * kC),
+                        &ctl.full[s]);
+            bulk_load(st + SS_KQW + r * kRegion + 8192, rec + REC_QW + r * 16384, 16384, &ctl.full[s]);
         }
-        tma_load_3d(st + 2 * kRegion, &p.tm_v, v0, h, tok, &ctl.full[s]);
-        if (own && p.gate_tma) {
-            tma_load_2d(st + kGates, &p.tm_a, h & ~7, tok, &ctl.full[s]);
-            tma_load_2d(st + kGates + 1024, &p.tm_b, h & ~7, tok, &ctl.full[s]);
-        }
+        bulk_load(st + SS_U, rec + REC_U + half * 8192, 8192, &ctl.full[s]);
+        bulk_load(st + SS_P, rec + REC_P, 8192, &ctl.full[s]);
+        bulk_load(st + SS_G, rec + REC_G, sizeof(GateRec), &ctl.full[s]);
     };
 
-    if (tid < kPrepThreads) {
-        // ============================================================== prep role
-        // Preps the chunks c with c % 2 == rank, for this CTA's chain and the peer's.
-        const int pt = tid;
-        const int q = warp & 3, hf = warp >> 2;    // TMEM lane quarter, column half
-        const IO *ga = static_cast<const IO *>(p.a);
-        const IO *gb = static_cast<const IO *>(p.b);
-        const float A_log = p.A_log[h], dt_bias = p.dt_bias[h];
-        bool failed = false;
-        for (int c = (int)rank; c < nchunks; c += 2) {
-            const int b = c & 1, s = c & 1;
-            const int64_t tc0 = t0 + (int64_t)c * kC;
-            const int Lc = (int)((L - (int64_t)c * kC) < kC ? (L - (int64_t)c * kC) : kC);
-            GateBuf &gbuf = ctl.gb[b];
-            bool ok = true;
-            if (c >= 2) {
-                ok = mbar_wait(&ctl.chain_done[b], ((c >> 1) - 1) & 1, kWaitBudget);
-                if (ok) ok = mbar_wait(&ctl.recvd[b], ((c >> 1) - 1) & 1, kWaitBudget);
-            }
-            if (ok) ok = mbar_wait(&ctl.full[s], (c >> 1) & 1, kWaitBudget);
-            if (bar_any(kBarPrep, kPrepThreads, !ok || *(volatile int *)&ctl.abort)) { failed = true; break; }
+    // S rows of this thread: d_k row `row`, columns v0 + 32 g + [0, 32).
+    float S[32];
+    {
+        const float4 *src = reinterpret_cast<const float4 *>(p.state_in + sbase + (size_t)row * kDK + v0 + 32 * g);
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+            const float4 f = p.state_in ? src[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
+            S[4 * q4] = f.x; S[4 * q4 + 1] = f.y; S[4 * q4 + 2] = f.z; S[4 * q4 + 3] = f.w;
+        }
+    }
+    auto write_sb = [&]() {   // S (fp32 registers) -> MN-major operand tile, row = d_k index
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8)
+            *reinterpret_cast<uint4 *>(sm + SS_SB + sw128_offset(row, 4 * g + q8)) = pack8<IO>(S + 8 * q8);
+    };
+    write_sb();
+    fence_async_smem();
+    if (tid == 0) {
+        if (nchunks > 0) issue_stage(0);
+        if (nchunks > 1) issue_stage(1);
+    }
+    __syncthreads();
 
-            // D1 = [K; Q] K^T (the stage has landed); the gates are computed meanwhile.
-            if (pt == 0) {
+    bool failed = false;
+    int c_fail = 0;
+    uint64_t *mma_pending = nullptr;               // thread 0: an MMA group whose wait gave up
+    for (int c = 0; c < nchunks; ++c) {
+        const int s = c & 1;
+        const uint8_t *st = sm + s * kScanStage;
+        const uint32_t aSt = smem_u32(st);
+        const GateRec &gr = *reinterpret_cast<const GateRec *>(st + SS_G);
+        const int64_t tc0 = t0 + (int64_t)c * kC;
+        const int Lc = (int)((L - (int64_t)c * kC) < kC ? (L - (int64_t)c * kC) : kC);
+
+        // D4 = [Q~; W] S0 once the stage has landed.
+        bool ok = true;
+        if (tid == 0) {
+            ok = mbar_wait(&ctl.full[s], (c >> 1) & 1, kWaitBudget);
+            if (ok) {
                 tc_fence_after();
-                const uint32_t st = aStage + s * kStage;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t off = (k >> 2) * kRegion + (k & 3) * 32;
-                    mma_f16(tmem + TM_D1, sw128_desc(st + off, 16, 1024),
-                            sw128_desc(st + off, 16, 1024), kIdD1, k > 0);
-                }
-                mma_commit(&ctl.d1);
-            }
-
-            // Gates and prefix sums (threads 0-63 = tokens of the chunk).
-            float gsum = 0.f, be = 0.f;
-            if (pt < kC) {
-                float ra = 0.f, rb = 0.f;
-                if (p.gate_tma) {
-                    const IO *gt = reinterpret_cast<const IO *>(sm + OFF_STAGE + s * kStage + kGates);
-                    ra = IoType<IO>::ld(gt + pt * 8 + (h & 7));
-                    rb = IoType<IO>::ld(gt + 512 + pt * 8 + (h & 7));
-                } else if (pt < Lc) {
-                    ra = IoType<IO>::ld(ga + (size_t)(tc0 + pt) * p.h_v + h);
-                    rb = IoType<IO>::ld(gb + (size_t)(tc0 + pt) * p.h_v + h);
-                }
-                if (pt < Lc) {
-                    gsum = decay_f(ra, A_log, dt_bias);
-                    be = sigmoid_f(rb);
-                }
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, gsum, off);
-                    if (lane >= off) gsum += y;
-                }
-                if (lane == 31) ctl.wsum[warp] = gsum;
-            }
-            named_bar(kBarPrep, kPrepThreads);
-            if (pt < kC) {
-                ctl.G[pt] = gsum + (warp == 1 ? ctl.wsum[0] : 0.f);
-                ctl.beta[pt] = be;
-            }
-            named_bar(kBarPrep, kPrepThreads);
-            const float GC = ctl.G[kC - 1], Gm = ctl.G[31];
-            const bool safe = (ctl.G[0] - GC) <= 80.f;   // e^{G_i - G_m} e^{G_m - G_j} cannot overflow
-            if (pt < kC) {
-                const float G = ctl.G[pt];
-                gbuf.gam[pt] = __expf(G);
-                gbuf.kf[pt] = __expf(GC - G);
-                ctl.E[pt] = __expf(G - Gm);
-                ctl.F[pt] = __expf(Gm - G);
-                if (pt == 0) gbuf.gC = __expf(GC);
-            }
-            named_bar(kBarPrep, kPrepThreads);   // E, F, gamma visible to every prep warp
-            ok = mbar_wait(&ctl.d1, (c >> 1) & 1, kWaitBudget);
-            tc_fence_after();
-
-            // A rows (lanes 0-63, fp32) and P rows (lanes 64-127, I/O type); each column
-            // half of the prep warps takes 32 of the 64 columns.
-            {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_base + TM_D1 + 32 * hf, r);
-                tmem_ld_wait();
-                const int i = (32 * q + lane) & 63;
-                const float Ei = ctl.E[i], Gi = ctl.G[i];
-                if (q < 2) {
-                    const float bi = ctl.beta[i];
-#pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        float x[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int j = 32 * hf + 4 * j4 + e;
-                            const float d = safe ? Ei * ctl.F[j] : __expf(Gi - ctl.G[j]);
-                            x[e] = (j < i) ? bi * d * __uint_as_float(r[4 * j4 + e]) : 0.f;
-                        }
-                        *reinterpret_cast<float4 *>(As + i * kAs + 32 * hf + 4 * j4) =
-                            make_float4(x[0], x[1], x[2], x[3]);
-                    }
-                } else {
-                    uint8_t *pz = sm + OFF_PZ + b * 8192;
-#pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8) {
-                        float x[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int j = 32 * hf + 8 * q8 + e;
-                            const float d = safe ? Ei * ctl.F[j] : __expf(Gi - ctl.G[j]);
-                            x[e] = (j <= i) ? p.scale * d * __uint_as_float(r[8 * q8 + e]) : 0.f;
-                        }
-                        *reinterpret_cast<uint4 *>(pz + sw128_offset(i, 4 * hf + q8)) = pack8<IO>(x);
-                    }
-                }
-            }
-            // D1 has read Q: scale the stage's Q rows in place, Q~ = diag(scale gamma) Q,
-            // so that [Q~; W] S0 yields the inter-chunk output term directly.
-            for (int e = pt; e < 1024; e += kPrepThreads) {
-                const int r = e >> 9, row = (e >> 3) & 63, ch = e & 7;
-                uint8_t *ptr = sm + OFF_STAGE + s * kStage + r * kRegion + 8192 + sw128_offset(row, ch);
-                const uint4 u = *reinterpret_cast<const uint4 *>(ptr);
-                const float f = p.scale * gbuf.gam[row];
-                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-                float x[8];
-#pragma unroll
-                for (int k2 = 0; k2 < 4; ++k2) {
-                    const float2 t2 = Pack<IO>::unpack(w[k2]);
-                    x[2 * k2] = t2.x * f;
-                    x[2 * k2 + 1] = t2.y * f;
-                }
-                *reinterpret_cast<uint4 *>(ptr) = pack8<IO>(x);
-            }
-            fence_async_smem();
-            if (bar_any(kBarPrep, kPrepThreads, !ok)) { failed = true; break; }
-
-            // T = (I + A)^-1, written as [T diag(beta gamma); T diag(beta)] (K-major).
-            invert_chunk<IO>(As, ctl.X, sm + OFF_TT, ctl.beta, gbuf.gam, pt);
-            fence_async_smem();
-            tc_fence_before();
-            named_bar(kBarPrep, kPrepThreads);
-
-            // D2 = [T'; T''] K and D3 = [T'; T''] V (B operands MN-major from the stage).
-            if (pt == 0) {
-                tc_fence_after();
-                const uint32_t st = aStage + s * kStage;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint64_t da = sw128_desc(aTT + k * 32, 16, 1024);
-                    mma_f16(tmem + TM_D2, da, sw128_desc(st + k * 2048, kRegion, 1024), kIdD2, k > 0);
-                    mma_f16(tmem + TM_D3 + 64 * b, da, sw128_desc(st + 2 * kRegion + k * 2048, 8192, 1024),
-                            kIdNV, k > 0);
-                }
-                mma_commit(&ctl.d23);
-            }
-            ok = mbar_wait(&ctl.d23, (c >> 1) & 1, kWaitBudget);
-            tc_fence_after();
-
-            // W (lanes 0-63 of D2) -> rows 128-191 of the stage's K|Q|W regions.
-            if (q < 2) {
-                const int i = 32 * q + lane;
-                uint8_t *reg = sm + OFF_STAGE + s * kStage + hf * kRegion;
-#pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lane_base + TM_D2 + 64 * hf + c0, r);
-                    tmem_ld_wait();
-                    float x[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
-#pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8)
-                        *reinterpret_cast<uint4 *>(reg + sw128_offset(128 + i, (c0 >> 3) + q8)) =
-                            pack8<IO>(x + 8 * q8);
-                }
-            }
-            fence_async_smem();
-            tc_fence_before();
-            if (bar_any(kBarPrep, kPrepThreads, !ok)) { failed = true; break; }
-            if (pt == 0) {
-                mbar_arrive(&ctl.prep_done[b]);
-                // Hand the chunk to the peer once it has released the previous one:
-                // the W rows of both d_k halves, P, T'' and the gate values.
-                ok = (c < 2) || mbar_wait(&ctl.peer_free[b], ((c >> 1) - 1) & 1, kWaitBudget);
-                if (ok) {
-                    const uint32_t rb = mapa_shared(smem_u32(&ctl.recv[b]), peer);
-                    uint8_t *st = sm + OFF_STAGE + s * kStage;
-#pragma unroll
-                    for (int r = 0; r < 2; ++r)
-                        bulk_copy_to_cluster(mapa_shared(smem_u32(st + r * kRegion + 16384), peer),
-                                             st + r * kRegion + 16384, 8192, rb);
-                    bulk_copy_to_cluster(mapa_shared(aPZ + b * 8192, peer), sm + OFF_PZ + b * 8192, 8192, rb);
-                    bulk_copy_to_cluster(mapa_shared(aTTR + 8192, peer), sm + OFF_TT + 8192, 8192, rb);
-                    bulk_copy_to_cluster(mapa_shared(smem_u32(&gbuf), peer), &gbuf, sizeof(GateBuf), rb);
-                }
-            }
-            if (bar_any(kBarPrep, kPrepThreads, !ok)) { failed = true; break; }
-        }
-        if (failed && pt == 0) {
-            ctl.abort = 1;
-            atomicOr(p.status, kDevTimeout);
-        }
-    } else {
-        // ============================================================== chain role
-        const int ct = tid - kPrepThreads;         // = TMEM lane = d_k row of S
-        const int cw = ct >> 5;
-        IO *go = static_cast<IO *>(p.o);
-        float S[kNV];
-        {
-            const float4 *src = reinterpret_cast<const float4 *>(p.state_in + sbase +
-                                                                 (size_t)ct * kDK + v0);
-#pragma unroll
-            for (int q4 = 0; q4 < kNV / 4; ++q4) {
-                const float4 f = p.state_in ? src[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
-                S[4 * q4] = f.x; S[4 * q4 + 1] = f.y; S[4 * q4 + 2] = f.z; S[4 * q4 + 3] = f.w;
-            }
-        }
-        auto write_sb = [&]() {   // S (fp32 registers) -> MN-major operand tile, row = ct
-#pragma unroll
-            for (int q8 = 0; q8 < 8; ++q8)
-                *reinterpret_cast<uint4 *>(sm + OFF_SB + sw128_offset(ct, q8)) = pack8<IO>(S + 8 * q8);
-        };
-        write_sb();
-        fence_async_smem();
-        if (ct == 0) {
-            if (nchunks > 0) issue_stage(0);
-            if (nchunks > 1) issue_stage(1);
-        }
-        named_bar(kBarChain, kChainThreads);
-        bool failed = false;
-        for (int c = 0; c < nchunks; ++c) {
-            const int b = c & 1, s = c & 1;
-            const bool own = owns(c);
-            const int64_t tc0 = t0 + (int64_t)c * kC;
-            const int Lc = (int)((L - (int64_t)c * kC) < kC ? (L - (int64_t)c * kC) : kC);
-            bool ok;
-            if (own) {
-                ok = mbar_wait(&ctl.prep_done[b], (c >> 1) & 1, kWaitBudget);
-            } else {
-                if (ct == 0) mbar_arrive_expect_tx(&ctl.recv[b], kPeerBytes);
-                ok = mbar_wait(&ctl.recv[b], (c >> 1) & 1, kWaitBudget);
-                if (ok) ok = mbar_wait(&ctl.full[s], (c >> 1) & 1, kWaitBudget);
-                if (ok && ct == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl.recvd[b]), peer));
-                if (ok) {   // Q~ = diag(scale gamma) Q in place, as the owner did for its copy
-                    for (int e = ct; e < 1024; e += kChainThreads) {
-                        const int r = e >> 9, row = (e >> 3) & 63, ch = e & 7;
-                        uint8_t *ptr = sm + OFF_STAGE + s * kStage + r * kRegion + 8192 +
-                                       sw128_offset(row, ch);
-                        const uint4 u = *reinterpret_cast<const uint4 *>(ptr);
-                        const float f = p.scale * ctl.gb[b].gam[row];
-                        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-                        float x[8];
-#pragma unroll
-                        for (int k2 = 0; k2 < 4; ++k2) {
-                            const float2 t2 = Pack<IO>::unpack(w[k2]);
-                            x[2 * k2] = t2.x * f;
-                            x[2 * k2 + 1] = t2.y * f;
-                        }
-                        *reinterpret_cast<uint4 *>(ptr) = pack8<IO>(x);
-                    }
-                    fence_async_smem();
-                }
-            }
-            if (ct == 0) bulk_wait_read();   // the previous output tile (in DB0) has been read
-            if (bar_any(kBarChain, kChainThreads, !ok || *(volatile int *)&ctl.abort)) { failed = true; break; }
-            tc_fence_after();
-            const uint32_t st = aStage + s * kStage;
-
-            // (Received chunks: U = T'' V of this half.)  D4 = [Q~; W] S0.
-            if (ct == 0) {
-                if (!own) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_f16(tmem + TM_D3 + 64 * b, sw128_desc(aTTR + k * 32, 16, 1024),
-                                sw128_desc(st + 2 * kRegion + k * 2048, 8192, 1024), kIdNV, k > 0);
-                }
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t off = (k >> 2) * kRegion + 8192 + (k & 3) * 32;
-                    mma_f16(tmem + TM_D4, sw128_desc(st + off, 16, 1024),
+                    mma_f16(tmem + TS_D4, sw128_desc(aSt + off, 16, 1024),
                             sw128_desc(aSB + k * 2048, 16384, 1024), kIdNV, k > 0);
                 }
                 mma_commit(&ctl.d4);
-            }
-            ok = mbar_wait(&ctl.d4, c & 1, kWaitBudget);
-            tc_fence_after();
-
-            // Delta = U - W S0 on lanes 64-127 (token rows), in two versions.
-            if (cw >= 2) {
-                const int j = ct - 64;
-                const float kfj = ctl.gb[b].kf[j];
-#pragma unroll
-                for (int c0 = 0; c0 < kNV; c0 += 32) {
-                    uint32_t ws[32], u[32];
-                    tmem_ld32(tmem + lane_base + TM_D4 + c0, ws);
-                    tmem_ld32(tmem + lane_base + TM_D3 + 64 * b + c0, u);
-                    tmem_ld_wait();
-                    float x[32], y[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        x[e] = __uint_as_float(u[e]) - __uint_as_float(ws[e]);
-                        y[e] = kfj * x[e];
-                    }
-#pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8) {
-                        const uint32_t off = sw128_offset(j, (c0 >> 3) + q8);
-                        *reinterpret_cast<uint4 *>(sm + OFF_DB0 + off) = pack8<IO>(x + 8 * q8);
-                        *reinterpret_cast<uint4 *>(sm + OFF_DB1 + off) = pack8<IO>(y + 8 * q8);
-                    }
-                }
-            }
-            fence_async_smem();
-            tc_fence_before();
-            if (bar_any(kBarChain, kChainThreads, !ok)) { failed = true; break; }
-
-            // D4[0:64] += P Delta (the A rows past P land in the spent W S0 lanes);
-            // DS = K^T diag(e^{G_C - G}) Delta.
-            if (ct == 0) {
-                tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    mma_f16(tmem + TM_D4, sw128_desc(aPZ + b * 8192 + k * 32, 16, 1024),
-                            sw128_desc(aDB0 + k * 2048, 8192, 1024), kIdNV, 1u);
-                    mma_f16(tmem + TM_DS, sw128_desc(st + k * 2048, kRegion, 1024),
-                            sw128_desc(aDB1 + k * 2048, 8192, 1024), kIdDS, k > 0);
-                }
-                mma_commit(&ctl.d5);
-            }
-            ok = mbar_wait(&ctl.d5, c & 1, kWaitBudget);
-            tc_fence_after();
-            // The stage's last readers are done: refill it with chunk c + 2.
-            if (ct == 0 && ok && c + 2 < nchunks) issue_stage(c + 2);
-
-            // S = gamma_C S0 + DS (fp32 registers), then the next chunk's operand tile.
-            {
-                const float gC = ctl.gb[b].gC;
-#pragma unroll
-                for (int c0 = 0; c0 < kNV; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lane_base + TM_DS + c0, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) S[c0 + e] = fmaf(gC, S[c0 + e], __uint_as_float(r[e]));
-                }
-                write_sb();
-            }
-            // o_i = (Q~ S0 + P Delta)_i on lanes 0-63.  A full chunk goes out as one TMA
-            // store of a 64 x 64 tile staged in DB0 (free once D4 and DS have read it); a
-            // sequence's ragged last chunk is stored row by row so that no row of the next
-            // sequence is touched.
-            const bool tile_store = (Lc == kC);
-            if (cw < 2) {
-                const int i = ct;
-#pragma unroll
-                for (int c0 = 0; c0 < kNV; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lane_base + TM_D4 + c0, r);
-                    tmem_ld_wait();
-                    float x[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
-                    if (tile_store) {
-#pragma unroll
-                        for (int q8 = 0; q8 < 4; ++q8)
-                            *reinterpret_cast<uint4 *>(sm + OFF_DB0 + sw128_offset(i, (c0 >> 3) + q8)) =
-                                pack8<IO>(x + 8 * q8);
-                    } else if (i < Lc) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(
-                            go + ((size_t)(tc0 + i) * p.h_v + h) * kDK + v0 + c0);
-#pragma unroll
-                        for (int q8 = 0; q8 < 4; ++q8) dst[q8] = pack8<IO>(x + 8 * q8);
-                    }
-                }
-            }
-            fence_async_smem();
-            tc_fence_before();
-            if (bar_any(kBarChain, kChainThreads, !ok)) { failed = true; break; }
-            if (ct == 0 && tile_store) {
-                tma_store_3d(&p.tm_o, sm + OFF_DB0, v0, h, (int)tc0);
-                bulk_commit();
-            }
-            if (ct == 0) {
-                if (own) mbar_arrive(&ctl.chain_done[b]);
-                else mbar_arrive_cluster(mapa_shared(smem_u32(&ctl.peer_free[b]), peer));
+                ok = mbar_wait(&ctl.d4, c & 1, kWaitBudget);
+                if (!ok) mma_pending = &ctl.d4;
             }
         }
-        if (ct == 0) bulk_wait_all();   // the output tiles have reached global memory
-        if (failed) {
-            if (ct == 0) {
-                ctl.abort = 1;
-                atomicOr(p.status, kDevTimeout);
-            }
-        } else {
-            float4 *dst = reinterpret_cast<float4 *>(p.state_out + sbase + (size_t)ct * kDK + v0);
+        if (bar_any(kBarChain, kScanThreads, !ok)) { failed = true; c_fail = c; break; }
+        tc_fence_after();
+        const float gC = gr.gC;   // read before the stage is refilled below
+
+        // Delta = U - W S0 on lanes 64-127 (token rows), this thread's 32 columns.
+        if (q >= 2) {
+            const int j = row - 64;
+            uint32_t ws[32];
+            tmem_ld32(tmem + lane_base + TS_D4 + 32 * g, ws);
+            float uf[32];
 #pragma unroll
-            for (int q4 = 0; q4 < kNV / 4; ++q4)
-                dst[q4] = make_float4(S[4 * q4], S[4 * q4 + 1], S[4 * q4 + 2], S[4 * q4 + 3]);
+            for (int q8 = 0; q8 < 4; ++q8) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(st + SS_U + sw128_offset(j, 4 * g + q8));
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int k2 = 0; k2 < 4; ++k2) {
+                    const float2 t2 = Pack<IO>::unpack(w[k2]);
+                    uf[8 * q8 + 2 * k2] = t2.x;
+                    uf[8 * q8 + 2 * k2 + 1] = t2.y;
+                }
+            }
+            tmem_ld_wait();
+            const float kfj = gr.kf[j];
+            float x[32], y[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                x[e] = uf[e] - __uint_as_float(ws[e]);
+                y[e] = kfj * x[e];
+            }
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8) {
+                const uint32_t off = sw128_offset(j, 4 * g + q8);
+                *reinterpret_cast<uint4 *>(sm + SS_DB0 + off) = pack8<IO>(x + 8 * q8);
+                *reinterpret_cast<uint4 *>(sm + SS_DB1 + off) = pack8<IO>(y + 8 * q8);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        named_bar(kBarChain, kScanThreads);
+
+        // DS = K^T diag(e^{G_C - G}) Delta;  D4[0:64] += P Delta (the A rows past P land
+        // in the spent W S0 lanes).
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_f16(tmem + TS_DS, sw128_desc(aSt + k * 2048, kRegion, 1024),
+                        sw128_desc(aDB1 + k * 2048, 8192, 1024), kIdDS, k > 0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_f16(tmem + TS_D4, sw128_desc(aSt + SS_P + k * 32, 16, 1024),
+                        sw128_desc(aDB0 + k * 2048, 8192, 1024), kIdNV, 1u);
+            mma_commit(&ctl.d5);
+            ok = mbar_wait(&ctl.d5, c & 1, kWaitBudget);
+            if (!ok) mma_pending = &ctl.d5;
+            // The stage's last readers are done: refill it with chunk c + 2.
+            if (ok && c + 2 < nchunks) issue_stage(c + 2);
+            bulk_wait_read();   // the previous output tile has been read
+        }
+        if (bar_any(kBarChain, kScanThreads, !ok)) { failed = true; c_fail = c; break; }
+        tc_fence_after();
+
+        // S = gamma_C S0 + DS (fp32 registers), then the next chunk's operand tile.
+        {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_base + TS_DS + 32 * g, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) S[e] = fmaf(gC, S[e], __uint_as_float(r[e]));
+            write_sb();
+        }
+        // o_i = (Q~ S0 + P Delta)_i on lanes 0-63.  A full chunk goes out as one TMA
+        // store of the staged 64 x 64 tile; a sequence's ragged last chunk is stored row
+        // by row so that no row of the next sequence is touched.
+        const bool tile_store = (Lc == kC);
+        if (q < 2) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_base + TS_D4 + 32 * g, r);
+            tmem_ld_wait();
+            float x[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
+            if (tile_store) {
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8)
+                    *reinterpret_cast<uint4 *>(sm + SS_OUT + sw128_offset(row, 4 * g + q8)) = pack8<IO>(x + 8 * q8);
+            } else if (row < Lc) {
+                uint4 *dst = reinterpret_cast<uint4 *>(go + ((size_t)(tc0 + row) * p.h_v + h) * kDK + v0 + 32 * g);
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8) dst[q8] = pack8<IO>(x + 8 * q8);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        named_bar(kBarChain, kScanThreads);
+        if (tid == 0 && tile_store) {
+            tma_store_3d(&p.tm_o, sm + SS_OUT, v0, h, (int)tc0);
+            bulk_commit();
         }
     }
-
+    if (failed && tid == 0) {
+        // Let the stage copies (chunks c_fail and c_fail + 1) and an MMA group already
+        // issued land before the CTA leaves (bounded).
+        atomicOr(p.status, kDevTimeout);
+        for (int w = c_fail; w < nchunks && w < c_fail + 2; ++w)
+            mbar_wait(&ctl.full[w & 1], (w >> 1) & 1, kWaitBudget);
+        if (mma_pending != nullptr) mbar_wait(mma_pending, c_fail & 1, kWaitBudget);
+    }
+    if (tid == 0) bulk_wait_all();   // the output tiles have reached global memory
+    if (!failed) {
+        float4 *dst = reinterpret_cast<float4 *>(p.state_out + sbase + (size_t)row * kDK + v0 + 32 * g);
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+            dst[q4] = make_float4(S[4 * q4], S[4 * q4 + 1], S[4 * q4 + 2], S[4 * q4 + 3]);
+    }
     tc_fence_before();
     __syncthreads();
-    cluster_sync();   // no remote copy or arrive may target a CTA that has exited
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(tmem, 128);
     }
 }
 
@@ -818,38 +846,56 @@ bool make_gate_map(CUtensorMap *m, const void *base, gdn_dtype io, int h_v, int6
     return r == CUDA_SUCCESS;
 }
 
+
 template <typename IO>
-cudaError_t launch_typed(const TcParams &tp, int64_t units, cudaStream_t stream) {
+cudaError_t launch_typed(const TcParams &tp, int64_t n_slots, cudaStream_t stream) {
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<IO>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+        cudaError_t e = cudaFuncSetAttribute(gdn_chunk_prep<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kPrepSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gdn_chunk_scan<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kScanSmem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const int64_t blocks = units * (kDK / kNV);
-    prefill_tc_kernel<IO><<<(unsigned)blocks, kThreads, kSmemAlloc, stream>>>(tp);
+    const int64_t prep_blocks = n_slots * tp.h_v;
+    const int64_t scan_blocks = (int64_t)tp.num_seqs * tp.h_v * (kDK / kNV);
+    if (prep_blocks > 0x7fffffffLL || scan_blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    gdn_chunk_prep<IO><<<(unsigned)prep_blocks, kPrepThreads, kPrepSmem, stream>>>(tp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    gdn_chunk_scan<IO><<<(unsigned)scan_blocks, kScanThreads, kScanSmem, stream>>>(tp);
     return cudaGetLastError();
+}
+
+// Chunk slots the prep kernel covers (an upper bound for packed sequences).
+int64_t chunk_slots(bool varlen, int64_t seqlen, int64_t batch, int64_t num_seqs) {
+    if (!varlen) return batch * ((seqlen + kC - 1) / kC);
+    return seqlen / kC + num_seqs + 1;
 }
 
 }  // namespace
 
+bool prefill_tc_shape_ok(gdn_dtype io, int d_k, int d_v, int64_t total_tokens) {
+    return (io == GDN_BF16 || io == GDN_F16) && d_k == kDK && d_v == kDK && total_tokens > 0 &&
+           total_tokens <= 0x7fffff00LL;
+}
+
+size_t prefill_tc_workspace(bool varlen, int64_t seqlen, int64_t batch, int64_t num_seqs, int h_v) {
+    return (size_t)chunk_slots(varlen, seqlen, batch, num_seqs) * (size_t)h_v * kRecord;
+}
+
 bool prefill_tc_supported(const ScanParams &p, gdn_dtype io, int64_t total_tokens) {
-    if (io != GDN_BF16 && io != GDN_F16) return false;
-    if (p.d_k != kDK || p.d_v != kDK) return false;
-    if (total_tokens <= 0 || total_tokens > 0x7fffff00LL) return false;
+    if (!prefill_tc_shape_ok(io, p.d_k, p.d_v, total_tokens)) return false;
     const void *ptrs[] = {p.q, p.k, p.v, p.o};
     for (const void *ptr : ptrs)
         if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return false;
-    if ((int64_t)p.num_seqs * p.h_v * 2 > 0x7fffffffLL) return false;
     return encode_fn() != nullptr;
 }
 
-int prefill_tc_columns(const ScanParams &) { return kNV; }
-
-cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_tokens, int nv,
+cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_tokens, void *workspace,
                               cudaStream_t stream) {
-    if (nv != kNV) return cudaErrorInvalidValue;
     TcParams tp;
     memset(&tp, 0, sizeof(tp));
     if (!make_map(&tp.tm_q, p.q, io, p.h_qk, total_tokens) ||
@@ -857,7 +903,7 @@ cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_t
         !make_map(&tp.tm_v, p.v, io, p.h_v, total_tokens) ||
         !make_map(&tp.tm_o, p.o, io, p.h_v, total_tokens))
         return cudaErrorInvalidValue;
-    // Gate logits ride along with each stage's TMA when their rows are 16-byte multiples.
+    // Gate logits ride along with the TMA when their rows are 16-byte multiples.
     tp.gate_tma = (p.h_v % 8 == 0 && reinterpret_cast<uintptr_t>(p.a) % 16 == 0 &&
                    reinterpret_cast<uintptr_t>(p.b) % 16 == 0 &&
                    make_gate_map(&tp.tm_a, p.a, io, p.h_v, total_tokens) &&
@@ -867,9 +913,12 @@ cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_t
     tp.state_in = p.state_in; tp.state_out = p.state_out; tp.o = p.o;
     tp.cu_seqlens = p.cu_seqlens; tp.seqlen = p.seqlen; tp.num_seqs = p.num_seqs;
     tp.h_qk = p.h_qk; tp.h_v = p.h_v; tp.scale = p.scale; tp.status = p.status;
-    const int64_t units = (int64_t)p.num_seqs * p.h_v;
-    if (io == GDN_BF16) return launch_typed<__nv_bfloat16>(tp, units, stream);
-    return launch_typed<__half>(tp, units, stream);
+    tp.chunks_per_seq = (int32_t)((p.seqlen + kC - 1) / kC);
+    tp.ws = static_cast<uint8_t *>(workspace);
+    const bool varlen = p.cu_seqlens != nullptr;
+    const int64_t n_slots = chunk_slots(varlen, p.seqlen, p.num_seqs, p.num_seqs);
+    if (io == GDN_BF16) return launch_typed<__nv_bfloat16>(tp, n_slots, stream);
+    return launch_typed<__half>(tp, n_slots, stream);
 }
 
 }  // namespace gdn
