@@ -100,6 +100,37 @@ gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, con
                        float *state_out, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * gdn_prefill_noalloc -- gdn_prefill without a caller-provided workspace.  The
+ * pages have no counterpart to this entry point; it exists for callers that may
+ * not allocate device memory: a plugin inside a host engine that owns the whole
+ * device-memory budget and hands out no allocator, or a latency-bound caller
+ * that cannot accept cudaMalloc's implicit device synchronisation.
+ *
+ * Arguments, layouts, results and errors are those of gdn_prefill, minus
+ * `workspace` and `workspace_bytes`.  The scratch is instead a fixed array of
+ * GDN_PREFILL_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library, one per device,
+ * created when the library's module is first used on that device; the call
+ * allocates nothing and frees nothing.  A shape whose
+ * gdn_prefill_workspace_bytes(shape) exceeds that size returns
+ * GDN_ERR_INVALID_ARG and launches nothing: 64 MiB holds 1,149 records of one
+ * (64-token chunk, value head), e.g. one 4,096-token sequence at 16 value heads.
+ * Shapes off the tensor-core path need no scratch and run as in gdn_prefill.
+ *
+ * All calls on a device share the one array.  Each call writes every scratch
+ * byte it reads before reading it, so no clearing is needed between calls, but
+ * two calls whose kernels overlap on the GPU (different streams, no ordering
+ * between them) race on the array and give wrong results: order such calls on
+ * one stream or with events.
+ */
+#define GDN_PREFILL_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+gdn_status gdn_prefill_noalloc(const gdn_shape *shape, const void *q, const void *k,
+                               const void *v, const void *a, const void *b, const float *A_log,
+                               const float *dt_bias, const float *state_in,
+                               const int32_t *cu_seqlens, float scale, void *o,
+                               float *state_out, void *stream);
+
+/*
  * gdn_decode_step -- one token per sequence (shape->seqlen must be 1 and
  * cu_seqlens is not taken): B = shape->batch = shape->num_seqs.  `state`
  * [B, h_v, d_k, d_v] fp32 is read and overwritten in place with the updated

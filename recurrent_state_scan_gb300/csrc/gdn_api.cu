@@ -104,6 +104,13 @@ gdn_status check_inputs(const gdn_shape *s, int64_t tokens, const void *q, const
 }
 
 }  // namespace
+
+// Record `message` as the calling thread's last error detail and return `status`
+// (for entry points defined in other translation units).
+gdn_status report_error(gdn_status status, const char *message) {
+    return fail(status, "%s", message);
+}
+
 }  // namespace gdn
 
 using namespace gdn;

@@ -88,6 +88,9 @@ __device__ __forceinline__ bool seq_range(const ScanParams &p, int64_t n, int64_
 // Launchers implemented in the kernel translation units.
 cudaError_t launch_scan_simt(const ScanParams &p, gdn_dtype io, cudaStream_t stream);
 
+// Sets the calling thread's last error message; returns `status`.
+gdn_status report_error(gdn_status status, const char *message);
+
 // Chunked tensor-core prefill (bf16/f16 I/O, d_k = d_v = 128): a chunk-prep kernel
 // that writes one workspace record per (chunk, value head), then a state-scan kernel.
 // prefill_tc_shape_ok: the shape rules alone (host-only).  prefill_tc_workspace: bytes

@@ -25,7 +25,7 @@ _DTYPE_CODE = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16, torch.float16: 
 # Every symbol include/gdn.h declares.
 EXPORTS = ("gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode_step",
            "gdn_prefill_plan", "gdn_last_device_status", "gdn_status_string",
-           "gdn_last_error_message")
+           "gdn_last_error_message", "gdn_prefill_noalloc")
 PATH_SIMT, PATH_TC = 1, 2
 
 
@@ -66,6 +66,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.gdn_prefill.restype = ctypes.c_int
     lib.gdn_prefill.argtypes = [S, P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P,
                                 ctypes.c_size_t, P]
+    lib.gdn_prefill_noalloc.restype = ctypes.c_int
+    lib.gdn_prefill_noalloc.argtypes = [S, P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P]
     lib.gdn_decode_step.restype = ctypes.c_int
     lib.gdn_decode_step.argtypes = [S, P, P, P, P, P, P, P, P, ctypes.c_float, P, P]
     lib.gdn_prefill_plan.restype = ctypes.c_int
@@ -177,6 +179,37 @@ def gdn_prefill(q, k, v, a, b, A_log, dt_bias, state_in=None, cu_seqlens=None,
                            _ptr(A_log), _ptr(dt_bias), _ptr(state_in), _ptr(cu_seqlens),
                            float(scale), _ptr(o), _ptr(state_out), _ptr(workspace), ws_bytes,
                            _stream(stream)))
+    return o, state_out
+
+
+# Size of the library's fixed scratch array behind gdn_prefill_noalloc.
+PREFILL_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+
+
+def gdn_prefill_noalloc(q, k, v, a, b, A_log, dt_bias, state_in, cu_seqlens, scale: float,
+                        *, o, state_out, stream=None):
+    """gdn_prefill for callers that may not allocate device memory: the outputs are
+    caller-provided and the tensor-core path's scratch is the library's fixed
+    64 MiB array, shared by every call on the device (calls that overlap on the GPU
+    race on it).  Shapes needing more scratch raise GDN_ERR_INVALID_ARG."""
+    lib = load()
+    shape = _shape_of(q, v, cu_seqlens)
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v), ("a", a), ("b", b), ("o", o)):
+        _need_cuda(name, t, dt)
+    for name, t in (("A_log", A_log), ("dt_bias", dt_bias), ("state_out", state_out)):
+        _need_cuda(name, t, torch.float32)
+    if state_in is not None:
+        _need_cuda("state_in", state_in, torch.float32)
+    if cu_seqlens is not None:
+        _need_cuda("cu_seqlens", cu_seqlens, torch.int32)
+    st_shape = (shape.num_seqs, shape.h_v, shape.d_k, shape.d_v)
+    if tuple(o.shape) != tuple(v.shape) or tuple(state_out.shape) != st_shape:
+        raise GdnError(GDN_ERR_INVALID_ARG, f"o must be {tuple(v.shape)} and state_out {st_shape}")
+    _check(lib.gdn_prefill_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a),
+                                   _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(state_in),
+                                   _ptr(cu_seqlens), float(scale), _ptr(o), _ptr(state_out),
+                                   _stream(stream)))
     return o, state_out
 
 

@@ -1,0 +1,58 @@
+"""gdn_prefill_noalloc, the prefill entry point for callers that may not allocate
+device memory (a plugin whose host engine owns the whole memory budget, or a
+latency-bound caller that cannot take cudaMalloc's device synchronisation).
+
+Its scratch is a fixed array inside the library, shared by every call on a device
+and holding whatever the previous call left there.  The GPU test makes two calls
+in a row on the same shape with different inputs, so the second call starts from
+the first call's records, and checks each against gdn_prefill (caller-provided
+workspace) on the same inputs, within the parity tolerance of the I/O type.  The
+file is named to be collected last, and passes alone or after the other tests.
+"""
+import ctypes
+
+import pytest
+import torch
+
+import workloads
+from gpu_util import TOL, rel_err, to_device
+
+
+def test_noalloc_rejects_oversized_shapes_on_the_host():
+    from recurrent_state_scan_gb300 import gdn
+    lib = gdn.load()
+    # 1 x 8192 tokens x 16 value heads needs 128 chunks x 16 records: above 64 MiB.
+    shape = gdn.make_shape(gdn.GDN_BF16, 1, 8192, 1, 16, 16, 128, 128)
+    assert gdn.gdn_prefill_workspace_bytes(shape) > gdn.PREFILL_NOALLOC_SCRATCH_BYTES
+    st = lib.gdn_prefill_noalloc(ctypes.byref(shape), *([None] * 9), 0.0, None, None, None)
+    assert st == gdn.GDN_ERR_INVALID_ARG
+    assert b"scratch" in lib.gdn_last_error_message()
+    # The largest advertised example fits: one 4096-token sequence at 16 value heads.
+    fits = gdn.make_shape(gdn.GDN_BF16, 1, 4096, 1, 16, 16, 128, 128)
+    assert gdn.gdn_prefill_workspace_bytes(fits) <= gdn.PREFILL_NOALLOC_SCRATCH_BYTES
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_gdn_prefill_on_two_calls_in_a_row():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from recurrent_state_scan_gb300 import (gdn_last_device_status, gdn_prefill,
+                                            gdn_prefill_noalloc, load)
+    load()
+    tol = TOL["bf16"]
+    for seed in (11, 12):
+        # Three packed sequences (5, 1 and 3 chunks, two with ragged tails), GQA 2 -> 4.
+        inp = workloads.draw(workloads.small_spec(io="bf16", lengths=[300, 64, 129], h_qk=2,
+                                                  h_v=4, seed=seed, state_std=0.05))
+        d = to_device(inp)
+        args = (d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["state_in"],
+                d["cu_seqlens"], inp.scale)
+        o_ref, s_ref = gdn_prefill(*args)
+        o = torch.empty_like(o_ref)
+        s = torch.empty_like(s_ref)
+        gdn_prefill_noalloc(*args, o=o, state_out=s)
+        torch.cuda.synchronize()
+        assert gdn_last_device_status() == 0
+        eo = rel_err(o.float().cpu().numpy(), o_ref.float().cpu().numpy())
+        es = rel_err(s.cpu().numpy(), s_ref.cpu().numpy())
+        assert eo <= tol and es <= tol, f"call with seed {seed}: rel err o {eo:.2e}, state {es:.2e}"
