@@ -42,7 +42,7 @@ using namespace tc;
 constexpr int kC = 64;                 // tokens per chunk
 constexpr int kDK = 128;               // d_k = d_v of this path
 constexpr int kNV = 64;                // state columns per scan CTA
-constexpr int kPrepThreads = 256, kScanThreads = 256;
+constexpr int kPrepThreads = 256;
 constexpr uint32_t kBarPrep = 1, kBarChain = 1;
 constexpr long long kWaitBudget = 4000000000LL;   // cycles (~2 s) before a wait gives up
 constexpr int kAs = 68;                // row stride (floats) of the fp32 A / T tile
@@ -531,7 +531,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
         if (issued & 2) mbar_wait(&ctl.d1, 0, kWaitBudget);
         if (issued & 4) mbar_wait(&ctl.d23, 0, kWaitBudget);
     }
-    if (pt == 0) bulk_wait_all();
+    if (pt == 0) bulk_wait_all();    // the records have reached global memory
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -550,18 +550,40 @@ constexpr int kScanStage = SS_G + 1024;        // 65 KB
 constexpr int SS_SB = 2 * kScanStage;          // S0 in the I/O type, MN-major (d_k rows)
 constexpr int SS_DB0 = SS_SB + 16384;          // Delta, MN-major (token rows)
 constexpr int SS_DB1 = SS_DB0 + 8192;          // diag(e^{G_C - G}) Delta
-constexpr int SS_OUT = SS_DB1 + 8192;          // output tile staging
-constexpr int kScanSmem = SS_OUT + 8192 + 1024;
-constexpr uint32_t kScanTx = 2 * 8192 + 2 * 16384 + 8192 + 8192 + sizeof(GateRec);
-constexpr uint32_t TS_D4 = 0, TS_DS = 64;      // TMEM columns
+constexpr int SS_OUT = SS_DB1 + 8192;          // output tile staging, two buffers
+constexpr int kScanSmem = SS_OUT + 2 * 8192 + 1024;
+// A stage arrives in two parts with their own barriers: part B ([Q~; W], read only by
+// D4) is refilled as soon as D4 has run; part A (K, U, P, gates) once the chunk's last
+// MMA has run and every thread has read the gates.
+constexpr uint32_t kTxA = 2 * 8192 + 8192 + 8192 + sizeof(GateRec);
+constexpr uint32_t kTxB = 2 * 16384;
+constexpr uint32_t TS_D4 = 0, TS_DS = 128;     // TMEM columns: D4 at 0 / 64 by chunk parity
+constexpr int kChainThreads = 256;             // warps 0-7: Delta, state update, readout
+constexpr int kScanAllThreads = kChainThreads + 32;   // + warp 8: MMA and copy issue
+constexpr uint32_t kBarOut = 2;                // named barrier of the 128 output threads
+constexpr uint32_t kBarDelta = 3;              // the 128 Delta threads and the issue warp
+constexpr int kLptMax = 128;                   // packed batches up to this size run longest first
 
 struct ScanCtl {
-    uint64_t full[2], d4, d5;
+    uint64_t full_a[2], full_b[2], d4, ds, dout, seen, drain;
     uint32_t tmem;
+    int32_t seq;
+    int32_t cu[kLptMax + 1];
 };
 
+// Scan CTAs: one per (sequence, value head, half of the 128 state columns).  Per chunk c,
+// with the chunk's stage in shared memory and S0 (the state entering it) in registers
+// and, as the I/O type, in SB:
+//   D4(c) = [Q~; W] S0                      (issued as soon as SB holds S0)
+//   Delta = U - W S0                        warps on TMEM lanes 64-127
+//   DS = K^T diag(e^{G_C - G}) Delta        (commit ds), then D4(c)[0:64] += P Delta (commit dout)
+//   S = gamma_C S0 + DS, SB <- S            warps 0-7; then D4(c + 1) is issued at once
+//   o = D4(c)[0:64]                         warps on lanes 0-63, overlapping chunk c + 1
+// D4 alternates between two TMEM column blocks so that the readout of chunk c and the
+// product of chunk c + 1 do not share columns.  Warp 8 issues every MMA and copy, so
+// that issuing never holds up the state update.
 template <typename IO>
-__global__ void __launch_bounds__(kScanThreads, 1) gdn_chunk_scan(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __grid_constant__ TcParams p) {
     constexpr bool kBf16 = std::is_same<IO, __nv_bfloat16>::value;
     constexpr uint32_t kIdNV = idesc_f16(kBf16, 128, kNV, false, true);
     constexpr uint32_t kIdDS = idesc_f16(kBf16, 128, kNV, true, true);
@@ -571,13 +593,33 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdn_chunk_scan(const __grid_c
                                               ~static_cast<uintptr_t>(1023));
     __shared__ ScanCtl ctl;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q = warp & 3, g = warp >> 2;         // TMEM lane quarter, 32-column group
+    const bool issue_warp = (warp == 8);
+    const int q = warp & 3, g = (warp >> 2) & 1;   // TMEM lane quarter, 32-column group
     const int row = 32 * q + lane;                 // this thread's TMEM lane
+    const bool out_thread = !issue_warp && q < 2;  // lanes 0-63: output rows
     const int half = blockIdx.x & 1;
     const int h = (blockIdx.x >> 1) % p.h_v;
-    const int64_t n = (int64_t)(blockIdx.x >> 1) / p.h_v;
+    int64_t n = (int64_t)(blockIdx.x >> 1) / p.h_v;
     const int hq = h / (p.h_v / p.h_qk);
     const int v0 = half * kNV;
+
+    // Packed sequences of unequal length: CTA position n takes the n-th longest sequence
+    // (ties by index), so that the longest chains start first.
+    if (p.cu_seqlens != nullptr && p.num_seqs <= kLptMax) {
+        for (int i = tid; i <= p.num_seqs; i += kScanAllThreads) ctl.cu[i] = p.cu_seqlens[i];
+        __syncthreads();
+        for (int j = tid; j < p.num_seqs; j += kScanAllThreads) {
+            const int64_t lj = (int64_t)ctl.cu[j + 1] - ctl.cu[j];
+            int rank = 0;
+            for (int i = 0; i < p.num_seqs; ++i) {
+                const int64_t li = (int64_t)ctl.cu[i + 1] - ctl.cu[i];
+                rank += (li > lj) || (li == lj && i < j);
+            }
+            if (rank == n) ctl.seq = j;
+        }
+        __syncthreads();
+        n = ctl.seq;
+    }
 
     int64_t t0, t1;
     if (!seq_range(p.cu_seqlens, p.seqlen, p.num_seqs, p.status, n, t0, t1)) return;
@@ -586,14 +628,19 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdn_chunk_scan(const __grid_c
     const int64_t base_slot = slot_base(p, n);
 
     if (warp == 0) {
-        tmem_alloc(&ctl.tmem, 128);
+        tmem_alloc(&ctl.tmem, 256);
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&ctl.full[0], 1);
-        mbar_init(&ctl.full[1], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ctl.full_a[i], 1);
+            mbar_init(&ctl.full_b[i], 1);
+        }
         mbar_init(&ctl.d4, 1);
-        mbar_init(&ctl.d5, 1);
+        mbar_init(&ctl.ds, 1);
+        mbar_init(&ctl.dout, 1);
+        mbar_init(&ctl.seen, 4);
+        mbar_init(&ctl.drain, 1);
         fence_mbar_init();
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_o);
@@ -606,196 +653,260 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdn_chunk_scan(const __grid_c
     const uint32_t aSB = smem_u32(sm + SS_SB), aDB0 = smem_u32(sm + SS_DB0), aDB1 = smem_u32(sm + SS_DB1);
     const size_t sbase = ((size_t)n * p.h_v + h) * kDK * kDK;
     IO *go = static_cast<IO *>(p.o);
-
-    // Chunk c into stage c & 1: K by TMA, the record's [Q~; W], U half, P and gates by
-    // bulk copy.  One thread.
-    auto issue_stage = [&](int c) {
-        const int s = c & 1;
-        uint8_t *st = sm + s * kScanStage;
-        const uint8_t *rec = p.ws + (size_t)((base_slot + c) * p.h_v + h) * kRecord;
-        mbar_arrive_expect_tx(&ctl.full[s], kScanTx);
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            tma_load_3d(st + SS_KQW + r * kRegion, &p.tm_k, r * 64, hq, (int)(t0 + (int64_t)c * kC),
-                        &ctl.full[s]);
-            bulk_load(st + SS_KQW + r * kRegion + 8192, rec + REC_QW + r * 16384, 16384, &ctl.full[s]);
-        }
-        bulk_load(st + SS_U, rec + REC_U + half * 8192, 8192, &ctl.full[s]);
-        bulk_load(st + SS_P, rec + REC_P, 8192, &ctl.full[s]);
-        bulk_load(st + SS_G, rec + REC_G, sizeof(GateRec), &ctl.full[s]);
-    };
-
-    // S rows of this thread: d_k row `row`, columns v0 + 32 g + [0, 32).
-    float S[32];
-    {
-        const float4 *src = reinterpret_cast<const float4 *>(p.state_in + sbase + (size_t)row * kDK + v0 + 32 * g);
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-            const float4 f = p.state_in ? src[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
-            S[4 * q4] = f.x; S[4 * q4 + 1] = f.y; S[4 * q4 + 2] = f.z; S[4 * q4 + 3] = f.w;
-        }
-    }
-    auto write_sb = [&]() {   // S (fp32 registers) -> MN-major operand tile, row = d_k index
-#pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8)
-            *reinterpret_cast<uint4 *>(sm + SS_SB + sw128_offset(row, 4 * g + q8)) = pack8<IO>(S + 8 * q8);
-    };
-    write_sb();
-    fence_async_smem();
-    if (tid == 0) {
-        if (nchunks > 0) issue_stage(0);
-        if (nchunks > 1) issue_stage(1);
-    }
-    __syncthreads();
-
     bool failed = false;
-    int c_fail = 0;
-    uint64_t *mma_pending = nullptr;               // thread 0: an MMA group whose wait gave up
-    for (int c = 0; c < nchunks; ++c) {
-        const int s = c & 1;
-        const uint8_t *st = sm + s * kScanStage;
-        const uint32_t aSt = smem_u32(st);
-        const GateRec &gr = *reinterpret_cast<const GateRec *>(st + SS_G);
-        const int64_t tc0 = t0 + (int64_t)c * kC;
-        const int Lc = (int)((L - (int64_t)c * kC) < kC ? (L - (int64_t)c * kC) : kC);
 
-        // D4 = [Q~; W] S0 once the stage has landed.
+    if (issue_warp) {
+        // ------------------------------------------------------------ warp 8: issue
+        const bool leader = (lane == 0);
+        int issued_a = 0, issued_b = 0, landed_a = 0, landed_b = 0;
+        auto record = [&](int c) {
+            return p.ws + (size_t)((base_slot + c) * p.h_v + h) * kRecord;
+        };
+        auto load_a = [&](int c) {   // K, U half, P, gates of chunk c into stage c & 1
+            const int s = c & 1;
+            uint8_t *st = sm + s * kScanStage;
+            const uint8_t *rec = record(c);
+            mbar_arrive_expect_tx(&ctl.full_a[s], kTxA);
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+                tma_load_3d(st + SS_KQW + r * kRegion, &p.tm_k, r * 64, hq, (int)(t0 + (int64_t)c * kC),
+                            &ctl.full_a[s]);
+            bulk_load(st + SS_U, rec + REC_U + half * 8192, 8192, &ctl.full_a[s]);
+            bulk_load(st + SS_P, rec + REC_P, 8192, &ctl.full_a[s]);
+            bulk_load(st + SS_G, rec + REC_G, sizeof(GateRec), &ctl.full_a[s]);
+            issued_a = c + 1;
+        };
+        auto load_b = [&](int c) {   // [Q~; W] of chunk c into stage c & 1
+            const int s = c & 1;
+            uint8_t *st = sm + s * kScanStage;
+            const uint8_t *rec = record(c);
+            mbar_arrive_expect_tx(&ctl.full_b[s], kTxB);
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+                bulk_load(st + SS_KQW + r * kRegion + 8192, rec + REC_QW + r * 16384, 16384, &ctl.full_b[s]);
+            issued_b = c + 1;
+        };
+        auto issue_d4 = [&](int c) -> bool {   // D4(c) = [Q~; W] S0 into block c & 1
+            const int s = c & 1;
+            if (!mbar_wait(&ctl.full_b[s], (c >> 1) & 1, kWaitBudget)) return false;
+            landed_b = c + 1;
+            tc_fence_after();
+            const uint32_t aSt = smem_u32(sm + s * kScanStage);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t off = (k >> 2) * kRegion + 8192 + (k & 3) * 32;
+                mma_f16(tmem + TS_D4 + 64 * s, sw128_desc(aSt + off, 16, 1024),
+                        sw128_desc(aSB + k * 2048, 16384, 1024), kIdNV, k > 0);
+            }
+            mma_commit(&ctl.d4);
+            return true;
+        };
         bool ok = true;
-        if (tid == 0) {
-            ok = mbar_wait(&ctl.full[s], (c >> 1) & 1, kWaitBudget);
+        if (leader) {
+            for (int c = 0; c < 2 && c < nchunks; ++c) {
+                load_b(c);
+                load_a(c);
+            }
+        }
+        named_bar(kBarChain, kScanAllThreads);     // SB holds the initial state
+        if (leader && nchunks > 0) ok = issue_d4(0);
+        for (int c = 0; c < nchunks; ++c) {
+            const int s = c & 1;
+            const uint32_t aSt = smem_u32(sm + s * kScanStage);
+            const uint32_t d4col = TS_D4 + 64 * s;
+            if (leader && ok) {
+                // D4(c) has read part B of stage s: refill it with chunk c + 2.
+                ok = mbar_wait(&ctl.d4, c & 1, kWaitBudget);
+                if (ok && c + 2 < nchunks) load_b(c + 2);
+            }
+            // Delta is in DB0 / DB1.
+            ok = !bar_any(kBarDelta, 160, !ok);
+            if (leader && ok) {
+                ok = mbar_wait(&ctl.full_a[s], (c >> 1) & 1, kWaitBudget);
+                if (ok) {
+                    landed_a = c + 1;
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_f16(tmem + TS_DS, sw128_desc(aSt + k * 2048, kRegion, 1024),
+                                sw128_desc(aDB1 + k * 2048, 8192, 1024), kIdDS, k > 0);
+                    mma_commit(&ctl.ds);
+                    // The readout warps have seen the previous dout phase, so this one
+                    // cannot complete ahead of their wait.
+                    if (c > 0) ok = mbar_wait(&ctl.seen, (c - 1) & 1, kWaitBudget);
+                }
+                if (ok) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_f16(tmem + d4col, sw128_desc(aSt + SS_P + k * 32, 16, 1024),
+                                sw128_desc(aDB0 + k * 2048, 8192, 1024), kIdNV, 1u);
+                    mma_commit(&ctl.dout);
+                }
+            }
+            // SB holds the next state.
+            if (bar_any(kBarChain, kScanAllThreads, !ok)) { failed = true; break; }
+            if (leader) {
+                if (c + 1 < nchunks) ok = issue_d4(c + 1);
+                // Chunk c's last MMA has run and every thread has read its gates:
+                // refill part A of stage s with chunk c + 2.
+                if (ok) ok = mbar_wait(&ctl.dout, c & 1, kWaitBudget);
+                if (ok && c + 2 < nchunks) load_a(c + 2);
+            }
+        }
+        if (!failed) failed = bar_any(kBarChain, kScanAllThreads, !ok);
+        if (failed && leader) {
+            // Let the copies and MMAs already issued land before the CTA leaves (bounded):
+            // one commit covers every earlier MMA of this thread.
+            for (int w = landed_a; w < issued_a; ++w) mbar_wait(&ctl.full_a[w & 1], (w >> 1) & 1, kWaitBudget);
+            for (int w = landed_b; w < issued_b; ++w) mbar_wait(&ctl.full_b[w & 1], (w >> 1) & 1, kWaitBudget);
+            mma_commit(&ctl.drain);
+            mbar_wait(&ctl.drain, 0, kWaitBudget);
+        }
+    } else {
+        // ------------------------------------------------------------ warps 0-7: chain
+        // S rows of this thread: d_k row `row`, columns v0 + 32 g + [0, 32).
+        float S[32];
+        {
+            const float4 *src = reinterpret_cast<const float4 *>(p.state_in + sbase + (size_t)row * kDK + v0 + 32 * g);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+                const float4 f = p.state_in ? src[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
+                S[4 * q4] = f.x; S[4 * q4 + 1] = f.y; S[4 * q4 + 2] = f.z; S[4 * q4 + 3] = f.w;
+            }
+        }
+        auto write_sb = [&]() {   // S (fp32 registers) -> MN-major operand tile, row = d_k index
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8)
+                *reinterpret_cast<uint4 *>(sm + SS_SB + sw128_offset(row, 4 * g + q8)) = pack8<IO>(S + 8 * q8);
+        };
+        write_sb();
+        fence_async_smem();
+        named_bar(kBarChain, kScanAllThreads);
+        bool ok0 = true;                           // readout waits (output threads)
+        for (int c = 0; c < nchunks; ++c) {
+            const int s = c & 1;
+            const uint8_t *st = sm + s * kScanStage;
+            const GateRec &gr = *reinterpret_cast<const GateRec *>(st + SS_G);
+            const uint32_t d4col = TS_D4 + 64 * s;
+            const int64_t tc0 = t0 + (int64_t)c * kC;
+            const int Lc = (int)((L - (int64_t)c * kC) < kC ? (L - (int64_t)c * kC) : kC);
+
+            // Every reader of the stage observes its arrival itself.
+            bool ok = ok0 && mbar_wait(&ctl.full_a[s], (c >> 1) & 1, kWaitBudget);
+            const float gC = gr.gC;
+
+            if (!out_thread) {
+                // Delta = U - W S0 on lanes 64-127 (token rows), this thread's 32 columns.
+                ok = ok && mbar_wait(&ctl.d4, c & 1, kWaitBudget);
+                if (ok) {
+                    tc_fence_after();
+                    const int j = row - 64;
+                    uint32_t ws[32];
+                    tmem_ld32(tmem + lane_base + d4col + 32 * g, ws);
+                    float uf[32];
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        const uint4 u = *reinterpret_cast<const uint4 *>(st + SS_U + sw128_offset(j, 4 * g + q8));
+                        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int k2 = 0; k2 < 4; ++k2) {
+                            const float2 t2 = Pack<IO>::unpack(w[k2]);
+                            uf[8 * q8 + 2 * k2] = t2.x;
+                            uf[8 * q8 + 2 * k2 + 1] = t2.y;
+                        }
+                    }
+                    tmem_ld_wait();
+                    const float kfj = gr.kf[j];
+                    float x[32], y[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        x[e] = uf[e] - __uint_as_float(ws[e]);
+                        y[e] = kfj * x[e];
+                    }
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        const uint32_t off = sw128_offset(j, 4 * g + q8);
+                        *reinterpret_cast<uint4 *>(sm + SS_DB0 + off) = pack8<IO>(x + 8 * q8);
+                        *reinterpret_cast<uint4 *>(sm + SS_DB1 + off) = pack8<IO>(y + 8 * q8);
+                    }
+                }
+                fence_async_smem();
+                tc_fence_before();
+                ok = !bar_any(kBarDelta, 160, !ok);
+            }
+
+            // S = gamma_C S0 + DS (fp32 registers), then the next chunk's operand tile.
+            ok = ok && mbar_wait(&ctl.ds, c & 1, kWaitBudget);
             if (ok) {
                 tc_fence_after();
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + TS_DS + 32 * g, r);
+                tmem_ld_wait();
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t off = (k >> 2) * kRegion + 8192 + (k & 3) * 32;
-                    mma_f16(tmem + TS_D4, sw128_desc(aSt + off, 16, 1024),
-                            sw128_desc(aSB + k * 2048, 16384, 1024), kIdNV, k > 0);
+                for (int e = 0; e < 32; ++e) S[e] = fmaf(gC, S[e], __uint_as_float(r[e]));
+                write_sb();
+            }
+            // The output buffer of this chunk was last stored from two chunks ago.
+            if (tid == 0) bulk_wait_read_1();
+            fence_async_smem();
+            tc_fence_before();
+            if (bar_any(kBarChain, kScanAllThreads, !ok)) { failed = true; break; }
+
+            // o_i = (Q~ S0 + P Delta)_i on lanes 0-63, while chunk c + 1 runs.  A full
+            // chunk goes out as one TMA store of the staged 64 x 64 tile; a sequence's
+            // ragged last chunk is stored row by row so that no row of the next sequence
+            // is touched.
+            if (out_thread) {
+                const bool tile_store = (Lc == kC);
+                uint8_t *ob = sm + SS_OUT + s * 8192;
+                bool ok_out = mbar_wait(&ctl.dout, c & 1, kWaitBudget);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl.seen);
+                if (ok_out) {
+                    tc_fence_after();
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_base + d4col + 32 * g, r);
+                    tmem_ld_wait();
+                    float x[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
+                    if (tile_store) {
+#pragma unroll
+                        for (int q8 = 0; q8 < 4; ++q8)
+                            *reinterpret_cast<uint4 *>(ob + sw128_offset(row, 4 * g + q8)) = pack8<IO>(x + 8 * q8);
+                    } else if (row < Lc) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(go + ((size_t)(tc0 + row) * p.h_v + h) * kDK + v0 + 32 * g);
+#pragma unroll
+                        for (int q8 = 0; q8 < 4; ++q8) dst[q8] = pack8<IO>(x + 8 * q8);
+                    }
                 }
-                mma_commit(&ctl.d4);
-                ok = mbar_wait(&ctl.d4, c & 1, kWaitBudget);
-                if (!ok) mma_pending = &ctl.d4;
-            }
-        }
-        if (bar_any(kBarChain, kScanThreads, !ok)) { failed = true; c_fail = c; break; }
-        tc_fence_after();
-        const float gC = gr.gC;   // read before the stage is refilled below
-
-        // Delta = U - W S0 on lanes 64-127 (token rows), this thread's 32 columns.
-        if (q >= 2) {
-            const int j = row - 64;
-            uint32_t ws[32];
-            tmem_ld32(tmem + lane_base + TS_D4 + 32 * g, ws);
-            float uf[32];
-#pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {
-                const uint4 u = *reinterpret_cast<const uint4 *>(st + SS_U + sw128_offset(j, 4 * g + q8));
-                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                for (int k2 = 0; k2 < 4; ++k2) {
-                    const float2 t2 = Pack<IO>::unpack(w[k2]);
-                    uf[8 * q8 + 2 * k2] = t2.x;
-                    uf[8 * q8 + 2 * k2 + 1] = t2.y;
+                fence_async_smem();
+                tc_fence_before();
+                ok_out = !bar_any(kBarOut, 128, !ok_out);
+                if (tid == 0 && ok_out && tile_store) {
+                    tma_store_3d(&p.tm_o, ob, v0, h, (int)tc0);
+                    bulk_commit();
                 }
-            }
-            tmem_ld_wait();
-            const float kfj = gr.kf[j];
-            float x[32], y[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                x[e] = uf[e] - __uint_as_float(ws[e]);
-                y[e] = kfj * x[e];
-            }
-#pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {
-                const uint32_t off = sw128_offset(j, 4 * g + q8);
-                *reinterpret_cast<uint4 *>(sm + SS_DB0 + off) = pack8<IO>(x + 8 * q8);
-                *reinterpret_cast<uint4 *>(sm + SS_DB1 + off) = pack8<IO>(y + 8 * q8);
+                ok0 = ok0 && ok_out;
             }
         }
-        fence_async_smem();
-        tc_fence_before();
-        named_bar(kBarChain, kScanThreads);
-
-        // DS = K^T diag(e^{G_C - G}) Delta;  D4[0:64] += P Delta (the A rows past P land
-        // in the spent W S0 lanes).
-        if (tid == 0) {
-            tc_fence_after();
+        // A readout wait of the last chunk that gave up is seen here.
+        if (!failed) failed = bar_any(kBarChain, kScanAllThreads, !ok0);
+        if (tid == 0) bulk_wait_all();    // the output tiles have reached global memory
+        if (failed) {
+            if (tid == 0) atomicOr(p.status, kDevTimeout);
+        } else {
+            float4 *dst = reinterpret_cast<float4 *>(p.state_out + sbase + (size_t)row * kDK + v0 + 32 * g);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_f16(tmem + TS_DS, sw128_desc(aSt + k * 2048, kRegion, 1024),
-                        sw128_desc(aDB1 + k * 2048, 8192, 1024), kIdDS, k > 0);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_f16(tmem + TS_D4, sw128_desc(aSt + SS_P + k * 32, 16, 1024),
-                        sw128_desc(aDB0 + k * 2048, 8192, 1024), kIdNV, 1u);
-            mma_commit(&ctl.d5);
-            ok = mbar_wait(&ctl.d5, c & 1, kWaitBudget);
-            if (!ok) mma_pending = &ctl.d5;
-            // The stage's last readers are done: refill it with chunk c + 2.
-            if (ok && c + 2 < nchunks) issue_stage(c + 2);
-            bulk_wait_read();   // the previous output tile has been read
+            for (int q4 = 0; q4 < 8; ++q4)
+                dst[q4] = make_float4(S[4 * q4], S[4 * q4 + 1], S[4 * q4 + 2], S[4 * q4 + 3]);
         }
-        if (bar_any(kBarChain, kScanThreads, !ok)) { failed = true; c_fail = c; break; }
-        tc_fence_after();
-
-        // S = gamma_C S0 + DS (fp32 registers), then the next chunk's operand tile.
-        {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_base + TS_DS + 32 * g, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) S[e] = fmaf(gC, S[e], __uint_as_float(r[e]));
-            write_sb();
-        }
-        // o_i = (Q~ S0 + P Delta)_i on lanes 0-63.  A full chunk goes out as one TMA
-        // store of the staged 64 x 64 tile; a sequence's ragged last chunk is stored row
-        // by row so that no row of the next sequence is touched.
-        const bool tile_store = (Lc == kC);
-        if (q < 2) {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_base + TS_D4 + 32 * g, r);
-            tmem_ld_wait();
-            float x[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
-            if (tile_store) {
-#pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8)
-                    *reinterpret_cast<uint4 *>(sm + SS_OUT + sw128_offset(row, 4 * g + q8)) = pack8<IO>(x + 8 * q8);
-            } else if (row < Lc) {
-                uint4 *dst = reinterpret_cast<uint4 *>(go + ((size_t)(tc0 + row) * p.h_v + h) * kDK + v0 + 32 * g);
-#pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) dst[q8] = pack8<IO>(x + 8 * q8);
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        named_bar(kBarChain, kScanThreads);
-        if (tid == 0 && tile_store) {
-            tma_store_3d(&p.tm_o, sm + SS_OUT, v0, h, (int)tc0);
-            bulk_commit();
-        }
-    }
-    if (failed && tid == 0) {
-        // Let the stage copies (chunks c_fail and c_fail + 1) and an MMA group already
-        // issued land before the CTA leaves (bounded).
-        atomicOr(p.status, kDevTimeout);
-        for (int w = c_fail; w < nchunks && w < c_fail + 2; ++w)
-            mbar_wait(&ctl.full[w & 1], (w >> 1) & 1, kWaitBudget);
-        if (mma_pending != nullptr) mbar_wait(mma_pending, c_fail & 1, kWaitBudget);
-    }
-    if (tid == 0) bulk_wait_all();   // the output tiles have reached global memory
-    if (!failed) {
-        float4 *dst = reinterpret_cast<float4 *>(p.state_out + sbase + (size_t)row * kDK + v0 + 32 * g);
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4)
-            dst[q4] = make_float4(S[4 * q4], S[4 * q4 + 1], S[4 * q4 + 2], S[4 * q4 + 3]);
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 128);
+        tmem_dealloc(tmem, 256);
     }
 }
 
@@ -865,7 +976,7 @@ cudaError_t launch_typed(const TcParams &tp, int64_t n_slots, cudaStream_t strea
     gdn_chunk_prep<IO><<<(unsigned)prep_blocks, kPrepThreads, kPrepSmem, stream>>>(tp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    gdn_chunk_scan<IO><<<(unsigned)scan_blocks, kScanThreads, kScanSmem, stream>>>(tp);
+    gdn_chunk_scan<IO><<<(unsigned)scan_blocks, kScanAllThreads, kScanSmem, stream>>>(tp);
     return cudaGetLastError();
 }
 
