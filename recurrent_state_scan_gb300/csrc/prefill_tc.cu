@@ -558,30 +558,49 @@ constexpr int kScanSmem = SS_OUT + 2 * 8192 + 1024;
 constexpr uint32_t kTxA = 2 * 8192 + 8192 + 8192 + sizeof(GateRec);
 constexpr uint32_t kTxB = 2 * 16384;
 constexpr uint32_t TS_D4 = 0, TS_DS = 128;     // TMEM columns: D4 at 0 / 64 by chunk parity
-constexpr int kChainThreads = 256;             // warps 0-7: Delta, state update, readout
-constexpr int kScanAllThreads = kChainThreads + 32;   // + warp 8: MMA and copy issue
-constexpr uint32_t kBarOut = 2;                // named barrier of the 128 output threads
-constexpr uint32_t kBarDelta = 3;              // the 128 Delta threads and the issue warp
+constexpr int kChainWarps = 8;                 // Delta, state update, readout
+constexpr int kScanAllThreads = 32 * kChainWarps + 32;   // + one warp that issues MMAs and copies
+constexpr uint32_t kBarOut = 2;                // named barrier of the 128 readout threads
 constexpr int kLptMax = 128;                   // packed batches up to this size run longest first
 
 struct ScanCtl {
-    uint64_t full_a[2], full_b[2], d4, ds, dout, seen, drain;
+    uint64_t full_a[2], full_b[2];             // stage parts landed
+    uint64_t d4, ds, dout;                     // MMA groups done (tcgen05.commit)
+    uint64_t delta_ready, sb_ready, out_done;  // chain warps -> issuing warp
+    uint64_t drain;
     uint32_t tmem;
+    int32_t abort;                             // a wait gave up: everyone leaves
     int32_t seq;
     int32_t cu[kLptMax + 1];
 };
 
+// Bounded wait that also gives up as soon as another thread has given up.  Waiting
+// threads sleep in the barrier rather than poll.
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int32_t *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitBudget) {
+            *abort = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
 // Scan CTAs: one per (sequence, value head, half of the 128 state columns).  Per chunk c,
 // with the chunk's stage in shared memory and S0 (the state entering it) in registers
 // and, as the I/O type, in SB:
-//   D4(c) = [Q~; W] S0                      (issued as soon as SB holds S0)
+//   D4(c) = [Q~; W] S0                      issued as soon as SB holds S0
 //   Delta = U - W S0                        warps on TMEM lanes 64-127
 //   DS = K^T diag(e^{G_C - G}) Delta        (commit ds), then D4(c)[0:64] += P Delta (commit dout)
-//   S = gamma_C S0 + DS, SB <- S            warps 0-7; then D4(c + 1) is issued at once
+//   S = gamma_C S0 + DS, SB <- S            all chain warps; D4(c + 1) is issued at once
 //   o = D4(c)[0:64]                         warps on lanes 0-63, overlapping chunk c + 1
 // D4 alternates between two TMEM column blocks so that the readout of chunk c and the
-// product of chunk c + 1 do not share columns.  Warp 8 issues every MMA and copy, so
-// that issuing never holds up the state update.
+// product of chunk c + 1 do not share columns.  One warp issues every MMA and copy; the
+// chain warps never wait for it at a barrier, only on the barriers of the work they
+// consume, and it learns of their progress through arrival counts.
 template <typename IO>
 __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __grid_constant__ TcParams p) {
     constexpr bool kBf16 = std::is_same<IO, __nv_bfloat16>::value;
@@ -592,11 +611,9 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
     __shared__ ScanCtl ctl;
+    volatile int32_t *abort = &ctl.abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool issue_warp = (warp == 8);
-    const int q = warp & 3, g = (warp >> 2) & 1;   // TMEM lane quarter, 32-column group
-    const int row = 32 * q + lane;                 // this thread's TMEM lane
-    const bool out_thread = !issue_warp && q < 2;  // lanes 0-63: output rows
+    const bool issue_warp = (warp == kChainWarps);
     const int half = blockIdx.x & 1;
     const int h = (blockIdx.x >> 1) % p.h_v;
     int64_t n = (int64_t)(blockIdx.x >> 1) / p.h_v;
@@ -639,8 +656,11 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
         mbar_init(&ctl.d4, 1);
         mbar_init(&ctl.ds, 1);
         mbar_init(&ctl.dout, 1);
-        mbar_init(&ctl.seen, 4);
+        mbar_init(&ctl.delta_ready, kChainWarps / 2);
+        mbar_init(&ctl.sb_ready, kChainWarps);
+        mbar_init(&ctl.out_done, kChainWarps / 2);
         mbar_init(&ctl.drain, 1);
+        ctl.abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_o);
@@ -649,123 +669,119 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl.tmem;
-    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    const uint32_t aSB = smem_u32(sm + SS_SB), aDB0 = smem_u32(sm + SS_DB0), aDB1 = smem_u32(sm + SS_DB1);
     const size_t sbase = ((size_t)n * p.h_v + h) * kDK * kDK;
-    IO *go = static_cast<IO *>(p.o);
-    bool failed = false;
 
     if (issue_warp) {
-        // ------------------------------------------------------------ warp 8: issue
-        const bool leader = (lane == 0);
-        int issued_a = 0, issued_b = 0, landed_a = 0, landed_b = 0;
-        auto record = [&](int c) {
-            return p.ws + (size_t)((base_slot + c) * p.h_v + h) * kRecord;
-        };
-        auto load_a = [&](int c) {   // K, U half, P, gates of chunk c into stage c & 1
-            const int s = c & 1;
-            uint8_t *st = sm + s * kScanStage;
-            const uint8_t *rec = record(c);
-            mbar_arrive_expect_tx(&ctl.full_a[s], kTxA);
+        // ------------------------------------------------------------ MMA and copy issue
+        if (lane == 0) {
+            const uint32_t aSB = smem_u32(sm + SS_SB), aDB0 = smem_u32(sm + SS_DB0),
+                           aDB1 = smem_u32(sm + SS_DB1);
+            int issued_a = 0, issued_b = 0, landed_a = 0, landed_b = 0;
+            auto record = [&](int c) {
+                return p.ws + (size_t)((base_slot + c) * p.h_v + h) * kRecord;
+            };
+            auto load_a = [&](int c) {   // K, U half, P and gates of chunk c into stage c & 1
+                const int s = c & 1;
+                uint8_t *st = sm + s * kScanStage;
+                const uint8_t *rec = record(c);
+                mbar_arrive_expect_tx(&ctl.full_a[s], kTxA);
 #pragma unroll
-            for (int r = 0; r < 2; ++r)
-                tma_load_3d(st + SS_KQW + r * kRegion, &p.tm_k, r * 64, hq, (int)(t0 + (int64_t)c * kC),
-                            &ctl.full_a[s]);
-            bulk_load(st + SS_U, rec + REC_U + half * 8192, 8192, &ctl.full_a[s]);
-            bulk_load(st + SS_P, rec + REC_P, 8192, &ctl.full_a[s]);
-            bulk_load(st + SS_G, rec + REC_G, sizeof(GateRec), &ctl.full_a[s]);
-            issued_a = c + 1;
-        };
-        auto load_b = [&](int c) {   // [Q~; W] of chunk c into stage c & 1
-            const int s = c & 1;
-            uint8_t *st = sm + s * kScanStage;
-            const uint8_t *rec = record(c);
-            mbar_arrive_expect_tx(&ctl.full_b[s], kTxB);
+                for (int r = 0; r < 2; ++r)
+                    tma_load_3d(st + SS_KQW + r * kRegion, &p.tm_k, r * 64, hq,
+                                (int)(t0 + (int64_t)c * kC), &ctl.full_a[s]);
+                bulk_load(st + SS_U, rec + REC_U + half * 8192, 8192, &ctl.full_a[s]);
+                bulk_load(st + SS_P, rec + REC_P, 8192, &ctl.full_a[s]);
+                bulk_load(st + SS_G, rec + REC_G, sizeof(GateRec), &ctl.full_a[s]);
+                issued_a = c + 1;
+            };
+            auto load_b = [&](int c) {   // [Q~; W] of chunk c into stage c & 1
+                const int s = c & 1;
+                uint8_t *st = sm + s * kScanStage;
+                const uint8_t *rec = record(c);
+                mbar_arrive_expect_tx(&ctl.full_b[s], kTxB);
 #pragma unroll
-            for (int r = 0; r < 2; ++r)
-                bulk_load(st + SS_KQW + r * kRegion + 8192, rec + REC_QW + r * 16384, 16384, &ctl.full_b[s]);
-            issued_b = c + 1;
-        };
-        auto issue_d4 = [&](int c) -> bool {   // D4(c) = [Q~; W] S0 into block c & 1
-            const int s = c & 1;
-            if (!mbar_wait(&ctl.full_b[s], (c >> 1) & 1, kWaitBudget)) return false;
-            landed_b = c + 1;
-            tc_fence_after();
-            const uint32_t aSt = smem_u32(sm + s * kScanStage);
+                for (int r = 0; r < 2; ++r)
+                    bulk_load(st + SS_KQW + r * kRegion + 8192, rec + REC_QW + r * 16384, 16384, &ctl.full_b[s]);
+                issued_b = c + 1;
+            };
+            // D4(c) = [Q~; W] S0 into block c & 1, once SB holds S0 and part B has landed.
+            auto issue_d4 = [&](int c) -> bool {
+                const int s = c & 1;
+                if (!wait_or_abort(&ctl.sb_ready, c & 1, abort)) return false;
+                if (!wait_or_abort(&ctl.full_b[s], (c >> 1) & 1, abort)) return false;
+                landed_b = c + 1;
+                tc_fence_after();
+                const uint32_t aSt = smem_u32(sm + s * kScanStage);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t off = (k >> 2) * kRegion + 8192 + (k & 3) * 32;
-                mma_f16(tmem + TS_D4 + 64 * s, sw128_desc(aSt + off, 16, 1024),
-                        sw128_desc(aSB + k * 2048, 16384, 1024), kIdNV, k > 0);
-            }
-            mma_commit(&ctl.d4);
-            return true;
-        };
-        bool ok = true;
-        if (leader) {
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t off = (k >> 2) * kRegion + 8192 + (k & 3) * 32;
+                    mma_f16(tmem + TS_D4 + 64 * s, sw128_desc(aSt + off, 16, 1024),
+                            sw128_desc(aSB + k * 2048, 16384, 1024), kIdNV, k > 0);
+                }
+                mma_commit(&ctl.d4);
+                return true;
+            };
+            bool ok = true;
             for (int c = 0; c < 2 && c < nchunks; ++c) {
                 load_b(c);
                 load_a(c);
             }
-        }
-        named_bar(kBarChain, kScanAllThreads);     // SB holds the initial state
-        if (leader && nchunks > 0) ok = issue_d4(0);
-        for (int c = 0; c < nchunks; ++c) {
-            const int s = c & 1;
-            const uint32_t aSt = smem_u32(sm + s * kScanStage);
-            const uint32_t d4col = TS_D4 + 64 * s;
-            if (leader && ok) {
+            if (nchunks > 0) ok = issue_d4(0);
+            for (int c = 0; ok && c < nchunks; ++c) {
+                const int s = c & 1;
+                const uint32_t aSt = smem_u32(sm + s * kScanStage);
                 // D4(c) has read part B of stage s: refill it with chunk c + 2.
-                ok = mbar_wait(&ctl.d4, c & 1, kWaitBudget);
-                if (ok && c + 2 < nchunks) load_b(c + 2);
-            }
-            // Delta is in DB0 / DB1.
-            ok = !bar_any(kBarDelta, 160, !ok);
-            if (leader && ok) {
-                ok = mbar_wait(&ctl.full_a[s], (c >> 1) & 1, kWaitBudget);
-                if (ok) {
-                    landed_a = c + 1;
-                    tc_fence_after();
+                ok = wait_or_abort(&ctl.d4, c & 1, abort);
+                if (!ok) break;
+                if (c + 2 < nchunks) load_b(c + 2);
+                // DS = K^T diag(e^{G_C - G}) Delta once Delta is in DB0 / DB1.
+                ok = wait_or_abort(&ctl.delta_ready, c & 1, abort) &&
+                     wait_or_abort(&ctl.full_a[s], (c >> 1) & 1, abort);
+                if (!ok) break;
+                landed_a = c + 1;
+                tc_fence_after();
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_f16(tmem + TS_DS, sw128_desc(aSt + k * 2048, kRegion, 1024),
-                                sw128_desc(aDB1 + k * 2048, 8192, 1024), kIdDS, k > 0);
-                    mma_commit(&ctl.ds);
-                    // The readout warps have seen the previous dout phase, so this one
-                    // cannot complete ahead of their wait.
-                    if (c > 0) ok = mbar_wait(&ctl.seen, (c - 1) & 1, kWaitBudget);
-                }
-                if (ok) {
+                for (int k = 0; k < 4; ++k)
+                    mma_f16(tmem + TS_DS, sw128_desc(aSt + k * 2048, kRegion, 1024),
+                            sw128_desc(aDB1 + k * 2048, 8192, 1024), kIdDS, k > 0);
+                mma_commit(&ctl.ds);
+                // D4(c)[0:64] += P Delta (the A rows past P land in the spent W S0 lanes).
+                // The readout of chunk c - 1 is done, so the readout warps have seen the
+                // previous dout phase and block (c + 1) & 1 is free for D4(c + 1).
+                if (c > 0 && !(ok = wait_or_abort(&ctl.out_done, (c - 1) & 1, abort))) break;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_f16(tmem + d4col, sw128_desc(aSt + SS_P + k * 32, 16, 1024),
-                                sw128_desc(aDB0 + k * 2048, 8192, 1024), kIdNV, 1u);
-                    mma_commit(&ctl.dout);
+                for (int k = 0; k < 4; ++k)
+                    mma_f16(tmem + TS_D4 + 64 * s, sw128_desc(aSt + SS_P + k * 32, 16, 1024),
+                            sw128_desc(aDB0 + k * 2048, 8192, 1024), kIdNV, 1u);
+                mma_commit(&ctl.dout);
+                if (c + 1 < nchunks && !(ok = issue_d4(c + 1))) break;
+                // Chunk c's last MMA has run and every thread has read its gates (they
+                // arrived on sb_ready after that): refill part A of stage s.
+                if (c + 2 < nchunks) {
+                    ok = wait_or_abort(&ctl.dout, c & 1, abort);
+                    if (!ok) break;
+                    load_a(c + 2);
                 }
             }
-            // SB holds the next state.
-            if (bar_any(kBarChain, kScanAllThreads, !ok)) { failed = true; break; }
-            if (leader) {
-                if (c + 1 < nchunks) ok = issue_d4(c + 1);
-                // Chunk c's last MMA has run and every thread has read its gates:
-                // refill part A of stage s with chunk c + 2.
-                if (ok) ok = mbar_wait(&ctl.dout, c & 1, kWaitBudget);
-                if (ok && c + 2 < nchunks) load_a(c + 2);
+            if (!ok) {
+                // Let the copies and MMAs already issued land before the CTA leaves
+                // (bounded): one commit covers every earlier MMA of this thread.
+                *abort = 1;
+                for (int w = landed_a; w < issued_a; ++w) mbar_wait(&ctl.full_a[w & 1], (w >> 1) & 1, kWaitBudget);
+                for (int w = landed_b; w < issued_b; ++w) mbar_wait(&ctl.full_b[w & 1], (w >> 1) & 1, kWaitBudget);
+                mma_commit(&ctl.drain);
+                mbar_wait(&ctl.drain, 0, kWaitBudget);
             }
         }
-        if (!failed) failed = bar_any(kBarChain, kScanAllThreads, !ok);
-        if (failed && leader) {
-            // Let the copies and MMAs already issued land before the CTA leaves (bounded):
-            // one commit covers every earlier MMA of this thread.
-            for (int w = landed_a; w < issued_a; ++w) mbar_wait(&ctl.full_a[w & 1], (w >> 1) & 1, kWaitBudget);
-            for (int w = landed_b; w < issued_b; ++w) mbar_wait(&ctl.full_b[w & 1], (w >> 1) & 1, kWaitBudget);
-            mma_commit(&ctl.drain);
-            mbar_wait(&ctl.drain, 0, kWaitBudget);
-        }
+        __syncwarp();
     } else {
-        // ------------------------------------------------------------ warps 0-7: chain
-        // S rows of this thread: d_k row `row`, columns v0 + 32 g + [0, 32).
-        float S[32];
+        // ------------------------------------------------------------ chain warps
+        const int q = warp & 3, g = warp >> 2;     // TMEM lane quarter, 32-column group
+        const int row = 32 * q + lane;             // this thread's TMEM lane
+        const bool out_warp = q < 2;               // lanes 0-63: output rows
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        IO *go = static_cast<IO *>(p.o);
+        float S[32];                               // S[row][v0 + 32 g + e]
         {
             const float4 *src = reinterpret_cast<const float4 *>(p.state_in + sbase + (size_t)row * kDK + v0 + 32 * g);
 #pragma unroll
@@ -774,136 +790,153 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                 S[4 * q4] = f.x; S[4 * q4 + 1] = f.y; S[4 * q4 + 2] = f.z; S[4 * q4 + 3] = f.w;
             }
         }
-        auto write_sb = [&]() {   // S (fp32 registers) -> MN-major operand tile, row = d_k index
+        // S (fp32 registers) -> MN-major operand tile (rows = d_k), then tell the issuer.
+        auto publish_sb = [&](bool write) {
+            if (write) {
 #pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8)
-                *reinterpret_cast<uint4 *>(sm + SS_SB + sw128_offset(row, 4 * g + q8)) = pack8<IO>(S + 8 * q8);
+                for (int q8 = 0; q8 < 4; ++q8)
+                    *reinterpret_cast<uint4 *>(sm + SS_SB + sw128_offset(row, 4 * g + q8)) = pack8<IO>(S + 8 * q8);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl.sb_ready);
         };
-        write_sb();
-        fence_async_smem();
-        named_bar(kBarChain, kScanAllThreads);
-        bool ok0 = true;                           // readout waits (output threads)
+        publish_sb(true);
+        bool ok = true;
         for (int c = 0; c < nchunks; ++c) {
             const int s = c & 1;
             const uint8_t *st = sm + s * kScanStage;
             const GateRec &gr = *reinterpret_cast<const GateRec *>(st + SS_G);
             const uint32_t d4col = TS_D4 + 64 * s;
-            const int64_t tc0 = t0 + (int64_t)c * kC;
-            const int Lc = (int)((L - (int64_t)c * kC) < kC ? (L - (int64_t)c * kC) : kC);
-
             // Every reader of the stage observes its arrival itself.
-            bool ok = ok0 && mbar_wait(&ctl.full_a[s], (c >> 1) & 1, kWaitBudget);
-            const float gC = gr.gC;
+            ok = ok && wait_or_abort(&ctl.full_a[s], (c >> 1) & 1, abort);
+            const float gC = ok ? gr.gC : 0.f;
 
-            if (!out_thread) {
+            if (!out_warp) {
                 // Delta = U - W S0 on lanes 64-127 (token rows), this thread's 32 columns.
-                ok = ok && mbar_wait(&ctl.d4, c & 1, kWaitBudget);
+                ok = ok && wait_or_abort(&ctl.d4, c & 1, abort);
                 if (ok) {
                     tc_fence_after();
                     const int j = row - 64;
-                    uint32_t ws[32];
-                    tmem_ld32(tmem + lane_base + d4col + 32 * g, ws);
-                    float uf[32];
-#pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8) {
-                        const uint4 u = *reinterpret_cast<const uint4 *>(st + SS_U + sw128_offset(j, 4 * g + q8));
-                        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                        for (int k2 = 0; k2 < 4; ++k2) {
-                            const float2 t2 = Pack<IO>::unpack(w[k2]);
-                            uf[8 * q8 + 2 * k2] = t2.x;
-                            uf[8 * q8 + 2 * k2 + 1] = t2.y;
-                        }
-                    }
-                    tmem_ld_wait();
                     const float kfj = gr.kf[j];
-                    float x[32], y[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        x[e] = uf[e] - __uint_as_float(ws[e]);
-                        y[e] = kfj * x[e];
-                    }
+                    for (int ps = 0; ps < 2; ++ps) {
+                        uint32_t ws[16];
+                        tmem_ld16(tmem + lane_base + d4col + 32 * g + 16 * ps, ws);
+                        float x[16];
 #pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8) {
-                        const uint32_t off = sw128_offset(j, 4 * g + q8);
-                        *reinterpret_cast<uint4 *>(sm + SS_DB0 + off) = pack8<IO>(x + 8 * q8);
-                        *reinterpret_cast<uint4 *>(sm + SS_DB1 + off) = pack8<IO>(y + 8 * q8);
+                        for (int q8 = 0; q8 < 2; ++q8) {
+                            const uint4 u = *reinterpret_cast<const uint4 *>(
+                                st + SS_U + sw128_offset(j, 4 * g + 2 * ps + q8));
+                            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                            for (int k2 = 0; k2 < 4; ++k2) {
+                                const float2 t2 = Pack<IO>::unpack(w[k2]);
+                                x[8 * q8 + 2 * k2] = t2.x;
+                                x[8 * q8 + 2 * k2 + 1] = t2.y;
+                            }
+                        }
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) x[e] -= __uint_as_float(ws[e]);
+#pragma unroll
+                        for (int q8 = 0; q8 < 2; ++q8)
+                            *reinterpret_cast<uint4 *>(sm + SS_DB0 + sw128_offset(j, 4 * g + 2 * ps + q8)) =
+                                pack8<IO>(x + 8 * q8);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) x[e] *= kfj;
+#pragma unroll
+                        for (int q8 = 0; q8 < 2; ++q8)
+                            *reinterpret_cast<uint4 *>(sm + SS_DB1 + sw128_offset(j, 4 * g + 2 * ps + q8)) =
+                                pack8<IO>(x + 8 * q8);
                     }
                 }
                 fence_async_smem();
                 tc_fence_before();
-                ok = !bar_any(kBarDelta, 160, !ok);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl.delta_ready);
             }
 
             // S = gamma_C S0 + DS (fp32 registers), then the next chunk's operand tile.
-            ok = ok && mbar_wait(&ctl.ds, c & 1, kWaitBudget);
+            ok = ok && wait_or_abort(&ctl.ds, c & 1, abort);
             if (ok) {
                 tc_fence_after();
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_base + TS_DS + 32 * g, r);
-                tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) S[e] = fmaf(gC, S[e], __uint_as_float(r[e]));
-                write_sb();
+                for (int ps = 0; ps < 2; ++ps) {
+                    uint32_t r[16];
+                    tmem_ld16(tmem + lane_base + TS_DS + 32 * g + 16 * ps, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) S[16 * ps + e] = fmaf(gC, S[16 * ps + e], __uint_as_float(r[e]));
+                }
             }
-            // The output buffer of this chunk was last stored from two chunks ago.
-            if (tid == 0) bulk_wait_read_1();
-            fence_async_smem();
-            tc_fence_before();
-            if (bar_any(kBarChain, kScanAllThreads, !ok)) { failed = true; break; }
+            publish_sb(ok);
+            if (!out_warp) {
+                if (!ok) break;
+                continue;
+            }
 
             // o_i = (Q~ S0 + P Delta)_i on lanes 0-63, while chunk c + 1 runs.  A full
             // chunk goes out as one TMA store of the staged 64 x 64 tile; a sequence's
             // ragged last chunk is stored row by row so that no row of the next sequence
-            // is touched.
-            if (out_thread) {
-                const bool tile_store = (Lc == kC);
-                uint8_t *ob = sm + SS_OUT + s * 8192;
-                bool ok_out = mbar_wait(&ctl.dout, c & 1, kWaitBudget);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl.seen);
-                if (ok_out) {
-                    tc_fence_after();
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lane_base + d4col + 32 * g, r);
+            // is touched.  The readout warps leave the loop together, at their barrier.
+            const int Lc = (int)((L - (int64_t)c * kC) < kC ? (L - (int64_t)c * kC) : kC);
+            const bool tile_store = (Lc == kC);
+            uint8_t *ob = sm + SS_OUT + s * 8192;
+            ok = ok && wait_or_abort(&ctl.dout, c & 1, abort);
+            if (ok) {
+                tc_fence_after();
+                uint4 packed[4];
+#pragma unroll
+                for (int ps = 0; ps < 2; ++ps) {
+                    uint32_t r[16];
+                    tmem_ld16(tmem + lane_base + d4col + 32 * g + 16 * ps, r);
                     tmem_ld_wait();
-                    float x[32];
+                    float x[16];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
-                    if (tile_store) {
-#pragma unroll
-                        for (int q8 = 0; q8 < 4; ++q8)
-                            *reinterpret_cast<uint4 *>(ob + sw128_offset(row, 4 * g + q8)) = pack8<IO>(x + 8 * q8);
-                    } else if (row < Lc) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(go + ((size_t)(tc0 + row) * p.h_v + h) * kDK + v0 + 32 * g);
-#pragma unroll
-                        for (int q8 = 0; q8 < 4; ++q8) dst[q8] = pack8<IO>(x + 8 * q8);
-                    }
+                    for (int e = 0; e < 16; ++e) x[e] = __uint_as_float(r[e]);
+                    packed[2 * ps] = pack8<IO>(x);
+                    packed[2 * ps + 1] = pack8<IO>(x + 8);
                 }
-                fence_async_smem();
                 tc_fence_before();
-                ok_out = !bar_any(kBarOut, 128, !ok_out);
-                if (tid == 0 && ok_out && tile_store) {
-                    tma_store_3d(&p.tm_o, ob, v0, h, (int)tc0);
-                    bulk_commit();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl.out_done);
+                if (tile_store) {
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8)
+                        *reinterpret_cast<uint4 *>(ob + sw128_offset(row, 4 * g + q8)) = packed[q8];
+                } else if (row < Lc) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(
+                        go + ((size_t)(t0 + (int64_t)c * kC + row) * p.h_v + h) * kDK + v0 + 32 * g);
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8) dst[q8] = packed[q8];
                 }
-                ok0 = ok0 && ok_out;
+            }
+            fence_async_smem();
+            if (tid == 0) bulk_wait_read();    // the previous tile store has read its buffer
+            if (bar_any(kBarOut, 128, !ok)) {
+                ok = false;
+                break;
+            }
+            if (tid == 0 && tile_store) {
+                tma_store_3d(&p.tm_o, ob, v0, h, (int)(t0 + (int64_t)c * kC));
+                bulk_commit();
             }
         }
-        // A readout wait of the last chunk that gave up is seen here.
-        if (!failed) failed = bar_any(kBarChain, kScanAllThreads, !ok0);
         if (tid == 0) bulk_wait_all();    // the output tiles have reached global memory
-        if (failed) {
-            if (tid == 0) atomicOr(p.status, kDevTimeout);
-        } else {
+        if (ok) {
             float4 *dst = reinterpret_cast<float4 *>(p.state_out + sbase + (size_t)row * kDK + v0 + 32 * g);
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4)
                 dst[q4] = make_float4(S[4 * q4], S[4 * q4 + 1], S[4 * q4 + 2], S[4 * q4 + 3]);
+        } else {
+            *abort = 1;
         }
     }
     tc_fence_before();
     __syncthreads();
+    if (tid == 0 && ctl.abort) atomicOr(p.status, kDevTimeout);
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, 256);
