@@ -108,11 +108,11 @@ gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, con
  *
  * Arguments, layouts, results and errors are those of gdn_prefill, minus
  * `workspace` and `workspace_bytes`.  The scratch is instead a fixed array of
- * GDN_PREFILL_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library, one per device,
+ * GDN_PREFILL_NOALLOC_SCRATCH_BYTES (96 MiB) inside the library, one per device,
  * created when the library's module is first used on that device; the call
  * allocates nothing and frees nothing.  A shape whose
  * gdn_prefill_workspace_bytes(shape) exceeds that size returns
- * GDN_ERR_INVALID_ARG and launches nothing: 64 MiB holds 1,149 records of one
+ * GDN_ERR_INVALID_ARG and launches nothing: 96 MiB holds 1,213 records of one
  * (64-token chunk, value head), e.g. one 4,096-token sequence at 16 value heads.
  * Shapes off the tensor-core path need no scratch and run as in gdn_prefill.
  *
@@ -122,7 +122,7 @@ gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, con
  * between them) race on the array and give wrong results: order such calls on
  * one stream or with events.
  */
-#define GDN_PREFILL_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+#define GDN_PREFILL_NOALLOC_SCRATCH_BYTES (96u * 1024u * 1024u)
 
 gdn_status gdn_prefill_noalloc(const gdn_shape *shape, const void *q, const void *k,
                                const void *v, const void *a, const void *b, const float *A_log,

@@ -47,12 +47,14 @@ constexpr uint32_t kBarPrep = 1, kBarChain = 1;
 constexpr long long kWaitBudget = 4000000000LL;   // cycles (~2 s) before a wait gives up
 constexpr int kAs = 68;                // row stride (floats) of the fp32 A / T tile
 
-// Workspace record of one (chunk, value head): shared-memory images for the scan.
-constexpr int REC_QW = 0;              // 2 d_k halves x [Q~ rows | W rows], 128 x 128 B each
-constexpr int REC_U = 32768;           // 2 column halves x 64 token rows x 128 B
-constexpr int REC_P = 49152;           // 64 rows x 128 B
-constexpr int REC_G = 57344;           // GateRec
-constexpr int kRecord = 58368;
+// Workspace record of one (chunk c, value head): shared-memory images for the scan.
+// Rows marked (c + 1) are written by the prep of the next chunk of the same sequence.
+constexpr int REC_QW = 0;              // 2 d_k halves x [Q~_c rows | W'_{c+1} rows], 128 x 128 B each
+constexpr int REC_PM = 32768;          // [P_c rows | M_{c+1} rows], 128 x 128 B
+constexpr int REC_U = 49152;           // U_c: 2 column halves x 64 token rows x 128 B
+constexpr int REC_W0 = 65536;          // W_c, 2 d_k halves x 64 rows (first chunk of a sequence only)
+constexpr int REC_G = 81920;           // GateRec
+constexpr int kRecord = 82944;
 
 struct __align__(16) GateRec {
     float gam[kC];      // e^{G_i}
@@ -269,9 +271,10 @@ constexpr int PP_AS = PP_TT + 16384;           // A, then T, fp32 [64][68]
 constexpr int kPrepSmem = PP_AS + 64 * kAs * 4 + 1024;
 
 struct PrepCtl {
-    uint64_t full, d1, d23;
+    uint64_t full, d1, d23, kprev, dm;
     uint32_t tmem;
     float G[kC], beta[kC], E[kC], F[kC], wsum[2];
+    float kfp[kC], wsum_p[2], gam_p;   // previous chunk: e^{G_C - G_j}, e^{G_C}
     GateRec gr;
 };
 
@@ -323,6 +326,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
         mbar_init(&ctl.full, 1);
         mbar_init(&ctl.d1, 1);
         mbar_init(&ctl.d23, 1);
+        mbar_init(&ctl.kprev, 1);
+        mbar_init(&ctl.dm, 1);
         fence_mbar_init();
     }
     // [T'; T''] blocks above the diagonal are never written: keep them zero.
@@ -335,7 +340,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
     const uint32_t tmem = ctl.tmem;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
 
-    uint32_t issued = 0;                           // MMA groups issued (thread 0): 2 = D1, 4 = D2/D3
+    uint32_t issued = 0;        // thread 0: 2 = D1, 4 = D2/D3, 8 = K_{c-1} load, 16 = M MMA
     if (pt == 0) {
         const int tok = (int)tc0;
         mbar_arrive_expect_tx(&ctl.full, 2 * 2 * 8192 + 2 * 8192 + (p.gate_tma ? 2048 : 0));
@@ -350,12 +355,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
             tma_load_2d(sm + PP_GT + 1024, &p.tm_b, h & ~7, tok, &ctl.full);
         }
     }
-    // Gate logits without TMA: plain loads, issued before the wait.
-    float ra = 0.f, rb = 0.f;
+    // Gate logits without TMA: plain loads, issued before the wait.  The previous chunk's
+    // decay logits (for W' and M) always come by plain loads.
+    float ra = 0.f, rb = 0.f, rap = 0.f;
     if (!p.gate_tma && pt < Lc) {
         ra = IoType<IO>::ld(static_cast<const IO *>(p.a) + (size_t)(tc0 + pt) * p.h_v + h);
         rb = IoType<IO>::ld(static_cast<const IO *>(p.b) + (size_t)(tc0 + pt) * p.h_v + h);
     }
+    if (c > 0 && pt < kC)
+        rap = IoType<IO>::ld(static_cast<const IO *>(p.a) + (size_t)(tc0 - kC + pt) * p.h_v + h);
     bool ok = mbar_wait(&ctl.full, 0, kWaitBudget);
     bool failed = bar_any(kBarPrep, kPrepThreads, !ok);
 
@@ -372,7 +380,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
             mma_commit(&ctl.d1);
             issued |= 2;
         }
-        float gsum = 0.f, be = 0.f;
+        float gsum = 0.f, be = 0.f, gsum_p = 0.f;
         if (pt < kC) {
             if (p.gate_tma) {
                 const IO *gt = reinterpret_cast<const IO *>(sm + PP_GT);
@@ -383,17 +391,30 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
                 gsum = decay_f(ra, p.A_log[h], p.dt_bias[h]);
                 be = sigmoid_f(rb);
             }
+            if (c > 0) gsum_p = decay_f(rap, p.A_log[h], p.dt_bias[h]);
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const float y = __shfl_up_sync(0xffffffffu, gsum, off);
-                if (lane >= off) gsum += y;
+                const float yp = __shfl_up_sync(0xffffffffu, gsum_p, off);
+                if (lane >= off) {
+                    gsum += y;
+                    gsum_p += yp;
+                }
             }
-            if (lane == 31) ctl.wsum[warp] = gsum;
+            if (lane == 31) {
+                ctl.wsum[warp] = gsum;
+                ctl.wsum_p[warp] = gsum_p;
+            }
         }
         named_bar(kBarPrep, kPrepThreads);
         if (pt < kC) {
             ctl.G[pt] = gsum + (warp == 1 ? ctl.wsum[0] : 0.f);
             ctl.beta[pt] = be;
+            // Previous chunk: e^{G_C - G_j} = e^{(sum of its g) - G_j}.
+            const float gp = gsum_p + (warp == 1 ? ctl.wsum_p[0] : 0.f);
+            const float gpc = ctl.wsum_p[0] + ctl.wsum_p[1];
+            ctl.kfp[pt] = __expf(gpc - gp);
+            if (pt == 0) ctl.gam_p = __expf(gpc);
         }
         named_bar(kBarPrep, kPrepThreads);
         const float GC = ctl.G[kC - 1], Gm = ctl.G[31];
@@ -467,7 +488,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
         fence_async_smem();
         named_bar(kBarPrep, kPrepThreads);
         if (pt == 0) {
-            bulk_store(rec + REC_P, sm + PP_PS, 8192);
+            bulk_store(rec + REC_PM, sm + PP_PS, 8192);
             bulk_commit();
         }
 
@@ -478,6 +499,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
         fence_async_smem();
         tc_fence_before();
         named_bar(kBarPrep, kPrepThreads);
+        // The previous chunk's keys (for M) into the spent A/T tile; they land during D2/D3.
+        if (pt == 0 && c > 0) {
+            mbar_arrive_expect_tx(&ctl.kprev, 2 * 8192);
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+                tma_load_3d(sm + PP_AS + r * 8192, &p.tm_k, r * 64, hq, (int)(tc0 - kC), &ctl.kprev);
+            issued |= 8;
+        }
 
         // D2 = [T'; T''] K -> columns 0-127 (W on lanes 0-63), D3 = [T'; T''] V ->
         // columns 128-255 (U on lanes 64-127).
@@ -498,7 +527,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
     if (!failed) {
         tc_fence_after();
         // W rows -> rows 128-191 of the K|Q|W regions; U rows -> the U image (over V).
+        // W' = e^{G_C of chunk c-1} W goes to the spent [T'; T''] tile for the previous
+        // chunk's record.
         const int row = 32 * q + lane;
+        const float gam_p = ctl.gam_p;
 #pragma unroll
         for (int c0 = 0; c0 < 64; c0 += 32) {
             uint32_t r[32];
@@ -512,16 +544,71 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
 #pragma unroll
             for (int q8 = 0; q8 < 4; ++q8)
                 *reinterpret_cast<uint4 *>(base + sw128_offset(rr, (c0 >> 3) + q8)) = pack8<IO>(x + 8 * q8);
+            if (q < 2 && c > 0) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[e] *= gam_p;
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8)
+                    *reinterpret_cast<uint4 *>(sm + PP_TT + hf * 8192 + sw128_offset(row, (c0 >> 3) + q8)) =
+                        pack8<IO>(x + 8 * q8);
+            }
         }
         fence_async_smem();
+        tc_fence_before();
         named_bar(kBarPrep, kPrepThreads);
+        uint8_t *const rec_prev = rec - (size_t)p.h_v * kRecord;   // chunk c - 1, same head
         if (pt == 0) {
 #pragma unroll
-            for (int r = 0; r < 2; ++r)
-                bulk_store(rec + REC_QW + r * 16384, sm + PP_KQW + r * kRegion + 8192, 16384);
+            for (int r = 0; r < 2; ++r) {
+                bulk_store(rec + REC_QW + r * 16384, sm + PP_KQW + r * kRegion + 8192, 8192);
+                if (c == 0)
+                    bulk_store(rec + REC_W0 + r * 8192, sm + PP_KQW + r * kRegion + 16384, 8192);
+                else
+                    bulk_store(rec_prev + REC_QW + r * 16384 + 8192, sm + PP_TT + r * 8192, 8192);
+            }
             bulk_store(rec + REC_U, sm + PP_V, 16384);
             bulk_store(rec + REC_G, &ctl.gr, sizeof(GateRec));
             bulk_commit();
+            // M_c = W_c K_{c-1}^T (columns scaled below) into TMEM columns 0-63.
+            if (c > 0) {
+                ok = mbar_wait(&ctl.kprev, 0, kWaitBudget);
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t aW = smem_u32(sm + PP_KQW + 16384), aKp = smem_u32(sm + PP_AS);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        mma_f16(tmem, sw128_desc(aW + (k >> 2) * kRegion + (k & 3) * 32, 16, 1024),
+                                sw128_desc(aKp + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), kIdD1, k > 0);
+                    mma_commit(&ctl.dm);
+                    issued |= 16;
+                }
+            }
+        }
+        if (c > 0) {
+            if (pt == 0) ok = ok && mbar_wait(&ctl.dm, 0, kWaitBudget);
+            failed = bar_any(kBarPrep, kPrepThreads, !ok);
+            if (!failed) {
+                // M_c[i][j] = (W_c K_{c-1}^T)[i][j] e^{G_C - G_j} of chunk c - 1, rows on lanes
+                // 0-63, into the P staging tile (the P store read it long ago).
+                tc_fence_after();
+                if (q < 2) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_base + 32 * hf, r);
+                    tmem_ld_wait();
+                    float x[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]) * ctl.kfp[32 * hf + e];
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8)
+                        *reinterpret_cast<uint4 *>(sm + PP_PS + sw128_offset(row, 4 * hf + q8)) = pack8<IO>(x + 8 * q8);
+                }
+                fence_async_smem();
+                named_bar(kBarPrep, kPrepThreads);
+                if (pt == 0) {
+                    bulk_store(rec_prev + REC_PM + 8192, sm + PP_PS, 8192);
+                    bulk_commit();
+                }
+            }
         }
     }
     if (failed && pt == 0) {
@@ -530,6 +617,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
         mbar_wait(&ctl.full, 0, kWaitBudget);
         if (issued & 2) mbar_wait(&ctl.d1, 0, kWaitBudget);
         if (issued & 4) mbar_wait(&ctl.d23, 0, kWaitBudget);
+        if (issued & 8) mbar_wait(&ctl.kprev, 0, kWaitBudget);
+        if (issued & 16) mbar_wait(&ctl.dm, 0, kWaitBudget);
     }
     if (pt == 0) bulk_wait_all();    // the records have reached global memory
     tc_fence_before();
@@ -541,32 +630,43 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
 }
 
 // ===================================================================== state scan
+// The chain runs one chunk ahead on W S: with S' = gamma_C S + K^T diag(e^{G_C - G}) Delta
+// the state after chunk c,
+//   W_{c+1} S' = W'_{c+1} S + M_{c+1} Delta,  W'_{c+1} = gamma_C W_{c+1},
+//   M_{c+1} = W_{c+1} K^T diag(e^{G_C - G})   (64 x 64, chunk c's K and gates),
+// so one M = 128 product X(c) = [P_c; M_{c+1}] Delta_c, accumulated onto
+// D4'(c) = [Q~_c; W'_{c+1}] S_c, yields both o_c (rows 0-63) and W_{c+1} S_{c+1}
+// (rows 64-127).  The next Delta waits only for X(c); the state update and D4'(c + 1)
+// run beside it.  The prep of chunk c + 1 writes W'_{c+1} and M_{c+1} into chunk c's
+// record; the first chunk of a sequence starts from W_0 S_0.
+//
 // Shared memory (from a 1024-aligned base): two stages, then the chain's own tiles.
-constexpr int SS_KQW = 0;                      // K (TMA) | Q~ W (record), two d_k regions
-constexpr int SS_U = 2 * kRegion;              // this column half of U, 64 x 128 B
-constexpr int SS_P = SS_U + 8192;              // P, 64 x 128 B (the MMA reads 64 more rows)
-constexpr int SS_G = SS_P + 8192;              // GateRec
-constexpr int kScanStage = SS_G + 1024;        // 65 KB
-constexpr int SS_SB = 2 * kScanStage;          // S0 in the I/O type, MN-major (d_k rows)
+constexpr int SS_KQW = 0;                      // K (TMA) | Q~_c | W'_{c+1}, two d_k regions
+constexpr int SS_U = 2 * kRegion;              // this column half of U_c, 64 x 128 B
+constexpr int SS_PM = SS_U + 8192;             // [P_c; M_{c+1}], 128 x 128 B
+constexpr int SS_G = SS_PM + 16384;            // GateRec
+constexpr int kScanStage = SS_G + 1024;        // 73 KB
+constexpr int SS_SB = 2 * kScanStage;          // S in the I/O type, MN-major (d_k rows)
 constexpr int SS_DB0 = SS_SB + 16384;          // Delta, MN-major (token rows)
 constexpr int SS_DB1 = SS_DB0 + 8192;          // diag(e^{G_C - G}) Delta
 constexpr int SS_OUT = SS_DB1 + 8192;          // output tile staging, two buffers
 constexpr int kScanSmem = SS_OUT + 2 * 8192 + 1024;
-// A stage arrives in two parts with their own barriers: part B ([Q~; W], read only by
-// D4) is refilled as soon as D4 has run; part A (K, U, P, gates) once the chunk's last
-// MMA has run and every thread has read the gates.
-constexpr uint32_t kTxA = 2 * 8192 + 8192 + 8192 + sizeof(GateRec);
+// A stage arrives in two parts with their own barriers: part B ([Q~; W'], read only by
+// D4') is refilled as soon as D4' has run; part A (K, U, [P; M], gates) once the chunk's
+// last MMA has run and every thread has read the gates.
+constexpr uint32_t kTxA = 2 * 8192 + 8192 + 16384 + sizeof(GateRec);
 constexpr uint32_t kTxB = 2 * 16384;
-constexpr uint32_t TS_D4 = 0, TS_DS = 128;     // TMEM columns: D4 at 0 / 64 by chunk parity
+constexpr uint32_t TS_D4 = 0, TS_DS = 128;     // TMEM columns: D4' at 0 / 64 by chunk parity
 constexpr int kChainWarps = 8;                 // Delta, state update, readout
-constexpr int kScanAllThreads = 32 * kChainWarps + 32;   // + one warp that issues MMAs and copies
+constexpr int kScanAllThreads = 32 * kChainWarps + 64;   // + an MMA-issue warp and a copy warp
 constexpr uint32_t kBarOut = 2;                // named barrier of the 128 readout threads
 constexpr int kLptMax = 128;                   // packed batches up to this size run longest first
 
 struct ScanCtl {
-    uint64_t full_a[2], full_b[2];             // stage parts landed
-    uint64_t d4, ds, dout;                     // MMA groups done (tcgen05.commit)
+    uint64_t full_a[2], full_b[2], full_w;     // stage parts landed; W_0
+    uint64_t d4, ds, x;                        // MMA groups done (tcgen05.commit)
     uint64_t delta_ready, sb_ready, out_done;  // chain warps -> issuing warp
+    uint64_t ld_b, ld_a;                       // copy warp -> issuing warp: phase c seen
     uint64_t drain;
     uint32_t tmem;
     int32_t abort;                             // a wait gave up: everyone leaves
@@ -575,11 +675,13 @@ struct ScanCtl {
 };
 
 // Bounded wait that also gives up as soon as another thread has given up.  Waiting
-// threads sleep in the barrier rather than poll.
+// threads sleep in the barrier rather than poll, except the single thread that issues
+// the MMAs, which polls so that it wakes the moment the phase completes.
+template <bool kPoll = false>
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int32_t *abort) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
+    while (!(kPoll ? mbar_try_wait(bar, parity) : mbar_try_wait_sleep(bar, parity, 20000u))) {
         if (*abort) return false;
         if (clock64() - t0 > kWaitBudget) {
             *abort = 1;
@@ -589,18 +691,18 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
     return true;
 }
 
-// Scan CTAs: one per (sequence, value head, half of the 128 state columns).  Per chunk c,
-// with the chunk's stage in shared memory and S0 (the state entering it) in registers
-// and, as the I/O type, in SB:
-//   D4(c) = [Q~; W] S0                      issued as soon as SB holds S0
-//   Delta = U - W S0                        warps on TMEM lanes 64-127
-//   DS = K^T diag(e^{G_C - G}) Delta        (commit ds), then D4(c)[0:64] += P Delta (commit dout)
-//   S = gamma_C S0 + DS, SB <- S            all chain warps; D4(c + 1) is issued at once
-//   o = D4(c)[0:64]                         warps on lanes 0-63, overlapping chunk c + 1
-// D4 alternates between two TMEM column blocks so that the readout of chunk c and the
-// product of chunk c + 1 do not share columns.  One warp issues every MMA and copy; the
-// chain warps never wait for it at a barrier, only on the barriers of the work they
-// consume, and it learns of their progress through arrival counts.
+// Scan CTAs: one per (sequence, value head, half of the 128 state columns).  Chunk c, with
+// S_c in registers (fp32) and in SB (I/O type):
+//   D4'(c) = [Q~_c; W'_{c+1}] S_c            issued once SB holds S_c      (commit d4)
+//   Delta_c = U_c - (W_c S_c)                warps on TMEM lanes 64-127, from X(c - 1)
+//   DS(c) = K_c^T diag(e^{G_C - G}) Delta_c                                 (commit ds)
+//   X(c) = [P_c; M_{c+1}] Delta_c            accumulated onto D4'(c)       (commit x)
+//   S_{c+1} = gamma_C S_c + DS(c), SB        all chain warps
+//   o_c = rows 0-63 of D4'(c) + X(c)         warps on lanes 0-63, overlapping chunk c + 1
+// X phases: 0 is W_0 S_0 (into block 1), c + 1 is X(c).  D4' alternates between two TMEM
+// column blocks.  One warp issues every MMA and copy; the chain warps wait only on the
+// barriers of the work they consume, and it learns of their progress through arrival
+// counts.
 template <typename IO>
 __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __grid_constant__ TcParams p) {
     constexpr bool kBf16 = std::is_same<IO, __nv_bfloat16>::value;
@@ -614,6 +716,7 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
     volatile int32_t *abort = &ctl.abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool issue_warp = (warp == kChainWarps);
+    const bool copy_warp = (warp == kChainWarps + 1);
     const int half = blockIdx.x & 1;
     const int h = (blockIdx.x >> 1) % p.h_v;
     int64_t n = (int64_t)(blockIdx.x >> 1) / p.h_v;
@@ -653,12 +756,15 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
             mbar_init(&ctl.full_a[i], 1);
             mbar_init(&ctl.full_b[i], 1);
         }
+        mbar_init(&ctl.full_w, 1);
         mbar_init(&ctl.d4, 1);
         mbar_init(&ctl.ds, 1);
-        mbar_init(&ctl.dout, 1);
+        mbar_init(&ctl.x, 1);
         mbar_init(&ctl.delta_ready, kChainWarps / 2);
         mbar_init(&ctl.sb_ready, kChainWarps);
         mbar_init(&ctl.out_done, kChainWarps / 2);
+        mbar_init(&ctl.ld_b, 1);
+        mbar_init(&ctl.ld_a, 1);
         mbar_init(&ctl.drain, 1);
         ctl.abort = 0;
         fence_mbar_init();
@@ -671,107 +777,153 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
     const uint32_t tmem = ctl.tmem;
     const size_t sbase = ((size_t)n * p.h_v + h) * kDK * kDK;
 
+    auto record = [&](int c) { return p.ws + (size_t)((base_slot + c) * p.h_v + h) * kRecord; };
+    auto load_a = [&](int c) {   // K, U half, [P; M] and gates of chunk c into stage c & 1
+        const int s = c & 1;
+        uint8_t *st = sm + s * kScanStage;
+        const uint8_t *rec = record(c);
+        mbar_arrive_expect_tx(&ctl.full_a[s], kTxA);
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+            tma_load_3d(st + SS_KQW + r * kRegion, &p.tm_k, r * 64, hq, (int)(t0 + (int64_t)c * kC),
+                        &ctl.full_a[s]);
+        bulk_load(st + SS_U, rec + REC_U + half * 8192, 8192, &ctl.full_a[s]);
+        bulk_load(st + SS_PM, rec + REC_PM, 16384, &ctl.full_a[s]);
+        bulk_load(st + SS_G, rec + REC_G, sizeof(GateRec), &ctl.full_a[s]);
+    };
+    auto load_b = [&](int c) {   // [Q~_c; W'_{c+1}] of chunk c into stage c & 1
+        const int s = c & 1;
+        uint8_t *st = sm + s * kScanStage;
+        const uint8_t *rec = record(c);
+        mbar_arrive_expect_tx(&ctl.full_b[s], kTxB);
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+            bulk_load(st + SS_KQW + r * kRegion + 8192, rec + REC_QW + r * 16384, 16384, &ctl.full_b[s]);
+    };
+
     if (issue_warp) {
-        // ------------------------------------------------------------ MMA and copy issue
-        if (lane == 0) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0 && nchunks > 0) {
             const uint32_t aSB = smem_u32(sm + SS_SB), aDB0 = smem_u32(sm + SS_DB0),
                            aDB1 = smem_u32(sm + SS_DB1);
-            int issued_a = 0, issued_b = 0, landed_a = 0, landed_b = 0;
-            auto record = [&](int c) {
-                return p.ws + (size_t)((base_slot + c) * p.h_v + h) * kRecord;
-            };
-            auto load_a = [&](int c) {   // K, U half, P and gates of chunk c into stage c & 1
-                const int s = c & 1;
-                uint8_t *st = sm + s * kScanStage;
-                const uint8_t *rec = record(c);
-                mbar_arrive_expect_tx(&ctl.full_a[s], kTxA);
-#pragma unroll
-                for (int r = 0; r < 2; ++r)
-                    tma_load_3d(st + SS_KQW + r * kRegion, &p.tm_k, r * 64, hq,
-                                (int)(t0 + (int64_t)c * kC), &ctl.full_a[s]);
-                bulk_load(st + SS_U, rec + REC_U + half * 8192, 8192, &ctl.full_a[s]);
-                bulk_load(st + SS_P, rec + REC_P, 8192, &ctl.full_a[s]);
-                bulk_load(st + SS_G, rec + REC_G, sizeof(GateRec), &ctl.full_a[s]);
-                issued_a = c + 1;
-            };
-            auto load_b = [&](int c) {   // [Q~; W] of chunk c into stage c & 1
-                const int s = c & 1;
-                uint8_t *st = sm + s * kScanStage;
-                const uint8_t *rec = record(c);
-                mbar_arrive_expect_tx(&ctl.full_b[s], kTxB);
-#pragma unroll
-                for (int r = 0; r < 2; ++r)
-                    bulk_load(st + SS_KQW + r * kRegion + 8192, rec + REC_QW + r * 16384, 16384, &ctl.full_b[s]);
-                issued_b = c + 1;
-            };
-            // D4(c) = [Q~; W] S0 into block c & 1, once SB holds S0 and part B has landed.
-            auto issue_d4 = [&](int c) -> bool {
-                const int s = c & 1;
-                if (!wait_or_abort(&ctl.sb_ready, c & 1, abort)) return false;
-                if (!wait_or_abort(&ctl.full_b[s], (c >> 1) & 1, abort)) return false;
-                landed_b = c + 1;
+            bool b1_issued = false;
+            // [rows 64-191 of a stage's regions] S into TMEM block `blk`.
+            auto issue_qw = [&](int s, int blk) {
                 tc_fence_after();
                 const uint32_t aSt = smem_u32(sm + s * kScanStage);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t off = (k >> 2) * kRegion + 8192 + (k & 3) * 32;
-                    mma_f16(tmem + TS_D4 + 64 * s, sw128_desc(aSt + off, 16, 1024),
+                    mma_f16(tmem + TS_D4 + 64 * blk, sw128_desc(aSt + off, 16, 1024),
                             sw128_desc(aSB + k * 2048, 16384, 1024), kIdNV, k > 0);
                 }
-                mma_commit(&ctl.d4);
-                return true;
             };
             bool ok = true;
-            for (int c = 0; c < 2 && c < nchunks; ++c) {
-                load_b(c);
-                load_a(c);
-            }
-            if (nchunks > 0) ok = issue_d4(0);
+            do {
+                // X phase 0: W_0 S_0 into block 1 (the Q~ rows there are unused).
+                if (!(ok = wait_or_abort<true>(&ctl.sb_ready, 0, abort) && wait_or_abort<true>(&ctl.full_w, 0, abort))) break;
+                issue_qw(1, 1);
+                mma_commit(&ctl.x);
+                // D4'(0) into block 0.
+                if (!(ok = wait_or_abort<true>(&ctl.full_b[0], 0, abort))) break;
+                issue_qw(0, 0);
+                mma_commit(&ctl.d4);
+                // Stage 1's part B, once W_0 S_0 has read its rows.
+                if (nchunks > 1) {
+                    if (!(ok = wait_or_abort<true>(&ctl.x, 0, abort))) break;
+                    load_b(1);
+                    b1_issued = true;
+                }
+            } while (false);
             for (int c = 0; ok && c < nchunks; ++c) {
                 const int s = c & 1;
                 const uint32_t aSt = smem_u32(sm + s * kScanStage);
-                // D4(c) has read part B of stage s: refill it with chunk c + 2.
-                ok = wait_or_abort(&ctl.d4, c & 1, abort);
+                // DS(c) once Delta_c is in DB0 / DB1; the copy warp has seen X phase c
+                // and sb_ready phase c, so neither can run two phases ahead of it.
+                ok = wait_or_abort<true>(&ctl.delta_ready, c & 1, abort) &&
+                     wait_or_abort<true>(&ctl.full_a[s], (c >> 1) & 1, abort) &&
+                     (c == 0 || wait_or_abort<true>(&ctl.ld_a, (c - 1) & 1, abort));
                 if (!ok) break;
-                if (c + 2 < nchunks) load_b(c + 2);
-                // DS = K^T diag(e^{G_C - G}) Delta once Delta is in DB0 / DB1.
-                ok = wait_or_abort(&ctl.delta_ready, c & 1, abort) &&
-                     wait_or_abort(&ctl.full_a[s], (c >> 1) & 1, abort);
-                if (!ok) break;
-                landed_a = c + 1;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_f16(tmem + TS_DS, sw128_desc(aSt + k * 2048, kRegion, 1024),
                             sw128_desc(aDB1 + k * 2048, 8192, 1024), kIdDS, k > 0);
                 mma_commit(&ctl.ds);
-                // D4(c)[0:64] += P Delta (the A rows past P land in the spent W S0 lanes).
-                // The readout of chunk c - 1 is done, so the readout warps have seen the
-                // previous dout phase and block (c + 1) & 1 is free for D4(c + 1).
-                if (c > 0 && !(ok = wait_or_abort(&ctl.out_done, (c - 1) & 1, abort))) break;
+                // X(c) onto D4'(c).  The readout of chunk c - 1 is done, so the readout
+                // warps have seen X phase c and block (c + 1) & 1 is free for D4'(c + 1).
+                if (c > 0 && !(ok = wait_or_abort<true>(&ctl.out_done, (c - 1) & 1, abort))) break;
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_f16(tmem + TS_D4 + 64 * s, sw128_desc(aSt + SS_P + k * 32, 16, 1024),
+                    mma_f16(tmem + TS_D4 + 64 * s, sw128_desc(aSt + SS_PM + k * 32, 16, 1024),
                             sw128_desc(aDB0 + k * 2048, 8192, 1024), kIdNV, 1u);
-                mma_commit(&ctl.dout);
-                if (c + 1 < nchunks && !(ok = issue_d4(c + 1))) break;
-                // Chunk c's last MMA has run and every thread has read its gates (they
-                // arrived on sb_ready after that): refill part A of stage s.
-                if (c + 2 < nchunks) {
-                    ok = wait_or_abort(&ctl.dout, c & 1, abort);
+                mma_commit(&ctl.x);
+                if (c + 1 < nchunks) {
+                    // D4'(c + 1) once SB holds S_{c+1} (and the copy warp has seen D4'(c)).
+                    ok = wait_or_abort<true>(&ctl.sb_ready, (c + 1) & 1, abort) &&
+                         wait_or_abort<true>(&ctl.full_b[(c + 1) & 1], ((c + 1) >> 1) & 1, abort) &&
+                         wait_or_abort<true>(&ctl.ld_b, c & 1, abort);
                     if (!ok) break;
-                    load_a(c + 2);
+                    issue_qw((c + 1) & 1, (c + 1) & 1);
+                    mma_commit(&ctl.d4);
                 }
             }
             if (!ok) {
-                // Let the copies and MMAs already issued land before the CTA leaves
-                // (bounded): one commit covers every earlier MMA of this thread.
+                // Let the MMAs already issued (and stage 1's part B) finish before the CTA
+                // leaves (bounded): one commit covers every earlier MMA of this thread.
                 *abort = 1;
-                for (int w = landed_a; w < issued_a; ++w) mbar_wait(&ctl.full_a[w & 1], (w >> 1) & 1, kWaitBudget);
-                for (int w = landed_b; w < issued_b; ++w) mbar_wait(&ctl.full_b[w & 1], (w >> 1) & 1, kWaitBudget);
+                if (b1_issued) mbar_wait(&ctl.full_b[1], 0, kWaitBudget);
                 mma_commit(&ctl.drain);
                 mbar_wait(&ctl.drain, 0, kWaitBudget);
             }
+        }
+        __syncwarp();
+    } else if (copy_warp) {
+        // ------------------------------------------------------------ stage copies
+        if (lane == 0 && nchunks > 0) {
+            int last_a[2] = {-1, -1}, last_b[2] = {-1, -1};
+            mbar_arrive_expect_tx(&ctl.full_w, 16384);
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+                bulk_load(sm + kScanStage + SS_KQW + r * kRegion + 16384, record(0) + REC_W0 + r * 8192, 8192,
+                          &ctl.full_w);
+            load_a(0);
+            load_b(0);
+            last_a[0] = 0;
+            last_b[0] = 0;
+            if (nchunks > 1) {
+                load_a(1);
+                last_a[1] = 1;
+            }
+            bool ok = true;
+            for (int c = 0; ok && c < nchunks; ++c) {
+                const int s = c & 1;
+                // D4'(c) has read part B of stage s: refill it with chunk c + 2.  The
+                // arrivals only say which phases this warp has seen, so they go first.
+                if (!(ok = wait_or_abort(&ctl.d4, c & 1, abort))) break;
+                mbar_arrive(&ctl.ld_b);
+                if (c + 2 < nchunks) {
+                    load_b(c + 2);
+                    last_b[s] = c + 2;
+                }
+                // X(c) has read the rest of stage s and every thread has read chunk c's
+                // gates (they arrive on sb_ready after that): refill part A.
+                if (!(ok = wait_or_abort(&ctl.x, (c + 1) & 1, abort) &&
+                           wait_or_abort(&ctl.sb_ready, (c + 1) & 1, abort)))
+                    break;
+                mbar_arrive(&ctl.ld_a);
+                if (c + 2 < nchunks) {
+                    load_a(c + 2);
+                    last_a[s] = c + 2;
+                }
+            }
+            // Copies still in flight land before the CTA leaves (bounded).
+            mbar_wait(&ctl.full_w, 0, kWaitBudget);
+            for (int s2 = 0; s2 < 2; ++s2) {
+                if (last_a[s2] >= 0) mbar_wait(&ctl.full_a[s2], (last_a[s2] >> 1) & 1, kWaitBudget);
+                if (last_b[s2] >= 0) mbar_wait(&ctl.full_b[s2], (last_b[s2] >> 1) & 1, kWaitBudget);
+            }
+            if (!ok) *abort = 1;
         }
         __syncwarp();
     } else {
@@ -808,22 +960,23 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
             const int s = c & 1;
             const uint8_t *st = sm + s * kScanStage;
             const GateRec &gr = *reinterpret_cast<const GateRec *>(st + SS_G);
-            const uint32_t d4col = TS_D4 + 64 * s;
             // Every reader of the stage observes its arrival itself.
             ok = ok && wait_or_abort(&ctl.full_a[s], (c >> 1) & 1, abort);
             const float gC = ok ? gr.gC : 0.f;
 
             if (!out_warp) {
-                // Delta = U - W S0 on lanes 64-127 (token rows), this thread's 32 columns.
-                ok = ok && wait_or_abort(&ctl.d4, c & 1, abort);
+                // Delta_c = U_c - W_c S_c on lanes 64-127 (token rows), this thread's 32
+                // columns; W_c S_c is in block (c - 1) & 1 after X phase c.
+                ok = ok && wait_or_abort(&ctl.x, c & 1, abort);
                 if (ok) {
                     tc_fence_after();
                     const int j = row - 64;
                     const float kfj = gr.kf[j];
+                    const uint32_t wcol = TS_D4 + 64 * ((c + 1) & 1);
 #pragma unroll
                     for (int ps = 0; ps < 2; ++ps) {
                         uint32_t ws[16];
-                        tmem_ld16(tmem + lane_base + d4col + 32 * g + 16 * ps, ws);
+                        tmem_ld16(tmem + lane_base + wcol + 32 * g + 16 * ps, ws);
                         float x[16];
 #pragma unroll
                         for (int q8 = 0; q8 < 2; ++q8) {
@@ -858,7 +1011,7 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                 if (lane == 0) mbar_arrive(&ctl.delta_ready);
             }
 
-            // S = gamma_C S0 + DS (fp32 registers), then the next chunk's operand tile.
+            // S_{c+1} = gamma_C S_c + DS(c) (fp32 registers), then the operand tile.
             ok = ok && wait_or_abort(&ctl.ds, c & 1, abort);
             if (ok) {
                 tc_fence_after();
@@ -877,21 +1030,21 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                 continue;
             }
 
-            // o_i = (Q~ S0 + P Delta)_i on lanes 0-63, while chunk c + 1 runs.  A full
+            // o_c = rows 0-63 of block c & 1 after X(c), while chunk c + 1 runs.  A full
             // chunk goes out as one TMA store of the staged 64 x 64 tile; a sequence's
             // ragged last chunk is stored row by row so that no row of the next sequence
             // is touched.  The readout warps leave the loop together, at their barrier.
             const int Lc = (int)((L - (int64_t)c * kC) < kC ? (L - (int64_t)c * kC) : kC);
             const bool tile_store = (Lc == kC);
             uint8_t *ob = sm + SS_OUT + s * 8192;
-            ok = ok && wait_or_abort(&ctl.dout, c & 1, abort);
+            ok = ok && wait_or_abort(&ctl.x, (c + 1) & 1, abort);
             if (ok) {
                 tc_fence_after();
                 uint4 packed[4];
 #pragma unroll
                 for (int ps = 0; ps < 2; ++ps) {
                     uint32_t r[16];
-                    tmem_ld16(tmem + lane_base + d4col + 32 * g + 16 * ps, r);
+                    tmem_ld16(tmem + lane_base + TS_D4 + 64 * s + 32 * g + 16 * ps, r);
                     tmem_ld_wait();
                     float x[16];
 #pragma unroll

@@ -183,14 +183,14 @@ def gdn_prefill(q, k, v, a, b, A_log, dt_bias, state_in=None, cu_seqlens=None,
 
 
 # Size of the library's fixed scratch array behind gdn_prefill_noalloc.
-PREFILL_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+PREFILL_NOALLOC_SCRATCH_BYTES = 96 * 1024 * 1024
 
 
 def gdn_prefill_noalloc(q, k, v, a, b, A_log, dt_bias, state_in, cu_seqlens, scale: float,
                         *, o, state_out, stream=None):
     """gdn_prefill for callers that may not allocate device memory: the outputs are
     caller-provided and the tensor-core path's scratch is the library's fixed
-    64 MiB array, shared by every call on the device (calls that overlap on the GPU
+    96 MiB array, shared by every call on the device (calls that overlap on the GPU
     race on it).  Shapes needing more scratch raise GDN_ERR_INVALID_ARG."""
     lib = load()
     shape = _shape_of(q, v, cu_seqlens)

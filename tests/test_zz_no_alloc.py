@@ -21,7 +21,7 @@ from gpu_util import TOL, rel_err, to_device
 def test_noalloc_rejects_oversized_shapes_on_the_host():
     from recurrent_state_scan_gb300 import gdn
     lib = gdn.load()
-    # 1 x 8192 tokens x 16 value heads needs 128 chunks x 16 records: above 64 MiB.
+    # 1 x 8192 tokens x 16 value heads needs 128 chunks x 16 records: above 96 MiB.
     shape = gdn.make_shape(gdn.GDN_BF16, 1, 8192, 1, 16, 16, 128, 128)
     assert gdn.gdn_prefill_workspace_bytes(shape) > gdn.PREFILL_NOALLOC_SCRATCH_BYTES
     st = lib.gdn_prefill_noalloc(ctypes.byref(shape), *([None] * 9), 0.0, None, None, None)
