@@ -91,19 +91,23 @@ def peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def source_digest() -> str:
+# Sources of the kernels each workload's traffic figure belongs to.
+KERNEL_SOURCES = {"decode": ("scan_simt.cu",), "prefill": ("prefill_tc.cu", "tc_ptx.cuh")}
+
+
+def source_digest(kind: str = "prefill") -> str:
+    """Hash of the kernel sources behind `kind` ("decode" or "prefill")."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "recurrent_state_scan_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, fn), "rb") as f:
-                h.update(fn.encode() + b"\0" + f.read())
+    for fn in KERNEL_SOURCES[kind]:
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
-    or None when there is none or the kernel sources changed since it was taken."""
+def profiled_traffic(workload: str, kind: str):
+    """DRAM bytes of one call from the committed ncu summary, or None when there is none
+    or the kernel sources changed since it was taken."""
     path = os.path.join(ROOT, "profiles", f"traffic_{workload}.md")
     if not os.path.exists(path):
         return None
@@ -113,7 +117,7 @@ def profiled_traffic(workload: str):
             if ":" in line and line.startswith("- "):
                 k, v = line[2:].split(":", 1)
                 vals[k.strip()] = v.strip().strip("`")
-    if vals.get("source_sha256") != source_digest():
+    if vals.get("source_sha256") != source_digest(kind):
         return None
     try:
         return int(vals["dram_bytes_per_launch"])
@@ -382,15 +386,18 @@ def main():
         value, unit = world * nbytes / sec / 1e9, "GB/s"
     else:
         value, unit = world * inp.total_tokens / sec, "tokens/s"
-    # Roofline of the dominant kernel (one launch per call: the call's device time).
+    # Roofline of the call: one kernel for decode; for prefill the chunk-prep kernel and
+    # the state-scan kernel, which run back to back and do no useful work alone.
     gbs = nbytes / sec / 1e9
     tfs = flops / sec / 1e12
     t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
     t_tc = flops / (pk["bf16_tflops"] * 1e12)
     roof = {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-            "frac": gbs / pk["hbm_gbs"], "traffic": profiled_traffic(inp_name),
+            "frac": gbs / pk["hbm_gbs"],
+            "traffic": profiled_traffic(inp_name, "decode" if s.decode else "prefill"),
             "peak_source": f"{pk_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"
-            if pk_kind == "measured" else "fallback 6.8 TB/s"}
+            if pk_kind == "measured" else "fallback 6.8 TB/s",
+            "kernels": "gdn_decode (scan_simt)" if s.decode else "gdn_chunk_prep + gdn_chunk_scan, one call"}
     if not s.decode:
         roof["tensor_tflops"] = tfs
         roof["tensor_frac_of_bf16_peak"] = tfs / pk["bf16_tflops"]
