@@ -91,6 +91,13 @@ typedef struct gdn_shape {
  * bf16/f16 I/O with d_k = d_v = 128 runs the chunked tensor-core path (q, k, v
  * and o must then be 16-byte aligned, else the SIMT path runs); other shapes and
  * fp32 I/O run the token-sequential SIMT path.  State math is fp32 always.
+ *
+ * On the tensor-core path a batched call whose scan uses few SMs is split along
+ * the time axis into chunk segments; the preparation of a later segment then runs
+ * on a stream internal to the library (one per device, created on first use)
+ * beside the scan of the earlier one.  The internal work is ordered after what
+ * `stream` held at the call and the call's last kernel is ordered after it, so
+ * the call keeps the stream-ordered semantics above.
  */
 size_t gdn_prefill_workspace_bytes(const gdn_shape *shape);
 

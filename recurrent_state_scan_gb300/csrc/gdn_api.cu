@@ -139,7 +139,8 @@ gdn_status gdn_prefill_plan(const gdn_shape *shape, int32_t *path, int32_t *laun
     const int64_t tokens = varlen ? shape->seqlen : shape->seqlen * (int64_t)shape->batch;
     const bool tc = prefill_tc_shape_ok((gdn_dtype)shape->io_dtype, shape->d_k, shape->d_v, tokens);
     if (path) *path = tc ? 2 : 1;
-    if (launches) *launches = shape->num_seqs > 0 ? (tc ? 2 : 1) : 0;
+    const int nseg = tc ? prefill_tc_segments(varlen, shape->seqlen, shape->batch, shape->h_v) : 1;
+    if (launches) *launches = shape->num_seqs > 0 ? (tc ? 2 * nseg : 1) : 0;
     return GDN_OK;
 }
 
@@ -159,6 +160,17 @@ gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, con
                        const void *a, const void *b, const float *A_log, const float *dt_bias,
                        const float *state_in, const int32_t *cu_seqlens, float scale, void *o,
                        float *state_out, void *workspace, size_t workspace_bytes, void *stream) {
+    return prefill_impl(shape, q, k, v, a, b, A_log, dt_bias, state_in, cu_seqlens, scale, o,
+                        state_out, workspace, workspace_bytes, true, stream);
+}
+
+}  // extern "C"
+
+gdn_status gdn::prefill_impl(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                             const void *a, const void *b, const float *A_log, const float *dt_bias,
+                             const float *state_in, const int32_t *cu_seqlens, float scale, void *o,
+                             float *state_out, void *workspace, size_t workspace_bytes,
+                             bool allow_overlap, void *stream) {
     gdn_status st = check_shape(shape, cu_seqlens != nullptr);
     if (st != GDN_OK) return st;
     const int64_t tokens = cu_seqlens ? shape->seqlen : shape->seqlen * (int64_t)shape->batch;
@@ -192,7 +204,7 @@ gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, con
             return fail(GDN_ERR_INVALID_ARG, "workspace of %zu bytes is below the %zu this call needs",
                         workspace == nullptr ? (size_t)0 : workspace_bytes, need);
         if (!aligned(workspace, 16)) return fail(GDN_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
-        e = launch_prefill_tc(p, io, tokens, workspace, (cudaStream_t)stream);
+        e = launch_prefill_tc(p, io, tokens, workspace, allow_overlap, (cudaStream_t)stream);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");
     } else {
         e = launch_scan_simt(p, io, (cudaStream_t)stream);
@@ -200,6 +212,8 @@ gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, con
     }
     return GDN_OK;
 }
+
+extern "C" {
 
 gdn_status gdn_decode_step(const gdn_shape *shape, const void *q, const void *k, const void *v,
                            const void *a, const void *b, const float *A_log,

@@ -99,7 +99,19 @@ gdn_status report_error(gdn_status status, const char *message);
 bool prefill_tc_shape_ok(gdn_dtype io, int d_k, int d_v, int64_t total_tokens);
 size_t prefill_tc_workspace(bool varlen, int64_t seqlen, int64_t batch, int64_t num_seqs, int h_v);
 bool prefill_tc_supported(const ScanParams &p, gdn_dtype io, int64_t total_tokens);
+// Chunk segments a call of this shape is split into (1: none).  Batched inputs whose scan
+// grid leaves most of the GPU idle run the prep of later segments on an internal stream
+// beside the scan of earlier ones; each segment costs one prep and one scan launch.
+int prefill_tc_segments(bool varlen, int64_t seqlen, int64_t batch, int h_v);
 cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_tokens,
-                              void *workspace, cudaStream_t stream);
+                              void *workspace, bool allow_overlap, cudaStream_t stream);
+
+// gdn_prefill with the segment overlap allowed or not (no internal stream is created
+// when it is not).
+gdn_status prefill_impl(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                        const void *a, const void *b, const float *A_log, const float *dt_bias,
+                        const float *state_in, const int32_t *cu_seqlens, float scale, void *o,
+                        float *state_out, void *workspace, size_t workspace_bytes,
+                        bool allow_overlap, void *stream);
 
 }  // namespace gdn

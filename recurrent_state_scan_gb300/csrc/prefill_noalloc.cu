@@ -62,6 +62,8 @@ extern "C" gdn_status gdn_prefill_noalloc(const gdn_shape *shape, const void *q,
     void *scratch = nullptr;
     gdn_status st = gdn::scratch_address(&scratch);
     if (st != GDN_OK) return st;
-    return gdn_prefill(shape, q, k, v, a, b, A_log, dt_bias, state_in, cu_seqlens, scale, o,
-                       state_out, scratch, (size_t)GDN_PREFILL_NOALLOC_SCRATCH_BYTES, stream);
+    // No segment overlap: it would create an internal stream on first use.
+    return gdn::prefill_impl(shape, q, k, v, a, b, A_log, dt_bias, state_in, cu_seqlens, scale, o,
+                             state_out, scratch, (size_t)GDN_PREFILL_NOALLOC_SCRATCH_BYTES, false,
+                             stream);
 }

@@ -29,6 +29,7 @@
 // their T row the unit row and their W, U and Delta rows exactly zero.
 #include <cudaTypedefs.h>
 
+#include <mutex>
 #include <type_traits>
 
 #include "gdn_internal.cuh"
@@ -74,6 +75,11 @@ struct TcParams {
     int64_t seqlen;
     int32_t num_seqs, h_qk, h_v;
     int32_t chunks_per_seq;         // batched input: chunks of every sequence
+    // Chunk range [seg_begin, seg_end) of every sequence that this launch covers.  A
+    // segment's first chunk starts from W S (like a sequence's first chunk); the state
+    // crosses segments through state_in / state_out.  seg_direct: the prep grid holds
+    // exactly (sequence, chunk of the range, head) instead of every workspace slot.
+    int32_t seg_begin, seg_end, seg_direct;
     float scale;
     int *status;
     uint8_t *ws;                    // workspace records
@@ -290,13 +296,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
     __shared__ PrepCtl ctl;
     const int pt = threadIdx.x, warp = pt >> 5, lane = pt & 31;
     const int q = warp & 3, hf = warp >> 2;        // TMEM lane quarter, column half
-    const int64_t slot = blockIdx.x / p.h_v;
     const int h = blockIdx.x % p.h_v;
     const int hq = h / (p.h_v / p.h_qk);
+    int64_t slot = blockIdx.x / p.h_v;
 
-    // Which sequence and chunk this slot holds (idle slots leave at once).
+    // Which sequence and chunk this CTA holds (idle slots leave at once).
     int64_t n;
-    if (p.cu_seqlens == nullptr) {
+    if (p.seg_direct) {
+        const int64_t per = p.seg_end - p.seg_begin;
+        n = slot / per;
+        if (n >= p.num_seqs) return;
+        slot = n * p.chunks_per_seq + p.seg_begin + slot % per;
+    } else if (p.cu_seqlens == nullptr) {
         n = slot / p.chunks_per_seq;
         if (n >= p.num_seqs) return;
     } else {
@@ -311,10 +322,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
     int64_t t0, t1;
     if (!seq_range(p.cu_seqlens, p.seqlen, p.num_seqs, p.status, n, t0, t1)) return;
     const int64_t c = slot - slot_base(p, n);
-    if (c * kC >= t1 - t0) return;
+    if (c * kC >= t1 - t0 || c < p.seg_begin || c >= p.seg_end) return;
     const int64_t tc0 = t0 + c * kC;
     const int Lc = (int)((t1 - tc0) < kC ? (t1 - tc0) : kC);
-    uint8_t *rec = p.ws + (size_t)blockIdx.x * kRecord;
+    uint8_t *rec = p.ws + ((size_t)slot * p.h_v + h) * kRecord;
+    // A segment's first chunk writes W for the scan to start from; every other chunk
+    // writes W' and M into its predecessor's record.
+    const bool first = (c == p.seg_begin);
 
     float *const As = reinterpret_cast<float *>(sm + PP_AS);
     const uint32_t aKQW = smem_u32(sm + PP_KQW), aTT = smem_u32(sm + PP_TT), aV = smem_u32(sm + PP_V);
@@ -362,7 +376,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
         ra = IoType<IO>::ld(static_cast<const IO *>(p.a) + (size_t)(tc0 + pt) * p.h_v + h);
         rb = IoType<IO>::ld(static_cast<const IO *>(p.b) + (size_t)(tc0 + pt) * p.h_v + h);
     }
-    if (c > 0 && pt < kC)
+    if (!first && pt < kC)
         rap = IoType<IO>::ld(static_cast<const IO *>(p.a) + (size_t)(tc0 - kC + pt) * p.h_v + h);
     bool ok = mbar_wait(&ctl.full, 0, kWaitBudget);
     bool failed = bar_any(kBarPrep, kPrepThreads, !ok);
@@ -391,7 +405,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
                 gsum = decay_f(ra, p.A_log[h], p.dt_bias[h]);
                 be = sigmoid_f(rb);
             }
-            if (c > 0) gsum_p = decay_f(rap, p.A_log[h], p.dt_bias[h]);
+            if (!first) gsum_p = decay_f(rap, p.A_log[h], p.dt_bias[h]);
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const float y = __shfl_up_sync(0xffffffffu, gsum, off);
@@ -500,7 +514,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
         tc_fence_before();
         named_bar(kBarPrep, kPrepThreads);
         // The previous chunk's keys (for M) into the spent A/T tile; they land during D2/D3.
-        if (pt == 0 && c > 0) {
+        if (pt == 0 && !first) {
             mbar_arrive_expect_tx(&ctl.kprev, 2 * 8192);
 #pragma unroll
             for (int r = 0; r < 2; ++r)
@@ -544,7 +558,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
 #pragma unroll
             for (int q8 = 0; q8 < 4; ++q8)
                 *reinterpret_cast<uint4 *>(base + sw128_offset(rr, (c0 >> 3) + q8)) = pack8<IO>(x + 8 * q8);
-            if (q < 2 && c > 0) {
+            if (q < 2 && !first) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) x[e] *= gam_p;
 #pragma unroll
@@ -561,7 +575,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 bulk_store(rec + REC_QW + r * 16384, sm + PP_KQW + r * kRegion + 8192, 8192);
-                if (c == 0)
+                if (first)
                     bulk_store(rec + REC_W0 + r * 8192, sm + PP_KQW + r * kRegion + 16384, 8192);
                 else
                     bulk_store(rec_prev + REC_QW + r * 16384 + 8192, sm + PP_TT + r * 8192, 8192);
@@ -570,7 +584,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
             bulk_store(rec + REC_G, &ctl.gr, sizeof(GateRec));
             bulk_commit();
             // M_c = W_c K_{c-1}^T (columns scaled below) into TMEM columns 0-63.
-            if (c > 0) {
+            if (!first) {
                 ok = mbar_wait(&ctl.kprev, 0, kWaitBudget);
                 if (ok) {
                     tc_fence_after();
@@ -584,7 +598,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
                 }
             }
         }
-        if (c > 0) {
+        if (!first) {
             if (pt == 0) ok = ok && mbar_wait(&ctl.dm, 0, kWaitBudget);
             failed = bar_any(kBarPrep, kPrepThreads, !ok);
             if (!failed) {
@@ -743,9 +757,15 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
 
     int64_t t0, t1;
     if (!seq_range(p.cu_seqlens, p.seqlen, p.num_seqs, p.status, n, t0, t1)) return;
+    // This launch walks chunks [seg_begin, seg_end) of the sequence; below, chunk c
+    // counts from the segment's first chunk, and t0 / L / base_slot are shifted to it.
+    const int64_t all_chunks = (t1 - t0 + kC - 1) / kC;
+    const int64_t cb = p.seg_begin < all_chunks ? p.seg_begin : all_chunks;
+    const int64_t ce = p.seg_end < all_chunks ? p.seg_end : all_chunks;
+    const int nchunks = (int)(ce - cb);
+    const int64_t base_slot = slot_base(p, n) + cb;
+    t0 += cb * kC;
     const int64_t L = t1 - t0;
-    const int nchunks = (int)((L + kC - 1) / kC);
-    const int64_t base_slot = slot_base(p, n);
 
     if (warp == 0) {
         tmem_alloc(&ctl.tmem, 256);
@@ -1144,8 +1164,49 @@ bool make_gate_map(CUtensorMap *m, const void *base, gdn_dtype io, int h_v, int6
 }
 
 
+// Streaming multiprocessors of the current device (looked up once per device; 0 when
+// there is no device).
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = v;
+    }
+    return cache[dev];
+}
+
+constexpr int kMaxSegments = 4;
+constexpr int kMinSegmentChunks = 32;
+
+// An internal stream and events of the current device, created on first use, on which
+// the prep of later chunk segments runs beside the scan of earlier ones.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t ev[kMaxSegments] = {};
+    bool ready = false;
+    std::mutex launch_mu;   // one call's event records and waits at a time
+};
+SideStream *side_stream() {
+    static SideStream cache[64];
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    SideStream &s = cache[dev];
+    if (!s.ready) {
+        if (cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+        for (int i = 0; i < kMaxSegments; ++i)
+            if (cudaEventCreateWithFlags(&s.ev[i], cudaEventDisableTiming) != cudaSuccess) return nullptr;
+        s.ready = true;
+    }
+    return &s;
+}
+
 template <typename IO>
-cudaError_t launch_typed(const TcParams &tp, int64_t n_slots, cudaStream_t stream) {
+cudaError_t configure() {
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(gdn_chunk_prep<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1156,14 +1217,75 @@ cudaError_t launch_typed(const TcParams &tp, int64_t n_slots, cudaStream_t strea
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const int64_t prep_blocks = n_slots * tp.h_v;
-    const int64_t scan_blocks = (int64_t)tp.num_seqs * tp.h_v * (kDK / kNV);
-    if (prep_blocks > 0x7fffffffLL || scan_blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    gdn_chunk_prep<IO><<<(unsigned)prep_blocks, kPrepThreads, kPrepSmem, stream>>>(tp);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    gdn_chunk_scan<IO><<<(unsigned)scan_blocks, kScanAllThreads, kScanSmem, stream>>>(tp);
+    return cudaSuccess;
+}
+
+template <typename IO>
+cudaError_t launch_prep(const TcParams &tp, int64_t ctas, cudaStream_t stream) {
+    if (ctas <= 0) return cudaSuccess;
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    gdn_chunk_prep<IO><<<(unsigned)ctas, kPrepThreads, kPrepSmem, stream>>>(tp);
     return cudaGetLastError();
+}
+
+template <typename IO>
+cudaError_t launch_scan(const TcParams &tp, cudaStream_t stream) {
+    const int64_t ctas = (int64_t)tp.num_seqs * tp.h_v * (kDK / kNV);
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    gdn_chunk_scan<IO><<<(unsigned)ctas, kScanAllThreads, kScanSmem, stream>>>(tp);
+    return cudaGetLastError();
+}
+
+// One call: the prep over every workspace slot, then the scan; or, split into `nseg`
+// chunk segments, the prep of segment k + 1 on the side stream beside the scan of
+// segment k.  Every launch stays ordered after the work already on `stream`, and the
+// last scan after every side launch.
+template <typename IO>
+cudaError_t launch_typed(TcParams tp, int64_t n_slots, int nseg, cudaStream_t stream) {
+    cudaError_t e = configure<IO>();
+    if (e != cudaSuccess) return e;
+    SideStream *side = nseg > 1 ? side_stream() : nullptr;
+    if (side == nullptr) {
+        tp.seg_begin = 0;
+        tp.seg_end = 0x7fffffff;
+        tp.seg_direct = 0;
+        e = launch_prep<IO>(tp, n_slots * tp.h_v, stream);
+        return e != cudaSuccess ? e : launch_scan<IO>(tp, stream);
+    }
+    const int cps = tp.chunks_per_seq;
+    auto bound = [&](int k) { return (int)((int64_t)k * cps / nseg); };
+    float *const state_out = tp.state_out;
+    const float *const state_in = tp.state_in;
+    tp.seg_direct = 1;
+    std::lock_guard<std::mutex> lock(side->launch_mu);
+    for (int k = 0; e == cudaSuccess && k < nseg; ++k) {
+        TcParams pk = tp;
+        if (k == 0) {
+            // The side stream starts once the first prep is done, i.e. when the first
+            // scan starts, so that later preps take the SMs the scan leaves free rather
+            // than delaying the first prep.
+            pk.seg_begin = bound(0);
+            pk.seg_end = bound(1);
+            e = launch_prep<IO>(pk, (int64_t)tp.num_seqs * (pk.seg_end - pk.seg_begin) * tp.h_v, stream);
+            if (e == cudaSuccess) e = cudaEventRecord(side->ev[0], stream);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->ev[0], 0);
+        }
+        if (e == cudaSuccess && k + 1 < nseg) {
+            pk.seg_begin = bound(k + 1);
+            pk.seg_end = bound(k + 2);
+            e = launch_prep<IO>(pk, (int64_t)tp.num_seqs * (pk.seg_end - pk.seg_begin) * tp.h_v, side->stream);
+            if (e == cudaSuccess) e = cudaEventRecord(side->ev[k + 1], side->stream);
+        }
+        if (e == cudaSuccess && k > 0) e = cudaStreamWaitEvent(stream, side->ev[k], 0);
+        if (e == cudaSuccess) {
+            pk.seg_begin = bound(k);
+            pk.seg_end = bound(k + 1);
+            pk.state_in = k == 0 ? state_in : state_out;
+            pk.state_out = state_out;
+            e = launch_scan<IO>(pk, stream);
+        }
+    }
+    return e;
 }
 
 // Chunk slots the prep kernel covers (an upper bound for packed sequences).
@@ -1183,6 +1305,14 @@ size_t prefill_tc_workspace(bool varlen, int64_t seqlen, int64_t batch, int64_t 
     return (size_t)chunk_slots(varlen, seqlen, batch, num_seqs) * (size_t)h_v * kRecord;
 }
 
+int prefill_tc_segments(bool varlen, int64_t seqlen, int64_t batch, int h_v) {
+    if (varlen) return 1;
+    const int sms = sm_count();
+    if (sms <= 0 || batch * h_v * (kDK / kNV) * 3 > sms) return 1;   // the scan alone fills the GPU
+    const int64_t nseg = ((seqlen + kC - 1) / kC) / kMinSegmentChunks;
+    return (int)(nseg < 1 ? 1 : (nseg > kMaxSegments ? kMaxSegments : nseg));
+}
+
 bool prefill_tc_supported(const ScanParams &p, gdn_dtype io, int64_t total_tokens) {
     if (!prefill_tc_shape_ok(io, p.d_k, p.d_v, total_tokens)) return false;
     const void *ptrs[] = {p.q, p.k, p.v, p.o};
@@ -1192,7 +1322,7 @@ bool prefill_tc_supported(const ScanParams &p, gdn_dtype io, int64_t total_token
 }
 
 cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_tokens, void *workspace,
-                              cudaStream_t stream) {
+                              bool allow_overlap, cudaStream_t stream) {
     TcParams tp;
     memset(&tp, 0, sizeof(tp));
     if (!make_map(&tp.tm_q, p.q, io, p.h_qk, total_tokens) ||
@@ -1214,8 +1344,9 @@ cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_t
     tp.ws = static_cast<uint8_t *>(workspace);
     const bool varlen = p.cu_seqlens != nullptr;
     const int64_t n_slots = chunk_slots(varlen, p.seqlen, p.num_seqs, p.num_seqs);
-    if (io == GDN_BF16) return launch_typed<__nv_bfloat16>(tp, n_slots, stream);
-    return launch_typed<__half>(tp, n_slots, stream);
+    const int nseg = allow_overlap ? prefill_tc_segments(varlen, p.seqlen, p.num_seqs, p.h_v) : 1;
+    if (io == GDN_BF16) return launch_typed<__nv_bfloat16>(tp, n_slots, nseg, stream);
+    return launch_typed<__half>(tp, n_slots, nseg, stream);
 }
 
 }  // namespace gdn
