@@ -44,7 +44,7 @@ constexpr int kC = 64;                 // tokens per chunk
 constexpr int kDK = 128;               // d_k = d_v of this path
 constexpr int kNV = 64;                // state columns per scan CTA
 constexpr int kPrepThreads = 256;
-constexpr uint32_t kBarPrep = 1, kBarChain = 1;
+constexpr uint32_t kBarPrep = 1;
 constexpr long long kWaitBudget = 4000000000LL;   // cycles (~2 s) before a wait gives up
 constexpr int kAs = 68;                // row stride (floats) of the fp32 A / T tile
 
@@ -64,8 +64,7 @@ struct __align__(16) GateRec {
 };
 
 struct TcParams {
-    CUtensorMap tm_q, tm_k, tm_v, tm_o, tm_a, tm_b;
-    int32_t gate_tma;               // gate logits by TMA (h_v % 8 == 0) or plain loads
+    CUtensorMap tm_q, tm_k, tm_v, tm_o;
     const void *a, *b;
     const float *A_log, *dt_bias;
     const float *state_in;
@@ -193,18 +192,22 @@ __device__ __forceinline__ void block_store(const Blk &d, const float (&acc)[2][
 // Blocks below the diagonal use tf32 warp MMAs; each is also kept transposed in the
 // unused upper block of As (T_ij at As[16 j + c][16 i + r]), so A below the diagonal
 // is never overwritten while it is still read.
-template <typename IO>
+// `side(t, n)` runs on the other 192 threads (t = 0 .. 191 of n = 192) during step 1.
+template <typename IO, typename Side>
 __device__ void invert_chunk(float *As, float (*X)[16][20], uint8_t *tt, const float *beta,
-                             const float *gam, int pt) {
+                             const float *gam, int pt, Side &&side) {
     if (pt < 64) {
+        // Column-oriented: once x_l is known it updates every later row's sum, so the
+        // serial chain is one FMA per row instead of a whole dot product.
         const int o = (pt >> 4) * 16, j = pt & 15, cj = o + j;
-        float x[16];
+        float x[16], acc[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float acc = 0.f;
+        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
 #pragma unroll
-            for (int l = 0; l < i; ++l) acc = fmaf(As[(o + i) * kAs + o + l], x[l], acc);
-            x[i] = (i < j) ? 0.f : ((i == j) ? 1.f : -acc);
+        for (int l = 0; l < 16; ++l) {
+            x[l] = (l < j) ? 0.f : ((l == j) ? 1.f : -acc[l]);
+#pragma unroll
+            for (int i = l + 1; i < 16; ++i) acc[i] = fmaf(As[(o + i) * kAs + o + l], x[l], acc[i]);
         }
         __syncwarp();
         const float f2 = beta[cj], f1 = f2 * gam[cj];
@@ -213,6 +216,8 @@ __device__ void invert_chunk(float *As, float (*X)[16][20], uint8_t *tt, const f
             As[(o + i) * kAs + cj] = x[i];
             tt_put<IO>(tt, o + i, cj, x[i], f1, f2);
         }
+    } else {
+        side(pt - 64, kPrepThreads - 64);
     }
     if (pt == 0) bulk_wait_read();   // X below reuses the staging tile of the P store
     named_bar(kBarPrep, kPrepThreads);
@@ -270,8 +275,7 @@ __device__ void invert_chunk(float *As, float (*X)[16][20], uint8_t *tt, const f
 constexpr int kRegion = 24576;                 // 192 rows x 128 B: K | Q | W for 64 d_k
 constexpr int PP_KQW = 0;                      // two regions
 constexpr int PP_V = 2 * kRegion;              // V, 2 x 64 x 128 B; later the U image
-constexpr int PP_GT = PP_V + 16384;            // gate logit tiles a, b: 64 tokens x 8 heads
-constexpr int PP_PS = PP_GT + 2048;            // P image; later the merges' scratch
+constexpr int PP_PS = PP_V + 16384;            // P image; later the merges' scratch, then M
 constexpr int PP_TT = PP_PS + 8192;            // [T'; T''], 128 x 128 B
 constexpr int PP_AS = PP_TT + 16384;           // A, then T, fp32 [64][68]
 constexpr int kPrepSmem = PP_AS + 64 * kAs * 4 + 1024;
@@ -357,50 +361,27 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
     uint32_t issued = 0;        // thread 0: 2 = D1, 4 = D2/D3, 8 = K_{c-1} load, 16 = M MMA
     if (pt == 0) {
         const int tok = (int)tc0;
-        mbar_arrive_expect_tx(&ctl.full, 2 * 2 * 8192 + 2 * 8192 + (p.gate_tma ? 2048 : 0));
+        mbar_arrive_expect_tx(&ctl.full, 2 * 2 * 8192 + 2 * 8192);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             tma_load_3d(sm + PP_KQW + r * kRegion, &p.tm_k, r * 64, hq, tok, &ctl.full);
             tma_load_3d(sm + PP_KQW + r * kRegion + 8192, &p.tm_q, r * 64, hq, tok, &ctl.full);
             tma_load_3d(sm + PP_V + r * 8192, &p.tm_v, r * 64, h, tok, &ctl.full);
         }
-        if (p.gate_tma) {
-            tma_load_2d(sm + PP_GT, &p.tm_a, h & ~7, tok, &ctl.full);
-            tma_load_2d(sm + PP_GT + 1024, &p.tm_b, h & ~7, tok, &ctl.full);
-        }
     }
-    // Gate logits without TMA: plain loads, issued before the wait.  The previous chunk's
-    // decay logits (for W' and M) always come by plain loads.
+    // The gates (this chunk's and, for W' and M, the previous chunk's decay) are computed
+    // from plain loads of the logits while K, Q and V are in flight.
     float ra = 0.f, rb = 0.f, rap = 0.f;
-    if (!p.gate_tma && pt < Lc) {
+    if (pt < Lc) {
         ra = IoType<IO>::ld(static_cast<const IO *>(p.a) + (size_t)(tc0 + pt) * p.h_v + h);
         rb = IoType<IO>::ld(static_cast<const IO *>(p.b) + (size_t)(tc0 + pt) * p.h_v + h);
     }
     if (!first && pt < kC)
         rap = IoType<IO>::ld(static_cast<const IO *>(p.a) + (size_t)(tc0 - kC + pt) * p.h_v + h);
-    bool ok = mbar_wait(&ctl.full, 0, kWaitBudget);
-    bool failed = bar_any(kBarPrep, kPrepThreads, !ok);
-
-    if (!failed) {
-        // D1 = [K; Q] K^T; the gates are computed meanwhile.
-        if (pt == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t off = (k >> 2) * kRegion + (k & 3) * 32;
-                mma_f16(tmem, sw128_desc(aKQW + off, 16, 1024), sw128_desc(aKQW + off, 16, 1024), kIdD1,
-                        k > 0);
-            }
-            mma_commit(&ctl.d1);
-            issued |= 2;
-        }
+    bool ok = true, failed = false;
+    {
         float gsum = 0.f, be = 0.f, gsum_p = 0.f;
         if (pt < kC) {
-            if (p.gate_tma) {
-                const IO *gt = reinterpret_cast<const IO *>(sm + PP_GT);
-                ra = IoType<IO>::ld(gt + pt * 8 + (h & 7));
-                rb = IoType<IO>::ld(gt + 512 + pt * 8 + (h & 7));
-            }
             if (pt < Lc) {
                 gsum = decay_f(ra, p.A_log[h], p.dt_bias[h]);
                 be = sigmoid_f(rb);
@@ -440,9 +421,25 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
             ctl.F[pt] = __expf(Gm - G);
             if (pt == 0) ctl.gr.gC = __expf(GC);
         }
-        ok = mbar_wait(&ctl.d1, 0, kWaitBudget);
-        failed = bar_any(kBarPrep, kPrepThreads, !ok);   // also publishes E, F, gamma
     }
+    // D1 = [K; Q] K^T once K and Q have landed.
+    if (pt == 0) {
+        ok = mbar_wait(&ctl.full, 0, kWaitBudget);
+        if (ok) {
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t off = (k >> 2) * kRegion + (k & 3) * 32;
+                mma_f16(tmem, sw128_desc(aKQW + off, 16, 1024), sw128_desc(aKQW + off, 16, 1024), kIdD1,
+                        k > 0);
+            }
+            mma_commit(&ctl.d1);
+            issued |= 2;
+            ok = mbar_wait(&ctl.d1, 0, kWaitBudget);
+        }
+    }
+    failed = bar_any(kBarPrep, kPrepThreads, !ok);   // also publishes E, F, gamma
+    if (!failed) ok = mbar_wait(&ctl.full, 0, kWaitBudget);   // every reader of Q and V
     if (!failed) {
         tc_fence_after();
         // A rows (lanes 0-63, fp32) and P rows (lanes 64-127, I/O type); each column half
@@ -483,22 +480,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
                 }
             }
         }
-        // D1 has read Q: scale it in place, Q~ = diag(scale gamma) Q.
-        for (int e = pt; e < 1024; e += kPrepThreads) {
-            const int r = e >> 9, row = (e >> 3) & 63, ch = e & 7;
-            uint8_t *ptr = sm + PP_KQW + r * kRegion + 8192 + sw128_offset(row, ch);
-            const uint4 u = *reinterpret_cast<const uint4 *>(ptr);
-            const float f = p.scale * ctl.gr.gam[row];
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-            float x[8];
-#pragma unroll
-            for (int k2 = 0; k2 < 4; ++k2) {
-                const float2 t2 = Pack<IO>::unpack(w[k2]);
-                x[2 * k2] = t2.x * f;
-                x[2 * k2 + 1] = t2.y * f;
-            }
-            *reinterpret_cast<uint4 *>(ptr) = pack8<IO>(x);
-        }
         fence_async_smem();
         named_bar(kBarPrep, kPrepThreads);
         if (pt == 0) {
@@ -507,9 +488,28 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
         }
 
         // T = (I + A)^-1, written as [T diag(beta gamma); T diag(beta)] (K-major); its
-        // merges reuse the P staging tile once the store above has read it.
+        // merges reuse the P staging tile once the store above has read it.  Meanwhile
+        // the threads outside its first step scale Q in place (D1 has read it):
+        // Q~ = diag(scale gamma) Q.
+        auto scale_q = [&](int t, int nt) {
+            for (int e = t; e < 1024; e += nt) {
+                const int r = e >> 9, row = (e >> 3) & 63, ch = e & 7;
+                uint8_t *ptr = sm + PP_KQW + r * kRegion + 8192 + sw128_offset(row, ch);
+                const uint4 u = *reinterpret_cast<const uint4 *>(ptr);
+                const float f = p.scale * ctl.gr.gam[row];
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                float x[8];
+#pragma unroll
+                for (int k2 = 0; k2 < 4; ++k2) {
+                    const float2 t2 = Pack<IO>::unpack(w[k2]);
+                    x[2 * k2] = t2.x * f;
+                    x[2 * k2 + 1] = t2.y * f;
+                }
+                *reinterpret_cast<uint4 *>(ptr) = pack8<IO>(x);
+            }
+        };
         invert_chunk<IO>(As, reinterpret_cast<float (*)[16][20]>(sm + PP_PS), sm + PP_TT, ctl.beta,
-                         ctl.gr.gam, pt);
+                         ctl.gr.gam, pt, scale_q);
         fence_async_smem();
         tc_fence_before();
         named_bar(kBarPrep, kPrepThreads);
@@ -1148,20 +1148,6 @@ bool make_map(CUtensorMap *m, const void *base, gdn_dtype io, int heads, int64_t
     return r == CUDA_SUCCESS;
 }
 
-// 2-D map over the [tokens][h_v] gate logits with 8-head x 64-token boxes.
-bool make_gate_map(CUtensorMap *m, const void *base, gdn_dtype io, int h_v, int64_t tokens) {
-    auto fn = encode_fn();
-    if (fn == nullptr) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)h_v, (cuuint64_t)tokens};
-    const cuuint64_t strides[1] = {(cuuint64_t)h_v * 2};
-    const cuuint32_t box[2] = {8, (cuuint32_t)kC};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = fn(m, io == GDN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                          2, const_cast<void *>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
 
 
 // Streaming multiprocessors of the current device (looked up once per device; 0 when
@@ -1330,12 +1316,6 @@ cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_t
         !make_map(&tp.tm_v, p.v, io, p.h_v, total_tokens) ||
         !make_map(&tp.tm_o, p.o, io, p.h_v, total_tokens))
         return cudaErrorInvalidValue;
-    // Gate logits ride along with the TMA when their rows are 16-byte multiples.
-    tp.gate_tma = (p.h_v % 8 == 0 && reinterpret_cast<uintptr_t>(p.a) % 16 == 0 &&
-                   reinterpret_cast<uintptr_t>(p.b) % 16 == 0 &&
-                   make_gate_map(&tp.tm_a, p.a, io, p.h_v, total_tokens) &&
-                   make_gate_map(&tp.tm_b, p.b, io, p.h_v, total_tokens))
-                      ? 1 : 0;
     tp.a = p.a; tp.b = p.b; tp.A_log = p.A_log; tp.dt_bias = p.dt_bias;
     tp.state_in = p.state_in; tp.state_out = p.state_out; tp.o = p.o;
     tp.cu_seqlens = p.cu_seqlens; tp.seqlen = p.seqlen; tp.num_seqs = p.num_seqs;

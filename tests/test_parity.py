@@ -218,3 +218,18 @@ def test_bad_device_cu_seqlens_sets_check_word():
     o, s = run_prefill(inp)                            # the context is still usable
     o_ref, s_ref = oracle.scan_inputs(inp)
     check(inp, o, s, o_ref, s_ref, what="after device check")
+
+
+def test_prefill_time_segments_with_ragged_tail():
+    """A batched call long enough to be split into time segments (a small scan grid and
+    65 chunks: two segments, the last chunk ragged) against the oracle, with an initial
+    state; the plan reports two launches per segment."""
+    from recurrent_state_scan_gb300 import gdn
+    spec = workloads.small_spec(io="bf16", batch=1, seqlen=4100, h_qk=2, h_v=4, seed=61,
+                                state_std=0.05)
+    inp = workloads.draw(spec)
+    path, launches = gdn.gdn_prefill_plan(gdn.shape_of_spec(spec, inp.n_seq, inp.total_tokens))
+    assert path == gdn.PATH_TC and launches == 4
+    o_ref, s_ref = oracle.scan_inputs(inp, threads=4)
+    o, s = run_prefill(inp)
+    check(inp, o, s, o_ref, s_ref, what="time segments")
