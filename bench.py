@@ -60,8 +60,9 @@ def io_bytes(inp) -> dict:
     return {
         "q": T * s.h_qk * s.d_k * es, "k": T * s.h_qk * s.d_k * es, "v": T * s.h_v * s.d_v * es,
         "a": T * s.h_v * es, "b": T * s.h_v * es, "params": 2 * s.h_v * 4,
-        "state_in": st if inp.state_in is not None else 0,
+        "state_in": st if (inp.state_in is not None or inp.pool is not None) else 0,
         "o": T * s.h_v * s.d_v * es, "state_out": st,
+        "slots": 4 * n if inp.pool is not None else 0,
     }
 
 
@@ -219,7 +220,10 @@ def time_oracle(inp, budget_s: float, min_reps: int = 1):
     oracle.build()
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.scan_inputs(inp, threads=threads)
+        if inp.pool is not None:
+            oracle.slot_scan_inputs(inp, threads=threads)
+        else:
+            oracle.scan_inputs(inp, threads=threads)
         reps += 1
         el = time.perf_counter() - t0
         if reps >= min_reps and el >= budget_s:
@@ -248,7 +252,8 @@ def cpu_baseline_line(inp, budget_s=10.0):
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, local):
-    from recurrent_state_scan_gb300 import gdn_decode_step, gdn_prefill, load
+    from recurrent_state_scan_gb300 import (gdn_decode_step, gdn_decode_step_slots, gdn_prefill,
+                                            load)
     load()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -261,6 +266,9 @@ def run_ours(args, rank, world, local):
     n_state = (inp.n_seq, s.h_v, s.d_k, s.d_v)
     state_out = torch.empty(n_state, dtype=torch.float32, device=dev)
     work_state = None if state0 is None else state0.clone()
+    # A state pool stays resident on the device, as a serving pool would.
+    pool = None if inp.pool is None else inp.pool.to(dev)
+    slots = None if inp.slots is None else inp.slots.to(dev)
     from recurrent_state_scan_gb300 import gdn
     ws_need = 0 if s.decode else gdn.gdn_prefill_workspace_bytes(
         gdn.shape_of_spec(s, inp.n_seq, inp.total_tokens))
@@ -269,7 +277,10 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        if s.decode:
+        if pool is not None:
+            gdn_decode_step_slots(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"],
+                                  t["dt_bias"], pool, slots, inp.scale, o=o, stream=stream)
+        elif s.decode:
             gdn_decode_step(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"], t["dt_bias"],
                             work_state, inp.scale, o=o, stream=stream)
         else:
@@ -304,17 +315,23 @@ def run_ours(args, rank, world, local):
         host = {n: v.pin_memory() for n, v in
                 [("q", inp.q), ("k", inp.k), ("v", inp.v), ("a", inp.a), ("b", inp.b),
                  ("A_log", inp.A_log), ("dt_bias", inp.dt_bias)] +
-                ([("state", inp.state_in)] if inp.state_in is not None else [])}
+                ([("state", inp.state_in)] if inp.state_in is not None else []) +
+                ([("slots", inp.slots)] if inp.slots is not None else [])}
         o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
         s_host = torch.empty(n_state, dtype=torch.float32).pin_memory()
         dbuf = {n: torch.empty_like(v, device=dev) for n, v in host.items()}
         h2d = sum(v.numel() * v.element_size() for v in host.values())
-        d2h = o_host.numel() * o_host.element_size() + s_host.numel() * 4
+        # With a resident pool only o comes back; otherwise o and the state.
+        d2h = o_host.numel() * o_host.element_size() + (0 if pool is not None else s_host.numel() * 4)
 
         def e2e_step():
             for n, v in host.items():
                 dbuf[n].copy_(v, non_blocking=True)
-            if s.decode:
+            if pool is not None:
+                gdn_decode_step_slots(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["a"], dbuf["b"],
+                                      dbuf["A_log"], dbuf["dt_bias"], pool, dbuf["slots"],
+                                      inp.scale, o=o, stream=stream)
+            elif s.decode:
                 gdn_decode_step(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["a"], dbuf["b"],
                                 dbuf["A_log"], dbuf["dt_bias"], dbuf["state"], inp.scale, o=o,
                                 stream=stream)
@@ -448,6 +465,11 @@ def config_of(inp, world):
         c["lengths"] = [int(x) for x in inp.lengths()]
     else:
         c["batch"], c["seq_len"] = s.batch, s.seqlen
+    if inp.pool is not None:
+        c["initial_state"] = "pool of %d states, N(0,%g)" % (s.pool_size, s.pool_std)
+        c["state_pool"] = {"entries": s.pool_size, "slots": "distinct, seeded permutation",
+                           "resident": "on the device; e2e moves the step's q, k, v, a, b and "
+                                       "slots in and o out"}
     return c
 
 

@@ -150,9 +150,33 @@ gdn_status gdn_decode_step(const gdn_shape *shape, const void *q, const void *k,
                            void *stream);
 
 /*
+ * gdn_decode_step_slots -- gdn_decode_step against a pool of states, for continuous
+ * batching: sequence b (b < B = shape->batch = shape->num_seqs) reads and updates
+ * pool entry slots[b] in place.  Follows the `gated_delta_slots` op of the nuvec-core
+ * page (src/fast/imp.rs, the fallback graph of FastOp::GatedDeltaSlots): the states at
+ * the slots are taken, the rule runs, and the new states are put back at the slots.
+ *
+ *   pool        DEVICE fp32 [pool_size, h_v, d_k, d_v], 16-byte aligned; entries not
+ *               named by `slots` are neither read nor written.
+ *   pool_size   number of pool entries (> 0).
+ *   slots       DEVICE int32 [B].  The rows should name distinct entries: with a
+ *               repeated entry, which row's state lands there, and what those rows
+ *               read, is unspecified.  A slot outside [0, pool_size) skips its row
+ *               (its o row is left as it was, no pool entry changes) and sets the
+ *               device check word, reported by gdn_last_device_status() as
+ *               GDN_ERR_DEVICE_CHECK.
+ *   q .. o, scale   as gdn_decode_step.
+ */
+gdn_status gdn_decode_step_slots(const gdn_shape *shape, const void *q, const void *k,
+                                 const void *v, const void *a, const void *b, const float *A_log,
+                                 const float *dt_bias, float *pool, int64_t pool_size,
+                                 const int32_t *slots, float scale, void *o, void *stream);
+
+/*
  * gdn_last_device_status -- synchronise `stream`, read the device check word
  * set by any earlier call on the current device, clear it, and return GDN_OK or
- * GDN_ERR_DEVICE_CHECK / GDN_ERR_TIMEOUT.
+ * GDN_ERR_DEVICE_CHECK (malformed cu_seqlens, or a slot outside the pool) /
+ * GDN_ERR_TIMEOUT.
  */
 gdn_status gdn_last_device_status(void *stream);
 

@@ -130,3 +130,42 @@ def scan_inputs(inp, units=None, threads: int = 1):
     return scan(inp.cu_seqlens, s.h_qk, s.h_v, s.d_k, s.d_v, f["q"], f["k"], f["v"],
                 a=f["a"], b=f["b"], A_log=f["A_log"], dt_bias=f["dt_bias"],
                 state_in=f["state_in"], scale=inp.scale, units=units, threads=threads)
+
+
+def slot_scan(cu_seqlens: Sequence[int], h_qk: int, h_v: int, d_k: int, d_v: int,
+              q, k, v, a, b, A_log, dt_bias, pool, slots, scale: Optional[float] = None,
+              threads: int = 1):
+    """The rule against a pool of states (nuvec-core src/fast/imp.rs, `gated_delta_slots`
+    and the fallback graph of FastOp::GatedDeltaSlots): take the states at the slots, run
+    the recurrence, put the new states back at the slots.
+
+    pool: [P, h_v, d_k, d_v]; slots: [n_seq] integers.  Sequence n starts from
+    pool[slots[n]] and its final state is written there; entries not named by a slot are
+    unchanged.  A slot outside [0, P) -- which the pages leave open -- skips its
+    sequence: its outputs stay zero and the pool is unchanged.  With repeated slots the
+    later sequence's state lands last.  Returns (o, new pool) in float64.
+    """
+    pool = np.array(_f64(pool), dtype=np.float64, copy=True).reshape(-1, h_v, d_k, d_v)
+    P = pool.shape[0]
+    slots = [int(x) for x in np.asarray(slots).reshape(-1)]
+    n_seq = len(cu_seqlens) - 1
+    assert len(slots) == n_seq
+    taken = np.zeros((n_seq, h_v, d_k, d_v), dtype=np.float64)
+    kept = [n for n in range(n_seq) if 0 <= slots[n] < P]
+    for n in kept:
+        taken[n] = pool[slots[n]]
+    units = [n * h_v + h for n in kept for h in range(h_v)]
+    o, s_out = scan(cu_seqlens, h_qk, h_v, d_k, d_v, q, k, v, a=a, b=b, A_log=A_log,
+                    dt_bias=dt_bias, state_in=taken, scale=scale, units=units, threads=threads)
+    for n in kept:
+        pool[slots[n]] = s_out[n]
+    return o, pool
+
+
+def slot_scan_inputs(inp, threads: int = 1):
+    """slot_scan on a drawn ``workloads.Inputs`` that carries a pool and slots."""
+    s = inp.spec
+    f = inp.f64
+    return slot_scan(inp.cu_seqlens, s.h_qk, s.h_v, s.d_k, s.d_v, f["q"], f["k"], f["v"],
+                     f["a"], f["b"], f["A_log"], f["dt_bias"], f["pool"], inp.slots.numpy(),
+                     scale=inp.scale, threads=threads)

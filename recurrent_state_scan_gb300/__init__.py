@@ -3,6 +3,7 @@
 The compute lives in libgdn (CUDA for sm_103a, C ABI declared in include/gdn.h);
 this package builds it in-tree and binds it with ctypes.
 """
-from .gdn import (GdnError, GdnShape, gdn_decode_step, gdn_last_device_status,  # noqa: F401
+from .gdn import (GdnError, GdnShape, gdn_decode_step, gdn_decode_step_slots,  # noqa: F401
+                  gdn_last_device_status,
                   gdn_prefill, gdn_prefill_noalloc, gdn_prefill_workspace_bytes,
                   gdn_status_string, load)

@@ -248,6 +248,43 @@ gdn_status gdn_decode_step(const gdn_shape *shape, const void *q, const void *k,
     return GDN_OK;
 }
 
+gdn_status gdn_decode_step_slots(const gdn_shape *shape, const void *q, const void *k,
+                                 const void *v, const void *a, const void *b, const float *A_log,
+                                 const float *dt_bias, float *pool, int64_t pool_size,
+                                 const int32_t *slots, float scale, void *o, void *stream) {
+    gdn_status st = check_shape(shape, false);
+    if (st != GDN_OK) return st;
+    if (shape->seqlen != 1)
+        return fail(GDN_ERR_INVALID_ARG, "decode takes seqlen 1 (got %lld)", (long long)shape->seqlen);
+    st = check_inputs(shape, shape->batch, q, k, v, a, b, A_log, dt_bias, o);
+    if (st != GDN_OK) return st;
+    if (shape->batch == 0) return GDN_OK;
+    if (pool == nullptr || slots == nullptr) return fail(GDN_ERR_INVALID_ARG, "pool or slots is NULL");
+    if (pool_size <= 0) return fail(GDN_ERR_INVALID_ARG, "pool_size %lld <= 0", (long long)pool_size);
+    if (!aligned(pool, 16) || !aligned(slots, 4))
+        return fail(GDN_ERR_INVALID_ARG, "pool must be 16-byte and slots 4-byte aligned");
+    if (!(scale == scale) || isinf(scale)) return fail(GDN_ERR_INVALID_ARG, "scale is not finite");
+    int *word = nullptr;
+    st = status_word(&word);
+    if (st != GDN_OK) return st;
+
+    ScanParams p{};
+    p.q = q; p.k = k; p.v = v; p.a = a; p.b = b;
+    p.A_log = A_log; p.dt_bias = dt_bias;
+    p.state_in = pool; p.state_out = pool; p.o = o;
+    p.cu_seqlens = nullptr;
+    p.seqlen = 1;
+    p.num_seqs = shape->batch;
+    p.h_qk = shape->h_qk; p.h_v = shape->h_v; p.d_k = shape->d_k; p.d_v = shape->d_v;
+    p.scale = scale == 0.0f ? 1.0f / sqrtf((float)shape->d_k) : scale;
+    p.status = word;
+    p.slots = slots;
+    p.pool_size = pool_size;
+    cudaError_t e = launch_scan_simt(p, (gdn_dtype)shape->io_dtype, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "slot decode launch");
+    return GDN_OK;
+}
+
 gdn_status gdn_last_device_status(void *stream) {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
@@ -263,6 +300,8 @@ gdn_status gdn_last_device_status(void *stream) {
     if (value & kDevTimeout) return fail(GDN_ERR_TIMEOUT, "a device-side wait timed out");
     if (value & kDevBadCuSeqlens)
         return fail(GDN_ERR_DEVICE_CHECK, "cu_seqlens is malformed on the device");
+    if (value & kDevBadSlot)
+        return fail(GDN_ERR_DEVICE_CHECK, "a slot index is outside the state pool");
     return GDN_OK;
 }
 

@@ -17,7 +17,7 @@
 namespace gdn {
 
 // Device check word values (OR-ed together by kernels that detect a problem).
-enum : int { kDevOk = 0, kDevBadCuSeqlens = 1, kDevTimeout = 2 };
+enum : int { kDevOk = 0, kDevBadCuSeqlens = 1, kDevTimeout = 2, kDevBadSlot = 4 };
 
 struct ScanParams {
     const void *q, *k, *v, *a, *b;
@@ -30,6 +30,8 @@ struct ScanParams {
     int32_t num_seqs, h_qk, h_v, d_k, d_v;
     float scale;
     int *status;                 // device check word
+    const int32_t *slots;        // device, may be null: sequence n's state is pool entry slots[n]
+    int64_t pool_size;           // entries of the state pool when slots is set
 };
 
 // ------------------------------------------------------------------ I/O types

@@ -50,8 +50,18 @@ __global__ void __launch_bounds__(kThreads) scan_simt_kernel(const ScanParams p)
 
     int64_t t0, t1;
     if (!seq_range(p, n, t0, t1)) return;
+    // A state pool: sequence n reads and writes entry slots[n]; a slot outside the pool
+    // skips the sequence and sets the check word.
+    int64_t ns = n;
+    if (p.slots != nullptr) {
+        ns = p.slots[n];
+        if (ns < 0 || ns >= p.pool_size) {
+            if (tid == 0) atomicOr(p.status, kDevBadSlot);
+            return;
+        }
+    }
 
-    const size_t sbase = ((size_t)n * p.h_v + h) * (size_t)p.d_k * p.d_v;
+    const size_t sbase = ((size_t)ns * p.h_v + h) * (size_t)p.d_k * p.d_v;
     float4 S[RPT];
 #pragma unroll
     for (int m = 0; m < RPT; ++m) {

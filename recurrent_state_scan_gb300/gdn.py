@@ -25,7 +25,7 @@ _DTYPE_CODE = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16, torch.float16: 
 # Every symbol include/gdn.h declares.
 EXPORTS = ("gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode_step",
            "gdn_prefill_plan", "gdn_last_device_status", "gdn_status_string",
-           "gdn_last_error_message", "gdn_prefill_noalloc")
+           "gdn_last_error_message", "gdn_prefill_noalloc", "gdn_decode_step_slots")
 PATH_SIMT, PATH_TC = 1, 2
 
 
@@ -66,6 +66,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.gdn_prefill.restype = ctypes.c_int
     lib.gdn_prefill.argtypes = [S, P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P,
                                 ctypes.c_size_t, P]
+    lib.gdn_decode_step_slots.restype = ctypes.c_int
+    lib.gdn_decode_step_slots.argtypes = [S, P, P, P, P, P, P, P, P, ctypes.c_int64, P,
+                                          ctypes.c_float, P, P]
     lib.gdn_prefill_noalloc.restype = ctypes.c_int
     lib.gdn_prefill_noalloc.argtypes = [S, P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P]
     lib.gdn_decode_step.restype = ctypes.c_int
@@ -280,3 +283,32 @@ def gdn_status_string(status: int) -> str:
 
 def default_scale(d_k: int) -> float:
     return 1.0 / math.sqrt(d_k)
+
+
+def gdn_decode_step_slots(q, k, v, a, b, A_log, dt_bias, pool, slots, scale: float = 0.0, *,
+                          o=None, stream=None):
+    """One token per sequence against a pool of states: sequence b reads and updates
+    ``pool[slots[b]]`` in place.  q, k [B,1,h_qk,d_k]; v [B,1,h_v,d_v]; a, b [B,1,h_v];
+    pool [P,h_v,d_k,d_v] fp32; slots int32 [B] on the device.  Returns o [B,1,h_v,d_v]."""
+    lib = load()
+    shape = _shape_of(q, v, None)
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v), ("a", a), ("b", b)):
+        _need_cuda(name, t, dt)
+    _need_cuda("A_log", A_log, torch.float32)
+    _need_cuda("dt_bias", dt_bias, torch.float32)
+    _need_cuda("pool", pool, torch.float32)
+    _need_cuda("slots", slots, torch.int32)
+    if pool.dim() != 4 or tuple(pool.shape[1:]) != (shape.h_v, shape.d_k, shape.d_v):
+        raise GdnError(GDN_ERR_INVALID_ARG, "pool must be [P, h_v, d_k, d_v]")
+    if tuple(slots.shape) != (shape.batch,):
+        raise GdnError(GDN_ERR_INVALID_ARG, "slots must be [B]")
+    if o is None:
+        o = torch.empty(v.shape, dtype=dt, device=v.device)
+    else:
+        _need_cuda("o", o, dt)
+    _check(lib.gdn_decode_step_slots(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a),
+                                     _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(pool),
+                                     int(pool.shape[0]), _ptr(slots), float(scale), _ptr(o),
+                                     _stream(stream)))
+    return o

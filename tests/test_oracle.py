@@ -311,10 +311,16 @@ def test_chunked_reassociation_matches_sequential(oracle_mod, C, L):
 
 
 def test_workload_recipe():
-    """The measured workloads' shapes and draws (c3's lengths are drawn first)."""
+    """The measured workloads' shapes and draws (c3's lengths are drawn first); the
+    slot-pool decode workload names distinct pool entries."""
     w = workloads.WORKLOADS
     assert set(w) == {"tiny_f32_prefill", "bf16_prefill_t4096", "bf16_decode_b256",
-                      "varlen_bf16_prefill", "gqa_f16_prefill"}
+                      "varlen_bf16_prefill", "gqa_f16_prefill", "bf16_slot_decode_b256"}
+    sp = w["bf16_slot_decode_b256"]
+    sl = workloads.draw(workloads.small_spec(io="bf16", batch=sp.batch, seqlen=1, h_qk=1, h_v=1,
+                                             d_k=4, d_v=4, decode=True, pool_size=sp.pool_size,
+                                             pool_std=0.05, seed=sp.seed)).slots.numpy()
+    assert len(set(sl.tolist())) == sp.batch and sl.min() >= 0 and sl.max() < sp.pool_size
     rng = np.random.default_rng(1003)
     lengths = rng.integers(512, 8193, 8)
     assert np.all((lengths >= 512) & (lengths <= 8192))
@@ -322,3 +328,85 @@ def test_workload_recipe():
                                               d_k=64, d_v=8))
     qn = np.linalg.norm(inp.f64["q"].reshape(-1, 64), axis=-1)
     assert np.all(np.abs(qn - 1.0) < 1e-2)   # unit norm up to the bf16 cast
+
+
+# ---------------------------------------------------------------- state pool (slots)
+
+def _pool_case(n=5, pool_size=9, seqlen=1, seed=3):
+    return workloads.draw(workloads.small_spec(io="f32", batch=n, seqlen=seqlen, h_qk=1, h_v=2,
+                                               d_k=16, d_v=8, decode=(seqlen == 1),
+                                               pool_size=pool_size, pool_std=0.05, seed=seed))
+
+
+def test_slot_scan_with_identity_slots_is_the_plain_scan(oracle_mod):
+    """take(pool, arange(n)) is the pool itself, so the slot op must equal the plain op
+    started from the pool (nuvec-core gated_delta_slots fallback: take, rule, put)."""
+    inp = _pool_case(n=4, pool_size=4)
+    f, s = inp.f64, inp.spec
+    o, pool = oracle_mod.slot_scan(inp.cu_seqlens, s.h_qk, s.h_v, s.d_k, s.d_v, f["q"], f["k"],
+                               f["v"], f["a"], f["b"], f["A_log"], f["dt_bias"], f["pool"],
+                               np.arange(4), scale=inp.scale)
+    o_ref, s_ref = oracle_mod.scan(inp.cu_seqlens, s.h_qk, s.h_v, s.d_k, s.d_v, f["q"], f["k"],
+                               f["v"], a=f["a"], b=f["b"], A_log=f["A_log"],
+                               dt_bias=f["dt_bias"], state_in=f["pool"], scale=inp.scale)
+    assert np.array_equal(o, o_ref) and np.array_equal(pool, s_ref)
+
+
+def test_slot_scan_leaves_unnamed_entries_and_commutes_with_a_pool_permutation(oracle_mod):
+    inp = _pool_case()
+    f, s = inp.f64, inp.spec
+    slots = inp.slots.numpy()
+    args = (inp.cu_seqlens, s.h_qk, s.h_v, s.d_k, s.d_v, f["q"], f["k"], f["v"], f["a"],
+            f["b"], f["A_log"], f["dt_bias"])
+    pool0 = f["pool"].reshape(9, s.h_v, s.d_k, s.d_v)
+    o, pool = oracle_mod.slot_scan(*args, pool0, slots, scale=inp.scale)
+    untouched = sorted(set(range(9)) - set(int(x) for x in slots))
+    assert untouched and np.array_equal(pool[untouched], pool0[untouched])
+    for x in slots:
+        assert not np.array_equal(pool[x], pool0[x])
+    # Relabel the pool entries with a permutation pi: entry e moves to pi[e].
+    pi = np.random.default_rng(5).permutation(9)
+    pool_p = np.empty_like(pool0)
+    pool_p[pi] = pool0
+    o_p, pool_pp = oracle_mod.slot_scan(*args, pool_p, pi[slots], scale=inp.scale)
+    assert np.array_equal(o_p, o)
+    assert np.array_equal(pool_pp[pi], pool)
+
+
+def test_slot_scan_skips_a_slot_outside_the_pool(oracle_mod):
+    inp = _pool_case()
+    f, s = inp.f64, inp.spec
+    slots = inp.slots.numpy().copy()
+    slots[2] = 9                                  # one past the end
+    o, pool = oracle_mod.slot_scan(inp.cu_seqlens, s.h_qk, s.h_v, s.d_k, s.d_v, f["q"], f["k"],
+                               f["v"], f["a"], f["b"], f["A_log"], f["dt_bias"], f["pool"],
+                               slots, scale=inp.scale)
+    pool0 = f["pool"].reshape(9, s.h_v, s.d_k, s.d_v)
+    assert np.all(o[2] == 0.0)
+    kept = [int(x) for i, x in enumerate(slots) if i != 2]
+    others = sorted(set(range(9)) - set(kept))
+    assert np.array_equal(pool[others], pool0[others])
+
+
+def test_slot_scan_over_several_steps_equals_single_steps(oracle_mod):
+    """The page's op runs T steps per row; T = 3 must equal three T = 1 slot steps that
+    each pick up the pool the previous one left (composition)."""
+    inp = _pool_case(n=3, pool_size=6, seqlen=3, seed=8)
+    f, s = inp.f64, inp.spec
+    slots = inp.slots.numpy()
+    o3, pool3 = oracle_mod.slot_scan(inp.cu_seqlens, s.h_qk, s.h_v, s.d_k, s.d_v, f["q"], f["k"],
+                                 f["v"], f["a"], f["b"], f["A_log"], f["dt_bias"], f["pool"],
+                                 slots, scale=inp.scale)
+    q = f["q"].reshape(3, 3, s.h_qk, s.d_k)
+    k = f["k"].reshape(3, 3, s.h_qk, s.d_k)
+    v = f["v"].reshape(3, 3, s.h_v, s.d_v)
+    a = f["a"].reshape(3, 3, s.h_v)
+    b = f["b"].reshape(3, 3, s.h_v)
+    pool = f["pool"]
+    cu1 = np.arange(4)
+    for t in range(3):
+        o1, pool = oracle_mod.slot_scan(cu1, s.h_qk, s.h_v, s.d_k, s.d_v, q[:, t], k[:, t], v[:, t],
+                                    a[:, t], b[:, t], f["A_log"], f["dt_bias"], pool, slots,
+                                    scale=inp.scale)
+        assert np.allclose(o1, o3.reshape(3, 3, s.h_v, s.d_v)[:, t], rtol=1e-12, atol=1e-14)
+    assert np.allclose(pool, pool3, rtol=1e-12, atol=1e-14)

@@ -44,6 +44,8 @@ class Spec:
     state_std: float = 0.0       # 0 -> zero initial state (state_in = None)
     decode: bool = False         # one token per sequence, state updated in place
     qk_scale: float = 1.0        # multiplies q,k after normalisation (tests only)
+    pool_size: int = 0           # > 0: states live in a pool of this many entries
+    pool_std: float = 0.0        # std of the pool entries
 
 
 # The five workloads the method is measured on.
@@ -63,6 +65,11 @@ WORKLOADS = {
     "gqa_f16_prefill": Spec(
         "gqa_f16_prefill", io="f16", batch=2, seqlen=8192, h_qk=16, h_v=32,
         d_k=128, d_v=128, seed=1004),
+    # Decode against a pool of 512 states, 256 sequences at distinct slots (the slot-pool
+    # decode row that follows the five above).
+    "bf16_slot_decode_b256": Spec(
+        "bf16_slot_decode_b256", io="bf16", batch=256, seqlen=1, h_qk=32, h_v=32,
+        d_k=128, d_v=128, seed=1005, decode=True, pool_size=512, pool_std=0.05),
 }
 
 
@@ -82,6 +89,8 @@ class Inputs:
     state_in: Optional[torch.Tensor]   # [n_seq, h_v, d_k, d_v] fp32 or None
     scale: float
     f64: dict
+    pool: Optional[torch.Tensor] = None    # [pool_size, h_v, d_k, d_v] fp32
+    slots: Optional[torch.Tensor] = None   # int32 [n_seq], distinct entries of the pool
 
     @property
     def n_seq(self) -> int:
@@ -141,6 +150,10 @@ def draw(spec: Spec) -> Inputs:
     state = None
     if spec.state_std > 0.0:
         state = rng.normal(0.0, spec.state_std, (n_seq, spec.h_v, spec.d_k, spec.d_v))
+    pool = slots = None
+    if spec.pool_size > 0:
+        pool = rng.normal(0.0, spec.pool_std, (spec.pool_size, spec.h_v, spec.d_k, spec.d_v))
+        slots = rng.permutation(spec.pool_size)[:n_seq].astype(np.int32)
 
     tq, tk, tv = _round(q, spec.io), _round(k, spec.io), _round(v, spec.io)
     ta, tb = _round(a, spec.io), _round(b, spec.io)
@@ -152,9 +165,14 @@ def draw(spec: Spec) -> Inputs:
         "A_log": _widen(tA), "dt_bias": _widen(tdt),
         "state_in": None if ts is None else _widen(ts),
     }
+    tp = tsl = None
+    if pool is not None:
+        tp = _round(pool, "f32")
+        tsl = torch.from_numpy(slots)
+        f64["pool"] = _widen(tp)
     return Inputs(spec=spec, cu_seqlens=cu, q=tq, k=tk, v=tv, a=ta, b=tb,
                   A_log=tA, dt_bias=tdt, state_in=ts,
-                  scale=1.0 / math.sqrt(spec.d_k), f64=f64)
+                  scale=1.0 / math.sqrt(spec.d_k), f64=f64, pool=tp, slots=tsl)
 
 
 def workload(name: str) -> Inputs:
@@ -163,9 +181,10 @@ def workload(name: str) -> Inputs:
 
 def small_spec(name="small", io="bf16", batch=1, seqlen=0, lengths=None, h_qk=2,
                h_v=2, d_k=128, d_v=128, seed=7, state_std=0.0, decode=False,
-               qk_scale=1.0) -> Spec:
+               qk_scale=1.0, pool_size=0, pool_std=0.0) -> Spec:
     """A test-sized workload with the same distributions as the measured ones."""
     return Spec(name=name, io=io, batch=batch, seqlen=seqlen,
                 lengths=None if lengths is None else tuple(int(x) for x in lengths),
                 h_qk=h_qk, h_v=h_v, d_k=d_k, d_v=d_v, seed=seed,
-                state_std=state_std, decode=decode, qk_scale=qk_scale)
+                state_std=state_std, decode=decode, qk_scale=qk_scale,
+                pool_size=pool_size, pool_std=pool_std)
