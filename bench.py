@@ -61,9 +61,15 @@ def io_bytes(inp) -> dict:
         "q": T * s.h_qk * s.d_k * es, "k": T * s.h_qk * s.d_k * es, "v": T * s.h_v * s.d_v * es,
         "a": T * s.h_v * es, "b": T * s.h_v * es, "params": 2 * s.h_v * 4,
         "state_in": st if (inp.state_in is not None or inp.pool is not None) else 0,
-        "o": T * s.h_v * s.d_v * es, "state_out": st,
+        "o": T * s.h_v * s.d_v * es, "state_out": st * (s.window if s.window else 1),
         "slots": 4 * n if inp.pool is not None else 0,
     }
+
+
+def bandwidth_metric(spec) -> bool:
+    """Decode-like steps (one token, or a short verify window of per-step states) are
+    measured in state GB/s on the token-sequential kernel; prefill in tokens/s."""
+    return bool(spec.decode or spec.window)
 
 
 def algorithmic_bytes(inp) -> int:
@@ -76,7 +82,7 @@ def algorithmic_flops(inp) -> float:
     q.k and k.k chunk products (4*C*d) counted once per q/k head.  Decode: 8*d_k*d_v."""
     s = inp.spec
     T = inp.total_tokens
-    if s.decode:
+    if bandwidth_metric(s):
         return 8.0 * T * s.h_v * s.d_k * s.d_v
     d = s.d_k
     return T * s.h_v * (6.0 * CHUNK * d + 6.0 * d * s.d_v) + T * s.h_qk * 4.0 * CHUNK * d
@@ -222,6 +228,8 @@ def time_oracle(inp, budget_s: float, min_reps: int = 1):
     while True:
         if inp.pool is not None:
             oracle.slot_scan_inputs(inp, threads=threads)
+        elif inp.spec.window:
+            oracle.window_scan_inputs(inp, threads=threads)
         else:
             oracle.scan_inputs(inp, threads=threads)
         reps += 1
@@ -240,7 +248,7 @@ def units_per_step(inp):
 def cpu_baseline_line(inp, budget_s=10.0):
     per, reps, threads = time_oracle(inp, budget_s)
     s = inp.spec
-    if s.decode:
+    if bandwidth_metric(s):
         val, unit = algorithmic_bytes(inp) / per / 1e9, "GB/s"
     else:
         val, unit = units_per_step(inp) / per, "tokens/s"
@@ -253,7 +261,7 @@ def cpu_baseline_line(inp, budget_s=10.0):
 
 def run_ours(args, rank, world, local):
     from recurrent_state_scan_gb300 import (gdn_decode_step, gdn_decode_step_slots, gdn_prefill,
-                                            load)
+                                            gdn_scan_window, load)
     load()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -270,14 +278,21 @@ def run_ours(args, rank, world, local):
     pool = None if inp.pool is None else inp.pool.to(dev)
     slots = None if inp.slots is None else inp.slots.to(dev)
     from recurrent_state_scan_gb300 import gdn
-    ws_need = 0 if s.decode else gdn.gdn_prefill_workspace_bytes(
+    window = None
+    if s.window:
+        window = torch.empty((s.window,) + n_state, dtype=torch.float32, device=dev)
+    ws_need = 0 if (s.decode or s.window) else gdn.gdn_prefill_workspace_bytes(
         gdn.shape_of_spec(s, inp.n_seq, inp.total_tokens))
     ws = torch.empty(ws_need, dtype=torch.uint8, device=dev) if ws_need else None
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        if pool is not None:
+        if window is not None:
+            gdn_scan_window(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"], t["dt_bias"],
+                            state0, inp.scale, window_len=s.window, o=o, window=window,
+                            stream=stream)
+        elif pool is not None:
             gdn_decode_step_slots(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"],
                                   t["dt_bias"], pool, slots, inp.scale, o=o, stream=stream)
         elif s.decode:
@@ -318,7 +333,8 @@ def run_ours(args, rank, world, local):
                 ([("state", inp.state_in)] if inp.state_in is not None else []) +
                 ([("slots", inp.slots)] if inp.slots is not None else [])}
         o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-        s_host = torch.empty(n_state, dtype=torch.float32).pin_memory()
+        s_host = torch.empty(((s.window,) if s.window else ()) + n_state,
+                             dtype=torch.float32).pin_memory()
         dbuf = {n: torch.empty_like(v, device=dev) for n, v in host.items()}
         h2d = sum(v.numel() * v.element_size() for v in host.values())
         # With a resident pool only o comes back; otherwise o and the state.
@@ -327,7 +343,12 @@ def run_ours(args, rank, world, local):
         def e2e_step():
             for n, v in host.items():
                 dbuf[n].copy_(v, non_blocking=True)
-            if pool is not None:
+            if window is not None:
+                gdn_scan_window(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["a"], dbuf["b"],
+                                dbuf["A_log"], dbuf["dt_bias"], dbuf.get("state"), inp.scale,
+                                window_len=s.window, o=o, window=window, stream=stream)
+                s_host.copy_(window, non_blocking=True)
+            elif pool is not None:
                 gdn_decode_step_slots(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["a"], dbuf["b"],
                                       dbuf["A_log"], dbuf["dt_bias"], pool, dbuf["slots"],
                                       inp.scale, o=o, stream=stream)
@@ -375,7 +396,7 @@ def main():
         for _ in range(args.warmup):
             time_oracle(inp, 0.0)
         per, reps, threads = time_oracle(inp, 0.0, min_reps=args.steps)
-        if s.decode:
+        if bandwidth_metric(s):
             value, unit = algorithmic_bytes(inp) / per / 1e9, "GB/s"
         else:
             value, unit = inp.total_tokens / per, "tokens/s"
@@ -399,7 +420,7 @@ def main():
     nbytes = algorithmic_bytes(inp)
     flops = algorithmic_flops(inp)
     sec = ms / 1e3
-    if s.decode:
+    if bandwidth_metric(s):
         value, unit = world * nbytes / sec / 1e9, "GB/s"
     else:
         value, unit = world * inp.total_tokens / sec, "tokens/s"
@@ -411,11 +432,11 @@ def main():
     t_tc = flops / (pk["bf16_tflops"] * 1e12)
     roof = {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
             "frac": gbs / pk["hbm_gbs"],
-            "traffic": profiled_traffic(inp_name, "decode" if s.decode else "prefill"),
+            "traffic": profiled_traffic(inp_name, "decode" if bandwidth_metric(s) else "prefill"),
             "peak_source": f"{pk_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"
             if pk_kind == "measured" else "fallback 6.8 TB/s",
-            "kernels": "gdn_decode (scan_simt)" if s.decode else "gdn_chunk_prep + gdn_chunk_scan, one call"}
-    if not s.decode:
+            "kernels": "gdn_decode (scan_simt)" if bandwidth_metric(s) else "gdn_chunk_prep + gdn_chunk_scan, one call"}
+    if not bandwidth_metric(s):
         roof["tensor_tflops"] = tfs
         roof["tensor_frac_of_bf16_peak"] = tfs / pk["bf16_tflops"]
         roof["roofline_time_us"] = max(t_hbm, t_tc) * 1e6
@@ -429,7 +450,7 @@ def main():
     }
     if e2e is not None:
         esec = e2e["ms_per_step"] / 1e3
-        ev = world * (nbytes / esec / 1e9 if s.decode else inp.total_tokens / esec)
+        ev = world * (nbytes / esec / 1e9 if bandwidth_metric(s) else inp.total_tokens / esec)
         line["e2e"] = {"value": ev, "unit": unit, "ms_per_step": e2e["ms_per_step"],
                        "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
                        "d2h_bytes_per_step": e2e["d2h_bytes_per_step"]}

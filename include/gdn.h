@@ -173,6 +173,27 @@ gdn_status gdn_decode_step_slots(const gdn_shape *shape, const void *q, const vo
                                  const int32_t *slots, float scale, void *o, void *stream);
 
 /*
+ * gdn_scan_window -- run B sequences of T tokens each (shape->batch = num_seqs = B,
+ * shape->seqlen = T, no cu_seqlens) and emit, instead of the final state, the states
+ * after each of the last `window_len` steps: window[w] for w < window_len is the state
+ * after step T - window_len + w; when T < window_len the first window_len - T slabs are
+ * zero (the `state_window` output of the onnxruntime-ep-mlx ssm.rs page,
+ * LinearAttention; with window_len = T this is every step's state, the
+ * `gated_delta_steps` output of the nuvec-core page).  Meant for speculative decoding:
+ * run the T draft tokens, then restore the state after the last accepted one.
+ *
+ *   window      DEVICE fp32 [window_len, B, h_v, d_k, d_v], 16-byte aligned, written
+ *               in full.
+ *   window_len  >= 1.
+ *   the rest    as gdn_prefill (state_in may be NULL for zeros).
+ * Runs the token-sequential path for every shape and I/O type.
+ */
+gdn_status gdn_scan_window(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                           const void *a, const void *b, const float *A_log, const float *dt_bias,
+                           const float *state_in, float scale, void *o, float *window,
+                           int32_t window_len, void *stream);
+
+/*
  * gdn_last_device_status -- synchronise `stream`, read the device check word
  * set by any earlier call on the current device, clear it, and return GDN_OK or
  * GDN_ERR_DEVICE_CHECK (malformed cu_seqlens, or a slot outside the pool) /

@@ -169,3 +169,44 @@ def slot_scan_inputs(inp, threads: int = 1):
     return slot_scan(inp.cu_seqlens, s.h_qk, s.h_v, s.d_k, s.d_v, f["q"], f["k"], f["v"],
                      f["a"], f["b"], f["A_log"], f["dt_bias"], f["pool"], inp.slots.numpy(),
                      scale=inp.scale, threads=threads)
+
+
+def window_scan(batch: int, seqlen: int, h_qk: int, h_v: int, d_k: int, d_v: int, q, k, v,
+                a, b, A_log, dt_bias, state_in, window_len: int, scale: Optional[float] = None,
+                threads: int = 1):
+    """The recurrence over B sequences of T tokens, keeping the states after the last
+    `window_len` steps (onnxruntime-ep-mlx ssm.rs, LinearAttention `state_window`: the
+    last min(T, W) step states in time order, after W - min(T, W) zero slabs).  Each step
+    is one call of `scan` on a single token, chained through its state.
+
+    Returns (o [B*T, h_v, d_v], window [W, B, h_v, d_k, d_v]) in float64.
+    """
+    B, T, W = int(batch), int(seqlen), int(window_len)
+    q = _f64(q).reshape(B, T, h_qk, d_k)
+    k = _f64(k).reshape(B, T, h_qk, d_k)
+    v = _f64(v).reshape(B, T, h_v, d_v)
+    a = _f64(a).reshape(B, T, h_v)
+    b = _f64(b).reshape(B, T, h_v)
+    state = (np.zeros((B, h_v, d_k, d_v)) if state_in is None
+             else _f64(state_in).reshape(B, h_v, d_k, d_v).copy())
+    o = np.zeros((B, T, h_v, d_v))
+    window = np.zeros((W, B, h_v, d_k, d_v))
+    cu1 = np.arange(B + 1)
+    for t in range(T):
+        o_t, state = scan(cu1, h_qk, h_v, d_k, d_v, q[:, t], k[:, t], v[:, t], a=a[:, t],
+                          b=b[:, t], A_log=A_log, dt_bias=dt_bias, state_in=state, scale=scale,
+                          threads=threads)
+        o[:, t] = o_t
+        w = W - (T - t)
+        if w >= 0:
+            window[w] = state
+    return o.reshape(B * T, h_v, d_v), window
+
+
+def window_scan_inputs(inp, threads: int = 1):
+    """window_scan on a drawn ``workloads.Inputs`` whose spec sets a window."""
+    s = inp.spec
+    f = inp.f64
+    return window_scan(s.batch, s.seqlen, s.h_qk, s.h_v, s.d_k, s.d_v, f["q"], f["k"], f["v"],
+                       f["a"], f["b"], f["A_log"], f["dt_bias"], f["state_in"], s.window,
+                       scale=inp.scale, threads=threads)

@@ -285,6 +285,42 @@ gdn_status gdn_decode_step_slots(const gdn_shape *shape, const void *q, const vo
     return GDN_OK;
 }
 
+gdn_status gdn_scan_window(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                           const void *a, const void *b, const float *A_log, const float *dt_bias,
+                           const float *state_in, float scale, void *o, float *window,
+                           int32_t window_len, void *stream) {
+    gdn_status st = check_shape(shape, false);
+    if (st != GDN_OK) return st;
+    const int64_t tokens = shape->seqlen * (int64_t)shape->batch;
+    st = check_inputs(shape, tokens, q, k, v, a, b, A_log, dt_bias, o);
+    if (st != GDN_OK) return st;
+    if (window_len < 1) return fail(GDN_ERR_INVALID_ARG, "window_len %d < 1", window_len);
+    if (shape->batch == 0) return GDN_OK;
+    if (window == nullptr) return fail(GDN_ERR_INVALID_ARG, "window is NULL");
+    if (!aligned(window, 16) || !aligned(state_in, 16))
+        return fail(GDN_ERR_INVALID_ARG, "state_in and window must be 16-byte aligned");
+    if (!(scale == scale) || isinf(scale)) return fail(GDN_ERR_INVALID_ARG, "scale is not finite");
+    int *word = nullptr;
+    st = status_word(&word);
+    if (st != GDN_OK) return st;
+
+    ScanParams p{};
+    p.q = q; p.k = k; p.v = v; p.a = a; p.b = b;
+    p.A_log = A_log; p.dt_bias = dt_bias;
+    p.state_in = state_in; p.state_out = nullptr; p.o = o;
+    p.cu_seqlens = nullptr;
+    p.seqlen = shape->seqlen;
+    p.num_seqs = shape->batch;
+    p.h_qk = shape->h_qk; p.h_v = shape->h_v; p.d_k = shape->d_k; p.d_v = shape->d_v;
+    p.scale = scale == 0.0f ? 1.0f / sqrtf((float)shape->d_k) : scale;
+    p.status = word;
+    p.window = window;
+    p.window_len = window_len;
+    cudaError_t e = launch_scan_simt(p, (gdn_dtype)shape->io_dtype, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "window scan launch");
+    return GDN_OK;
+}
+
 gdn_status gdn_last_device_status(void *stream) {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");

@@ -32,6 +32,8 @@ struct ScanParams {
     int *status;                 // device check word
     const int32_t *slots;        // device, may be null: sequence n's state is pool entry slots[n]
     int64_t pool_size;           // entries of the state pool when slots is set
+    float *window;               // may be null: [window_len, N, h_v, d_k, d_v], the states after
+    int32_t window_len;          //   the last window_len steps (leading slabs zero when T is shorter)
 };
 
 // ------------------------------------------------------------------ I/O types

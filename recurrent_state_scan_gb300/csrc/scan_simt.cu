@@ -72,6 +72,16 @@ __global__ void __launch_bounds__(kThreads) scan_simt_kernel(const ScanParams p)
                                                           (size_t)i * p.d_v + col0));
     }
 
+    // This thread's rows and columns of slab w of the state window.
+    auto store_slab = [&](int64_t w, const float4 (&X)[RPT]) {
+        float *base = p.window + (((size_t)w * p.num_seqs + n) * p.h_v + h) * (size_t)p.d_k * p.d_v;
+#pragma unroll
+        for (int m = 0; m < RPT; ++m) {
+            const int i = rg + RPP * m;
+            if (col_ok && i < p.d_k) __stcs(reinterpret_cast<float4 *>(base + (size_t)i * p.d_v + col0), X[m]);
+        }
+    };
+
     const IO *q = static_cast<const IO *>(p.q);
     const IO *k = static_cast<const IO *>(p.k);
     const IO *v = static_cast<const IO *>(p.v);
@@ -146,8 +156,19 @@ __global__ void __launch_bounds__(kThreads) scan_simt_kernel(const ScanParams p)
             S[m].z = fmaf(alpha, S[m].z, kk * d4.z);
             S[m].w = fmaf(alpha, S[m].w, kk * d4.w);
         }
+        // One of the last window_len steps: its state goes to slab window_len - (t1 - t).
+        if (p.window != nullptr && t1 - t <= p.window_len)
+            store_slab(p.window_len - (t1 - t), S);
+    }
+    // Fewer steps than slabs: the leading slabs are zero.
+    if (p.window != nullptr) {
+        float4 Z[RPT];
+#pragma unroll
+        for (int m = 0; m < RPT; ++m) Z[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int64_t w = 0; w < (int64_t)p.window_len - (t1 - t0); ++w) store_slab(w, Z);
     }
 
+    if (p.state_out == nullptr) return;
 #pragma unroll
     for (int m = 0; m < RPT; ++m) {
         const int i = rg + RPP * m;

@@ -25,7 +25,8 @@ _DTYPE_CODE = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16, torch.float16: 
 # Every symbol include/gdn.h declares.
 EXPORTS = ("gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode_step",
            "gdn_prefill_plan", "gdn_last_device_status", "gdn_status_string",
-           "gdn_last_error_message", "gdn_prefill_noalloc", "gdn_decode_step_slots")
+           "gdn_last_error_message", "gdn_prefill_noalloc", "gdn_decode_step_slots",
+           "gdn_scan_window")
 PATH_SIMT, PATH_TC = 1, 2
 
 
@@ -66,6 +67,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.gdn_prefill.restype = ctypes.c_int
     lib.gdn_prefill.argtypes = [S, P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P,
                                 ctypes.c_size_t, P]
+    lib.gdn_scan_window.restype = ctypes.c_int
+    lib.gdn_scan_window.argtypes = [S, P, P, P, P, P, P, P, P, ctypes.c_float, P, P,
+                                    ctypes.c_int32, P]
     lib.gdn_decode_step_slots.restype = ctypes.c_int
     lib.gdn_decode_step_slots.argtypes = [S, P, P, P, P, P, P, P, P, ctypes.c_int64, P,
                                           ctypes.c_float, P, P]
@@ -259,14 +263,14 @@ def shape_of_spec(spec, n_seq: int, total_tokens: int) -> GdnShape:
 
 
 def launches_per_call(spec, n_seq: int = 0, total_tokens: int = 0) -> int:
-    if spec.decode:
+    if spec.decode or getattr(spec, "window", 0):
         return 1
     return gdn_prefill_plan(shape_of_spec(spec, n_seq, total_tokens))[1]
 
 
 def path_dtype(spec, n_seq: int = 0, total_tokens: int = 0) -> str:
     """Arithmetic type of the path: MMA operand type on the tensor-core path, else f32."""
-    if spec.decode:
+    if spec.decode or getattr(spec, "window", 0):
         return "f32"
     path = gdn_prefill_plan(shape_of_spec(spec, n_seq, total_tokens))[0]
     return spec.io if path == PATH_TC else "f32"
@@ -312,3 +316,35 @@ def gdn_decode_step_slots(q, k, v, a, b, A_log, dt_bias, pool, slots, scale: flo
                                      int(pool.shape[0]), _ptr(slots), float(scale), _ptr(o),
                                      _stream(stream)))
     return o
+
+
+def gdn_scan_window(q, k, v, a, b, A_log, dt_bias, state_in=None, scale: float = 0.0, *,
+                    window_len: int, o=None, window=None, stream=None):
+    """Run B sequences of T tokens and return (o, window): window[w] is the state after
+    step T - window_len + w, with zero slabs first when T < window_len.
+    q, k [B,T,h_qk,d_k]; v [B,T,h_v,d_v]; a, b [B,T,h_v]; state_in [B,h_v,d_k,d_v] or None;
+    window [window_len, B, h_v, d_k, d_v] fp32."""
+    lib = load()
+    shape = _shape_of(q, v, None)
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v), ("a", a), ("b", b)):
+        _need_cuda(name, t, dt)
+    _need_cuda("A_log", A_log, torch.float32)
+    _need_cuda("dt_bias", dt_bias, torch.float32)
+    st_shape = (shape.batch, shape.h_v, shape.d_k, shape.d_v)
+    if state_in is not None:
+        _need_cuda("state_in", state_in, torch.float32)
+        if tuple(state_in.shape) != st_shape:
+            raise GdnError(GDN_ERR_INVALID_ARG, f"state_in must be {st_shape}")
+    if o is None:
+        o = torch.empty(v.shape, dtype=dt, device=v.device)
+    else:
+        _need_cuda("o", o, dt)
+    if window is None:
+        window = torch.empty((int(window_len),) + st_shape, dtype=torch.float32, device=v.device)
+    else:
+        _need_cuda("window", window, torch.float32)
+    _check(lib.gdn_scan_window(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b),
+                               _ptr(A_log), _ptr(dt_bias), _ptr(state_in), float(scale), _ptr(o),
+                               _ptr(window), int(window_len), _stream(stream)))
+    return o, window

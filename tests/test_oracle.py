@@ -315,7 +315,8 @@ def test_workload_recipe():
     slot-pool decode workload names distinct pool entries."""
     w = workloads.WORKLOADS
     assert set(w) == {"tiny_f32_prefill", "bf16_prefill_t4096", "bf16_decode_b256",
-                      "varlen_bf16_prefill", "gqa_f16_prefill", "bf16_slot_decode_b256"}
+                      "varlen_bf16_prefill", "gqa_f16_prefill", "bf16_slot_decode_b256",
+                      "bf16_window_b256_t4"}
     sp = w["bf16_slot_decode_b256"]
     sl = workloads.draw(workloads.small_spec(io="bf16", batch=sp.batch, seqlen=1, h_qk=1, h_v=1,
                                              d_k=4, d_v=4, decode=True, pool_size=sp.pool_size,
@@ -410,3 +411,50 @@ def test_slot_scan_over_several_steps_equals_single_steps(oracle_mod):
                                     scale=inp.scale)
         assert np.allclose(o1, o3.reshape(3, 3, s.h_v, s.d_v)[:, t], rtol=1e-12, atol=1e-14)
     assert np.allclose(pool, pool3, rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------- state window
+
+def _window_case(B=2, T=5, seed=9):
+    return workloads.draw(workloads.small_spec(io="f32", batch=B, seqlen=T, h_qk=1, h_v=2,
+                                               d_k=16, d_v=8, state_std=0.05, seed=seed))
+
+
+def _window(oracle_mod, inp, W):
+    s, f = inp.spec, inp.f64
+    return oracle_mod.window_scan(s.batch, s.seqlen, s.h_qk, s.h_v, s.d_k, s.d_v, f["q"], f["k"],
+                                  f["v"], f["a"], f["b"], f["A_log"], f["dt_bias"],
+                                  f["state_in"], W, scale=inp.scale)
+
+
+def test_window_last_slab_is_the_final_state_and_outputs_agree(oracle_mod):
+    inp = _window_case()
+    o_ref, s_ref = oracle_mod.scan_inputs(inp)
+    o, win = _window(oracle_mod, inp, 1)
+    assert np.array_equal(win[0], s_ref)
+    assert np.array_equal(o, o_ref.reshape(o.shape))
+
+
+def test_window_slabs_are_the_states_of_shorter_runs(oracle_mod):
+    """window[W-1-j] is the final state of the same run stopped j steps early."""
+    inp = _window_case(T=6)
+    o, win = _window(oracle_mod, inp, 4)
+    s, f = inp.spec, inp.f64
+    for j in range(4):
+        L = s.seqlen - j
+        sub = lambda x, last: x.reshape(s.batch, s.seqlen, *last)[:, :L].reshape(-1)
+        _, s_short = oracle_mod.scan(np.arange(s.batch + 1) * L, s.h_qk, s.h_v, s.d_k, s.d_v,
+                                     sub(f["q"], (s.h_qk, s.d_k)), sub(f["k"], (s.h_qk, s.d_k)),
+                                     sub(f["v"], (s.h_v, s.d_v)), a=sub(f["a"], (s.h_v,)),
+                                     b=sub(f["b"], (s.h_v,)), A_log=f["A_log"],
+                                     dt_bias=f["dt_bias"], state_in=f["state_in"], scale=inp.scale)
+        assert np.allclose(win[3 - j], s_short, rtol=1e-12, atol=1e-15)
+
+
+def test_window_longer_than_the_run_starts_with_zero_slabs(oracle_mod):
+    inp = _window_case(T=3)
+    _, win = _window(oracle_mod, inp, 5)
+    assert np.all(win[:2] == 0.0)
+    _, s_ref = oracle_mod.scan_inputs(inp)
+    assert np.array_equal(win[4], s_ref)
+    assert np.all(np.any(win[2:] != 0.0, axis=(1, 2, 3, 4)))

@@ -46,6 +46,7 @@ class Spec:
     qk_scale: float = 1.0        # multiplies q,k after normalisation (tests only)
     pool_size: int = 0           # > 0: states live in a pool of this many entries
     pool_std: float = 0.0        # std of the pool entries
+    window: int = 0              # > 0: emit the states after the last `window` steps
 
 
 # The five workloads the method is measured on.
@@ -70,6 +71,11 @@ WORKLOADS = {
     "bf16_slot_decode_b256": Spec(
         "bf16_slot_decode_b256", io="bf16", batch=256, seqlen=1, h_qk=32, h_v=32,
         d_k=128, d_v=128, seed=1005, decode=True, pool_size=512, pool_std=0.05),
+    # Speculative verify: 4 draft tokens for each of 256 sequences, emitting the state
+    # after every step (the per-step-state row).
+    "bf16_window_b256_t4": Spec(
+        "bf16_window_b256_t4", io="bf16", batch=256, seqlen=4, h_qk=32, h_v=32,
+        d_k=128, d_v=128, seed=1006, state_std=0.05, window=4),
 }
 
 
@@ -181,10 +187,10 @@ def workload(name: str) -> Inputs:
 
 def small_spec(name="small", io="bf16", batch=1, seqlen=0, lengths=None, h_qk=2,
                h_v=2, d_k=128, d_v=128, seed=7, state_std=0.0, decode=False,
-               qk_scale=1.0, pool_size=0, pool_std=0.0) -> Spec:
+               qk_scale=1.0, pool_size=0, pool_std=0.0, window=0) -> Spec:
     """A test-sized workload with the same distributions as the measured ones."""
     return Spec(name=name, io=io, batch=batch, seqlen=seqlen,
                 lengths=None if lengths is None else tuple(int(x) for x in lengths),
                 h_qk=h_qk, h_v=h_v, d_k=d_k, d_v=d_v, seed=seed,
                 state_std=state_std, decode=decode, qk_scale=qk_scale,
-                pool_size=pool_size, pool_std=pool_std)
+                pool_size=pool_size, pool_std=pool_std, window=window)
