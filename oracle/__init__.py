@@ -52,6 +52,12 @@ def _load():
             ctypes.c_int64, I64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
             ctypes.c_int32, D, D, D, D, D, D, D, D, D, D, ctypes.c_double,
             ctypes.c_int32, I64, ctypes.c_int64, ctypes.c_int32, D, D]
+        lib.gdn_ref_scan_ex.restype = ctypes.c_int
+        lib.gdn_ref_scan_ex.argtypes = [
+            ctypes.c_int64, I64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+            ctypes.c_int32, D, D, D, D, D, D, D, D, D, D, ctypes.c_double,
+            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, I64, ctypes.c_int64, ctypes.c_int32,
+            D, D]
         for name in ("gdn_ref_softplus", "gdn_ref_sigmoid"):
             getattr(lib, name).restype = ctypes.c_double
             getattr(lib, name).argtypes = [ctypes.c_double]
@@ -89,7 +95,8 @@ def decay(a: float, A_log: float, dt_bias: float) -> float:
 def scan(cu_seqlens: Sequence[int], h_qk: int, h_v: int, d_k: int, d_v: int,
          q, k, v, a=None, b=None, A_log=None, dt_bias=None, g=None, beta=None,
          state_in=None, scale: Optional[float] = None, rule: str = "gated_delta",
-         units: Optional[Sequence[int]] = None, threads: int = 1):
+         units: Optional[Sequence[int]] = None, threads: int = 1,
+         decay_per_key: bool = False, beta_shared: bool = False):
     """Run the recurrence over packed tokens.
 
     q, k: [T_total, h_qk, d_k]; v: [T_total, h_v, d_v]; a, b, g, beta: [T_total, h_v];
@@ -97,6 +104,9 @@ def scan(cu_seqlens: Sequence[int], h_qk: int, h_v: int, d_k: int, d_v: int,
     If ``a`` is None the gates are ``g`` (log-space, None = 0) and ``beta``
     (None = 1).  ``scale`` None means 1/sqrt(d_k).  ``units`` restricts the run
     to the listed (n * h_v + h) units; other rows of the outputs stay zero.
+    ``decay_per_key``: a (or g) is [T_total, h_v, d_k] and A_log, dt_bias are
+    [h_v, d_k] -- row i of the state decays by its own factor.  ``beta_shared``: b
+    (or beta) is [T_total], one beta for all heads.
     Returns (o [T_total, h_v, d_v], state_out [n_seq, h_v, d_k, d_v]) in float64.
     """
     lib = _load()
@@ -113,13 +123,14 @@ def scan(cu_seqlens: Sequence[int], h_qk: int, h_v: int, d_k: int, d_v: int,
     o = np.zeros(total * h_v * d_v, dtype=np.float64)
     s_out = np.zeros(max(n_seq, 0) * h_v * d_k * d_v, dtype=np.float64)
     ulist = None if units is None else np.ascontiguousarray(np.asarray(units, dtype=np.int64))
-    rc = lib.gdn_ref_scan(
+    rc = lib.gdn_ref_scan_ex(
         n_seq, _ptr(cu, ctypes.c_int64), h_qk, h_v, d_k, d_v, _ptr(q), _ptr(k), _ptr(v),
         _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(g), _ptr(beta), _ptr(state_in),
-        float(scale), RULES[rule], _ptr(ulist, ctypes.c_int64),
-        0 if ulist is None else len(ulist), int(threads), _ptr(o), _ptr(s_out))
+        float(scale), RULES[rule], int(bool(decay_per_key)), int(bool(beta_shared)),
+        _ptr(ulist, ctypes.c_int64), 0 if ulist is None else len(ulist), int(threads), _ptr(o),
+        _ptr(s_out))
     if rc != 0:
-        raise ValueError(f"gdn_ref_scan failed with code {rc}")
+        raise ValueError(f"gdn_ref_scan_ex failed with code {rc}")
     return o.reshape(total, h_v, d_v), s_out.reshape(max(n_seq, 0), h_v, d_k, d_v)
 
 

@@ -26,6 +26,9 @@
  *    runs and the present state equals the past state.
  *  - nuvec-core 0.6.1, src/fast/imp.rs, `gated_delta_graph`: the same four steps
  *    written with whole-array operations (a cross-check of the step order).
+ *  - The CUDA page's gate variants: Step 1 with `decay_per_key_dim` (one decay per
+ *    key dimension, S[i,:] *= exp(g_i), with A_log and dt_bias per (head, key dim))
+ *    and a beta shared by all heads (`beta_per_head` false, beta [B, T, 1]).
  *
  * Readings where the pages are silent (each is listed in the design notes):
  *  - `scale` multiplies the finished fp64 dot product q^T S (post-multiply).
@@ -65,6 +68,8 @@ typedef struct {
     double scale;
     int32_t rule;
     double *o, *state_out;
+    int32_t decay_per_key;   /* a / g_in [T, h_v, d_k]; A_log, dt_bias [h_v, d_k] */
+    int32_t beta_shared;     /* b / beta_in [T] (one beta for every head) */
 } job_t;
 
 /* One (sequence n, value head h): the recurrence over its tokens, in order. */
@@ -87,19 +92,28 @@ static void run_unit(const job_t *J, int64_t n, int32_t h, double *S, double *r)
         const double *vt = J->v + ((size_t)t * J->h_v + h) * dv;
         double *ot = J->o + ((size_t)t * J->h_v + h) * dv;
         const size_t gi = (size_t)t * J->h_v + h;
-        double g, beta;
+        const size_t bi = J->beta_shared ? (size_t)t : gi;
+        double g = 0.0, beta;
         if (J->a) {
-            g = gdn_ref_decay(J->a[gi], J->A_log[h], J->dt_bias[h]);
-            beta = gdn_ref_sigmoid(J->b[gi]);
+            if (!J->decay_per_key) g = gdn_ref_decay(J->a[gi], J->A_log[h], J->dt_bias[h]);
+            beta = gdn_ref_sigmoid(J->b[bi]);
         } else {
-            g = J->g_in ? J->g_in[gi] : 0.0;
-            beta = J->beta_in ? J->beta_in[gi] : 1.0;
+            if (!J->decay_per_key) g = J->g_in ? J->g_in[gi] : 0.0;
+            beta = J->beta_in ? J->beta_in[bi] : 1.0;
         }
 
-        /* Step 1: decay. */
-        if (has_decay) {
+        /* Step 1: decay, one factor per head or one per key dimension (row i of S). */
+        if (has_decay && !J->decay_per_key) {
             const double alpha = exp(g);
             for (size_t e = 0; e < sz; ++e) S[e] *= alpha;
+        } else if (has_decay) {
+            for (int32_t i = 0; i < dk; ++i) {
+                const size_t ki = gi * dk + i, hk = (size_t)h * dk + i;
+                const double gk = J->a ? gdn_ref_decay(J->a[ki], J->A_log[hk], J->dt_bias[hk])
+                                       : (J->g_in ? J->g_in[ki] : 0.0);
+                const double alpha = exp(gk);
+                for (int32_t j = 0; j < dv; ++j) S[(size_t)i * dv + j] *= alpha;
+            }
         }
         if (has_delta) {
             /* Step 2: retrieval r_j = sum_i S_ij k_i, left to right over i. */
@@ -147,7 +161,7 @@ static void *worker(void *arg) {
 }
 
 /*
- * gdn_ref_scan: the recurrence for every (sequence, value head), or for the
+ * gdn_ref_scan_ex: the recurrence for every (sequence, value head), or for the
  * listed subset of them.
  *
  *   cu         [n_seq+1] token offsets of each sequence in the packed axis
@@ -158,18 +172,22 @@ static void *worker(void *arg) {
  *   A_log, dt_bias [h_v]
  *   state_in   [n_seq, h_v, d_k, d_v] or NULL (zeros)
  *   rule       0 gated_delta, 1 delta, 2 gated, 3 linear
+ *   decay_per_key  a (or g_in) is [T_total, h_v, d_k] and A_log, dt_bias are
+ *              [h_v, d_k]: row i of S decays by its own factor
+ *   beta_shared    b (or beta_in) is [T_total]: one beta for every head
  *   units      NULL for all n_seq*h_v units, else n_units ids (n*h_v + h);
  *              only those units' o rows and states are written
  *   o          [T_total, h_v, d_v];  state_out [n_seq, h_v, d_k, d_v]
  * Returns 0, or a negative code for bad arguments / allocation failure.
  */
-int gdn_ref_scan(int64_t n_seq, const int64_t *cu, int32_t h_qk, int32_t h_v,
-                 int32_t d_k, int32_t d_v, const double *q, const double *k,
-                 const double *v, const double *a, const double *b,
-                 const double *A_log, const double *dt_bias, const double *g_in,
-                 const double *beta_in, const double *state_in, double scale,
-                 int32_t rule, const int64_t *units, int64_t n_units,
-                 int32_t n_threads, double *o, double *state_out) {
+int gdn_ref_scan_ex(int64_t n_seq, const int64_t *cu, int32_t h_qk, int32_t h_v,
+                    int32_t d_k, int32_t d_v, const double *q, const double *k,
+                    const double *v, const double *a, const double *b,
+                    const double *A_log, const double *dt_bias, const double *g_in,
+                    const double *beta_in, const double *state_in, double scale,
+                    int32_t rule, int32_t decay_per_key, int32_t beta_shared,
+                    const int64_t *units, int64_t n_units, int32_t n_threads, double *o,
+                    double *state_out) {
     if (n_seq < 0 || !cu || h_qk <= 0 || h_v <= 0 || h_v % h_qk != 0 || d_k <= 0 ||
         d_v <= 0 || rule < 0 || rule > 3 || !o || !state_out)
         return -1;
@@ -177,7 +195,8 @@ int gdn_ref_scan(int64_t n_seq, const int64_t *cu, int32_t h_qk, int32_t h_v,
     for (int64_t n = 0; n < n_seq; ++n)
         if (cu[n + 1] < cu[n]) return -1;
     job_t J = {n_seq, cu, h_qk, h_v, d_k, d_v, q, k, v, a, b, A_log, dt_bias,
-               g_in, beta_in, state_in, scale, rule, o, state_out};
+               g_in, beta_in, state_in, scale, rule, o, state_out, decay_per_key != 0,
+               beta_shared != 0};
     const int64_t total = units ? n_units : n_seq * (int64_t)h_v;
     if (n_threads < 1) n_threads = 1;
     if (n_threads > 256) n_threads = 256;
@@ -201,4 +220,17 @@ int gdn_ref_scan(int64_t n_seq, const int64_t *cu, int32_t h_qk, int32_t h_v,
     for (int32_t i = 0; i < n_threads; ++i)
         if (W[i].rc) rc = W[i].rc;
     return rc;
+}
+
+/* gdn_ref_scan_ex with one decay and one beta per (token, head). */
+int gdn_ref_scan(int64_t n_seq, const int64_t *cu, int32_t h_qk, int32_t h_v,
+                 int32_t d_k, int32_t d_v, const double *q, const double *k,
+                 const double *v, const double *a, const double *b,
+                 const double *A_log, const double *dt_bias, const double *g_in,
+                 const double *beta_in, const double *state_in, double scale,
+                 int32_t rule, const int64_t *units, int64_t n_units,
+                 int32_t n_threads, double *o, double *state_out) {
+    return gdn_ref_scan_ex(n_seq, cu, h_qk, h_v, d_k, d_v, q, k, v, a, b, A_log, dt_bias, g_in,
+                           beta_in, state_in, scale, rule, 0, 0, units, n_units, n_threads, o,
+                           state_out);
 }

@@ -458,3 +458,74 @@ def test_window_longer_than_the_run_starts_with_zero_slabs(oracle_mod):
     _, s_ref = oracle_mod.scan_inputs(inp)
     assert np.array_equal(win[4], s_ref)
     assert np.all(np.any(win[2:] != 0.0, axis=(1, 2, 3, 4)))
+
+
+# ---------------------------------------------------------------- gate and rule variants
+
+def _variant_case(T=7, h_v=2, d_k=6, d_v=4, seed=21):
+    rng = np.random.default_rng(seed)
+    q = _rand_unit(rng, T, 1, d_k)
+    k = _rand_unit(rng, T, 1, d_k)
+    v = rng.standard_normal((T, h_v, d_v))
+    return rng, q, k, v
+
+
+def test_per_key_decay_with_equal_factors_is_the_per_head_decay(oracle_mod):
+    rng, q, k, v = _variant_case()
+    T, h_v, d_k, d_v = 7, 2, 6, 4
+    a = rng.standard_normal((T, h_v))
+    b = rng.standard_normal((T, h_v))
+    A_log = rng.uniform(-1, 1, h_v)
+    dt = rng.normal(0, 0.1, h_v)
+    cu = [0, T]
+    o1, s1 = oracle_mod.scan(cu, 1, h_v, d_k, d_v, q, k, v, a=a, b=b, A_log=A_log, dt_bias=dt)
+    rep = lambda x: np.repeat(x[..., None], d_k, axis=-1)
+    o2, s2 = oracle_mod.scan(cu, 1, h_v, d_k, d_v, q, k, v, a=rep(a), b=b, A_log=rep(A_log),
+                             dt_bias=rep(dt), decay_per_key=True)
+    assert np.array_equal(o1, o2) and np.array_equal(s1, s2)
+
+
+def test_per_key_decay_gated_rule_closed_form(oracle_mod):
+    """Rule `gated` with one decay per key dimension from a zero state:
+    S_t = sum_{s<=t} diag(prod_{r=s+1..t} alpha_r) k_s v_s^T, o_t = scale S_t^T q_t."""
+    rng, q, k, v = _variant_case()
+    T, h_v, d_k, d_v = 7, 2, 6, 4
+    g = -rng.uniform(0.0, 0.7, (T, h_v, d_k))
+    scale = 0.37
+    o, s = oracle_mod.scan([0, T], 1, h_v, d_k, d_v, q, k, v, g=g, scale=scale, rule="gated",
+                           decay_per_key=True)
+    alpha = np.exp(g)
+    for h in range(h_v):
+        for t in range(T):
+            St = np.zeros((d_k, d_v))
+            for s_ in range(t + 1):
+                f = np.prod(alpha[s_ + 1:t + 1, h, :], axis=0)
+                St += np.outer(f * k[s_, 0], v[s_, h])
+            assert _rel(o[t, h], scale * St.T @ q[t, 0]) < 1e-12
+        assert _rel(s[0, h], St) < 1e-12
+
+
+def test_shared_beta_equals_the_replicated_per_head_beta(oracle_mod):
+    rng, q, k, v = _variant_case()
+    T, h_v, d_k, d_v = 7, 2, 6, 4
+    a = rng.standard_normal((T, h_v))
+    b1 = rng.standard_normal(T)
+    A_log = rng.uniform(-1, 1, h_v)
+    dt = rng.normal(0, 0.1, h_v)
+    o1, s1 = oracle_mod.scan([0, T], 1, h_v, d_k, d_v, q, k, v, a=a, b=b1, A_log=A_log,
+                             dt_bias=dt, beta_shared=True)
+    o2, s2 = oracle_mod.scan([0, T], 1, h_v, d_k, d_v, q, k, v, a=a,
+                             b=np.repeat(b1[:, None], h_v, axis=1), A_log=A_log, dt_bias=dt)
+    assert np.array_equal(o1, o2) and np.array_equal(s1, s2)
+
+
+def test_delta_rule_is_gated_delta_without_decay(oracle_mod):
+    rng, q, k, v = _variant_case()
+    T, h_v, d_k, d_v = 7, 2, 6, 4
+    beta = rng.uniform(0, 1, (T, h_v))
+    s0 = rng.normal(0, 0.1, (1, h_v, d_k, d_v))
+    o1, s1 = oracle_mod.scan([0, T], 1, h_v, d_k, d_v, q, k, v, beta=beta, state_in=s0,
+                             rule="delta")
+    o2, s2 = oracle_mod.scan([0, T], 1, h_v, d_k, d_v, q, k, v, g=np.zeros((T, h_v)),
+                             beta=beta, state_in=s0, rule="gated_delta")
+    assert np.array_equal(o1, o2) and np.array_equal(s1, s2)
