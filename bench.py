@@ -57,9 +57,10 @@ def io_bytes(inp) -> dict:
     T = inp.total_tokens
     n = inp.n_seq
     st = n * s.h_v * s.d_k * s.d_v * 4
+    per = s.h_v * (s.d_k if s.decay_per_key else 1)   # decay gates per token
     return {
         "q": T * s.h_qk * s.d_k * es, "k": T * s.h_qk * s.d_k * es, "v": T * s.h_v * s.d_v * es,
-        "a": T * s.h_v * es, "b": T * s.h_v * es, "params": 2 * s.h_v * 4,
+        "a": T * per * es, "b": T * (1 if s.beta_shared else s.h_v) * es, "params": 2 * per * 4,
         "state_in": st if (inp.state_in is not None or inp.pool is not None) else 0,
         "o": T * s.h_v * s.d_v * es, "state_out": st * (s.window if s.window else 1),
         "slots": 4 * n if inp.pool is not None else 0,
@@ -261,7 +262,7 @@ def cpu_baseline_line(inp, budget_s=10.0):
 
 def run_ours(args, rank, world, local):
     from recurrent_state_scan_gb300 import (gdn_decode_step, gdn_decode_step_slots, gdn_prefill,
-                                            gdn_scan_window, load)
+                                            gdn_scan_variant, gdn_scan_window, load)
     load()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -286,9 +287,16 @@ def run_ours(args, rank, world, local):
     ws = torch.empty(ws_need, dtype=torch.uint8, device=dev) if ws_need else None
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    variant = s.decay_per_key or s.beta_shared
 
     def step():
-        if window is not None:
+        if variant:
+            # Decode steps update the state in place; prefill writes state_out.
+            gdn_scan_variant(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"], t["dt_bias"],
+                             work_state if s.decode else state0, cu, inp.scale,
+                             decay_per_key=s.decay_per_key, beta_shared=s.beta_shared, o=o,
+                             state_out=work_state if s.decode else state_out, stream=stream)
+        elif window is not None:
             gdn_scan_window(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"], t["dt_bias"],
                             state0, inp.scale, window_len=s.window, o=o, window=window,
                             stream=stream)
@@ -343,7 +351,14 @@ def run_ours(args, rank, world, local):
         def e2e_step():
             for n, v in host.items():
                 dbuf[n].copy_(v, non_blocking=True)
-            if window is not None:
+            if variant:
+                st_out = dbuf["state"] if s.decode else state_out
+                gdn_scan_variant(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["a"], dbuf["b"],
+                                 dbuf["A_log"], dbuf["dt_bias"], dbuf.get("state"), cu, inp.scale,
+                                 decay_per_key=s.decay_per_key, beta_shared=s.beta_shared, o=o,
+                                 state_out=st_out, stream=stream)
+                s_host.copy_(st_out, non_blocking=True)
+            elif window is not None:
                 gdn_scan_window(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["a"], dbuf["b"],
                                 dbuf["A_log"], dbuf["dt_bias"], dbuf.get("state"), inp.scale,
                                 window_len=s.window, o=o, window=window, stream=stream)
@@ -486,6 +501,10 @@ def config_of(inp, world):
         c["lengths"] = [int(x) for x in inp.lengths()]
     else:
         c["batch"], c["seq_len"] = s.batch, s.seqlen
+    if s.decay_per_key or s.beta_shared:
+        c["gates"] = {"decay": "per key dimension" if s.decay_per_key else "per head",
+                      "beta": "shared by all heads" if s.beta_shared else "per head",
+                      "rule": "gated_delta"}
     if inp.pool is not None:
         c["initial_state"] = "pool of %d states, N(0,%g)" % (s.pool_size, s.pool_std)
         c["state_pool"] = {"entries": s.pool_size, "slots": "distinct, seeded permutation",

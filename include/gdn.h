@@ -55,6 +55,24 @@ typedef enum {
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1, GDN_F16 = 2 } gdn_dtype;
 
+/* The update rules of the onnx-runtime-ep-cuda page's rule list (UpdateRule). */
+typedef enum {
+    GDN_RULE_GATED_DELTA = 0,   /* decay, retrieval, delta update, readout (the default) */
+    GDN_RULE_DELTA = 1,         /* no decay: S += k (x) beta (v - S^T k)                  */
+    GDN_RULE_GATED = 2,         /* decay, then S += k (x) v                              */
+    GDN_RULE_LINEAR = 3         /* S += k (x) v                                           */
+} gdn_rule;
+
+/* Gate and rule variant of gdn_scan_variant (all zero: gdn_prefill's gates). */
+typedef struct gdn_variant {
+    int32_t rule;            /* gdn_rule                                                   */
+    int32_t decay_per_key;   /* 0: a [.., h_v], A_log and dt_bias [h_v];
+                                1: a [.., h_v, d_k], A_log and dt_bias [h_v, d_k] (fp32):
+                                   row i of S decays by exp(-exp(A_log[h,i]) *
+                                   softplus(a[..,h,i] + dt_bias[h,i]))                    */
+    int32_t beta_shared;     /* 0: b [.., h_v]; 1: b [B, T, 1], one beta for every head  */
+} gdn_variant;
+
 /* Problem geometry shared by every entry point. */
 typedef struct gdn_shape {
     int32_t io_dtype;   /* gdn_dtype of q, k, v, a, b and o                          */
@@ -192,6 +210,23 @@ gdn_status gdn_scan_window(const gdn_shape *shape, const void *q, const void *k,
                            const void *a, const void *b, const float *A_log, const float *dt_bias,
                            const float *state_in, float scale, void *o, float *window,
                            int32_t window_len, void *stream);
+
+/*
+ * gdn_scan_variant -- gdn_prefill with the gate and rule variants of the
+ * onnx-runtime-ep-cuda page's LinearAttention: the update rules {gated_delta,
+ * delta, gated, linear} (UpdateRule), Step 1's per-key-dim decay
+ * (`decay_per_key_dim`) and a beta shared by all heads (`beta_per_head` false).
+ * Arguments and layouts are gdn_prefill's, with a, A_log and dt_bias shaped by
+ * variant->decay_per_key and b by variant->beta_shared.  Rules without decay do
+ * not read a, A_log or dt_bias (which may be NULL); rules without the delta term do
+ * not read b (which may be NULL).  Runs the token-sequential path for every shape
+ * and I/O type, including T = 1 with state_out aliasing state_in (a decode step).
+ */
+gdn_status gdn_scan_variant(const gdn_shape *shape, const gdn_variant *variant, const void *q,
+                            const void *k, const void *v, const void *a, const void *b,
+                            const float *A_log, const float *dt_bias, const float *state_in,
+                            const int32_t *cu_seqlens, float scale, void *o, float *state_out,
+                            void *stream);
 
 /*
  * gdn_last_device_status -- synchronise `stream`, read the device check word

@@ -134,13 +134,15 @@ def scan(cu_seqlens: Sequence[int], h_qk: int, h_v: int, d_k: int, d_v: int,
     return o.reshape(total, h_v, d_v), s_out.reshape(max(n_seq, 0), h_v, d_k, d_v)
 
 
-def scan_inputs(inp, units=None, threads: int = 1):
-    """Run the oracle on a drawn ``workloads.Inputs`` (the float64 copies)."""
+def scan_inputs(inp, units=None, threads: int = 1, rule: str = "gated_delta"):
+    """Run the oracle on a drawn ``workloads.Inputs`` (the float64 copies), with the
+    spec's gate layout (per-key decay, shared beta)."""
     s = inp.spec
     f = inp.f64
     return scan(inp.cu_seqlens, s.h_qk, s.h_v, s.d_k, s.d_v, f["q"], f["k"], f["v"],
                 a=f["a"], b=f["b"], A_log=f["A_log"], dt_bias=f["dt_bias"],
-                state_in=f["state_in"], scale=inp.scale, units=units, threads=threads)
+                state_in=f["state_in"], scale=inp.scale, rule=rule, units=units,
+                threads=threads, decay_per_key=s.decay_per_key, beta_shared=s.beta_shared)
 
 
 def slot_scan(cu_seqlens: Sequence[int], h_qk: int, h_v: int, d_k: int, d_v: int,

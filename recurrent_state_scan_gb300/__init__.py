@@ -6,4 +6,4 @@ this package builds it in-tree and binds it with ctypes.
 from .gdn import (GdnError, GdnShape, gdn_decode_step, gdn_decode_step_slots,  # noqa: F401
                   gdn_last_device_status,
                   gdn_prefill, gdn_prefill_noalloc, gdn_prefill_workspace_bytes,
-                  gdn_scan_window, gdn_status_string, load)
+                  gdn_scan_variant, gdn_scan_window, gdn_status_string, load)

@@ -321,6 +321,59 @@ gdn_status gdn_scan_window(const gdn_shape *shape, const void *q, const void *k,
     return GDN_OK;
 }
 
+gdn_status gdn_scan_variant(const gdn_shape *shape, const gdn_variant *variant, const void *q,
+                            const void *k, const void *v, const void *a, const void *b,
+                            const float *A_log, const float *dt_bias, const float *state_in,
+                            const int32_t *cu_seqlens, float scale, void *o, float *state_out,
+                            void *stream) {
+    gdn_status st = check_shape(shape, cu_seqlens != nullptr);
+    if (st != GDN_OK) return st;
+    if (variant == nullptr) return fail(GDN_ERR_INVALID_ARG, "variant is NULL");
+    if (variant->rule < GDN_RULE_GATED_DELTA || variant->rule > GDN_RULE_LINEAR)
+        return fail(GDN_ERR_INVALID_ARG, "rule %d is not a gdn_rule", variant->rule);
+    const bool has_decay = variant->rule == GDN_RULE_GATED_DELTA || variant->rule == GDN_RULE_GATED;
+    const bool has_delta = variant->rule == GDN_RULE_GATED_DELTA || variant->rule == GDN_RULE_DELTA;
+    const int64_t tokens = cu_seqlens ? shape->seqlen : shape->seqlen * (int64_t)shape->batch;
+    if (tokens > 0) {
+        if (!q || !k || !v || !o) return fail(GDN_ERR_INVALID_ARG, "q, k, v or o is NULL");
+        if (has_decay && (!a || !A_log || !dt_bias))
+            return fail(GDN_ERR_INVALID_ARG, "a decaying rule needs a, A_log and dt_bias");
+        if (has_delta && !b) return fail(GDN_ERR_INVALID_ARG, "a delta rule needs b");
+        const size_t es = io_size(shape->io_dtype);
+        const void *io_ptrs[] = {q, k, v, a, b, o};
+        for (const void *ptr : io_ptrs)
+            if (ptr && !aligned(ptr, es))
+                return fail(GDN_ERR_INVALID_ARG, "pointer is not %zu-byte aligned", es);
+        if ((A_log && !aligned(A_log, 4)) || (dt_bias && !aligned(dt_bias, 4)))
+            return fail(GDN_ERR_INVALID_ARG, "A_log/dt_bias must be 4-byte aligned");
+    }
+    if (shape->num_seqs == 0) return GDN_OK;
+    if (state_out == nullptr) return fail(GDN_ERR_INVALID_ARG, "state_out is NULL");
+    if (!aligned(state_out, 16) || !aligned(state_in, 16))
+        return fail(GDN_ERR_INVALID_ARG, "state_in/state_out must be 16-byte aligned");
+    if (!(scale == scale) || isinf(scale)) return fail(GDN_ERR_INVALID_ARG, "scale is not finite");
+    int *word = nullptr;
+    st = status_word(&word);
+    if (st != GDN_OK) return st;
+
+    ScanParams p{};
+    p.q = q; p.k = k; p.v = v; p.a = a; p.b = b;
+    p.A_log = A_log; p.dt_bias = dt_bias;
+    p.state_in = state_in; p.state_out = state_out; p.o = o;
+    p.cu_seqlens = cu_seqlens;
+    p.seqlen = shape->seqlen;
+    p.num_seqs = shape->num_seqs;
+    p.h_qk = shape->h_qk; p.h_v = shape->h_v; p.d_k = shape->d_k; p.d_v = shape->d_v;
+    p.scale = scale == 0.0f ? 1.0f / sqrtf((float)shape->d_k) : scale;
+    p.status = word;
+    p.rule = variant->rule;
+    p.decay_per_key = variant->decay_per_key != 0;
+    p.beta_shared = variant->beta_shared != 0;
+    cudaError_t e = launch_scan_simt(p, (gdn_dtype)shape->io_dtype, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "variant scan launch");
+    return GDN_OK;
+}
+
 gdn_status gdn_last_device_status(void *stream) {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");

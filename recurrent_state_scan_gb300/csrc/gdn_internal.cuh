@@ -34,6 +34,10 @@ struct ScanParams {
     int64_t pool_size;           // entries of the state pool when slots is set
     float *window;               // may be null: [window_len, N, h_v, d_k, d_v], the states after
     int32_t window_len;          //   the last window_len steps (leading slabs zero when T is shorter)
+    // Gate and rule variants (all zero: gated delta rule, one decay and one beta per head).
+    int32_t rule;                // gdn_rule: 0 gated_delta, 1 delta, 2 gated, 3 linear
+    int32_t decay_per_key;       // a [.., h_v, d_k], A_log / dt_bias [h_v, d_k]
+    int32_t beta_shared;         // b [.., 1]: one beta for every head
 };
 
 // ------------------------------------------------------------------ I/O types

@@ -18,19 +18,31 @@
 //    registers; the readout uses S'^T q = alpha S^T q + (q.k) delta, which is the
 //    updated-state readout re-associated, so no second pass is needed.
 //  - Cross-row partial sums go through shared memory (three barriers per token).
+//  - The page's variants (its rule list and Step 1's per-key-dim decay) run through the
+//    same kernel: a rule drops the decay and/or the delta; with one decay factor a_i per
+//    key dimension, row i of S is scaled by a_i, which folds into the reductions as the
+//    weights a_i k_i and a_i q_i (compile-time, so the per-head path is unchanged).
 #include "gdn_internal.cuh"
 
 namespace gdn {
 namespace {
 
-template <typename IO, int DKMAX, int LPR, int kThreads>
-__global__ void __launch_bounds__(kThreads) scan_simt_kernel(const ScanParams p) {
+// Up to d_k = 128 four 128-thread CTAs must fit on an SM (at most 128 registers a
+// thread): the state tiles of four CTAs in flight are what keeps HBM busy.
+template <int DKMAX, int kThreads>
+constexpr int simt_min_blocks() { return DKMAX <= 128 ? 512 / kThreads : 1; }
+
+template <typename IO, int DKMAX, int LPR, int kThreads, bool kPerKey>
+__global__ void __launch_bounds__(kThreads, (simt_min_blocks<DKMAX, kThreads>()))
+    scan_simt_kernel(const ScanParams p) {
     constexpr int RPP = kThreads / LPR;   // rows covered per pass
     constexpr int RPT = DKMAX / RPP;      // rows held per thread
     constexpr int TILE = 4 * LPR;         // state columns per CTA
     static_assert(RPT >= 1 && DKMAX % RPP == 0, "bad tiling");
+    constexpr int kBetaThread = kThreads > 32 ? 32 : 0;
 
     __shared__ float sq[DKMAX], sk[DKMAX];
+    __shared__ float sa[kPerKey ? DKMAX : 1];   // per-key decay factors of this token
     __shared__ float sv[TILE], sdelta[TILE];
     __shared__ __align__(16) float red_k[RPP * TILE];
     __shared__ __align__(16) float red_q[RPP * TILE];
@@ -88,7 +100,8 @@ __global__ void __launch_bounds__(kThreads) scan_simt_kernel(const ScanParams p)
     const IO *ga = static_cast<const IO *>(p.a);
     const IO *gb = static_cast<const IO *>(p.b);
     IO *o = static_cast<IO *>(p.o);
-    const float A_log = p.A_log[h], dt_bias = p.dt_bias[h];
+    const bool has_decay = (p.rule == GDN_RULE_GATED_DELTA || p.rule == GDN_RULE_GATED);
+    const bool has_delta = (p.rule == GDN_RULE_GATED_DELTA || p.rule == GDN_RULE_DELTA);
 
     for (int64_t t = t0; t < t1; ++t) {
         __syncthreads();   // previous token's shared values are no longer read
@@ -102,10 +115,20 @@ __global__ void __launch_bounds__(kThreads) scan_simt_kernel(const ScanParams p)
             const int c = tile * TILE + j;
             sv[j] = c < p.d_v ? IoType<IO>::ld(v + v_off + c) : 0.f;
         }
-        if (tid == 0) {
-            const size_t gi = (size_t)t * p.h_v + h;
-            s_alpha = expf(decay_f(IoType<IO>::ld(ga + gi), A_log, dt_bias));
-            s_beta = sigmoid_f(IoType<IO>::ld(gb + gi));
+        // The two scalar gates come from two different warps, so their loads overlap.
+        const size_t gi = (size_t)t * p.h_v + h;
+        if (tid == 0)
+            s_alpha = (has_decay && !kPerKey)
+                          ? expf(decay_f(IoType<IO>::ld(ga + gi), p.A_log[h], p.dt_bias[h]))
+                          : 1.f;
+        if (tid == kBetaThread)
+            s_beta = has_delta ? sigmoid_f(IoType<IO>::ld(gb + (p.beta_shared ? (size_t)t : gi))) : 1.f;
+        if (kPerKey) {
+            const size_t gk = ((size_t)t * p.h_v + h) * p.d_k, hk = (size_t)h * p.d_k;
+            for (int i = tid; i < DKMAX; i += kThreads)
+                sa[i] = (has_decay && i < p.d_k)
+                            ? expf(decay_f(IoType<IO>::ld(ga + gk + i), p.A_log[hk + i], p.dt_bias[hk + i]))
+                            : 1.f;
         }
         __syncthreads();
 
@@ -114,7 +137,8 @@ __global__ void __launch_bounds__(kThreads) scan_simt_kernel(const ScanParams p)
 #pragma unroll
         for (int m = 0; m < RPT; ++m) {
             const int i = rg + RPP * m;
-            const float kk = sk[i], qq = sq[i];
+            const float ai = kPerKey ? sa[i] : 1.f;
+            const float kk = ai * sk[i], qq = ai * sq[i];
             pk.x = fmaf(S[m].x, kk, pk.x); pk.y = fmaf(S[m].y, kk, pk.y);
             pk.z = fmaf(S[m].z, kk, pk.z); pk.w = fmaf(S[m].w, kk, pk.w);
             pq.x = fmaf(S[m].x, qq, pq.x); pq.y = fmaf(S[m].y, qq, pq.y);
@@ -139,8 +163,9 @@ __global__ void __launch_bounds__(kThreads) scan_simt_kernel(const ScanParams p)
                 rk += red_k[r * TILE + tid];
                 rq += red_q[r * TILE + tid];
             }
-            // r = (alpha S)^T k; delta = beta (v - r); o = scale (alpha S + k delta^T)^T q
-            const float delta = s_beta * (sv[tid] - alpha * rk);
+            // r = (alpha S)^T k; delta = beta (v - r) (or v without the delta rule);
+            // o = scale (alpha S + k delta^T)^T q
+            const float delta = has_delta ? s_beta * (sv[tid] - alpha * rk) : sv[tid];
             sdelta[tid] = delta;
             const int c = tile * TILE + tid;
             if (c < p.d_v) IoType<IO>::st(o + v_off + c, p.scale * fmaf(s_qk, delta, alpha * rq));
@@ -151,10 +176,11 @@ __global__ void __launch_bounds__(kThreads) scan_simt_kernel(const ScanParams p)
 #pragma unroll
         for (int m = 0; m < RPT; ++m) {
             const float kk = sk[rg + RPP * m];
-            S[m].x = fmaf(alpha, S[m].x, kk * d4.x);
-            S[m].y = fmaf(alpha, S[m].y, kk * d4.y);
-            S[m].z = fmaf(alpha, S[m].z, kk * d4.z);
-            S[m].w = fmaf(alpha, S[m].w, kk * d4.w);
+            const float am = kPerKey ? sa[rg + RPP * m] : alpha;
+            S[m].x = fmaf(am, S[m].x, kk * d4.x);
+            S[m].y = fmaf(am, S[m].y, kk * d4.y);
+            S[m].z = fmaf(am, S[m].z, kk * d4.z);
+            S[m].w = fmaf(am, S[m].w, kk * d4.w);
         }
         // One of the last window_len steps: its state goes to slab window_len - (t1 - t).
         if (p.window != nullptr && t1 - t <= p.window_len)
@@ -184,7 +210,10 @@ cudaError_t launch_cfg(const ScanParams &p, cudaStream_t stream) {
     const int64_t blocks = (int64_t)p.num_seqs * p.h_v * tiles;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    scan_simt_kernel<IO, DKMAX, LPR, NT><<<(unsigned)blocks, NT, 0, stream>>>(p);
+    if (p.decay_per_key)
+        scan_simt_kernel<IO, DKMAX, LPR, NT, true><<<(unsigned)blocks, NT, 0, stream>>>(p);
+    else
+        scan_simt_kernel<IO, DKMAX, LPR, NT, false><<<(unsigned)blocks, NT, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

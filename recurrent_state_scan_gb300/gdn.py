@@ -26,8 +26,10 @@ _DTYPE_CODE = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16, torch.float16: 
 EXPORTS = ("gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode_step",
            "gdn_prefill_plan", "gdn_last_device_status", "gdn_status_string",
            "gdn_last_error_message", "gdn_prefill_noalloc", "gdn_decode_step_slots",
-           "gdn_scan_window")
+           "gdn_scan_window", "gdn_scan_variant")
 PATH_SIMT, PATH_TC = 1, 2
+# gdn_rule codes.
+RULES = {"gated_delta": 0, "delta": 1, "gated": 2, "linear": 3}
 
 
 class GdnShape(ctypes.Structure):
@@ -35,6 +37,11 @@ class GdnShape(ctypes.Structure):
                 ("seqlen", ctypes.c_int64), ("num_seqs", ctypes.c_int32),
                 ("h_qk", ctypes.c_int32), ("h_v", ctypes.c_int32),
                 ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32)]
+
+
+class GdnVariant(ctypes.Structure):
+    _fields_ = [("rule", ctypes.c_int32), ("decay_per_key", ctypes.c_int32),
+                ("beta_shared", ctypes.c_int32)]
 
 
 class GdnError(RuntimeError):
@@ -70,6 +77,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.gdn_scan_window.restype = ctypes.c_int
     lib.gdn_scan_window.argtypes = [S, P, P, P, P, P, P, P, P, ctypes.c_float, P, P,
                                     ctypes.c_int32, P]
+    lib.gdn_scan_variant.restype = ctypes.c_int
+    lib.gdn_scan_variant.argtypes = [S, ctypes.POINTER(GdnVariant), P, P, P, P, P, P, P, P, P,
+                                     ctypes.c_float, P, P, P]
     lib.gdn_decode_step_slots.restype = ctypes.c_int
     lib.gdn_decode_step_slots.argtypes = [S, P, P, P, P, P, P, P, P, ctypes.c_int64, P,
                                           ctypes.c_float, P, P]
@@ -262,15 +272,22 @@ def shape_of_spec(spec, n_seq: int, total_tokens: int) -> GdnShape:
                       spec.d_v)
 
 
+def _simt_only(spec) -> bool:
+    """Specs that run the token-sequential kernel alone: decode, state windows and the
+    gate variants of gdn_scan_variant."""
+    return bool(spec.decode or getattr(spec, "window", 0) or getattr(spec, "decay_per_key", False)
+                or getattr(spec, "beta_shared", False))
+
+
 def launches_per_call(spec, n_seq: int = 0, total_tokens: int = 0) -> int:
-    if spec.decode or getattr(spec, "window", 0):
+    if _simt_only(spec):
         return 1
     return gdn_prefill_plan(shape_of_spec(spec, n_seq, total_tokens))[1]
 
 
 def path_dtype(spec, n_seq: int = 0, total_tokens: int = 0) -> str:
     """Arithmetic type of the path: MMA operand type on the tensor-core path, else f32."""
-    if spec.decode or getattr(spec, "window", 0):
+    if _simt_only(spec):
         return "f32"
     path = gdn_prefill_plan(shape_of_spec(spec, n_seq, total_tokens))[0]
     return spec.io if path == PATH_TC else "f32"
@@ -348,3 +365,61 @@ def gdn_scan_window(q, k, v, a, b, A_log, dt_bias, state_in=None, scale: float =
                                _ptr(A_log), _ptr(dt_bias), _ptr(state_in), float(scale), _ptr(o),
                                _ptr(window), int(window_len), _stream(stream)))
     return o, window
+
+
+def gdn_scan_variant(q, k, v, a=None, b=None, A_log=None, dt_bias=None, state_in=None,
+                     cu_seqlens=None, scale: float = 0.0, *, rule: str = "gated_delta",
+                     decay_per_key: bool = False, beta_shared: bool = False, o=None,
+                     state_out=None, stream=None):
+    """gdn_prefill with another update rule ("gated_delta", "delta", "gated", "linear"),
+    per-key-dim decay (a [B,T,h_v,d_k]; A_log, dt_bias [h_v,d_k]) or one beta for all
+    heads (b [B,T,1]).  a, A_log, dt_bias are unused (may be None) by rules without
+    decay, b by rules without the delta term.  Returns (o, state_out); ``state_out``
+    may be ``state_in`` itself (an in-place update)."""
+    lib = load()
+    if rule not in RULES:
+        raise GdnError(GDN_ERR_INVALID_ARG, f"unknown rule {rule!r}")
+    shape = _shape_of(q, v, cu_seqlens)
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda(name, t, dt)
+    if tuple(k.shape) != tuple(q.shape):
+        raise GdnError(GDN_ERR_INVALID_ARG, "k must match q")
+    lead = tuple(v.shape[:2])
+    decay = rule in ("gated_delta", "gated")
+    if decay:
+        _need_cuda("a", a, dt)
+        _need_cuda("A_log", A_log, torch.float32)
+        _need_cuda("dt_bias", dt_bias, torch.float32)
+        per = (shape.h_v, shape.d_k) if decay_per_key else (shape.h_v,)
+        if tuple(a.shape) != lead + per or tuple(A_log.shape) != per or \
+                tuple(dt_bias.shape) != per:
+            raise GdnError(GDN_ERR_INVALID_ARG, f"a must be {lead + per}, A_log and dt_bias {per}")
+    if rule in ("gated_delta", "delta"):
+        _need_cuda("b", b, dt)
+        want = lead + ((1,) if beta_shared else (shape.h_v,))
+        if tuple(b.shape) != want:
+            raise GdnError(GDN_ERR_INVALID_ARG, f"b must be {want}")
+    st_shape = (shape.num_seqs, shape.h_v, shape.d_k, shape.d_v)
+    if state_in is not None:
+        _need_cuda("state_in", state_in, torch.float32)
+        if tuple(state_in.shape) != st_shape:
+            raise GdnError(GDN_ERR_INVALID_ARG, f"state_in must be {st_shape}")
+    if cu_seqlens is not None:
+        _need_cuda("cu_seqlens", cu_seqlens, torch.int32)
+    if o is None:
+        o = torch.empty(v.shape, dtype=dt, device=v.device)
+    else:
+        _need_cuda("o", o, dt)
+    if state_out is None:
+        state_out = torch.empty(st_shape, dtype=torch.float32, device=v.device)
+    else:
+        _need_cuda("state_out", state_out, torch.float32)
+    var = GdnVariant(RULES[rule], int(bool(decay_per_key)), int(bool(beta_shared)))
+    _check(lib.gdn_scan_variant(ctypes.byref(shape), ctypes.byref(var), _ptr(q), _ptr(k),
+                                _ptr(v), _ptr(a if decay else None),
+                                _ptr(b if rule in ("gated_delta", "delta") else None),
+                                _ptr(A_log if decay else None), _ptr(dt_bias if decay else None),
+                                _ptr(state_in), _ptr(cu_seqlens), float(scale), _ptr(o),
+                                _ptr(state_out), _stream(stream)))
+    return o, state_out

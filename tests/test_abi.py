@@ -101,3 +101,23 @@ def test_decode_rejects_bad_arguments():
 
 def test_workspace_query_is_host_only():
     assert gdn.gdn_prefill_workspace_bytes(_shape()) >= 0
+
+
+def test_variant_rejects_bad_rules_and_missing_gates():
+    lib = gdn.load()
+    p = ctypes.c_void_p(0x1000)
+
+    def call(rule, a=p, b=p, A=p, decay_per_key=0, beta_shared=0, variant=True):
+        var = gdn.GdnVariant(rule, decay_per_key, beta_shared)
+        return lib.gdn_scan_variant(ctypes.byref(_shape()), ctypes.byref(var) if variant else None,
+                                    p, p, p, a, b, A, A, None, None, 0.0, p,
+                                    ctypes.c_void_p(0x2000), None)
+
+    assert call(4) == gdn.GDN_ERR_INVALID_ARG                       # no such rule
+    assert call(-1) == gdn.GDN_ERR_INVALID_ARG
+    assert call(0, variant=False) == gdn.GDN_ERR_INVALID_ARG
+    assert call(gdn.RULES["gated_delta"], b=None) == gdn.GDN_ERR_INVALID_ARG
+    assert call(gdn.RULES["gated_delta"], a=None) == gdn.GDN_ERR_INVALID_ARG
+    assert call(gdn.RULES["gated"], A=None) == gdn.GDN_ERR_INVALID_ARG
+    assert call(gdn.RULES["delta"], b=None) == gdn.GDN_ERR_INVALID_ARG
+    assert call(gdn.RULES["linear"], a=ctypes.c_void_p(0x1001)) == gdn.GDN_ERR_INVALID_ARG

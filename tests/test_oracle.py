@@ -316,7 +316,11 @@ def test_workload_recipe():
     w = workloads.WORKLOADS
     assert set(w) == {"tiny_f32_prefill", "bf16_prefill_t4096", "bf16_decode_b256",
                       "varlen_bf16_prefill", "gqa_f16_prefill", "bf16_slot_decode_b256",
-                      "bf16_window_b256_t4"}
+                      "bf16_window_b256_t4", "bf16_perkey_decode_b256"}
+    pk = workloads.draw(workloads.small_spec(io="bf16", batch=3, seqlen=2, h_qk=1, h_v=2, d_k=8,
+                                             d_v=4, decay_per_key=True, beta_shared=True))
+    assert tuple(pk.a.shape) == (3, 2, 2, 8) and tuple(pk.A_log.shape) == (2, 8)
+    assert tuple(pk.dt_bias.shape) == (2, 8) and tuple(pk.b.shape) == (3, 2, 1)
     sp = w["bf16_slot_decode_b256"]
     sl = workloads.draw(workloads.small_spec(io="bf16", batch=sp.batch, seqlen=1, h_qk=1, h_v=1,
                                              d_k=4, d_v=4, decode=True, pool_size=sp.pool_size,

@@ -47,6 +47,8 @@ class Spec:
     pool_size: int = 0           # > 0: states live in a pool of this many entries
     pool_std: float = 0.0        # std of the pool entries
     window: int = 0              # > 0: emit the states after the last `window` steps
+    decay_per_key: bool = False  # a [B,T,h_v,d_k], A_log and dt_bias [h_v,d_k]
+    beta_shared: bool = False    # b [B,T,1]: one beta for every head
 
 
 # The five workloads the method is measured on.
@@ -76,6 +78,10 @@ WORKLOADS = {
     "bf16_window_b256_t4": Spec(
         "bf16_window_b256_t4", io="bf16", batch=256, seqlen=4, h_qk=32, h_v=32,
         d_k=128, d_v=128, seed=1006, state_std=0.05, window=4),
+    # Decode with one decay per key dimension (the gate-variant row).
+    "bf16_perkey_decode_b256": Spec(
+        "bf16_perkey_decode_b256", io="bf16", batch=256, seqlen=1, h_qk=32, h_v=32,
+        d_k=128, d_v=128, seed=1007, state_std=0.05, decode=True, decay_per_key=True),
 }
 
 
@@ -88,10 +94,10 @@ class Inputs:
     q: torch.Tensor               # [B, T, h_qk, d_k] (varlen: B=1, T=total)
     k: torch.Tensor
     v: torch.Tensor               # [B, T, h_v, d_v]
-    a: torch.Tensor               # [B, T, h_v]
-    b: torch.Tensor
-    A_log: torch.Tensor           # [h_v] fp32
-    dt_bias: torch.Tensor         # [h_v] fp32
+    a: torch.Tensor               # [B, T, h_v] ([B, T, h_v, d_k] with decay_per_key)
+    b: torch.Tensor               # [B, T, h_v] ([B, T, 1] with beta_shared)
+    A_log: torch.Tensor           # [h_v] fp32 ([h_v, d_k] with decay_per_key)
+    dt_bias: torch.Tensor         # [h_v] fp32 ([h_v, d_k] with decay_per_key)
     state_in: Optional[torch.Tensor]   # [n_seq, h_v, d_k, d_v] fp32 or None
     scale: float
     f64: dict
@@ -149,10 +155,11 @@ def draw(spec: Spec) -> Inputs:
     q = _l2_normalise(rng.standard_normal((B, T, spec.h_qk, spec.d_k))) * spec.qk_scale
     k = _l2_normalise(rng.standard_normal((B, T, spec.h_qk, spec.d_k))) * spec.qk_scale
     v = rng.standard_normal((B, T, spec.h_v, spec.d_v))
-    a = rng.standard_normal((B, T, spec.h_v))
-    b = rng.standard_normal((B, T, spec.h_v))
-    A_log = rng.uniform(-1.0, 1.0, spec.h_v)
-    dt_bias = rng.normal(0.0, 0.1, spec.h_v)
+    per = (spec.h_v, spec.d_k) if spec.decay_per_key else (spec.h_v,)
+    a = rng.standard_normal((B, T) + per)
+    b = rng.standard_normal((B, T, 1 if spec.beta_shared else spec.h_v))
+    A_log = rng.uniform(-1.0, 1.0, per)
+    dt_bias = rng.normal(0.0, 0.1, per)
     state = None
     if spec.state_std > 0.0:
         state = rng.normal(0.0, spec.state_std, (n_seq, spec.h_v, spec.d_k, spec.d_v))
@@ -187,10 +194,12 @@ def workload(name: str) -> Inputs:
 
 def small_spec(name="small", io="bf16", batch=1, seqlen=0, lengths=None, h_qk=2,
                h_v=2, d_k=128, d_v=128, seed=7, state_std=0.0, decode=False,
-               qk_scale=1.0, pool_size=0, pool_std=0.0, window=0) -> Spec:
+               qk_scale=1.0, pool_size=0, pool_std=0.0, window=0, decay_per_key=False,
+               beta_shared=False) -> Spec:
     """A test-sized workload with the same distributions as the measured ones."""
     return Spec(name=name, io=io, batch=batch, seqlen=seqlen,
                 lengths=None if lengths is None else tuple(int(x) for x in lengths),
                 h_qk=h_qk, h_v=h_v, d_k=d_k, d_v=d_v, seed=seed,
                 state_std=state_std, decode=decode, qk_scale=qk_scale,
-                pool_size=pool_size, pool_std=pool_std, window=window)
+                pool_size=pool_size, pool_std=pool_std, window=window,
+                decay_per_key=decay_per_key, beta_shared=beta_shared)
