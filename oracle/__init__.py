@@ -21,6 +21,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gdn_ref.c")
+_SRCS = (_SRC, os.path.join(_HERE, "neighbours_ref.c"))
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "libgdn_ref.so")
 
@@ -33,10 +34,10 @@ def build(force: bool = False) -> str:
     """Compile the oracle with gcc (no fast-math, no FMA contraction)."""
     os.makedirs(_BUILD, exist_ok=True)
     if force or not os.path.exists(_LIB_PATH) or \
-            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+            any(os.path.getmtime(_LIB_PATH) < os.path.getmtime(src) for src in _SRCS):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
-                        "-pthread", _SRC, "-o", tmp, "-lm"], check=True)
+                        "-pthread", *_SRCS, "-o", tmp, "-lm"], check=True)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -63,6 +64,13 @@ def _load():
             getattr(lib, name).argtypes = [ctypes.c_double]
         lib.gdn_ref_decay.restype = ctypes.c_double
         lib.gdn_ref_decay.argtypes = [ctypes.c_double] * 3
+        I32 = ctypes.c_int32
+        lib.gdn_ref_causal_conv.restype = ctypes.c_int
+        lib.gdn_ref_causal_conv.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, I32,
+                                            I32, I32, I32, I32, D, D, D, D, D, D]
+        lib.gdn_ref_gated_rmsnorm.restype = ctypes.c_int
+        lib.gdn_ref_gated_rmsnorm.argtypes = [ctypes.c_int64, ctypes.c_int64, D, D, D,
+                                              ctypes.c_double, I32, D]
         _lib = lib
     return _lib
 
@@ -223,3 +231,76 @@ def window_scan_inputs(inp, threads: int = 1):
     return window_scan(s.batch, s.seqlen, s.h_qk, s.h_v, s.d_k, s.d_v, f["q"], f["k"], f["v"],
                        f["a"], f["b"], f["A_log"], f["dt_bias"], f["state_in"], s.window,
                        scale=inp.scale, threads=threads)
+
+
+# ---------------------------------------------------------------- neighbouring ops
+
+ACTIVATIONS = {"silu": 1, "swish": 1, "sigmoid": 2}
+
+
+def causal_conv(x, w, bias=None, state_in=None, *, dilation: int = 1,
+                channels_last: bool = True, silu: bool = False, state_window: int = 0):
+    """CausalConvWithState (onnxruntime-ep-mlx src/ops/ssm.rs, `causal_conv_op`).
+
+    x: [B, L, C] (channels_last) or [B, C, L]; w: [C, 1, K] (or [C, K, 1], the same
+    memory); bias: [C] or None; state_in: [B, carry, C] / [B, C, carry], with a leading
+    [W] axis when state_window = W > 0, or None (zeros); carry = (K - 1) * dilation.
+    Returns (y like x, state_out like state_in) in float64.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    B = x.shape[0]
+    C = x.shape[2] if channels_last else x.shape[1]
+    L = x.shape[1] if channels_last else x.shape[2]
+    w = _f64(w)
+    K = w.size // C
+    assert K * C == w.size
+    carry = (K - 1) * dilation
+    st_shape = (B, carry, C) if channels_last else (B, C, carry)
+    if state_window:
+        st_shape = (state_window,) + st_shape
+    if state_in is not None:
+        assert np.size(state_in) == int(np.prod(st_shape))
+    y = np.zeros(B * L * C, dtype=np.float64)
+    s_out = np.zeros(int(np.prod(st_shape)), dtype=np.float64)
+    rc = _load().gdn_ref_causal_conv(B, L, C, K, dilation, int(bool(channels_last)),
+                                     int(bool(silu)), int(state_window), _ptr(_f64(x)), _ptr(w),
+                                     _ptr(_f64(bias)), _ptr(_f64(state_in)), _ptr(y), _ptr(s_out))
+    if rc != 0:
+        raise ValueError(f"gdn_ref_causal_conv failed with code {rc}")
+    return y.reshape(x.shape), s_out.reshape(st_shape)
+
+
+def conv_slots(x, w, pool, slots, bias=None, *, dilation: int = 1, silu: bool = False):
+    """The convolution against a pool of states (nuvec-core src/fast/imp.rs,
+    `causal_conv1d_slots` and the fallback graph of FastOp::ConvSlots): take the states
+    at the slots, prepend them to x [B, L, C], convolve, and put each row's last carry
+    inputs back at its slot.  pool: [P, carry, C].  A slot outside [0, P) skips its row
+    (outputs zero, pool unchanged).  Returns (y, new pool) in float64."""
+    x = np.asarray(x, dtype=np.float64)
+    B, L, C = x.shape
+    pool = np.array(pool, dtype=np.float64, copy=True)
+    P = pool.shape[0]
+    y = np.zeros_like(x)
+    for b, s in enumerate(int(v) for v in np.asarray(slots).reshape(-1)):
+        if not 0 <= s < P:
+            continue
+        yb, sb = causal_conv(x[b:b + 1], w, bias, pool[s:s + 1], dilation=dilation, silu=silu)
+        y[b] = yb[0]
+        pool[s] = sb[0]
+    return y, pool
+
+
+def gated_rmsnorm(x, scale, gate, eps: float = 1e-5, activation: str = "silu"):
+    """GatedRMSNorm (onnxruntime-ep-mlx src/ops/ssm.rs, `gated_rms_norm_op`): rows of
+    C = len(scale) consecutive values of x.  Returns y (shape of x) in float64."""
+    x = np.asarray(x, dtype=np.float64)
+    scale = _f64(scale)
+    width = scale.size
+    assert x.size % width == 0 and np.size(gate) == x.size
+    y = np.zeros(x.size, dtype=np.float64)
+    rc = _load().gdn_ref_gated_rmsnorm(x.size // width, width, _ptr(_f64(x)), _ptr(scale),
+                                       _ptr(_f64(gate)), float(eps), ACTIVATIONS[activation],
+                                       _ptr(y))
+    if rc != 0:
+        raise ValueError(f"gdn_ref_gated_rmsnorm failed with code {rc}")
+    return y.reshape(x.shape)
