@@ -13,6 +13,7 @@ and scaling is weak.  `--impl reference` times the CPU oracle on host cores.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -42,7 +43,7 @@ def parse_args():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
-    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.ALL_WORKLOADS)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -100,7 +101,8 @@ def peaks():
 
 
 # Sources of the kernels each workload's traffic figure belongs to.
-KERNEL_SOURCES = {"decode": ("scan_simt.cu",), "prefill": ("prefill_tc.cu", "tc_ptx.cuh")}
+KERNEL_SOURCES = {"decode": ("scan_simt.cu",), "prefill": ("prefill_tc.cu", "tc_ptx.cuh"),
+                  "neighbours": ("neighbours.cu",)}
 
 
 def source_digest(kind: str = "prefill") -> str:
@@ -258,6 +260,249 @@ def cpu_baseline_line(inp, budget_s=10.0):
                       f"({threads} threads over (sequence, head) units), {per * reps:.1f} s"}
 
 
+# ---------------------------------------------------------------- neighbouring ops
+#
+# The causal convolution and the gated RMS norm are single HBM-bound kernels: a step is
+# one call over the whole workload, measured in GB/s of algorithmic bytes (every input
+# read once, every output written once).
+
+def neighbour_io_bytes(inp) -> dict:
+    if isinstance(inp, workloads.ConvInputs):
+        s = inp.spec
+        es = inp.x.element_size()
+        n = inp.x.numel()
+        carry = (s.kernel - 1) * s.dilation
+        one = s.batch * carry * s.channels * es
+        win = max(s.state_window, 1)
+        return {"x": n * es, "y": n * es, "weight": inp.w.numel() * es,
+                "bias": 0 if inp.bias is None else inp.bias.numel() * es,
+                "state_in": one if (inp.state_in is not None or inp.pool is not None) else 0,
+                "state_out": one * win, "slots": 0 if inp.slots is None else 4 * s.batch}
+    es = inp.x.element_size()
+    n = inp.x.numel()
+    return {"x": n * es, "gate": n * es, "y": n * es, "scale": inp.scale.numel() * es}
+
+
+def neighbour_oracle(inp):
+    import oracle
+    f = inp.f64
+    if isinstance(inp, workloads.ConvInputs):
+        s = inp.spec
+        if inp.pool is not None:
+            return oracle.conv_slots(f["x"], f["w"], f["pool"], inp.slots.numpy(), f["bias"],
+                                     dilation=s.dilation, silu=s.silu)
+        return oracle.causal_conv(f["x"], f["w"], f["bias"], f["state_in"], dilation=s.dilation,
+                                  channels_last=s.channels_last, silu=s.silu,
+                                  state_window=s.state_window)
+    return oracle.gated_rmsnorm(f["x"], f["scale"], f["gate"], inp.spec.eps, inp.spec.activation)
+
+
+def neighbour_sample(inp):
+    """A bounded sample of a convolution workload for the CPU oracle: its first 512
+    channels when the whole would take the oracle more than a second or so (the oracle
+    walks each channel's tokens, a strided pass over x).  Returns (inputs, description)."""
+    if not isinstance(inp, workloads.ConvInputs) or inp.x.numel() <= (1 << 24):
+        return inp, f"the whole {inp.spec.name} workload"
+    s = inp.spec
+    c = min(512, s.channels)
+    cut = lambda t: None if t is None else np.ascontiguousarray(t[..., :c])
+    f = {n: cut(v) for n, v in inp.f64.items() if n != "w" and n != "bias"}
+    f["w"] = inp.f64["w"][:c]
+    f["bias"] = None if inp.f64["bias"] is None else inp.f64["bias"][:c]
+    small = workloads.ConvInputs(
+        spec=dataclasses.replace(s, channels=c),
+        x=inp.x[..., :c].contiguous(), w=inp.w[:c].contiguous(),
+        bias=None if inp.bias is None else inp.bias[:c].contiguous(),
+        state_in=None if inp.state_in is None else inp.state_in[..., :c].contiguous(),
+        pool=None if inp.pool is None else inp.pool[..., :c].contiguous(),
+        slots=inp.slots, f64=f)
+    return small, f"the first {c} of {s.channels} channels of {s.name} (all rows and tokens)"
+
+
+def time_neighbour_oracle(inp, budget_s: float, min_reps: int = 1):
+    import oracle
+    oracle.build()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        neighbour_oracle(inp)
+        reps += 1
+        el = time.perf_counter() - t0
+        if reps >= min_reps and el >= budget_s:
+            break
+    return el / reps, reps, 1
+
+
+def neighbour_config(inp, world):
+    s = inp.spec
+    c = {"workload": s.name, "io_dtype": s.io, "l2": "flushed before every step (256 MiB write, untimed)",
+         "parallelism": f"replicas: the full workload on each of {world} GPU(s), no collective"}
+    if isinstance(inp, workloads.ConvInputs):
+        c.update({"op": "causal depthwise conv with carried state", "batch": s.batch,
+                  "seq_len": s.seqlen, "channels": s.channels, "kernel": s.kernel,
+                  "dilation": s.dilation, "activation": "silu" if s.silu else "none",
+                  "layout": "channels last" if s.channels_last else "channels first",
+                  "past_state": "N(0,%g)" % s.state_std if s.state_std else "zero",
+                  "state_update": "in place" if s.decode else "separate present state"})
+    else:
+        c.update({"op": "gated RMS norm", "shape": list(s.shape), "eps": s.eps,
+                  "activation": s.activation})
+    return c
+
+
+def main_neighbour(args, rank, world, local):
+    inp = workloads.any_workload(args.workload)
+    nbytes = int(sum(neighbour_io_bytes(inp).values()))
+    conv = isinstance(inp, workloads.ConvInputs)
+    s = inp.spec
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        sample, what = neighbour_sample(inp)
+        sbytes = int(sum(neighbour_io_bytes(sample).values()))
+        for _ in range(args.warmup):
+            time_neighbour_oracle(sample, 0.0)
+        per, reps, threads = time_neighbour_oracle(sample, 0.0, min_reps=args.steps)
+        value = sbytes / per / 1e9
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": neighbour_config(inp, world),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{what} per step, {reps} steps"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}), flush=True)
+        return
+
+    from recurrent_state_scan_gb300 import (gdn_causal_conv, gdn_causal_conv_slots,
+                                            gdn_gated_rmsnorm, load)
+    load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    if conv:
+        names = [("x", inp.x), ("w", inp.w), ("bias", inp.bias), ("state", inp.state_in),
+                 ("pool", inp.pool), ("slots", inp.slots)]
+    else:
+        names = [("x", inp.x), ("scale", inp.scale), ("gate", inp.gate)]
+    t = {n: v.to(dev) for n, v in names if v is not None}
+    y = torch.empty_like(t["x"])
+    act = ("silu" if s.silu else "none") if conv else s.activation
+    st_out = None
+    if conv and inp.pool is None and not s.decode:
+        from recurrent_state_scan_gb300 import gdn
+        st_out = torch.empty(gdn.conv_state_shape(s.batch, s.channels, s.kernel, s.dilation,
+                                                  s.channels_last, s.state_window),
+                             dtype=t["x"].dtype, device=dev)
+
+    def call(d):
+        if not conv:
+            gdn_gated_rmsnorm(d["x"], d["scale"], d["gate"], s.eps, act, y=y, stream=stream)
+        elif "pool" in d:
+            gdn_causal_conv_slots(d["x"], d["w"], d["pool"], d["slots"], d.get("bias"),
+                                  dilation=s.dilation, activation=act, y=y, stream=stream)
+        else:
+            gdn_causal_conv(d["x"], d["w"], d.get("bias"), d.get("state"), dilation=s.dilation,
+                            channels_last=s.channels_last, activation=act,
+                            state_window=s.state_window, y=y,
+                            state_out=d.get("state") if s.decode else st_out, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        call(t)
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        call(t)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in zip(starts, ends)])), world)
+
+    e2e = None
+    if not args.no_e2e:
+        # Pinned host inputs -> device -> call -> y (and the state, unless it lives in a
+        # resident pool) back to the host.
+        host = {n: v.pin_memory() for n, v in names if v is not None and n != "pool"}
+        dbuf = {n: torch.empty_like(v, device=dev) for n, v in host.items()}
+        if "pool" in t:
+            dbuf["pool"] = t["pool"]
+        y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        st_dev = (dbuf.get("state") if s.decode else st_out) if conv and "pool" not in t else None
+        st_host = None if st_dev is None else torch.empty(st_dev.shape, dtype=st_dev.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = y_host.numel() * y_host.element_size() + \
+            (0 if st_host is None else st_host.numel() * st_host.element_size())
+
+        def e2e_step():
+            for n, v in host.items():
+                dbuf[n].copy_(v, non_blocking=True)
+            call(dbuf)
+            if st_host is not None:
+                st_host.copy_(dbuf.get("state") if s.decode else st_out, non_blocking=True)
+            y_host.copy_(y, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier(world)
+        for i in range(args.steps):
+            flush.zero_()
+            es[i].record(stream)
+            e2e_step()
+            ee[i].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        ems = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in zip(es, ee)])), world)
+        e2e = {"value": world * nbytes / (ems / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": ems,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    pk, pk_kind = peaks()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    kernel = "gdn::causal_conv_kernel" if conv else "gdn::gated_rmsnorm_kernel"
+    line = {
+        "metric": METRIC, "value": world * gbs, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": neighbour_config(inp, world),
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm_gbs"],
+                     "traffic": profiled_traffic(args.workload, "neighbours"),
+                     "peak_source": f"{pk_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+                     if pk_kind == "measured" else "fallback 6.8 TB/s",
+                     "kernels": kernel},
+        "gpu_launches": args.steps,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if clocks is not None:
+        line["clocks"] = clocks
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample, what = neighbour_sample(inp)
+        per, reps, threads = time_neighbour_oracle(sample, 10.0)
+        line["cpu_baseline"] = {
+            "value": sum(neighbour_io_bytes(sample).values()) / per / 1e9, "unit": "GB/s",
+            "cores": threads, "kind": "oracle",
+            "sample": f"{what} x{reps} through the float64 C oracle (one thread), "
+                      f"{per * reps:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, local):
@@ -402,6 +647,8 @@ def main():
     args = parse_args()
     rank, world, local = dist_init()
     inp_name = args.workload
+    if inp_name not in workloads.WORKLOADS:
+        return main_neighbour(args, rank, world, local)
     if args.impl == "reference":
         # The reference arm is the CPU oracle, timed as it stands, on rank 0 only.
         if rank != 0:

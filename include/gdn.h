@@ -228,6 +228,73 @@ gdn_status gdn_scan_variant(const gdn_shape *shape, const gdn_variant *variant, 
                             const int32_t *cu_seqlens, float scale, void *o, float *state_out,
                             void *stream);
 
+/* ------------------------------------------------------------------------------------
+ * The layer ops around the scan (onnxruntime-ep-mlx 0.31.1, src/ops/ssm.rs): the causal
+ * depthwise convolution that produces q, k, v, and the gated RMS norm of the output.
+ * ---------------------------------------------------------------------------------- */
+
+/* Activations: the convolution takes NONE or SILU, the norm SILU or SIGMOID. */
+typedef enum { GDN_ACT_NONE = 0, GDN_ACT_SILU = 1, GDN_ACT_SIGMOID = 2 } gdn_activation;
+
+/* Geometry of a causal depthwise convolution; carry = (kernel - 1) * dilation. */
+typedef struct gdn_conv_shape {
+    int32_t io_dtype;        /* gdn_dtype of x, weight, bias, state and y alike           */
+    int32_t batch;           /* B rows                                                      */
+    int64_t seqlen;          /* L tokens per row (0 allowed)                                */
+    int32_t channels;        /* C                                                           */
+    int32_t kernel;          /* K taps, 1..64                                               */
+    int32_t dilation;        /* >= 1, with carry <= 4096                                    */
+    int32_t channels_last;   /* 1: x, y [B, L, C], state [B, carry, C];
+                                0: x, y [B, C, L], state [B, C, carry]                      */
+    int32_t activation;      /* GDN_ACT_NONE or GDN_ACT_SILU                                */
+    int32_t state_window;    /* 0, or W in 1..8: state_in and state_out gain a leading [W]
+                                axis (the states after each of the last W tokens)          */
+} gdn_conv_shape;
+
+/*
+ * gdn_causal_conv -- CausalConvWithState (ssm.rs `causal_conv_op`).  Every channel c of
+ * row b is convolved on its own over the padded sequence pad = [past state ; x]:
+ *   y[b, t, c] = act(bias[c] + sum_{j<K} weight[c, j] * pad[t + j * dilation])
+ * (taps in order, no flip), computed in fp32 and rounded once to the I/O dtype.
+ *   weight   [C, 1, K] (the same memory as [C, K, 1]); bias [C] or NULL.
+ *   state_in the past state (NULL = zeros); with state_window W only slab W - 1 is read.
+ *   state_out the present state (NULL = not written): pad[L .. L + carry), an exact copy;
+ *            with a window, slab s holds the carry positions ending at token L - W + s,
+ *            zero slabs first when L < W, and the past window itself when L = 0.
+ * state_out may be state_in itself (the update is then in place); other overlaps, or y
+ * overlapping an input, give undefined results.  All pointers are device memory owned by
+ * the caller and aligned to the I/O element size.  Bad geometry or pointers return
+ * GDN_ERR_INVALID_ARG before anything is launched.
+ */
+gdn_status gdn_causal_conv(const gdn_conv_shape *shape, const void *x, const void *weight,
+                           const void *bias, const void *state_in, void *y, void *state_out,
+                           void *stream);
+
+/*
+ * gdn_causal_conv_slots -- gdn_causal_conv against a pool of states, for continuous
+ * batching (nuvec-core 0.6.1, src/fast/imp.rs, `causal_conv1d_slots`): row b starts from
+ * pool[slots[b]] and its present state is written back there, in place.  Channels last
+ * and no state window: x, y [B, L, C], pool [pool_size, carry, C], slots int32 [B] on the
+ * device, distinct.  A slot outside [0, pool_size) skips its row (y untouched, pool
+ * unchanged) and sets the device check word (gdn_last_device_status).
+ */
+gdn_status gdn_causal_conv_slots(const gdn_conv_shape *shape, const void *x, const void *weight,
+                                 const void *bias, void *pool, int64_t pool_size,
+                                 const int32_t *slots, void *y, void *stream);
+
+/*
+ * gdn_gated_rmsnorm -- GatedRMSNorm (ssm.rs `gated_rms_norm_op`) over `rows` rows of
+ * `width` consecutive values (width = the scale's length; x, gate and y are [rows, width]
+ * in memory, any leading shape):
+ *   y = x / sqrt(mean(x^2) + epsilon) * scale * act(gate),
+ *   act(g) = g * sigmoid(g) (GDN_ACT_SILU) or sigmoid(g) (GDN_ACT_SIGMOID),
+ * in fp32, rounded once to io_dtype, which x, scale, gate and y share.  y may be x.
+ * Bad arguments return GDN_ERR_INVALID_ARG before anything is launched.
+ */
+gdn_status gdn_gated_rmsnorm(int32_t io_dtype, int64_t rows, int32_t width, const void *x,
+                             const void *scale, const void *gate, float epsilon,
+                             int32_t activation, void *y, void *stream);
+
 /*
  * gdn_last_device_status -- synchronise `stream`, read the device check word
  * set by any earlier call on the current device, clear it, and return GDN_OK or

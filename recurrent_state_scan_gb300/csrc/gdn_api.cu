@@ -374,6 +374,112 @@ gdn_status gdn_scan_variant(const gdn_shape *shape, const gdn_variant *variant, 
     return GDN_OK;
 }
 
+namespace {
+
+// Geometry rules of the convolution; with_window: the state window is allowed.
+gdn_status check_conv(const gdn_conv_shape *s, bool with_window) {
+    if (s == nullptr) return fail(GDN_ERR_INVALID_ARG, "shape is NULL");
+    if (s->io_dtype != GDN_F32 && s->io_dtype != GDN_BF16 && s->io_dtype != GDN_F16)
+        return fail(GDN_ERR_INVALID_ARG, "io_dtype %d is not a gdn_dtype", s->io_dtype);
+    if (s->batch < 0 || s->seqlen < 0 || s->channels <= 0)
+        return fail(GDN_ERR_INVALID_ARG, "batch, seqlen must be >= 0 and channels > 0");
+    if (s->kernel < 1 || s->kernel > 64 || s->dilation < 1)
+        return fail(GDN_ERR_INVALID_ARG, "kernel must be in 1..64 and dilation >= 1");
+    if ((int64_t)(s->kernel - 1) * s->dilation > 4096)
+        return fail(GDN_ERR_INVALID_ARG, "carry (kernel - 1) * dilation exceeds 4096");
+    if (s->channels_last != 0 && s->channels_last != 1)
+        return fail(GDN_ERR_INVALID_ARG, "channels_last must be 0 or 1");
+    if (s->activation != GDN_ACT_NONE && s->activation != GDN_ACT_SILU)
+        return fail(GDN_ERR_INVALID_ARG, "the convolution's activation is NONE or SILU");
+    if (s->state_window < 0 || s->state_window > 8 || (!with_window && s->state_window != 0))
+        return fail(GDN_ERR_INVALID_ARG, "state_window must be in 0..8 (0 with slots)");
+    return GDN_OK;
+}
+
+gdn_status conv_impl(const gdn_conv_shape *shape, const void *x, const void *weight,
+                     const void *bias, const void *state_in, void *y, void *state_out,
+                     const int32_t *slots, int64_t pool_size, void *stream) {
+    const size_t es = io_size(shape->io_dtype);
+    const bool any = shape->batch > 0 && shape->seqlen > 0;
+    if (any && (!x || !y)) return fail(GDN_ERR_INVALID_ARG, "x or y is NULL");
+    if (shape->batch > 0 && !weight) return fail(GDN_ERR_INVALID_ARG, "weight is NULL");
+    const void *ptrs[] = {x, weight, bias, state_in, y, state_out};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned(ptr, es))
+            return fail(GDN_ERR_INVALID_ARG, "pointer is not %zu-byte aligned", es);
+    if (shape->batch == 0) return GDN_OK;
+    int *word = nullptr;
+    gdn_status st = status_word(&word);
+    if (st != GDN_OK) return st;
+    ConvLaunch l{};
+    l.io = (gdn_dtype)shape->io_dtype;
+    l.x = x; l.w = weight; l.bias = bias; l.state_in = state_in;
+    l.y = y; l.state_out = state_out;
+    l.batch = shape->batch; l.seqlen = shape->seqlen;
+    l.channels = shape->channels; l.kernel = shape->kernel; l.dilation = shape->dilation;
+    l.channels_last = shape->channels_last; l.activation = shape->activation;
+    l.window = shape->state_window;
+    l.slots = slots; l.pool_size = pool_size;
+    l.status = word;
+    // Four channels per thread: channels last, C % 4 == 0, every pointer 4-element aligned.
+    l.vec4 = shape->channels_last && shape->channels % 4 == 0;
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned(ptr, 4 * es)) l.vec4 = false;
+    l.align16 = (!x || aligned(x, 16)) && (!state_in || aligned(state_in, 16));
+    cudaError_t e = launch_causal_conv(l, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "causal conv launch");
+    return GDN_OK;
+}
+
+}  // namespace
+
+gdn_status gdn_causal_conv(const gdn_conv_shape *shape, const void *x, const void *weight,
+                           const void *bias, const void *state_in, void *y, void *state_out,
+                           void *stream) {
+    gdn_status st = check_conv(shape, true);
+    if (st != GDN_OK) return st;
+    return conv_impl(shape, x, weight, bias, state_in, y, state_out, nullptr, 0, stream);
+}
+
+gdn_status gdn_causal_conv_slots(const gdn_conv_shape *shape, const void *x, const void *weight,
+                                 const void *bias, void *pool, int64_t pool_size,
+                                 const int32_t *slots, void *y, void *stream) {
+    gdn_status st = check_conv(shape, false);
+    if (st != GDN_OK) return st;
+    if (!shape->channels_last) return fail(GDN_ERR_INVALID_ARG, "the pool form is channels last");
+    if (pool_size < 0) return fail(GDN_ERR_INVALID_ARG, "pool_size must be >= 0");
+    if (shape->batch > 0 && (!slots || !aligned(slots, 4)))
+        return fail(GDN_ERR_INVALID_ARG, "slots is NULL or misaligned");
+    if (shape->batch > 0 && shape->kernel > 1 && !pool)
+        return fail(GDN_ERR_INVALID_ARG, "pool is NULL");
+    return conv_impl(shape, x, weight, bias, pool, y, pool, slots, pool_size, stream);
+}
+
+gdn_status gdn_gated_rmsnorm(int32_t io_dtype, int64_t rows, int32_t width, const void *x,
+                             const void *scale, const void *gate, float epsilon,
+                             int32_t activation, void *y, void *stream) {
+    if (io_dtype != GDN_F32 && io_dtype != GDN_BF16 && io_dtype != GDN_F16)
+        return fail(GDN_ERR_INVALID_ARG, "io_dtype %d is not a gdn_dtype", io_dtype);
+    if (rows < 0 || width <= 0) return fail(GDN_ERR_INVALID_ARG, "rows >= 0 and width > 0");
+    if (activation != GDN_ACT_SILU && activation != GDN_ACT_SIGMOID)
+        return fail(GDN_ERR_INVALID_ARG, "the norm's activation is SILU or SIGMOID");
+    if (!(epsilon >= 0.0f) || isinf(epsilon))
+        return fail(GDN_ERR_INVALID_ARG, "epsilon must be finite and >= 0");
+    if (rows == 0) return GDN_OK;
+    if (!x || !scale || !gate || !y) return fail(GDN_ERR_INVALID_ARG, "x, scale, gate or y is NULL");
+    const size_t es = io_size(io_dtype);
+    const void *ptrs[] = {x, scale, gate, y};
+    bool vec4 = width % 4 == 0;
+    for (const void *ptr : ptrs) {
+        if (!aligned(ptr, es)) return fail(GDN_ERR_INVALID_ARG, "pointer is not %zu-byte aligned", es);
+        if (!aligned(ptr, 4 * es)) vec4 = false;
+    }
+    cudaError_t e = launch_gated_rmsnorm((gdn_dtype)io_dtype, rows, width, x, scale, gate, epsilon,
+                                         activation, y, vec4, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "gated RMS norm launch");
+    return GDN_OK;
+}
+
 gdn_status gdn_last_device_status(void *stream) {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");

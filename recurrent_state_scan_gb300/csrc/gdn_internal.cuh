@@ -96,6 +96,24 @@ __device__ __forceinline__ bool seq_range(const ScanParams &p, int64_t n, int64_
 // Launchers implemented in the kernel translation units.
 cudaError_t launch_scan_simt(const ScanParams &p, gdn_dtype io, cudaStream_t stream);
 
+// Causal depthwise convolution with a carried state (validated arguments).
+struct ConvLaunch {
+    gdn_dtype io;
+    const void *x, *w, *bias, *state_in;
+    void *y, *state_out;
+    int64_t batch, seqlen;
+    int32_t channels, kernel, dilation, channels_last, activation, window;
+    const int32_t *slots;   // may be null
+    int64_t pool_size;
+    int *status;            // device check word
+    bool vec4;              // channels last, C % 4 == 0 and every pointer 4-element aligned
+    bool align16;           // x and state_in 16-byte aligned (shared-memory staging)
+};
+cudaError_t launch_causal_conv(const ConvLaunch &l, cudaStream_t stream);
+cudaError_t launch_gated_rmsnorm(gdn_dtype io, int64_t rows, int32_t width, const void *x,
+                                 const void *scale, const void *gate, float eps,
+                                 int32_t activation, void *y, bool vec4, cudaStream_t stream);
+
 // Sets the calling thread's last error message; returns `status`.
 gdn_status report_error(gdn_status status, const char *message);
 

@@ -26,10 +26,13 @@ _DTYPE_CODE = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16, torch.float16: 
 EXPORTS = ("gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode_step",
            "gdn_prefill_plan", "gdn_last_device_status", "gdn_status_string",
            "gdn_last_error_message", "gdn_prefill_noalloc", "gdn_decode_step_slots",
-           "gdn_scan_window", "gdn_scan_variant")
+           "gdn_scan_window", "gdn_scan_variant", "gdn_causal_conv", "gdn_causal_conv_slots",
+           "gdn_gated_rmsnorm")
 PATH_SIMT, PATH_TC = 1, 2
 # gdn_rule codes.
 RULES = {"gated_delta": 0, "delta": 1, "gated": 2, "linear": 3}
+# gdn_activation codes.
+ACTIVATIONS = {"none": 0, "silu": 1, "swish": 1, "sigmoid": 2}
 
 
 class GdnShape(ctypes.Structure):
@@ -42,6 +45,14 @@ class GdnShape(ctypes.Structure):
 class GdnVariant(ctypes.Structure):
     _fields_ = [("rule", ctypes.c_int32), ("decay_per_key", ctypes.c_int32),
                 ("beta_shared", ctypes.c_int32)]
+
+
+class GdnConvShape(ctypes.Structure):
+    _fields_ = [("io_dtype", ctypes.c_int32), ("batch", ctypes.c_int32),
+                ("seqlen", ctypes.c_int64), ("channels", ctypes.c_int32),
+                ("kernel", ctypes.c_int32), ("dilation", ctypes.c_int32),
+                ("channels_last", ctypes.c_int32), ("activation", ctypes.c_int32),
+                ("state_window", ctypes.c_int32)]
 
 
 class GdnError(RuntimeError):
@@ -77,6 +88,14 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.gdn_scan_window.restype = ctypes.c_int
     lib.gdn_scan_window.argtypes = [S, P, P, P, P, P, P, P, P, ctypes.c_float, P, P,
                                     ctypes.c_int32, P]
+    CS = ctypes.POINTER(GdnConvShape)
+    lib.gdn_causal_conv.restype = ctypes.c_int
+    lib.gdn_causal_conv.argtypes = [CS, P, P, P, P, P, P, P]
+    lib.gdn_causal_conv_slots.restype = ctypes.c_int
+    lib.gdn_causal_conv_slots.argtypes = [CS, P, P, P, P, ctypes.c_int64, P, P, P]
+    lib.gdn_gated_rmsnorm.restype = ctypes.c_int
+    lib.gdn_gated_rmsnorm.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, P, P, P,
+                                      ctypes.c_float, ctypes.c_int32, P, P]
     lib.gdn_scan_variant.restype = ctypes.c_int
     lib.gdn_scan_variant.argtypes = [S, ctypes.POINTER(GdnVariant), P, P, P, P, P, P, P, P, P,
                                      ctypes.c_float, P, P, P]
@@ -423,3 +442,111 @@ def gdn_scan_variant(q, k, v, a=None, b=None, A_log=None, dt_bias=None, state_in
                                 _ptr(state_in), _ptr(cu_seqlens), float(scale), _ptr(o),
                                 _ptr(state_out), _stream(stream)))
     return o, state_out
+
+
+# ---------------------------------------------------------------- neighbouring ops
+
+def _conv_geometry(x, weight, channels_last: bool):
+    if x.dim() != 3:
+        raise GdnError(GDN_ERR_INVALID_ARG, "x must be [B, L, C] (or [B, C, L])")
+    if x.dtype not in _DTYPE_CODE:
+        raise GdnError(GDN_ERR_INVALID_ARG, f"unsupported io dtype {x.dtype}")
+    B = x.shape[0]
+    L, C = (x.shape[1], x.shape[2]) if channels_last else (x.shape[2], x.shape[1])
+    if weight.numel() == 0 or weight.numel() % C != 0 or weight.shape[0] != C:
+        raise GdnError(GDN_ERR_INVALID_ARG, "weight must be [C, 1, K] or [C, K, 1]")
+    return B, L, C, weight.numel() // C
+
+
+def conv_state_shape(B: int, C: int, K: int, dilation: int = 1, channels_last: bool = True,
+                     state_window: int = 0):
+    carry = (K - 1) * dilation
+    shape = (B, carry, C) if channels_last else (B, C, carry)
+    return ((state_window,) + shape) if state_window else shape
+
+
+def gdn_causal_conv(x, weight, bias=None, state_in=None, *, dilation: int = 1,
+                    channels_last: bool = True, activation: str = "none",
+                    state_window: int = 0, y=None, state_out=None, stream=None):
+    """Causal depthwise convolution with a carried state; returns (y, state_out).
+
+    x [B, L, C] (channels_last) or [B, C, L]; weight [C, 1, K]; bias [C] or None;
+    state_in [B, carry, C] / [B, C, carry] with a leading [W] axis when state_window = W,
+    or None (zeros); carry = (K - 1) * dilation.  ``state_out`` may be ``state_in``."""
+    lib = load()
+    B, L, C, K = _conv_geometry(x, weight, channels_last)
+    dt = x.dtype
+    _need_cuda("x", x, dt)
+    _need_cuda("weight", weight, dt)
+    if bias is not None:
+        _need_cuda("bias", bias, dt)
+        if tuple(bias.shape) != (C,):
+            raise GdnError(GDN_ERR_INVALID_ARG, f"bias must be [{C}]")
+    st_shape = conv_state_shape(B, C, K, dilation, channels_last, state_window)
+    for name, t in (("state_in", state_in), ("state_out", state_out)):
+        if t is not None:
+            _need_cuda(name, t, dt)
+            if tuple(t.shape) != st_shape:
+                raise GdnError(GDN_ERR_INVALID_ARG, f"{name} must be {st_shape}")
+    if y is None:
+        y = torch.empty(x.shape, dtype=dt, device=x.device)
+    else:
+        _need_cuda("y", y, dt)
+    if state_out is None:
+        state_out = torch.empty(st_shape, dtype=dt, device=x.device)
+    shape = GdnConvShape(_DTYPE_CODE[dt], B, L, C, K, int(dilation), int(bool(channels_last)),
+                         ACTIVATIONS[activation], int(state_window))
+    _check(lib.gdn_causal_conv(ctypes.byref(shape), _ptr(x), _ptr(weight), _ptr(bias),
+                               _ptr(state_in), _ptr(y), _ptr(state_out), _stream(stream)))
+    return y, state_out
+
+
+def gdn_causal_conv_slots(x, weight, pool, slots, bias=None, *, dilation: int = 1,
+                          activation: str = "none", y=None, stream=None):
+    """The convolution against a pool of states: row b reads and updates
+    ``pool[slots[b]]`` in place.  x [B, L, C]; pool [P, carry, C]; slots int32 [B].
+    Returns y [B, L, C]."""
+    lib = load()
+    B, L, C, K = _conv_geometry(x, weight, True)
+    dt = x.dtype
+    for name, t in (("x", x), ("weight", weight), ("pool", pool)):
+        _need_cuda(name, t, dt)
+    _need_cuda("slots", slots, torch.int32)
+    carry = (K - 1) * dilation
+    if pool.dim() != 3 or tuple(pool.shape[1:]) != (carry, C):
+        raise GdnError(GDN_ERR_INVALID_ARG, f"pool must be [P, {carry}, {C}]")
+    if tuple(slots.shape) != (B,):
+        raise GdnError(GDN_ERR_INVALID_ARG, "slots must be [B]")
+    if bias is not None:
+        _need_cuda("bias", bias, dt)
+    if y is None:
+        y = torch.empty(x.shape, dtype=dt, device=x.device)
+    else:
+        _need_cuda("y", y, dt)
+    shape = GdnConvShape(_DTYPE_CODE[dt], B, L, C, K, int(dilation), 1, ACTIVATIONS[activation], 0)
+    _check(lib.gdn_causal_conv_slots(ctypes.byref(shape), _ptr(x), _ptr(weight), _ptr(bias),
+                                     _ptr(pool), int(pool.shape[0]), _ptr(slots), _ptr(y),
+                                     _stream(stream)))
+    return y
+
+
+def gdn_gated_rmsnorm(x, scale, gate, eps: float = 1e-5, activation: str = "silu", *, y=None,
+                      stream=None):
+    """y = x / sqrt(mean(x^2) + eps) * scale * act(gate) over rows of len(scale) values."""
+    lib = load()
+    dt = x.dtype
+    if dt not in _DTYPE_CODE:
+        raise GdnError(GDN_ERR_INVALID_ARG, f"unsupported io dtype {dt}")
+    for name, t in (("x", x), ("scale", scale), ("gate", gate)):
+        _need_cuda(name, t, dt)
+    width = scale.numel()
+    if scale.dim() != 1 or width == 0 or x.numel() % width != 0 or gate.shape != x.shape:
+        raise GdnError(GDN_ERR_INVALID_ARG, "scale must be [C] dividing x's size; gate like x")
+    if y is None:
+        y = torch.empty(x.shape, dtype=dt, device=x.device)
+    else:
+        _need_cuda("y", y, dt)
+    _check(lib.gdn_gated_rmsnorm(_DTYPE_CODE[dt], x.numel() // width, width, _ptr(x), _ptr(scale),
+                                 _ptr(gate), float(eps), ACTIVATIONS[activation], _ptr(y),
+                                 _stream(stream)))
+    return y

@@ -121,3 +121,59 @@ def test_variant_rejects_bad_rules_and_missing_gates():
     assert call(gdn.RULES["gated"], A=None) == gdn.GDN_ERR_INVALID_ARG
     assert call(gdn.RULES["delta"], b=None) == gdn.GDN_ERR_INVALID_ARG
     assert call(gdn.RULES["linear"], a=ctypes.c_void_p(0x1001)) == gdn.GDN_ERR_INVALID_ARG
+
+
+def _conv_shape(**kw):
+    base = dict(io_dtype=gdn.GDN_BF16, batch=2, seqlen=8, channels=16, kernel=4, dilation=1,
+                channels_last=1, activation=1, state_window=0)
+    base.update(kw)
+    return gdn.GdnConvShape(*[base[n] for n, _ in gdn.GdnConvShape._fields_])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(io_dtype=9), dict(batch=-1), dict(seqlen=-1), dict(channels=0), dict(kernel=0),
+    dict(kernel=65), dict(dilation=0), dict(kernel=4, dilation=2000), dict(channels_last=2),
+    dict(activation=2), dict(state_window=9), dict(state_window=-1),
+])
+def test_conv_rejects_bad_geometry_before_launch(kw):
+    lib = gdn.load()
+    p = ctypes.c_void_p(0x1000)
+    assert lib.gdn_causal_conv(ctypes.byref(_conv_shape(**kw)), p, p, p, p, p, p, None) == \
+        gdn.GDN_ERR_INVALID_ARG
+
+
+def test_conv_rejects_null_and_misaligned_pointers():
+    lib = gdn.load()
+    p, odd = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x1001)
+    s = ctypes.byref(_conv_shape())
+    assert lib.gdn_causal_conv(s, None, p, None, None, p, None, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_causal_conv(s, p, None, None, None, p, None, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_causal_conv(s, p, p, odd, None, p, None, None) == gdn.GDN_ERR_INVALID_ARG
+    # The pool form: channels last, no window, slots present.
+    assert lib.gdn_causal_conv_slots(ctypes.byref(_conv_shape(channels_last=0)), p, p, None, p, 4,
+                                     p, p, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_causal_conv_slots(ctypes.byref(_conv_shape(state_window=2)), p, p, None, p, 4,
+                                     p, p, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_causal_conv_slots(s, p, p, None, p, 4, None, p, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_causal_conv_slots(s, p, p, None, p, -1, p, p, None) == gdn.GDN_ERR_INVALID_ARG
+    # No rows: nothing to do.
+    assert lib.gdn_causal_conv(ctypes.byref(_conv_shape(batch=0)), None, None, None, None, None,
+                               None, None) == gdn.GDN_OK
+
+
+def test_norm_rejects_bad_arguments_before_launch():
+    lib = gdn.load()
+    p, odd = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x1001)
+
+    def call(io=gdn.GDN_BF16, rows=4, width=128, x=p, eps=1e-6, act=1):
+        return lib.gdn_gated_rmsnorm(io, rows, width, x, p, p, eps, act, p, None)
+
+    assert call(io=5) == gdn.GDN_ERR_INVALID_ARG
+    assert call(rows=-1) == gdn.GDN_ERR_INVALID_ARG
+    assert call(width=0) == gdn.GDN_ERR_INVALID_ARG
+    assert call(act=0) == gdn.GDN_ERR_INVALID_ARG           # the norm has no "none"
+    assert call(eps=-1.0) == gdn.GDN_ERR_INVALID_ARG
+    assert call(eps=float("nan")) == gdn.GDN_ERR_INVALID_ARG
+    assert call(x=None) == gdn.GDN_ERR_INVALID_ARG
+    assert call(x=odd) == gdn.GDN_ERR_INVALID_ARG
+    assert call(rows=0, x=None) == gdn.GDN_OK

@@ -203,3 +203,125 @@ def small_spec(name="small", io="bf16", batch=1, seqlen=0, lengths=None, h_qk=2,
                 state_std=state_std, decode=decode, qk_scale=qk_scale,
                 pool_size=pool_size, pool_std=pool_std, window=window,
                 decay_per_key=decay_per_key, beta_shared=beta_shared)
+
+
+# ---------------------------------------------------------------- neighbouring ops
+#
+# The causal convolution that feeds q, k, v and the gated RMS norm of the scan's output.
+# Recipe (one default_rng(seed), float64 draws in this order): x ~ N(0, 1); the weight
+# ~ U(-1/sqrt(K), 1/sqrt(K)) (a depthwise conv's fan-in is K); the bias (when asked)
+# likewise; the past state ~ N(0, state_std) (state_std 0: none) -- a window of them when
+# state_window > 0, or a pool of pool_size entries followed by the slots, the first B
+# entries of a permutation of the pool.  The norm draws x ~ N(0, 1), the gate ~ N(0, 1)
+# and the scale ~ N(1, 0.1).  Every draw is rounded once to the I/O dtype.
+
+@dataclasses.dataclass(frozen=True)
+class ConvSpec:
+    name: str
+    io: str
+    batch: int
+    seqlen: int
+    channels: int
+    seed: int
+    kernel: int = 4
+    dilation: int = 1
+    channels_last: bool = True
+    silu: bool = True
+    bias: bool = False
+    state_std: float = 0.0
+    state_window: int = 0
+    pool_size: int = 0
+    decode: bool = False         # one token per row, the state updated in place
+
+
+@dataclasses.dataclass
+class ConvInputs:
+    spec: ConvSpec
+    x: torch.Tensor               # [B, L, C] (channels first: [B, C, L])
+    w: torch.Tensor               # [C, 1, K]
+    bias: Optional[torch.Tensor]  # [C]
+    state_in: Optional[torch.Tensor]   # [(W,) B, carry, C] / [(W,) B, C, carry]
+    pool: Optional[torch.Tensor]       # [pool_size, carry, C]
+    slots: Optional[torch.Tensor]      # int32 [B]
+    f64: dict
+
+
+@dataclasses.dataclass(frozen=True)
+class NormSpec:
+    name: str
+    io: str
+    shape: tuple                 # x's shape; the last dimension is the row width
+    seed: int
+    eps: float = 1e-6
+    activation: str = "silu"
+
+
+@dataclasses.dataclass
+class NormInputs:
+    spec: NormSpec
+    x: torch.Tensor
+    scale: torch.Tensor
+    gate: torch.Tensor
+    f64: dict
+
+
+def draw_conv(spec: ConvSpec) -> ConvInputs:
+    rng = np.random.default_rng(spec.seed)
+    B, L, C, K = spec.batch, spec.seqlen, spec.channels, spec.kernel
+    carry = (K - 1) * spec.dilation
+    x = rng.standard_normal((B, L, C) if spec.channels_last else (B, C, L))
+    lim = 1.0 / math.sqrt(K)
+    w = rng.uniform(-lim, lim, (C, 1, K))
+    bias = rng.uniform(-lim, lim, C) if spec.bias else None
+    st_one = (B, carry, C) if spec.channels_last else (B, C, carry)
+    state = pool = slots = None
+    if spec.pool_size > 0:
+        pool = rng.normal(0.0, spec.state_std, (spec.pool_size, carry, C))
+        slots = rng.permutation(spec.pool_size)[:B].astype(np.int32)
+    elif spec.state_std > 0.0:
+        shape = ((spec.state_window,) + st_one) if spec.state_window else st_one
+        state = rng.normal(0.0, spec.state_std, shape)
+    t = {n: (None if a is None else _round(a, spec.io))
+         for n, a in (("x", x), ("w", w), ("bias", bias), ("state_in", state), ("pool", pool))}
+    f64 = {n: (None if v is None else _widen(v).reshape(v.shape)) for n, v in t.items()}
+    return ConvInputs(spec=spec, x=t["x"], w=t["w"], bias=t["bias"], state_in=t["state_in"],
+                      pool=t["pool"], slots=None if slots is None else torch.from_numpy(slots),
+                      f64=f64)
+
+
+def draw_norm(spec: NormSpec) -> NormInputs:
+    rng = np.random.default_rng(spec.seed)
+    x = rng.standard_normal(spec.shape)
+    gate = rng.standard_normal(spec.shape)
+    scale = rng.normal(1.0, 0.1, spec.shape[-1])
+    t = {"x": _round(x, spec.io), "gate": _round(gate, spec.io), "scale": _round(scale, spec.io)}
+    f64 = {n: _widen(v).reshape(v.shape) for n, v in t.items()}
+    return NormInputs(spec=spec, x=t["x"], scale=t["scale"], gate=t["gate"], f64=f64)
+
+
+# The measured neighbour workloads.  Channels: q, k, v side by side, at the GQA prefill's
+# head counts (2 x 16 x 128 + 32 x 128 = 8192) and the decode step's (3 x 32 x 128 = 12288).
+CONV_WORKLOADS = {
+    "bf16_conv_prefill_gqa": ConvSpec(
+        "bf16_conv_prefill_gqa", io="bf16", batch=2, seqlen=8192, channels=8192, seed=1010,
+        state_std=1.0),
+    "bf16_conv_decode_b256": ConvSpec(
+        "bf16_conv_decode_b256", io="bf16", batch=256, seqlen=1, channels=12288, seed=1011,
+        state_std=1.0, decode=True),
+}
+NORM_WORKLOADS = {
+    # The scan output of the GQA prefill, [2, 8192, 32, 128], normalised per head.
+    "bf16_norm_gqa": NormSpec("bf16_norm_gqa", io="bf16", shape=(2, 8192, 32, 128), seed=1012),
+}
+
+
+def any_workload(name: str):
+    """Draw any named workload: the scan's, the convolution's or the norm's."""
+    if name in WORKLOADS:
+        return draw(WORKLOADS[name])
+    if name in CONV_WORKLOADS:
+        return draw_conv(CONV_WORKLOADS[name])
+    return draw_norm(NORM_WORKLOADS[name])
+
+
+ALL_WORKLOADS = sorted(list(WORKLOADS) + list(CONV_WORKLOADS) + list(NORM_WORKLOADS))
