@@ -697,7 +697,7 @@ def main():
             "traffic": profiled_traffic(inp_name, "decode" if bandwidth_metric(s) else "prefill"),
             "peak_source": f"{pk_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"
             if pk_kind == "measured" else "fallback 6.8 TB/s",
-            "kernels": "gdn_decode (scan_simt)" if bandwidth_metric(s) else "gdn_chunk_prep + gdn_chunk_scan, one call"}
+            "kernels": prefill_kernels(inp)}
     if not bandwidth_metric(s):
         roof["tensor_tflops"] = tfs
         roof["tensor_frac_of_bf16_peak"] = tfs / pk["bf16_tflops"]
@@ -725,6 +725,20 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def prefill_kernels(inp) -> str:
+    """The kernels one call runs, named for the roofline entry."""
+    from recurrent_state_scan_gb300 import gdn
+    if bandwidth_metric(inp.spec):
+        return "gdn_decode (scan_simt)"
+    path, _ = gdn.gdn_prefill_plan(gdn.shape_of_spec(inp.spec, inp.n_seq, inp.total_tokens))
+    if path == gdn.PATH_TC_TP:
+        return ("gdn_chunk_prep + gdn_chunk_scan (time-parallel segments) + gdn_tp_combine, "
+                "and the cuBLAS correction GEMM, one call")
+    if path == gdn.PATH_TC:
+        return "gdn_chunk_prep + gdn_chunk_scan, one call"
+    return "scan_simt, one call"
 
 
 def dtype_of(inp) -> str:

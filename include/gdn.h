@@ -110,11 +110,16 @@ typedef struct gdn_shape {
  * and o must then be 16-byte aligned, else the SIMT path runs); other shapes and
  * fp32 I/O run the token-sequential SIMT path.  State math is fp32 always.
  *
- * On the tensor-core path a batched call whose scan uses few SMs is split along
- * the time axis into chunk segments; the preparation of a later segment then runs
- * on a stream internal to the library (one per device, created on first use)
- * beside the scan of the earlier one.  The internal work is ordered after what
- * `stream` held at the call and the call's last kernel is ordered after it, so
+ * On the tensor-core path a batched call whose scan uses few SMs is cut along the
+ * time axis into segments that are scanned at once (each from a zero state and, for
+ * the correction, from the identity with the values zeroed), then combined; the
+ * correction o += R S_k of each later segment is a cuBLAS batched GEMM (one handle per
+ * device, created on first use, working in the workspace).  That needs the full
+ * gdn_prefill_workspace_bytes(shape); a workspace that holds only the chunk records
+ * (81 KiB per chunk and value head) instead splits the call into chunk segments whose
+ * preparation runs on a stream internal to the library (one per device, created on
+ * first use) beside the scan of the earlier one.  Either way the work is ordered after
+ * what `stream` held at the call and the call's last kernel is ordered after it, so
  * the call keeps the stream-ordered semantics above.
  */
 size_t gdn_prefill_workspace_bytes(const gdn_shape *shape);
@@ -306,8 +311,11 @@ gdn_status gdn_last_device_status(void *stream);
 /*
  * gdn_prefill_plan -- report, without launching anything, which kernel path
  * gdn_prefill takes for `shape` (*path: 1 = token-sequential SIMT scan,
- * 2 = chunked tensor-core scan) and how many kernels one call launches
- * (*launches).  Returns the same status gdn_prefill's shape checks would.
+ * 2 = chunked tensor-core scan, 3 = chunked tensor-core scan run time-parallel) and how
+ * many of the library's own kernels one call launches (*launches; the time-parallel
+ * scan's correction GEMMs are cuBLAS calls on top).  Path 3 assumes the workspace that
+ * gdn_prefill_workspace_bytes reports; with less (down to the records alone) the call
+ * takes path 2.  Returns the same status gdn_prefill's shape checks would.
  */
 gdn_status gdn_prefill_plan(const gdn_shape *shape, int32_t *path, int32_t *launches);
 

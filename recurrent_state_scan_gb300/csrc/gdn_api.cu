@@ -138,9 +138,12 @@ gdn_status gdn_prefill_plan(const gdn_shape *shape, int32_t *path, int32_t *laun
     const bool varlen = shape->batch == 1 && shape->num_seqs != 1;
     const int64_t tokens = varlen ? shape->seqlen : shape->seqlen * (int64_t)shape->batch;
     const bool tc = prefill_tc_shape_ok((gdn_dtype)shape->io_dtype, shape->d_k, shape->d_v, tokens);
-    if (path) *path = tc ? 2 : 1;
+    // Time-parallel scan: prep, scan and one combine per segment boundary (the correction
+    // GEMMs are library calls); else the prep and scan of every chunk segment.
+    const int tps = tc ? prefill_tc_tp_nseg(varlen, shape->seqlen, shape->batch, shape->h_v) : 1;
+    if (path) *path = tc ? (tps > 1 ? 3 : 2) : 1;
     const int nseg = tc ? prefill_tc_segments(varlen, shape->seqlen, shape->batch, shape->h_v) : 1;
-    if (launches) *launches = shape->num_seqs > 0 ? (tc ? 2 * nseg : 1) : 0;
+    if (launches) *launches = shape->num_seqs > 0 ? (tc ? (tps > 1 ? 1 + tps : 2 * nseg) : 1) : 0;
     return GDN_OK;
 }
 
@@ -153,7 +156,10 @@ size_t gdn_prefill_workspace_bytes(const gdn_shape *shape) {
     const bool packed = shape->batch == 1;
     const int64_t tokens = packed ? shape->seqlen : shape->seqlen * (int64_t)shape->batch;
     if (!prefill_tc_shape_ok((gdn_dtype)shape->io_dtype, shape->d_k, shape->d_v, tokens)) return 0;
-    return prefill_tc_workspace(packed, shape->seqlen, shape->batch, shape->num_seqs, shape->h_v);
+    // Records, plus the time-parallel scan's buffers when a batched call of this shape
+    // would use it (with batch 1 the shape may also be a packed call: the sum covers both).
+    return prefill_tc_workspace(packed, shape->seqlen, shape->batch, shape->num_seqs, shape->h_v) +
+           prefill_tc_tp_bytes(false, shape->seqlen, shape->batch, shape->h_v);
 }
 
 gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, const void *v,
@@ -204,7 +210,8 @@ gdn_status gdn::prefill_impl(const gdn_shape *shape, const void *q, const void *
             return fail(GDN_ERR_INVALID_ARG, "workspace of %zu bytes is below the %zu this call needs",
                         workspace == nullptr ? (size_t)0 : workspace_bytes, need);
         if (!aligned(workspace, 16)) return fail(GDN_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
-        e = launch_prefill_tc(p, io, tokens, workspace, allow_overlap, (cudaStream_t)stream);
+        e = launch_prefill_tc(p, io, tokens, workspace, workspace_bytes, allow_overlap,
+                              (cudaStream_t)stream);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");
     } else {
         e = launch_scan_simt(p, io, (cudaStream_t)stream);

@@ -129,8 +129,15 @@ bool prefill_tc_supported(const ScanParams &p, gdn_dtype io, int64_t total_token
 // grid leaves most of the GPU idle run the prep of later segments on an internal stream
 // beside the scan of earlier ones; each segment costs one prep and one scan launch.
 int prefill_tc_segments(bool varlen, int64_t seqlen, int64_t batch, int h_v);
+// Time-parallel scan of batched shapes whose scan grid leaves most of the GPU idle: the
+// segments it uses (1: none) and the workspace bytes it needs after the records (0: none).
+int prefill_tc_tp_nseg(bool varlen, int64_t seqlen, int64_t batch, int h_v);
+size_t prefill_tc_tp_bytes(bool varlen, int64_t seqlen, int64_t batch, int h_v);
+// workspace_bytes: the caller's workspace size; the time-parallel scan runs only when the
+// workspace also holds its buffers (and allow_overlap is set).
 cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_tokens,
-                              void *workspace, bool allow_overlap, cudaStream_t stream);
+                              void *workspace, size_t workspace_bytes, bool allow_overlap,
+                              cudaStream_t stream);
 
 // gdn_prefill with the segment overlap allowed or not (no internal stream is created
 // when it is not).

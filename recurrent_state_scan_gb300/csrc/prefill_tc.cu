@@ -27,6 +27,7 @@
 // half needs only its half of U and Delta.  All MMAs use M = 128, so accumulator row r
 // is TMEM lane r.  Rows past the end of a sequence get g = 0 and beta = 0, which makes
 // their T row the unit row and their W, U and Delta rows exactly zero.
+#include <cublas_v2.h>
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -82,6 +83,15 @@ struct TcParams {
     float scale;
     int *status;
     uint8_t *ws;                    // workspace records
+    // Time-parallel scan (tp_seg > 0): every sequence is cut into tp_nseg segments of
+    // tp_seg chunks, all scanned at once.  Segment k > 0 runs twice: from a zero state
+    // (outputs to o, end state to tp_psi[k]) and as the operator pass, from the identity
+    // with U = 0 (outputs R to tm_r, end state Phi_k to tp_phi[k]).  Segment 0 runs once
+    // from state_in (end state to tp_psi[0]).  A combine and a correction GEMM follow.
+    int32_t tp_seg, tp_nseg;
+    float *tp_phi, *tp_psi;         // [tp_nseg][N][h_v][128][128] fp32
+    CUtensorMap tm_r;               // R: [tokens][h_v][128] in the I/O type
+    void *tp_r;
 };
 
 // First workspace slot of sequence n.  Batched: n * chunks_per_seq.  Packed: slot
@@ -332,7 +342,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
     uint8_t *rec = p.ws + ((size_t)slot * p.h_v + h) * kRecord;
     // A segment's first chunk writes W for the scan to start from; every other chunk
     // writes W' and M into its predecessor's record.
-    const bool first = (c == p.seg_begin);
+    const bool first = (c == p.seg_begin) || (p.tp_seg > 0 && c % p.tp_seg == 0);
 
     float *const As = reinterpret_cast<float *>(sm + PP_AS);
     const uint32_t aKQW = smem_u32(sm + PP_KQW), aTT = smem_u32(sm + PP_TT), aV = smem_u32(sm + PP_V);
@@ -731,9 +741,20 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool issue_warp = (warp == kChainWarps);
     const bool copy_warp = (warp == kChainWarps + 1);
-    const int half = blockIdx.x & 1;
-    const int h = (blockIdx.x >> 1) % p.h_v;
-    int64_t n = (int64_t)(blockIdx.x >> 1) / p.h_v;
+    // Time-parallel job of this CTA: 0 is segment 0; 2k - 1 is segment k from a zero
+    // state; 2k is segment k's operator pass (identity state, U = 0).
+    int64_t unit = blockIdx.x;
+    int job = 0;
+    if (p.tp_seg > 0) {
+        const int64_t units = (int64_t)p.num_seqs * p.h_v * (kDK / kNV);
+        job = (int)(unit / units);
+        unit %= units;
+    }
+    const int tseg = (job + 1) / 2;
+    const bool op_pass = job > 0 && (job & 1) == 0;
+    const int half = (int)(unit & 1);
+    const int h = (int)((unit >> 1) % p.h_v);
+    int64_t n = (unit >> 1) / p.h_v;
     const int hq = h / (p.h_v / p.h_qk);
     const int v0 = half * kNV;
 
@@ -760,8 +781,10 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
     // This launch walks chunks [seg_begin, seg_end) of the sequence; below, chunk c
     // counts from the segment's first chunk, and t0 / L / base_slot are shifted to it.
     const int64_t all_chunks = (t1 - t0 + kC - 1) / kC;
-    const int64_t cb = p.seg_begin < all_chunks ? p.seg_begin : all_chunks;
-    const int64_t ce = p.seg_end < all_chunks ? p.seg_end : all_chunks;
+    const int64_t seg_b = p.tp_seg > 0 ? (int64_t)tseg * p.tp_seg : p.seg_begin;
+    const int64_t seg_e = p.tp_seg > 0 ? seg_b + p.tp_seg : p.seg_end;
+    const int64_t cb = seg_b < all_chunks ? seg_b : all_chunks;
+    const int64_t ce = seg_e < all_chunks ? seg_e : all_chunks;
     const int nchunks = (int)(ce - cb);
     const int64_t base_slot = slot_base(p, n) + cb;
     t0 += cb * kC;
@@ -789,7 +812,7 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
         ctl.abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&p.tm_k);
-        tma_prefetch_desc(&p.tm_o);
+        tma_prefetch_desc(op_pass ? &p.tm_r : &p.tm_o);
     }
     tc_fence_before();
     __syncthreads();
@@ -952,13 +975,19 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
         const int row = 32 * q + lane;             // this thread's TMEM lane
         const bool out_warp = q < 2;               // lanes 0-63: output rows
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-        IO *go = static_cast<IO *>(p.o);
+        IO *go = static_cast<IO *>(op_pass ? p.tp_r : p.o);
+        const CUtensorMap *omap = op_pass ? &p.tm_r : &p.tm_o;
         float S[32];                               // S[row][v0 + 32 g + e]
-        {
+        if (op_pass) {
+            // The identity, this thread's row and columns.
+#pragma unroll
+            for (int e = 0; e < 32; ++e) S[e] = (row == v0 + 32 * g + e) ? 1.f : 0.f;
+        } else {
+            const bool zero = p.state_in == nullptr || tseg > 0;
             const float4 *src = reinterpret_cast<const float4 *>(p.state_in + sbase + (size_t)row * kDK + v0 + 32 * g);
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
-                const float4 f = p.state_in ? src[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 f = zero ? make_float4(0.f, 0.f, 0.f, 0.f) : src[q4];
                 S[4 * q4] = f.x; S[4 * q4 + 1] = f.y; S[4 * q4 + 2] = f.z; S[4 * q4 + 3] = f.w;
             }
         }
@@ -1011,6 +1040,10 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                             }
                         }
                         tmem_ld_wait();
+                        if (op_pass) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) x[e] = 0.f;
+                        }
 #pragma unroll
                         for (int e = 0; e < 16; ++e) x[e] -= __uint_as_float(ws[e]);
 #pragma unroll
@@ -1093,13 +1126,16 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                 break;
             }
             if (tid == 0 && tile_store) {
-                tma_store_3d(&p.tm_o, ob, v0, h, (int)(t0 + (int64_t)c * kC));
+                tma_store_3d(omap, ob, v0, h, (int)(t0 + (int64_t)c * kC));
                 bulk_commit();
             }
         }
         if (tid == 0) bulk_wait_all();    // the output tiles have reached global memory
         if (ok) {
-            float4 *dst = reinterpret_cast<float4 *>(p.state_out + sbase + (size_t)row * kDK + v0 + 32 * g);
+            float *sdst = p.state_out;
+            if (p.tp_seg > 0)
+                sdst = (op_pass ? p.tp_phi : p.tp_psi) + (size_t)tseg * p.num_seqs * p.h_v * kDK * kDK;
+            float4 *dst = reinterpret_cast<float4 *>(sdst + sbase + (size_t)row * kDK + v0 + 32 * g);
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4)
                 dst[q4] = make_float4(S[4 * q4], S[4 * q4 + 1], S[4 * q4 + 2], S[4 * q4 + 3]);
@@ -1113,6 +1149,62 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, 256);
+    }
+}
+
+// ===================================================================== time-parallel combine
+// The state entering segment k of a sequence: S_1 = Psi_0 (segment 0 ran from state_in),
+// S_{k+1} = Phi_k S_k + Psi_k.  One launch per step k: a CTA owns a 32 x 32 tile of
+// S_{k+1} for one (sequence, head), with its 32 rows of Phi_k and 32 columns of S_k staged
+// in shared memory, and writes it over Psi_k (each element is read, then written, by one
+// thread), so Psi_k holds S_{k+1} afterwards.  It also writes its 32 rows of S_k, in the
+// I/O type, for the correction GEMM; the last step writes state_out as well.
+template <typename IO>
+__global__ void __launch_bounds__(256) gdn_tp_combine(const __grid_constant__ TcParams p, IO *sk, int k) {
+    __shared__ float Ph[32][kDK + 1];     // rows rb .. rb + 31 of Phi_k
+    __shared__ float Sc[kDK][33];         // columns cb .. cb + 31 of S_k
+    const size_t off = (size_t)blockIdx.x * kDK * kDK;           // (n, h) slab
+    const size_t slab = (size_t)p.num_seqs * p.h_v * kDK * kDK;   // one segment
+    const int cb = 32 * (blockIdx.y & 3), rb = 32 * (blockIdx.y >> 2);
+    const int tid = threadIdx.x;
+    const float *sprev = p.tp_psi + (size_t)(k - 1) * slab + off;   // S_k
+    const float *phi = p.tp_phi + (size_t)k * slab + off;
+    float *psi = p.tp_psi + (size_t)k * slab + off;
+    // All 32 loads of a thread in flight at once, then the stores to shared memory.
+    float ph[16], sc[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+        const int e = tid + 256 * u;
+        ph[u] = phi[(size_t)(rb + (e >> 7)) * kDK + (e & 127)];
+        sc[u] = sprev[(size_t)(e >> 5) * kDK + cb + (e & 31)];
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+        const int e = tid + 256 * u;
+        Ph[e >> 7][e & 127] = ph[u];
+        Sc[e >> 5][e & 31] = sc[u];
+    }
+    __syncthreads();
+    // This CTA's rows of S_k for the GEMM (every element of S_k is written by one CTA).
+    IO *skk = sk + (size_t)k * slab + off;
+    for (int e = tid; e < 32 * 32; e += 256)
+        IoType<IO>::st(skk + (size_t)(rb + (e >> 5)) * kDK + cb + (e & 31), Sc[rb + (e >> 5)][e & 31]);
+    // Thread: column j, rows i0 .. i0 + 3.
+    const int j = tid & 31, i0 = 4 * (tid >> 5);
+    float acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = psi[(size_t)(rb + i0 + i) * kDK + cb + j];
+#pragma unroll 8
+    for (int m = 0; m < kDK; ++m) {
+        const float sv = Sc[m][j];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] = fmaf(Ph[i0 + i][m], sv, acc[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const size_t at = (size_t)(rb + i0 + i) * kDK + cb + j;
+        psi[at] = acc[i];
+        if (k == p.tp_nseg - 1) p.state_out[off + at] = acc[i];
     }
 }
 
@@ -1280,7 +1372,130 @@ int64_t chunk_slots(bool varlen, int64_t seqlen, int64_t batch, int64_t num_seqs
     return seqlen / kC + num_seqs + 1;
 }
 
+constexpr int kMaxTpSegments = 4;
+constexpr int kMinTpChunks = 16;
+constexpr size_t kBlasWorkspace = 4u << 20;
+
+// Segments of the time-parallel scan for a batched shape (1: not used).  Every segment
+// after the first costs two scan CTAs per (sequence, head, column half), and all of them
+// must fit on the GPU at once.
+int tp_segments(bool varlen, int64_t seqlen, int64_t batch, int h_v) {
+    if (varlen) return 1;
+    const int sms = sm_count();
+    const int64_t units = batch * h_v * (kDK / kNV);
+    const int64_t chunks = (seqlen + kC - 1) / kC;
+    int best = 1;
+    for (int s2 = 2; s2 <= kMaxTpSegments; ++s2)
+        if (units * (2 * s2 - 1) <= sms && chunks >= (int64_t)s2 * kMinTpChunks) best = s2;
+    return best;
+}
+
+// Bytes the time-parallel scan adds after the records: R, Phi, Psi, the S_k copies and
+// the GEMM library's workspace, each 1 KiB aligned.
+struct TpLayout {
+    size_t r, phi, psi, sk, blas, total;
+};
+TpLayout tp_layout(int64_t seqlen, int64_t batch, int h_v, int nseg) {
+    auto up = [](size_t x) { return (x + 1023) & ~(size_t)1023; };
+    TpLayout L{};
+    const size_t tok = (size_t)seqlen * batch;
+    const size_t states = (size_t)nseg * batch * h_v * kDK * kDK;
+    L.r = 0;
+    L.phi = L.r + up(tok * h_v * kDK * 2);
+    L.psi = L.phi + up(states * 4);
+    L.sk = L.psi + up(states * 4);
+    L.blas = L.sk + up(states * 2);
+    L.total = L.blas + kBlasWorkspace;
+    return L;
+}
+
+// One GEMM library handle per device, created on first use (it allocates once).
+struct Blas {
+    cublasHandle_t h = nullptr;
+    bool tried = false;
+    std::mutex mu;   // the handle's stream and workspace belong to one call at a time
+};
+Blas *blas() {
+    static Blas cache[64];
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    Blas &b = cache[dev];
+    if (!b.tried) {
+        b.tried = true;
+        if (cublasCreate(&b.h) != CUBLAS_STATUS_SUCCESS) b.h = nullptr;
+    }
+    return b.h ? &b : nullptr;
+}
+
+// The time-parallel call: prep, the scan of every segment and operator pass at once, the
+// combine, then o_t += R_t S_k for the tokens of every segment k >= 1 (one batched GEMM
+// over heads per sequence and segment, bf16/f16 in, fp32 accumulation).
+template <typename IO>
+cudaError_t launch_tp(TcParams tp, int64_t n_slots, int nseg, uint8_t *extra, Blas *bl,
+                      cudaStream_t stream) {
+    cudaError_t e = configure<IO>();
+    if (e != cudaSuccess) return e;
+    const TpLayout L = tp_layout(tp.seqlen, tp.num_seqs, tp.h_v, nseg);
+    const int cps = tp.chunks_per_seq;
+    tp.tp_nseg = nseg;
+    tp.tp_seg = (cps + nseg - 1) / nseg;
+    tp.tp_r = extra + L.r;
+    tp.tp_phi = reinterpret_cast<float *>(extra + L.phi);
+    tp.tp_psi = reinterpret_cast<float *>(extra + L.psi);
+    IO *sk = reinterpret_cast<IO *>(extra + L.sk);
+    tp.seg_begin = 0;
+    tp.seg_end = 0x7fffffff;
+    tp.seg_direct = 0;
+    e = launch_prep<IO>(tp, n_slots * tp.h_v, stream);
+    if (e != cudaSuccess) return e;
+    const int64_t units = (int64_t)tp.num_seqs * tp.h_v * (kDK / kNV);
+    gdn_chunk_scan<IO><<<(unsigned)(units * (2 * nseg - 1)), kScanAllThreads, kScanSmem, stream>>>(tp);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    for (int k = 1; k < nseg; ++k) {
+        gdn_tp_combine<IO><<<dim3((unsigned)(tp.num_seqs * tp.h_v), 16), 256, 0, stream>>>(tp, sk, k);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+
+    std::lock_guard<std::mutex> lock(bl->mu);
+    if (cublasSetStream(bl->h, stream) != CUBLAS_STATUS_SUCCESS ||
+        cublasSetWorkspace(bl->h, extra + L.blas, kBlasWorkspace) != CUBLAS_STATUS_SUCCESS)
+        return cudaErrorUnknown;
+    const cudaDataType_t dt = std::is_same<IO, __nv_bfloat16>::value ? CUDA_R_16BF : CUDA_R_16F;
+    const float one = 1.f;
+    const int64_t row = (int64_t)tp.h_v * kDK;            // elements between tokens
+    const size_t slab = (size_t)tp.num_seqs * tp.h_v * kDK * kDK;
+    for (int64_t n = 0; n < tp.num_seqs; ++n)
+        for (int k = 1; k < nseg; ++k) {
+            const int64_t tb = (int64_t)k * tp.tp_seg * kC;
+            if (tb >= tp.seqlen) break;
+            const int64_t cnt = (tp.seqlen - tb) < (int64_t)tp.tp_seg * kC ? (tp.seqlen - tb)
+                                                                           : (int64_t)tp.tp_seg * kC;
+            const size_t tok = (size_t)(n * tp.seqlen + tb);
+            // Column-major view: o^T (128 x cnt) += S_k^T (128 x 128) R^T (128 x cnt), per head.
+            const IO *A = sk + k * slab + (size_t)n * tp.h_v * kDK * kDK;
+            const IO *B = static_cast<const IO *>(tp.tp_r) + tok * row;
+            IO *C = static_cast<IO *>(tp.o) + tok * row;
+            if (cublasGemmStridedBatchedEx(bl->h, CUBLAS_OP_N, CUBLAS_OP_N, kDK, (int)cnt, kDK, &one,
+                                           A, dt, kDK, (long long)kDK * kDK, B, dt, (int)row, kDK,
+                                           &one, C, dt, (int)row, kDK, tp.h_v, CUBLAS_COMPUTE_32F,
+                                           CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+                return cudaErrorUnknown;
+        }
+    return cudaSuccess;
+}
+
 }  // namespace
+
+size_t prefill_tc_tp_bytes(bool varlen, int64_t seqlen, int64_t batch, int h_v) {
+    const int nseg = tp_segments(varlen, seqlen, batch, h_v);
+    return nseg > 1 ? tp_layout(seqlen, batch, h_v, nseg).total : 0;
+}
+
+int prefill_tc_tp_nseg(bool varlen, int64_t seqlen, int64_t batch, int h_v) {
+    return tp_segments(varlen, seqlen, batch, h_v);
+}
 
 bool prefill_tc_shape_ok(gdn_dtype io, int d_k, int d_v, int64_t total_tokens) {
     return (io == GDN_BF16 || io == GDN_F16) && d_k == kDK && d_v == kDK && total_tokens > 0 &&
@@ -1308,7 +1523,7 @@ bool prefill_tc_supported(const ScanParams &p, gdn_dtype io, int64_t total_token
 }
 
 cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_tokens, void *workspace,
-                              bool allow_overlap, cudaStream_t stream) {
+                              size_t workspace_bytes, bool allow_overlap, cudaStream_t stream) {
     TcParams tp;
     memset(&tp, 0, sizeof(tp));
     if (!make_map(&tp.tm_q, p.q, io, p.h_qk, total_tokens) ||
@@ -1324,6 +1539,21 @@ cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_t
     tp.ws = static_cast<uint8_t *>(workspace);
     const bool varlen = p.cu_seqlens != nullptr;
     const int64_t n_slots = chunk_slots(varlen, p.seqlen, p.num_seqs, p.num_seqs);
+    // The time-parallel scan, when the shape suits it, the caller allows internal
+    // resources and the workspace holds its buffers.
+    const size_t records = prefill_tc_workspace(varlen, p.seqlen, p.num_seqs, p.num_seqs, p.h_v);
+    const int tps = allow_overlap ? tp_segments(varlen, p.seqlen, p.num_seqs, p.h_v) : 1;
+    if (tps > 1 && workspace_bytes >= records + tp_layout(p.seqlen, p.num_seqs, p.h_v, tps).total) {
+        Blas *bl = blas();
+        if (bl != nullptr) {
+            uint8_t *extra = static_cast<uint8_t *>(workspace) + records;
+            if (!make_map(&tp.tm_r, extra + tp_layout(p.seqlen, p.num_seqs, p.h_v, tps).r, io, p.h_v,
+                          total_tokens))
+                return cudaErrorInvalidValue;
+            if (io == GDN_BF16) return launch_tp<__nv_bfloat16>(tp, n_slots, tps, extra, bl, stream);
+            return launch_tp<__half>(tp, n_slots, tps, extra, bl, stream);
+        }
+    }
     const int nseg = allow_overlap ? prefill_tc_segments(varlen, p.seqlen, p.num_seqs, p.h_v) : 1;
     if (io == GDN_BF16) return launch_typed<__nv_bfloat16>(tp, n_slots, nseg, stream);
     return launch_typed<__half>(tp, n_slots, nseg, stream);

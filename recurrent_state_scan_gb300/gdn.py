@@ -28,7 +28,7 @@ EXPORTS = ("gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode_step",
            "gdn_last_error_message", "gdn_prefill_noalloc", "gdn_decode_step_slots",
            "gdn_scan_window", "gdn_scan_variant", "gdn_causal_conv", "gdn_causal_conv_slots",
            "gdn_gated_rmsnorm")
-PATH_SIMT, PATH_TC = 1, 2
+PATH_SIMT, PATH_TC, PATH_TC_TP = 1, 2, 3
 # gdn_rule codes.
 RULES = {"gated_delta": 0, "delta": 1, "gated": 2, "linear": 3}
 # gdn_activation codes.
@@ -309,7 +309,7 @@ def path_dtype(spec, n_seq: int = 0, total_tokens: int = 0) -> str:
     if _simt_only(spec):
         return "f32"
     path = gdn_prefill_plan(shape_of_spec(spec, n_seq, total_tokens))[0]
-    return spec.io if path == PATH_TC else "f32"
+    return spec.io if path in (PATH_TC, PATH_TC_TP) else "f32"
 
 
 def gdn_last_device_status(stream=None) -> int:

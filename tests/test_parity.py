@@ -115,7 +115,8 @@ def test_prefill_small(case):
 def test_plan_takes_the_tensor_core_path_for_16bit_d128():
     from recurrent_state_scan_gb300 import gdn
     for io in (gdn.GDN_BF16, gdn.GDN_F16):
-        assert gdn.gdn_prefill_plan(gdn.make_shape(io, 1, 4096, 1, 16, 16, 128, 128))[0] == gdn.PATH_TC
+        assert gdn.gdn_prefill_plan(gdn.make_shape(io, 1, 4096, 1, 16, 16, 128, 128))[0] in \
+            (gdn.PATH_TC, gdn.PATH_TC_TP)
     assert gdn.gdn_prefill_plan(gdn.make_shape(gdn.GDN_F32, 1, 64, 1, 2, 2, 32, 32))[0] == gdn.PATH_SIMT
     assert gdn.gdn_prefill_plan(gdn.make_shape(gdn.GDN_BF16, 1, 64, 1, 2, 2, 64, 64))[0] == gdn.PATH_SIMT
 
@@ -220,16 +221,44 @@ def test_bad_device_cu_seqlens_sets_check_word():
     check(inp, o, s, o_ref, s_ref, what="after device check")
 
 
-def test_prefill_time_segments_with_ragged_tail():
-    """A batched call long enough to be split into time segments (a small scan grid and
-    65 chunks: two segments, the last chunk ragged) against the oracle, with an initial
-    state; the plan reports two launches per segment."""
+def test_prefill_time_parallel_with_ragged_tail():
+    """A batched call with a small scan grid and 65 chunks runs the time-parallel scan: four
+    segments of 17 chunks (the last one 14, its last chunk ragged), each scanned from zero
+    beside its operator pass, then combined; against the oracle, with an initial state.
+    The plan reports prep, scan and three combine steps."""
     from recurrent_state_scan_gb300 import gdn
     spec = workloads.small_spec(io="bf16", batch=1, seqlen=4100, h_qk=2, h_v=4, seed=61,
                                 state_std=0.05)
     inp = workloads.draw(spec)
     path, launches = gdn.gdn_prefill_plan(gdn.shape_of_spec(spec, inp.n_seq, inp.total_tokens))
-    assert path == gdn.PATH_TC and launches == 4
+    assert path == gdn.PATH_TC_TP and launches == 5
     o_ref, s_ref = oracle.scan_inputs(inp, threads=4)
     o, s = run_prefill(inp)
-    check(inp, o, s, o_ref, s_ref, what="time segments")
+    check(inp, o, s, o_ref, s_ref, what="time-parallel scan")
+
+
+@pytest.mark.parametrize("io,B,T,hqk,hv,state", [
+    ("f16", 2, 2048, 2, 2, False),     # two segments of 16 chunks
+    ("bf16", 1, 3000, 1, 2, True),     # GQA, ragged tail
+    ("bf16", 3, 4096, 2, 2, True),     # three sequences, four segments
+])
+def test_prefill_time_parallel_shapes(io, B, T, hqk, hv, state):
+    spec = workloads.small_spec(io=io, batch=B, seqlen=T, h_qk=hqk, h_v=hv, seed=62 + T,
+                                state_std=0.05 if state else 0.0)
+    inp = workloads.draw(spec)
+    o_ref, s_ref = oracle.scan_inputs(inp, threads=8)
+    o, s = run_prefill(inp)
+    check(inp, o, s, o_ref, s_ref, what="time-parallel scan")
+
+
+def test_prefill_time_segments_with_a_records_only_workspace():
+    """Given room for the chunk records only (81 KiB per chunk and value head), the same
+    call falls back to the overlapped prep/scan segments, with the same results."""
+    spec = workloads.small_spec(io="bf16", batch=1, seqlen=4100, h_qk=2, h_v=4, seed=61,
+                                state_std=0.05)
+    inp = workloads.draw(spec)
+    records = ((4100 + 63) // 64) * 4 * 82944
+    ws = torch.empty(records, dtype=torch.uint8, device="cuda")
+    o_ref, s_ref = oracle.scan_inputs(inp, threads=4)
+    o, s = run_prefill(inp, workspace=ws)
+    check(inp, o, s, o_ref, s_ref, what="overlapped segments")
