@@ -317,6 +317,18 @@ def test_workload_recipe():
     assert set(w) == {"tiny_f32_prefill", "bf16_prefill_t4096", "bf16_decode_b256",
                       "varlen_bf16_prefill", "gqa_f16_prefill", "bf16_slot_decode_b256",
                       "bf16_window_b256_t4", "bf16_perkey_decode_b256"}
+    assert set(workloads.CONV_WORKLOADS) == {"bf16_conv_prefill_gqa", "bf16_conv_decode_b256"}
+    assert set(workloads.NORM_WORKLOADS) == {"bf16_norm_gqa"}
+    cv = workloads.draw_conv(workloads.ConvSpec("t", "bf16", 2, 5, 8, 3, state_std=1.0,
+                                                state_window=2, bias=True))
+    assert tuple(cv.x.shape) == (2, 5, 8) and tuple(cv.w.shape) == (8, 1, 4)
+    assert tuple(cv.state_in.shape) == (2, 2, 3, 8) and tuple(cv.bias.shape) == (8,)
+    assert float(cv.w.abs().max()) <= 0.5        # U(-1/sqrt(K), 1/sqrt(K)), K = 4
+    pool = workloads.draw_conv(workloads.ConvSpec("t", "bf16", 3, 1, 8, 4, state_std=1.0,
+                                                  pool_size=6))
+    assert len(set(pool.slots.tolist())) == 3 and tuple(pool.pool.shape) == (6, 3, 8)
+    nm = workloads.draw_norm(workloads.NormSpec("n", "f16", (2, 3, 16), 5))
+    assert tuple(nm.x.shape) == tuple(nm.gate.shape) == (2, 3, 16) and tuple(nm.scale.shape) == (16,)
     pk = workloads.draw(workloads.small_spec(io="bf16", batch=3, seqlen=2, h_qk=1, h_v=2, d_k=8,
                                              d_v=4, decay_per_key=True, beta_shared=True))
     assert tuple(pk.a.shape) == (3, 2, 2, 8) and tuple(pk.A_log.shape) == (2, 8)
