@@ -204,6 +204,185 @@ __global__ void __launch_bounds__(kThreads, (simt_min_blocks<DKMAX, kThreads>())
     }
 }
 
+// ------------------------------------------------------------------ streaming decode step
+// The decode step (one token per sequence, d_k = 128, d_v a multiple of 64, the plain
+// gated delta rule, optionally against a state pool) with persistent CTAs: each CTA walks
+// (sequence, head, 64-column tile) units in a grid-stride loop and prefetches the next
+// unit's inputs while it computes the current one.  The tiling and the math per unit are
+// those of scan_simt_kernel (128 threads, 16 rows x 4 columns a thread), so one unit is
+// one token of that kernel.
+//  - The next unit's state tile streams into shared memory with 16-byte cp.async copies,
+//    each thread copying exactly the elements it will hold, so it needs no barrier of its
+//    own: the thread waits for its copies (cp.async.wait_group) and moves them to
+//    registers.  The copies are issued only after this unit's reductions have read every
+//    state register, so the copy-in never overtakes a pending read of the same slot.
+//  - q, k and the 64 values of v for the next unit come the same way into a staging tile
+//    that the unit's barriers protect; its two gate logits and parameters are prefetched
+//    into registers by the two threads that evaluate them.
+__device__ __forceinline__ void stream_cp16(void *smem, const void *gmem) {
+    const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(a), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void stream_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void stream_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+template <typename IO>
+__global__ void __launch_bounds__(128, 4) decode_stream_kernel(const ScanParams p) {
+    constexpr int kThreads = 128, LPR = 16, RPP = kThreads / LPR, RPT = 128 / RPP, TILE = 64;
+    constexpr int ES = (int)sizeof(IO);
+    constexpr int QB = 128 * ES, VB = TILE * ES;            // staged bytes of q (= k) and v
+    constexpr int kBetaThread = 32;
+    __shared__ __align__(16) float4 pre[RPT][kThreads];      // the next unit's state slots
+    __shared__ __align__(16) unsigned char stage[2 * QB + VB];   // next q | k | v tile
+    __shared__ float sq[128], sk[128], sv[TILE], sdelta[TILE];
+    __shared__ __align__(16) float red_k[RPP * TILE];
+    __shared__ __align__(16) float red_q[RPP * TILE];
+    __shared__ float s_alpha, s_beta, s_qk;
+
+    const int tid = threadIdx.x;
+    const int lr = tid % LPR, rg = tid / LPR;
+    const int tiles = p.d_v / TILE;
+    const int64_t units = (int64_t)p.num_seqs * p.h_v * tiles;
+    const IO *q = static_cast<const IO *>(p.q);
+    const IO *k = static_cast<const IO *>(p.k);
+    const IO *v = static_cast<const IO *>(p.v);
+    const IO *ga = static_cast<const IO *>(p.a);
+    const IO *gb = static_cast<const IO *>(p.b);
+    IO *o = static_cast<IO *>(p.o);
+
+    struct Unit {
+        int64_t n, srow;
+        int h, hq, tile;
+        bool ok;
+    };
+    auto unit_of = [&](int64_t u) {
+        Unit x;
+        x.tile = (int)(u % tiles);
+        const int64_t r = u / tiles;
+        x.h = (int)(r % p.h_v);
+        x.n = r / p.h_v;
+        x.hq = x.h / (p.h_v / p.h_qk);
+        x.srow = x.n;
+        x.ok = true;
+        if (p.slots != nullptr) {
+            x.srow = p.slots[x.n];
+            x.ok = x.srow >= 0 && x.srow < p.pool_size;
+        }
+        return x;
+    };
+    float ra = 0.f, rb = 0.f, rA = 0.f, rD = 0.f;   // the next unit's gate inputs
+    // Issue the copies of unit u (its state slots, q, k, v) and its gate loads.
+    auto prefetch = [&](const Unit &x) {
+        const int col0 = x.tile * TILE + 4 * lr;
+        const size_t sbase = ((size_t)x.srow * p.h_v + x.h) * (size_t)128 * p.d_v;
+#pragma unroll
+        for (int m = 0; m < RPT; ++m) {
+            if (x.ok && p.state_in != nullptr)
+                stream_cp16(&pre[m][tid], p.state_in + sbase + (size_t)(rg + RPP * m) * p.d_v + col0);
+            else
+                pre[m][tid] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        const size_t qk_off = ((size_t)x.n * p.h_qk + x.hq) * 128;
+        const size_t v_off = ((size_t)x.n * p.h_v + x.h) * p.d_v + (size_t)x.tile * TILE;
+        for (int c = tid; c < (2 * QB + VB) / 16; c += kThreads) {
+            const int byte = 16 * c;
+            const void *src = byte < QB ? static_cast<const void *>(reinterpret_cast<const unsigned char *>(q + qk_off) + byte)
+                            : byte < 2 * QB ? static_cast<const void *>(reinterpret_cast<const unsigned char *>(k + qk_off) + (byte - QB))
+                                            : static_cast<const void *>(reinterpret_cast<const unsigned char *>(v + v_off) + (byte - 2 * QB));
+            stream_cp16(stage + byte, src);
+        }
+        stream_commit();
+        const size_t gi = (size_t)x.n * p.h_v + x.h;
+        if (tid == 0) {
+            ra = IoType<IO>::ld(ga + gi);
+            rA = p.A_log[x.h];
+            rD = p.dt_bias[x.h];
+        }
+        if (tid == kBetaThread) rb = IoType<IO>::ld(gb + gi);
+    };
+
+    int64_t u = blockIdx.x;
+    if (u >= units) return;
+    Unit cur = unit_of(u);
+    prefetch(cur);
+    for (; u < units; u += gridDim.x) {
+        stream_wait_all();          // this thread's copies of the unit have landed
+        __syncthreads();            // everyone's copies (q, k, v) have landed
+        float4 S[RPT];
+#pragma unroll
+        for (int m = 0; m < RPT; ++m) S[m] = pre[m][tid];
+        sq[tid] = IoType<IO>::ld(reinterpret_cast<const IO *>(stage) + tid);
+        sk[tid] = IoType<IO>::ld(reinterpret_cast<const IO *>(stage + QB) + tid);
+        if (tid < TILE) sv[tid] = IoType<IO>::ld(reinterpret_cast<const IO *>(stage + 2 * QB) + tid);
+        if (tid == 0) s_alpha = expf(decay_f(ra, rA, rD));
+        if (tid == kBetaThread) s_beta = sigmoid_f(rb);
+        __syncthreads();
+
+        // Partial retrieval S^T k and readout S^T q over this thread's rows.
+        float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+#pragma unroll
+        for (int m = 0; m < RPT; ++m) {
+            const int i = rg + RPP * m;
+            const float kk = sk[i], qq = sq[i];
+            pk.x = fmaf(S[m].x, kk, pk.x); pk.y = fmaf(S[m].y, kk, pk.y);
+            pk.z = fmaf(S[m].z, kk, pk.z); pk.w = fmaf(S[m].w, kk, pk.w);
+            pq.x = fmaf(S[m].x, qq, pq.x); pq.y = fmaf(S[m].y, qq, pq.y);
+            pq.z = fmaf(S[m].z, qq, pq.z); pq.w = fmaf(S[m].w, qq, pq.w);
+        }
+        *reinterpret_cast<float4 *>(&red_k[rg * TILE + 4 * lr]) = pk;
+        *reinterpret_cast<float4 *>(&red_q[rg * TILE + 4 * lr]) = pq;
+        if (tid < 32) {
+            float acc = 0.f;
+            for (int i = tid; i < 128; i += 32) acc = fmaf(sq[i], sk[i], acc);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (tid == 0) s_qk = acc;
+        }
+        __syncthreads();            // every thread has read the staging tile and its state
+
+        // The next unit streams in while this one finishes.
+        const Unit x = cur;
+        const int64_t un = u + gridDim.x;
+        if (un < units) {
+            cur = unit_of(un);
+            prefetch(cur);
+        }
+
+        const float alpha = s_alpha;
+        if (tid < TILE) {
+            float rk = 0.f, rq = 0.f;
+#pragma unroll 8
+            for (int r = 0; r < RPP; ++r) {
+                rk += red_k[r * TILE + tid];
+                rq += red_q[r * TILE + tid];
+            }
+            // r = (alpha S)^T k; delta = beta (v - r); o = scale (alpha S + k delta^T)^T q
+            const float delta = s_beta * (sv[tid] - alpha * rk);
+            sdelta[tid] = delta;
+            if (x.ok)
+                IoType<IO>::st(o + ((size_t)x.n * p.h_v + x.h) * p.d_v + x.tile * TILE + tid,
+                               p.scale * fmaf(s_qk, delta, alpha * rq));
+        }
+        __syncthreads();
+
+        const float4 d4 = *reinterpret_cast<const float4 *>(&sdelta[4 * lr]);
+        const int col0 = x.tile * TILE + 4 * lr;
+        const size_t sbase = ((size_t)x.srow * p.h_v + x.h) * (size_t)128 * p.d_v;
+#pragma unroll
+        for (int m = 0; m < RPT; ++m) {
+            const float kk = sk[rg + RPP * m];
+            S[m].x = fmaf(alpha, S[m].x, kk * d4.x);
+            S[m].y = fmaf(alpha, S[m].y, kk * d4.y);
+            S[m].z = fmaf(alpha, S[m].z, kk * d4.z);
+            S[m].w = fmaf(alpha, S[m].w, kk * d4.w);
+            if (x.ok)
+                __stcs(reinterpret_cast<float4 *>(p.state_out + sbase + (size_t)(rg + RPP * m) * p.d_v + col0),
+                       S[m]);
+        }
+        if (!x.ok && tid == 0 && x.tile == 0) atomicOr(p.status, kDevBadSlot);
+    }
+}
+
 template <typename IO, int DKMAX, int LPR, int NT>
 cudaError_t launch_cfg(const ScanParams &p, cudaStream_t stream) {
     const int tiles = (p.d_v + 4 * LPR - 1) / (4 * LPR);
@@ -228,8 +407,38 @@ cudaError_t launch_dk(const ScanParams &p, cudaStream_t stream) {
     return launch_cfg<IO, DKMAX, 16, 128>(p, stream);
 }
 
+// The decode step the streaming kernel covers: one token per sequence, d_k = 128, d_v a
+// multiple of 64, the plain rule and gates, a final state, 16-byte aligned q, k, v and state.
+bool stream_decode_ok(const ScanParams &p) {
+    auto a16 = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
+    return p.cu_seqlens == nullptr && p.seqlen == 1 && p.d_k == 128 && p.d_v % 64 == 0 &&
+           p.window == nullptr && p.rule == GDN_RULE_GATED_DELTA && !p.decay_per_key &&
+           !p.beta_shared && p.state_out != nullptr && a16(p.q) && a16(p.k) && a16(p.v) &&
+           a16(p.state_in) && a16(p.state_out);
+}
+
+int stream_ctas() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152 * 4;
+    if (cache[dev] == 0) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+            sms = 152;
+        cache[dev] = 4 * sms;   // four resident CTAs per SM (39 KB of shared memory each)
+    }
+    return cache[dev];
+}
+
 template <typename IO>
 cudaError_t launch_io(const ScanParams &p, cudaStream_t stream) {
+    if (stream_decode_ok(p)) {
+        const int64_t units = (int64_t)p.num_seqs * p.h_v * (p.d_v / 64);
+        if (units <= 0) return cudaSuccess;
+        const int64_t ctas = stream_ctas();
+        decode_stream_kernel<IO><<<(unsigned)(units < ctas ? units : ctas), 128, 0, stream>>>(p);
+        return cudaGetLastError();
+    }
     if (p.d_k <= 32) return launch_dk<IO, 32>(p, stream);
     if (p.d_k <= 64) return launch_dk<IO, 64>(p, stream);
     if (p.d_k <= 128) return launch_dk<IO, 128>(p, stream);
