@@ -731,7 +731,7 @@ def prefill_kernels(inp) -> str:
     """The kernels one call runs, named for the roofline entry."""
     from recurrent_state_scan_gb300 import gdn
     if bandwidth_metric(inp.spec):
-        if inp.spec.window or inp.spec.decay_per_key or inp.spec.beta_shared:
+        if inp.spec.window:
             return "scan_simt_kernel, one call"
         return "decode_stream_kernel (persistent, prefetching), one call"
     path, _ = gdn.gdn_prefill_plan(gdn.shape_of_spec(inp.spec, inp.n_seq, inp.total_tokens))

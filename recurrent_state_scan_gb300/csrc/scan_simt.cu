@@ -205,8 +205,8 @@ __global__ void __launch_bounds__(kThreads, (simt_min_blocks<DKMAX, kThreads>())
 }
 
 // ------------------------------------------------------------------ streaming decode step
-// The decode step (one token per sequence, d_k = 128, d_v a multiple of 64, the plain
-// gated delta rule, optionally against a state pool) with persistent CTAs: each CTA walks
+// The decode step (one token per sequence, d_k = 128, d_v a multiple of 64, any rule and
+// gate layout, optionally against a state pool) with persistent CTAs: each CTA walks
 // (sequence, head, 64-column tile) units in a grid-stride loop and prefetches the next
 // unit's inputs while it computes the current one.  The tiling and the math per unit are
 // those of scan_simt_kernel (128 threads, 16 rows x 4 columns a thread), so one unit is
@@ -216,9 +216,10 @@ __global__ void __launch_bounds__(kThreads, (simt_min_blocks<DKMAX, kThreads>())
 //    own: the thread waits for its copies (cp.async.wait_group) and moves them to
 //    registers.  The copies are issued only after this unit's reductions have read every
 //    state register, so the copy-in never overtakes a pending read of the same slot.
-//  - q, k and the 64 values of v for the next unit come the same way into a staging tile
-//    that the unit's barriers protect; its two gate logits and parameters are prefetched
-//    into registers by the two threads that evaluate them.
+//  - q, k, the 64 values of v and, with per-key decay, the d_k decay logits for the next
+//    unit come the same way into a staging tile that the unit's barriers protect; its
+//    scalar gate inputs (and per-key parameters) are prefetched into the registers of the
+//    threads that evaluate them.
 __device__ __forceinline__ void stream_cp16(void *smem, const void *gmem) {
     const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(smem));
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(a), "l"(gmem) : "memory");
@@ -226,15 +227,17 @@ __device__ __forceinline__ void stream_cp16(void *smem, const void *gmem) {
 __device__ __forceinline__ void stream_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void stream_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
-template <typename IO>
+template <typename IO, bool kPerKey>
 __global__ void __launch_bounds__(128, 4) decode_stream_kernel(const ScanParams p) {
     constexpr int kThreads = 128, LPR = 16, RPP = kThreads / LPR, RPT = 128 / RPP, TILE = 64;
     constexpr int ES = (int)sizeof(IO);
-    constexpr int QB = 128 * ES, VB = TILE * ES;            // staged bytes of q (= k) and v
+    constexpr int QB = 128 * ES, VB = TILE * ES;            // staged bytes of q (= k, a) and v
+    constexpr int SB = 2 * QB + VB + (kPerKey ? QB : 0);    // next q | k | v [| a] tile
     constexpr int kBetaThread = 32;
     __shared__ __align__(16) float4 pre[RPT][kThreads];      // the next unit's state slots
-    __shared__ __align__(16) unsigned char stage[2 * QB + VB];   // next q | k | v tile
+    __shared__ __align__(16) unsigned char stage[SB];
     __shared__ float sq[128], sk[128], sv[TILE], sdelta[TILE];
+    __shared__ float sa[kPerKey ? 128 : 1];                  // per-key decay factors
     __shared__ __align__(16) float red_k[RPP * TILE];
     __shared__ __align__(16) float red_q[RPP * TILE];
     __shared__ float s_alpha, s_beta, s_qk;
@@ -249,6 +252,8 @@ __global__ void __launch_bounds__(128, 4) decode_stream_kernel(const ScanParams 
     const IO *ga = static_cast<const IO *>(p.a);
     const IO *gb = static_cast<const IO *>(p.b);
     IO *o = static_cast<IO *>(p.o);
+    const bool has_decay = (p.rule == GDN_RULE_GATED_DELTA || p.rule == GDN_RULE_GATED);
+    const bool has_delta = (p.rule == GDN_RULE_GATED_DELTA || p.rule == GDN_RULE_DELTA);
 
     struct Unit {
         int64_t n, srow;
@@ -284,21 +289,30 @@ __global__ void __launch_bounds__(128, 4) decode_stream_kernel(const ScanParams 
         }
         const size_t qk_off = ((size_t)x.n * p.h_qk + x.hq) * 128;
         const size_t v_off = ((size_t)x.n * p.h_v + x.h) * p.d_v + (size_t)x.tile * TILE;
-        for (int c = tid; c < (2 * QB + VB) / 16; c += kThreads) {
+        const size_t gi = (size_t)x.n * p.h_v + x.h;
+        for (int c = tid; c < SB / 16; c += kThreads) {
             const int byte = 16 * c;
-            const void *src = byte < QB ? static_cast<const void *>(reinterpret_cast<const unsigned char *>(q + qk_off) + byte)
-                            : byte < 2 * QB ? static_cast<const void *>(reinterpret_cast<const unsigned char *>(k + qk_off) + (byte - QB))
-                                            : static_cast<const void *>(reinterpret_cast<const unsigned char *>(v + v_off) + (byte - 2 * QB));
+            const unsigned char *src;
+            if (byte < QB) src = reinterpret_cast<const unsigned char *>(q + qk_off) + byte;
+            else if (byte < 2 * QB) src = reinterpret_cast<const unsigned char *>(k + qk_off) + (byte - QB);
+            else if (byte < 2 * QB + VB) src = reinterpret_cast<const unsigned char *>(v + v_off) + (byte - 2 * QB);
+            else if (has_decay) src = reinterpret_cast<const unsigned char *>(ga + gi * 128) + (byte - 2 * QB - VB);
+            else continue;   // no decay: a is not read (and may be NULL)
             stream_cp16(stage + byte, src);
         }
         stream_commit();
-        const size_t gi = (size_t)x.n * p.h_v + x.h;
-        if (tid == 0) {
+        if (kPerKey) {
+            // This thread's key dimension: its decay parameters.
+            if (has_decay) {
+                rA = p.A_log[(size_t)x.h * 128 + tid];
+                rD = p.dt_bias[(size_t)x.h * 128 + tid];
+            }
+        } else if (tid == 0 && has_decay) {
             ra = IoType<IO>::ld(ga + gi);
             rA = p.A_log[x.h];
             rD = p.dt_bias[x.h];
         }
-        if (tid == kBetaThread) rb = IoType<IO>::ld(gb + gi);
+        if (tid == kBetaThread && has_delta) rb = IoType<IO>::ld(gb + (p.beta_shared ? (size_t)x.n : gi));
     };
 
     int64_t u = blockIdx.x;
@@ -314,8 +328,12 @@ __global__ void __launch_bounds__(128, 4) decode_stream_kernel(const ScanParams 
         sq[tid] = IoType<IO>::ld(reinterpret_cast<const IO *>(stage) + tid);
         sk[tid] = IoType<IO>::ld(reinterpret_cast<const IO *>(stage + QB) + tid);
         if (tid < TILE) sv[tid] = IoType<IO>::ld(reinterpret_cast<const IO *>(stage + 2 * QB) + tid);
-        if (tid == 0) s_alpha = expf(decay_f(ra, rA, rD));
-        if (tid == kBetaThread) s_beta = sigmoid_f(rb);
+        if (kPerKey)
+            sa[tid] = has_decay ? expf(decay_f(IoType<IO>::ld(reinterpret_cast<const IO *>(stage + 2 * QB + VB) + tid),
+                                               rA, rD))
+                                : 1.f;
+        if (tid == 0) s_alpha = (has_decay && !kPerKey) ? expf(decay_f(ra, rA, rD)) : 1.f;
+        if (tid == kBetaThread) s_beta = has_delta ? sigmoid_f(rb) : 1.f;
         __syncthreads();
 
         // Partial retrieval S^T k and readout S^T q over this thread's rows.
@@ -323,7 +341,8 @@ __global__ void __launch_bounds__(128, 4) decode_stream_kernel(const ScanParams 
 #pragma unroll
         for (int m = 0; m < RPT; ++m) {
             const int i = rg + RPP * m;
-            const float kk = sk[i], qq = sq[i];
+            const float ai = kPerKey ? sa[i] : 1.f;
+            const float kk = ai * sk[i], qq = ai * sq[i];
             pk.x = fmaf(S[m].x, kk, pk.x); pk.y = fmaf(S[m].y, kk, pk.y);
             pk.z = fmaf(S[m].z, kk, pk.z); pk.w = fmaf(S[m].w, kk, pk.w);
             pq.x = fmaf(S[m].x, qq, pq.x); pq.y = fmaf(S[m].y, qq, pq.y);
@@ -356,8 +375,9 @@ __global__ void __launch_bounds__(128, 4) decode_stream_kernel(const ScanParams 
                 rk += red_k[r * TILE + tid];
                 rq += red_q[r * TILE + tid];
             }
-            // r = (alpha S)^T k; delta = beta (v - r); o = scale (alpha S + k delta^T)^T q
-            const float delta = s_beta * (sv[tid] - alpha * rk);
+            // r = (alpha S)^T k; delta = beta (v - r) (or v without the delta rule);
+            // o = scale (alpha S + k delta^T)^T q
+            const float delta = has_delta ? s_beta * (sv[tid] - alpha * rk) : sv[tid];
             sdelta[tid] = delta;
             if (x.ok)
                 IoType<IO>::st(o + ((size_t)x.n * p.h_v + x.h) * p.d_v + x.tile * TILE + tid,
@@ -371,10 +391,11 @@ __global__ void __launch_bounds__(128, 4) decode_stream_kernel(const ScanParams 
 #pragma unroll
         for (int m = 0; m < RPT; ++m) {
             const float kk = sk[rg + RPP * m];
-            S[m].x = fmaf(alpha, S[m].x, kk * d4.x);
-            S[m].y = fmaf(alpha, S[m].y, kk * d4.y);
-            S[m].z = fmaf(alpha, S[m].z, kk * d4.z);
-            S[m].w = fmaf(alpha, S[m].w, kk * d4.w);
+            const float am = kPerKey ? sa[rg + RPP * m] : alpha;
+            S[m].x = fmaf(am, S[m].x, kk * d4.x);
+            S[m].y = fmaf(am, S[m].y, kk * d4.y);
+            S[m].z = fmaf(am, S[m].z, kk * d4.z);
+            S[m].w = fmaf(am, S[m].w, kk * d4.w);
             if (x.ok)
                 __stcs(reinterpret_cast<float4 *>(p.state_out + sbase + (size_t)(rg + RPP * m) * p.d_v + col0),
                        S[m]);
@@ -408,13 +429,14 @@ cudaError_t launch_dk(const ScanParams &p, cudaStream_t stream) {
 }
 
 // The decode step the streaming kernel covers: one token per sequence, d_k = 128, d_v a
-// multiple of 64, the plain rule and gates, a final state, 16-byte aligned q, k, v and state.
+// multiple of 64, no window, a final state, 16-byte aligned q, k, v, state (and a, with
+// per-key decay).
 bool stream_decode_ok(const ScanParams &p) {
     auto a16 = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
+    const bool decay = p.rule == GDN_RULE_GATED_DELTA || p.rule == GDN_RULE_GATED;
     return p.cu_seqlens == nullptr && p.seqlen == 1 && p.d_k == 128 && p.d_v % 64 == 0 &&
-           p.window == nullptr && p.rule == GDN_RULE_GATED_DELTA && !p.decay_per_key &&
-           !p.beta_shared && p.state_out != nullptr && a16(p.q) && a16(p.k) && a16(p.v) &&
-           a16(p.state_in) && a16(p.state_out);
+           p.window == nullptr && p.state_out != nullptr && a16(p.q) && a16(p.k) && a16(p.v) &&
+           a16(p.state_in) && a16(p.state_out) && (!p.decay_per_key || !decay || a16(p.a));
 }
 
 int stream_ctas() {
@@ -436,7 +458,11 @@ cudaError_t launch_io(const ScanParams &p, cudaStream_t stream) {
         const int64_t units = (int64_t)p.num_seqs * p.h_v * (p.d_v / 64);
         if (units <= 0) return cudaSuccess;
         const int64_t ctas = stream_ctas();
-        decode_stream_kernel<IO><<<(unsigned)(units < ctas ? units : ctas), 128, 0, stream>>>(p);
+        const unsigned grid = (unsigned)(units < ctas ? units : ctas);
+        if (p.decay_per_key)
+            decode_stream_kernel<IO, true><<<grid, 128, 0, stream>>>(p);
+        else
+            decode_stream_kernel<IO, false><<<grid, 128, 0, stream>>>(p);
         return cudaGetLastError();
     }
     if (p.d_k <= 32) return launch_dk<IO, 32>(p, stream);
