@@ -28,9 +28,18 @@
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream).  Calls are asynchronous on that stream; nothing synchronises.
  *  - Errors found on the host return a status and launch nothing.  Errors only
- *    the device can see (a malformed device cu_seqlens) set a device check word,
- *    skip the affected work without faulting, and are reported by
- *    gdn_last_device_status().
+ *    the device can see (a malformed device cu_seqlens, a slot outside a state
+ *    pool) set a device check word, skip the affected work without faulting, and
+ *    are reported by gdn_last_device_status().
+ *  - Internal resources: gdn_prefill may create, once per device, a CUDA stream
+ *    and a cuBLAS handle (see gdn_prefill_workspace_bytes); gdn_prefill_noalloc
+ *    and every other call create nothing.
+ *
+ * Entry points: gdn_prefill (and gdn_prefill_noalloc, gdn_prefill_plan,
+ * gdn_prefill_workspace_bytes), gdn_decode_step, gdn_decode_step_slots (a state
+ * pool), gdn_scan_window (the states after each of the last W steps),
+ * gdn_scan_variant (other update rules and gate layouts), and the layer ops
+ * around the scan: gdn_causal_conv, gdn_causal_conv_slots and gdn_gated_rmsnorm.
  *  - gdn_last_error_message() gives a human-readable detail of the last
  *    non-OK status returned on the calling thread.
  */
@@ -49,7 +58,8 @@ typedef enum {
     GDN_ERR_INVALID_ARG = 1,   /* bad shape, null or misaligned pointer, bad size  */
     GDN_ERR_UNSUPPORTED = 2,   /* valid arguments, geometry not built (d_k > 256)   */
     GDN_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed              */
-    GDN_ERR_DEVICE_CHECK = 4,  /* the device found malformed cu_seqlens             */
+    GDN_ERR_DEVICE_CHECK = 4,  /* the device found malformed cu_seqlens or a slot
+                                  outside the pool                                  */
     GDN_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up                */
 } gdn_status;
 
@@ -140,10 +150,11 @@ gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, con
  * `workspace` and `workspace_bytes`.  The scratch is instead a fixed array of
  * GDN_PREFILL_NOALLOC_SCRATCH_BYTES (96 MiB) inside the library, one per device,
  * created when the library's module is first used on that device; the call
- * allocates nothing and frees nothing.  A shape whose
- * gdn_prefill_workspace_bytes(shape) exceeds that size returns
- * GDN_ERR_INVALID_ARG and launches nothing: 96 MiB holds 1,213 records of one
- * (64-token chunk, value head), e.g. one 4,096-token sequence at 16 value heads.
+ * allocates nothing and frees nothing.  It runs the records-only path (no
+ * time-parallel scan, no internal stream), so it needs the chunk records alone: a
+ * shape needing more than that size returns GDN_ERR_INVALID_ARG and launches
+ * nothing.  96 MiB holds 1,213 records of one (64-token chunk, value head), e.g. one
+ * 4,096-token sequence at 16 value heads.
  * Shapes off the tensor-core path need no scratch and run as in gdn_prefill.
  *
  * All calls on a device share the one array.  Each call writes every scratch

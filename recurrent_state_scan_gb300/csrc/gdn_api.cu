@@ -150,16 +150,11 @@ gdn_status gdn_prefill_plan(const gdn_shape *shape, int32_t *path, int32_t *laun
 // Packed sequences come with batch == 1; a single batch-1 sequence is sized as packed too,
 // which covers both readings.
 size_t gdn_prefill_workspace_bytes(const gdn_shape *shape) {
-    if (shape == nullptr || shape->seqlen < 0 || shape->batch < 0 || shape->num_seqs < 0 ||
-        shape->h_v <= 0)
-        return 0;
-    const bool packed = shape->batch == 1;
-    const int64_t tokens = packed ? shape->seqlen : shape->seqlen * (int64_t)shape->batch;
-    if (!prefill_tc_shape_ok((gdn_dtype)shape->io_dtype, shape->d_k, shape->d_v, tokens)) return 0;
+    const size_t records = gdn::prefill_records_bytes(shape);
+    if (records == 0) return 0;
     // Records, plus the time-parallel scan's buffers when a batched call of this shape
     // would use it (with batch 1 the shape may also be a packed call: the sum covers both).
-    return prefill_tc_workspace(packed, shape->seqlen, shape->batch, shape->num_seqs, shape->h_v) +
-           prefill_tc_tp_bytes(false, shape->seqlen, shape->batch, shape->h_v);
+    return records + prefill_tc_tp_bytes(false, shape->seqlen, shape->batch, shape->h_v);
 }
 
 gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, const void *v,
@@ -171,6 +166,16 @@ gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, con
 }
 
 }  // extern "C"
+
+size_t gdn::prefill_records_bytes(const gdn_shape *shape) {
+    if (shape == nullptr || shape->seqlen < 0 || shape->batch < 0 || shape->num_seqs < 0 ||
+        shape->h_v <= 0)
+        return 0;
+    const bool packed = shape->batch == 1;
+    const int64_t tokens = packed ? shape->seqlen : shape->seqlen * (int64_t)shape->batch;
+    if (!prefill_tc_shape_ok((gdn_dtype)shape->io_dtype, shape->d_k, shape->d_v, tokens)) return 0;
+    return prefill_tc_workspace(packed, shape->seqlen, shape->batch, shape->num_seqs, shape->h_v);
+}
 
 gdn_status gdn::prefill_impl(const gdn_shape *shape, const void *q, const void *k, const void *v,
                              const void *a, const void *b, const float *A_log, const float *dt_bias,

@@ -129,6 +129,9 @@ bool prefill_tc_supported(const ScanParams &p, gdn_dtype io, int64_t total_token
 // grid leaves most of the GPU idle run the prep of later segments on an internal stream
 // beside the scan of earlier ones; each segment costs one prep and one scan launch.
 int prefill_tc_segments(bool varlen, int64_t seqlen, int64_t batch, int h_v);
+// Bytes of chunk records a prefill of this shape needs on the tensor-core path (0 off it);
+// the packed reading when batch is 1.
+size_t prefill_records_bytes(const gdn_shape *shape);
 // Time-parallel scan of batched shapes whose scan grid leaves most of the GPU idle: the
 // segments it uses (1: none) and the workspace bytes it needs after the records (0: none).
 int prefill_tc_tp_nseg(bool varlen, int64_t seqlen, int64_t batch, int h_v);

@@ -49,8 +49,9 @@ extern "C" gdn_status gdn_prefill_noalloc(const gdn_shape *shape, const void *q,
                                           float scale, void *o, float *state_out, void *stream) {
     if (shape == nullptr) return gdn::report_error(GDN_ERR_INVALID_ARG, "shape is NULL");
     // Every scratch byte the kernels read is written earlier in the same call, so
-    // nothing left by a previous call needs clearing.
-    const size_t need = gdn_prefill_workspace_bytes(shape);
+    // nothing left by a previous call needs clearing.  The call runs the records-only
+    // path (no time-parallel buffers, no internal stream), so the records are the need.
+    const size_t need = gdn::prefill_records_bytes(shape);
     if (need > (size_t)GDN_PREFILL_NOALLOC_SCRATCH_BYTES) {
         char msg[256];
         snprintf(msg, sizeof(msg),

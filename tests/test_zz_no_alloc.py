@@ -27,9 +27,14 @@ def test_noalloc_rejects_oversized_shapes_on_the_host():
     st = lib.gdn_prefill_noalloc(ctypes.byref(shape), *([None] * 9), 0.0, None, None, None)
     assert st == gdn.GDN_ERR_INVALID_ARG
     assert b"scratch" in lib.gdn_last_error_message()
-    # The largest advertised example fits: one 4096-token sequence at 16 value heads.
+    # The largest advertised example passes the size check: one 4096-token sequence at 16
+    # value heads needs 64 x 16 records (the call then stops at its NULL inputs, or at the
+    # missing device).  gdn_prefill's own workspace query also counts the time-parallel
+    # buffers, which this entry point never uses.
     fits = gdn.make_shape(gdn.GDN_BF16, 1, 4096, 1, 16, 16, 128, 128)
-    assert gdn.gdn_prefill_workspace_bytes(fits) <= gdn.PREFILL_NOALLOC_SCRATCH_BYTES
+    assert 64 * 16 * 82944 <= gdn.PREFILL_NOALLOC_SCRATCH_BYTES
+    st = lib.gdn_prefill_noalloc(ctypes.byref(fits), *([None] * 9), 0.0, None, None, None)
+    assert st != gdn.GDN_OK and b"scratch" not in lib.gdn_last_error_message()
 
 
 @pytest.mark.gpu
@@ -56,3 +61,27 @@ def test_noalloc_matches_gdn_prefill_on_two_calls_in_a_row():
         eo = rel_err(o.float().cpu().numpy(), o_ref.float().cpu().numpy())
         es = rel_err(s.cpu().numpy(), s_ref.cpu().numpy())
         assert eo <= tol and es <= tol, f"call with seed {seed}: rel err o {eo:.2e}, state {es:.2e}"
+
+
+@pytest.mark.gpu
+def test_noalloc_runs_the_largest_advertised_shape():
+    """One 4096-token sequence at 16 value heads (the bf16 prefill workload) fits the fixed
+    scratch and matches gdn_prefill, which runs the time-parallel scan on that shape."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from recurrent_state_scan_gb300 import (gdn_last_device_status, gdn_prefill,
+                                            gdn_prefill_noalloc, load)
+    load()
+    inp = workloads.workload("bf16_prefill_t4096")
+    d = to_device(inp)
+    args = (d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["state_in"],
+            d["cu_seqlens"], inp.scale)
+    o_ref, s_ref = gdn_prefill(*args)
+    o = torch.empty_like(o_ref)
+    s = torch.empty_like(s_ref)
+    gdn_prefill_noalloc(*args, o=o, state_out=s)
+    torch.cuda.synchronize()
+    assert gdn_last_device_status() == 0
+    tol = TOL["bf16"]
+    assert rel_err(o.float().cpu().numpy(), o_ref.float().cpu().numpy()) <= tol
+    assert rel_err(s.cpu().numpy(), s_ref.cpu().numpy()) <= tol
