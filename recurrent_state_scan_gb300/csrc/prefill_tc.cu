@@ -1283,17 +1283,23 @@ SideStream *side_stream() {
     return &s;
 }
 
+// The kernels' dynamic shared-memory limits, a per-device function attribute (set once
+// per device and I/O type).
 template <typename IO>
 cudaError_t configure() {
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(gdn_chunk_prep<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kPrepSmem);
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(gdn_chunk_prep<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPrepSmem);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(gdn_chunk_scan<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kScanSmem);
         if (e != cudaSuccess) return e;
-        configured = true;
+        configured[dev] = true;
     }
     return cudaSuccess;
 }
