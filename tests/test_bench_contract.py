@@ -3,6 +3,7 @@ figure, and the JSON line of the reference arm (the CPU oracle) for a scan workl
 neighbour-op workload."""
 import json
 import os
+import socket
 import subprocess
 import sys
 
@@ -86,3 +87,23 @@ def test_reference_arm_neighbour_workload():
     d = _reference_line("bf16_conv_decode_b256")
     _check_line(d, "bf16_conv_decode_b256")
     assert d["unit"] == "GB/s"
+
+
+def test_reference_arm_under_torchrun_prints_one_line():
+    """Two ranks (gloo on the CPU): rank 0 alone runs the reference arm and prints its
+    line; the other rank exits 0 without work."""
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    env = dict(os.environ, MASTER_ADDR="127.0.0.1")
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                        "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
+                        "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+                        "--gpus", "2", "--impl", "reference", "--workload", "tiny_f32_prefill",
+                        "--steps", "1", "--warmup", "0"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
