@@ -383,6 +383,11 @@ constexpr int kStagedChunk = 256;      // tokens per CTA
 constexpr int kStagedDepth = 3;        // stages in flight
 constexpr int kStagedMinTokens = 64;
 
+__device__ __forceinline__ void stream_commit_conv() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N> __device__ __forceinline__ void stream_wait_conv() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
@@ -516,6 +521,143 @@ __global__ void __launch_bounds__(256, 3) causal_conv_staged_kernel(const ConvPa
     }
 }
 
+// The decode step (L = 1, K <= 4 at dilation 1, channels last, no window, 16-bit I/O,
+// four channels a thread): persistent CTAs walk (row, 1024-channel slab) items.  Each
+// thread streams the next item's carry + 1 positions, its taps and its bias into its own
+// slots of a double-buffered shared-memory tile with 8-byte cp.async copies, then
+// computes the current item from the other buffer, so its copies are always in flight.
+// No slot is shared between threads, so cp.async.wait_group alone orders the reads.
+// Item i + stride never shares a row and slab with item i (distinct slots), so its early
+// reads cannot see this item's state write.
+__device__ __forceinline__ void cp_async8(void *smem, const void *gmem) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+
+template <typename IO>
+__global__ void __launch_bounds__(256) causal_conv_decode_stream_kernel(const ConvParams p) {
+    static_assert(sizeof(IO) == 2, "16-bit I/O");
+    constexpr int kSlots = 9;   // positions 0..3, taps 0..3, bias
+    __shared__ __align__(16) uint2 buf[2][kSlots][256];
+    const IO *x = static_cast<const IO *>(p.x);
+    const IO *w = static_cast<const IO *>(p.w);
+    const IO *bias = static_cast<const IO *>(p.bias);
+    const IO *past = static_cast<const IO *>(p.state_in);
+    IO *y = static_cast<IO *>(p.y);
+    IO *sout = static_cast<IO *>(p.state_out);
+    const int tid = threadIdx.x;
+    const int64_t nslab = (p.C + 1023) / 1024;
+    const int64_t items = p.B * nslab;
+
+    auto fetch = [&](int64_t it, int bsel) {
+        const int64_t b = it / nslab;
+        const int64_t c0 = (it % nslab) * 1024 + 4 * tid;
+        if (c0 < p.C) {
+            int64_t srow = b;
+            bool ok = true;
+            if (p.slots != nullptr) {
+                srow = p.slots[b];
+                ok = srow >= 0 && srow < p.pool_size;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (j < p.carry && ok && past != nullptr)
+                    cp_async8(&buf[bsel][j][tid], past + (srow * p.carry + j) * p.C + c0);
+                else if (j == p.carry)
+                    cp_async8(&buf[bsel][j][tid], x + b * p.C + c0);
+                else
+                    buf[bsel][j][tid] = make_uint2(0u, 0u);
+            }
+            // Taps: K consecutive values per channel, 4 channels = 4K values from w + c0 K.
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (j < p.K) cp_async8(&buf[bsel][4 + j][tid], w + c0 * p.K + 4 * j);
+                else buf[bsel][4 + j][tid] = make_uint2(0u, 0u);
+            }
+            if (bias != nullptr) cp_async8(&buf[bsel][8][tid], bias + c0);
+            else buf[bsel][8][tid] = make_uint2(0u, 0u);
+        }
+        stream_commit_conv();
+    };
+
+    int64_t it = blockIdx.x;
+    if (it >= items) return;
+    fetch(it, 0);
+    for (int k = 0; it < items; it += gridDim.x, ++k) {
+        const int cb = k & 1;
+        if (it + gridDim.x < items) fetch(it + gridDim.x, cb ^ 1);
+        else stream_commit_conv();
+        stream_wait_conv<1>();   // this item's copies have landed; the next item's may fly
+        const int64_t b = it / nslab;
+        const int64_t c0 = (it % nslab) * 1024 + 4 * tid;
+        if (c0 >= p.C) continue;
+        int64_t srow = b;
+        if (p.slots != nullptr) {
+            srow = p.slots[b];
+            if (srow < 0 || srow >= p.pool_size) {
+                if (c0 == 0) atomicOr(p.status, kDevBadSlot);
+                continue;
+            }
+        }
+        // Unpack: positions pos[j][i], taps in the weight layout w[c][j] (channel-major).
+        float pos[4][4], tap[4][4], bv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint2 u = buf[cb][j][tid];
+            const IO *h = reinterpret_cast<const IO *>(&u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pos[j][i] = IoType<IO>::ld(h + i);
+        }
+        // The 4K tap values of channels c0..c0+3, in order w[c0][0..K-1], w[c0+1][0..K-1]...
+        float wflat[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint2 u = buf[cb][4 + j][tid];
+            const IO *h = reinterpret_cast<const IO *>(&u);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) wflat[4 * j + e] = IoType<IO>::ld(h + e);
+        }
+        // Static indices for each K (a runtime index would put wflat in local memory).
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float t = 0.f;
+                if (p.K == 4) t = wflat[4 * i + j];
+                else if (p.K == 3) t = j < 3 ? wflat[(3 * i + j) % 16] : 0.f;
+                else if (p.K == 2) t = j < 2 ? wflat[(2 * i + j) % 16] : 0.f;
+                else t = j < 1 ? wflat[i] : 0.f;
+                tap[j][i] = t;
+            }
+        {
+            const uint2 u = buf[cb][8][tid];
+            const IO *h = reinterpret_cast<const IO *>(&u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) bv[i] = IoType<IO>::ld(h + i);
+        }
+        float out[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            // The output reads padded positions 0 .. K - 1 (carry = K - 1), oldest first.
+            float acc = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (j < p.K) acc = fmaf(tap[j][i], pos[j][i], acc);
+            acc += bv[i];
+            out[i] = p.silu ? silu_fast(acc) : acc;
+        }
+        st_vec<IO, 4>(y + b * p.C + c0, out);
+        if (sout != nullptr) {
+            // The present state: padded positions 1 .. carry, copied bit for bit.
+#pragma unroll
+            for (int j = 0; j < 3; ++j)
+                if (j < p.carry)
+                    *reinterpret_cast<uint2 *>(sout + (srow * p.carry + j) * p.C + c0) = buf[cb][j + 1][tid];
+        }
+    }
+    stream_wait_conv<0>();
+}
+
 struct NormParams {
     const void *x, *scale, *gate;
     void *y;
@@ -637,6 +779,25 @@ unsigned grid_for(int64_t items, int threads) {
     return (unsigned)(need < 1 ? 1 : (need < cap ? need : cap));
 }
 
+// The streaming decode step (16-bit I/O, four channels a thread): as many CTAs as are
+// resident at once, each walking its share of the (row, slab) items.
+template <typename IO, int VEC>
+cudaError_t launch_conv_decode_stream(const ConvParams &p, cudaStream_t stream) {
+    if constexpr (VEC == 4 && sizeof(IO) == 2) {
+        int per_sm = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm, causal_conv_decode_stream_kernel<IO>, 256, 0);
+        if (e != cudaSuccess) return e;
+        const int64_t resident = (int64_t)sm_count_cached() * (per_sm > 0 ? per_sm : 1);
+        const int64_t work = p.B * ((p.C + 1023) / 1024);
+        causal_conv_decode_stream_kernel<IO>
+            <<<(unsigned)(work < resident ? work : resident), 256, 0, stream>>>(p);
+        return cudaGetLastError();
+    } else {
+        return cudaErrorInvalidValue;
+    }
+}
+
 template <typename IO, int VEC>
 cudaError_t launch_conv_vec(const ConvParams &p, bool align16, cudaStream_t stream) {
     const int64_t items = p.B * p.tiles * (p.C / VEC);
@@ -660,6 +821,8 @@ cudaError_t launch_conv_vec(const ConvParams &p, bool align16, cudaStream_t stre
         dim3 grid((unsigned)((p.C + kStagedWidth - 1) / kStagedWidth), (unsigned)chunks,
                   (unsigned)p.B);
         causal_conv_staged_kernel<IO><<<grid, 256, smem, stream>>>(p);
+    } else if (VEC == 4 && sizeof(IO) == 2 && p.tt == 1 && p.L == 1 && p.window == 0) {
+        return launch_conv_decode_stream<IO, VEC>(p, stream);
     } else if (p.tt == 1) {
         const int64_t gx = (p.C / VEC + 255) / 256;
         dim3 grid((unsigned)gx, (unsigned)(p.B < 65535 ? p.B : 65535));

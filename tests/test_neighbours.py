@@ -130,6 +130,18 @@ def test_conv_long_rows_in_place():
     _exact(so, s_ref)
 
 
+@pytest.mark.parametrize("io", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("K,bias,state", [(4, True, True), (3, False, True), (2, True, False),
+                                          (1, True, True), (4, False, False)])
+def test_conv_decode_step(io, K, bias, state):
+    """One token per row (the streaming decode kernel for 16-bit I/O), in place."""
+    inp = _conv_case(io, 5, 1, 1032, K, 1, bias=bias, state=state, seed=500 + K)
+    y_ref, s_ref = _conv_ref(inp)
+    y, so = _run_conv(inp, in_place=state)
+    _close(y, y_ref, io)
+    _exact(so, s_ref)
+
+
 def test_conv_without_past_state_starts_from_zeros():
     inp = _conv_case("bf16", 2, 9, 32, 4, 1, state=False, seed=5)
     y, so = _run_conv(inp)
