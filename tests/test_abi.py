@@ -177,3 +177,45 @@ def test_norm_rejects_bad_arguments_before_launch():
     assert call(x=None) == gdn.GDN_ERR_INVALID_ARG
     assert call(x=odd) == gdn.GDN_ERR_INVALID_ARG
     assert call(rows=0, x=None) == gdn.GDN_OK
+
+
+def _header_text():
+    text = ""
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text += open(os.path.join(ROOT, "include", fn)).read()
+    return re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+
+
+def test_header_enums_match_the_binding():
+    """Every enum value the header defines equals the binding's constant of that name."""
+    vals = dict((n, int(v)) for n, v in re.findall(r"\b(GDN_[A-Z0-9_]+)\s*=\s*(\d+)", _header_text()))
+    assert {k: vals[k] for k in ("GDN_F32", "GDN_BF16", "GDN_F16")} == \
+        {"GDN_F32": gdn.GDN_F32, "GDN_BF16": gdn.GDN_BF16, "GDN_F16": gdn.GDN_F16}
+    for name in ("GDN_OK", "GDN_ERR_INVALID_ARG", "GDN_ERR_UNSUPPORTED", "GDN_ERR_CUDA",
+                 "GDN_ERR_DEVICE_CHECK", "GDN_ERR_TIMEOUT"):
+        assert vals[name] == getattr(gdn, name), name
+    for rule, code in gdn.RULES.items():
+        assert vals["GDN_RULE_" + rule.upper()] == code
+    assert vals["GDN_ACT_NONE"] == gdn.ACTIVATIONS["none"]
+    assert vals["GDN_ACT_SILU"] == gdn.ACTIVATIONS["silu"]
+    assert vals["GDN_ACT_SIGMOID"] == gdn.ACTIVATIONS["sigmoid"]
+
+
+def test_header_structs_match_the_binding():
+    """The ctypes structures list the header's fields in order, with the same widths."""
+    text = _header_text()
+    for cname, pyclass in (("gdn_shape", gdn.GdnShape), ("gdn_variant", gdn.GdnVariant),
+                           ("gdn_conv_shape", gdn.GdnConvShape)):
+        body = re.search(r"typedef struct " + cname + r"\s*\{(.*?)\}\s*" + cname + ";", text, re.S)
+        assert body, cname
+        fields = re.findall(r"(int32_t|int64_t)\s+([a-z_]+)\s*;", body.group(1))
+        assert [n for _, n in fields] == [n for n, _ in pyclass._fields_], cname
+        widths = {"int32_t": ctypes.c_int32, "int64_t": ctypes.c_int64}
+        assert [widths[t] for t, _ in fields] == [t for _, t in pyclass._fields_], cname
+
+
+def test_noalloc_scratch_size_matches_the_header():
+    m = re.search(r"#define GDN_PREFILL_NOALLOC_SCRATCH_BYTES \((\d+)u \* 1024u \* 1024u\)",
+                  open(os.path.join(ROOT, "include", "gdn.h")).read())
+    assert m and int(m.group(1)) * 1024 * 1024 == gdn.PREFILL_NOALLOC_SCRATCH_BYTES
