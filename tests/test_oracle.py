@@ -545,3 +545,34 @@ def test_delta_rule_is_gated_delta_without_decay(oracle_mod):
     o2, s2 = oracle_mod.scan([0, T], 1, h_v, d_k, d_v, q, k, v, g=np.zeros((T, h_v)),
                              beta=beta, state_in=s0, rule="gated_delta")
     assert np.array_equal(o1, o2) and np.array_equal(s1, s2)
+
+
+@pytest.mark.parametrize("m", [1, 17, 39])
+def test_time_parallel_decomposition(oracle_mod, m):
+    """The recurrence is linear in the state, which the time-parallel prefill relies on.
+    Cut a sequence after token m, with S_m the state there:
+      - the run from S_m equals the run from zero plus the run with v = 0 from S_m;
+      - the run with v = 0 from S_m equals, column by column, the run with v = 0 from the
+        identity (the operator pass, d_v = d_k) times S_m;
+    so o_t = o0_t + R_t S_m and S_end = Phi S_m + Psi, with R, Phi from the operator pass."""
+    rng = np.random.default_rng(70 + m)
+    T, hq, hv, dk, dv = 40, 1, 2, 8, 6
+    q = rng.standard_normal((T, hq, dk))
+    k = rng.standard_normal((T, hq, dk)) / np.sqrt(dk)
+    v = rng.standard_normal((T, hv, dv))
+    a, b = rng.standard_normal((T, hv)), rng.standard_normal((T, hv))
+    A_log, dt = rng.uniform(-1, 1, hv), rng.normal(0, 0.1, hv)
+    s0 = rng.normal(0, 0.1, (1, hv, dk, dv))
+    gates = lambda sl: dict(a=a[sl], b=b[sl], A_log=A_log, dt_bias=dt)
+    full_o, full_s = oracle_mod.scan([0, T], hq, hv, dk, dv, q, k, v, state_in=s0, **gates(slice(None)))
+    _, s_m = oracle_mod.scan([0, m], hq, hv, dk, dv, q[:m], k[:m], v[:m], state_in=s0,
+                             **gates(slice(0, m)))
+    rest = slice(m, T)
+    o0, psi = oracle_mod.scan([0, T - m], hq, hv, dk, dv, q[rest], k[rest], v[rest], **gates(rest))
+    eye = np.broadcast_to(np.eye(dk), (1, hv, dk, dk)).copy()
+    R, phi = oracle_mod.scan([0, T - m], hq, hv, dk, dk, q[rest], k[rest],
+                             np.zeros((T - m, hv, dk)), state_in=eye, **gates(rest))
+    for h in range(hv):
+        o_pred = o0[:, h] + R[:, h] @ s_m[0, h]
+        assert _rel(o_pred, full_o[m:, h]) < 1e-12
+        assert _rel(phi[0, h] @ s_m[0, h] + psi[0, h], full_s[0, h]) < 1e-12
