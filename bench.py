@@ -3,9 +3,13 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-A step is one gdn_prefill call over one batch of the named synthetic workload
-(default: bf16 prefill, B=1, H=16, d_k=d_v=128, T=4096), inputs resident in
+A step is one library call over one batch of the named synthetic workload
+(default: the packed varlen bf16 prefill, 8 sequences of U[512, 8192] tokens,
+H=16, d_k=d_v=128, the largest of the prefill workloads), inputs resident in
 HBM, L2 flushed (256 MiB write) before every step and outside its timing.
+The same line also carries the other full-size workloads (the 4096-token bf16
+prefill, the GQA f16 prefill and the B=256 decode step), each timed the same
+way, under "configs".
 Each GPU (torchrun rank) runs its own full copy of the workload: the units
 (sequence, head) are independent, so there is no collective on the data path
 and scaling is weak.  `--impl reference` times the CPU oracle on host cores.
@@ -32,7 +36,9 @@ import torch  # noqa: E402
 import workloads  # noqa: E402
 
 METRIC = "gated-delta-rule tokens/s (prefill) & state GB/s (decode), % of roofline"
-DEFAULT_WORKLOAD = "bf16_prefill_t4096"
+DEFAULT_WORKLOAD = "varlen_bf16_prefill"
+# Full-size workloads timed after the main one and reported beside it.
+EXTRA_WORKLOADS = ("bf16_prefill_t4096", "gqa_f16_prefill", "bf16_decode_b256")
 CHUNK = 64                         # tokens per chunk of the tensor-core prefill
 FLUSH_BYTES = 256 << 20            # > 129 MB L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -47,6 +53,8 @@ def parse_args():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-extra-configs", action="store_true",
+                   help="time only the named workload (no 'configs' entry)")
     return p.parse_args()
 
 
@@ -505,13 +513,13 @@ def main_neighbour(args, rank, world, local):
 
 # ---------------------------------------------------------------- our arm
 
-def run_ours(args, rank, world, local):
+def run_ours(args, rank, world, local, name=None, with_e2e=True):
     from recurrent_state_scan_gb300 import (gdn_decode_step, gdn_decode_step_slots, gdn_prefill,
                                             gdn_scan_variant, gdn_scan_window, load)
     load()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    inp = workloads.workload(args.workload)
+    inp = workloads.workload(name or args.workload)
     s = inp.spec
     t = {n: getattr(inp, n).to(dev) for n in ("q", "k", "v", "a", "b", "A_log", "dt_bias")}
     state0 = None if inp.state_in is None else inp.state_in.to(dev)
@@ -579,7 +587,7 @@ def run_ours(args, rank, world, local):
 
     # End to end through the public API: pinned host inputs -> device -> call -> host.
     e2e = None
-    if not args.no_e2e:
+    if with_e2e and not args.no_e2e:
         host = {n: v.pin_memory() for n, v in
                 [("q", inp.q), ("k", inp.k), ("v", inp.v), ("a", inp.a), ("b", inp.b),
                  ("A_log", inp.A_log), ("dt_bias", inp.dt_bias)] +
@@ -678,36 +686,13 @@ def main():
 
     inp, ms, times_ms, clocks, e2e = run_ours(args, rank, world, local)
     s = inp.spec
-    pk, pk_kind = peaks()
     nbytes = algorithmic_bytes(inp)
-    flops = algorithmic_flops(inp)
-    sec = ms / 1e3
-    if bandwidth_metric(s):
-        value, unit = world * nbytes / sec / 1e9, "GB/s"
-    else:
-        value, unit = world * inp.total_tokens / sec, "tokens/s"
-    # Roofline of the call: one kernel for decode; for prefill the chunk-prep kernel and
-    # the state-scan kernel, which run back to back and do no useful work alone.
-    gbs = nbytes / sec / 1e9
-    tfs = flops / sec / 1e12
-    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
-    t_tc = flops / (pk["bf16_tflops"] * 1e12)
-    roof = {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-            "frac": gbs / pk["hbm_gbs"],
-            "traffic": profiled_traffic(inp_name, "decode" if bandwidth_metric(s) else "prefill"),
-            "peak_source": f"{pk_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"
-            if pk_kind == "measured" else "fallback 6.8 TB/s",
-            "kernels": prefill_kernels(inp)}
-    if not bandwidth_metric(s):
-        roof["tensor_tflops"] = tfs
-        roof["tensor_frac_of_bf16_peak"] = tfs / pk["bf16_tflops"]
-        roof["roofline_time_us"] = max(t_hbm, t_tc) * 1e6
-        roof["frac_of_roofline"] = max(t_hbm, t_tc) / sec
+    value, unit = throughput(inp, ms, world)
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype_of(inp), "data": "synthetic",
-        "config": config_of(inp, world), "roofline": roof,
+        "config": config_of(inp, world), "roofline": roofline_entry(inp, ms),
         "gpu_launches": args.steps * launches_per_call(inp),
     }
     if e2e is not None:
@@ -718,6 +703,22 @@ def main():
                        "d2h_bytes_per_step": e2e["d2h_bytes_per_step"]}
     if clocks is not None:
         line["clocks"] = clocks
+    if not args.no_extra_configs and inp_name == DEFAULT_WORKLOAD:
+        # The other full-size workloads, each timed like the main one (no e2e leg).
+        extra = {}
+        for name in EXTRA_WORKLOADS:
+            if name == inp_name:
+                continue
+            x_inp, x_ms, _, x_clocks, _ = run_ours(args, rank, world, local, name=name,
+                                                   with_e2e=False)
+            x_val, x_unit = throughput(x_inp, x_ms, world)
+            extra[name] = {"value": x_val, "unit": x_unit, "ms_per_step": x_ms,
+                           "dtype": dtype_of(x_inp), "config": config_of(x_inp, world),
+                           "roofline": roofline_entry(x_inp, x_ms),
+                           "gpu_launches": args.steps * launches_per_call(x_inp)}
+            if x_clocks is not None:
+                extra[name]["clocks"] = x_clocks
+        line["configs"] = extra
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_line(inp)
     if rank == 0:
@@ -725,6 +726,41 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def throughput(inp, ms, world):
+    """(value, unit) of one step: state GB/s for decode-like steps, tokens/s for prefill,
+    summed over the ranks (each runs its own copy of the workload)."""
+    sec = ms / 1e3
+    if bandwidth_metric(inp.spec):
+        return world * algorithmic_bytes(inp) / sec / 1e9, "GB/s"
+    return world * inp.total_tokens / sec, "tokens/s"
+
+
+def roofline_entry(inp, ms):
+    """Roofline of one call on one GPU: algorithmic bytes (and, for prefill, FLOPs) over
+    the call's device time, against the measured peaks."""
+    s = inp.spec
+    pk, pk_kind = peaks()
+    nbytes = algorithmic_bytes(inp)
+    flops = algorithmic_flops(inp)
+    sec = ms / 1e3
+    gbs = nbytes / sec / 1e9
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+    t_tc = flops / (pk["bf16_tflops"] * 1e12)
+    roof = {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": gbs / pk["hbm_gbs"],
+            "traffic": profiled_traffic(s.name, "decode" if bandwidth_metric(s) else "prefill"),
+            "peak_source": f"{pk_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+            if pk_kind == "measured" else "fallback 6.8 TB/s",
+            "kernels": prefill_kernels(inp)}
+    if not bandwidth_metric(s):
+        tfs = flops / sec / 1e12
+        roof["tensor_tflops"] = tfs
+        roof["tensor_frac_of_bf16_peak"] = tfs / pk["bf16_tflops"]
+        roof["roofline_time_us"] = max(t_hbm, t_tc) * 1e6
+        roof["frac_of_roofline"] = max(t_hbm, t_tc) / sec
+    return roof
 
 
 def prefill_kernels(inp) -> str:

@@ -153,8 +153,11 @@ gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, con
  * allocates nothing and frees nothing.  It runs the records-only path (no
  * time-parallel scan, no internal stream), so it needs the chunk records alone: a
  * shape needing more than that size returns GDN_ERR_INVALID_ARG and launches
- * nothing.  96 MiB holds 1,213 records of one (64-token chunk, value head), e.g. one
- * 4,096-token sequence at 16 value heads.
+ * nothing.  A record covers one (64-token chunk, value head) and takes 82,944 bytes, so
+ * 96 MiB holds 1,213 records.  The count is read the way the call itself runs: a batched
+ * call (cu_seqlens NULL) needs batch * ceil(seqlen / 64) * h_v records, a packed call
+ * (cu_seqlens given) (floor(seqlen / 64) + num_seqs + 1) * h_v.  One batched sequence of
+ * up to 4,800 tokens at 16 value heads fits (75 x 16 = 1,200 records); 4,801 does not.
  * Shapes off the tensor-core path need no scratch and run as in gdn_prefill.
  *
  * All calls on a device share the one array.  Each call writes every scratch

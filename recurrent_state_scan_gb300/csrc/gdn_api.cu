@@ -33,20 +33,13 @@ gdn_status cuda_fail(cudaError_t e, const char *what) {
     return fail(GDN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-// Address of the check word on the current device (looked up once per device).
+// Address of the check word in the current device's context, looked up on every call so
+// that a context created again after cudaDeviceReset never sees a stale address.
 gdn_status status_word(int **out) {
-    static int *cache[64] = {nullptr};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= 64) return fail(GDN_ERR_UNSUPPORTED, "device ordinal %d >= 64", dev);
-    if (cache[dev] == nullptr) {
-        void *ptr = nullptr;
-        e = cudaGetSymbolAddress(&ptr, g_device_status);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(check word)");
-        cache[dev] = static_cast<int *>(ptr);
-    }
-    *out = cache[dev];
+    void *ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_device_status);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(check word)");
+    *out = static_cast<int *>(ptr);
     return GDN_OK;
 }
 
@@ -168,13 +161,16 @@ gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, con
 }  // extern "C"
 
 size_t gdn::prefill_records_bytes(const gdn_shape *shape) {
+    return prefill_records_bytes_for(shape, shape != nullptr && shape->batch == 1);
+}
+
+size_t gdn::prefill_records_bytes_for(const gdn_shape *shape, bool varlen) {
     if (shape == nullptr || shape->seqlen < 0 || shape->batch < 0 || shape->num_seqs < 0 ||
         shape->h_v <= 0)
         return 0;
-    const bool packed = shape->batch == 1;
-    const int64_t tokens = packed ? shape->seqlen : shape->seqlen * (int64_t)shape->batch;
+    const int64_t tokens = varlen ? shape->seqlen : shape->seqlen * (int64_t)shape->batch;
     if (!prefill_tc_shape_ok((gdn_dtype)shape->io_dtype, shape->d_k, shape->d_v, tokens)) return 0;
-    return prefill_tc_workspace(packed, shape->seqlen, shape->batch, shape->num_seqs, shape->h_v);
+    return prefill_tc_workspace(varlen, shape->seqlen, shape->batch, shape->num_seqs, shape->h_v);
 }
 
 gdn_status gdn::prefill_impl(const gdn_shape *shape, const void *q, const void *k, const void *v,

@@ -132,6 +132,8 @@ int prefill_tc_segments(bool varlen, int64_t seqlen, int64_t batch, int h_v);
 // Bytes of chunk records a prefill of this shape needs on the tensor-core path (0 off it);
 // the packed reading when batch is 1.
 size_t prefill_records_bytes(const gdn_shape *shape);
+// The same for a call that is packed (cu_seqlens given) or batched, as the dispatch reads it.
+size_t prefill_records_bytes_for(const gdn_shape *shape, bool varlen);
 // Time-parallel scan of batched shapes whose scan grid leaves most of the GPU idle: the
 // segments it uses (1: none) and the workspace bytes it needs after the records (0: none).
 int prefill_tc_tp_nseg(bool varlen, int64_t seqlen, int64_t batch, int h_v);

@@ -17,25 +17,19 @@ namespace {
 // Scratch of the tensor-core prefill for calls through gdn_prefill_noalloc.
 static __device__ __align__(256) unsigned char g_prefill_scratch[GDN_PREFILL_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_prefill_scratch, looked up once per device.
+// Device address of g_prefill_scratch in the current device's context.  It is looked up
+// on every call (a cheap runtime query), so that a context torn down and created again
+// (cudaDeviceReset) never leaves a stale address behind.
 gdn_status scratch_address(void **out) {
-    static void *cache[64] = {nullptr};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return report_error(GDN_ERR_CUDA, "cudaGetDevice failed");
-    if (dev < 0 || dev >= 64) return report_error(GDN_ERR_UNSUPPORTED, "device ordinal >= 64");
-    if (cache[dev] == nullptr) {
-        void *ptr = nullptr;
-        e = cudaGetSymbolAddress((void **)&ptr, g_prefill_scratch);
-        if (e != cudaSuccess || ptr == nullptr) {
-            char msg[256];
-            snprintf(msg, sizeof(msg), "cudaGetSymbolAddress(prefill scratch): %s",
-                     cudaGetErrorString(e));
-            return report_error(GDN_ERR_CUDA, msg);
-        }
-        cache[dev] = ptr;
+    void *ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress((void **)&ptr, g_prefill_scratch);
+    if (e != cudaSuccess || ptr == nullptr) {
+        char msg[256];
+        snprintf(msg, sizeof(msg), "cudaGetSymbolAddress(prefill scratch): %s",
+                 cudaGetErrorString(e));
+        return report_error(GDN_ERR_CUDA, msg);
     }
-    *out = cache[dev];
+    *out = ptr;
     return GDN_OK;
 }
 
@@ -51,7 +45,7 @@ extern "C" gdn_status gdn_prefill_noalloc(const gdn_shape *shape, const void *q,
     // Every scratch byte the kernels read is written earlier in the same call, so
     // nothing left by a previous call needs clearing.  The call runs the records-only
     // path (no time-parallel buffers, no internal stream), so the records are the need.
-    const size_t need = gdn::prefill_records_bytes(shape);
+    const size_t need = gdn::prefill_records_bytes_for(shape, cu_seqlens != nullptr);
     if (need > (size_t)GDN_PREFILL_NOALLOC_SCRATCH_BYTES) {
         char msg[256];
         snprintf(msg, sizeof(msg),

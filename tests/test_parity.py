@@ -50,24 +50,19 @@ def test_decode_b256_full():
     check(inp, o, s, o_ref, s_ref, what="decode B=256")
 
 
-SAMPLED = {
-    # (workload, sampled (sequence * h_v + head) units)
-    "bf16_prefill_t4096": [0, 7, 15],
-    "varlen_bf16_prefill": [0 * 16 + 3, 1 * 16 + 0, 6 * 16 + 15, 7 * 16 + 9],
-    "gqa_f16_prefill": [0, 1, 31, 32 + 14, 32 + 15],
-}
+FULL_SIZE_PREFILL = ["bf16_prefill_t4096", "varlen_bf16_prefill", "gqa_f16_prefill"]
 
 
-@pytest.mark.parametrize("name", sorted(SAMPLED))
-def test_prefill_workloads_sampled_units(name):
-    """Full-size run in the benchmark's launch configuration; the oracle computes
-    a sample of (sequence, head) units in full (every token, the final state)."""
+@pytest.mark.parametrize("name", FULL_SIZE_PREFILL)
+def test_prefill_workloads_full(name):
+    """Full-size run in the benchmark's launch configuration against the oracle over the
+    whole workload: every token of every (sequence, head) unit and every final state."""
+    import os
     inp = workloads.workload(name)
     o, s = run_prefill(inp)
-    assert np.all(np.isfinite(o)) and np.all(np.isfinite(s))
-    units = SAMPLED[name]
-    o_ref, s_ref = oracle.scan_inputs(inp, units=units, threads=len(units))
-    check(inp, o, s, o_ref, s_ref, units=units, what=name)
+    o_ref, s_ref = oracle.scan_inputs(inp, threads=os.cpu_count() or 1)
+    eo, es = check(inp, o, s, o_ref, s_ref, what=name)
+    print(f"{name}: max|d|/max|ref| o {eo:.3e}, state {es:.3e}")
 
 
 # ---------------------------------------------------------------- small shapes, edges

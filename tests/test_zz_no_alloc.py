@@ -6,16 +6,19 @@ Its scratch is a fixed array inside the library, shared by every call on a devic
 and holding whatever the previous call left there.  The GPU test makes two calls
 in a row on the same shape with different inputs, so the second call starts from
 the first call's records, and checks each against gdn_prefill (caller-provided
-workspace) on the same inputs, within the parity tolerance of the I/O type.  The
-file is named to be collected last, and passes alone or after the other tests.
+workspace) and against the float64 CPU oracle on the same inputs, within the parity
+tolerance of the I/O type.  The file is named to be collected last, and passes alone
+or after the other tests.
 """
 import ctypes
+import os
 
 import pytest
 import torch
 
+import oracle
 import workloads
-from gpu_util import TOL, rel_err, to_device
+from gpu_util import TOL, check, rel_err, to_device
 
 
 def test_noalloc_rejects_oversized_shapes_on_the_host():
@@ -26,7 +29,7 @@ def test_noalloc_rejects_oversized_shapes_on_the_host():
     assert gdn.gdn_prefill_workspace_bytes(shape) > gdn.PREFILL_NOALLOC_SCRATCH_BYTES
     st = lib.gdn_prefill_noalloc(ctypes.byref(shape), *([None] * 9), 0.0, None, None, None)
     assert st == gdn.GDN_ERR_INVALID_ARG
-    assert b"scratch" in lib.gdn_last_error_message()
+    assert b"above the fixed" in lib.gdn_last_error_message()
     # The largest advertised example passes the size check: one 4096-token sequence at 16
     # value heads needs 64 x 16 records (the call then stops at its NULL inputs, or at the
     # missing device).  gdn_prefill's own workspace query also counts the time-parallel
@@ -34,7 +37,33 @@ def test_noalloc_rejects_oversized_shapes_on_the_host():
     fits = gdn.make_shape(gdn.GDN_BF16, 1, 4096, 1, 16, 16, 128, 128)
     assert 64 * 16 * 82944 <= gdn.PREFILL_NOALLOC_SCRATCH_BYTES
     st = lib.gdn_prefill_noalloc(ctypes.byref(fits), *([None] * 9), 0.0, None, None, None)
-    assert st != gdn.GDN_OK and b"scratch" not in lib.gdn_last_error_message()
+    assert st != gdn.GDN_OK and b"above the fixed" not in lib.gdn_last_error_message()
+
+
+def test_noalloc_size_boundary_follows_the_call_layout():
+    """A batched call (no cu_seqlens) is sized as batch * ceil(T / 64) * h_v records of
+    82,944 bytes: 4,800 tokens at 16 value heads (1,200 records) fit the 96 MiB array and
+    4,801 (1,216 records) do not.  A packed call of the same tokens needs
+    (floor(T / 64) + N + 1) * h_v records."""
+    from recurrent_state_scan_gb300 import gdn
+    lib = gdn.load()
+    rec = 82944
+    assert 1200 * rec <= gdn.PREFILL_NOALLOC_SCRATCH_BYTES < 1216 * rec
+    for T, fits in ((4800, True), (4801, False)):
+        shape = gdn.make_shape(gdn.GDN_BF16, 1, T, 1, 16, 16, 128, 128)
+        st = lib.gdn_prefill_noalloc(ctypes.byref(shape), *([None] * 9), 0.0, None, None, None)
+        assert st != gdn.GDN_OK
+        assert (b"above the fixed" in lib.gdn_last_error_message()) == (not fits), T
+    # Packed, one sequence of 4,672 tokens: (73 + 1 + 1) * 16 = 1,200 records fit; a
+    # packed 4,800 would need (75 + 2) * 16 = 1,232 and is refused before any pointer is read.
+    cu = ctypes.c_void_p(16)   # never dereferenced: the size check comes first
+    for T, fits in ((4672, True), (4800, False)):
+        shape = gdn.make_shape(gdn.GDN_BF16, 1, T, 1, 16, 16, 128, 128)
+        args = [None] * 9
+        args[8] = cu
+        st = lib.gdn_prefill_noalloc(ctypes.byref(shape), *args, 0.0, None, None, None)
+        assert st != gdn.GDN_OK
+        assert (b"above the fixed" in lib.gdn_last_error_message()) == (not fits), T
 
 
 @pytest.mark.gpu
@@ -61,6 +90,9 @@ def test_noalloc_matches_gdn_prefill_on_two_calls_in_a_row():
         eo = rel_err(o.float().cpu().numpy(), o_ref.float().cpu().numpy())
         es = rel_err(s.cpu().numpy(), s_ref.cpu().numpy())
         assert eo <= tol and es <= tol, f"call with seed {seed}: rel err o {eo:.2e}, state {es:.2e}"
+        o_or, s_or = oracle.scan_inputs(inp, threads=4)
+        check(inp, o.float().cpu().numpy().reshape(-1, inp.spec.h_v, inp.spec.d_v),
+              s.cpu().numpy(), o_or, s_or, what=f"noalloc call with seed {seed} vs oracle")
 
 
 @pytest.mark.gpu
@@ -85,3 +117,6 @@ def test_noalloc_runs_the_largest_advertised_shape():
     tol = TOL["bf16"]
     assert rel_err(o.float().cpu().numpy(), o_ref.float().cpu().numpy()) <= tol
     assert rel_err(s.cpu().numpy(), s_ref.cpu().numpy()) <= tol
+    o_or, s_or = oracle.scan_inputs(inp, threads=os.cpu_count() or 1)
+    check(inp, o.float().cpu().numpy().reshape(-1, inp.spec.h_v, inp.spec.d_v), s.cpu().numpy(),
+          o_or, s_or, what="noalloc bf16 prefill T=4096 vs oracle")
