@@ -772,8 +772,8 @@ def prefill_kernels(inp) -> str:
         return "decode_stream_kernel (persistent, prefetching), one call"
     path, _ = gdn.gdn_prefill_plan(gdn.shape_of_spec(inp.spec, inp.n_seq, inp.total_tokens))
     if path == gdn.PATH_TC_TP:
-        return ("gdn_chunk_prep + gdn_chunk_scan (time-parallel segments) + gdn_tp_combine, "
-                "and the cuBLAS correction GEMM, one call")
+        return ("gdn_chunk_prep + gdn_chunk_scan (time-parallel segments) + gdn_tp_combine "
+                "+ gdn_tp_correct, one call")
     if path == gdn.PATH_TC:
         return "gdn_chunk_prep + gdn_chunk_scan, one call"
     return "scan_simt, one call"

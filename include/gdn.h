@@ -31,9 +31,10 @@
  *    the device can see (a malformed device cu_seqlens, a slot outside a state
  *    pool) set a device check word, skip the affected work without faulting, and
  *    are reported by gdn_last_device_status().
- *  - Internal resources: gdn_prefill may create, once per device, a CUDA stream
- *    and a cuBLAS handle (see gdn_prefill_workspace_bytes); gdn_prefill_noalloc
- *    and every other call create nothing.
+ *  - Internal resources: gdn_prefill may create, once per device, a CUDA stream and
+ *    two events (see gdn_prefill_workspace_bytes); gdn_prefill_noalloc and every
+ *    other call create nothing.  No call allocates device memory or uses a library
+ *    kernel.
  *
  * Entry points: gdn_prefill (and gdn_prefill_noalloc, gdn_prefill_plan,
  * gdn_prefill_workspace_bytes), gdn_decode_step, gdn_decode_step_slots (a state
@@ -122,15 +123,15 @@ typedef struct gdn_shape {
  *
  * On the tensor-core path a batched call whose scan uses few SMs is cut along the
  * time axis into segments that are scanned at once (each from a zero state and, for
- * the correction, from the identity with the values zeroed), then combined; the
- * correction o += R S_k of each later segment is a cuBLAS batched GEMM (one handle per
- * device, created on first use, working in the workspace).  That needs the full
- * gdn_prefill_workspace_bytes(shape); a workspace that holds only the chunk records
- * (81 KiB per chunk and value head) instead splits the call into chunk segments whose
- * preparation runs on a stream internal to the library (one per device, created on
- * first use) beside the scan of the earlier one.  Either way the work is ordered after
- * what `stream` held at the call and the call's last kernel is ordered after it, so
- * the call keeps the stream-ordered semantics above.
+ * the correction, from the identity with the values zeroed), then combined; a last
+ * kernel adds the correction o += R S_k of each later segment on the tensor cores,
+ * with S_k taken in fp32.  That needs the full gdn_prefill_workspace_bytes(shape); a
+ * workspace that holds only the chunk records (81 KiB per chunk and value head)
+ * instead splits the call into chunk segments whose preparation runs on a stream
+ * internal to the library (one per device, created on first use) beside the scan of
+ * the earlier one.  Either way the work is ordered after what `stream` held at the
+ * call and the call's last kernel is ordered after it, so the call keeps the
+ * stream-ordered semantics above.
  */
 size_t gdn_prefill_workspace_bytes(const gdn_shape *shape);
 
@@ -326,12 +327,23 @@ gdn_status gdn_last_device_status(void *stream);
  * gdn_prefill_plan -- report, without launching anything, which kernel path
  * gdn_prefill takes for `shape` (*path: 1 = token-sequential SIMT scan,
  * 2 = chunked tensor-core scan, 3 = chunked tensor-core scan run time-parallel) and how
- * many of the library's own kernels one call launches (*launches; the time-parallel
- * scan's correction GEMMs are cuBLAS calls on top).  Path 3 assumes the workspace that
+ * many kernels one call launches (*launches).  Path 3 assumes the workspace that
  * gdn_prefill_workspace_bytes reports; with less (down to the records alone) the call
  * takes path 2.  Returns the same status gdn_prefill's shape checks would.
  */
 gdn_status gdn_prefill_plan(const gdn_shape *shape, int32_t *path, int32_t *launches);
+
+/*
+ * gdn_set_wait_budget -- a test hook, process-wide and not part of the operation: the
+ * cycles a bounded wait of the tensor-core prefill kernels (chunk prep and state scan)
+ * may take before the waiting CTA gives up, for gdn_prefill calls made after it
+ * (0 = the default, about two seconds).  A wait that runs out makes the CTA let the
+ * copies and MMAs it has issued finish under the full two-second budget, free its
+ * tensor memory and leave; gdn_last_device_status() then returns GDN_ERR_TIMEOUT and
+ * the call's outputs are undefined.  Nothing is left running or waiting on the device.
+ * A negative value returns GDN_ERR_INVALID_ARG.
+ */
+gdn_status gdn_set_wait_budget(int64_t cycles);
 
 /* Static name of a status code. */
 const char *gdn_status_string(gdn_status status);

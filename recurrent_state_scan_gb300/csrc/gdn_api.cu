@@ -131,12 +131,12 @@ gdn_status gdn_prefill_plan(const gdn_shape *shape, int32_t *path, int32_t *laun
     const bool varlen = shape->batch == 1 && shape->num_seqs != 1;
     const int64_t tokens = varlen ? shape->seqlen : shape->seqlen * (int64_t)shape->batch;
     const bool tc = prefill_tc_shape_ok((gdn_dtype)shape->io_dtype, shape->d_k, shape->d_v, tokens);
-    // Time-parallel scan: prep, scan and one combine per segment boundary (the correction
-    // GEMMs are library calls); else the prep and scan of every chunk segment.
+    // Time-parallel scan: prep, scan, one combine per segment boundary and the correction;
+    // else the prep and scan of every chunk segment.
     const int tps = tc ? prefill_tc_tp_nseg(varlen, shape->seqlen, shape->batch, shape->h_v) : 1;
     if (path) *path = tc ? (tps > 1 ? 3 : 2) : 1;
     const int nseg = tc ? prefill_tc_segments(varlen, shape->seqlen, shape->batch, shape->h_v) : 1;
-    if (launches) *launches = shape->num_seqs > 0 ? (tc ? (tps > 1 ? 1 + tps : 2 * nseg) : 1) : 0;
+    if (launches) *launches = shape->num_seqs > 0 ? (tc ? (tps > 1 ? 2 + tps : 2 * nseg) : 1) : 0;
     return GDN_OK;
 }
 
@@ -148,6 +148,12 @@ size_t gdn_prefill_workspace_bytes(const gdn_shape *shape) {
     // Records, plus the time-parallel scan's buffers when a batched call of this shape
     // would use it (with batch 1 the shape may also be a packed call: the sum covers both).
     return records + prefill_tc_tp_bytes(false, shape->seqlen, shape->batch, shape->h_v);
+}
+
+gdn_status gdn_set_wait_budget(int64_t cycles) {
+    if (cycles < 0) return fail(GDN_ERR_INVALID_ARG, "wait budget %lld < 0", (long long)cycles);
+    __atomic_store_n(&g_wait_budget, (long long)cycles, __ATOMIC_RELAXED);
+    return GDN_OK;
 }
 
 gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, const void *v,

@@ -144,6 +144,10 @@ cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_t
                               void *workspace, size_t workspace_bytes, bool allow_overlap,
                               cudaStream_t stream);
 
+// Cycles a bounded wait of the tensor-core prefill kernels may take before the CTA gives
+// up (0: about two seconds), set by gdn_set_wait_budget.
+extern long long g_wait_budget;
+
 // gdn_prefill with the segment overlap allowed or not (no internal stream is created
 // when it is not).
 gdn_status prefill_impl(const gdn_shape *shape, const void *q, const void *k, const void *v,

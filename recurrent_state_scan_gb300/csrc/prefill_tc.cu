@@ -27,7 +27,6 @@
 // half needs only its half of U and Delta.  All MMAs use M = 128, so accumulator row r
 // is TMEM lane r.  Rows past the end of a sequence get g = 0 and beta = 0, which makes
 // their T row the unit row and their W, U and Delta rows exactly zero.
-#include <cublas_v2.h>
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -83,6 +82,7 @@ struct TcParams {
     float scale;
     int *status;
     uint8_t *ws;                    // workspace records
+    long long wait_budget;          // cycles a bounded wait may take (0: kWaitBudget)
     // Time-parallel scan (tp_seg > 0): every sequence is cut into tp_nseg segments of
     // tp_seg chunks, all scanned at once.  Segment k > 0 runs twice: from a zero state
     // (outputs to o, end state to tp_psi[k]) and as the operator pass, from the identity
@@ -309,6 +309,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
                                               ~static_cast<uintptr_t>(1023));
     __shared__ PrepCtl ctl;
     const int pt = threadIdx.x, warp = pt >> 5, lane = pt & 31;
+    const long long budget = p.wait_budget > 0 ? p.wait_budget : kWaitBudget;
     const int q = warp & 3, hf = warp >> 2;        // TMEM lane quarter, column half
     const int h = blockIdx.x % p.h_v;
     const int hq = h / (p.h_v / p.h_qk);
@@ -434,7 +435,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
     }
     // D1 = [K; Q] K^T once K and Q have landed.
     if (pt == 0) {
-        ok = mbar_wait(&ctl.full, 0, kWaitBudget);
+        ok = mbar_wait(&ctl.full, 0, budget);
         if (ok) {
             tc_fence_after();
 #pragma unroll
@@ -445,11 +446,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
             }
             mma_commit(&ctl.d1);
             issued |= 2;
-            ok = mbar_wait(&ctl.d1, 0, kWaitBudget);
+            ok = mbar_wait(&ctl.d1, 0, budget);
         }
     }
     failed = bar_any(kBarPrep, kPrepThreads, !ok);   // also publishes E, F, gamma
-    if (!failed) ok = mbar_wait(&ctl.full, 0, kWaitBudget);   // every reader of Q and V
+    if (!failed) ok = mbar_wait(&ctl.full, 0, budget);   // every reader of Q and V
     if (!failed) {
         tc_fence_after();
         // A rows (lanes 0-63, fp32) and P rows (lanes 64-127, I/O type); each column half
@@ -545,7 +546,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
             mma_commit(&ctl.d23);
             issued |= 4;
         }
-        ok = mbar_wait(&ctl.d23, 0, kWaitBudget);
+        ok = mbar_wait(&ctl.d23, 0, budget);
         failed = bar_any(kBarPrep, kPrepThreads, !ok);
     }
     if (!failed) {
@@ -595,7 +596,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
             bulk_commit();
             // M_c = W_c K_{c-1}^T (columns scaled below) into TMEM columns 0-63.
             if (!first) {
-                ok = mbar_wait(&ctl.kprev, 0, kWaitBudget);
+                ok = mbar_wait(&ctl.kprev, 0, budget);
                 if (ok) {
                     tc_fence_after();
                     const uint32_t aW = smem_u32(sm + PP_KQW + 16384), aKp = smem_u32(sm + PP_AS);
@@ -609,7 +610,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
             }
         }
         if (!first) {
-            if (pt == 0) ok = ok && mbar_wait(&ctl.dm, 0, kWaitBudget);
+            if (pt == 0) ok = ok && mbar_wait(&ctl.dm, 0, budget);
             failed = bar_any(kBarPrep, kPrepThreads, !ok);
             if (!failed) {
                 // M_c[i][j] = (W_c K_{c-1}^T)[i][j] e^{G_C - G_j} of chunk c - 1, rows on lanes
@@ -702,17 +703,25 @@ struct ScanCtl {
 // threads sleep in the barrier rather than poll, except the single thread that issues
 // the MMAs, which polls so that it wakes the moment the phase completes.
 template <bool kPoll = false>
-__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int32_t *abort) {
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int32_t *abort,
+                                              long long budget) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!(kPoll ? mbar_try_wait(bar, parity) : mbar_try_wait_sleep(bar, parity, 20000u))) {
         if (*abort) return false;
-        if (clock64() - t0 > kWaitBudget) {
+        if (clock64() - t0 > budget) {
             *abort = 1;
             return false;
         }
     }
     return true;
+}
+
+// The same, agreed by the whole warp: the tensor-memory loads that follow a wait are
+// warp-wide instructions, so every lane must take the same branch after it.
+__device__ __forceinline__ bool warp_wait_or_abort(uint64_t *bar, uint32_t parity, volatile int32_t *abort,
+                                                   long long budget) {
+    return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort, budget));
 }
 
 // Scan CTAs: one per (sequence, value head, half of the 128 state columns).  Chunk c, with
@@ -738,6 +747,7 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                                               ~static_cast<uintptr_t>(1023));
     __shared__ ScanCtl ctl;
     volatile int32_t *abort = &ctl.abort;
+    const long long budget = p.wait_budget > 0 ? p.wait_budget : kWaitBudget;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool issue_warp = (warp == kChainWarps);
     const bool copy_warp = (warp == kChainWarps + 1);
@@ -864,16 +874,16 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
             bool ok = true;
             do {
                 // X phase 0: W_0 S_0 into block 1 (the Q~ rows there are unused).
-                if (!(ok = wait_or_abort<true>(&ctl.sb_ready, 0, abort) && wait_or_abort<true>(&ctl.full_w, 0, abort))) break;
+                if (!(ok = wait_or_abort<true>(&ctl.sb_ready, 0, abort, budget) && wait_or_abort<true>(&ctl.full_w, 0, abort, budget))) break;
                 issue_qw(1, 1);
                 mma_commit(&ctl.x);
                 // D4'(0) into block 0.
-                if (!(ok = wait_or_abort<true>(&ctl.full_b[0], 0, abort))) break;
+                if (!(ok = wait_or_abort<true>(&ctl.full_b[0], 0, abort, budget))) break;
                 issue_qw(0, 0);
                 mma_commit(&ctl.d4);
                 // Stage 1's part B, once W_0 S_0 has read its rows.
                 if (nchunks > 1) {
-                    if (!(ok = wait_or_abort<true>(&ctl.x, 0, abort))) break;
+                    if (!(ok = wait_or_abort<true>(&ctl.x, 0, abort, budget))) break;
                     load_b(1);
                     b1_issued = true;
                 }
@@ -883,9 +893,9 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                 const uint32_t aSt = smem_u32(sm + s * kScanStage);
                 // DS(c) once Delta_c is in DB0 / DB1; the copy warp has seen X phase c
                 // and sb_ready phase c, so neither can run two phases ahead of it.
-                ok = wait_or_abort<true>(&ctl.delta_ready, c & 1, abort) &&
-                     wait_or_abort<true>(&ctl.full_a[s], (c >> 1) & 1, abort) &&
-                     (c == 0 || wait_or_abort<true>(&ctl.ld_a, (c - 1) & 1, abort));
+                ok = wait_or_abort<true>(&ctl.delta_ready, c & 1, abort, budget) &&
+                     wait_or_abort<true>(&ctl.full_a[s], (c >> 1) & 1, abort, budget) &&
+                     (c == 0 || wait_or_abort<true>(&ctl.ld_a, (c - 1) & 1, abort, budget));
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
@@ -895,7 +905,7 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                 mma_commit(&ctl.ds);
                 // X(c) onto D4'(c).  The readout of chunk c - 1 is done, so the readout
                 // warps have seen X phase c and block (c + 1) & 1 is free for D4'(c + 1).
-                if (c > 0 && !(ok = wait_or_abort<true>(&ctl.out_done, (c - 1) & 1, abort))) break;
+                if (c > 0 && !(ok = wait_or_abort<true>(&ctl.out_done, (c - 1) & 1, abort, budget))) break;
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_f16(tmem + TS_D4 + 64 * s, sw128_desc(aSt + SS_PM + k * 32, 16, 1024),
@@ -903,9 +913,9 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                 mma_commit(&ctl.x);
                 if (c + 1 < nchunks) {
                     // D4'(c + 1) once SB holds S_{c+1} (and the copy warp has seen D4'(c)).
-                    ok = wait_or_abort<true>(&ctl.sb_ready, (c + 1) & 1, abort) &&
-                         wait_or_abort<true>(&ctl.full_b[(c + 1) & 1], ((c + 1) >> 1) & 1, abort) &&
-                         wait_or_abort<true>(&ctl.ld_b, c & 1, abort);
+                    ok = wait_or_abort<true>(&ctl.sb_ready, (c + 1) & 1, abort, budget) &&
+                         wait_or_abort<true>(&ctl.full_b[(c + 1) & 1], ((c + 1) >> 1) & 1, abort, budget) &&
+                         wait_or_abort<true>(&ctl.ld_b, c & 1, abort, budget);
                     if (!ok) break;
                     issue_qw((c + 1) & 1, (c + 1) & 1);
                     mma_commit(&ctl.d4);
@@ -943,7 +953,7 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                 const int s = c & 1;
                 // D4'(c) has read part B of stage s: refill it with chunk c + 2.  The
                 // arrivals only say which phases this warp has seen, so they go first.
-                if (!(ok = wait_or_abort(&ctl.d4, c & 1, abort))) break;
+                if (!(ok = wait_or_abort(&ctl.d4, c & 1, abort, budget))) break;
                 mbar_arrive(&ctl.ld_b);
                 if (c + 2 < nchunks) {
                     load_b(c + 2);
@@ -951,8 +961,8 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                 }
                 // X(c) has read the rest of stage s and every thread has read chunk c's
                 // gates (they arrive on sb_ready after that): refill part A.
-                if (!(ok = wait_or_abort(&ctl.x, (c + 1) & 1, abort) &&
-                           wait_or_abort(&ctl.sb_ready, (c + 1) & 1, abort)))
+                if (!(ok = wait_or_abort(&ctl.x, (c + 1) & 1, abort, budget) &&
+                           wait_or_abort(&ctl.sb_ready, (c + 1) & 1, abort, budget)))
                     break;
                 mbar_arrive(&ctl.ld_a);
                 if (c + 2 < nchunks) {
@@ -1010,13 +1020,13 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
             const uint8_t *st = sm + s * kScanStage;
             const GateRec &gr = *reinterpret_cast<const GateRec *>(st + SS_G);
             // Every reader of the stage observes its arrival itself.
-            ok = ok && wait_or_abort(&ctl.full_a[s], (c >> 1) & 1, abort);
+            ok = ok && warp_wait_or_abort(&ctl.full_a[s], (c >> 1) & 1, abort, budget);
             const float gC = ok ? gr.gC : 0.f;
 
             if (!out_warp) {
                 // Delta_c = U_c - W_c S_c on lanes 64-127 (token rows), this thread's 32
                 // columns; W_c S_c is in block (c - 1) & 1 after X phase c.
-                ok = ok && wait_or_abort(&ctl.x, c & 1, abort);
+                ok = ok && warp_wait_or_abort(&ctl.x, c & 1, abort, budget);
                 if (ok) {
                     tc_fence_after();
                     const int j = row - 64;
@@ -1065,7 +1075,7 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
             }
 
             // S_{c+1} = gamma_C S_c + DS(c) (fp32 registers), then the operand tile.
-            ok = ok && wait_or_abort(&ctl.ds, c & 1, abort);
+            ok = ok && warp_wait_or_abort(&ctl.ds, c & 1, abort, budget);
             if (ok) {
                 tc_fence_after();
 #pragma unroll
@@ -1090,7 +1100,7 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
             const int Lc = (int)((L - (int64_t)c * kC) < kC ? (L - (int64_t)c * kC) : kC);
             const bool tile_store = (Lc == kC);
             uint8_t *ob = sm + SS_OUT + s * 8192;
-            ok = ok && wait_or_abort(&ctl.x, (c + 1) & 1, abort);
+            ok = ok && warp_wait_or_abort(&ctl.x, (c + 1) & 1, abort, budget);
             if (ok) {
                 tc_fence_after();
                 uint4 packed[4];
@@ -1157,10 +1167,10 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
 // S_{k+1} = Phi_k S_k + Psi_k.  One launch per step k: a CTA owns a 32 x 32 tile of
 // S_{k+1} for one (sequence, head), with its 32 rows of Phi_k and 32 columns of S_k staged
 // in shared memory, and writes it over Psi_k (each element is read, then written, by one
-// thread), so Psi_k holds S_{k+1} afterwards.  It also writes its 32 rows of S_k, in the
-// I/O type, for the correction GEMM; the last step writes state_out as well.
+// thread), so Psi_k holds S_{k+1} afterwards and Psi_{k-1} holds S_k, in fp32, for the
+// correction below; the last step writes state_out as well.
 template <typename IO>
-__global__ void __launch_bounds__(256) gdn_tp_combine(const __grid_constant__ TcParams p, IO *sk, int k) {
+__global__ void __launch_bounds__(256) gdn_tp_combine(const __grid_constant__ TcParams p, int k) {
     __shared__ float Ph[32][kDK + 1];     // rows rb .. rb + 31 of Phi_k
     __shared__ float Sc[kDK][33];         // columns cb .. cb + 31 of S_k
     const size_t off = (size_t)blockIdx.x * kDK * kDK;           // (n, h) slab
@@ -1185,10 +1195,6 @@ __global__ void __launch_bounds__(256) gdn_tp_combine(const __grid_constant__ Tc
         Sc[e >> 5][e & 31] = sc[u];
     }
     __syncthreads();
-    // This CTA's rows of S_k for the GEMM (every element of S_k is written by one CTA).
-    IO *skk = sk + (size_t)k * slab + off;
-    for (int e = tid; e < 32 * 32; e += 256)
-        IoType<IO>::st(skk + (size_t)(rb + (e >> 5)) * kDK + cb + (e & 31), Sc[rb + (e >> 5)][e & 31]);
     // Thread: column j, rows i0 .. i0 + 3.
     const int j = tid & 31, i0 = 4 * (tid >> 5);
     float acc[4];
@@ -1205,6 +1211,174 @@ __global__ void __launch_bounds__(256) gdn_tp_combine(const __grid_constant__ Tc
         const size_t at = (size_t)(rb + i0 + i) * kDK + cb + j;
         psi[at] = acc[i];
         if (k == p.tp_nseg - 1) p.state_out[off + at] = acc[i];
+    }
+}
+
+// ===================================================================== time-parallel correction
+// o_t += R_t S_k for the tokens t of segment k >= 1, where o_t came from the run of the
+// segment from a zero state and R_t from its operator pass.  One CTA per (sequence, head,
+// segment k, 128-token tile): D = R_tile S_k on tcgen05 (M = 128 tokens, N = 128 value
+// columns, K = 128 key rows), with R by TMA and S_k read in fp32 and split into two 16-bit
+// parts S_hi + S_lo (S_k - S_hi rounded), so that S_k enters the product to about 2^-16
+// relative; then o = round(o + D) row by row.
+constexpr int kCorrThreads = 128;
+constexpr int CR_R = 0;               // R tile: 2 d_k regions of 128 token rows (K-major)
+constexpr int CR_SH = 32768;          // S_hi: 2 d_v regions of 128 d_k rows (MN-major)
+constexpr int CR_SL = 65536;          // S_lo
+constexpr int kCorrSmem = 98304 + 1024;
+
+// x rounded to the nearest value of the I/O type, as a float.
+template <typename IO>
+__device__ __forceinline__ float round_io(float x) {
+    const float2 r = Pack<IO>::unpack(Pack<IO>::two(x, 0.f));
+    return r.x;
+}
+
+template <typename IO>
+__global__ void __launch_bounds__(kCorrThreads) gdn_tp_correct(const __grid_constant__ TcParams p) {
+    constexpr bool kBf16 = std::is_same<IO, __nv_bfloat16>::value;
+    constexpr uint32_t kId = idesc_f16(kBf16, 128, 128, false, true);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+    __shared__ uint64_t full, done;
+    __shared__ uint32_t tmem_base;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int unit = blockIdx.x;                       // (sequence, head)
+    const int h = unit % p.h_v;
+    const int64_t n = unit / p.h_v;
+    const int tiles = (p.tp_seg + 1) / 2;              // 128-token tiles per segment
+    const int k = 1 + (int)(blockIdx.y / tiles);
+    const int tile = (int)(blockIdx.y % tiles);
+    const int64_t seg0 = (int64_t)k * p.tp_seg * kC;
+    const int64_t seg1 = seg0 + (int64_t)p.tp_seg * kC < p.seqlen ? seg0 + (int64_t)p.tp_seg * kC : p.seqlen;
+    const int64_t tb = seg0 + (int64_t)tile * 128;
+    if (tb >= seg1) return;
+    const int rows = (int)(seg1 - tb < 128 ? seg1 - tb : 128);
+    const int64_t tok0 = n * p.seqlen + tb;            // batched layout (the path runs batched calls only)
+
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, 128);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&full, 1);
+        mbar_init(&done, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&full, 4 * 8192);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            tma_load_3d(sm + CR_R + r * 16384, &p.tm_r, r * 64, h, (int)tok0, &full);
+            tma_load_3d(sm + CR_R + r * 16384 + 8192, &p.tm_r, r * 64, h, (int)(tok0 + 64), &full);
+        }
+    }
+    // This thread's row of o (token tok0 + tid), read now so that the loads overlap the
+    // rest; rows past the segment's end are neither read nor written.
+    const bool live = tid < rows;
+    IO *const orow = static_cast<IO *>(p.o) + ((size_t)(tok0 + (live ? tid : 0)) * p.h_v + h) * kDK;
+    uint4 ov[16];
+    if (live) {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) ov[q] = reinterpret_cast<const uint4 *>(orow)[q];
+    }
+    // S_k (fp32, row-major [d_k][d_v]) -> S_hi, S_lo in 16-byte chunks of 8 value columns
+    // (128-byte swizzle); a warp reads two whole rows (1 KiB) per step, eight steps in flight.
+    {
+        const float *S = p.tp_psi + ((size_t)(k - 1) * p.num_seqs * p.h_v + (size_t)unit) * kDK * kDK;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float4 a[8], b[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = tid + kCorrThreads * (8 * half + i);
+                const float4 *src = reinterpret_cast<const float4 *>(S + (size_t)(e >> 4) * kDK) + 2 * (e & 15);
+                a[i] = src[0];
+                b[i] = src[1];
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = tid + kCorrThreads * (8 * half + i);
+                const int row = e >> 4, ch = e & 15;
+                const float x[8] = {a[i].x, a[i].y, a[i].z, a[i].w, b[i].x, b[i].y, b[i].z, b[i].w};
+                float hi[8], lo[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    hi[q] = round_io<IO>(x[q]);
+                    lo[q] = x[q] - hi[q];
+                }
+                const uint32_t off = (ch >> 3) * 16384 + sw128_offset(row, ch & 7);
+                *reinterpret_cast<uint4 *>(sm + CR_SH + off) = pack8<IO>(hi);
+                *reinterpret_cast<uint4 *>(sm + CR_SL + off) = pack8<IO>(lo);
+            }
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    bool ok = true;
+    if (tid == 0) {
+        const long long budget = p.wait_budget > 0 ? p.wait_budget : kWaitBudget;
+        bool issued = false;
+        ok = mbar_wait(&full, 0, budget);
+        if (ok) {
+            tc_fence_after();
+            const uint32_t aR = smem_u32(sm + CR_R), aH = smem_u32(sm + CR_SH), aL = smem_u32(sm + CR_SL);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t da = sw128_desc(aR + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                mma_f16(tmem, da, sw128_desc(aH + kk * 2048, 16384, 1024), kId, kk > 0);
+                mma_f16(tmem, da, sw128_desc(aL + kk * 2048, 16384, 1024), kId, 1u);
+            }
+            mma_commit(&done);
+            issued = true;
+            ok = mbar_wait(&done, 0, budget);
+        }
+        if (!ok) {
+            // Let the copy and the MMAs already issued land before the CTA leaves (bounded).
+            atomicOr(p.status, kDevTimeout);
+            mbar_wait(&full, 0, kWaitBudget);
+            if (issued) mbar_wait(&done, 0, kWaitBudget);
+        }
+    }
+    ok = !bar_any(kBarPrep, kCorrThreads, !ok);       // the same value in every thread
+    if (ok) {
+        // Thread = token row tid (its TMEM lane): o = round(o + D).  The tensor-memory load
+        // is a warp-wide instruction, so every lane takes it; rows past the segment's end
+        // skip only their global read and write.
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < kDK; c0 += 32) {
+            uint32_t r[32];
+            __syncwarp();                              // every lane at the warp-wide load
+            tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + c0, r);
+            tmem_ld_wait();
+            if (!live) continue;
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8) {
+                const uint4 u = ov[c0 / 8 + q8];
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                float x[8];
+#pragma unroll
+                for (int k2 = 0; k2 < 4; ++k2) {
+                    const float2 t2 = Pack<IO>::unpack(w[k2]);
+                    x[2 * k2] = t2.x + __uint_as_float(r[8 * q8 + 2 * k2]);
+                    x[2 * k2 + 1] = t2.y + __uint_as_float(r[8 * q8 + 2 * k2 + 1]);
+                }
+                reinterpret_cast<uint4 *>(orow)[c0 / 8 + q8] = pack8<IO>(x);
+            }
+        }
+    }
+    // Rows past the segment's end (and every row after a failed wait) are left as they are.
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 128);
     }
 }
 
@@ -1298,6 +1472,9 @@ cudaError_t configure() {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(gdn_chunk_scan<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kScanSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gdn_tp_correct<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kCorrSmem);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
@@ -1380,8 +1557,6 @@ int64_t chunk_slots(bool varlen, int64_t seqlen, int64_t batch, int64_t num_seqs
 
 constexpr int kMaxTpSegments = 4;
 constexpr int kMinTpChunks = 16;
-constexpr size_t kBlasWorkspace = 4u << 20;
-
 // Segments of the time-parallel scan for a batched shape (1: not used).  Every segment
 // after the first costs two scan CTAs per (sequence, head, column half), and all of them
 // must fit on the GPU at once.
@@ -1396,10 +1571,9 @@ int tp_segments(bool varlen, int64_t seqlen, int64_t batch, int h_v) {
     return best;
 }
 
-// Bytes the time-parallel scan adds after the records: R, Phi, Psi, the S_k copies and
-// the GEMM library's workspace, each 1 KiB aligned.
+// Bytes the time-parallel scan adds after the records: R, Phi and Psi, each 1 KiB aligned.
 struct TpLayout {
-    size_t r, phi, psi, sk, blas, total;
+    size_t r, phi, psi, total;
 };
 TpLayout tp_layout(int64_t seqlen, int64_t batch, int h_v, int nseg) {
     auto up = [](size_t x) { return (x + 1023) & ~(size_t)1023; };
@@ -1409,38 +1583,15 @@ TpLayout tp_layout(int64_t seqlen, int64_t batch, int h_v, int nseg) {
     L.r = 0;
     L.phi = L.r + up(tok * h_v * kDK * 2);
     L.psi = L.phi + up(states * 4);
-    L.sk = L.psi + up(states * 4);
-    L.blas = L.sk + up(states * 2);
-    L.total = L.blas + kBlasWorkspace;
+    L.total = L.psi + up(states * 4);
     return L;
 }
 
-// One GEMM library handle per device, created on first use (it allocates once).
-struct Blas {
-    cublasHandle_t h = nullptr;
-    bool tried = false;
-    std::mutex mu;   // the handle's stream and workspace belong to one call at a time
-};
-Blas *blas() {
-    static Blas cache[64];
-    static std::mutex mu;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    Blas &b = cache[dev];
-    if (!b.tried) {
-        b.tried = true;
-        if (cublasCreate(&b.h) != CUBLAS_STATUS_SUCCESS) b.h = nullptr;
-    }
-    return b.h ? &b : nullptr;
-}
-
 // The time-parallel call: prep, the scan of every segment and operator pass at once, the
-// combine, then o_t += R_t S_k for the tokens of every segment k >= 1 (one batched GEMM
-// over heads per sequence and segment, bf16/f16 in, fp32 accumulation).
+// combine (one launch per segment boundary), then o_t += R_t S_k for the tokens of every
+// segment k >= 1.
 template <typename IO>
-cudaError_t launch_tp(TcParams tp, int64_t n_slots, int nseg, uint8_t *extra, Blas *bl,
-                      cudaStream_t stream) {
+cudaError_t launch_tp(TcParams tp, int64_t n_slots, int nseg, uint8_t *extra, cudaStream_t stream) {
     cudaError_t e = configure<IO>();
     if (e != cudaSuccess) return e;
     const TpLayout L = tp_layout(tp.seqlen, tp.num_seqs, tp.h_v, nseg);
@@ -1450,7 +1601,6 @@ cudaError_t launch_tp(TcParams tp, int64_t n_slots, int nseg, uint8_t *extra, Bl
     tp.tp_r = extra + L.r;
     tp.tp_phi = reinterpret_cast<float *>(extra + L.phi);
     tp.tp_psi = reinterpret_cast<float *>(extra + L.psi);
-    IO *sk = reinterpret_cast<IO *>(extra + L.sk);
     tp.seg_begin = 0;
     tp.seg_end = 0x7fffffff;
     tp.seg_direct = 0;
@@ -1460,39 +1610,18 @@ cudaError_t launch_tp(TcParams tp, int64_t n_slots, int nseg, uint8_t *extra, Bl
     gdn_chunk_scan<IO><<<(unsigned)(units * (2 * nseg - 1)), kScanAllThreads, kScanSmem, stream>>>(tp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     for (int k = 1; k < nseg; ++k) {
-        gdn_tp_combine<IO><<<dim3((unsigned)(tp.num_seqs * tp.h_v), 16), 256, 0, stream>>>(tp, sk, k);
+        gdn_tp_combine<IO><<<dim3((unsigned)(tp.num_seqs * tp.h_v), 16), 256, 0, stream>>>(tp, k);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-
-    std::lock_guard<std::mutex> lock(bl->mu);
-    if (cublasSetStream(bl->h, stream) != CUBLAS_STATUS_SUCCESS ||
-        cublasSetWorkspace(bl->h, extra + L.blas, kBlasWorkspace) != CUBLAS_STATUS_SUCCESS)
-        return cudaErrorUnknown;
-    const cudaDataType_t dt = std::is_same<IO, __nv_bfloat16>::value ? CUDA_R_16BF : CUDA_R_16F;
-    const float one = 1.f;
-    const int64_t row = (int64_t)tp.h_v * kDK;            // elements between tokens
-    const size_t slab = (size_t)tp.num_seqs * tp.h_v * kDK * kDK;
-    for (int64_t n = 0; n < tp.num_seqs; ++n)
-        for (int k = 1; k < nseg; ++k) {
-            const int64_t tb = (int64_t)k * tp.tp_seg * kC;
-            if (tb >= tp.seqlen) break;
-            const int64_t cnt = (tp.seqlen - tb) < (int64_t)tp.tp_seg * kC ? (tp.seqlen - tb)
-                                                                           : (int64_t)tp.tp_seg * kC;
-            const size_t tok = (size_t)(n * tp.seqlen + tb);
-            // Column-major view: o^T (128 x cnt) += S_k^T (128 x 128) R^T (128 x cnt), per head.
-            const IO *A = sk + k * slab + (size_t)n * tp.h_v * kDK * kDK;
-            const IO *B = static_cast<const IO *>(tp.tp_r) + tok * row;
-            IO *C = static_cast<IO *>(tp.o) + tok * row;
-            if (cublasGemmStridedBatchedEx(bl->h, CUBLAS_OP_N, CUBLAS_OP_N, kDK, (int)cnt, kDK, &one,
-                                           A, dt, kDK, (long long)kDK * kDK, B, dt, (int)row, kDK,
-                                           &one, C, dt, (int)row, kDK, tp.h_v, CUBLAS_COMPUTE_32F,
-                                           CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-                return cudaErrorUnknown;
-        }
-    return cudaSuccess;
+    const unsigned tiles = (unsigned)((tp.tp_seg + 1) / 2);
+    gdn_tp_correct<IO><<<dim3((unsigned)(tp.num_seqs * tp.h_v), (unsigned)(nseg - 1) * tiles), kCorrThreads,
+                         kCorrSmem, stream>>>(tp);
+    return cudaGetLastError();
 }
 
 }  // namespace
+
+long long g_wait_budget = 0;   // 0: the kernels' default budget
 
 size_t prefill_tc_tp_bytes(bool varlen, int64_t seqlen, int64_t batch, int h_v) {
     const int nseg = tp_segments(varlen, seqlen, batch, h_v);
@@ -1543,6 +1672,7 @@ cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_t
     tp.h_qk = p.h_qk; tp.h_v = p.h_v; tp.scale = p.scale; tp.status = p.status;
     tp.chunks_per_seq = (int32_t)((p.seqlen + kC - 1) / kC);
     tp.ws = static_cast<uint8_t *>(workspace);
+    tp.wait_budget = __atomic_load_n(&g_wait_budget, __ATOMIC_RELAXED);
     const bool varlen = p.cu_seqlens != nullptr;
     const int64_t n_slots = chunk_slots(varlen, p.seqlen, p.num_seqs, p.num_seqs);
     // The time-parallel scan, when the shape suits it, the caller allows internal
@@ -1550,15 +1680,11 @@ cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_t
     const size_t records = prefill_tc_workspace(varlen, p.seqlen, p.num_seqs, p.num_seqs, p.h_v);
     const int tps = allow_overlap ? tp_segments(varlen, p.seqlen, p.num_seqs, p.h_v) : 1;
     if (tps > 1 && workspace_bytes >= records + tp_layout(p.seqlen, p.num_seqs, p.h_v, tps).total) {
-        Blas *bl = blas();
-        if (bl != nullptr) {
-            uint8_t *extra = static_cast<uint8_t *>(workspace) + records;
-            if (!make_map(&tp.tm_r, extra + tp_layout(p.seqlen, p.num_seqs, p.h_v, tps).r, io, p.h_v,
-                          total_tokens))
-                return cudaErrorInvalidValue;
-            if (io == GDN_BF16) return launch_tp<__nv_bfloat16>(tp, n_slots, tps, extra, bl, stream);
-            return launch_tp<__half>(tp, n_slots, tps, extra, bl, stream);
-        }
+        uint8_t *extra = static_cast<uint8_t *>(workspace) + records;
+        if (!make_map(&tp.tm_r, extra + tp_layout(p.seqlen, p.num_seqs, p.h_v, tps).r, io, p.h_v, total_tokens))
+            return cudaErrorInvalidValue;
+        if (io == GDN_BF16) return launch_tp<__nv_bfloat16>(tp, n_slots, tps, extra, stream);
+        return launch_tp<__half>(tp, n_slots, tps, extra, stream);
     }
     const int nseg = allow_overlap ? prefill_tc_segments(varlen, p.seqlen, p.num_seqs, p.h_v) : 1;
     if (io == GDN_BF16) return launch_typed<__nv_bfloat16>(tp, n_slots, nseg, stream);

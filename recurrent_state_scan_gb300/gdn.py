@@ -27,7 +27,7 @@ EXPORTS = ("gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode_step",
            "gdn_prefill_plan", "gdn_last_device_status", "gdn_status_string",
            "gdn_last_error_message", "gdn_prefill_noalloc", "gdn_decode_step_slots",
            "gdn_scan_window", "gdn_scan_variant", "gdn_causal_conv", "gdn_causal_conv_slots",
-           "gdn_gated_rmsnorm")
+           "gdn_gated_rmsnorm", "gdn_set_wait_budget")
 PATH_SIMT, PATH_TC, PATH_TC_TP = 1, 2, 3
 # gdn_rule codes.
 RULES = {"gated_delta": 0, "delta": 1, "gated": 2, "linear": 3}
@@ -115,6 +115,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.gdn_status_string.argtypes = [ctypes.c_int]
     lib.gdn_last_error_message.restype = ctypes.c_char_p
     lib.gdn_last_error_message.argtypes = []
+    lib.gdn_set_wait_budget.restype = ctypes.c_int
+    lib.gdn_set_wait_budget.argtypes = [ctypes.c_int64]
     _lib = lib
     return lib
 
@@ -296,6 +298,12 @@ def _simt_only(spec) -> bool:
     gate variants of gdn_scan_variant."""
     return bool(spec.decode or getattr(spec, "window", 0) or getattr(spec, "decay_per_key", False)
                 or getattr(spec, "beta_shared", False))
+
+
+def gdn_set_wait_budget(cycles: int) -> None:
+    """Test hook: cycles a bounded wait of the tensor-core prefill kernels may take before
+    the CTA gives up (0: the default, about two seconds)."""
+    _check(load().gdn_set_wait_budget(int(cycles)))
 
 
 def launches_per_call(spec, n_seq: int = 0, total_tokens: int = 0) -> int:

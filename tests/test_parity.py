@@ -219,14 +219,14 @@ def test_bad_device_cu_seqlens_sets_check_word():
 def test_prefill_time_parallel_with_ragged_tail():
     """A batched call with a small scan grid and 65 chunks runs the time-parallel scan: four
     segments of 17 chunks (the last one 14, its last chunk ragged), each scanned from zero
-    beside its operator pass, then combined; against the oracle, with an initial state.
-    The plan reports prep, scan and three combine steps."""
+    beside its operator pass, then combined and corrected; against the oracle, with an
+    initial state.  The plan reports prep, scan, three combine steps and the correction."""
     from recurrent_state_scan_gb300 import gdn
     spec = workloads.small_spec(io="bf16", batch=1, seqlen=4100, h_qk=2, h_v=4, seed=61,
                                 state_std=0.05)
     inp = workloads.draw(spec)
     path, launches = gdn.gdn_prefill_plan(gdn.shape_of_spec(spec, inp.n_seq, inp.total_tokens))
-    assert path == gdn.PATH_TC_TP and launches == 5
+    assert path == gdn.PATH_TC_TP and launches == 6
     o_ref, s_ref = oracle.scan_inputs(inp, threads=4)
     o, s = run_prefill(inp)
     check(inp, o, s, o_ref, s_ref, what="time-parallel scan")
@@ -257,3 +257,25 @@ def test_prefill_time_segments_with_a_records_only_workspace():
     o_ref, s_ref = oracle.scan_inputs(inp, threads=4)
     o, s = run_prefill(inp, workspace=ws)
     check(inp, o, s, o_ref, s_ref, what="overlapped segments")
+
+
+def test_time_parallel_error_next_to_the_sequential_chain():
+    """On the 4096-token bf16 prefill the time-parallel path (segments scanned at once, then
+    o += R S_k with S_k in fp32) and the sequential chain over the chunk records (a
+    records-only workspace) are both compared with the oracle; the time-parallel path may
+    not lose more than a third of a bf16 rounding step on top of the chain's error."""
+    import os
+    from recurrent_state_scan_gb300 import gdn
+    inp = workloads.workload("bf16_prefill_t4096")
+    shape = gdn.shape_of_spec(inp.spec, inp.n_seq, inp.total_tokens)
+    assert gdn.gdn_prefill_plan(shape)[0] == gdn.PATH_TC_TP
+    o_ref, s_ref = oracle.scan_inputs(inp, threads=os.cpu_count() or 1)
+    o_tp, s_tp = run_prefill(inp)
+    records = ((4096 // 64) + 1 + 1) * 16 * 82944
+    o_ch, s_ch = run_prefill(inp, workspace=torch.empty(records, dtype=torch.uint8, device="cuda"))
+    e_tp = (rel_err(o_tp, o_ref), rel_err(s_tp, s_ref))
+    e_ch = (rel_err(o_ch, o_ref), rel_err(s_ch, s_ref))
+    print(f"time-parallel: o {e_tp[0]:.3e} state {e_tp[1]:.3e}; sequential chain: o {e_ch[0]:.3e} "
+          f"state {e_ch[1]:.3e}")
+    assert max(e_tp + e_ch) <= TOL["bf16"]
+    assert e_tp[0] <= e_ch[0] + 2 ** -9 / 3 and e_tp[1] <= e_ch[1] + 2 ** -9 / 3
