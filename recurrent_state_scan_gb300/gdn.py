@@ -9,7 +9,6 @@ loaded every call raises -- there is no CPU or PyTorch fallback.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 from typing import Optional
 
@@ -327,10 +326,6 @@ def gdn_last_device_status(stream=None) -> int:
 
 def gdn_status_string(status: int) -> str:
     return load().gdn_status_string(int(status)).decode()
-
-
-def default_scale(d_k: int) -> float:
-    return 1.0 / math.sqrt(d_k)
 
 
 def gdn_decode_step_slots(q, k, v, a, b, A_log, dt_bias, pool, slots, scale: float = 0.0, *,
