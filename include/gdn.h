@@ -126,7 +126,7 @@ typedef struct gdn_shape {
  * the correction, from the identity with the values zeroed), then combined; a last
  * kernel adds the correction o += R S_k of each later segment on the tensor cores,
  * with S_k taken in fp32.  That needs the full gdn_prefill_workspace_bytes(shape); a
- * workspace that holds only the chunk records (81 KiB per chunk and value head)
+ * workspace that holds only the chunk records (65 KiB per chunk and value head)
  * instead splits the call into chunk segments whose preparation runs on a stream
  * internal to the library (one per device, created on first use) beside the scan of
  * the earlier one.  Either way the work is ordered after what `stream` held at the
@@ -154,11 +154,11 @@ gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, con
  * allocates nothing and frees nothing.  It runs the records-only path (no
  * time-parallel scan, no internal stream), so it needs the chunk records alone: a
  * shape needing more than that size returns GDN_ERR_INVALID_ARG and launches
- * nothing.  A record covers one (64-token chunk, value head) and takes 82,944 bytes, so
- * 96 MiB holds 1,213 records.  The count is read the way the call itself runs: a batched
+ * nothing.  A record covers one (64-token chunk, value head) and takes 66,560 bytes, so
+ * 96 MiB holds 1,512 records.  The count is read the way the call itself runs: a batched
  * call (cu_seqlens NULL) needs batch * ceil(seqlen / 64) * h_v records, a packed call
  * (cu_seqlens given) (floor(seqlen / 64) + num_seqs + 1) * h_v.  One batched sequence of
- * up to 4,800 tokens at 16 value heads fits (75 x 16 = 1,200 records); 4,801 does not.
+ * up to 6,016 tokens at 16 value heads fits (94 x 16 = 1,504 records); 6,017 does not.
  * Shapes off the tensor-core path need no scratch and run as in gdn_prefill.
  *
  * All calls on a device share the one array.  Each call writes every scratch

@@ -12,17 +12,19 @@
 // re-association of the same sums, exact up to rounding.
 //
 // Two kernels, stream-ordered:
-//  * gdn_chunk_prep -- one CTA per (chunk, value head), all in parallel: everything that
-//    does not depend on the state.  Gates and their prefix sums, D1 = [K; Q] K^T
-//    (tcgen05), A and P, T = (I + A)^-1 (fp32 diagonal blocks, tf32 warp-MMA merges),
-//    D2 = [T'; T''] K -> W and D3 = [T'; T''] V -> U (tcgen05), Q~ = diag(scale gamma) Q.
-//    It writes one workspace record per (chunk, head): shared-memory images of [Q~; W],
-//    U, P and the gate values, laid out exactly as the scan loads them.
+//  * gdn_chunk_prep -- one CTA per (chunk, value head), all in parallel, three CTAs to an
+//    SM: everything that does not depend on the state.  Gates and their prefix sums,
+//    D1 = [K; Q] K^T (tcgen05), A and P, T = (I + A)^-1 (fp32 diagonal blocks, tf32
+//    warp-MMA merges), D2 = [T'; T''] K -> W and D3 = [T'; T''] V -> U (tcgen05), and
+//    for the scan's lookahead W' = gamma_C(prev) W and M = W K_prev^T diag(e^{G_C - G}).
+//    It writes one workspace record per (chunk, head): images of W', [P; M], U and the
+//    gate values, laid out exactly as the scan loads them.
 //  * gdn_chunk_scan -- one CTA per (sequence, value head, half of the 128 state columns),
-//    walking the sequence's chunks in order: D4 = [Q~; W] S0 (tcgen05),
-//    Delta = U - W S0, DS = K^T diag(e^{G_C-G}) Delta and D4 += [P; .] Delta (tcgen05),
-//    S = gamma_C S0 + DS with S in fp32 registers, o by TMA store.  Records and K arrive
-//    by bulk copy / TMA into two stages, one chunk ahead.
+//    walking the sequence's chunks in order: D4 = [Q; W'] S0 (tcgen05),
+//    Delta = U - W S0, DS = K^T diag(e^{G_C-G}) Delta and X = [P; M] Delta (tcgen05),
+//    S = gamma_C S0 + DS with S in fp32 registers, o = scale gamma (Q S0) + P Delta by
+//    TMA store.  Records, Q and K arrive by bulk copy / TMA into two stages, one chunk
+//    ahead.
 // Columns of S evolve independently (the page's "Parallelization" note), so a column
 // half needs only its half of U and Delta.  All MMAs use M = 128, so accumulator row r
 // is TMEM lane r.  Rows past the end of a sequence get g = 0 and beta = 0, which makes
@@ -50,12 +52,12 @@ constexpr int kAs = 68;                // row stride (floats) of the fp32 A / T 
 
 // Workspace record of one (chunk c, value head): shared-memory images for the scan.
 // Rows marked (c + 1) are written by the prep of the next chunk of the same sequence.
-constexpr int REC_QW = 0;              // 2 d_k halves x [Q~_c rows | W'_{c+1} rows], 128 x 128 B each
-constexpr int REC_PM = 32768;          // [P_c rows | M_{c+1} rows], 128 x 128 B
-constexpr int REC_U = 49152;           // U_c: 2 column halves x 64 token rows x 128 B
-constexpr int REC_W0 = 65536;          // W_c, 2 d_k halves x 64 rows (first chunk of a sequence only)
-constexpr int REC_G = 81920;           // GateRec
-constexpr int kRecord = 82944;
+constexpr int REC_W = 0;               // W_{c+1}: 2 d_k halves x 64 rows x 128 B
+constexpr int REC_PM = 16384;          // [P_c rows | M_{c+1} rows], 128 x 128 B
+constexpr int REC_U = 32768;           // U_c: 2 column halves x 64 token rows x 128 B
+constexpr int REC_W0 = 49152;          // W_c, 2 d_k halves x 64 rows (first chunk of a segment only)
+constexpr int REC_G = 65536;           // GateRec
+constexpr int kRecord = 66560;
 
 struct __align__(16) GateRec {
     float gam[kC];      // e^{G_i}
@@ -199,13 +201,13 @@ __device__ __forceinline__ void block_store(const Blk &d, const float (&acc)[2][
 //  2. 16 -> 32: T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22 (one warp each).
 //  3. 32 -> 64: Y = A_[23][01] T_[01][01], then T_[23][01] = -T_[23][23] Y, one 16x16
 //     block per warp.
-// Blocks below the diagonal use tf32 warp MMAs; each is also kept transposed in the
-// unused upper block of As (T_ij at As[16 j + c][16 i + r]), so A below the diagonal
-// is never overwritten while it is still read.
-// `side(t, n)` runs on the other 192 threads (t = 0 .. 191 of n = 192) during step 1.
-template <typename IO, typename Side>
-__device__ void invert_chunk(float *As, float (*X)[16][20], uint8_t *tt, const float *beta,
-                             const float *gam, int pt, Side &&side) {
+// Blocks below the diagonal use tf32 warp MMAs.  A is strictly lower, so the blocks of
+// As above the diagonal are free: step 2 keeps T_10 and T_32 there transposed (T_ij at
+// As[16 j + c][16 i + r]), so A below the diagonal is never overwritten while it is still
+// read, and the four other upper blocks hold the intermediate products.  Step 3's blocks
+// go only to the operand tile: nothing reads them in fp32 again.
+template <typename IO>
+__device__ void invert_chunk(float *As, uint8_t *tt, const float *beta, const float *gam, int pt) {
     if (pt < 64) {
         // Column-oriented: once x_l is known it updates every later row's sum, so the
         // serial chain is one FMA per row instead of a whole dot product.
@@ -226,18 +228,19 @@ __device__ void invert_chunk(float *As, float (*X)[16][20], uint8_t *tt, const f
             As[(o + i) * kAs + cj] = x[i];
             tt_put<IO>(tt, o + i, cj, x[i], f1, f2);
         }
-    } else {
-        side(pt - 64, kPrepThreads - 64);
     }
-    if (pt == 0) bulk_wait_read();   // X below reuses the staging tile of the P store
     named_bar(kBarPrep, kPrepThreads);
     const int w = pt >> 5, lane = pt & 31, g = lane >> 2, t = lane & 3;
     auto diag = [&](int b) { return Blk{As + 16 * b * kAs + 16 * b, kAs, 1}; };
     auto low = [&](int i, int j) { return Blk{As + 16 * i * kAs + 16 * j, kAs, 1}; };  // A_ij
     auto tlo = [&](int i, int j) { return Blk{As + 16 * j * kAs + 16 * i, 1, kAs}; };  // T_ij
-    auto scratch = [&](int k) { return Blk{&X[k][0][0], 20, 1}; };
-    auto emit = [&](int i, int j, const float (&acc)[2][4]) {   // T_ij = -acc
-        block_store(tlo(i, j), acc, -1.f, g, t);
+    // Intermediate k in upper block (0, 2), (1, 3), (0, 3) or (1, 2).
+    auto scratch = [&](int k) {
+        const int rb = (k == 1 || k == 3) ? 1 : 0, cb = (k == 0 || k == 3) ? 2 : 3;
+        return Blk{As + 16 * rb * kAs + 16 * cb, kAs, 1};
+    };
+    auto emit = [&](int i, int j, const float (&acc)[2][4], bool keep) {   // T_ij = -acc
+        if (keep) block_store(tlo(i, j), acc, -1.f, g, t);
 #pragma unroll
         for (int nh = 0; nh < 2; ++nh) {
             const int c = 16 * j + 8 * nh + 2 * t, r = 16 * i + g;
@@ -253,7 +256,7 @@ __device__ void invert_chunk(float *As, float (*X)[16][20], uint8_t *tt, const f
         __syncwarp();
         float res[2][4] = {};
         block_mma(res, diag(hi), scratch(w), g, t);
-        emit(hi, lo, res);
+        emit(hi, lo, res, true);
     }
     named_bar(kBarPrep, kPrepThreads);
     const int bi = 2 + (w >> 1), bj = w & 1;        // this warp's block of T_[23][01]
@@ -276,30 +279,32 @@ __device__ void invert_chunk(float *As, float (*X)[16][20], uint8_t *tt, const f
             block_mma(res, tlo(3, 2), scratch(bj), g, t);
             block_mma(res, diag(3), scratch(2 + bj), g, t);
         }
-        emit(bi, bj, res);
+        emit(bi, bj, res, false);
     }
 }
 
 // ===================================================================== chunk prep
-// Shared memory (from a 1024-aligned base).
-constexpr int kRegion = 24576;                 // 192 rows x 128 B: K | Q | W for 64 d_k
-constexpr int PP_KQW = 0;                      // two regions
-constexpr int PP_V = 2 * kRegion;              // V, 2 x 64 x 128 B; later the U image
-constexpr int PP_PS = PP_V + 16384;            // P image; later the merges' scratch, then M
-constexpr int PP_TT = PP_PS + 8192;            // [T'; T''], 128 x 128 B
-constexpr int PP_AS = PP_TT + 16384;           // A, then T, fp32 [64][68]
+// Shared memory (from a 1024-aligned base): 66 KB, so that three CTAs share an SM.  The
+// record's pieces go to global memory straight from registers.
+constexpr int kRegP = 16384;                   // 128 rows x 128 B for 64 d_k: [K; Q]
+constexpr int PP_KQ = 0;                       // two regions; V lands over Q, W over K
+constexpr int PP_TT = 2 * kRegP;               // [T'; T''], 128 x 128 B
+constexpr int PP_AS = PP_TT + 16384;           // A, then T, fp32 [64][68]; later K_{c-1}
 constexpr int kPrepSmem = PP_AS + 64 * kAs * 4 + 1024;
+constexpr uint32_t kPrepCols = 128;            // TMEM columns of a prep CTA
 
 struct PrepCtl {
-    uint64_t full, d1, d23, kprev, dm;
+    uint64_t full, vfull, d1, d2, d3, kprev, dm;
     uint32_t tmem;
-    float G[kC], beta[kC], E[kC], F[kC], wsum[2];
-    float kfp[kC], wsum_p[2], gam_p;   // previous chunk: e^{G_C - G_j}, e^{G_C}
-    GateRec gr;
+    float G[kC], beta[kC], gam[kC], E[kC], F[kC], wsum[2];
+    float kfp[kC], wsum_p[2];          // previous chunk: e^{G_C - G_j}
 };
 
+// One CTA per (chunk, value head).  TMEM (128 columns) holds one product at a time:
+// D1 = [K; Q] K^T, then D2 = [T'; T''] K (W on lanes 0-63), D3 = [T'; T''] V (U on lanes
+// 64-127) and M = W K_{c-1}^T, each read out before the next is issued.
 template <typename IO>
-__global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_constant__ TcParams p) {
     constexpr bool kBf16 = std::is_same<IO, __nv_bfloat16>::value;
     constexpr uint32_t kIdD1 = idesc_f16(kBf16, 128, 64, false, false);
     constexpr uint32_t kIdD2 = idesc_f16(kBf16, 128, 128, false, true);
@@ -341,20 +346,23 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
     const int64_t tc0 = t0 + c * kC;
     const int Lc = (int)((t1 - tc0) < kC ? (t1 - tc0) : kC);
     uint8_t *rec = p.ws + ((size_t)slot * p.h_v + h) * kRecord;
+    uint8_t *const rec_prev = rec - (size_t)p.h_v * kRecord;   // chunk c - 1, same head
     // A segment's first chunk writes W for the scan to start from; every other chunk
     // writes W' and M into its predecessor's record.
     const bool first = (c == p.seg_begin) || (p.tp_seg > 0 && c % p.tp_seg == 0);
 
     float *const As = reinterpret_cast<float *>(sm + PP_AS);
-    const uint32_t aKQW = smem_u32(sm + PP_KQW), aTT = smem_u32(sm + PP_TT), aV = smem_u32(sm + PP_V);
+    const uint32_t aKQ = smem_u32(sm + PP_KQ), aTT = smem_u32(sm + PP_TT);
     if (warp == 0) {
-        tmem_alloc(&ctl.tmem, 256);
+        tmem_alloc(&ctl.tmem, kPrepCols);
         tmem_relinquish();
     }
     if (pt == 0) {
         mbar_init(&ctl.full, 1);
+        mbar_init(&ctl.vfull, 1);
         mbar_init(&ctl.d1, 1);
-        mbar_init(&ctl.d23, 1);
+        mbar_init(&ctl.d2, 1);
+        mbar_init(&ctl.d3, 1);
         mbar_init(&ctl.kprev, 1);
         mbar_init(&ctl.dm, 1);
         fence_mbar_init();
@@ -369,19 +377,19 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
     const uint32_t tmem = ctl.tmem;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
 
-    uint32_t issued = 0;        // thread 0: 2 = D1, 4 = D2/D3, 8 = K_{c-1} load, 16 = M MMA
+    // thread 0: 1 = V load, 2 = D1, 4 = D2, 8 = K_{c-1} load, 16 = M, 32 = D3
+    uint32_t issued = 0;
+    const int tok = (int)tc0;
     if (pt == 0) {
-        const int tok = (int)tc0;
-        mbar_arrive_expect_tx(&ctl.full, 2 * 2 * 8192 + 2 * 8192);
+        mbar_arrive_expect_tx(&ctl.full, 4 * 8192);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-            tma_load_3d(sm + PP_KQW + r * kRegion, &p.tm_k, r * 64, hq, tok, &ctl.full);
-            tma_load_3d(sm + PP_KQW + r * kRegion + 8192, &p.tm_q, r * 64, hq, tok, &ctl.full);
-            tma_load_3d(sm + PP_V + r * 8192, &p.tm_v, r * 64, h, tok, &ctl.full);
+            tma_load_3d(sm + PP_KQ + r * kRegP, &p.tm_k, r * 64, hq, tok, &ctl.full);
+            tma_load_3d(sm + PP_KQ + r * kRegP + 8192, &p.tm_q, r * 64, hq, tok, &ctl.full);
         }
     }
     // The gates (this chunk's and, for W' and M, the previous chunk's decay) are computed
-    // from plain loads of the logits while K, Q and V are in flight.
+    // from plain loads of the logits while K and Q are in flight.
     float ra = 0.f, rb = 0.f, rap = 0.f;
     if (pt < Lc) {
         ra = IoType<IO>::ld(static_cast<const IO *>(p.a) + (size_t)(tc0 + pt) * p.h_v + h);
@@ -418,43 +426,51 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
             ctl.beta[pt] = be;
             // Previous chunk: e^{G_C - G_j} = e^{(sum of its g) - G_j}.
             const float gp = gsum_p + (warp == 1 ? ctl.wsum_p[0] : 0.f);
-            const float gpc = ctl.wsum_p[0] + ctl.wsum_p[1];
-            ctl.kfp[pt] = __expf(gpc - gp);
-            if (pt == 0) ctl.gam_p = __expf(gpc);
+            ctl.kfp[pt] = __expf(ctl.wsum_p[0] + ctl.wsum_p[1] - gp);
         }
         named_bar(kBarPrep, kPrepThreads);
         const float GC = ctl.G[kC - 1], Gm = ctl.G[31];
         if (pt < kC) {
             const float G = ctl.G[pt];
-            ctl.gr.gam[pt] = __expf(G);
-            ctl.gr.kf[pt] = __expf(GC - G);
+            const float gm = __expf(G);
+            GateRec *grec = reinterpret_cast<GateRec *>(rec + REC_G);
+            ctl.gam[pt] = gm;
+            grec->gam[pt] = gm;
+            grec->kf[pt] = __expf(GC - G);
             ctl.E[pt] = __expf(G - Gm);
             ctl.F[pt] = __expf(Gm - G);
-            if (pt == 0) ctl.gr.gC = __expf(GC);
+            if (pt == 0) grec->gC = __expf(GC);
         }
     }
-    // D1 = [K; Q] K^T once K and Q have landed.
+    // D1 = [K; Q] K^T once K and Q have landed; then V over the Q rows, which D1 has read.
     if (pt == 0) {
         ok = mbar_wait(&ctl.full, 0, budget);
         if (ok) {
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const uint32_t off = (k >> 2) * kRegion + (k & 3) * 32;
-                mma_f16(tmem, sw128_desc(aKQW + off, 16, 1024), sw128_desc(aKQW + off, 16, 1024), kIdD1,
+                const uint32_t off = (k >> 2) * kRegP + (k & 3) * 32;
+                mma_f16(tmem, sw128_desc(aKQ + off, 16, 1024), sw128_desc(aKQ + off, 16, 1024), kIdD1,
                         k > 0);
             }
             mma_commit(&ctl.d1);
             issued |= 2;
             ok = mbar_wait(&ctl.d1, 0, budget);
         }
+        if (ok) {
+            mbar_arrive_expect_tx(&ctl.vfull, 2 * 8192);
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+                tma_load_3d(sm + PP_KQ + r * kRegP + 8192, &p.tm_v, r * 64, h, tok, &ctl.vfull);
+            issued |= 1;
+        }
     }
     failed = bar_any(kBarPrep, kPrepThreads, !ok);   // also publishes E, F, gamma
-    if (!failed) ok = mbar_wait(&ctl.full, 0, budget);   // every reader of Q and V
+    if (!failed) ok = mbar_wait(&ctl.full, 0, budget);   // K, written by TMA, is rewritten below
     if (!failed) {
         tc_fence_after();
-        // A rows (lanes 0-63, fp32) and P rows (lanes 64-127, I/O type); each column half
-        // of the warps takes 32 of the 64 columns.
+        // A rows (lanes 0-63, fp32, to As) and P rows (lanes 64-127, I/O type, to the
+        // record); each column half of the warps takes 32 of the 64 columns.
         {
             uint32_t r[32];
             tmem_ld32(tmem + lane_base + 32 * hf, r);
@@ -478,143 +494,148 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
                         make_float4(x[0], x[1], x[2], x[3]);
                 }
             } else {
+                // Two 16-byte chunks of a row at a time: logical chunks 2m and 2m + 1 sit
+                // side by side in the 128-byte swizzle, swapped on odd rows.
 #pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
-                    float x[8];
+                for (int m = 0; m < 2; ++m) {
+                    uint4 u[2];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int j = 32 * hf + 8 * q8 + e;
-                        const float d = safe ? Ei * ctl.F[j] : __expf(Gi - ctl.G[j]);
-                        x[e] = (j <= i) ? p.scale * d * __uint_as_float(r[8 * q8 + e]) : 0.f;
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int q8 = 2 * m + h2;
+                        float x[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int j = 32 * hf + 8 * q8 + e;
+                            const float d = safe ? Ei * ctl.F[j] : __expf(Gi - ctl.G[j]);
+                            x[e] = (j <= i) ? p.scale * d * __uint_as_float(r[8 * q8 + e]) : 0.f;
+                        }
+                        u[h2] = pack8<IO>(x);
                     }
-                    *reinterpret_cast<uint4 *>(sm + PP_PS + sw128_offset(i, 4 * hf + q8)) = pack8<IO>(x);
+                    uint8_t *dst = rec + REC_PM + sw128_offset(i, (4 * hf + 2 * m) & ~1);
+                    if (i & 1) st_global_v8(dst - 16, u[1], u[0]);   // chunk pair starts at the odd slot - 1
+                    else st_global_v8(dst, u[0], u[1]);
                 }
             }
         }
-        fence_async_smem();
+        tc_fence_before();
         named_bar(kBarPrep, kPrepThreads);
-        if (pt == 0) {
-            bulk_store(rec + REC_PM, sm + PP_PS, 8192);
-            bulk_commit();
-        }
 
-        // T = (I + A)^-1, written as [T diag(beta gamma); T diag(beta)] (K-major); its
-        // merges reuse the P staging tile once the store above has read it.  Meanwhile
-        // the threads outside its first step scale Q in place (D1 has read it):
-        // Q~ = diag(scale gamma) Q.
-        auto scale_q = [&](int t, int nt) {
-            for (int e = t; e < 1024; e += nt) {
-                const int r = e >> 9, row = (e >> 3) & 63, ch = e & 7;
-                uint8_t *ptr = sm + PP_KQW + r * kRegion + 8192 + sw128_offset(row, ch);
-                const uint4 u = *reinterpret_cast<const uint4 *>(ptr);
-                const float f = p.scale * ctl.gr.gam[row];
-                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-                float x[8];
-#pragma unroll
-                for (int k2 = 0; k2 < 4; ++k2) {
-                    const float2 t2 = Pack<IO>::unpack(w[k2]);
-                    x[2 * k2] = t2.x * f;
-                    x[2 * k2 + 1] = t2.y * f;
-                }
-                *reinterpret_cast<uint4 *>(ptr) = pack8<IO>(x);
-            }
-        };
-        invert_chunk<IO>(As, reinterpret_cast<float (*)[16][20]>(sm + PP_PS), sm + PP_TT, ctl.beta,
-                         ctl.gr.gam, pt, scale_q);
+        // T = (I + A)^-1, written as [T diag(beta gamma); T diag(beta)] (K-major).
+        invert_chunk<IO>(As, sm + PP_TT, ctl.beta, ctl.gam, pt);
         fence_async_smem();
         tc_fence_before();
         named_bar(kBarPrep, kPrepThreads);
-        // The previous chunk's keys (for M) into the spent A/T tile; they land during D2/D3.
-        if (pt == 0 && !first) {
-            mbar_arrive_expect_tx(&ctl.kprev, 2 * 8192);
-#pragma unroll
-            for (int r = 0; r < 2; ++r)
-                tma_load_3d(sm + PP_AS + r * 8192, &p.tm_k, r * 64, hq, (int)(tc0 - kC), &ctl.kprev);
-            issued |= 8;
-        }
-
-        // D2 = [T'; T''] K -> columns 0-127 (W on lanes 0-63), D3 = [T'; T''] V ->
-        // columns 128-255 (U on lanes 64-127).
         if (pt == 0) {
+            // The previous chunk's keys (for M) into the spent A/T tile.
+            if (!first) {
+                mbar_arrive_expect_tx(&ctl.kprev, 2 * 8192);
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+                    tma_load_3d(sm + PP_AS + r * 8192, &p.tm_k, r * 64, hq, tok - kC, &ctl.kprev);
+                issued |= 8;
+            }
+            // D2 = [T'; T''] K: W on lanes 0-63.
             tc_fence_after();
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint64_t da = sw128_desc(aTT + k * 32, 16, 1024);
-                mma_f16(tmem, da, sw128_desc(aKQW + k * 2048, kRegion, 1024), kIdD2, k > 0);
-                mma_f16(tmem + 128, da, sw128_desc(aV + k * 2048, 8192, 1024), kIdD2, k > 0);
-            }
-            mma_commit(&ctl.d23);
+            for (int k = 0; k < 4; ++k)
+                mma_f16(tmem, sw128_desc(aTT + k * 32, 16, 1024), sw128_desc(aKQ + k * 2048, kRegP, 1024),
+                        kIdD2, k > 0);
+            mma_commit(&ctl.d2);
             issued |= 4;
+            ok = mbar_wait(&ctl.d2, 0, budget);
         }
-        ok = mbar_wait(&ctl.d23, 0, budget);
         failed = bar_any(kBarPrep, kPrepThreads, !ok);
     }
+    const int row = 32 * q + lane;
     if (!failed) {
+        // W (fp32, lanes 0-63) in the I/O type over the spent K rows: the A operand of M and
+        // the image of the record's W (the previous chunk's W_{c+1}, or W_0 for a segment's
+        // first chunk).
         tc_fence_after();
-        // W rows -> rows 128-191 of the K|Q|W regions; U rows -> the U image (over V).
-        // W' = e^{G_C of chunk c-1} W goes to the spent [T'; T''] tile for the previous
-        // chunk's record.
-        const int row = 32 * q + lane;
-        const float gam_p = ctl.gam_p;
+        if (q < 2) {
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_base + (q < 2 ? 0 : 128) + 64 * hf + c0, r);
-            tmem_ld_wait();
-            float x[32];
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + 64 * hf + c0, r);
+                tmem_ld_wait();
+                float x[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
-            uint8_t *base = (q < 2) ? sm + PP_KQW + hf * kRegion : sm + PP_V + hf * 8192;
-            const int rr = (q < 2) ? 128 + row : row - 64;
-#pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8)
-                *reinterpret_cast<uint4 *>(base + sw128_offset(rr, (c0 >> 3) + q8)) = pack8<IO>(x + 8 * q8);
-            if (q < 2 && !first) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) x[e] *= gam_p;
+                for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
 #pragma unroll
                 for (int q8 = 0; q8 < 4; ++q8)
-                    *reinterpret_cast<uint4 *>(sm + PP_TT + hf * 8192 + sw128_offset(row, (c0 >> 3) + q8)) =
+                    *reinterpret_cast<uint4 *>(sm + PP_KQ + hf * kRegP + sw128_offset(row, (c0 >> 3) + q8)) =
                         pack8<IO>(x + 8 * q8);
             }
         }
         fence_async_smem();
         tc_fence_before();
         named_bar(kBarPrep, kPrepThreads);
-        uint8_t *const rec_prev = rec - (size_t)p.h_v * kRecord;   // chunk c - 1, same head
+        // D3 = [T'; T''] V (U on lanes 64-127) while W goes out.
         if (pt == 0) {
+            uint8_t *dst = first ? rec + REC_W0 : rec_prev + REC_W;
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                bulk_store(rec + REC_QW + r * 16384, sm + PP_KQW + r * kRegion + 8192, 8192);
-                if (first)
-                    bulk_store(rec + REC_W0 + r * 8192, sm + PP_KQW + r * kRegion + 16384, 8192);
-                else
-                    bulk_store(rec_prev + REC_QW + r * 16384 + 8192, sm + PP_TT + r * 8192, 8192);
-            }
-            bulk_store(rec + REC_U, sm + PP_V, 16384);
-            bulk_store(rec + REC_G, &ctl.gr, sizeof(GateRec));
+            for (int r = 0; r < 2; ++r) bulk_store(dst + r * 8192, sm + PP_KQ + r * kRegP, 8192);
             bulk_commit();
-            // M_c = W_c K_{c-1}^T (columns scaled below) into TMEM columns 0-63.
+            ok = mbar_wait(&ctl.vfull, 0, budget);
+            if (ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_f16(tmem, sw128_desc(aTT + k * 32, 16, 1024),
+                            sw128_desc(aKQ + 8192 + k * 2048, kRegP, 1024), kIdD2, k > 0);
+                mma_commit(&ctl.d3);
+                issued |= 32;
+                ok = mbar_wait(&ctl.d3, 0, budget);
+            }
+        }
+        failed = bar_any(kBarPrep, kPrepThreads, !ok);
+    }
+    if (!failed) {
+        // U (lanes 64-127) into the spent [T'; T''] tile, as the record's U image.
+        tc_fence_after();
+        if (q >= 2) {
+            const int j = row - 64;
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + 64 * hf + c0, r);
+                tmem_ld_wait();
+                float x[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8)
+                    *reinterpret_cast<uint4 *>(sm + PP_TT + hf * 8192 + sw128_offset(j, (c0 >> 3) + q8)) =
+                        pack8<IO>(x + 8 * q8);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        named_bar(kBarPrep, kPrepThreads);
+        // U goes out; then M_c = W_c K_{c-1}^T (U has left TMEM: M overwrites its lanes).
+        if (pt == 0) {
+            bulk_store(rec + REC_U, sm + PP_TT, 16384);
+            bulk_commit();
             if (!first) {
                 ok = mbar_wait(&ctl.kprev, 0, budget);
                 if (ok) {
                     tc_fence_after();
-                    const uint32_t aW = smem_u32(sm + PP_KQW + 16384), aKp = smem_u32(sm + PP_AS);
+                    const uint32_t aKp = smem_u32(sm + PP_AS);
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        mma_f16(tmem, sw128_desc(aW + (k >> 2) * kRegion + (k & 3) * 32, 16, 1024),
+                        mma_f16(tmem, sw128_desc(aKQ + (k >> 2) * kRegP + (k & 3) * 32, 16, 1024),
                                 sw128_desc(aKp + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), kIdD1, k > 0);
                     mma_commit(&ctl.dm);
                     issued |= 16;
+                    ok = mbar_wait(&ctl.dm, 0, budget);
                 }
             }
         }
         if (!first) {
-            if (pt == 0) ok = ok && mbar_wait(&ctl.dm, 0, budget);
             failed = bar_any(kBarPrep, kPrepThreads, !ok);
             if (!failed) {
                 // M_c[i][j] = (W_c K_{c-1}^T)[i][j] e^{G_C - G_j} of chunk c - 1, rows on lanes
-                // 0-63, into the P staging tile (the P store read it long ago).
+                // 0-63, staged over the spent V rows for the previous chunk's record.
                 tc_fence_after();
                 if (q < 2) {
                     uint32_t r[32];
@@ -625,12 +646,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
                     for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]) * ctl.kfp[32 * hf + e];
 #pragma unroll
                     for (int q8 = 0; q8 < 4; ++q8)
-                        *reinterpret_cast<uint4 *>(sm + PP_PS + sw128_offset(row, 4 * hf + q8)) = pack8<IO>(x + 8 * q8);
+                        *reinterpret_cast<uint4 *>(sm + PP_KQ + 8192 + sw128_offset(row, 4 * hf + q8)) =
+                            pack8<IO>(x + 8 * q8);
                 }
                 fence_async_smem();
                 named_bar(kBarPrep, kPrepThreads);
                 if (pt == 0) {
-                    bulk_store(rec_prev + REC_PM + 8192, sm + PP_PS, 8192);
+                    bulk_store(rec_prev + REC_PM + 8192, sm + PP_KQ + 8192, 8192);
                     bulk_commit();
                 }
             }
@@ -640,17 +662,19 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
         // Let the copies and MMAs already issued land before the CTA leaves (bounded).
         atomicOr(p.status, kDevTimeout);
         mbar_wait(&ctl.full, 0, kWaitBudget);
+        if (issued & 1) mbar_wait(&ctl.vfull, 0, kWaitBudget);
         if (issued & 2) mbar_wait(&ctl.d1, 0, kWaitBudget);
-        if (issued & 4) mbar_wait(&ctl.d23, 0, kWaitBudget);
+        if (issued & 4) mbar_wait(&ctl.d2, 0, kWaitBudget);
+        if (issued & 32) mbar_wait(&ctl.d3, 0, kWaitBudget);
         if (issued & 8) mbar_wait(&ctl.kprev, 0, kWaitBudget);
         if (issued & 16) mbar_wait(&ctl.dm, 0, kWaitBudget);
     }
-    if (pt == 0) bulk_wait_all();    // the records have reached global memory
+    if (pt == 0) bulk_wait_read();   // the record stores have read their staging tiles
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, kPrepCols);
     }
 }
 
@@ -659,14 +683,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep(const __grid_c
 // the state after chunk c,
 //   W_{c+1} S' = W'_{c+1} S + M_{c+1} Delta,  W'_{c+1} = gamma_C W_{c+1},
 //   M_{c+1} = W_{c+1} K^T diag(e^{G_C - G})   (64 x 64, chunk c's K and gates),
-// so one M = 128 product X(c) = [P_c; M_{c+1}] Delta_c, accumulated onto
-// D4'(c) = [Q~_c; W'_{c+1}] S_c, yields both o_c (rows 0-63) and W_{c+1} S_{c+1}
-// (rows 64-127).  The next Delta waits only for X(c); the state update and D4'(c + 1)
-// run beside it.  The prep of chunk c + 1 writes W'_{c+1} and M_{c+1} into chunk c's
-// record; the first chunk of a sequence starts from W_0 S_0.
+// so one M = 128 product X(c) = [P_c; M_{c+1}] Delta_c beside D4'(c) = [Q_c; W_{c+1}] S_c
+// yields both o_c = scale diag(gamma) (rows 0-63 of D4') + (rows 0-63 of X) and
+// W_{c+1} S_{c+1} = gamma_C (rows 64-127 of D4') + (rows 64-127 of X).  The next Delta waits only
+// for X(c); the state update and D4'(c + 1) run beside it.  The prep of chunk c + 1
+// writes W'_{c+1} and M_{c+1} into chunk c's record; the first chunk of a segment starts
+// from W_0 S_0.
 //
 // Shared memory (from a 1024-aligned base): two stages, then the chain's own tiles.
-constexpr int SS_KQW = 0;                      // K (TMA) | Q~_c | W'_{c+1}, two d_k regions
+constexpr int kRegion = 24576;                 // 192 rows x 128 B for 64 d_k: K | Q | W
+constexpr int SS_KQW = 0;                      // K_c, Q_c (TMA) | W_{c+1}, two d_k regions
 constexpr int SS_U = 2 * kRegion;              // this column half of U_c, 64 x 128 B
 constexpr int SS_PM = SS_U + 8192;             // [P_c; M_{c+1}], 128 x 128 B
 constexpr int SS_G = SS_PM + 16384;            // GateRec
@@ -676,12 +702,13 @@ constexpr int SS_DB0 = SS_SB + 16384;          // Delta, MN-major (token rows)
 constexpr int SS_DB1 = SS_DB0 + 8192;          // diag(e^{G_C - G}) Delta
 constexpr int SS_OUT = SS_DB1 + 8192;          // output tile staging, two buffers
 constexpr int kScanSmem = SS_OUT + 2 * 8192 + 1024;
-// A stage arrives in two parts with their own barriers: part B ([Q~; W'], read only by
+// A stage arrives in two parts with their own barriers: part B ([Q; W], read only by
 // D4') is refilled as soon as D4' has run; part A (K, U, [P; M], gates) once the chunk's
 // last MMA has run and every thread has read the gates.
 constexpr uint32_t kTxA = 2 * 8192 + 8192 + 16384 + sizeof(GateRec);
 constexpr uint32_t kTxB = 2 * 16384;
-constexpr uint32_t TS_D4 = 0, TS_DS = 128;     // TMEM columns: D4' at 0 / 64 by chunk parity
+// TMEM columns: D4' at 0 / 64 and X at 128 / 192 by chunk parity, DS at 256.
+constexpr uint32_t TS_D4 = 0, TS_X = 128, TS_DS = 256, kScanCols = 512;
 constexpr int kChainWarps = 8;                 // Delta, state update, readout
 constexpr int kScanAllThreads = 32 * kChainWarps + 64;   // + an MMA-issue warp and a copy warp
 constexpr uint32_t kBarOut = 2;                // named barrier of the 128 readout threads
@@ -726,14 +753,15 @@ __device__ __forceinline__ bool warp_wait_or_abort(uint64_t *bar, uint32_t parit
 
 // Scan CTAs: one per (sequence, value head, half of the 128 state columns).  Chunk c, with
 // S_c in registers (fp32) and in SB (I/O type):
-//   D4'(c) = [Q~_c; W'_{c+1}] S_c            issued once SB holds S_c      (commit d4)
-//   Delta_c = U_c - (W_c S_c)                warps on TMEM lanes 64-127, from X(c - 1)
+//   D4'(c) = [Q_c; W_{c+1}] S_c              issued once SB holds S_c      (commit d4)
+//   Delta_c = U_c - (W_c S_c)                warps on TMEM lanes 64-127:
+//                                            gamma_C(c - 1) D4'(c - 1) + X(c - 1)
 //   DS(c) = K_c^T diag(e^{G_C - G}) Delta_c                                 (commit ds)
-//   X(c) = [P_c; M_{c+1}] Delta_c            accumulated onto D4'(c)       (commit x)
+//   X(c) = [P_c; M_{c+1}] Delta_c                                          (commit x)
 //   S_{c+1} = gamma_C S_c + DS(c), SB        all chain warps
-//   o_c = rows 0-63 of D4'(c) + X(c)         warps on lanes 0-63, overlapping chunk c + 1
-// X phases: 0 is W_0 S_0 (into block 1), c + 1 is X(c).  D4' alternates between two TMEM
-// column blocks.  One warp issues every MMA and copy; the chain warps wait only on the
+//   o_c = scale gamma (Q_c S_c) + P_c Delta_c    warps on lanes 0-63, overlapping chunk c + 1
+// X phases: 0 is W_0 S_0 (into D4' block 1), c + 1 is X(c).  D4' and X alternate between
+// two TMEM column blocks each.  One warp issues every MMA and copy; the chain warps wait only on the
 // barriers of the work they consume, and it learns of their progress through arrival
 // counts.
 template <typename IO>
@@ -801,7 +829,7 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
     const int64_t L = t1 - t0;
 
     if (warp == 0) {
-        tmem_alloc(&ctl.tmem, 256);
+        tmem_alloc(&ctl.tmem, kScanCols);
         tmem_relinquish();
     }
     if (tid == 0) {
@@ -822,6 +850,7 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
         ctl.abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_q);
         tma_prefetch_desc(op_pass ? &p.tm_r : &p.tm_o);
     }
     tc_fence_before();
@@ -844,14 +873,17 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
         bulk_load(st + SS_PM, rec + REC_PM, 16384, &ctl.full_a[s]);
         bulk_load(st + SS_G, rec + REC_G, sizeof(GateRec), &ctl.full_a[s]);
     };
-    auto load_b = [&](int c) {   // [Q~_c; W'_{c+1}] of chunk c into stage c & 1
+    auto load_b = [&](int c) {   // [Q_c; W_{c+1}] of chunk c into stage c & 1
         const int s = c & 1;
         uint8_t *st = sm + s * kScanStage;
         const uint8_t *rec = record(c);
         mbar_arrive_expect_tx(&ctl.full_b[s], kTxB);
 #pragma unroll
-        for (int r = 0; r < 2; ++r)
-            bulk_load(st + SS_KQW + r * kRegion + 8192, rec + REC_QW + r * 16384, 16384, &ctl.full_b[s]);
+        for (int r = 0; r < 2; ++r) {
+            tma_load_3d(st + SS_KQW + r * kRegion + 8192, &p.tm_q, r * 64, hq, (int)(t0 + (int64_t)c * kC),
+                        &ctl.full_b[s]);
+            bulk_load(st + SS_KQW + r * kRegion + 16384, rec + REC_W + r * 8192, 8192, &ctl.full_b[s]);
+        }
     };
 
     if (issue_warp) {
@@ -903,13 +935,14 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                     mma_f16(tmem + TS_DS, sw128_desc(aSt + k * 2048, kRegion, 1024),
                             sw128_desc(aDB1 + k * 2048, 8192, 1024), kIdDS, k > 0);
                 mma_commit(&ctl.ds);
-                // X(c) onto D4'(c).  The readout of chunk c - 1 is done, so the readout
-                // warps have seen X phase c and block (c + 1) & 1 is free for D4'(c + 1).
+                // X(c) into block c & 1.  The readout of chunk c - 1 is done, so the readout
+                // warps have seen X phase c, the X block of chunk c - 2 is free, and D4'
+                // block (c + 1) & 1 is free for D4'(c + 1).
                 if (c > 0 && !(ok = wait_or_abort<true>(&ctl.out_done, (c - 1) & 1, abort, budget))) break;
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_f16(tmem + TS_D4 + 64 * s, sw128_desc(aSt + SS_PM + k * 32, 16, 1024),
-                            sw128_desc(aDB0 + k * 2048, 8192, 1024), kIdNV, 1u);
+                    mma_f16(tmem + TS_X + 64 * s, sw128_desc(aSt + SS_PM + k * 32, 16, 1024),
+                            sw128_desc(aDB0 + k * 2048, 8192, 1024), kIdNV, k > 0);
                 mma_commit(&ctl.x);
                 if (c + 1 < nchunks) {
                     // D4'(c + 1) once SB holds S_{c+1} (and the copy warp has seen D4'(c)).
@@ -1015,27 +1048,37 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
         };
         publish_sb(true);
         bool ok = true;
+        float gC_prev = 1.f;   // e^{G_C} of chunk c - 1 (1 before the first: W_0 S_0 is exact)
         for (int c = 0; c < nchunks; ++c) {
             const int s = c & 1;
             const uint8_t *st = sm + s * kScanStage;
             const GateRec &gr = *reinterpret_cast<const GateRec *>(st + SS_G);
-            // Every reader of the stage observes its arrival itself.
+            // Every reader of the stage observes its arrival itself.  The gates are read
+            // here: part A of the stage is refilled once every thread has arrived on sb_ready.
             ok = ok && warp_wait_or_abort(&ctl.full_a[s], (c >> 1) & 1, abort, budget);
             const float gC = ok ? gr.gC : 0.f;
+            const float fo = (ok && out_warp) ? p.scale * gr.gam[row] : 0.f;   // o row scale
 
             if (!out_warp) {
                 // Delta_c = U_c - W_c S_c on lanes 64-127 (token rows), this thread's 32
-                // columns; W_c S_c is in block (c - 1) & 1 after X phase c.
+                // columns; W_c S_c is the sum of blocks (c - 1) & 1 of D4' and X after X
+                // phase c (D4' alone for c = 0: W_0 S_0).
                 ok = ok && warp_wait_or_abort(&ctl.x, c & 1, abort, budget);
                 if (ok) {
                     tc_fence_after();
                     const int j = row - 64;
                     const float kfj = gr.kf[j];
-                    const uint32_t wcol = TS_D4 + 64 * ((c + 1) & 1);
+                    const uint32_t wcol = TS_D4 + 64 * ((c + 1) & 1), xcol = TS_X + 64 * ((c + 1) & 1);
 #pragma unroll
                     for (int ps = 0; ps < 2; ++ps) {
-                        uint32_t ws[16];
+                        uint32_t ws[16], xs[16];
                         tmem_ld16(tmem + lane_base + wcol + 32 * g + 16 * ps, ws);
+                        if (c > 0) {
+                            tmem_ld16(tmem + lane_base + xcol + 32 * g + 16 * ps, xs);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) xs[e] = 0u;   // +0.0f
+                        }
                         float x[16];
 #pragma unroll
                         for (int q8 = 0; q8 < 2; ++q8) {
@@ -1055,7 +1098,7 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                             for (int e = 0; e < 16; ++e) x[e] = 0.f;
                         }
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) x[e] -= __uint_as_float(ws[e]);
+                        for (int e = 0; e < 16; ++e) x[e] -= fmaf(gC_prev, __uint_as_float(ws[e]), __uint_as_float(xs[e]));
 #pragma unroll
                         for (int q8 = 0; q8 < 2; ++q8)
                             *reinterpret_cast<uint4 *>(sm + SS_DB0 + sw128_offset(j, 4 * g + 2 * ps + q8)) =
@@ -1088,12 +1131,14 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                 }
             }
             publish_sb(ok);
+            gC_prev = gC;
             if (!out_warp) {
                 if (!ok) break;
                 continue;
             }
 
-            // o_c = rows 0-63 of block c & 1 after X(c), while chunk c + 1 runs.  A full
+            // o_c = scale gamma (rows 0-63 of D4' block c & 1) + (rows 0-63 of X block
+            // c & 1) after X(c), while chunk c + 1 runs.  A full
             // chunk goes out as one TMA store of the staged 64 x 64 tile; a sequence's
             // ragged last chunk is stored row by row so that no row of the next sequence
             // is touched.  The readout warps leave the loop together, at their barrier.
@@ -1106,12 +1151,13 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                 uint4 packed[4];
 #pragma unroll
                 for (int ps = 0; ps < 2; ++ps) {
-                    uint32_t r[16];
+                    uint32_t r[16], rx[16];
                     tmem_ld16(tmem + lane_base + TS_D4 + 64 * s + 32 * g + 16 * ps, r);
+                    tmem_ld16(tmem + lane_base + TS_X + 64 * s + 32 * g + 16 * ps, rx);
                     tmem_ld_wait();
                     float x[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) x[e] = __uint_as_float(r[e]);
+                    for (int e = 0; e < 16; ++e) x[e] = fmaf(fo, __uint_as_float(r[e]), __uint_as_float(rx[e]));
                     packed[2 * ps] = pack8<IO>(x);
                     packed[2 * ps + 1] = pack8<IO>(x + 8);
                 }
@@ -1158,7 +1204,7 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
     if (tid == 0 && ctl.abort) atomicOr(p.status, kDevTimeout);
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, kScanCols);
     }
 }
 
@@ -1469,6 +1515,10 @@ cudaError_t configure() {
     if (!configured[dev]) {
         e = cudaFuncSetAttribute(gdn_chunk_prep<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kPrepSmem);
+        // Three prep CTAs to an SM need the largest shared-memory carve-out.
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gdn_chunk_prep<IO>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(gdn_chunk_scan<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kScanSmem);

@@ -132,6 +132,12 @@ __device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t 
                  "r"(smem_u32(src)), "r"(bytes)
                  : "memory");
 }
+// 32-byte global store (8 x 32 bits) from registers.
+__device__ __forceinline__ void st_global_v8(void *dst, const uint4 &lo, const uint4 &hi) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(lo.x), "r"(lo.y),
+                 "r"(lo.z), "r"(lo.w), "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until the shared-memory sources of this thread's committed bulk stores are read.
 __device__ __forceinline__ void bulk_wait_read() {

@@ -5,6 +5,10 @@ import torch
 
 TOL = {"f32": 1e-4, "bf16": 2e-2, "f16": 2e-2}
 
+# Bytes of one chunk record (one 64-token chunk and value head) of the tensor-core
+# prefill's workspace, as include/gdn.h states it.
+RECORD_BYTES = 66560
+
 
 def rel_err(gpu, ref) -> float:
     """max |gpu - ref| / max |ref| (the parity metric)."""

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import workloads
-from gpu_util import TOL, check, rel_err, run_prefill, to_device
+from gpu_util import RECORD_BYTES, TOL, check, rel_err, run_prefill, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -247,12 +247,12 @@ def test_prefill_time_parallel_shapes(io, B, T, hqk, hv, state):
 
 
 def test_prefill_time_segments_with_a_records_only_workspace():
-    """Given room for the chunk records only (81 KiB per chunk and value head), the same
+    """Given room for the chunk records only (65 KiB per chunk and value head), the same
     call falls back to the overlapped prep/scan segments, with the same results."""
     spec = workloads.small_spec(io="bf16", batch=1, seqlen=4100, h_qk=2, h_v=4, seed=61,
                                 state_std=0.05)
     inp = workloads.draw(spec)
-    records = ((4100 + 63) // 64) * 4 * 82944
+    records = ((4100 + 63) // 64) * 4 * RECORD_BYTES
     ws = torch.empty(records, dtype=torch.uint8, device="cuda")
     o_ref, s_ref = oracle.scan_inputs(inp, threads=4)
     o, s = run_prefill(inp, workspace=ws)
@@ -271,7 +271,7 @@ def test_time_parallel_error_next_to_the_sequential_chain():
     assert gdn.gdn_prefill_plan(shape)[0] == gdn.PATH_TC_TP
     o_ref, s_ref = oracle.scan_inputs(inp, threads=os.cpu_count() or 1)
     o_tp, s_tp = run_prefill(inp)
-    records = ((4096 // 64) + 1 + 1) * 16 * 82944
+    records = ((4096 // 64) + 1 + 1) * 16 * RECORD_BYTES
     o_ch, s_ch = run_prefill(inp, workspace=torch.empty(records, dtype=torch.uint8, device="cuda"))
     e_tp = (rel_err(o_tp, o_ref), rel_err(s_tp, s_ref))
     e_ch = (rel_err(o_ch, o_ref), rel_err(s_ch, s_ref))

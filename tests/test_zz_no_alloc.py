@@ -18,7 +18,7 @@ import torch
 
 import oracle
 import workloads
-from gpu_util import TOL, check, rel_err, to_device
+from gpu_util import RECORD_BYTES, TOL, check, rel_err, to_device
 
 
 def test_noalloc_rejects_oversized_shapes_on_the_host():
@@ -35,29 +35,39 @@ def test_noalloc_rejects_oversized_shapes_on_the_host():
     # missing device).  gdn_prefill's own workspace query also counts the time-parallel
     # buffers, which this entry point never uses.
     fits = gdn.make_shape(gdn.GDN_BF16, 1, 4096, 1, 16, 16, 128, 128)
-    assert 64 * 16 * 82944 <= gdn.PREFILL_NOALLOC_SCRATCH_BYTES
+    assert 64 * 16 * RECORD_BYTES <= gdn.PREFILL_NOALLOC_SCRATCH_BYTES
     st = lib.gdn_prefill_noalloc(ctypes.byref(fits), *([None] * 9), 0.0, None, None, None)
     assert st != gdn.GDN_OK and b"above the fixed" not in lib.gdn_last_error_message()
 
 
+def test_record_size_is_the_documented_one():
+    """Two sequences of one chunk at one value head, batched: the workspace is exactly two
+    records.  (A batch of one is sized the packed way, two spare records per head.)"""
+    from recurrent_state_scan_gb300 import gdn
+    two = gdn.make_shape(gdn.GDN_BF16, 2, 64, 2, 1, 1, 128, 128)
+    assert gdn.gdn_prefill_workspace_bytes(two) == 2 * RECORD_BYTES
+    one = gdn.make_shape(gdn.GDN_BF16, 1, 64, 1, 1, 1, 128, 128)
+    assert gdn.gdn_prefill_workspace_bytes(one) == 3 * RECORD_BYTES
+
+
 def test_noalloc_size_boundary_follows_the_call_layout():
     """A batched call (no cu_seqlens) is sized as batch * ceil(T / 64) * h_v records of
-    82,944 bytes: 4,800 tokens at 16 value heads (1,200 records) fit the 96 MiB array and
-    4,801 (1,216 records) do not.  A packed call of the same tokens needs
-    (floor(T / 64) + N + 1) * h_v records."""
+    66,560 bytes: 6,016 tokens at 16 value heads (1,504 records) fit the 96 MiB array
+    (1,512 records) and 6,017 (1,520 records) do not.  A packed call of the same tokens
+    needs (floor(T / 64) + N + 1) * h_v records."""
     from recurrent_state_scan_gb300 import gdn
     lib = gdn.load()
-    rec = 82944
-    assert 1200 * rec <= gdn.PREFILL_NOALLOC_SCRATCH_BYTES < 1216 * rec
-    for T, fits in ((4800, True), (4801, False)):
+    rec = RECORD_BYTES
+    assert 1512 * rec <= gdn.PREFILL_NOALLOC_SCRATCH_BYTES < 1513 * rec
+    for T, fits in ((6016, True), (6017, False)):
         shape = gdn.make_shape(gdn.GDN_BF16, 1, T, 1, 16, 16, 128, 128)
         st = lib.gdn_prefill_noalloc(ctypes.byref(shape), *([None] * 9), 0.0, None, None, None)
         assert st != gdn.GDN_OK
         assert (b"above the fixed" in lib.gdn_last_error_message()) == (not fits), T
-    # Packed, one sequence of 4,672 tokens: (73 + 1 + 1) * 16 = 1,200 records fit; a
-    # packed 4,800 would need (75 + 2) * 16 = 1,232 and is refused before any pointer is read.
+    # Packed, one sequence of 5,951 tokens: (92 + 1 + 1) * 16 = 1,504 records fit; a
+    # packed 5,952 would need (93 + 2) * 16 = 1,520 and is refused before any pointer is read.
     cu = ctypes.c_void_p(16)   # never dereferenced: the size check comes first
-    for T, fits in ((4672, True), (4800, False)):
+    for T, fits in ((5951, True), (5952, False)):
         shape = gdn.make_shape(gdn.GDN_BF16, 1, T, 1, 16, 16, 128, 128)
         args = [None] * 9
         args[8] = cu
