@@ -85,6 +85,7 @@ struct TcParams {
     int *status;
     uint8_t *ws;                    // workspace records
     long long wait_budget;          // cycles a bounded wait may take (0: kWaitBudget)
+    int64_t prep_items;             // (chunk slot, value head) items of this prep launch
     // Time-parallel scan (tp_seg > 0): every sequence is cut into tp_nseg segments of
     // tp_seg chunks, all scanned at once.  Segment k > 0 runs twice: from a zero state
     // (outputs to o, end state to tp_psi[k]) and as the operator pass, from the identity
@@ -206,8 +207,10 @@ __device__ __forceinline__ void block_store(const Blk &d, const float (&acc)[2][
 // As[16 j + c][16 i + r]), so A below the diagonal is never overwritten while it is still
 // read, and the four other upper blocks hold the intermediate products.  Step 3's blocks
 // go only to the operand tile: nothing reads them in fp32 again.
-template <typename IO>
-__device__ void invert_chunk(float *As, uint8_t *tt, const float *beta, const float *gam, int pt) {
+// `side(t)` runs on the other 192 threads (t = 0 .. 191) during step 1.
+template <typename IO, typename Side>
+__device__ void invert_chunk(float *As, uint8_t *tt, const float *beta, const float *gam, int pt,
+                             Side &&side) {
     if (pt < 64) {
         // Column-oriented: once x_l is known it updates every later row's sum, so the
         // serial chain is one FMA per row instead of a whole dot product.
@@ -228,6 +231,8 @@ __device__ void invert_chunk(float *As, uint8_t *tt, const float *beta, const fl
             As[(o + i) * kAs + cj] = x[i];
             tt_put<IO>(tt, o + i, cj, x[i], f1, f2);
         }
+    } else {
+        side(pt - 64);
     }
     named_bar(kBarPrep, kPrepThreads);
     const int w = pt >> 5, lane = pt & 31, g = lane >> 2, t = lane & 3;
@@ -293,16 +298,66 @@ constexpr int PP_AS = PP_TT + 16384;           // A, then T, fp32 [64][68]; late
 constexpr int kPrepSmem = PP_AS + 64 * kAs * 4 + 1024;
 constexpr uint32_t kPrepCols = 128;            // TMEM columns of a prep CTA
 
+// One (chunk slot, value head) item of the prep.  Idle slots (past a sequence's last
+// chunk, outside the launch's chunk range, or of a sequence whose device cu_seqlens
+// entries are malformed) are not valid.
+struct PrepItem {
+    int64_t slot, tc0;
+    int32_t h, hq, Lc, first, valid, pad;
+};
+
+__device__ PrepItem prep_item(const TcParams &p, int64_t item) {
+    PrepItem it;
+    it.valid = 0;
+    if (item >= p.prep_items) return it;
+    it.h = (int32_t)(item % p.h_v);
+    it.hq = it.h / (p.h_v / p.h_qk);
+    int64_t slot = item / p.h_v, n;
+    if (p.seg_direct) {
+        const int64_t per = p.seg_end - p.seg_begin;
+        n = slot / per;
+        if (n >= p.num_seqs) return it;
+        slot = n * p.chunks_per_seq + p.seg_begin + slot % per;
+    } else if (p.cu_seqlens == nullptr) {
+        n = slot / p.chunks_per_seq;
+        if (n >= p.num_seqs) return it;
+    } else {
+        int64_t lo = 0, hi = p.num_seqs - 1;       // last n with slot_base(n) <= slot
+        if (slot_base(p, 0) > slot) return it;
+        while (lo < hi) {
+            const int64_t mid = (lo + hi + 1) >> 1;
+            if (slot_base(p, mid) <= slot) lo = mid; else hi = mid - 1;
+        }
+        n = lo;
+    }
+    int64_t t0, t1;
+    if (!seq_range(p.cu_seqlens, p.seqlen, p.num_seqs, p.status, n, t0, t1)) return it;
+    const int64_t c = slot - slot_base(p, n);
+    if (c * kC >= t1 - t0 || c < p.seg_begin || c >= p.seg_end) return it;
+    it.slot = slot;
+    it.tc0 = t0 + c * kC;
+    it.Lc = (int32_t)((t1 - it.tc0) < kC ? (t1 - it.tc0) : kC);
+    // A segment's first chunk writes W for the scan to start from; every other chunk
+    // writes W and M into its predecessor's record.
+    it.first = (c == p.seg_begin) || (p.tp_seg > 0 && c % p.tp_seg == 0);
+    it.valid = 1;
+    return it;
+}
+
 struct PrepCtl {
     uint64_t full, vfull, d1, d2, d3, kprev, dm;
+    PrepItem nxt;                      // the CTA's next item
     uint32_t tmem;
     float G[kC], beta[kC], gam[kC], E[kC], F[kC], wsum[2];
     float kfp[kC], wsum_p[2];          // previous chunk: e^{G_C - G_j}
 };
 
-// One CTA per (chunk, value head).  TMEM (128 columns) holds one product at a time:
-// D1 = [K; Q] K^T, then D2 = [T'; T''] K (W on lanes 0-63), D3 = [T'; T''] V (U on lanes
-// 64-127) and M = W K_{c-1}^T, each read out before the next is issued.
+// Persistent CTAs, three to an SM, walk the (chunk slot, value head) items with the
+// grid's stride.  TMEM (128 columns) holds one product at a time: D1 = [K; Q] K^T, then
+// D2 = [T'; T''] K (W on lanes 0-63), D3 = [T'; T''] V (U on lanes 64-127) and
+// M = W K_{c-1}^T, each read out before the next is issued.  While an item's diagonal
+// blocks are inverted, one thread looks up the CTA's next item.  (Prefetching the next
+// item's tiles into L2 there was measured slower.)
 template <typename IO>
 __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_constant__ TcParams p) {
     constexpr bool kBf16 = std::is_same<IO, __nv_bfloat16>::value;
@@ -316,41 +371,6 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
     const int pt = threadIdx.x, warp = pt >> 5, lane = pt & 31;
     const long long budget = p.wait_budget > 0 ? p.wait_budget : kWaitBudget;
     const int q = warp & 3, hf = warp >> 2;        // TMEM lane quarter, column half
-    const int h = blockIdx.x % p.h_v;
-    const int hq = h / (p.h_v / p.h_qk);
-    int64_t slot = blockIdx.x / p.h_v;
-
-    // Which sequence and chunk this CTA holds (idle slots leave at once).
-    int64_t n;
-    if (p.seg_direct) {
-        const int64_t per = p.seg_end - p.seg_begin;
-        n = slot / per;
-        if (n >= p.num_seqs) return;
-        slot = n * p.chunks_per_seq + p.seg_begin + slot % per;
-    } else if (p.cu_seqlens == nullptr) {
-        n = slot / p.chunks_per_seq;
-        if (n >= p.num_seqs) return;
-    } else {
-        int64_t lo = 0, hi = p.num_seqs - 1;       // last n with slot_base(n) <= slot
-        if (slot_base(p, 0) > slot) return;
-        while (lo < hi) {
-            const int64_t mid = (lo + hi + 1) >> 1;
-            if (slot_base(p, mid) <= slot) lo = mid; else hi = mid - 1;
-        }
-        n = lo;
-    }
-    int64_t t0, t1;
-    if (!seq_range(p.cu_seqlens, p.seqlen, p.num_seqs, p.status, n, t0, t1)) return;
-    const int64_t c = slot - slot_base(p, n);
-    if (c * kC >= t1 - t0 || c < p.seg_begin || c >= p.seg_end) return;
-    const int64_t tc0 = t0 + c * kC;
-    const int Lc = (int)((t1 - tc0) < kC ? (t1 - tc0) : kC);
-    uint8_t *rec = p.ws + ((size_t)slot * p.h_v + h) * kRecord;
-    uint8_t *const rec_prev = rec - (size_t)p.h_v * kRecord;   // chunk c - 1, same head
-    // A segment's first chunk writes W for the scan to start from; every other chunk
-    // writes W' and M into its predecessor's record.
-    const bool first = (c == p.seg_begin) || (p.tp_seg > 0 && c % p.tp_seg == 0);
-
     float *const As = reinterpret_cast<float *>(sm + PP_AS);
     const uint32_t aKQ = smem_u32(sm + PP_KQ), aTT = smem_u32(sm + PP_TT);
     if (warp == 0) {
@@ -366,19 +386,40 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
         mbar_init(&ctl.kprev, 1);
         mbar_init(&ctl.dm, 1);
         fence_mbar_init();
+        ctl.nxt = prep_item(p, blockIdx.x);
     }
-    // [T'; T''] blocks above the diagonal are never written: keep them zero.
-    for (int e = pt; e < 16384 / 16; e += kPrepThreads)
-        *reinterpret_cast<uint4 *>(sm + PP_TT + 16 * e) = make_uint4(0, 0, 0, 0);
-    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl.tmem;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-
+    const int row = 32 * q + lane;
+    // mbarrier parities: full, vfull, d1, d2 and d3 complete once per item, kprev and dm
+    // once per item that is not a segment's first chunk.
+    uint32_t ph = 0, phk = 0;
     // thread 0: 1 = V load, 2 = D1, 4 = D2, 8 = K_{c-1} load, 16 = M, 32 = D3
     uint32_t issued = 0;
+    bool ok = true, failed = false;
+    for (int64_t item = blockIdx.x; item < p.prep_items; item += gridDim.x) {
+    const PrepItem it = ctl.nxt;
+    if (!it.valid) {
+        __syncthreads();   // every thread has read ctl.nxt
+        if (pt == 0) ctl.nxt = prep_item(p, item + gridDim.x);
+        __syncthreads();
+        continue;
+    }
+    const int h = it.h, hq = it.hq, Lc = it.Lc;
+    const bool first = it.first != 0;
+    const int64_t tc0 = it.tc0;
+    uint8_t *rec = p.ws + ((size_t)it.slot * p.h_v + h) * kRecord;
+    uint8_t *const rec_prev = rec - (size_t)p.h_v * kRecord;   // chunk c - 1, same head
+    issued = 0;
+
+    // [T'; T''] blocks above the diagonal are never written: keep them zero (the previous
+    // item's U staging has been read out of this tile).
+    for (int e = pt; e < 16384 / 16; e += kPrepThreads)
+        *reinterpret_cast<uint4 *>(sm + PP_TT + 16 * e) = make_uint4(0, 0, 0, 0);
+    fence_async_smem();
     const int tok = (int)tc0;
     if (pt == 0) {
         mbar_arrive_expect_tx(&ctl.full, 4 * 8192);
@@ -444,7 +485,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
     }
     // D1 = [K; Q] K^T once K and Q have landed; then V over the Q rows, which D1 has read.
     if (pt == 0) {
-        ok = mbar_wait(&ctl.full, 0, budget);
+        ok = mbar_wait(&ctl.full, ph, budget);
         if (ok) {
             tc_fence_after();
 #pragma unroll
@@ -455,7 +496,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
             }
             mma_commit(&ctl.d1);
             issued |= 2;
-            ok = mbar_wait(&ctl.d1, 0, budget);
+            ok = mbar_wait(&ctl.d1, ph, budget);
         }
         if (ok) {
             mbar_arrive_expect_tx(&ctl.vfull, 2 * 8192);
@@ -466,7 +507,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
         }
     }
     failed = bar_any(kBarPrep, kPrepThreads, !ok);   // also publishes E, F, gamma
-    if (!failed) ok = mbar_wait(&ctl.full, 0, budget);   // K, written by TMA, is rewritten below
+    if (!failed) ok = mbar_wait(&ctl.full, ph, budget);   // K, written by TMA, is rewritten below
     if (!failed) {
         tc_fence_after();
         // A rows (lanes 0-63, fp32, to As) and P rows (lanes 64-127, I/O type, to the
@@ -521,7 +562,11 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
         named_bar(kBarPrep, kPrepThreads);
 
         // T = (I + A)^-1, written as [T diag(beta gamma); T diag(beta)] (K-major).
-        invert_chunk<IO>(As, sm + PP_TT, ctl.beta, ctl.gam, pt);
+        // Meanwhile one thread of warp 2 looks up the CTA's next item.
+        auto next_item = [&](int t) {
+            if (t == 0) ctl.nxt = prep_item(p, item + gridDim.x);
+        };
+        invert_chunk<IO>(As, sm + PP_TT, ctl.beta, ctl.gam, pt, next_item);
         fence_async_smem();
         tc_fence_before();
         named_bar(kBarPrep, kPrepThreads);
@@ -542,7 +587,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
                         kIdD2, k > 0);
             mma_commit(&ctl.d2);
             issued |= 4;
-            ok = mbar_wait(&ctl.d2, 0, budget);
+            ok = mbar_wait(&ctl.d2, ph, budget);
         }
         failed = bar_any(kBarPrep, kPrepThreads, !ok);
     }
@@ -576,7 +621,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
 #pragma unroll
             for (int r = 0; r < 2; ++r) bulk_store(dst + r * 8192, sm + PP_KQ + r * kRegP, 8192);
             bulk_commit();
-            ok = mbar_wait(&ctl.vfull, 0, budget);
+            ok = mbar_wait(&ctl.vfull, ph, budget);
             if (ok) {
                 tc_fence_after();
 #pragma unroll
@@ -585,7 +630,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
                             sw128_desc(aKQ + 8192 + k * 2048, kRegP, 1024), kIdD2, k > 0);
                 mma_commit(&ctl.d3);
                 issued |= 32;
-                ok = mbar_wait(&ctl.d3, 0, budget);
+                ok = mbar_wait(&ctl.d3, ph, budget);
             }
         }
         failed = bar_any(kBarPrep, kPrepThreads, !ok);
@@ -617,7 +662,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
             bulk_store(rec + REC_U, sm + PP_TT, 16384);
             bulk_commit();
             if (!first) {
-                ok = mbar_wait(&ctl.kprev, 0, budget);
+                ok = mbar_wait(&ctl.kprev, phk, budget);
                 if (ok) {
                     tc_fence_after();
                     const uint32_t aKp = smem_u32(sm + PP_AS);
@@ -627,7 +672,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
                                 sw128_desc(aKp + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), kIdD1, k > 0);
                     mma_commit(&ctl.dm);
                     issued |= 16;
-                    ok = mbar_wait(&ctl.dm, 0, budget);
+                    ok = mbar_wait(&ctl.dm, phk, budget);
                 }
             }
         }
@@ -658,16 +703,26 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
             }
         }
     }
+    if (failed) break;    // the whole CTA, with this item's parities and copies in flight
+    // Before the next item's loads overwrite them, the record stores have read their
+    // staging tiles and every thread is done with this item's tiles and TMEM.
+    if (pt == 0) bulk_wait_read();
+    ph ^= 1u;
+    if (!first) phk ^= 1u;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    }   // items
     if (failed && pt == 0) {
         // Let the copies and MMAs already issued land before the CTA leaves (bounded).
         atomicOr(p.status, kDevTimeout);
-        mbar_wait(&ctl.full, 0, kWaitBudget);
-        if (issued & 1) mbar_wait(&ctl.vfull, 0, kWaitBudget);
-        if (issued & 2) mbar_wait(&ctl.d1, 0, kWaitBudget);
-        if (issued & 4) mbar_wait(&ctl.d2, 0, kWaitBudget);
-        if (issued & 32) mbar_wait(&ctl.d3, 0, kWaitBudget);
-        if (issued & 8) mbar_wait(&ctl.kprev, 0, kWaitBudget);
-        if (issued & 16) mbar_wait(&ctl.dm, 0, kWaitBudget);
+        mbar_wait(&ctl.full, ph, kWaitBudget);
+        if (issued & 1) mbar_wait(&ctl.vfull, ph, kWaitBudget);
+        if (issued & 2) mbar_wait(&ctl.d1, ph, kWaitBudget);
+        if (issued & 4) mbar_wait(&ctl.d2, ph, kWaitBudget);
+        if (issued & 32) mbar_wait(&ctl.d3, ph, kWaitBudget);
+        if (issued & 8) mbar_wait(&ctl.kprev, phk, kWaitBudget);
+        if (issued & 16) mbar_wait(&ctl.dm, phk, kWaitBudget);
     }
     if (pt == 0) bulk_wait_read();   // the record stores have read their staging tiles
     tc_fence_before();
@@ -1505,6 +1560,9 @@ SideStream *side_stream() {
 
 // The kernels' dynamic shared-memory limits, a per-device function attribute (set once
 // per device and I/O type).
+// Resident prep CTAs per device and I/O type (SMs x CTAs per SM), set by configure().
+int g_prep_slots[64][2] = {};
+
 template <typename IO>
 cudaError_t configure() {
     static bool configured[64] = {false};
@@ -1526,16 +1584,40 @@ cudaError_t configure() {
             e = cudaFuncSetAttribute(gdn_tp_correct<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kCorrSmem);
         if (e != cudaSuccess) return e;
+        // Persistent prep CTAs: as many as the SMs' shared memory holds, at most the three
+        // the launch bounds size the registers for.
+        int sms = 0, smem_sm = 0, reserved = 0;
+        cudaFuncAttributes fa;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, gdn_chunk_prep<IO>);
+        if (e != cudaSuccess) return e;
+        const int per_cta = kPrepSmem + (int)fa.sharedSizeBytes + reserved;
+        int per_sm = per_cta > 0 ? smem_sm / per_cta : 0;
+        if (per_sm > 3) per_sm = 3;
+        if (sms <= 0 || per_sm <= 0) return cudaErrorInvalidConfiguration;
+        g_prep_slots[dev][std::is_same<IO, __nv_bfloat16>::value] = sms * per_sm;
         configured[dev] = true;
     }
     return cudaSuccess;
 }
 
 template <typename IO>
-cudaError_t launch_prep(const TcParams &tp, int64_t ctas, cudaStream_t stream) {
-    if (ctas <= 0) return cudaSuccess;
-    if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    gdn_chunk_prep<IO><<<(unsigned)ctas, kPrepThreads, kPrepSmem, stream>>>(tp);
+cudaError_t launch_prep(const TcParams &tp, int64_t items, cudaStream_t stream) {
+    if (items <= 0) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const int slots = g_prep_slots[dev][std::is_same<IO, __nv_bfloat16>::value];
+    if (slots <= 0) return cudaErrorInvalidConfiguration;
+    TcParams pk = tp;
+    pk.prep_items = items;
+    // Persistent CTAs pay off on long item lists; up to three items per resident CTA, one
+    // CTA per item leaves a shorter tail.
+    const int64_t ctas = items <= 3 * (int64_t)slots ? items : slots;
+    gdn_chunk_prep<IO><<<(unsigned)ctas, kPrepThreads, kPrepSmem, stream>>>(pk);
     return cudaGetLastError();
 }
 
