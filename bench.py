@@ -110,7 +110,7 @@ def peaks():
 
 # Sources of the kernels each workload's traffic figure belongs to.
 KERNEL_SOURCES = {"decode": ("scan_simt.cu",), "prefill": ("prefill_tc.cu", "tc_ptx.cuh"),
-                  "neighbours": ("neighbours.cu",)}
+                  "neighbours": ("neighbours.cu",), "layer": ("layer_decode.cu",)}
 
 
 def source_digest(kind: str = "prefill") -> str:
@@ -511,6 +511,192 @@ def main_neighbour(args, rank, world, local):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------- the fused layer step
+#
+# One decode token of the whole layer (conv -> step -> gated norm) in one call.  A step is
+# one gdn_decode_layer call; its bytes are every input read once and every output written
+# once, the recurrent state both ways.
+
+def layer_io_bytes(inp) -> dict:
+    s = inp.spec
+    es = inp.x.element_size()
+    B, C, K = s.batch, inp.x.shape[2], s.kernel
+    return {"x": B * C * es, "conv_weight": C * K * es, "conv_bias": 0 if inp.bias is None else C * es,
+            "conv_state_in": B * (K - 1) * C * es, "conv_state_out": B * (K - 1) * C * es,
+            "a": B * s.h_v * es, "b": B * s.h_v * es, "A_log": 4 * s.h_v, "dt_bias": 4 * s.h_v,
+            "state": 2 * B * s.h_v * 128 * s.d_v * 4, "norm_scale": s.d_v * es,
+            "gate": B * s.h_v * s.d_v * es, "y": B * s.h_v * s.d_v * es}
+
+
+def layer_oracle(inp, rows: int):
+    """The float64 oracle chain on the first `rows` sequences: conv -> step -> gated norm."""
+    import oracle
+    s, f = inp.spec, inp.f64
+    B, dqk = rows, s.h_qk * 128
+    yc, _ = oracle.causal_conv(f["x"][:B], f["w"], f["bias"], f["conv_state"][:B], silu=True)
+    q = yc[:, 0, :dqk].reshape(B, s.h_qk, 128)
+    k = yc[:, 0, dqk:2 * dqk].reshape(B, s.h_qk, 128)
+    v = yc[:, 0, 2 * dqk:].reshape(B, s.h_v, s.d_v)
+    o, _ = oracle.scan(np.arange(B + 1), s.h_qk, s.h_v, 128, s.d_v, q, k, v,
+                       a=f["a"][:B].reshape(B, s.h_v), b=f["b"][:B].reshape(B, s.h_v),
+                       A_log=f["A_log"], dt_bias=f["dt_bias"], state_in=f["state"][:B],
+                       threads=cpu_threads())
+    oracle.gated_rmsnorm(o.reshape(B, 1, s.h_v, s.d_v), f["norm_scale"], f["gate"][:B], eps=s.eps)
+
+
+def time_layer_oracle(inp, budget_s: float, min_reps: int = 1):
+    rows = max(1, inp.spec.batch // 8)
+    reps, t0 = 0, time.perf_counter()
+    while reps < min_reps or time.perf_counter() - t0 < budget_s:
+        layer_oracle(inp, rows)
+        reps += 1
+    return (time.perf_counter() - t0) / reps, reps, rows
+
+
+def layer_config(inp, world):
+    s = inp.spec
+    return {"workload": s.name, "io_dtype": s.io, "op": "decode token of the layer: causal conv "
+            "(silu) over [q | k | v] channels -> gated delta-rule step -> gated RMS norm (silu)",
+            "batch": s.batch, "h_qk": s.h_qk, "h_v": s.h_v, "d_k": 128, "d_v": s.d_v,
+            "conv_kernel": s.kernel, "state": "fp32, in place", "conv_state": "two buffers, alternating",
+            "l2": "flushed before every step (256 MiB write, untimed)",
+            "parallelism": f"replicas: the full workload on each of {world} GPU(s), no collective"}
+
+
+def main_layer(args, rank, world, local):
+    inp = workloads.any_workload(args.workload)
+    s = inp.spec
+    nbytes = int(sum(layer_io_bytes(inp).values()))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        for _ in range(args.warmup):
+            time_layer_oracle(inp, 0.0)
+        per, reps, rows = time_layer_oracle(inp, 0.0, min_reps=args.steps)
+        value = nbytes * rows / s.batch / per / 1e9
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": layer_config(inp, world),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle",
+                             "sample": f"the first {rows} of {s.batch} sequences per step, {reps} steps"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+            flush=True)
+        return
+
+    from recurrent_state_scan_gb300 import (gdn_causal_conv, gdn_decode_layer, gdn_decode_step,
+                                            gdn_gated_rmsnorm, load)
+    load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    names = ("x", "w", "bias", "conv_state", "a", "b", "A_log", "dt_bias", "state", "norm_scale", "gate")
+    t = {n: getattr(inp, n).to(dev) for n in names if getattr(inp, n) is not None}
+    cs = [t["conv_state"], torch.empty_like(t["conv_state"])]
+    y = torch.empty((s.batch, 1, s.h_v, s.d_v), dtype=t["x"].dtype, device=dev)
+    step_no = [0]
+
+    def call(d):
+        i = step_no[0] % 2
+        step_no[0] += 1
+        gdn_decode_layer(d["x"], d["w"], d.get("bias"), cs[i], cs[1 - i], d["a"], d["b"], d["A_log"],
+                         d["dt_bias"], d["state"], d["norm_scale"], d["gate"], h_qk=s.h_qk, h_v=s.h_v,
+                         eps=s.eps, y=y, stream=stream)
+
+    dqk = s.h_qk * 128
+
+    def separate(d):
+        # The same token through the separate calls: conv, the q / k / v cut, step, norm.
+        i = step_no[0] % 2
+        step_no[0] += 1
+        yc, _ = gdn_causal_conv(d["x"], d["w"], d.get("bias"), cs[i], activation="silu",
+                                state_out=cs[1 - i], stream=stream)
+        q = yc[:, :, :dqk].reshape(s.batch, 1, s.h_qk, 128).contiguous()
+        k = yc[:, :, dqk:2 * dqk].reshape(s.batch, 1, s.h_qk, 128).contiguous()
+        v = yc[:, :, 2 * dqk:].reshape(s.batch, 1, s.h_v, s.d_v).contiguous()
+        o = gdn_decode_step(q, k, v, d["a"], d["b"], d["A_log"], d["dt_bias"], d["state"], stream=stream)
+        gdn_gated_rmsnorm(o, d["norm_scale"], d["gate"], s.eps, y=y, stream=stream)
+
+    def timed(fn, d):
+        for _ in range(args.warmup):
+            flush.zero_()
+            fn(d)
+        torch.cuda.synchronize(dev)
+        st = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        en = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            flush.zero_()
+            st[i].record(stream)
+            fn(d)
+            en[i].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        return max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in zip(st, en)])), world)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    ms = timed(call, t)
+    clocks = sampler.stop() if sampler else None
+    ms_sep = timed(separate, t)
+
+    e2e = None
+    if not args.no_e2e:
+        # Pinned host inputs of the token (x, a, b, gate) in, y out; the recurrent state,
+        # the conv states and the weights stay resident.
+        host = {n: getattr(inp, n).pin_memory() for n in ("x", "a", "b", "gate")}
+        dbuf = dict(t)
+        for n, v in host.items():
+            dbuf[n] = torch.empty_like(v, device=dev)
+        y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = y_host.numel() * y_host.element_size()
+
+        def e2e_step(d):
+            for n, v in host.items():
+                d[n].copy_(v, non_blocking=True)
+            call(d)
+            y_host.copy_(y, non_blocking=True)
+
+        ems = timed(e2e_step, dbuf)
+        e2e = {"value": world * nbytes / (ems / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": ems,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    pk, pk_kind = peaks()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": world * gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": layer_config(inp, world),
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm_gbs"], "traffic": profiled_traffic(args.workload, "layer"),
+                     "peak_source": f"{pk_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+                     if pk_kind == "measured" else "fallback 6.8 TB/s",
+                     "kernels": "gdn::decode_layer_kernel"},
+        "separate_calls": {"ms_per_step": ms_sep, "launches": 6,
+                           "calls": "gdn_causal_conv, three q/k/v slice copies, gdn_decode_step, "
+                                    "gdn_gated_rmsnorm"},
+        "gpu_launches": args.steps,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if clocks is not None:
+        line["clocks"] = clocks
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        per, reps, rows = time_layer_oracle(inp, 10.0)
+        line["cpu_baseline"] = {"value": nbytes * rows / s.batch / per / 1e9, "unit": "GB/s",
+                                "cores": cpu_threads(), "kind": "oracle",
+                                "sample": f"the first {rows} of {s.batch} sequences x{reps} through the "
+                                          f"float64 C oracle chain, {per * reps:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, local, name=None, with_e2e=True):
@@ -655,6 +841,8 @@ def main():
     args = parse_args()
     rank, world, local = dist_init()
     inp_name = args.workload
+    if inp_name in workloads.LAYER_WORKLOADS:
+        return main_layer(args, rank, world, local)
     if inp_name not in workloads.WORKLOADS:
         return main_neighbour(args, rank, world, local)
     if args.impl == "reference":

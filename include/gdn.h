@@ -316,6 +316,50 @@ gdn_status gdn_gated_rmsnorm(int32_t io_dtype, int64_t rows, int32_t width, cons
                              int32_t activation, void *y, void *stream);
 
 /*
+ * gdn_layer_params -- the neighbouring ops of gdn_decode_layer.
+ */
+typedef struct gdn_layer_params {
+    int32_t conv_kernel;       /* K taps of the causal convolution, 1..8 (dilation 1)      */
+    int32_t conv_activation;   /* GDN_ACT_NONE or GDN_ACT_SILU                              */
+    int32_t norm_activation;   /* GDN_ACT_SILU or GDN_ACT_SIGMOID                           */
+    float norm_epsilon;        /* finite, >= 0                                              */
+} gdn_layer_params;
+
+/*
+ * gdn_decode_layer -- one decode token of a whole gated delta-rule layer in one launch:
+ * the three ops gdn_causal_conv (onnxruntime-ep-mlx ssm.rs `causal_conv_op`),
+ * gdn_decode_step (onnx-runtime-ep-cuda linear_attention.rs `linear_attention_core`,
+ * Steps 1-4) and gdn_gated_rmsnorm (ssm.rs `gated_rms_norm_op`) applied in that order,
+ * with q, k and v taken from the convolution's output and the norm applied to the step's
+ * output o.  Each intermediate is rounded to io_dtype exactly as the separate calls would
+ * store it, but none is written to memory.
+ *   x            [B, 1, C] the layer's mixed row, C = 2 h_qk d_k + h_v d_v, read as
+ *                [q (h_qk x d_k) | k (h_qk x d_k) | v (h_v x d_v)], heads outer.
+ *   conv_weight  [C, 1, K]; conv_bias [C] or NULL; the convolution uses dilation 1.
+ *   conv_state_in  [B, K - 1, C] (channels last, oldest position first) or NULL (zeros);
+ *   conv_state_out [B, K - 1, C] or NULL (not written): the last K - 1 inputs.  It must
+ *                not overlap conv_state_in: several CTAs read the same q and k channels, so
+ *                the update cannot be in place.  Callers alternate two buffers.
+ *   a, b         [B, 1, h_v]; A_log, dt_bias [h_v] fp32; state [B, h_v, d_k, d_v] fp32,
+ *                updated in place; scale 0 means 1 / sqrt(d_k).
+ *   norm_scale   [d_v]; gate [B, 1, h_v, d_v]; y [B, 1, h_v, d_v], the normed output:
+ *                y = o / sqrt(mean(o^2) + norm_epsilon) * norm_scale * act(gate) per
+ *                (sequence, value head) row.
+ * Shape (gdn_shape): seqlen 1, no cu_seqlens, d_k = 128, d_v a multiple of 64 up to 256,
+ * any io_dtype, which x, conv_weight, conv_bias, the conv states, a, b, norm_scale, gate
+ * and y share.  Every pointer is device memory owned by the caller and 16-byte aligned.
+ * Bad arguments return GDN_ERR_INVALID_ARG before anything is launched.  The pages run
+ * these ops as three kernels; the fused form exists to read q, k, v and o from no
+ * intermediate buffer.
+ */
+gdn_status gdn_decode_layer(const gdn_shape *shape, const gdn_layer_params *layer, const void *x,
+                            const void *conv_weight, const void *conv_bias,
+                            const void *conv_state_in, void *conv_state_out, const void *a,
+                            const void *b, const float *A_log, const float *dt_bias, float *state,
+                            float scale, const void *norm_scale, const void *gate, void *y,
+                            void *stream);
+
+/*
  * gdn_last_device_status -- synchronise `stream`, read the device check word
  * set by any earlier call on the current device, clear it, and return GDN_OK or
  * GDN_ERR_DEVICE_CHECK (malformed cu_seqlens, or a slot outside the pool) /

@@ -494,6 +494,68 @@ gdn_status gdn_gated_rmsnorm(int32_t io_dtype, int64_t rows, int32_t width, cons
     return GDN_OK;
 }
 
+gdn_status gdn_decode_layer(const gdn_shape *shape, const gdn_layer_params *layer, const void *x,
+                            const void *conv_weight, const void *conv_bias,
+                            const void *conv_state_in, void *conv_state_out, const void *a,
+                            const void *b, const float *A_log, const float *dt_bias, float *state,
+                            float scale, const void *norm_scale, const void *gate, void *y,
+                            void *stream) {
+    gdn_status st = check_shape(shape, false);
+    if (st != GDN_OK) return st;
+    if (shape->seqlen != 1)
+        return fail(GDN_ERR_INVALID_ARG, "decode takes seqlen 1 (got %lld)", (long long)shape->seqlen);
+    if (shape->d_k != 128) return fail(GDN_ERR_UNSUPPORTED, "the layer step is built for d_k = 128");
+    if (shape->d_v % 64 != 0)
+        return fail(GDN_ERR_UNSUPPORTED, "the layer step needs d_v a multiple of 64 (got %d)", shape->d_v);
+    if (layer == nullptr) return fail(GDN_ERR_INVALID_ARG, "layer is NULL");
+    if (layer->conv_kernel < 1 || layer->conv_kernel > 8)
+        return fail(GDN_ERR_INVALID_ARG, "conv_kernel %d is not in 1..8", layer->conv_kernel);
+    if (layer->conv_activation != GDN_ACT_NONE && layer->conv_activation != GDN_ACT_SILU)
+        return fail(GDN_ERR_INVALID_ARG, "the convolution's activation is NONE or SILU");
+    if (layer->norm_activation != GDN_ACT_SILU && layer->norm_activation != GDN_ACT_SIGMOID)
+        return fail(GDN_ERR_INVALID_ARG, "the norm's activation is SILU or SIGMOID");
+    if (!(layer->norm_epsilon >= 0.0f) || isinf(layer->norm_epsilon))
+        return fail(GDN_ERR_INVALID_ARG, "norm_epsilon must be finite and >= 0");
+    if (!(scale == scale) || isinf(scale)) return fail(GDN_ERR_INVALID_ARG, "scale is not finite");
+    if (shape->batch == 0) return GDN_OK;
+    const void *need[] = {x, conv_weight, a, b, A_log, dt_bias, state, norm_scale, gate, y};
+    const char *names[] = {"x", "conv_weight", "a", "b", "A_log", "dt_bias", "state", "norm_scale",
+                           "gate", "y"};
+    for (int i = 0; i < 10; ++i)
+        if (need[i] == nullptr) return fail(GDN_ERR_INVALID_ARG, "%s is NULL", names[i]);
+    const void *al16[] = {x, conv_weight, conv_bias, conv_state_in, conv_state_out, state, norm_scale, gate};
+    for (const void *ptr : al16)
+        if (ptr != nullptr && !aligned(ptr, 16))
+            return fail(GDN_ERR_INVALID_ARG, "x, the conv tensors, state, norm_scale and gate must be 16-byte aligned");
+    const size_t es = io_size(shape->io_dtype);
+    if (!aligned(a, es) || !aligned(b, es) || !aligned(y, es) || !aligned(A_log, 4) || !aligned(dt_bias, 4))
+        return fail(GDN_ERR_INVALID_ARG, "a, b, y, A_log or dt_bias is misaligned");
+    const int64_t C = 2LL * shape->h_qk * shape->d_k + (int64_t)shape->h_v * shape->d_v;
+    const size_t state_bytes = (size_t)shape->batch * (size_t)(layer->conv_kernel - 1) * (size_t)C * es;
+    if (conv_state_in != nullptr && conv_state_out != nullptr && state_bytes > 0) {
+        const uintptr_t i0 = reinterpret_cast<uintptr_t>(conv_state_in), o0 = reinterpret_cast<uintptr_t>(conv_state_out);
+        if (i0 < o0 + state_bytes && o0 < i0 + state_bytes)
+            return fail(GDN_ERR_INVALID_ARG, "conv_state_out overlaps conv_state_in (the update cannot be in place)");
+    }
+    int *word = nullptr;
+    st = status_word(&word);
+    if (st != GDN_OK) return st;
+    LayerDecodeParams p{};
+    p.x = x; p.conv_w = conv_weight; p.conv_b = conv_bias;
+    p.conv_state_in = conv_state_in; p.conv_state_out = conv_state_out;
+    p.a = a; p.b = b; p.A_log = A_log; p.dt_bias = dt_bias; p.state = state;
+    p.norm_scale = norm_scale; p.gate = gate; p.y = y;
+    p.batch = shape->batch; p.h_qk = shape->h_qk; p.h_v = shape->h_v; p.d_v = shape->d_v;
+    p.conv_k = layer->conv_kernel;
+    p.conv_silu = layer->conv_activation == GDN_ACT_SILU;
+    p.norm_act = layer->norm_activation;
+    p.scale = scale == 0.0f ? 1.0f / sqrtf((float)shape->d_k) : scale;
+    p.eps = layer->norm_epsilon;
+    cudaError_t e = launch_decode_layer(p, (gdn_dtype)shape->io_dtype, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "layer decode launch");
+    return GDN_OK;
+}
+
 gdn_status gdn_last_device_status(void *stream) {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");

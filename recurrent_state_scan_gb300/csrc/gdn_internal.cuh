@@ -114,6 +114,22 @@ cudaError_t launch_gated_rmsnorm(gdn_dtype io, int64_t rows, int32_t width, cons
                                  const void *scale, const void *gate, float eps,
                                  int32_t activation, void *y, bool vec4, cudaStream_t stream);
 
+// One decode step of the whole layer: causal conv -> gated delta-rule step -> gated RMS
+// norm (validated arguments; d_k = 128, d_v a multiple of 64 up to 256).
+struct LayerDecodeParams {
+    const void *x, *conv_w, *conv_b, *conv_state_in;   // conv_b, conv_state_in may be null
+    void *conv_state_out;                              // may be null; never overlaps the input
+    const void *a, *b;
+    const float *A_log, *dt_bias;
+    float *state;                                      // [B, h_v, 128, d_v], in place
+    const void *norm_scale, *gate;
+    void *y;
+    int32_t batch, h_qk, h_v, d_v;
+    int32_t conv_k, conv_silu, norm_act;
+    float scale, eps;
+};
+cudaError_t launch_decode_layer(const LayerDecodeParams &p, gdn_dtype io, cudaStream_t stream);
+
 // Sets the calling thread's last error message; returns `status`.
 gdn_status report_error(gdn_status status, const char *message);
 

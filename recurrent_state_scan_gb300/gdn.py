@@ -26,7 +26,7 @@ EXPORTS = ("gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode_step",
            "gdn_prefill_plan", "gdn_last_device_status", "gdn_status_string",
            "gdn_last_error_message", "gdn_prefill_noalloc", "gdn_decode_step_slots",
            "gdn_scan_window", "gdn_scan_variant", "gdn_causal_conv", "gdn_causal_conv_slots",
-           "gdn_gated_rmsnorm", "gdn_set_wait_budget")
+           "gdn_gated_rmsnorm", "gdn_set_wait_budget", "gdn_decode_layer")
 PATH_SIMT, PATH_TC, PATH_TC_TP = 1, 2, 3
 # gdn_rule codes.
 RULES = {"gated_delta": 0, "delta": 1, "gated": 2, "linear": 3}
@@ -52,6 +52,11 @@ class GdnConvShape(ctypes.Structure):
                 ("kernel", ctypes.c_int32), ("dilation", ctypes.c_int32),
                 ("channels_last", ctypes.c_int32), ("activation", ctypes.c_int32),
                 ("state_window", ctypes.c_int32)]
+
+
+class GdnLayerParams(ctypes.Structure):
+    _fields_ = [("conv_kernel", ctypes.c_int32), ("conv_activation", ctypes.c_int32),
+                ("norm_activation", ctypes.c_int32), ("norm_epsilon", ctypes.c_float)]
 
 
 class GdnError(RuntimeError):
@@ -116,6 +121,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.gdn_last_error_message.argtypes = []
     lib.gdn_set_wait_budget.restype = ctypes.c_int
     lib.gdn_set_wait_budget.argtypes = [ctypes.c_int64]
+    lib.gdn_decode_layer.restype = ctypes.c_int
+    lib.gdn_decode_layer.argtypes = [S, ctypes.POINTER(GdnLayerParams), P, P, P, P, P, P, P, P, P,
+                                     P, ctypes.c_float, P, P, P, P]
     _lib = lib
     return lib
 
@@ -552,4 +560,48 @@ def gdn_gated_rmsnorm(x, scale, gate, eps: float = 1e-5, activation: str = "silu
     _check(lib.gdn_gated_rmsnorm(_DTYPE_CODE[dt], x.numel() // width, width, _ptr(x), _ptr(scale),
                                  _ptr(gate), float(eps), ACTIVATIONS[activation], _ptr(y),
                                  _stream(stream)))
+    return y
+
+
+def gdn_decode_layer(x, conv_weight, conv_bias, conv_state_in, conv_state_out, a, b, A_log,
+                     dt_bias, state, norm_scale, gate, *, h_qk: int, h_v: int, d_k: int = 128,
+                     scale: float = 0.0, conv_activation: str = "silu",
+                     norm_activation: str = "silu", eps: float = 1e-5, y=None, stream=None):
+    """One decode token of the layer: causal conv over x [B, 1, C] (channels read as
+    [q | k | v], C = 2 h_qk d_k + h_v d_v), the gated delta-rule step on state
+    [B, h_v, d_k, d_v] (in place), then the gated RMS norm of o with norm_scale [d_v] and
+    gate [B, 1, h_v, d_v].  conv_weight [C, 1, K]; conv_bias [C] or None; conv states
+    [B, K - 1, C] (conv_state_in None = zeros; conv_state_out None = not written; the two
+    may not overlap).  Returns y [B, 1, h_v, d_v]."""
+    lib = load()
+    dt = x.dtype
+    if dt not in _DTYPE_CODE:
+        raise GdnError(GDN_ERR_INVALID_ARG, f"unsupported io dtype {dt}")
+    for name, t in (("x", x), ("conv_weight", conv_weight), ("a", a), ("b", b),
+                    ("norm_scale", norm_scale), ("gate", gate)):
+        _need_cuda(name, t, dt)
+    for name, t in (("conv_bias", conv_bias), ("conv_state_in", conv_state_in),
+                    ("conv_state_out", conv_state_out)):
+        if t is not None:
+            _need_cuda(name, t, dt)
+    _need_cuda("state", state, torch.float32)
+    _need_cuda("A_log", A_log, torch.float32)
+    _need_cuda("dt_bias", dt_bias, torch.float32)
+    if x.dim() != 3 or x.shape[1] != 1:
+        raise GdnError(GDN_ERR_INVALID_ARG, "x must be [B, 1, C]")
+    B, C = x.shape[0], x.shape[2]
+    d_v = norm_scale.numel()
+    if C != 2 * h_qk * d_k + h_v * d_v or conv_weight.numel() % C != 0:
+        raise GdnError(GDN_ERR_INVALID_ARG, "x's channels must be 2 h_qk d_k + h_v d_v; weight [C, 1, K]")
+    K = conv_weight.numel() // C
+    if y is None:
+        y = torch.empty((B, 1, h_v, d_v), dtype=dt, device=x.device)
+    else:
+        _need_cuda("y", y, dt)
+    shape = make_shape(_DTYPE_CODE[dt], B, 1, B, h_qk, h_v, d_k, d_v)
+    layer = GdnLayerParams(K, ACTIVATIONS[conv_activation], ACTIVATIONS[norm_activation], float(eps))
+    _check(lib.gdn_decode_layer(ctypes.byref(shape), ctypes.byref(layer), _ptr(x), _ptr(conv_weight),
+                                _ptr(conv_bias), _ptr(conv_state_in), _ptr(conv_state_out), _ptr(a),
+                                _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(state), float(scale),
+                                _ptr(norm_scale), _ptr(gate), _ptr(y), _stream(stream)))
     return y

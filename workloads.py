@@ -315,13 +315,84 @@ NORM_WORKLOADS = {
 }
 
 
+@dataclasses.dataclass(frozen=True)
+class LayerSpec:
+    """One decode token of the whole layer: conv over [q | k | v] channels, the step,
+    the gated RMS norm."""
+    name: str
+    io: str
+    batch: int
+    h_qk: int
+    h_v: int
+    seed: int
+    d_v: int = 128
+    kernel: int = 4
+    bias: bool = False
+    conv_state_std: float = 1.0
+    state_std: float = 0.05
+    eps: float = 1e-6
+
+
+@dataclasses.dataclass
+class LayerInputs:
+    spec: LayerSpec
+    x: torch.Tensor               # [B, 1, C], C = 2 h_qk 128 + h_v d_v
+    w: torch.Tensor               # [C, 1, K]
+    bias: Optional[torch.Tensor]  # [C]
+    conv_state: torch.Tensor      # [B, K - 1, C]
+    a: torch.Tensor               # [B, 1, h_v]
+    b: torch.Tensor
+    A_log: torch.Tensor           # [h_v] fp32
+    dt_bias: torch.Tensor
+    state: torch.Tensor           # [B, h_v, 128, d_v] fp32
+    norm_scale: torch.Tensor      # [d_v]
+    gate: torch.Tensor            # [B, 1, h_v, d_v]
+    f64: dict
+
+
+def draw_layer(spec: LayerSpec) -> LayerInputs:
+    rng = np.random.default_rng(spec.seed)
+    B, K = spec.batch, spec.kernel
+    C = 2 * spec.h_qk * 128 + spec.h_v * spec.d_v
+    x = rng.standard_normal((B, 1, C))
+    lim = 1.0 / math.sqrt(K)
+    w = rng.uniform(-lim, lim, (C, 1, K))
+    bias = rng.uniform(-lim, lim, C) if spec.bias else None
+    conv_state = rng.normal(0.0, spec.conv_state_std, (B, K - 1, C))
+    a = rng.standard_normal((B, 1, spec.h_v))
+    b = rng.standard_normal((B, 1, spec.h_v))
+    A_log = rng.uniform(-1.0, 1.0, spec.h_v)
+    dt_bias = rng.normal(0.0, 0.1, spec.h_v)
+    state = rng.normal(0.0, spec.state_std, (B, spec.h_v, 128, spec.d_v))
+    norm_scale = rng.normal(1.0, 0.1, spec.d_v)
+    gate = rng.standard_normal((B, 1, spec.h_v, spec.d_v))
+    t = {n: (None if v is None else _round(v, spec.io))
+         for n, v in (("x", x), ("w", w), ("bias", bias), ("conv_state", conv_state), ("a", a),
+                      ("b", b), ("norm_scale", norm_scale), ("gate", gate))}
+    t["A_log"] = _round(A_log, "f32")
+    t["dt_bias"] = _round(dt_bias, "f32")
+    t["state"] = _round(state, "f32")
+    f64 = {n: (None if v is None else _widen(v).reshape(v.shape)) for n, v in t.items()}
+    return LayerInputs(spec=spec, f64=f64, **t)
+
+
+LAYER_WORKLOADS = {
+    # The decode step's shape (B = 256, 32 heads, d = 128) with a 4-tap conv in front.
+    "bf16_layer_decode_b256": LayerSpec("bf16_layer_decode_b256", io="bf16", batch=256, h_qk=32,
+                                        h_v=32, seed=1013),
+}
+
+
 def any_workload(name: str):
     """Draw any named workload: the scan's, the convolution's or the norm's."""
     if name in WORKLOADS:
         return draw(WORKLOADS[name])
     if name in CONV_WORKLOADS:
         return draw_conv(CONV_WORKLOADS[name])
+    if name in LAYER_WORKLOADS:
+        return draw_layer(LAYER_WORKLOADS[name])
     return draw_norm(NORM_WORKLOADS[name])
 
 
-ALL_WORKLOADS = sorted(list(WORKLOADS) + list(CONV_WORKLOADS) + list(NORM_WORKLOADS))
+ALL_WORKLOADS = sorted(list(WORKLOADS) + list(CONV_WORKLOADS) + list(NORM_WORKLOADS) +
+                       list(LAYER_WORKLOADS))
