@@ -765,7 +765,8 @@ constexpr uint32_t kTxB = 2 * 16384;
 // TMEM columns: D4' at 0 / 64 and X at 128 / 192 by chunk parity, DS at 256.
 constexpr uint32_t TS_D4 = 0, TS_X = 128, TS_DS = 256, kScanCols = 512;
 constexpr int kChainWarps = 8;                 // Delta, state update, readout
-constexpr int kScanAllThreads = 32 * kChainWarps + 64;   // + an MMA-issue warp and a copy warp
+// + an MMA-issue warp, a copy warp and two state warps (S rows 64-127, TMEM lanes 64-127)
+constexpr int kScanAllThreads = 32 * kChainWarps + 128;
 constexpr uint32_t kBarOut = 2;                // named barrier of the 128 readout threads
 constexpr int kLptMax = 128;                   // packed batches up to this size run longest first
 
@@ -813,7 +814,7 @@ __device__ __forceinline__ bool warp_wait_or_abort(uint64_t *bar, uint32_t parit
 //                                            gamma_C(c - 1) D4'(c - 1) + X(c - 1)
 //   DS(c) = K_c^T diag(e^{G_C - G}) Delta_c                                 (commit ds)
 //   X(c) = [P_c; M_{c+1}] Delta_c                                          (commit x)
-//   S_{c+1} = gamma_C S_c + DS(c), SB        all chain warps
+//   S_{c+1} = gamma_C S_c + DS(c), SB        readout warps (rows 0-63), state warps (64-127)
 //   o_c = scale gamma (Q_c S_c) + P_c Delta_c    warps on lanes 0-63, overlapping chunk c + 1
 // X phases: 0 is W_0 S_0 (into D4' block 1), c + 1 is X(c).  D4' and X alternate between
 // two TMEM column blocks each.  One warp issues every MMA and copy; the chain warps wait only on the
@@ -834,6 +835,7 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool issue_warp = (warp == kChainWarps);
     const bool copy_warp = (warp == kChainWarps + 1);
+    const bool state_warp = (warp >= kChainWarps + 2);
     // Time-parallel job of this CTA: 0 is segment 0; 2k - 1 is segment k from a zero
     // state; 2k is segment k's operator pass (identity state, U = 0).
     int64_t unit = blockIdx.x;
@@ -896,8 +898,8 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
         mbar_init(&ctl.d4, 1);
         mbar_init(&ctl.ds, 1);
         mbar_init(&ctl.x, 1);
-        mbar_init(&ctl.delta_ready, kChainWarps / 2);
-        mbar_init(&ctl.sb_ready, kChainWarps);
+        mbar_init(&ctl.delta_ready, kChainWarps / 2);   // the Delta warps
+        mbar_init(&ctl.sb_ready, kChainWarps / 2 + 2);   // readout warps and state warps
         mbar_init(&ctl.out_done, kChainWarps / 2);
         mbar_init(&ctl.ld_b, 1);
         mbar_init(&ctl.ld_a, 1);
@@ -1067,7 +1069,7 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
             if (!ok) *abort = 1;
         }
         __syncwarp();
-    } else {
+    } else if (!state_warp) {
         // ------------------------------------------------------------ chain warps
         const int q = warp & 3, g = warp >> 2;     // TMEM lane quarter, 32-column group
         const int row = 32 * q + lane;             // this thread's TMEM lane
@@ -1075,8 +1077,10 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
         IO *go = static_cast<IO *>(op_pass ? p.tp_r : p.o);
         const CUtensorMap *omap = op_pass ? &p.tm_r : &p.tm_o;
+        // The readout warps hold S rows 0-63 (this thread's row, 32 columns); the Delta
+        // warps hold none: rows 64-127 belong to the state warps.
         float S[32];                               // S[row][v0 + 32 g + e]
-        if (op_pass) {
+        if (op_pass || !out_warp) {
             // The identity, this thread's row and columns.
 #pragma unroll
             for (int e = 0; e < 32; ++e) S[e] = (row == v0 + 32 * g + e) ? 1.f : 0.f;
@@ -1101,7 +1105,7 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl.sb_ready);
         };
-        publish_sb(true);
+        if (out_warp) publish_sb(true);
         bool ok = true;
         float gC_prev = 1.f;   // e^{G_C} of chunk c - 1 (1 before the first: W_0 S_0 is exact)
         for (int c = 0; c < nchunks; ++c) {
@@ -1170,6 +1174,10 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl.delta_ready);
+                // The next Delta waits only for X(c): the state warps update rows 64-127.
+                gC_prev = gC;
+                if (!ok) break;
+                continue;
             }
 
             // S_{c+1} = gamma_C S_c + DS(c) (fp32 registers), then the operand tile.
@@ -1186,11 +1194,6 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                 }
             }
             publish_sb(ok);
-            gC_prev = gC;
-            if (!out_warp) {
-                if (!ok) break;
-                continue;
-            }
 
             // o_c = scale gamma (rows 0-63 of D4' block c & 1) + (rows 0-63 of X block
             // c & 1) after X(c), while chunk c + 1 runs.  A full
@@ -1242,13 +1245,77 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
             }
         }
         if (tid == 0) bulk_wait_all();    // the output tiles have reached global memory
-        if (ok) {
+        if (ok && out_warp) {
             float *sdst = p.state_out;
             if (p.tp_seg > 0)
                 sdst = (op_pass ? p.tp_phi : p.tp_psi) + (size_t)tseg * p.num_seqs * p.h_v * kDK * kDK;
             float4 *dst = reinterpret_cast<float4 *>(sdst + sbase + (size_t)row * kDK + v0 + 32 * g);
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4)
+                dst[q4] = make_float4(S[4 * q4], S[4 * q4 + 1], S[4 * q4 + 2], S[4 * q4 + 3]);
+        } else if (!ok) {
+            *abort = 1;
+        }
+    } else {
+        // ------------------------------------------------------------ state warps
+        // S rows 64-127 (this thread's row, all 64 columns of the half): S_{c+1} =
+        // gamma_C S_c + DS(c) from TMEM lanes 64-127, then the operand tile.
+        const int q = warp & 3;                    // 2 or 3
+        const int row = 32 * q + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        float S[kNV];                              // S[row][v0 + e]
+        if (op_pass) {
+#pragma unroll
+            for (int e = 0; e < kNV; ++e) S[e] = (row == v0 + e) ? 1.f : 0.f;
+        } else {
+            const bool zero = p.state_in == nullptr || tseg > 0;
+            const float4 *src = reinterpret_cast<const float4 *>(p.state_in + sbase + (size_t)row * kDK + v0);
+#pragma unroll
+            for (int q4 = 0; q4 < kNV / 4; ++q4) {
+                const float4 f = zero ? make_float4(0.f, 0.f, 0.f, 0.f) : src[q4];
+                S[4 * q4] = f.x; S[4 * q4 + 1] = f.y; S[4 * q4 + 2] = f.z; S[4 * q4 + 3] = f.w;
+            }
+        }
+        auto publish_rows = [&](bool write) {
+            if (write) {
+#pragma unroll
+                for (int q8 = 0; q8 < kNV / 8; ++q8)
+                    *reinterpret_cast<uint4 *>(sm + SS_SB + sw128_offset(row, q8)) = pack8<IO>(S + 8 * q8);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl.sb_ready);
+        };
+        publish_rows(true);
+        bool ok = true;
+        for (int c = 0; c < nchunks; ++c) {
+            const int s = c & 1;
+            const GateRec &gr = *reinterpret_cast<const GateRec *>(sm + s * kScanStage + SS_G);
+            ok = ok && warp_wait_or_abort(&ctl.full_a[s], (c >> 1) & 1, abort, budget);
+            const float gC = ok ? gr.gC : 0.f;
+            ok = ok && warp_wait_or_abort(&ctl.ds, c & 1, abort, budget);
+            if (ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int ps = 0; ps < kNV / 16; ++ps) {
+                    uint32_t r[16];
+                    tmem_ld16(tmem + lane_base + TS_DS + 16 * ps, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) S[16 * ps + e] = fmaf(gC, S[16 * ps + e], __uint_as_float(r[e]));
+                }
+            }
+            publish_rows(ok);
+            if (!ok) break;
+        }
+        if (ok) {
+            float *sdst = p.state_out;
+            if (p.tp_seg > 0)
+                sdst = (op_pass ? p.tp_phi : p.tp_psi) + (size_t)tseg * p.num_seqs * p.h_v * kDK * kDK;
+            float4 *dst = reinterpret_cast<float4 *>(sdst + sbase + (size_t)row * kDK + v0);
+#pragma unroll
+            for (int q4 = 0; q4 < kNV / 4; ++q4)
                 dst[q4] = make_float4(S[4 * q4], S[4 * q4 + 1], S[4 * q4 + 2], S[4 * q4 + 3]);
         } else {
             *abort = 1;
