@@ -39,8 +39,9 @@
  * Entry points: gdn_prefill (and gdn_prefill_noalloc, gdn_prefill_plan,
  * gdn_prefill_workspace_bytes), gdn_decode_step, gdn_decode_step_slots (a state
  * pool), gdn_scan_window (the states after each of the last W steps),
- * gdn_scan_variant (other update rules and gate layouts), and the layer ops
- * around the scan: gdn_causal_conv, gdn_causal_conv_slots and gdn_gated_rmsnorm.
+ * gdn_scan_variant and gdn_prefill_variant (other update rules and gate layouts),
+ * the layer ops around the scan: gdn_causal_conv, gdn_causal_conv_slots and
+ * gdn_gated_rmsnorm, and gdn_decode_layer (conv -> decode step -> norm in one kernel).
  *  - gdn_last_error_message() gives a human-readable detail of the last
  *    non-OK status returned on the calling thread.
  */
@@ -230,6 +231,22 @@ gdn_status gdn_scan_window(const gdn_shape *shape, const void *q, const void *k,
                            const void *a, const void *b, const float *A_log, const float *dt_bias,
                            const float *state_in, float scale, void *o, float *window,
                            int32_t window_len, void *stream);
+
+/*
+ * gdn_prefill_variant -- gdn_prefill with a gate / rule variant (see gdn_scan_variant for
+ * the variants and how they shape a, b, A_log and dt_bias), taking the path gdn_prefill
+ * takes: for 16-bit I/O at d_k = d_v = 128 the chunked tensor-core prefill, on which the
+ * four update rules and the shared beta are switches of the same algebra (no decay:
+ * g = 0; no delta term: A = 0, beta = 1 and W = 0, so the chunk update adds K^T V).  A
+ * per-key-dim decay runs the token-sequential path, which needs no workspace.  workspace
+ * and workspace_bytes are gdn_prefill's (gdn_prefill_workspace_bytes sizes them for the
+ * same shape).  Errors are gdn_scan_variant's plus gdn_prefill's workspace rule.
+ */
+gdn_status gdn_prefill_variant(const gdn_shape *shape, const gdn_variant *variant, const void *q,
+                               const void *k, const void *v, const void *a, const void *b,
+                               const float *A_log, const float *dt_bias, const float *state_in,
+                               const int32_t *cu_seqlens, float scale, void *o, float *state_out,
+                               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * gdn_scan_variant -- gdn_prefill with the gate and rule variants of the

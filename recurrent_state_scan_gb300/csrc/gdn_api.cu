@@ -96,6 +96,31 @@ gdn_status check_inputs(const gdn_shape *s, int64_t tokens, const void *q, const
     return GDN_OK;
 }
 
+// Inputs of a call with a gate / rule variant: q, k, v and o always; a, A_log and
+// dt_bias for a decaying rule, b for a delta rule (the others may be NULL).
+gdn_status check_variant(const gdn_shape *shape, const gdn_variant *variant, int64_t tokens,
+                         const void *q, const void *k, const void *v, const void *a, const void *b,
+                         const float *A_log, const float *dt_bias, const void *o) {
+    if (variant->rule < GDN_RULE_GATED_DELTA || variant->rule > GDN_RULE_LINEAR)
+        return fail(GDN_ERR_INVALID_ARG, "rule %d is not a gdn_rule", variant->rule);
+    const bool has_decay = variant->rule == GDN_RULE_GATED_DELTA || variant->rule == GDN_RULE_GATED;
+    const bool has_delta = variant->rule == GDN_RULE_GATED_DELTA || variant->rule == GDN_RULE_DELTA;
+    if (tokens > 0) {
+        if (!q || !k || !v || !o) return fail(GDN_ERR_INVALID_ARG, "q, k, v or o is NULL");
+        if (has_decay && (!a || !A_log || !dt_bias))
+            return fail(GDN_ERR_INVALID_ARG, "a decaying rule needs a, A_log and dt_bias");
+        if (has_delta && !b) return fail(GDN_ERR_INVALID_ARG, "a delta rule needs b");
+        const size_t es = io_size(shape->io_dtype);
+        const void *io_ptrs[] = {q, k, v, a, b, o};
+        for (const void *ptr : io_ptrs)
+            if (ptr && !aligned(ptr, es))
+                return fail(GDN_ERR_INVALID_ARG, "pointer is not %zu-byte aligned", es);
+        if ((A_log && !aligned(A_log, 4)) || (dt_bias && !aligned(dt_bias, 4)))
+            return fail(GDN_ERR_INVALID_ARG, "A_log/dt_bias must be 4-byte aligned");
+    }
+    return GDN_OK;
+}
+
 }  // namespace
 
 // Record `message` as the calling thread's last error detail and return `status`
@@ -183,11 +208,15 @@ gdn_status gdn::prefill_impl(const gdn_shape *shape, const void *q, const void *
                              const void *a, const void *b, const float *A_log, const float *dt_bias,
                              const float *state_in, const int32_t *cu_seqlens, float scale, void *o,
                              float *state_out, void *workspace, size_t workspace_bytes,
-                             bool allow_overlap, void *stream) {
+                             bool allow_overlap, void *stream, const gdn_variant *variant) {
     gdn_status st = check_shape(shape, cu_seqlens != nullptr);
     if (st != GDN_OK) return st;
     const int64_t tokens = cu_seqlens ? shape->seqlen : shape->seqlen * (int64_t)shape->batch;
-    st = check_inputs(shape, tokens, q, k, v, a, b, A_log, dt_bias, o);
+    if (variant == nullptr) {
+        st = check_inputs(shape, tokens, q, k, v, a, b, A_log, dt_bias, o);
+    } else {
+        st = check_variant(shape, variant, tokens, q, k, v, a, b, A_log, dt_bias, o);
+    }
     if (st != GDN_OK) return st;
     if (shape->num_seqs == 0) return GDN_OK;
     if (state_out == nullptr) return fail(GDN_ERR_INVALID_ARG, "state_out is NULL");
@@ -208,9 +237,14 @@ gdn_status gdn::prefill_impl(const gdn_shape *shape, const void *q, const void *
     p.h_qk = shape->h_qk; p.h_v = shape->h_v; p.d_k = shape->d_k; p.d_v = shape->d_v;
     p.scale = scale == 0.0f ? 1.0f / sqrtf((float)shape->d_k) : scale;
     p.status = word;
+    if (variant != nullptr) {
+        p.rule = variant->rule;
+        p.decay_per_key = variant->decay_per_key != 0;
+        p.beta_shared = variant->beta_shared != 0;
+    }
     const gdn_dtype io = (gdn_dtype)shape->io_dtype;
     cudaError_t e;
-    if (prefill_tc_supported(p, io, tokens)) {
+    if (!p.decay_per_key && prefill_tc_supported(p, io, tokens)) {
         const size_t need = prefill_tc_workspace(cu_seqlens != nullptr, shape->seqlen, shape->batch,
                                                  shape->num_seqs, shape->h_v);
         if (workspace == nullptr || workspace_bytes < need)
@@ -335,6 +369,16 @@ gdn_status gdn_scan_window(const gdn_shape *shape, const void *q, const void *k,
     return GDN_OK;
 }
 
+gdn_status gdn_prefill_variant(const gdn_shape *shape, const gdn_variant *variant, const void *q,
+                               const void *k, const void *v, const void *a, const void *b,
+                               const float *A_log, const float *dt_bias, const float *state_in,
+                               const int32_t *cu_seqlens, float scale, void *o, float *state_out,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+    if (variant == nullptr) return fail(GDN_ERR_INVALID_ARG, "variant is NULL");
+    return prefill_impl(shape, q, k, v, a, b, A_log, dt_bias, state_in, cu_seqlens, scale, o,
+                        state_out, workspace, workspace_bytes, true, stream, variant);
+}
+
 gdn_status gdn_scan_variant(const gdn_shape *shape, const gdn_variant *variant, const void *q,
                             const void *k, const void *v, const void *a, const void *b,
                             const float *A_log, const float *dt_bias, const float *state_in,
@@ -343,24 +387,9 @@ gdn_status gdn_scan_variant(const gdn_shape *shape, const gdn_variant *variant, 
     gdn_status st = check_shape(shape, cu_seqlens != nullptr);
     if (st != GDN_OK) return st;
     if (variant == nullptr) return fail(GDN_ERR_INVALID_ARG, "variant is NULL");
-    if (variant->rule < GDN_RULE_GATED_DELTA || variant->rule > GDN_RULE_LINEAR)
-        return fail(GDN_ERR_INVALID_ARG, "rule %d is not a gdn_rule", variant->rule);
-    const bool has_decay = variant->rule == GDN_RULE_GATED_DELTA || variant->rule == GDN_RULE_GATED;
-    const bool has_delta = variant->rule == GDN_RULE_GATED_DELTA || variant->rule == GDN_RULE_DELTA;
     const int64_t tokens = cu_seqlens ? shape->seqlen : shape->seqlen * (int64_t)shape->batch;
-    if (tokens > 0) {
-        if (!q || !k || !v || !o) return fail(GDN_ERR_INVALID_ARG, "q, k, v or o is NULL");
-        if (has_decay && (!a || !A_log || !dt_bias))
-            return fail(GDN_ERR_INVALID_ARG, "a decaying rule needs a, A_log and dt_bias");
-        if (has_delta && !b) return fail(GDN_ERR_INVALID_ARG, "a delta rule needs b");
-        const size_t es = io_size(shape->io_dtype);
-        const void *io_ptrs[] = {q, k, v, a, b, o};
-        for (const void *ptr : io_ptrs)
-            if (ptr && !aligned(ptr, es))
-                return fail(GDN_ERR_INVALID_ARG, "pointer is not %zu-byte aligned", es);
-        if ((A_log && !aligned(A_log, 4)) || (dt_bias && !aligned(dt_bias, 4)))
-            return fail(GDN_ERR_INVALID_ARG, "A_log/dt_bias must be 4-byte aligned");
-    }
+    st = check_variant(shape, variant, tokens, q, k, v, a, b, A_log, dt_bias, o);
+    if (st != GDN_OK) return st;
     if (shape->num_seqs == 0) return GDN_OK;
     if (state_out == nullptr) return fail(GDN_ERR_INVALID_ARG, "state_out is NULL");
     if (!aligned(state_out, 16) || !aligned(state_in, 16))

@@ -165,11 +165,12 @@ cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_t
 extern long long g_wait_budget;
 
 // gdn_prefill with the segment overlap allowed or not (no internal stream is created
-// when it is not).
+// when it is not), and optionally a gate / rule variant (per-key decay runs on the
+// token-sequential kernel, everything else on the path gdn_prefill would take).
 gdn_status prefill_impl(const gdn_shape *shape, const void *q, const void *k, const void *v,
                         const void *a, const void *b, const float *A_log, const float *dt_bias,
                         const float *state_in, const int32_t *cu_seqlens, float scale, void *o,
                         float *state_out, void *workspace, size_t workspace_bytes,
-                        bool allow_overlap, void *stream);
+                        bool allow_overlap, void *stream, const gdn_variant *variant = nullptr);
 
 }  // namespace gdn

@@ -86,6 +86,10 @@ struct TcParams {
     uint8_t *ws;                    // workspace records
     long long wait_budget;          // cycles a bounded wait may take (0: kWaitBudget)
     int64_t prep_items;             // (chunk slot, value head) items of this prep launch
+    // Update rule (the CUDA page's UpdateRule list): without decay g = 0; without the
+    // delta term A = 0, beta = 1 and W = 0 (the T diag(beta gamma) half of the operand
+    // tile is zero), so Delta = U = V.  beta_shared: b is [tokens], one beta for all heads.
+    int32_t has_decay, has_delta, beta_shared;
     // Time-parallel scan (tp_seg > 0): every sequence is cut into tp_nseg segments of
     // tp_seg chunks, all scanned at once.  Segment k > 0 runs twice: from a zero state
     // (outputs to o, end state to tp_psi[k]) and as the operator pass, from the identity
@@ -151,12 +155,14 @@ __device__ __forceinline__ void tt_put(uint8_t *tt, int r, int c, float x, float
     IoType<IO>::st(reinterpret_cast<IO *>(tt + off), x * f1);
     IoType<IO>::st(reinterpret_cast<IO *>(tt + 8192 + off), x * f2);   // row r + 64
 }
+// t1 scales the T diag(beta gamma) half (0 for rules without the delta term: W = 0).
 template <typename IO>
 __device__ __forceinline__ void tt_put2(uint8_t *tt, int r, int c, float x0, float x1,
-                                        const float *beta, const float *gam) {
+                                        const float *beta, const float *gam, float t1) {
     const uint32_t off = sw128_offset(r, c >> 3) + (c & 7) * 2;
     const float b0 = beta[c], b1 = beta[c + 1];
-    *reinterpret_cast<uint32_t *>(tt + off) = Pack<IO>::two(x0 * b0 * gam[c], x1 * b1 * gam[c + 1]);
+    *reinterpret_cast<uint32_t *>(tt + off) =
+        Pack<IO>::two(x0 * b0 * gam[c] * t1, x1 * b1 * gam[c + 1] * t1);
     *reinterpret_cast<uint32_t *>(tt + 8192 + off) = Pack<IO>::two(x0 * b0, x1 * b1);
 }
 
@@ -209,8 +215,8 @@ __device__ __forceinline__ void block_store(const Blk &d, const float (&acc)[2][
 // go only to the operand tile: nothing reads them in fp32 again.
 // `side(t)` runs on the other 192 threads (t = 0 .. 191) during step 1.
 template <typename IO, typename Side>
-__device__ void invert_chunk(float *As, uint8_t *tt, const float *beta, const float *gam, int pt,
-                             Side &&side) {
+__device__ void invert_chunk(float *As, uint8_t *tt, const float *beta, const float *gam, float t1,
+                             int pt, Side &&side) {
     if (pt < 64) {
         // Column-oriented: once x_l is known it updates every later row's sum, so the
         // serial chain is one FMA per row instead of a whole dot product.
@@ -225,7 +231,7 @@ __device__ void invert_chunk(float *As, uint8_t *tt, const float *beta, const fl
             for (int i = l + 1; i < 16; ++i) acc[i] = fmaf(As[(o + i) * kAs + o + l], x[l], acc[i]);
         }
         __syncwarp();
-        const float f2 = beta[cj], f1 = f2 * gam[cj];
+        const float f2 = beta[cj], f1 = f2 * gam[cj] * t1;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             As[(o + i) * kAs + cj] = x[i];
@@ -249,8 +255,8 @@ __device__ void invert_chunk(float *As, uint8_t *tt, const float *beta, const fl
 #pragma unroll
         for (int nh = 0; nh < 2; ++nh) {
             const int c = 16 * j + 8 * nh + 2 * t, r = 16 * i + g;
-            tt_put2<IO>(tt, r, c, -acc[nh][0], -acc[nh][1], beta, gam);
-            tt_put2<IO>(tt, r + 8, c, -acc[nh][2], -acc[nh][3], beta, gam);
+            tt_put2<IO>(tt, r, c, -acc[nh][0], -acc[nh][1], beta, gam, t1);
+            tt_put2<IO>(tt, r + 8, c, -acc[nh][2], -acc[nh][3], beta, gam, t1);
         }
     };
     if (w < 2) {                                    // 16 -> 32
@@ -433,20 +439,22 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
     // from plain loads of the logits while K and Q are in flight.
     float ra = 0.f, rb = 0.f, rap = 0.f;
     if (pt < Lc) {
-        ra = IoType<IO>::ld(static_cast<const IO *>(p.a) + (size_t)(tc0 + pt) * p.h_v + h);
-        rb = IoType<IO>::ld(static_cast<const IO *>(p.b) + (size_t)(tc0 + pt) * p.h_v + h);
+        if (p.has_decay) ra = IoType<IO>::ld(static_cast<const IO *>(p.a) + (size_t)(tc0 + pt) * p.h_v + h);
+        if (p.has_delta)
+            rb = IoType<IO>::ld(static_cast<const IO *>(p.b) +
+                                (p.beta_shared ? (size_t)(tc0 + pt) : (size_t)(tc0 + pt) * p.h_v + h));
     }
-    if (!first && pt < kC)
+    if (!first && pt < kC && p.has_decay)
         rap = IoType<IO>::ld(static_cast<const IO *>(p.a) + (size_t)(tc0 - kC + pt) * p.h_v + h);
     bool ok = true, failed = false;
     {
         float gsum = 0.f, be = 0.f, gsum_p = 0.f;
         if (pt < kC) {
             if (pt < Lc) {
-                gsum = decay_f(ra, p.A_log[h], p.dt_bias[h]);
-                be = sigmoid_f(rb);
+                gsum = p.has_decay ? decay_f(ra, p.A_log[h], p.dt_bias[h]) : 0.f;
+                be = p.has_delta ? sigmoid_f(rb) : 1.f;
             }
-            if (!first) gsum_p = decay_f(rap, p.A_log[h], p.dt_bias[h]);
+            if (!first && p.has_decay) gsum_p = decay_f(rap, p.A_log[h], p.dt_bias[h]);
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const float y = __shfl_up_sync(0xffffffffu, gsum, off);
@@ -529,7 +537,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
                     for (int e = 0; e < 4; ++e) {
                         const int j = 32 * hf + 4 * j4 + e;
                         const float d = safe ? Ei * ctl.F[j] : __expf(Gi - ctl.G[j]);
-                        x[e] = (j < i) ? bi * d * __uint_as_float(r[4 * j4 + e]) : 0.f;
+                        x[e] = (j < i && p.has_delta) ? bi * d * __uint_as_float(r[4 * j4 + e]) : 0.f;
                     }
                     *reinterpret_cast<float4 *>(As + i * kAs + 32 * hf + 4 * j4) =
                         make_float4(x[0], x[1], x[2], x[3]);
@@ -566,7 +574,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
         auto next_item = [&](int t) {
             if (t == 0) ctl.nxt = prep_item(p, item + gridDim.x);
         };
-        invert_chunk<IO>(As, sm + PP_TT, ctl.beta, ctl.gam, pt, next_item);
+        invert_chunk<IO>(As, sm + PP_TT, ctl.beta, ctl.gam, p.has_delta ? 1.f : 0.f, pt, next_item);
         fence_async_smem();
         tc_fence_before();
         named_bar(kBarPrep, kPrepThreads);
@@ -1872,6 +1880,9 @@ cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_t
     tp.chunks_per_seq = (int32_t)((p.seqlen + kC - 1) / kC);
     tp.ws = static_cast<uint8_t *>(workspace);
     tp.wait_budget = __atomic_load_n(&g_wait_budget, __ATOMIC_RELAXED);
+    tp.has_decay = p.rule == GDN_RULE_GATED_DELTA || p.rule == GDN_RULE_GATED;
+    tp.has_delta = p.rule == GDN_RULE_GATED_DELTA || p.rule == GDN_RULE_DELTA;
+    tp.beta_shared = p.beta_shared;
     const bool varlen = p.cu_seqlens != nullptr;
     const int64_t n_slots = chunk_slots(varlen, p.seqlen, p.num_seqs, p.num_seqs);
     // The time-parallel scan, when the shape suits it, the caller allows internal

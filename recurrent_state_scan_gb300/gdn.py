@@ -26,7 +26,7 @@ EXPORTS = ("gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode_step",
            "gdn_prefill_plan", "gdn_last_device_status", "gdn_status_string",
            "gdn_last_error_message", "gdn_prefill_noalloc", "gdn_decode_step_slots",
            "gdn_scan_window", "gdn_scan_variant", "gdn_causal_conv", "gdn_causal_conv_slots",
-           "gdn_gated_rmsnorm", "gdn_set_wait_budget", "gdn_decode_layer")
+           "gdn_gated_rmsnorm", "gdn_set_wait_budget", "gdn_decode_layer", "gdn_prefill_variant")
 PATH_SIMT, PATH_TC, PATH_TC_TP = 1, 2, 3
 # gdn_rule codes.
 RULES = {"gated_delta": 0, "delta": 1, "gated": 2, "linear": 3}
@@ -121,6 +121,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.gdn_last_error_message.argtypes = []
     lib.gdn_set_wait_budget.restype = ctypes.c_int
     lib.gdn_set_wait_budget.argtypes = [ctypes.c_int64]
+    lib.gdn_prefill_variant.restype = ctypes.c_int
+    lib.gdn_prefill_variant.argtypes = [S, ctypes.POINTER(GdnVariant), P, P, P, P, P, P, P, P, P,
+                                        ctypes.c_float, P, P, P, ctypes.c_size_t, P]
     lib.gdn_decode_layer.restype = ctypes.c_int
     lib.gdn_decode_layer.argtypes = [S, ctypes.POINTER(GdnLayerParams), P, P, P, P, P, P, P, P, P,
                                      P, ctypes.c_float, P, P, P, P]
@@ -397,16 +400,10 @@ def gdn_scan_window(q, k, v, a, b, A_log, dt_bias, state_in=None, scale: float =
     return o, window
 
 
-def gdn_scan_variant(q, k, v, a=None, b=None, A_log=None, dt_bias=None, state_in=None,
-                     cu_seqlens=None, scale: float = 0.0, *, rule: str = "gated_delta",
-                     decay_per_key: bool = False, beta_shared: bool = False, o=None,
-                     state_out=None, stream=None):
-    """gdn_prefill with another update rule ("gated_delta", "delta", "gated", "linear"),
-    per-key-dim decay (a [B,T,h_v,d_k]; A_log, dt_bias [h_v,d_k]) or one beta for all
-    heads (b [B,T,1]).  a, A_log, dt_bias are unused (may be None) by rules without
-    decay, b by rules without the delta term.  Returns (o, state_out); ``state_out``
-    may be ``state_in`` itself (an in-place update)."""
-    lib = load()
+def _variant_args(q, k, v, a, b, A_log, dt_bias, state_in, cu_seqlens, rule, decay_per_key,
+                  beta_shared, o, state_out):
+    """Validate a variant call; returns (shape, variant, o, state_out, the pointers a, b,
+    A_log, dt_bias the rule reads)."""
     if rule not in RULES:
         raise GdnError(GDN_ERR_INVALID_ARG, f"unknown rule {rule!r}")
     shape = _shape_of(q, v, cu_seqlens)
@@ -417,6 +414,7 @@ def gdn_scan_variant(q, k, v, a=None, b=None, A_log=None, dt_bias=None, state_in
         raise GdnError(GDN_ERR_INVALID_ARG, "k must match q")
     lead = tuple(v.shape[:2])
     decay = rule in ("gated_delta", "gated")
+    delta = rule in ("gated_delta", "delta")
     if decay:
         _need_cuda("a", a, dt)
         _need_cuda("A_log", A_log, torch.float32)
@@ -425,7 +423,7 @@ def gdn_scan_variant(q, k, v, a=None, b=None, A_log=None, dt_bias=None, state_in
         if tuple(a.shape) != lead + per or tuple(A_log.shape) != per or \
                 tuple(dt_bias.shape) != per:
             raise GdnError(GDN_ERR_INVALID_ARG, f"a must be {lead + per}, A_log and dt_bias {per}")
-    if rule in ("gated_delta", "delta"):
+    if delta:
         _need_cuda("b", b, dt)
         want = lead + ((1,) if beta_shared else (shape.h_v,))
         if tuple(b.shape) != want:
@@ -446,12 +444,48 @@ def gdn_scan_variant(q, k, v, a=None, b=None, A_log=None, dt_bias=None, state_in
     else:
         _need_cuda("state_out", state_out, torch.float32)
     var = GdnVariant(RULES[rule], int(bool(decay_per_key)), int(bool(beta_shared)))
-    _check(lib.gdn_scan_variant(ctypes.byref(shape), ctypes.byref(var), _ptr(q), _ptr(k),
-                                _ptr(v), _ptr(a if decay else None),
-                                _ptr(b if rule in ("gated_delta", "delta") else None),
-                                _ptr(A_log if decay else None), _ptr(dt_bias if decay else None),
-                                _ptr(state_in), _ptr(cu_seqlens), float(scale), _ptr(o),
+    gates = (_ptr(a if decay else None), _ptr(b if delta else None),
+             _ptr(A_log if decay else None), _ptr(dt_bias if decay else None))
+    return shape, var, o, state_out, gates
+
+
+def gdn_scan_variant(q, k, v, a=None, b=None, A_log=None, dt_bias=None, state_in=None,
+                     cu_seqlens=None, scale: float = 0.0, *, rule: str = "gated_delta",
+                     decay_per_key: bool = False, beta_shared: bool = False, o=None,
+                     state_out=None, stream=None):
+    """gdn_prefill with another update rule ("gated_delta", "delta", "gated", "linear"),
+    per-key-dim decay (a [B,T,h_v,d_k]; A_log, dt_bias [h_v,d_k]) or one beta for all
+    heads (b [B,T,1]), on the token-sequential kernel.  a, A_log, dt_bias are unused (may
+    be None) by rules without decay, b by rules without the delta term.  Returns
+    (o, state_out); ``state_out`` may be ``state_in`` itself (an in-place update)."""
+    lib = load()
+    shape, var, o, state_out, gates = _variant_args(q, k, v, a, b, A_log, dt_bias, state_in,
+                                                    cu_seqlens, rule, decay_per_key, beta_shared,
+                                                    o, state_out)
+    _check(lib.gdn_scan_variant(ctypes.byref(shape), ctypes.byref(var), _ptr(q), _ptr(k), _ptr(v),
+                                *gates, _ptr(state_in), _ptr(cu_seqlens), float(scale), _ptr(o),
                                 _ptr(state_out), _stream(stream)))
+    return o, state_out
+
+
+def gdn_prefill_variant(q, k, v, a=None, b=None, A_log=None, dt_bias=None, state_in=None,
+                        cu_seqlens=None, scale: float = 0.0, *, rule: str = "gated_delta",
+                        decay_per_key: bool = False, beta_shared: bool = False, o=None,
+                        state_out=None, workspace=None, stream=None):
+    """gdn_scan_variant on gdn_prefill's path: the chunked tensor-core prefill for 16-bit
+    I/O at d_k = d_v = 128 (any rule, shared or per-head beta), the token-sequential
+    kernel for per-key-dim decay or other shapes.  ``workspace`` as gdn_prefill's."""
+    lib = load()
+    shape, var, o, state_out, gates = _variant_args(q, k, v, a, b, A_log, dt_bias, state_in,
+                                                    cu_seqlens, rule, decay_per_key, beta_shared,
+                                                    o, state_out)
+    need = int(lib.gdn_prefill_workspace_bytes(ctypes.byref(shape)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=v.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.gdn_prefill_variant(ctypes.byref(shape), ctypes.byref(var), _ptr(q), _ptr(k), _ptr(v),
+                                   *gates, _ptr(state_in), _ptr(cu_seqlens), float(scale), _ptr(o),
+                                   _ptr(state_out), _ptr(workspace), ws_bytes, _stream(stream)))
     return o, state_out
 
 
