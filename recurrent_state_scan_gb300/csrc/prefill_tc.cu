@@ -12,15 +12,16 @@
 // re-association of the same sums, exact up to rounding.
 //
 // Two kernels, stream-ordered:
-//  * gdn_chunk_prep -- one CTA per (chunk, value head), all in parallel, three CTAs to an
-//    SM: everything that does not depend on the state.  Gates and their prefix sums,
+//  * gdn_chunk_prep -- persistent CTAs, three to an SM, walk the (chunk, value head)
+//    items: everything that does not depend on the state.  Gates and their prefix sums,
 //    D1 = [K; Q] K^T (tcgen05), A and P, T = (I + A)^-1 (fp32 diagonal blocks, tf32
 //    warp-MMA merges), D2 = [T'; T''] K -> W and D3 = [T'; T''] V -> U (tcgen05), and
-//    for the scan's lookahead W' = gamma_C(prev) W and M = W K_prev^T diag(e^{G_C - G}).
-//    It writes one workspace record per (chunk, head): images of W', [P; M], U and the
-//    gate values, laid out exactly as the scan loads them.
+//    for the scan's lookahead M = W K_prev^T diag(e^{G_C - G}) against the previous
+//    chunk's keys.  It writes one workspace record per (chunk, head): images of W, [P; M],
+//    U and the gate values, laid out exactly as the scan loads them (the scan applies
+//    gamma_C of the previous chunk to the W S rows in fp32).
 //  * gdn_chunk_scan -- one CTA per (sequence, value head, half of the 128 state columns),
-//    walking the sequence's chunks in order: D4 = [Q; W'] S0 (tcgen05),
+//    walking the sequence's chunks in order: D4 = [Q; W] S0 (tcgen05),
 //    Delta = U - W S0, DS = K^T diag(e^{G_C-G}) Delta and X = [P; M] Delta (tcgen05),
 //    S = gamma_C S0 + DS with S in fp32 registers, o = scale gamma (Q S0) + P Delta by
 //    TMA store.  Records, Q and K arrive by bulk copy / TMA into two stages, one chunk
@@ -364,9 +365,15 @@ struct PrepCtl {
 // M = W K_{c-1}^T, each read out before the next is issued.  While an item's diagonal
 // blocks are inverted, one thread looks up the CTA's next item.  (Prefetching the next
 // item's tiles into L2 there was measured slower.)
-template <typename IO>
+// kVariant: the update-rule switches and the shared beta are read from the parameters;
+// without it the gated delta rule with one beta per head is compiled in (the switches
+// cost the default rule about 5% when they were runtime values).
+template <typename IO, bool kVariant>
 __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_constant__ TcParams p) {
     constexpr bool kBf16 = std::is_same<IO, __nv_bfloat16>::value;
+    const bool has_decay = !kVariant || p.has_decay != 0;
+    const bool has_delta = !kVariant || p.has_delta != 0;
+    const bool beta_shared = kVariant && p.beta_shared != 0;
     constexpr uint32_t kIdD1 = idesc_f16(kBf16, 128, 64, false, false);
     constexpr uint32_t kIdD2 = idesc_f16(kBf16, 128, 128, false, true);
 
@@ -439,22 +446,22 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
     // from plain loads of the logits while K and Q are in flight.
     float ra = 0.f, rb = 0.f, rap = 0.f;
     if (pt < Lc) {
-        if (p.has_decay) ra = IoType<IO>::ld(static_cast<const IO *>(p.a) + (size_t)(tc0 + pt) * p.h_v + h);
-        if (p.has_delta)
+        if (has_decay) ra = IoType<IO>::ld(static_cast<const IO *>(p.a) + (size_t)(tc0 + pt) * p.h_v + h);
+        if (has_delta)
             rb = IoType<IO>::ld(static_cast<const IO *>(p.b) +
-                                (p.beta_shared ? (size_t)(tc0 + pt) : (size_t)(tc0 + pt) * p.h_v + h));
+                                (beta_shared ? (size_t)(tc0 + pt) : (size_t)(tc0 + pt) * p.h_v + h));
     }
-    if (!first && pt < kC && p.has_decay)
+    if (!first && pt < kC && has_decay)
         rap = IoType<IO>::ld(static_cast<const IO *>(p.a) + (size_t)(tc0 - kC + pt) * p.h_v + h);
     bool ok = true, failed = false;
     {
         float gsum = 0.f, be = 0.f, gsum_p = 0.f;
         if (pt < kC) {
             if (pt < Lc) {
-                gsum = p.has_decay ? decay_f(ra, p.A_log[h], p.dt_bias[h]) : 0.f;
-                be = p.has_delta ? sigmoid_f(rb) : 1.f;
+                gsum = has_decay ? decay_f(ra, p.A_log[h], p.dt_bias[h]) : 0.f;
+                be = has_delta ? sigmoid_f(rb) : 1.f;
             }
-            if (!first && p.has_decay) gsum_p = decay_f(rap, p.A_log[h], p.dt_bias[h]);
+            if (!first && has_decay) gsum_p = decay_f(rap, p.A_log[h], p.dt_bias[h]);
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const float y = __shfl_up_sync(0xffffffffu, gsum, off);
@@ -537,7 +544,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
                     for (int e = 0; e < 4; ++e) {
                         const int j = 32 * hf + 4 * j4 + e;
                         const float d = safe ? Ei * ctl.F[j] : __expf(Gi - ctl.G[j]);
-                        x[e] = (j < i && p.has_delta) ? bi * d * __uint_as_float(r[4 * j4 + e]) : 0.f;
+                        x[e] = (j < i && has_delta) ? bi * d * __uint_as_float(r[4 * j4 + e]) : 0.f;
                     }
                     *reinterpret_cast<float4 *>(As + i * kAs + 32 * hf + 4 * j4) =
                         make_float4(x[0], x[1], x[2], x[3]);
@@ -574,7 +581,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
         auto next_item = [&](int t) {
             if (t == 0) ctl.nxt = prep_item(p, item + gridDim.x);
         };
-        invert_chunk<IO>(As, sm + PP_TT, ctl.beta, ctl.gam, p.has_delta ? 1.f : 0.f, pt, next_item);
+        invert_chunk<IO>(As, sm + PP_TT, ctl.beta, ctl.gam, has_delta ? 1.f : 0.f, pt, next_item);
         fence_async_smem();
         tc_fence_before();
         named_bar(kBarPrep, kPrepThreads);
@@ -1646,11 +1653,17 @@ cudaError_t configure() {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(gdn_chunk_prep<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(gdn_chunk_prep<IO, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kPrepSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gdn_chunk_prep<IO, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
         // Three prep CTAs to an SM need the largest shared-memory carve-out.
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gdn_chunk_prep<IO>, cudaFuncAttributePreferredSharedMemoryCarveout,
+            e = cudaFuncSetAttribute(gdn_chunk_prep<IO, false>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gdn_chunk_prep<IO, true>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      (int)cudaSharedmemCarveoutMaxShared);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(gdn_chunk_scan<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1666,7 +1679,7 @@ cudaError_t configure() {
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
-        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, gdn_chunk_prep<IO>);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, gdn_chunk_prep<IO, false>);
         if (e != cudaSuccess) return e;
         const int per_cta = kPrepSmem + (int)fa.sharedSizeBytes + reserved;
         int per_sm = per_cta > 0 ? smem_sm / per_cta : 0;
@@ -1692,7 +1705,10 @@ cudaError_t launch_prep(const TcParams &tp, int64_t items, cudaStream_t stream) 
     // Persistent CTAs pay off on long item lists; up to three items per resident CTA, one
     // CTA per item leaves a shorter tail.
     const int64_t ctas = items <= 3 * (int64_t)slots ? items : slots;
-    gdn_chunk_prep<IO><<<(unsigned)ctas, kPrepThreads, kPrepSmem, stream>>>(pk);
+    if (tp.has_decay && tp.has_delta && !tp.beta_shared)
+        gdn_chunk_prep<IO, false><<<(unsigned)ctas, kPrepThreads, kPrepSmem, stream>>>(pk);
+    else
+        gdn_chunk_prep<IO, true><<<(unsigned)ctas, kPrepThreads, kPrepSmem, stream>>>(pk);
     return cudaGetLastError();
 }
 
