@@ -478,7 +478,11 @@ def main_neighbour(args, rank, world, local):
 
     pk, pk_kind = peaks()
     gbs = nbytes / (ms / 1e3) / 1e9
-    kernel = "gdn::causal_conv_kernel" if conv else "gdn::gated_rmsnorm_kernel"
+    if conv:   # the kernel that takes the workload's shape (16-bit, channels last)
+        kernel = ("gdn::causal_conv_decode_stream_kernel" if inp.spec.decode
+                  else "gdn::causal_conv_bulk_kernel")
+    else:
+        kernel = "gdn::gated_rmsnorm_rows_kernel"
     line = {
         "metric": METRIC, "value": world * gbs, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -697,6 +701,192 @@ def main_layer(args, rank, world, local):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------- prefill + gated norm
+
+def prefill_norm_io_bytes(inp) -> dict:
+    """The prefill's bytes with o replaced by y, plus the gate and the norm scale."""
+    p = inp.prefill
+    b = io_bytes(p)
+    es = p.v.element_size()
+    y = b.pop("o")
+    return dict(b, gate=y, y=y, norm_scale=p.spec.d_v * es)
+
+
+def prefill_norm_oracle(inp, tokens: int):
+    """The float64 oracle chain over the first sequences that hold `tokens` tokens: the
+    scan, o rounded to the I/O type, the gated RMS norm.  Returns the tokens covered."""
+    import oracle
+    p, s = inp.prefill, inp.prefill.spec
+    cu = [int(c) for c in p.cu_seqlens]
+    n = 1
+    while n < p.n_seq and cu[n] < tokens:
+        n += 1
+    T = int(cu[n])
+    f = {k: v for k, v in ((k, getattr(p, k)) for k in ("q", "k", "v", "a", "b"))}
+    q = f["q"].reshape(-1, s.h_qk, s.d_k)[:T].double().numpy()
+    k = f["k"].reshape(-1, s.h_qk, s.d_k)[:T].double().numpy()
+    v = f["v"].reshape(-1, s.h_v, s.d_v)[:T].double().numpy()
+    a = f["a"].reshape(-1, s.h_v)[:T].double().numpy()
+    b = f["b"].reshape(-1, s.h_v)[:T].double().numpy()
+    st = None if p.state_in is None else p.state_in[:n].double().numpy()
+    o, _ = oracle.scan(np.asarray(cu[:n + 1]), s.h_qk, s.h_v, s.d_k, s.d_v, q, k, v, a=a, b=b,
+                       A_log=p.A_log.double().numpy(), dt_bias=p.dt_bias.double().numpy(),
+                       state_in=st, scale=p.scale, threads=cpu_threads())
+    o_io = torch.from_numpy(np.ascontiguousarray(o)).to(p.v.dtype).double().numpy()
+    g = inp.gate.reshape(-1, s.h_v, s.d_v)[:T].double().numpy()
+    oracle.gated_rmsnorm(o_io.reshape(-1, s.d_v), inp.norm_scale.double().numpy(),
+                         g.reshape(-1, s.d_v), inp.spec.eps, inp.spec.activation)
+    return T
+
+
+def time_prefill_norm_oracle(inp, budget_s: float, min_reps: int = 1, tokens: int = 4096):
+    reps, t0, done = 0, time.perf_counter(), 0
+    while reps < min_reps or time.perf_counter() - t0 < budget_s:
+        done = prefill_norm_oracle(inp, tokens)
+        reps += 1
+    return (time.perf_counter() - t0) / reps, reps, done
+
+
+def main_prefill_norm(args, rank, world, local):
+    inp = workloads.any_workload(args.workload)
+    p, s = inp.prefill, inp.prefill.spec
+    nbytes = int(sum(prefill_norm_io_bytes(inp).values()))
+    config = dict(config_of(p, world), workload=inp.spec.name,
+                  op="packed prefill, then the gated RMS norm (silu gate) of each head's "
+                     "output row: gdn_prefill_norm, the norm in the scan's readout",
+                  norm={"eps": inp.spec.eps, "activation": inp.spec.activation})
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        for _ in range(args.warmup):
+            time_prefill_norm_oracle(inp, 0.0)
+        per, reps, done = time_prefill_norm_oracle(inp, 0.0, min_reps=args.steps)
+        value = done / per
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config,
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(),
+                             "kind": "oracle",
+                             "sample": f"the first {done} of {p.total_tokens} tokens per step "
+                                       f"(whole sequences), {reps} steps"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}), flush=True)
+        return
+
+    from recurrent_state_scan_gb300 import (gdn, gdn_gated_rmsnorm, gdn_prefill, gdn_prefill_norm,
+                                            load)
+    load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    t = {n: getattr(p, n).to(dev) for n in ("q", "k", "v", "a", "b", "A_log", "dt_bias")}
+    t["gate"], t["norm_scale"] = inp.gate.to(dev), inp.norm_scale.to(dev)
+    state0 = None if p.state_in is None else p.state_in.to(dev)
+    cu = torch.tensor(p.cu_seqlens, dtype=torch.int32, device=dev) if p.varlen else None
+    y = torch.empty(t["v"].shape, dtype=t["v"].dtype, device=dev)
+    o = torch.empty_like(y)
+    state_out = torch.empty((p.n_seq, s.h_v, s.d_k, s.d_v), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, gdn.gdn_prefill_workspace_bytes(gdn.shape_of_spec(s, p.n_seq,
+                                                                               p.total_tokens))),
+                     dtype=torch.uint8, device=dev)
+    eps, act = inp.spec.eps, inp.spec.activation
+
+    def call(d):
+        gdn_prefill_norm(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], state0,
+                         cu, p.scale, norm_scale=d["norm_scale"], gate=d["gate"], eps=eps,
+                         activation=act, y=y, state_out=state_out, workspace=ws, stream=stream)
+
+    def separate(d):
+        gdn_prefill(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], state0, cu,
+                    p.scale, o=o, state_out=state_out, workspace=ws, stream=stream)
+        gdn_gated_rmsnorm(o, d["norm_scale"], d["gate"], eps, act, y=y, stream=stream)
+
+    def timed(fn, d):
+        for _ in range(args.warmup):
+            flush.zero_()
+            fn(d)
+        torch.cuda.synchronize(dev)
+        st = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        en = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            flush.zero_()
+            st[i].record(stream)
+            fn(d)
+            en[i].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        return max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in zip(st, en)])), world)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    ms = timed(call, t)
+    clocks = sampler.stop() if sampler else None
+    ms_sep = timed(separate, t)
+
+    e2e = None
+    if not args.no_e2e:
+        # Pinned host inputs (q, k, v, a, b, the gate) in, y and the state out.
+        host = {n: getattr(p, n).pin_memory() for n in ("q", "k", "v", "a", "b")}
+        host["gate"] = inp.gate.pin_memory()
+        dbuf = dict(t)
+        for n, v in host.items():
+            dbuf[n] = torch.empty_like(v, device=dev)
+        y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        s_host = torch.empty(state_out.shape, dtype=torch.float32).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = y_host.numel() * y_host.element_size() + s_host.numel() * 4
+
+        def e2e_step(d):
+            for n, v in host.items():
+                d[n].copy_(v, non_blocking=True)
+            call(d)
+            y_host.copy_(y, non_blocking=True)
+            s_host.copy_(state_out, non_blocking=True)
+
+        ems = timed(e2e_step, dbuf)
+        e2e = {"value": world * p.total_tokens / (ems / 1e3), "unit": "tokens/s",
+               "ms_per_step": ems, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    pk, pk_kind = peaks()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": world * p.total_tokens / (ms / 1e3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype_of(p),
+        "data": "synthetic", "config": config,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm_gbs"],
+                     "traffic": profiled_traffic(args.workload, "prefill"),
+                     "peak_source": f"{pk_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+                     if pk_kind == "measured" else "fallback 6.8 TB/s",
+                     "kernels": "gdn_chunk_prep + gdn_chunk_scan with the norm (cluster pairs), "
+                                "one call"},
+        "separate_calls": {"ms_per_step": ms_sep, "launches": 3,
+                           "calls": "gdn_prefill (prep, scan), gdn_gated_rmsnorm"},
+        "gpu_launches": args.steps * 2,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if clocks is not None:
+        line["clocks"] = clocks
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        per, reps, done = time_prefill_norm_oracle(inp, 10.0)
+        line["cpu_baseline"] = {"value": done / per, "unit": "tokens/s", "cores": cpu_threads(),
+                                "kind": "oracle",
+                                "sample": f"the first {done} of {p.total_tokens} tokens (whole "
+                                          f"sequences) x{reps} through the float64 C oracle "
+                                          f"chain, {per * reps:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, local, name=None, with_e2e=True):
@@ -843,6 +1033,8 @@ def main():
     inp_name = args.workload
     if inp_name in workloads.LAYER_WORKLOADS:
         return main_layer(args, rank, world, local)
+    if inp_name in workloads.PREFILL_NORM_WORKLOADS:
+        return main_prefill_norm(args, rank, world, local)
     if inp_name not in workloads.WORKLOADS:
         return main_neighbour(args, rank, world, local)
     if args.impl == "reference":

@@ -41,7 +41,8 @@
  * pool), gdn_scan_window (the states after each of the last W steps),
  * gdn_scan_variant and gdn_prefill_variant (other update rules and gate layouts),
  * the layer ops around the scan: gdn_causal_conv, gdn_causal_conv_slots and
- * gdn_gated_rmsnorm, and gdn_decode_layer (conv -> decode step -> norm in one kernel).
+ * gdn_gated_rmsnorm, gdn_prefill_norm (the prefill with the norm in its readout) and
+ * gdn_decode_layer (conv -> decode step -> norm in one kernel).
  *  - gdn_last_error_message() gives a human-readable detail of the last
  *    non-OK status returned on the calling thread.
  */
@@ -333,6 +334,34 @@ gdn_status gdn_gated_rmsnorm(int32_t io_dtype, int64_t rows, int32_t width, cons
                              int32_t activation, void *y, void *stream);
 
 /*
+ * gdn_prefill_norm -- gdn_prefill followed by the gated RMS norm of its output over each
+ * d_v row, the two steps on either side of o in the layer (the CUDA page's
+ * linear_attention_core Steps 1-4, then the onnxruntime-ep-mlx ssm.rs page's
+ * GatedRMSNorm): y[t, h, :] = o * rsqrt(mean(o^2) + epsilon) * norm_scale * act(gate[t, h, :]),
+ * with o rounded to the I/O type first, as gdn_prefill would store it, and act as in
+ * gdn_gated_rmsnorm.
+ *   norm_scale  DEVICE [d_v], io dtype.
+ *   gate        DEVICE, o's layout ([B, T, h_v, d_v], or packed), io dtype; must not
+ *               overlap y (GDN_ERR_INVALID_ARG).
+ *   epsilon     finite and >= 0; activation GDN_ACT_SILU or GDN_ACT_SIGMOID.
+ *   y           DEVICE, o's layout.  o itself is not an output.
+ *   the rest    as gdn_prefill (workspace sized by gdn_prefill_workspace_bytes).
+ * On the chunked tensor-core path (16-bit I/O, d_k = d_v = 128) with a 16-byte aligned
+ * gate, the norm runs in the state scan's readout: the two CTAs that own a head's two
+ * 64-column halves of the state run as a thread-block cluster and exchange each row's sum
+ * of squares through shared memory, so o never reaches global memory; that path never
+ * takes the time-parallel scan.  Elsewhere the norm is a second launch, in place on y.
+ * Errors: gdn_prefill's, and gdn_gated_rmsnorm's argument rules.
+ */
+gdn_status gdn_prefill_norm(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                            const void *a, const void *b, const float *A_log,
+                            const float *dt_bias, const float *state_in,
+                            const int32_t *cu_seqlens, float scale, const void *norm_scale,
+                            const void *gate, float epsilon, int32_t activation, void *y,
+                            float *state_out, void *workspace, size_t workspace_bytes,
+                            void *stream);
+
+/*
  * gdn_layer_params -- the neighbouring ops of gdn_decode_layer.
  */
 typedef struct gdn_layer_params {
@@ -397,11 +426,12 @@ gdn_status gdn_prefill_plan(const gdn_shape *shape, int32_t *path, int32_t *laun
 /*
  * gdn_set_wait_budget -- a test hook, process-wide and not part of the operation: the
  * cycles a bounded wait of the tensor-core prefill kernels (chunk prep and state scan)
- * may take before the waiting CTA gives up, for gdn_prefill calls made after it
- * (0 = the default, about two seconds).  A wait that runs out makes the CTA let the
- * copies and MMAs it has issued finish under the full two-second budget, free its
- * tensor memory and leave; gdn_last_device_status() then returns GDN_ERR_TIMEOUT and
- * the call's outputs are undefined.  Nothing is left running or waiting on the device.
+ * or of the causal conv's bulk-copy pipeline (16-bit rows of 64 tokens or more) may take
+ * before the waiting CTA gives up, for calls made after it (0 = the default, about two
+ * seconds).  A wait that runs out makes the CTA let the copies and MMAs it has issued
+ * finish under the full two-second budget, free its tensor memory and leave;
+ * gdn_last_device_status() then returns GDN_ERR_TIMEOUT and the call's outputs are
+ * undefined.  Nothing is left running or waiting on the device.
  * A negative value returns GDN_ERR_INVALID_ARG.
  */
 gdn_status gdn_set_wait_budget(int64_t cycles);

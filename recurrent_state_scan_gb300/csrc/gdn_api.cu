@@ -189,6 +189,18 @@ gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, con
                         state_out, workspace, workspace_bytes, true, stream);
 }
 
+gdn_status gdn_prefill_norm(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                            const void *a, const void *b, const float *A_log,
+                            const float *dt_bias, const float *state_in,
+                            const int32_t *cu_seqlens, float scale, const void *norm_scale,
+                            const void *gate, float epsilon, int32_t activation, void *y,
+                            float *state_out, void *workspace, size_t workspace_bytes,
+                            void *stream) {
+    const NormEpilogue norm{norm_scale, gate, epsilon, activation};
+    return prefill_impl(shape, q, k, v, a, b, A_log, dt_bias, state_in, cu_seqlens, scale, y,
+                        state_out, workspace, workspace_bytes, true, stream, nullptr, &norm);
+}
+
 }  // extern "C"
 
 size_t gdn::prefill_records_bytes(const gdn_shape *shape) {
@@ -208,7 +220,8 @@ gdn_status gdn::prefill_impl(const gdn_shape *shape, const void *q, const void *
                              const void *a, const void *b, const float *A_log, const float *dt_bias,
                              const float *state_in, const int32_t *cu_seqlens, float scale, void *o,
                              float *state_out, void *workspace, size_t workspace_bytes,
-                             bool allow_overlap, void *stream, const gdn_variant *variant) {
+                             bool allow_overlap, void *stream, const gdn_variant *variant,
+                             const NormEpilogue *norm) {
     gdn_status st = check_shape(shape, cu_seqlens != nullptr);
     if (st != GDN_OK) return st;
     const int64_t tokens = cu_seqlens ? shape->seqlen : shape->seqlen * (int64_t)shape->batch;
@@ -218,6 +231,22 @@ gdn_status gdn::prefill_impl(const gdn_shape *shape, const void *q, const void *
         st = check_variant(shape, variant, tokens, q, k, v, a, b, A_log, dt_bias, o);
     }
     if (st != GDN_OK) return st;
+    const size_t es = io_size(shape->io_dtype);
+    if (norm != nullptr) {
+        if (norm->activation != GDN_ACT_SILU && norm->activation != GDN_ACT_SIGMOID)
+            return fail(GDN_ERR_INVALID_ARG, "the norm's activation is SILU or SIGMOID");
+        if (!(norm->eps >= 0.0f) || isinf(norm->eps))
+            return fail(GDN_ERR_INVALID_ARG, "epsilon must be finite and >= 0");
+        if (tokens > 0) {
+            if (!norm->scale || !norm->gate) return fail(GDN_ERR_INVALID_ARG, "norm_scale or gate is NULL");
+            if (!aligned(norm->scale, es) || !aligned(norm->gate, es))
+                return fail(GDN_ERR_INVALID_ARG, "norm_scale/gate is not %zu-byte aligned", es);
+            const size_t bytes = (size_t)tokens * shape->h_v * shape->d_v * es;
+            const uintptr_t g0 = reinterpret_cast<uintptr_t>(norm->gate), y0 = reinterpret_cast<uintptr_t>(o);
+            if (g0 < y0 + bytes && y0 < g0 + bytes)
+                return fail(GDN_ERR_INVALID_ARG, "y overlaps gate");
+        }
+    }
     if (shape->num_seqs == 0) return GDN_OK;
     if (state_out == nullptr) return fail(GDN_ERR_INVALID_ARG, "state_out is NULL");
     if (!aligned(state_out, 16) || !aligned(state_in, 16))
@@ -244,7 +273,15 @@ gdn_status gdn::prefill_impl(const gdn_shape *shape, const void *q, const void *
     }
     const gdn_dtype io = (gdn_dtype)shape->io_dtype;
     cudaError_t e;
+    bool norm_after = norm != nullptr && tokens > 0;   // the norm as its own launch, in place
     if (!p.decay_per_key && prefill_tc_supported(p, io, tokens)) {
+        if (norm_after && aligned(norm->gate, 16)) {
+            p.norm_scale = norm->scale;
+            p.norm_gate = norm->gate;
+            p.norm_eps = norm->eps;
+            p.norm_silu = norm->activation == GDN_ACT_SILU;
+            norm_after = false;
+        }
         const size_t need = prefill_tc_workspace(cu_seqlens != nullptr, shape->seqlen, shape->batch,
                                                  shape->num_seqs, shape->h_v);
         if (workspace == nullptr || workspace_bytes < need)
@@ -257,6 +294,15 @@ gdn_status gdn::prefill_impl(const gdn_shape *shape, const void *q, const void *
     } else {
         e = launch_scan_simt(p, io, (cudaStream_t)stream);
         if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    }
+    if (norm_after) {
+        bool vec4 = shape->d_v % 4 == 0;
+        const void *ptrs[] = {o, norm->scale, norm->gate};
+        for (const void *ptr : ptrs)
+            if (!aligned(ptr, 4 * es)) vec4 = false;
+        e = launch_gated_rmsnorm(io, tokens * shape->h_v, shape->d_v, o, norm->scale, norm->gate,
+                                 norm->eps, norm->activation, o, vec4, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "gated RMS norm launch");
     }
     return GDN_OK;
 }

@@ -7,6 +7,7 @@
 // its gates wide and casts once; here g and beta are never stored at all).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -38,6 +39,11 @@ struct ScanParams {
     int32_t rule;                // gdn_rule: 0 gated_delta, 1 delta, 2 gated, 3 linear
     int32_t decay_per_key;       // a [.., h_v, d_k], A_log / dt_bias [h_v, d_k]
     int32_t beta_shared;         // b [.., 1]: one beta for every head
+    // Gated RMS norm of o fused into the tensor-core scan's readout (norm_gate set): o is
+    // then written as y = o / rms(o) * norm_scale * act(gate) over each d_v row.
+    const void *norm_scale, *norm_gate;
+    float norm_eps;
+    int32_t norm_silu;           // act = silu (1) or sigmoid (0)
 };
 
 // ------------------------------------------------------------------ I/O types
@@ -164,13 +170,30 @@ cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_t
 // up (0: about two seconds), set by gdn_set_wait_budget.
 extern long long g_wait_budget;
 
+// A TMA tensor map over a 3-D tensor of 16-bit values (dims innermost first, the two outer
+// strides in bytes, multiples of 16), no swizzle, out-of-range elements read as zero.
+// False when the driver's encoder is missing or rejects the arguments.
+bool encode_map_3d(CUtensorMap *m, const void *base, gdn_dtype io, const uint64_t dims[3],
+                   const uint64_t strides[2], const uint32_t box[3]);
+
+// The gated RMS norm applied to o after the scan (gdn_prefill_norm).
+struct NormEpilogue {
+    const void *scale;   // [d_v]
+    const void *gate;    // like o
+    float eps;
+    int32_t activation;  // GDN_ACT_SILU or GDN_ACT_SIGMOID
+};
+
 // gdn_prefill with the segment overlap allowed or not (no internal stream is created
-// when it is not), and optionally a gate / rule variant (per-key decay runs on the
-// token-sequential kernel, everything else on the path gdn_prefill would take).
+// when it is not), optionally a gate / rule variant (per-key decay runs on the
+// token-sequential kernel, everything else on the path gdn_prefill would take), and
+// optionally the gated RMS norm of o (fused into the tensor-core scan's readout; after the
+// scan, in place, on the other paths).
 gdn_status prefill_impl(const gdn_shape *shape, const void *q, const void *k, const void *v,
                         const void *a, const void *b, const float *A_log, const float *dt_bias,
                         const float *state_in, const int32_t *cu_seqlens, float scale, void *o,
                         float *state_out, void *workspace, size_t workspace_bytes,
-                        bool allow_overlap, void *stream, const gdn_variant *variant = nullptr);
+                        bool allow_overlap, void *stream, const gdn_variant *variant = nullptr,
+                        const NormEpilogue *norm = nullptr);
 
 }  // namespace gdn

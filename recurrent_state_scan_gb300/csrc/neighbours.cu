@@ -20,7 +20,10 @@
 // Gated RMS norm (onnxruntime-ep-mlx 0.31.1, src/ops/ssm.rs, `gated_rms_norm_op`): one
 // warp per row of `width` values; y = x * rsqrt(mean(x^2) + eps) * scale * act(gate),
 // act = silu or sigmoid, all in fp32, rounded once to the I/O dtype.
+#include <type_traits>
+
 #include "gdn_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace gdn {
 namespace {
@@ -521,6 +524,223 @@ __global__ void __launch_bounds__(256, 3) causal_conv_staged_kernel(const ConvPa
     }
 }
 
+// Long rows of 16-bit values on the staged kernel's shapes, with the copies and the
+// arithmetic cut down to what the bytes need.  A CTA owns kStagedWidth channels of one
+// row over kStagedChunk tokens, in stages of kStagedTokens + 3 rows (tokens t - 3 ..
+// t + 31 of the stage starting at t), kTmaDepth stages deep.
+//  - Warp 0 brings a stage in with one TMA tensor copy (a 256-channel x 35-token box of x;
+//    tokens past the row read as zero) counted on the stage's `full` barrier.  The first
+//    stage of a row's first chunk copies tokens 0 .. 31 and its lanes write the three rows
+//    before them from the past state (or zeros) themselves; every lane of warp 0 arrives
+//    on `full`, so those stores are seen by whoever waits on it.
+//  - Each warp computes from a stage once `full` completes and then arrives on the
+//    stage's `empty` barrier; warp 0 refills a buffer once all eight warps have released
+//    it.  No CTA-wide barrier runs per stage.
+//  - Thread (cg, tg) computes 8 channels x 4 tokens: one 16-byte shared-memory load per
+//    window row and one 16-byte store per token, so a warp's store is a whole 512-byte
+//    row.  The taps (K = KT) and the activation are compile-time.  The sum is the staged
+//    kernel's: fp32, oldest tap first, then the bias, rounded once.
+//  - Every wait is bounded; a wait that runs out stops the CTA, whose warp 0 first lets
+//    the copies it issued land.
+constexpr int kTmaDepth = 4;
+constexpr int kTmaRows = kStagedTokens + 3;
+// Cycles (about two seconds) a wait may take by default, and always when a CTA that gave
+// up lets its own copies land.
+constexpr long long kConvDrainBudget = 4000000000LL;
+
+// Wait for phase `parity` of `bar` for at most `budget` cycles (or until `abort` is set),
+// polling with a short sleep: a blocking try_wait could hold the thread past the budget.
+__device__ __forceinline__ bool conv_wait(uint64_t *bar, uint32_t parity, long long budget,
+                                          volatile int *abort) {
+    const uint32_t addr = tc::smem_u32(bar);
+    const long long t0 = clock64();
+    for (;;) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if ((abort != nullptr && *abort) || clock64() - t0 > budget) return false;
+        __nanosleep(32);
+    }
+}
+
+struct ConvTmaMaps {
+    CUtensorMap stage;   // box 256 channels x 35 tokens x 1 row of x [B][L][C]
+    CUtensorMap first;   // box 256 x 32 x 1: a row's first stage, after the past rows
+};
+
+template <typename IO, int KT, bool SILU>
+__global__ void __launch_bounds__(256, 2)
+causal_conv_tma_kernel(const ConvParams p, const __grid_constant__ ConvTmaMaps maps, long long budget) {
+    static_assert(sizeof(IO) == 2, "16-bit I/O");
+    constexpr int ROWB = kStagedWidth * 2;
+    constexpr int BUFB = kTmaRows * ROWB;
+    extern __shared__ unsigned char smem_raw[];   // kTmaDepth x kTmaRows x ROWB, + 128
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+    __shared__ uint64_t full[kTmaDepth], empty[kTmaDepth];
+    __shared__ int abort_flag;
+    volatile int *abort = &abort_flag;
+    const IO *x = static_cast<const IO *>(p.x);
+    const IO *w = static_cast<const IO *>(p.w);
+    const IO *bias = static_cast<const IO *>(p.bias);
+    const IO *past = static_cast<const IO *>(p.state_in);
+    IO *y = static_cast<IO *>(p.y);
+    IO *sout = static_cast<IO *>(p.state_out);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t cbase = (int64_t)blockIdx.x * kStagedWidth;
+    const int64_t chunk = blockIdx.y;
+    const int64_t b = blockIdx.z;
+    int64_t srow = b;
+    if (p.slots != nullptr) {
+        srow = p.slots[b];
+        if (srow < 0 || srow >= p.pool_size) {
+            if (chunk == 0 && blockIdx.x == 0 && tid == 0) atomicOr(p.status, kDevBadSlot);
+            return;
+        }
+    }
+    const int64_t t_begin = chunk * kStagedChunk;
+    const int64_t t_end = t_begin + kStagedChunk < p.L ? t_begin + kStagedChunk : p.L;
+    const int nstage = (int)((t_end - t_begin + kStagedTokens - 1) / kStagedTokens);
+    const int width = p.C - cbase < kStagedWidth ? (int)(p.C - cbase) : kStagedWidth;
+
+    if (tid == 0) {
+#pragma unroll
+        for (int i = 0; i < kTmaDepth; ++i) {
+            tc::mbar_init(&full[i], 32);    // every lane of warp 0
+            tc::mbar_init(&empty[i], 8);    // one arrival per warp
+        }
+        tc::fence_mbar_init();
+        abort_flag = 0;
+    }
+    __syncthreads();
+
+    // Warp 0: stage st into its buffer (after its previous use has been released).
+    auto issue = [&](int st) -> bool {
+        const int i = st % kTmaDepth;
+        if (st >= kTmaDepth &&
+            !conv_wait(&empty[i], (uint32_t)(st / kTmaDepth - 1) & 1u, budget, abort))
+            return false;
+        unsigned char *buf = smem + i * BUFB;
+        const int64_t ts = t_begin + (int64_t)st * kStagedTokens;   // first token of the stage
+        const bool first = ts == 0;
+        if (first && lane < 3) {
+            // Rows 0..2: tokens -3..-1, i.e. padded positions q = lane + carry - 3.
+            const int64_t q = lane + p.carry - 3;
+            const IO *src = (q >= 0 && past != nullptr) ? past + (srow * p.carry + q) * p.C + cbase : nullptr;
+            for (int o = 0; o < width * 2; o += 16)
+                *reinterpret_cast<uint4 *>(buf + lane * ROWB + o) =
+                    src ? *reinterpret_cast<const uint4 *>(reinterpret_cast<const unsigned char *>(src) + o)
+                        : make_uint4(0u, 0u, 0u, 0u);
+            tc::fence_async_smem();   // before later tensor copies into the same rows
+        }
+        if (lane == 0) {
+            tc::mbar_arrive_expect_tx(&full[i], first ? kStagedTokens * ROWB : BUFB);
+            if (first)
+                tc::tma_load_3d(buf + 3 * ROWB, &maps.first, (int)cbase, 0, (int)b, &full[i]);
+            else
+                tc::tma_load_3d(buf, &maps.stage, (int)cbase, (int)(ts - 3), (int)b, &full[i]);
+        } else {
+            tc::mbar_arrive(&full[i]);
+        }
+        return true;
+    };
+
+    const int cg = tid & 31, tg = tid >> 5;
+    const int64_t c0 = cbase + cg * 8;
+    const bool live = cg * 8 < width;
+    float wv[KT][8], bv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        bv[i] = 0.0f;
+#pragma unroll
+        for (int m = 0; m < KT; ++m) wv[m][i] = 0.0f;
+    }
+    if (live) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+#pragma unroll
+            for (int m = 0; m < KT; ++m) wv[m][i] = IoType<IO>::ld(w + (c0 + i) * KT + m);
+            if (bias != nullptr) bv[i] = IoType<IO>::ld(bias + c0 + i);
+        }
+    }
+
+    int issued = 0;   // warp 0: stages issued so far
+    bool ok = true;
+    if (warp == 0) {
+        if (lane == 0) tc::tma_prefetch_desc(&maps.stage);
+        for (; issued < kTmaDepth - 1 && issued < nstage; ++issued) issue(issued);
+    }
+    for (int st = 0; ok && st < nstage; ++st) {
+        if (warp == 0 && issued < nstage) {
+            if (!issue(issued)) ok = false;
+            else ++issued;
+        }
+        if (ok && !conv_wait(&full[st % kTmaDepth], (uint32_t)(st / kTmaDepth) & 1u, budget, abort))
+            ok = false;
+        if (!ok) break;
+        const unsigned char *buf = smem + (st % kTmaDepth) * BUFB;
+        const int j0 = tg * 4;
+        const int64_t t0 = t_begin + (int64_t)st * kStagedTokens + j0;
+        if (live && t0 < t_end) {
+            // Output j0 + k reads rows j0 + k + m + 4 - KT, m < KT.
+            float win[KT + 3][8];
+#pragma unroll
+            for (int r = 0; r < KT + 3; ++r) {
+                const uint4 raw =
+                    *reinterpret_cast<const uint4 *>(buf + (j0 + r + 4 - KT) * ROWB + cg * 16);
+                const IO *h = reinterpret_cast<const IO *>(&raw);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) win[r][i] = IoType<IO>::ld(h + i);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint4 raw;
+                IO *h = reinterpret_cast<IO *>(&raw);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float acc = wv[0][i] * win[k][i];
+#pragma unroll
+                    for (int m = 1; m < KT; ++m) acc = fmaf(wv[m][i], win[k + m][i], acc);
+                    acc += bv[i];
+                    IoType<IO>::st(h + i, SILU ? silu_fast(acc) : acc);
+                }
+                if (t0 + k < t_end)
+                    *reinterpret_cast<uint4 *>(y + (b * p.L + t0 + k) * p.C + c0) = raw;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&empty[st % kTmaDepth]);
+    }
+    if (!ok) {
+        *abort = 1;
+        if (tid == 0) atomicOr(p.status, kDevTimeout);
+        if (warp == 0) {
+            // Let the copies this CTA issued land before it exits: the latest phase of each
+            // buffer's `full` barrier.
+            for (int s2 = issued - kTmaDepth < 0 ? 0 : issued - kTmaDepth; s2 < issued; ++s2)
+                conv_wait(&full[s2 % kTmaDepth], (uint32_t)(s2 / kTmaDepth) & 1u, kConvDrainBudget, nullptr);
+        }
+        return;
+    }
+
+    // The present state: positions L .. L + carry - 1, 8 channels a thread (warp 0 of the
+    // row's first chunk, after its own reads of the past state).
+    if (chunk != 0 || sout == nullptr || !live || tg != 0) return;
+    for (int64_t j = 0; j < p.carry; ++j) {
+        const int64_t q = p.L + j;   // padded position
+        const IO *a = q >= p.carry ? x + (b * p.L + (q - p.carry)) * p.C + c0
+                                   : (past == nullptr ? nullptr : past + (srow * p.carry + q) * p.C + c0);
+        uint4 *d = reinterpret_cast<uint4 *>(sout + (srow * p.carry + j) * p.C + c0);
+        *d = a == nullptr ? make_uint4(0u, 0u, 0u, 0u) : *reinterpret_cast<const uint4 *>(a);
+    }
+}
+
 // The decode step (L = 1, K <= 4 at dilation 1, channels last, no window, 16-bit I/O,
 // four channels a thread): persistent CTAs walk (row, 1024-channel slab) items.  Each
 // thread streams the next item's carry + 1 positions, its taps and its bias into its own
@@ -798,11 +1018,69 @@ cudaError_t launch_conv_decode_stream(const ConvParams &p, cudaStream_t stream) 
     }
 }
 
+template <typename IO, int KT, bool SILU>
+cudaError_t launch_conv_tma_k(const ConvParams &p, const ConvTmaMaps &maps, cudaStream_t stream) {
+    constexpr int smem = kTmaDepth * kTmaRows * kStagedWidth * 2 + 128;
+    static bool attr_set[64] = {false};   // the limit is a per-device function attribute
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(causal_conv_tma_kernel<IO, KT, SILU>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    const long long set = __atomic_load_n(&g_wait_budget, __ATOMIC_RELAXED);
+    dim3 grid((unsigned)((p.C + kStagedWidth - 1) / kStagedWidth),
+              (unsigned)((p.L + kStagedChunk - 1) / kStagedChunk), (unsigned)p.B);
+    causal_conv_tma_kernel<IO, KT, SILU>
+        <<<grid, 256, smem, stream>>>(p, maps, set > 0 ? set : kConvDrainBudget);
+    return cudaGetLastError();
+}
+
+template <typename IO, bool SILU>
+cudaError_t launch_conv_tma_s(const ConvParams &p, const ConvTmaMaps &maps, cudaStream_t stream) {
+    switch (p.K) {
+        case 1: return launch_conv_tma_k<IO, 1, SILU>(p, maps, stream);
+        case 2: return launch_conv_tma_k<IO, 2, SILU>(p, maps, stream);
+        case 3: return launch_conv_tma_k<IO, 3, SILU>(p, maps, stream);
+        case 4: return launch_conv_tma_k<IO, 4, SILU>(p, maps, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+// The two tensor maps of the TMA conv over x [B][L][C] (false: encoder missing or the
+// shape out of the encoder's range, and the caller takes another kernel).
+template <typename IO>
+bool conv_tma_maps(const ConvParams &p, ConvTmaMaps *m) {
+    const gdn_dtype io = std::is_same<IO, __nv_bfloat16>::value ? GDN_BF16 : GDN_F16;
+    const uint64_t dims[3] = {(uint64_t)p.C, (uint64_t)p.L, (uint64_t)p.B};
+    const uint64_t strides[2] = {(uint64_t)p.C * 2, (uint64_t)p.C * 2 * (uint64_t)p.L};
+    const uint32_t box[3] = {(uint32_t)kStagedWidth, (uint32_t)kTmaRows, 1};
+    const uint32_t box_first[3] = {(uint32_t)kStagedWidth, (uint32_t)kStagedTokens, 1};
+    return encode_map_3d(&m->stage, p.x, io, dims, strides, box) &&
+           encode_map_3d(&m->first, p.x, io, dims, strides, box_first);
+}
+
 template <typename IO, int VEC>
 cudaError_t launch_conv_vec(const ConvParams &p, bool align16, cudaStream_t stream) {
     const int64_t items = p.B * p.tiles * (p.C / VEC);
     if (items == 0) return cudaSuccess;
     const int64_t chunks = (p.L + kStagedChunk - 1) / kStagedChunk;
+    // 16-bit values on the staged shapes whose output and state are 16-byte aligned too:
+    // the TMA kernel.
+    if constexpr (VEC == 4 && sizeof(IO) == 2) {
+        const bool out16 = reinterpret_cast<uintptr_t>(p.y) % 16 == 0 &&
+                           reinterpret_cast<uintptr_t>(p.state_out) % 16 == 0;
+        ConvTmaMaps maps;
+        if (align16 && out16 && p.tt == kShortTile && p.window == 0 &&
+            p.L >= kStagedMinTokens && p.C % 8 == 0 && p.B <= 65535 && chunks <= 65535 &&
+            p.L + 3 < 0x7fffffffLL && conv_tma_maps<IO>(p, &maps))
+            return p.silu ? launch_conv_tma_s<IO, true>(p, maps, stream)
+                          : launch_conv_tma_s<IO, false>(p, maps, stream);
+    }
     if (VEC == 4 && align16 && p.tt == kShortTile && p.window == 0 &&
         p.L >= kStagedMinTokens && p.C % 8 == 0 && p.B <= 65535 && chunks <= 65535) {
         const int smem = kStagedDepth * (kStagedTokens + 3) * kStagedWidth * (int)sizeof(IO);

@@ -100,6 +100,13 @@ struct TcParams {
     float *tp_phi, *tp_psi;         // [tp_nseg][N][h_v][128][128] fp32
     CUtensorMap tm_r;               // R: [tokens][h_v][128] in the I/O type
     void *tp_r;
+    // Gated RMS norm in the scan's readout (norm_gate set; never with the time-parallel
+    // scan): each d_v row of o becomes o / rms(o) * norm_scale * act(gate), written in o's
+    // place, with o rounded to the I/O type first as a separate norm would read it.
+    const void *norm_scale;         // [128] I/O type
+    const void *norm_gate;          // [tokens][h_v][128] I/O type, 16-byte aligned
+    float norm_eps;
+    int32_t norm_silu;              // act = silu (1) or sigmoid (0)
 };
 
 // First workspace slot of sequence n.  Batched: n * chunks_per_seq.  Packed: slot
@@ -133,6 +140,29 @@ template <typename IO>
 __device__ __forceinline__ uint4 pack8(const float *x) {
     return make_uint4(Pack<IO>::two(x[0], x[1]), Pack<IO>::two(x[2], x[3]),
                       Pack<IO>::two(x[4], x[5]), Pack<IO>::two(x[6], x[7]));
+}
+// The eight values of a packed 16-byte group, widened to fp32.
+template <typename IO>
+__device__ __forceinline__ void unpack8(const uint4 &u, float *x) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = Pack<IO>::unpack(w[i]);
+        x[2 * i] = t.x;
+        x[2 * i + 1] = t.y;
+    }
+}
+// 16-byte global -> shared copy (cp.async) and its group bookkeeping.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Store one fp32 value into shared memory of a CTA of this cluster (shared::cluster address).
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
 // OR-reduction of `pred` over the `count` threads of named barrier `id`.
@@ -772,6 +802,15 @@ constexpr int SS_DB0 = SS_SB + 16384;          // Delta, MN-major (token rows)
 constexpr int SS_DB1 = SS_DB0 + 8192;          // diag(e^{G_C - G}) Delta
 constexpr int SS_OUT = SS_DB1 + 8192;          // output tile staging, two buffers
 constexpr int kScanSmem = SS_OUT + 2 * 8192 + 1024;
+// With the norm epilogue: the gate rows of two chunks (each readout thread copies its own
+// row's 32 columns, so no barrier guards them), this half's norm scale, the per-row sums
+// of squares of the two 32-column groups, and the other half's row sums (two chunks),
+// which the other CTA of the pair writes.
+constexpr int SS_Z = SS_OUT + 2 * 8192;
+constexpr int SS_NS = SS_Z + 2 * 8192;
+constexpr int SS_SSP = SS_NS + 256;
+constexpr int SS_PEER = SS_SSP + 512;
+constexpr int kScanSmemNorm = SS_PEER + 512 + 1024;
 // A stage arrives in two parts with their own barriers: part B ([Q; W], read only by
 // D4') is refilled as soon as D4' has run; part A (K, U, [P; M], gates) once the chunk's
 // last MMA has run and every thread has read the gates.
@@ -791,6 +830,7 @@ struct ScanCtl {
     uint64_t delta_ready, sb_ready, out_done;  // chain warps -> issuing warp
     uint64_t ld_b, ld_a;                       // copy warp -> issuing warp: phase c seen
     uint64_t drain;
+    uint64_t peer_full[2];                     // norm: the other half's row sums of chunk c (c & 1)
     uint32_t tmem;
     int32_t abort;                             // a wait gave up: everyone leaves
     int32_t seq;
@@ -822,6 +862,31 @@ __device__ __forceinline__ bool warp_wait_or_abort(uint64_t *bar, uint32_t parit
     return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort, budget));
 }
 
+// The norm epilogue's wait for the other CTA of the pair: it stores its row sums into this
+// CTA's shared memory and then arrives here with release at cluster scope, so this wait
+// acquires at cluster scope.  Bounded, and it gives up as soon as another thread has.
+__device__ __forceinline__ bool wait_peer_or_abort(uint64_t *bar, uint32_t parity,
+                                                   volatile int32_t *abort, long long budget) {
+    const uint32_t addr = smem_u32(bar);
+    const long long t0 = clock64();
+    for (;;) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(addr), "r"(parity), "r"(20000u)
+            : "memory");
+        if (done) return true;
+        if (*abort) return false;
+        if (clock64() - t0 > budget) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
 // Scan CTAs: one per (sequence, value head, half of the 128 state columns).  Chunk c, with
 // S_c in registers (fp32) and in SB (I/O type):
 //   D4'(c) = [Q_c; W_{c+1}] S_c              issued once SB holds S_c      (commit d4)
@@ -835,7 +900,12 @@ __device__ __forceinline__ bool warp_wait_or_abort(uint64_t *bar, uint32_t parit
 // two TMEM column blocks each.  One warp issues every MMA and copy; the chain warps wait only on the
 // barriers of the work they consume, and it learns of their progress through arrival
 // counts.
-template <typename IO>
+// kNorm: the gated RMS norm of each o row is applied in the readout.  The two column
+// halves of a (sequence, head) run as a cluster pair; per chunk, each readout thread
+// squares its 32 rounded o values, the two column groups are summed through shared
+// memory, and each row's sum goes to the other CTA (a store into its shared memory, then
+// an arrival on its barrier), so both halves scale the row by the same 1 / rms.
+template <typename IO, bool kNorm = false>
 __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __grid_constant__ TcParams p) {
     constexpr bool kBf16 = std::is_same<IO, __nv_bfloat16>::value;
     constexpr uint32_t kIdNV = idesc_f16(kBf16, 128, kNV, false, true);
@@ -919,6 +989,10 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
         mbar_init(&ctl.ld_b, 1);
         mbar_init(&ctl.ld_a, 1);
         mbar_init(&ctl.drain, 1);
+        if (kNorm) {
+            mbar_init(&ctl.peer_full[0], 64);   // the other CTA's 64 row sums
+            mbar_init(&ctl.peer_full[1], 64);
+        }
         ctl.abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&p.tm_k);
@@ -928,6 +1002,8 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Both CTAs of the pair have initialised their barriers before either signals the other.
+    if constexpr (kNorm) cluster_sync();
     const uint32_t tmem = ctl.tmem;
     const size_t sbase = ((size_t)n * p.h_v + h) * kDK * kDK;
 
@@ -1121,11 +1197,80 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
             if (lane == 0) mbar_arrive(&ctl.sb_ready);
         };
         if (out_warp) publish_sb(true);
+        // Norm epilogue: the gate row of chunk c2 (this thread's row, its 32 columns) into
+        // buffer c2 & 1 by cp.async, one group per chunk (empty past the end), so that
+        // cp.async.wait_group 1 in chunk c's readout means "chunk c's row has landed".
+        float *const nsc = reinterpret_cast<float *>(sm + SS_NS);
+        float *const ssp = reinterpret_cast<float *>(sm + SS_SSP);
+        float *const peer_ss = reinterpret_cast<float *>(sm + SS_PEER);
+        auto fetch_gate = [&](int c2) {
+            if (c2 < nchunks && (int64_t)row < L - (int64_t)c2 * kC) {
+                const IO *src = static_cast<const IO *>(p.norm_gate) +
+                                ((size_t)(t0 + (int64_t)c2 * kC + row) * p.h_v + h) * kDK + v0 + 32 * g;
+                uint8_t *dst = sm + SS_Z + (c2 & 1) * 8192 + row * 128 + g * 64;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) cp_async16(dst + 16 * i, src + 8 * i);
+            }
+            cp_async_commit();
+        };
+        // o rounded to the I/O type (pk, this thread's 32 columns) -> the gated RMS norm of
+        // its row, in pk.  The row's sum of squares adds the other 32-column group (through
+        // ssp) and the other column half (the pair's CTA writes it into peer_ss).  Every
+        // readout thread comes here, whatever ok says, for the barrier.
+        auto norm_rows = [&](int c, bool ok, uint4 (&pk)[4]) -> bool {
+            float v[32];
+            float ss = 0.f;
+            if (ok) {
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8) unpack8<IO>(pk[q8], v + 8 * q8);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) ss = fmaf(v[e], v[e], ss);
+            }
+            ssp[64 * g + row] = ss;
+            named_bar(kBarOut, 128);
+            const float local = ssp[row] + ssp[64 + row];
+            if (ok && g == 0) {
+                const uint32_t peer = cluster_ctarank() ^ 1u;
+                st_cluster_f32(mapa_shared(smem_u32(peer_ss + 64 * (c & 1) + row), peer), local);
+                mbar_arrive_cluster(mapa_shared(smem_u32(&ctl.peer_full[c & 1]), peer));
+            }
+            ok = ok && wait_peer_or_abort(&ctl.peer_full[c & 1], (c >> 1) & 1, abort, budget);
+            if (ok) {
+                cp_async_wait<1>();
+                const float inv = rsqrtf((local + peer_ss[64 * (c & 1) + row]) / (float)kDK + p.norm_eps);
+                const uint8_t *zr = sm + SS_Z + (c & 1) * 8192 + row * 128 + g * 64;
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    float z[8], y[8];
+                    unpack8<IO>(*reinterpret_cast<const uint4 *>(zr + 16 * q8), z);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float sg = __fdividef(1.0f, 1.0f + __expf(-z[i]));
+                        const float act = p.norm_silu ? z[i] * sg : sg;
+                        y[i] = v[8 * q8 + i] * inv * nsc[32 * g + 8 * q8 + i] * act;
+                    }
+                    pk[q8] = pack8<IO>(y);
+                }
+            }
+            return ok;
+        };
+        if constexpr (kNorm) {
+            if (out_warp) {
+                if (q == 0)
+                    nsc[32 * g + lane] =
+                        IoType<IO>::ld(static_cast<const IO *>(p.norm_scale) + v0 + 32 * g + lane);
+                fetch_gate(0);
+                named_bar(kBarOut, 128);   // nsc
+            }
+        }
         bool ok = true;
         float gC_prev = 1.f;   // e^{G_C} of chunk c - 1 (1 before the first: W_0 S_0 is exact)
         for (int c = 0; c < nchunks; ++c) {
             const int s = c & 1;
             const uint8_t *st = sm + s * kScanStage;
+            if constexpr (kNorm) {
+                if (out_warp) fetch_gate(c + 1);
+            }
             const GateRec &gr = *reinterpret_cast<const GateRec *>(st + SS_G);
             // Every reader of the stage observes its arrival itself.  The gates are read
             // here: part A of the stage is refilled once every thread has arrived on sb_ready.
@@ -1219,9 +1364,9 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
             const bool tile_store = (Lc == kC);
             uint8_t *ob = sm + SS_OUT + s * 8192;
             ok = ok && warp_wait_or_abort(&ctl.x, (c + 1) & 1, abort, budget);
+            uint4 packed[4];
             if (ok) {
                 tc_fence_after();
-                uint4 packed[4];
 #pragma unroll
                 for (int ps = 0; ps < 2; ++ps) {
                     uint32_t r[16], rx[16];
@@ -1237,6 +1382,9 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl.out_done);
+            }
+            if constexpr (kNorm) ok = norm_rows(c, ok, packed);
+            if (ok) {
                 if (tile_store) {
 #pragma unroll
                     for (int q8 = 0; q8 < 4; ++q8)
@@ -1260,6 +1408,9 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
             }
         }
         if (tid == 0) bulk_wait_all();    // the output tiles have reached global memory
+        if constexpr (kNorm) {
+            if (out_warp) cp_async_wait<0>();   // no gate copy is left in flight
+        }
         if (ok && out_warp) {
             float *sdst = p.state_out;
             if (p.tp_seg > 0)
@@ -1338,6 +1489,8 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
     }
     tc_fence_before();
     __syncthreads();
+    // Neither CTA of a pair leaves while the other may still write into its shared memory.
+    if constexpr (kNorm) cluster_sync();
     if (tid == 0 && ctl.abort) atomicOr(p.status, kDevTimeout);
     if (warp == 0) {
         tc_fence_after();
@@ -1669,6 +1822,9 @@ cudaError_t configure() {
             e = cudaFuncSetAttribute(gdn_chunk_scan<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kScanSmem);
         if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gdn_chunk_scan<IO, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmemNorm);
+        if (e == cudaSuccess)
             e = cudaFuncSetAttribute(gdn_tp_correct<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kCorrSmem);
         if (e != cudaSuccess) return e;
@@ -1716,6 +1872,22 @@ template <typename IO>
 cudaError_t launch_scan(const TcParams &tp, cudaStream_t stream) {
     const int64_t ctas = (int64_t)tp.num_seqs * tp.h_v * (kDK / kNV);
     if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (tp.norm_gate != nullptr) {
+        // The two column halves of a (sequence, head), CTAs 2i and 2i + 1, as a cluster.
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)ctas);
+        cfg.blockDim = dim3(kScanAllThreads);
+        cfg.dynamicSmemBytes = kScanSmemNorm;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, gdn_chunk_scan<IO, true>, tp);
+    }
     gdn_chunk_scan<IO><<<(unsigned)ctas, kScanAllThreads, kScanSmem, stream>>>(tp);
     return cudaGetLastError();
 }
@@ -1846,6 +2018,21 @@ cudaError_t launch_tp(TcParams tp, int64_t n_slots, int nseg, uint8_t *extra, cu
 
 long long g_wait_budget = 0;   // 0: the kernels' default budget
 
+bool encode_map_3d(CUtensorMap *m, const void *base, gdn_dtype io, const uint64_t dims[3],
+                   const uint64_t strides[2], const uint32_t box[3]) {
+    auto fn = encode_fn();
+    if (fn == nullptr || io == GDN_F32) return false;
+    const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+    const cuuint64_t st[2] = {strides[0], strides[1]};
+    const cuuint32_t bx[3] = {box[0], box[1], box[2]};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, io == GDN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          3, const_cast<void *>(base), d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 size_t prefill_tc_tp_bytes(bool varlen, int64_t seqlen, int64_t batch, int h_v) {
     const int nseg = tp_segments(varlen, seqlen, batch, h_v);
     return nseg > 1 ? tp_layout(seqlen, batch, h_v, nseg).total : 0;
@@ -1899,12 +2086,18 @@ cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_t
     tp.has_decay = p.rule == GDN_RULE_GATED_DELTA || p.rule == GDN_RULE_GATED;
     tp.has_delta = p.rule == GDN_RULE_GATED_DELTA || p.rule == GDN_RULE_DELTA;
     tp.beta_shared = p.beta_shared;
+    tp.norm_scale = p.norm_scale;
+    tp.norm_gate = p.norm_gate;
+    tp.norm_eps = p.norm_eps;
+    tp.norm_silu = p.norm_silu;
     const bool varlen = p.cu_seqlens != nullptr;
     const int64_t n_slots = chunk_slots(varlen, p.seqlen, p.num_seqs, p.num_seqs);
     // The time-parallel scan, when the shape suits it, the caller allows internal
-    // resources and the workspace holds its buffers.
+    // resources and the workspace holds its buffers (not with the norm epilogue: the
+    // correction adds to o after the scan).
     const size_t records = prefill_tc_workspace(varlen, p.seqlen, p.num_seqs, p.num_seqs, p.h_v);
-    const int tps = allow_overlap ? tp_segments(varlen, p.seqlen, p.num_seqs, p.h_v) : 1;
+    const int tps = allow_overlap && p.norm_gate == nullptr
+                        ? tp_segments(varlen, p.seqlen, p.num_seqs, p.h_v) : 1;
     if (tps > 1 && workspace_bytes >= records + tp_layout(p.seqlen, p.num_seqs, p.h_v, tps).total) {
         uint8_t *extra = static_cast<uint8_t *>(workspace) + records;
         if (!make_map(&tp.tm_r, extra + tp_layout(p.seqlen, p.num_seqs, p.h_v, tps).r, io, p.h_v, total_tokens))

@@ -26,7 +26,8 @@ EXPORTS = ("gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode_step",
            "gdn_prefill_plan", "gdn_last_device_status", "gdn_status_string",
            "gdn_last_error_message", "gdn_prefill_noalloc", "gdn_decode_step_slots",
            "gdn_scan_window", "gdn_scan_variant", "gdn_causal_conv", "gdn_causal_conv_slots",
-           "gdn_gated_rmsnorm", "gdn_set_wait_budget", "gdn_decode_layer", "gdn_prefill_variant")
+           "gdn_gated_rmsnorm", "gdn_set_wait_budget", "gdn_decode_layer", "gdn_prefill_variant",
+           "gdn_prefill_norm")
 PATH_SIMT, PATH_TC, PATH_TC_TP = 1, 2, 3
 # gdn_rule codes.
 RULES = {"gated_delta": 0, "delta": 1, "gated": 2, "linear": 3}
@@ -124,6 +125,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.gdn_prefill_variant.restype = ctypes.c_int
     lib.gdn_prefill_variant.argtypes = [S, ctypes.POINTER(GdnVariant), P, P, P, P, P, P, P, P, P,
                                         ctypes.c_float, P, P, P, ctypes.c_size_t, P]
+    lib.gdn_prefill_norm.restype = ctypes.c_int
+    lib.gdn_prefill_norm.argtypes = [S, P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P,
+                                     ctypes.c_float, ctypes.c_int32, P, P, P, ctypes.c_size_t, P]
     lib.gdn_decode_layer.restype = ctypes.c_int
     lib.gdn_decode_layer.argtypes = [S, ctypes.POINTER(GdnLayerParams), P, P, P, P, P, P, P, P, P,
                                      P, ctypes.c_float, P, P, P, P]
@@ -232,6 +236,57 @@ def gdn_prefill(q, k, v, a, b, A_log, dt_bias, state_in=None, cu_seqlens=None,
 
 # Size of the library's fixed scratch array behind gdn_prefill_noalloc.
 PREFILL_NOALLOC_SCRATCH_BYTES = 96 * 1024 * 1024
+
+
+
+def gdn_prefill_norm(q, k, v, a, b, A_log, dt_bias, state_in=None, cu_seqlens=None,
+                     scale: float = 0.0, *, norm_scale, gate, eps: float = 1e-6,
+                     activation: str = "silu", y=None, state_out=None, workspace=None,
+                     stream=None):
+    """gdn_prefill, then the gated RMS norm of o over each d_v row; returns (y, state_out).
+
+    norm_scale [d_v] and gate (o's shape) in the io dtype; y has o's shape.  On the chunked
+    tensor-core path the norm runs in the scan's readout and o is never stored."""
+    lib = load()
+    shape = _shape_of(q, v, cu_seqlens)
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v), ("a", a), ("b", b), ("gate", gate),
+                    ("norm_scale", norm_scale)):
+        _need_cuda(name, t, dt)
+    _need_cuda("A_log", A_log, torch.float32)
+    _need_cuda("dt_bias", dt_bias, torch.float32)
+    if tuple(k.shape) != tuple(q.shape) or tuple(a.shape) != tuple(v.shape[:3]) or \
+            tuple(b.shape) != tuple(a.shape):
+        raise GdnError(GDN_ERR_INVALID_ARG, "k must match q, and a, b must be [B, T, h_v]")
+    if tuple(gate.shape) != tuple(v.shape) or tuple(norm_scale.shape) != (shape.d_v,):
+        raise GdnError(GDN_ERR_INVALID_ARG, "gate must match v, norm_scale must be [d_v]")
+    if activation not in ("silu", "swish", "sigmoid"):
+        raise GdnError(GDN_ERR_INVALID_ARG, "activation is silu or sigmoid")
+    st_shape = (shape.num_seqs, shape.h_v, shape.d_k, shape.d_v)
+    if state_in is not None:
+        _need_cuda("state_in", state_in, torch.float32)
+        if tuple(state_in.shape) != st_shape:
+            raise GdnError(GDN_ERR_INVALID_ARG, f"state_in must be {st_shape}")
+    if cu_seqlens is not None:
+        _need_cuda("cu_seqlens", cu_seqlens, torch.int32)
+    if y is None:
+        y = torch.empty(v.shape, dtype=dt, device=v.device)
+    else:
+        _need_cuda("y", y, dt)
+    if state_out is None:
+        state_out = torch.empty(st_shape, dtype=torch.float32, device=v.device)
+    else:
+        _need_cuda("state_out", state_out, torch.float32)
+    need = int(lib.gdn_prefill_workspace_bytes(ctypes.byref(shape)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=v.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.gdn_prefill_norm(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b),
+                                _ptr(A_log), _ptr(dt_bias), _ptr(state_in), _ptr(cu_seqlens),
+                                float(scale), _ptr(norm_scale), _ptr(gate), float(eps),
+                                ACTIVATIONS[activation], _ptr(y), _ptr(state_out),
+                                _ptr(workspace), ws_bytes, _stream(stream)))
+    return y, state_out
 
 
 def gdn_prefill_noalloc(q, k, v, a, b, A_log, dt_bias, state_in, cu_seqlens, scale: float,

@@ -122,6 +122,40 @@ def test_conv_long_rows_through_shared_memory(io, L, C, K):
     _exact(so, s_ref)
 
 
+@pytest.mark.parametrize("io", ["bf16", "f16"])
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
+@pytest.mark.parametrize("silu,bias,state", [(True, True, True), (False, False, False)])
+def test_conv_long_rows_every_tap_count(io, K, silu, bias, state):
+    """16-bit long rows run on the bulk-copy kernel, compiled per tap count and activation.
+    Without a past state a row's first stage has zero-filled rows; 520 channels leave an
+    8-channel slab; 333 tokens end in a ragged stage of a ragged chunk."""
+    inp = _conv_case(io, 2, 333, 520, K, 1, silu=silu, bias=bias, state=state,
+                     seed=700 + 10 * K + int(silu))
+    y, so = _run_conv(inp)
+    y_ref, s_ref = _conv_ref(inp)
+    _close(y, y_ref, io)
+    _exact(so, s_ref)
+
+
+def test_conv_long_rows_with_an_output_off_16_bytes():
+    """y 8 bytes past a 16-byte boundary: the 8-byte-store staged kernel takes the call and
+    gives the same values."""
+    from recurrent_state_scan_gb300 import gdn_causal_conv
+    inp = _conv_case("bf16", 2, 300, 64, 4, 1, seed=9)
+    x, w, b, st = inp.x.cuda(), inp.w.cuda(), inp.bias.cuda(), inp.state_in.cuda()
+    buf = torch.empty(x.numel() + 4, dtype=x.dtype, device="cuda")
+    y = buf[4:].view(x.shape)
+    assert y.data_ptr() % 16 == 8
+    gdn_causal_conv(x, w, b, st, activation="silu", y=y)
+    torch.cuda.synchronize()
+    _status_ok()
+    y_ref, _ = _conv_ref(inp)
+    _close(y, y_ref, "bf16")
+    y16, _ = gdn_causal_conv(x, w, b, st, activation="silu")
+    torch.cuda.synchronize()
+    assert torch.equal(y16, y)
+
+
 def test_conv_long_rows_in_place():
     inp = _conv_case("bf16", 3, 300, 48, 4, 1, seed=8)
     y_ref, s_ref = _conv_ref(inp)

@@ -44,3 +44,75 @@ def test_short_wait_budget_reports_timeout_then_recovers():
     o, s = run_prefill(inp)
     o_ref, s_ref = oracle.scan_inputs(inp)
     check(inp, o, s, o_ref, s_ref, what="prefill after a timed-out call")
+
+
+@pytest.mark.gpu
+def test_short_wait_budget_times_out_the_conv_pipeline_then_recovers():
+    """The bulk-copy causal conv (16-bit long rows) waits for each stage's copies with the
+    same budget.  Its stages are prefetched three deep, so only a CTA's first wait can run
+    long; rows larger than L2 make those first copies come from DRAM, past a 50-cycle
+    budget.  The CTAs then give up, let their copies land and report GDN_ERR_TIMEOUT; the
+    next call is exact again (checked on the first 300 tokens of row 0, which depend on
+    nothing later)."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import numpy as np
+    from recurrent_state_scan_gb300 import gdn, gdn_causal_conv, gdn_last_device_status
+    inp = workloads.draw_conv(workloads.ConvSpec("t", "bf16", 4, 8192, 4096, 23, kernel=4,
+                                                 silu=True, bias=True, state_std=1.0))
+    x, w, b, st = inp.x.cuda(), inp.w.cuda(), inp.bias.cuda(), inp.state_in.cuda()
+    torch.empty(256 << 20, dtype=torch.uint8, device="cuda").zero_()   # evict x from L2
+    torch.cuda.synchronize()
+    assert gdn_last_device_status() == gdn.GDN_OK
+    gdn.gdn_set_wait_budget(50)
+    try:
+        gdn_causal_conv(x, w, b, st, activation="silu")
+        torch.cuda.synchronize()
+        assert gdn_last_device_status() == gdn.GDN_ERR_TIMEOUT
+    finally:
+        gdn.gdn_set_wait_budget(0)
+    assert gdn_last_device_status() == gdn.GDN_OK
+    y, _ = gdn_causal_conv(x, w, b, st, activation="silu")
+    torch.cuda.synchronize()
+    assert gdn_last_device_status() == gdn.GDN_OK
+    xs = inp.x[:1, :300].double().numpy()
+    y_ref, _ = oracle.causal_conv(xs, inp.w.double().numpy(), inp.bias.double().numpy(),
+                                  inp.state_in[:1].double().numpy(), silu=True)
+    ref = np.asarray(y_ref)
+    bound = 2.0 ** -8 * np.abs(ref) + 1e-5 * np.max(np.abs(ref))
+    assert np.all(np.abs(y[:1, :300].double().cpu().numpy() - ref) <= bound)
+
+
+@pytest.mark.gpu
+def test_short_wait_budget_times_out_the_norm_pairs_then_recovers():
+    """gdn_prefill_norm on the tensor-core path: the scan CTAs run as cluster pairs that
+    wait on each other for every chunk's row sums.  Under a short budget the waits run
+    out, every CTA of a pair leaves (they meet at the cluster barrier on the way out) and
+    the call reports GDN_ERR_TIMEOUT; the next call equals the separate calls."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from recurrent_state_scan_gb300 import (gdn, gdn_gated_rmsnorm, gdn_last_device_status,
+                                            gdn_prefill, gdn_prefill_norm)
+    inp = workloads.draw(workloads.small_spec(io="bf16", lengths=[300, 130], h_qk=1, h_v=2,
+                                              seed=19, state_std=0.05))
+    n = workloads.draw_norm(workloads.NormSpec("t", "bf16", (inp.total_tokens, 2, 128), 20))
+    d = to_device(inp)
+    scale, gate = n.scale.cuda(), n.gate.cuda().view(d["v"].shape)
+    args = (d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["state_in"],
+            d["cu_seqlens"], inp.scale)
+    assert gdn_last_device_status() == gdn.GDN_OK
+    gdn.gdn_set_wait_budget(200)
+    try:
+        gdn_prefill_norm(*args, norm_scale=scale, gate=gate, eps=1e-6)
+        torch.cuda.synchronize()
+        assert gdn_last_device_status() == gdn.GDN_ERR_TIMEOUT
+    finally:
+        gdn.gdn_set_wait_budget(0)
+    assert gdn_last_device_status() == gdn.GDN_OK
+    y, st = gdn_prefill_norm(*args, norm_scale=scale, gate=gate, eps=1e-6)
+    o, st2 = gdn_prefill(*args)
+    y2 = gdn_gated_rmsnorm(o, scale, gate, 1e-6, "silu")
+    torch.cuda.synchronize()
+    assert gdn_last_device_status() == gdn.GDN_OK
+    assert torch.equal(st, st2)
+    assert torch.allclose(y.float(), y2.float(), rtol=2.0 ** -7, atol=1e-5)

@@ -383,10 +383,47 @@ LAYER_WORKLOADS = {
 }
 
 
+@dataclasses.dataclass(frozen=True)
+class PrefillNormSpec:
+    """A prefill workload whose output goes through the gated RMS norm (gdn_prefill_norm)."""
+    name: str
+    prefill: str                 # a WORKLOADS name
+    seed: int
+    eps: float = 1e-6
+    activation: str = "silu"
+
+
+@dataclasses.dataclass
+class PrefillNormInputs:
+    spec: PrefillNormSpec
+    prefill: Inputs
+    norm_scale: torch.Tensor     # [d_v]
+    gate: torch.Tensor           # o's shape
+
+
+def draw_prefill_norm(spec: PrefillNormSpec) -> PrefillNormInputs:
+    inp = draw(WORKLOADS[spec.prefill])
+    rng = np.random.default_rng(spec.seed)
+    gate = rng.standard_normal(tuple(inp.v.shape))
+    scale = rng.normal(1.0, 0.1, inp.spec.d_v)
+    return PrefillNormInputs(spec=spec, prefill=inp, norm_scale=_round(scale, inp.spec.io),
+                             gate=_round(gate, inp.spec.io))
+
+
+PREFILL_NORM_WORKLOADS = {
+    # The packed varlen prefill (8 sequences, 31,979 tokens, 16 heads, d = 128) with the
+    # gated RMS norm of each head's output row.
+    "varlen_bf16_prefill_norm": PrefillNormSpec("varlen_bf16_prefill_norm", "varlen_bf16_prefill",
+                                                seed=1014),
+}
+
+
 def any_workload(name: str):
     """Draw any named workload: the scan's, the convolution's or the norm's."""
     if name in WORKLOADS:
         return draw(WORKLOADS[name])
+    if name in PREFILL_NORM_WORKLOADS:
+        return draw_prefill_norm(PREFILL_NORM_WORKLOADS[name])
     if name in CONV_WORKLOADS:
         return draw_conv(CONV_WORKLOADS[name])
     if name in LAYER_WORKLOADS:
@@ -395,4 +432,4 @@ def any_workload(name: str):
 
 
 ALL_WORKLOADS = sorted(list(WORKLOADS) + list(CONV_WORKLOADS) + list(NORM_WORKLOADS) +
-                       list(LAYER_WORKLOADS))
+                       list(LAYER_WORKLOADS) + list(PREFILL_NORM_WORKLOADS))
