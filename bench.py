@@ -480,7 +480,7 @@ def main_neighbour(args, rank, world, local):
     gbs = nbytes / (ms / 1e3) / 1e9
     if conv:   # the kernel that takes the workload's shape (16-bit, channels last)
         kernel = ("gdn::causal_conv_decode_stream_kernel" if inp.spec.decode
-                  else "gdn::causal_conv_bulk_kernel")
+                  else "gdn::causal_conv_tma_kernel")
     else:
         kernel = "gdn::gated_rmsnorm_rows_kernel"
     line = {
@@ -753,7 +753,7 @@ def main_prefill_norm(args, rank, world, local):
     nbytes = int(sum(prefill_norm_io_bytes(inp).values()))
     config = dict(config_of(p, world), workload=inp.spec.name,
                   op="packed prefill, then the gated RMS norm (silu gate) of each head's "
-                     "output row: gdn_prefill_norm, the norm in the scan's readout",
+                     "output row: gdn_prefill_norm (the norm in place on y)",
                   norm={"eps": inp.spec.eps, "activation": inp.spec.activation})
     if args.impl == "reference":
         if rank != 0:
@@ -794,10 +794,14 @@ def main_prefill_norm(args, rank, world, local):
                      dtype=torch.uint8, device=dev)
     eps, act = inp.spec.eps, inp.spec.activation
 
-    def call(d):
+    def call(d, fuse=False):
         gdn_prefill_norm(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], state0,
                          cu, p.scale, norm_scale=d["norm_scale"], gate=d["gate"], eps=eps,
-                         activation=act, y=y, state_out=state_out, workspace=ws, stream=stream)
+                         activation=act, fuse=fuse, y=y, state_out=state_out, workspace=ws,
+                         stream=stream)
+
+    def fused(d):
+        call(d, fuse=True)
 
     def separate(d):
         gdn_prefill(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], state0, cu,
@@ -826,6 +830,7 @@ def main_prefill_norm(args, rank, world, local):
     ms = timed(call, t)
     clocks = sampler.stop() if sampler else None
     ms_sep = timed(separate, t)
+    ms_fused = timed(fused, t)
 
     e2e = None
     if not args.no_e2e:
@@ -863,11 +868,12 @@ def main_prefill_norm(args, rank, world, local):
                      "traffic": profiled_traffic(args.workload, "prefill"),
                      "peak_source": f"{pk_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"
                      if pk_kind == "measured" else "fallback 6.8 TB/s",
-                     "kernels": "gdn_chunk_prep + gdn_chunk_scan with the norm (cluster pairs), "
-                                "one call"},
+                     "kernels": "gdn_chunk_prep + gdn_chunk_scan + gated_rmsnorm_rows_kernel, one call"},
         "separate_calls": {"ms_per_step": ms_sep, "launches": 3,
                            "calls": "gdn_prefill (prep, scan), gdn_gated_rmsnorm"},
-        "gpu_launches": args.steps * 2,
+        "fused_readout": {"ms_per_step": ms_fused, "launches": 2,
+                          "kernels": "gdn_chunk_prep + gdn_chunk_scan with the norm (cluster pairs)"},
+        "gpu_launches": args.steps * 3,
     }
     if e2e is not None:
         line["e2e"] = e2e

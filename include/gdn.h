@@ -41,7 +41,7 @@
  * pool), gdn_scan_window (the states after each of the last W steps),
  * gdn_scan_variant and gdn_prefill_variant (other update rules and gate layouts),
  * the layer ops around the scan: gdn_causal_conv, gdn_causal_conv_slots and
- * gdn_gated_rmsnorm, gdn_prefill_norm (the prefill with the norm in its readout) and
+ * gdn_gated_rmsnorm, gdn_prefill_norm (the prefill and the norm in one call) and
  * gdn_decode_layer (conv -> decode step -> norm in one kernel).
  *  - gdn_last_error_message() gives a human-readable detail of the last
  *    non-OK status returned on the calling thread.
@@ -346,19 +346,23 @@ gdn_status gdn_gated_rmsnorm(int32_t io_dtype, int64_t rows, int32_t width, cons
  *   epsilon     finite and >= 0; activation GDN_ACT_SILU or GDN_ACT_SIGMOID.
  *   y           DEVICE, o's layout.  o itself is not an output.
  *   the rest    as gdn_prefill (workspace sized by gdn_prefill_workspace_bytes).
- * On the chunked tensor-core path (16-bit I/O, d_k = d_v = 128) with a 16-byte aligned
- * gate, the norm runs in the state scan's readout: the two CTAs that own a head's two
- * 64-column halves of the state run as a thread-block cluster and exchange each row's sum
- * of squares through shared memory, so o never reaches global memory; that path never
- * takes the time-parallel scan.  Elsewhere the norm is a second launch, in place on y.
+ *   fuse        0: the prefill writes o into y and the norm runs after it, in place (two
+ *               launches of this library's kernels on top of the prefill's; the faster
+ *               form on GB300).  1: on the chunked tensor-core path (16-bit I/O,
+ *               d_k = d_v = 128) with a 16-byte aligned gate, the norm runs in the state
+ *               scan's readout: the two CTAs that own a head's two 64-column halves of the
+ *               state run as a thread-block cluster and exchange each row's sum of squares
+ *               through shared memory, so o never reaches global memory (that path never
+ *               takes the time-parallel scan); elsewhere as 0.  The results agree to one
+ *               rounding of the I/O type.
  * Errors: gdn_prefill's, and gdn_gated_rmsnorm's argument rules.
  */
 gdn_status gdn_prefill_norm(const gdn_shape *shape, const void *q, const void *k, const void *v,
                             const void *a, const void *b, const float *A_log,
                             const float *dt_bias, const float *state_in,
                             const int32_t *cu_seqlens, float scale, const void *norm_scale,
-                            const void *gate, float epsilon, int32_t activation, void *y,
-                            float *state_out, void *workspace, size_t workspace_bytes,
+                            const void *gate, float epsilon, int32_t activation, int32_t fuse,
+                            void *y, float *state_out, void *workspace, size_t workspace_bytes,
                             void *stream);
 
 /*

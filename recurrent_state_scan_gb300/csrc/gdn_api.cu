@@ -193,10 +193,10 @@ gdn_status gdn_prefill_norm(const gdn_shape *shape, const void *q, const void *k
                             const void *a, const void *b, const float *A_log,
                             const float *dt_bias, const float *state_in,
                             const int32_t *cu_seqlens, float scale, const void *norm_scale,
-                            const void *gate, float epsilon, int32_t activation, void *y,
-                            float *state_out, void *workspace, size_t workspace_bytes,
+                            const void *gate, float epsilon, int32_t activation, int32_t fuse,
+                            void *y, float *state_out, void *workspace, size_t workspace_bytes,
                             void *stream) {
-    const NormEpilogue norm{norm_scale, gate, epsilon, activation};
+    const NormEpilogue norm{norm_scale, gate, epsilon, activation, fuse != 0};
     return prefill_impl(shape, q, k, v, a, b, A_log, dt_bias, state_in, cu_seqlens, scale, y,
                         state_out, workspace, workspace_bytes, true, stream, nullptr, &norm);
 }
@@ -275,7 +275,7 @@ gdn_status gdn::prefill_impl(const gdn_shape *shape, const void *q, const void *
     cudaError_t e;
     bool norm_after = norm != nullptr && tokens > 0;   // the norm as its own launch, in place
     if (!p.decay_per_key && prefill_tc_supported(p, io, tokens)) {
-        if (norm_after && aligned(norm->gate, 16)) {
+        if (norm_after && norm->fuse && aligned(norm->gate, 16)) {
             p.norm_scale = norm->scale;
             p.norm_gate = norm->gate;
             p.norm_eps = norm->eps;

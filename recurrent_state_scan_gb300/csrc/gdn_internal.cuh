@@ -182,6 +182,7 @@ struct NormEpilogue {
     const void *gate;    // like o
     float eps;
     int32_t activation;  // GDN_ACT_SILU or GDN_ACT_SIGMOID
+    bool fuse;           // in the tensor-core scan's readout where the path allows
 };
 
 // gdn_prefill with the segment overlap allowed or not (no internal stream is created

@@ -802,15 +802,15 @@ constexpr int SS_DB0 = SS_SB + 16384;          // Delta, MN-major (token rows)
 constexpr int SS_DB1 = SS_DB0 + 8192;          // diag(e^{G_C - G}) Delta
 constexpr int SS_OUT = SS_DB1 + 8192;          // output tile staging, two buffers
 constexpr int kScanSmem = SS_OUT + 2 * 8192 + 1024;
-// With the norm epilogue: the gate rows of two chunks (each readout thread copies its own
-// row's 32 columns, so no barrier guards them), this half's norm scale, the per-row sums
-// of squares of the two 32-column groups, and the other half's row sums (two chunks),
+// With the norm epilogue: the gate rows of two chunks (each state-warp thread copies its
+// own row, so no barrier guards them), this half's norm scale, the per-row sums of squares
+// of the two 32-column groups (two chunks), and the other half's row sums (four chunks),
 // which the other CTA of the pair writes.
 constexpr int SS_Z = SS_OUT + 2 * 8192;
 constexpr int SS_NS = SS_Z + 2 * 8192;
-constexpr int SS_SSP = SS_NS + 256;
-constexpr int SS_PEER = SS_SSP + 512;
-constexpr int kScanSmemNorm = SS_PEER + 512 + 1024;
+constexpr int SS_SSP = SS_NS + 256;            // [chunk & 1][column group][row]
+constexpr int SS_PEER = SS_SSP + 1024;         // [chunk & 3][row]
+constexpr int kScanSmemNorm = SS_PEER + 1024 + 1024;
 // A stage arrives in two parts with their own barriers: part B ([Q; W], read only by
 // D4') is refilled as soon as D4' has run; part A (K, U, [P; M], gates) once the chunk's
 // last MMA has run and every thread has read the gates.
@@ -822,6 +822,7 @@ constexpr int kChainWarps = 8;                 // Delta, state update, readout
 // + an MMA-issue warp, a copy warp and two state warps (S rows 64-127, TMEM lanes 64-127)
 constexpr int kScanAllThreads = 32 * kChainWarps + 128;
 constexpr uint32_t kBarOut = 2;                // named barrier of the 128 readout threads
+constexpr uint32_t kBarNorm = 3;               // named barrier of the 64 state-warp threads
 constexpr int kLptMax = 128;                   // packed batches up to this size run longest first
 
 struct ScanCtl {
@@ -830,7 +831,8 @@ struct ScanCtl {
     uint64_t delta_ready, sb_ready, out_done;  // chain warps -> issuing warp
     uint64_t ld_b, ld_a;                       // copy warp -> issuing warp: phase c seen
     uint64_t drain;
-    uint64_t peer_full[2];                     // norm: the other half's row sums of chunk c (c & 1)
+    uint64_t peer_full[4];                     // norm: the other half's row sums of chunk c (c & 3)
+    uint64_t o_staged[2], ob_free[2];          // norm: readout -> state warps, and back
     uint32_t tmem;
     int32_t abort;                             // a wait gave up: everyone leaves
     int32_t seq;
@@ -990,8 +992,11 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
         mbar_init(&ctl.ld_a, 1);
         mbar_init(&ctl.drain, 1);
         if (kNorm) {
-            mbar_init(&ctl.peer_full[0], 64);   // the other CTA's 64 row sums
-            mbar_init(&ctl.peer_full[1], 64);
+            for (int i = 0; i < 4; ++i) mbar_init(&ctl.peer_full[i], 64);   // the other CTA's row sums
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&ctl.o_staged[i], 1);
+                mbar_init(&ctl.ob_free[i], 1);
+            }
         }
         ctl.abort = 0;
         fence_mbar_init();
@@ -1197,80 +1202,32 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
             if (lane == 0) mbar_arrive(&ctl.sb_ready);
         };
         if (out_warp) publish_sb(true);
-        // Norm epilogue: the gate row of chunk c2 (this thread's row, its 32 columns) into
-        // buffer c2 & 1 by cp.async, one group per chunk (empty past the end), so that
-        // cp.async.wait_group 1 in chunk c's readout means "chunk c's row has landed".
-        float *const nsc = reinterpret_cast<float *>(sm + SS_NS);
+        // Norm epilogue: the readout warps stage chunk c's rounded o in its output tile and
+        // publish the rows' sums of squares (ssp, and the other CTA's peer_ss); the state
+        // warps turn the tile into y one chunk later and store it.
         float *const ssp = reinterpret_cast<float *>(sm + SS_SSP);
         float *const peer_ss = reinterpret_cast<float *>(sm + SS_PEER);
-        auto fetch_gate = [&](int c2) {
-            if (c2 < nchunks && (int64_t)row < L - (int64_t)c2 * kC) {
-                const IO *src = static_cast<const IO *>(p.norm_gate) +
-                                ((size_t)(t0 + (int64_t)c2 * kC + row) * p.h_v + h) * kDK + v0 + 32 * g;
-                uint8_t *dst = sm + SS_Z + (c2 & 1) * 8192 + row * 128 + g * 64;
+        // o (or y) of chunk cc to its tile staging buffer, or row by row for a ragged chunk.
+        auto store_rows = [&](int cc, const uint4 (&pk)[4]) {
+            const int Lcc = (int)((L - (int64_t)cc * kC) < kC ? (L - (int64_t)cc * kC) : kC);
+            if (Lcc == kC) {
+                uint8_t *obb = sm + SS_OUT + (cc & 1) * 8192;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) cp_async16(dst + 16 * i, src + 8 * i);
+                for (int q8 = 0; q8 < 4; ++q8)
+                    *reinterpret_cast<uint4 *>(obb + sw128_offset(row, 4 * g + q8)) = pk[q8];
+            } else if (row < Lcc) {
+                uint4 *dst = reinterpret_cast<uint4 *>(
+                    go + ((size_t)(t0 + (int64_t)cc * kC + row) * p.h_v + h) * kDK + v0 + 32 * g);
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8) dst[q8] = pk[q8];
             }
-            cp_async_commit();
         };
-        // o rounded to the I/O type (pk, this thread's 32 columns) -> the gated RMS norm of
-        // its row, in pk.  The row's sum of squares adds the other 32-column group (through
-        // ssp) and the other column half (the pair's CTA writes it into peer_ss).  Every
-        // readout thread comes here, whatever ok says, for the barrier.
-        auto norm_rows = [&](int c, bool ok, uint4 (&pk)[4]) -> bool {
-            float v[32];
-            float ss = 0.f;
-            if (ok) {
-#pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) unpack8<IO>(pk[q8], v + 8 * q8);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) ss = fmaf(v[e], v[e], ss);
-            }
-            ssp[64 * g + row] = ss;
-            named_bar(kBarOut, 128);
-            const float local = ssp[row] + ssp[64 + row];
-            if (ok && g == 0) {
-                const uint32_t peer = cluster_ctarank() ^ 1u;
-                st_cluster_f32(mapa_shared(smem_u32(peer_ss + 64 * (c & 1) + row), peer), local);
-                mbar_arrive_cluster(mapa_shared(smem_u32(&ctl.peer_full[c & 1]), peer));
-            }
-            ok = ok && wait_peer_or_abort(&ctl.peer_full[c & 1], (c >> 1) & 1, abort, budget);
-            if (ok) {
-                cp_async_wait<1>();
-                const float inv = rsqrtf((local + peer_ss[64 * (c & 1) + row]) / (float)kDK + p.norm_eps);
-                const uint8_t *zr = sm + SS_Z + (c & 1) * 8192 + row * 128 + g * 64;
-#pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
-                    float z[8], y[8];
-                    unpack8<IO>(*reinterpret_cast<const uint4 *>(zr + 16 * q8), z);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float sg = __fdividef(1.0f, 1.0f + __expf(-z[i]));
-                        const float act = p.norm_silu ? z[i] * sg : sg;
-                        y[i] = v[8 * q8 + i] * inv * nsc[32 * g + 8 * q8 + i] * act;
-                    }
-                    pk[q8] = pack8<IO>(y);
-                }
-            }
-            return ok;
-        };
-        if constexpr (kNorm) {
-            if (out_warp) {
-                if (q == 0)
-                    nsc[32 * g + lane] =
-                        IoType<IO>::ld(static_cast<const IO *>(p.norm_scale) + v0 + 32 * g + lane);
-                fetch_gate(0);
-                named_bar(kBarOut, 128);   // nsc
-            }
-        }
+        auto is_tile = [&](int cc) { return L - (int64_t)cc * kC >= kC; };
         bool ok = true;
         float gC_prev = 1.f;   // e^{G_C} of chunk c - 1 (1 before the first: W_0 S_0 is exact)
         for (int c = 0; c < nchunks; ++c) {
             const int s = c & 1;
             const uint8_t *st = sm + s * kScanStage;
-            if constexpr (kNorm) {
-                if (out_warp) fetch_gate(c + 1);
-            }
             const GateRec &gr = *reinterpret_cast<const GateRec *>(st + SS_G);
             // Every reader of the stage observes its arrival itself.  The gates are read
             // here: part A of the stage is refilled once every thread has arrived on sb_ready.
@@ -1360,9 +1317,6 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
             // chunk goes out as one TMA store of the staged 64 x 64 tile; a sequence's
             // ragged last chunk is stored row by row so that no row of the next sequence
             // is touched.  The readout warps leave the loop together, at their barrier.
-            const int Lc = (int)((L - (int64_t)c * kC) < kC ? (L - (int64_t)c * kC) : kC);
-            const bool tile_store = (Lc == kC);
-            uint8_t *ob = sm + SS_OUT + s * 8192;
             ok = ok && warp_wait_or_abort(&ctl.x, (c + 1) & 1, abort, budget);
             uint4 packed[4];
             if (ok) {
@@ -1383,18 +1337,32 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl.out_done);
             }
-            if constexpr (kNorm) ok = norm_rows(c, ok, packed);
-            if (ok) {
-                if (tile_store) {
+            if constexpr (kNorm) {
+                // The tile of chunk c - 2 has been turned into y and stored from this buffer.
+                if (c >= 2) ok = ok && warp_wait_or_abort(&ctl.ob_free[c & 1], ((c - 2) >> 1) & 1, abort, budget);
+                float ss = 0.f;
+                if (ok) {
+                    uint8_t *obb = sm + SS_OUT + (c & 1) * 8192;
 #pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8)
-                        *reinterpret_cast<uint4 *>(ob + sw128_offset(row, 4 * g + q8)) = packed[q8];
-                } else if (row < Lc) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(
-                        go + ((size_t)(t0 + (int64_t)c * kC + row) * p.h_v + h) * kDK + v0 + 32 * g);
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        *reinterpret_cast<uint4 *>(obb + sw128_offset(row, 4 * g + q8)) = packed[q8];
+                        float v[8];
+                        unpack8<IO>(packed[q8], v);
 #pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8) dst[q8] = packed[q8];
+                        for (int i = 0; i < 8; ++i) ss = fmaf(v[i], v[i], ss);
+                    }
                 }
+                ssp[128 * (c & 1) + 64 * g + row] = ss;
+                named_bar(kBarOut, 128);
+                if (ok && g == 0) {
+                    const float local = ssp[128 * (c & 1) + row] + ssp[128 * (c & 1) + 64 + row];
+                    const uint32_t peer = cluster_ctarank() ^ 1u;
+                    st_cluster_f32(mapa_shared(smem_u32(peer_ss + 64 * (c & 3) + row), peer), local);
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&ctl.peer_full[c & 3]), peer));
+                }
+                if (tid == 0) mbar_arrive(&ctl.o_staged[c & 1]);   // after every readout thread's writes
+            } else if (ok) {
+                store_rows(c, packed);
             }
             fence_async_smem();
             if (tid == 0) bulk_wait_read();    // the previous tile store has read its buffer
@@ -1402,15 +1370,12 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                 ok = false;
                 break;
             }
-            if (tid == 0 && tile_store) {
-                tma_store_3d(omap, ob, v0, h, (int)(t0 + (int64_t)c * kC));
+            if (!kNorm && tid == 0 && is_tile(c)) {
+                tma_store_3d(omap, sm + SS_OUT + (c & 1) * 8192, v0, h, (int)(t0 + (int64_t)c * kC));
                 bulk_commit();
             }
         }
         if (tid == 0) bulk_wait_all();    // the output tiles have reached global memory
-        if constexpr (kNorm) {
-            if (out_warp) cp_async_wait<0>();   // no gate copy is left in flight
-        }
         if (ok && out_warp) {
             float *sdst = p.state_out;
             if (p.tp_seg > 0)
@@ -1454,9 +1419,84 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
             if (lane == 0) mbar_arrive(&ctl.sb_ready);
         };
         publish_rows(true);
+
+        // Norm epilogue (kNorm), one chunk behind the readout: this thread owns token row
+        // nrow of the staged tile (all 64 columns of the half).  Chunk cc's gate row comes
+        // in by cp.async at the top of iteration cc (one group per chunk, empty past the
+        // end), so cp.async.wait_group 1 in iteration cc + 1 means it has landed.
+        const int nrow = 32 * (warp - (kChainWarps + 2)) + lane;
+        float *const nsc = reinterpret_cast<float *>(sm + SS_NS);
+        const float *const ssp = reinterpret_cast<const float *>(sm + SS_SSP);
+        const float *const peer_ss = reinterpret_cast<const float *>(sm + SS_PEER);
+        const CUtensorMap *omap = &p.tm_o;
+        auto fetch_gate = [&](int c2) {
+            if (c2 < nchunks && (int64_t)nrow < L - (int64_t)c2 * kC) {
+                const IO *src = static_cast<const IO *>(p.norm_gate) +
+                                ((size_t)(t0 + (int64_t)c2 * kC + nrow) * p.h_v + h) * kDK + v0;
+                uint8_t *dst = sm + SS_Z + (c2 & 1) * 8192;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) cp_async16(dst + sw128_offset(nrow, i), src + 8 * i);
+            }
+            cp_async_commit();
+        };
+        // y = o * rsqrt(mean(o^2) + eps) * scale * act(gate) for chunk cc's rows, in place in
+        // its staging tile (or straight to memory for a ragged chunk), then one TMA store.
+        // Every state thread comes here, whatever ok says, for the barrier.
+        auto norm_tile = [&](int cc, bool ok) -> bool {
+            ok = ok && wait_or_abort(&ctl.o_staged[cc & 1], (cc >> 1) & 1, abort, budget) &&
+                 wait_peer_or_abort(&ctl.peer_full[cc & 3], (cc >> 2) & 1, abort, budget);
+            const int Lcc = (int)((L - (int64_t)cc * kC) < kC ? (L - (int64_t)cc * kC) : kC);
+            uint8_t *obb = sm + SS_OUT + (cc & 1) * 8192;
+            if (ok && nrow < Lcc) {
+                const float local = ssp[128 * (cc & 1) + nrow] + ssp[128 * (cc & 1) + 64 + nrow];
+                const float inv = rsqrtf((local + peer_ss[64 * (cc & 3) + nrow]) / (float)kDK + p.norm_eps);
+                const uint8_t *zr = sm + SS_Z + (cc & 1) * 8192;
+                uint4 *gdst = reinterpret_cast<uint4 *>(
+                    static_cast<IO *>(p.o) + ((size_t)(t0 + (int64_t)cc * kC + nrow) * p.h_v + h) * kDK + v0);
+                // Not unrolled: the warps of this CTA run several large code paths at once,
+                // and an unrolled copy of this loop cost instruction-cache misses everywhere.
+#pragma unroll 1
+                for (int q8 = 0; q8 < 8; ++q8) {
+                    float v[8], z[8], y[8];
+                    unpack8<IO>(*reinterpret_cast<const uint4 *>(obb + sw128_offset(nrow, q8)), v);
+                    unpack8<IO>(*reinterpret_cast<const uint4 *>(zr + sw128_offset(nrow, q8)), z);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float sg = __fdividef(1.0f, 1.0f + __expf(-z[i]));
+                        const float act = p.norm_silu ? z[i] * sg : sg;
+                        y[i] = v[i] * inv * nsc[8 * q8 + i] * act;
+                    }
+                    if (Lcc == kC) *reinterpret_cast<uint4 *>(obb + sw128_offset(nrow, q8)) = pack8<IO>(y);
+                    else gdst[q8] = pack8<IO>(y);
+                }
+            }
+            fence_async_smem();
+            if (bar_any(kBarNorm, 64, !ok)) return false;
+            if (nrow == 0 && Lcc == kC) {
+                tma_store_3d(omap, obb, v0, h, (int)(t0 + (int64_t)cc * kC));
+                bulk_commit();
+            }
+            return true;
+        };
+        // Chunk cc's staging tile is free again once its store has read it.
+        auto free_tile = [&](int cc) {
+            if (nrow == 0) {
+                bulk_wait_read();
+                mbar_arrive(&ctl.ob_free[cc & 1]);
+            }
+        };
+        if constexpr (kNorm) {
+            nsc[nrow] = IoType<IO>::ld(static_cast<const IO *>(p.norm_scale) + v0 + nrow);
+            named_bar(kBarNorm, 64);
+        }
+
         bool ok = true;
         for (int c = 0; c < nchunks; ++c) {
             const int s = c & 1;
+            if constexpr (kNorm) {
+                fetch_gate(c);
+                if (c >= 2) free_tile(c - 2);
+            }
             const GateRec &gr = *reinterpret_cast<const GateRec *>(sm + s * kScanStage + SS_G);
             ok = ok && warp_wait_or_abort(&ctl.full_a[s], (c >> 1) & 1, abort, budget);
             const float gC = ok ? gr.gC : 0.f;
@@ -1473,7 +1513,26 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                 }
             }
             publish_rows(ok);
+            if constexpr (kNorm) {
+                // ok is agreed by both state warps here (they meet at a barrier inside
+                // norm_tile, and at one of their own in chunk 0), so they leave together.
+                if (c >= 1) {
+                    cp_async_wait<1>();
+                    ok = norm_tile(c - 1, ok);
+                } else {
+                    ok = !bar_any(kBarNorm, 64, !ok);
+                }
+            }
             if (!ok) break;
+        }
+        if constexpr (kNorm) {
+            // The last chunk's norm, and every store read and written before the CTA leaves.
+            if (ok && nchunks > 0) {
+                cp_async_wait<0>();
+                ok = norm_tile(nchunks - 1, ok);
+            }
+            cp_async_wait<0>();
+            if (nrow == 0) bulk_wait_all();
         }
         if (ok) {
             float *sdst = p.state_out;

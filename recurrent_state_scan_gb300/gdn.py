@@ -127,7 +127,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                         ctypes.c_float, P, P, P, ctypes.c_size_t, P]
     lib.gdn_prefill_norm.restype = ctypes.c_int
     lib.gdn_prefill_norm.argtypes = [S, P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P,
-                                     ctypes.c_float, ctypes.c_int32, P, P, P, ctypes.c_size_t, P]
+                                     ctypes.c_float, ctypes.c_int32, ctypes.c_int32, P, P, P,
+                                     ctypes.c_size_t, P]
     lib.gdn_decode_layer.restype = ctypes.c_int
     lib.gdn_decode_layer.argtypes = [S, ctypes.POINTER(GdnLayerParams), P, P, P, P, P, P, P, P, P,
                                      P, ctypes.c_float, P, P, P, P]
@@ -241,12 +242,13 @@ PREFILL_NOALLOC_SCRATCH_BYTES = 96 * 1024 * 1024
 
 def gdn_prefill_norm(q, k, v, a, b, A_log, dt_bias, state_in=None, cu_seqlens=None,
                      scale: float = 0.0, *, norm_scale, gate, eps: float = 1e-6,
-                     activation: str = "silu", y=None, state_out=None, workspace=None,
-                     stream=None):
+                     activation: str = "silu", fuse: bool = False, y=None, state_out=None,
+                     workspace=None, stream=None):
     """gdn_prefill, then the gated RMS norm of o over each d_v row; returns (y, state_out).
 
-    norm_scale [d_v] and gate (o's shape) in the io dtype; y has o's shape.  On the chunked
-    tensor-core path the norm runs in the scan's readout and o is never stored."""
+    norm_scale [d_v] and gate (o's shape) in the io dtype; y has o's shape.  fuse: run the
+    norm in the tensor-core scan's readout (o never stored) where the path allows; by
+    default the norm is a second launch, in place on y."""
     lib = load()
     shape = _shape_of(q, v, cu_seqlens)
     dt = q.dtype
@@ -284,7 +286,7 @@ def gdn_prefill_norm(q, k, v, a, b, A_log, dt_bias, state_in=None, cu_seqlens=No
     _check(lib.gdn_prefill_norm(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b),
                                 _ptr(A_log), _ptr(dt_bias), _ptr(state_in), _ptr(cu_seqlens),
                                 float(scale), _ptr(norm_scale), _ptr(gate), float(eps),
-                                ACTIVATIONS[activation], _ptr(y), _ptr(state_out),
+                                ACTIVATIONS[activation], int(bool(fuse)), _ptr(y), _ptr(state_out),
                                 _ptr(workspace), ws_bytes, _stream(stream)))
     return y, state_out
 

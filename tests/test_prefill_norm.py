@@ -1,8 +1,9 @@
 """GPU parity of gdn_prefill_norm -- the prefill followed by the gated RMS norm of its output
 over each d_v row (the CUDA page's linear_attention_core Steps 1-4, then the
-onnxruntime-ep-mlx ssm.rs page's GatedRMSNorm).  On the chunked tensor-core path the norm
-runs in the scan's readout, with the two column halves of a head as a cluster pair;
-elsewhere it is a second launch, in place.
+onnxruntime-ep-mlx ssm.rs page's GatedRMSNorm).  By default the norm is a second launch,
+in place on y; with fuse=True, on the chunked tensor-core path, it runs in the scan
+(the two column halves of a head as a cluster pair, the state warps norming each staged
+tile one chunk behind the readout).  Both forms are checked.
 
 References:
   * the float64 oracle chain: the oracle's scan, its o rounded to the I/O type (the GPU
@@ -43,7 +44,7 @@ def _norm_inputs(inp, activation, seed):
     return n.scale, n.gate, n.spec.eps
 
 
-def _fused(inp, scale, gate, eps, activation, gate_offset=0):
+def _fused(inp, scale, gate, eps, activation, gate_offset=0, fuse=True):
     from recurrent_state_scan_gb300 import gdn_last_device_status, gdn_prefill_norm
     d = to_device(inp)
     g = gate.cuda().view(d["v"].shape)
@@ -55,7 +56,7 @@ def _fused(inp, scale, gate, eps, activation, gate_offset=0):
     shape_o = d["v"].shape
     y, st = gdn_prefill_norm(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
                              d["state_in"], d["cu_seqlens"], inp.scale, norm_scale=scale.cuda(),
-                             gate=g, eps=eps, activation=activation)
+                             gate=g, eps=eps, activation=activation, fuse=fuse)
     torch.cuda.synchronize()
     assert gdn_last_device_status() == 0
     assert y.shape == shape_o
@@ -82,10 +83,10 @@ def _oracle(inp, scale, gate, eps, activation):
     return y_ref.reshape(-1, s.h_v, s.d_v), s_ref
 
 
-def _against_oracle(inp, activation, seed):
+def _against_oracle(inp, activation, seed, fuse=True):
     s = inp.spec
     scale, gate, eps = _norm_inputs(inp, activation, seed)
-    y, st = _fused(inp, scale, gate, eps, activation)
+    y, st = _fused(inp, scale, gate, eps, activation, fuse=fuse)
     y_ref, s_ref = _oracle(inp, scale, gate, eps, activation)
     ey = rel_err(y.float().cpu().numpy().reshape(-1, s.h_v, s.d_v), y_ref)
     es = rel_err(st.cpu().numpy(), s_ref)
@@ -93,10 +94,10 @@ def _against_oracle(inp, activation, seed):
     assert ey <= TOL[s.io] and es <= TOL[s.io]
 
 
-def _against_separate(inp, activation, seed, gate_offset=0):
+def _against_separate(inp, activation, seed, gate_offset=0, fuse=True):
     s = inp.spec
     scale, gate, eps = _norm_inputs(inp, activation, seed)
-    y, st = _fused(inp, scale, gate, eps, activation, gate_offset)
+    y, st = _fused(inp, scale, gate, eps, activation, gate_offset, fuse=fuse)
     y2, st2 = _separate(inp, scale, gate, eps, activation)
     a = y.double().cpu().numpy()
     b = y2.double().cpu().numpy()
@@ -106,22 +107,24 @@ def _against_separate(inp, activation, seed, gate_offset=0):
     assert torch.equal(st, st2)
 
 
+@pytest.mark.parametrize("fuse", [False, True])
 @pytest.mark.parametrize("io", ["bf16", "f16"])
 @pytest.mark.parametrize("activation", ["silu", "sigmoid"])
-def test_batched_against_the_oracle_chain(io, activation):
+def test_batched_against_the_oracle_chain(io, activation, fuse):
     """Two 300-token sequences (a ragged last chunk), GQA 2 -> 4 heads, an initial state."""
     inp = workloads.draw(workloads.small_spec(io=io, batch=2, seqlen=300, h_qk=2, h_v=4,
                                               d_k=128, d_v=128, state_std=0.05, seed=501))
-    _against_oracle(inp, activation, 601)
+    _against_oracle(inp, activation, 601, fuse=fuse)
 
 
-def test_packed_against_the_oracle_chain():
+@pytest.mark.parametrize("fuse", [False, True])
+def test_packed_against_the_oracle_chain(fuse):
     """Packed sequences of 1, 129, 64 and 250 tokens: rows of the next sequence share a
     chunk tile with a ragged last chunk, and are neither normed nor stored by it."""
     inp = workloads.draw(workloads.small_spec(io="bf16", lengths=(1, 129, 64, 250), h_qk=1,
                                               h_v=2, d_k=128, d_v=128, state_std=0.05,
                                               seed=502))
-    _against_oracle(inp, "silu", 602)
+    _against_oracle(inp, "silu", 602, fuse=fuse)
 
 
 @pytest.mark.parametrize("io", ["bf16", "f16"])
@@ -132,8 +135,9 @@ def test_equals_the_separate_calls(io):
 
 
 def test_gate_off_16_bytes_takes_the_second_launch():
-    """A gate 8 bytes past a 16-byte boundary: the tensor-core prefill writes o into y and
-    the norm runs after it, in place; same values as the fused readout."""
+    """fuse=True with a gate 8 bytes past a 16-byte boundary: the tensor-core prefill
+    writes o into y and the norm runs after it, in place; same values as the separate
+    calls."""
     inp = workloads.draw(workloads.small_spec(io="bf16", batch=2, seqlen=200, h_qk=2, h_v=2,
                                               d_k=128, d_v=128, state_std=0.05, seed=504))
     _against_separate(inp, "sigmoid", 604, gate_offset=4)
@@ -147,11 +151,12 @@ def test_off_the_tensor_core_path(io, d_k):
     _against_oracle(inp, "silu", 605)
 
 
+@pytest.mark.parametrize("fuse", [False, True])
 @pytest.mark.parametrize("name", ["varlen_bf16_prefill", "gqa_f16_prefill"])
-def test_full_size_against_the_separate_calls(name):
+def test_full_size_against_the_separate_calls(name, fuse):
     """Every element of the full-size packed and GQA workloads (32K and 16K tokens)."""
     inp = workloads.workload(name)
-    _against_separate(inp, "silu", 606)
+    _against_separate(inp, "silu", 606, fuse=fuse)
 
 
 def test_full_size_varlen_against_the_oracle_chain():

@@ -85,8 +85,8 @@ def test_short_wait_budget_times_out_the_conv_pipeline_then_recovers():
 
 @pytest.mark.gpu
 def test_short_wait_budget_times_out_the_norm_pairs_then_recovers():
-    """gdn_prefill_norm on the tensor-core path: the scan CTAs run as cluster pairs that
-    wait on each other for every chunk's row sums.  Under a short budget the waits run
+    """gdn_prefill_norm fused on the tensor-core path: the scan CTAs run as cluster pairs
+    that wait on each other for every chunk's row sums.  Under a short budget the waits run
     out, every CTA of a pair leaves (they meet at the cluster barrier on the way out) and
     the call reports GDN_ERR_TIMEOUT; the next call equals the separate calls."""
     if not torch.cuda.is_available():
@@ -103,13 +103,13 @@ def test_short_wait_budget_times_out_the_norm_pairs_then_recovers():
     assert gdn_last_device_status() == gdn.GDN_OK
     gdn.gdn_set_wait_budget(200)
     try:
-        gdn_prefill_norm(*args, norm_scale=scale, gate=gate, eps=1e-6)
+        gdn_prefill_norm(*args, norm_scale=scale, gate=gate, eps=1e-6, fuse=True)
         torch.cuda.synchronize()
         assert gdn_last_device_status() == gdn.GDN_ERR_TIMEOUT
     finally:
         gdn.gdn_set_wait_budget(0)
     assert gdn_last_device_status() == gdn.GDN_OK
-    y, st = gdn_prefill_norm(*args, norm_scale=scale, gate=gate, eps=1e-6)
+    y, st = gdn_prefill_norm(*args, norm_scale=scale, gate=gate, eps=1e-6, fuse=True)
     o, st2 = gdn_prefill(*args)
     y2 = gdn_gated_rmsnorm(o, scale, gate, 1e-6, "silu")
     torch.cuda.synchronize()
