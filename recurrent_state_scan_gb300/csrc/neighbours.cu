@@ -922,6 +922,72 @@ __global__ void __launch_bounds__(256) gated_rmsnorm_kernel(const NormParams p) 
     }
 }
 
+// Rows of 128 16-bit values: half a warp per row, 8 values (one 16-byte access) a lane,
+// and each warp takes 2 x RPW rows at a time, loading x and the gate of all of them before
+// the reductions (16 lanes, four shuffle steps).  The math is the other norm kernels'.
+template <typename IO, int RPW>
+__global__ void __launch_bounds__(256) gated_rmsnorm_w128_kernel(const NormParams p) {
+    static_assert(sizeof(IO) == 2, "16-bit I/O");
+    const IO *x = static_cast<const IO *>(p.x);
+    const IO *gate = static_cast<const IO *>(p.gate);
+    IO *y = static_cast<IO *>(p.y);
+    const int lane = threadIdx.x & 31, half = lane >> 4, col = (lane & 15) * 8;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    float sc[8];
+    {
+        const uint4 raw = *reinterpret_cast<const uint4 *>(static_cast<const IO *>(p.scale) + col);
+        const IO *h = reinterpret_cast<const IO *>(&raw);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sc[e] = IoType<IO>::ld(h + e);
+    }
+    for (int64_t r0 = (blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5)) * (2 * RPW);
+         r0 < p.rows; r0 += warps * (2 * RPW)) {
+        uint4 xr[RPW], gr[RPW];
+#pragma unroll
+        for (int k = 0; k < RPW; ++k) {
+            const int64_t r = r0 + 2 * k + half;
+            xr[k] = gr[k] = make_uint4(0u, 0u, 0u, 0u);
+            if (r < p.rows) {
+                xr[k] = *reinterpret_cast<const uint4 *>(x + r * 128 + col);
+                gr[k] = *reinterpret_cast<const uint4 *>(gate + r * 128 + col);
+            }
+        }
+        float ss[RPW];
+#pragma unroll
+        for (int k = 0; k < RPW; ++k) {
+            const IO *h = reinterpret_cast<const IO *>(&xr[k]);
+            ss[k] = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float v = IoType<IO>::ld(h + e);
+                ss[k] = fmaf(v, v, ss[k]);
+            }
+        }
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1)
+#pragma unroll
+            for (int k = 0; k < RPW; ++k) ss[k] += __shfl_xor_sync(0xffffffffu, ss[k], off);
+#pragma unroll
+        for (int k = 0; k < RPW; ++k) {
+            const int64_t r = r0 + 2 * k + half;
+            if (r >= p.rows) continue;
+            const float inv = rsqrtf(ss[k] / 128.0f + p.eps);
+            const IO *hx = reinterpret_cast<const IO *>(&xr[k]);
+            const IO *hg = reinterpret_cast<const IO *>(&gr[k]);
+            uint4 out;
+            IO *ho = reinterpret_cast<IO *>(&out);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float g = IoType<IO>::ld(hg + e);
+                const float sg = sigmoid_fast(g);
+                const float act = p.activation == GDN_ACT_SILU ? g * sg : sg;
+                IoType<IO>::st(ho + e, IoType<IO>::ld(hx + e) * inv * sc[e] * act);
+            }
+            *reinterpret_cast<uint4 *>(y + r * 128 + col) = out;
+        }
+    }
+}
+
 // Rows of at most 32 * VEC values: a lane holds VEC values of a row, and a warp takes
 // RPW consecutive rows at a time, reading x and the gate of all of them before reducing,
 // so 2 * RPW loads per lane are in flight.
@@ -1128,6 +1194,16 @@ cudaError_t launch_norm_io(const NormParams &p, bool vec4, cudaStream_t stream) 
     const int64_t threads = p.rows * 32;
     if (threads == 0) return cudaSuccess;
     constexpr int RPW = 4;
+    if constexpr (sizeof(IO) == 2) {
+        // Rows of 128 with every pointer 16-byte aligned: half a warp per row.
+        const bool a16 = ((reinterpret_cast<uintptr_t>(p.x) | reinterpret_cast<uintptr_t>(p.gate) |
+                           reinterpret_cast<uintptr_t>(p.y) | reinterpret_cast<uintptr_t>(p.scale)) & 15) == 0;
+        if (p.width == 128 && a16) {
+            gated_rmsnorm_w128_kernel<IO, RPW>
+                <<<grid_for((p.rows + 2 * RPW - 1) / (2 * RPW) * 32, 256), 256, 0, stream>>>(p);
+            return cudaGetLastError();
+        }
+    }
     if (vec4 && p.width <= 128)
         gated_rmsnorm_rows_kernel<IO, 4, RPW>
             <<<grid_for((p.rows + RPW - 1) / RPW * 32, 256), 256, 0, stream>>>(p);

@@ -291,6 +291,24 @@ def test_norm_matches_oracle(io, width, activation):
     _close(_run_norm(inp), _norm_ref(inp), io)
 
 
+def test_norm_rows_of_128_off_16_bytes():
+    """16-bit rows of 128 take the half-warp kernel when every pointer is 16-byte aligned;
+    x and y 8 bytes off that boundary take the four-rows-a-warp kernel, same values."""
+    from recurrent_state_scan_gb300 import gdn_gated_rmsnorm
+    inp = _norm_case("bf16", (7, 9, 128), seed=11)
+    ref = _norm_ref(inp)
+    x = inp.x.cuda()
+    buf = torch.empty(x.numel() + 4, dtype=x.dtype, device="cuda")
+    xo = buf[4:].view(x.shape)
+    xo.copy_(x)
+    assert xo.data_ptr() % 16 == 8
+    y = gdn_gated_rmsnorm(xo, inp.scale.cuda(), inp.gate.cuda(), inp.spec.eps, "silu")
+    y16 = gdn_gated_rmsnorm(x, inp.scale.cuda(), inp.gate.cuda(), inp.spec.eps, "silu")
+    torch.cuda.synchronize()
+    _close(y, ref, "bf16")
+    _close(y16, ref, "bf16")
+
+
 def test_norm_in_place_and_eps():
     inp = _norm_case("bf16", (5, 4, 128), eps=0.5, seed=9)
     ref = _norm_ref(inp)
