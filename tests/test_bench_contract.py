@@ -49,6 +49,15 @@ def test_neighbour_bytes():
     assert b == {"x": m, "gate": m, "y": m, "scale": 128 * 2}
 
 
+def test_prefill_norm_bytes():
+    """The prefill's bytes with o replaced by y, plus the gate and the norm scale."""
+    inp = workloads.any_workload("varlen_bf16_prefill_norm")
+    b = bench.prefill_norm_io_bytes(inp)
+    o = 31979 * 16 * 128 * 2
+    assert "o" not in b and b["y"] == o and b["gate"] == o and b["norm_scale"] == 128 * 2
+    assert sum(b.values()) == bench.algorithmic_bytes(inp.prefill) + o + 128 * 2
+
+
 def test_neighbour_sample_is_bounded():
     inp = workloads.any_workload("bf16_conv_prefill_gqa")
     small, what = bench.neighbour_sample(inp)
@@ -87,6 +96,12 @@ def test_reference_arm_neighbour_workload():
     d = _reference_line("bf16_conv_decode_b256")
     _check_line(d, "bf16_conv_decode_b256")
     assert d["unit"] == "GB/s"
+
+
+def test_reference_arm_prefill_norm_workload():
+    d = _reference_line("varlen_bf16_prefill_norm")
+    _check_line(d, "varlen_bf16_prefill_norm")
+    assert d["unit"] == "tokens/s" and "of 31979 tokens" in d["cpu_baseline"]["sample"]
 
 
 def test_reference_arm_under_torchrun_prints_one_line():
