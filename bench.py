@@ -67,9 +67,12 @@ def io_bytes(inp) -> dict:
     n = inp.n_seq
     st = n * s.h_v * s.d_k * s.d_v * 4
     per = s.h_v * (s.d_k if s.decay_per_key else 1)   # decay gates per token
+    decay = getattr(s, "rule", "gated_delta") in ("gated_delta", "gated")
+    delta = getattr(s, "rule", "gated_delta") in ("gated_delta", "delta")
     return {
         "q": T * s.h_qk * s.d_k * es, "k": T * s.h_qk * s.d_k * es, "v": T * s.h_v * s.d_v * es,
-        "a": T * per * es, "b": T * (1 if s.beta_shared else s.h_v) * es, "params": 2 * per * 4,
+        "a": T * per * es if decay else 0, "b": T * (1 if s.beta_shared else s.h_v) * es if delta else 0,
+        "params": 2 * per * 4 if decay else 0,
         "state_in": st if (inp.state_in is not None or inp.pool is not None) else 0,
         "o": T * s.h_v * s.d_v * es, "state_out": st * (s.window if s.window else 1),
         "slots": 4 * n if inp.pool is not None else 0,
@@ -897,7 +900,8 @@ def main_prefill_norm(args, rank, world, local):
 
 def run_ours(args, rank, world, local, name=None, with_e2e=True):
     from recurrent_state_scan_gb300 import (gdn_decode_step, gdn_decode_step_slots, gdn_prefill,
-                                            gdn_scan_variant, gdn_scan_window, load)
+                                            gdn_prefill_variant, gdn_scan_variant, gdn_scan_window,
+                                            load)
     load()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -922,10 +926,16 @@ def run_ours(args, rank, world, local, name=None, with_e2e=True):
     ws = torch.empty(ws_need, dtype=torch.uint8, device=dev) if ws_need else None
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    variant = s.decay_per_key or s.beta_shared
+    variant = s.decay_per_key or s.beta_shared or s.rule != "gated_delta"
 
     def step():
-        if variant:
+        if variant and not s.decode:
+            # Prefill variants take gdn_prefill's path (per-key decay: token-sequential).
+            gdn_prefill_variant(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"], t["dt_bias"],
+                                state0, cu, inp.scale, rule=s.rule, decay_per_key=s.decay_per_key,
+                                beta_shared=s.beta_shared, o=o, state_out=state_out, workspace=ws,
+                                stream=stream)
+        elif variant:
             # Decode steps update the state in place; prefill writes state_out.
             gdn_scan_variant(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"], t["dt_bias"],
                              work_state if s.decode else state0, cu, inp.scale,
@@ -986,7 +996,14 @@ def run_ours(args, rank, world, local, name=None, with_e2e=True):
         def e2e_step():
             for n, v in host.items():
                 dbuf[n].copy_(v, non_blocking=True)
-            if variant:
+            if variant and not s.decode:
+                gdn_prefill_variant(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["a"], dbuf["b"],
+                                    dbuf["A_log"], dbuf["dt_bias"], dbuf.get("state"), cu, inp.scale,
+                                    rule=s.rule, decay_per_key=s.decay_per_key,
+                                    beta_shared=s.beta_shared, o=o, state_out=state_out,
+                                    workspace=ws, stream=stream)
+                s_host.copy_(state_out, non_blocking=True)
+            elif variant:
                 st_out = dbuf["state"] if s.decode else state_out
                 gdn_scan_variant(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["a"], dbuf["b"],
                                  dbuf["A_log"], dbuf["dt_bias"], dbuf.get("state"), cu, inp.scale,
@@ -1156,6 +1173,8 @@ def prefill_kernels(inp) -> str:
         if inp.spec.window:
             return "scan_simt_kernel, one call"
         return "decode_stream_kernel (persistent, prefetching), one call"
+    if inp.spec.decay_per_key:
+        return "scan_simt_kernel (per-key-dim decay), one call"
     path, _ = gdn.gdn_prefill_plan(gdn.shape_of_spec(inp.spec, inp.n_seq, inp.total_tokens))
     if path == gdn.PATH_TC_TP:
         return ("gdn_chunk_prep + gdn_chunk_scan (time-parallel segments) + gdn_tp_combine "
@@ -1186,10 +1205,10 @@ def config_of(inp, world):
         c["lengths"] = [int(x) for x in inp.lengths()]
     else:
         c["batch"], c["seq_len"] = s.batch, s.seqlen
-    if s.decay_per_key or s.beta_shared:
+    if s.decay_per_key or s.beta_shared or s.rule != "gated_delta":
         c["gates"] = {"decay": "per key dimension" if s.decay_per_key else "per head",
                       "beta": "shared by all heads" if s.beta_shared else "per head",
-                      "rule": "gated_delta"}
+                      "rule": s.rule}
     if inp.pool is not None:
         c["initial_state"] = "pool of %d states, N(0,%g)" % (s.pool_size, s.pool_std)
         c["state_pool"] = {"entries": s.pool_size, "slots": "distinct, seeded permutation",

@@ -142,11 +142,13 @@ def scan(cu_seqlens: Sequence[int], h_qk: int, h_v: int, d_k: int, d_v: int,
     return o.reshape(total, h_v, d_v), s_out.reshape(max(n_seq, 0), h_v, d_k, d_v)
 
 
-def scan_inputs(inp, units=None, threads: int = 1, rule: str = "gated_delta"):
+def scan_inputs(inp, units=None, threads: int = 1, rule: Optional[str] = None):
     """Run the oracle on a drawn ``workloads.Inputs`` (the float64 copies), with the
-    spec's gate layout (per-key decay, shared beta)."""
+    spec's gate layout (per-key decay, shared beta) and update rule (``rule`` overrides
+    it)."""
     s = inp.spec
     f = inp.f64
+    rule = rule or getattr(s, "rule", "gated_delta")
     return scan(inp.cu_seqlens, s.h_qk, s.h_v, s.d_k, s.d_v, f["q"], f["k"], f["v"],
                 a=f["a"], b=f["b"], A_log=f["A_log"], dt_bias=f["dt_bias"],
                 state_in=f["state_in"], scale=inp.scale, rule=rule, units=units,

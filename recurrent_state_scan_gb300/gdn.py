@@ -361,10 +361,10 @@ def shape_of_spec(spec, n_seq: int, total_tokens: int) -> GdnShape:
 
 
 def _simt_only(spec) -> bool:
-    """Specs that run the token-sequential kernel alone: decode, state windows and the
-    gate variants of gdn_scan_variant."""
-    return bool(spec.decode or getattr(spec, "window", 0) or getattr(spec, "decay_per_key", False)
-                or getattr(spec, "beta_shared", False))
+    """Specs that run the token-sequential kernel alone: decode, state windows and
+    per-key-dim decay (the rules and the shared beta of a prefill take gdn_prefill's path
+    through gdn_prefill_variant)."""
+    return bool(spec.decode or getattr(spec, "window", 0) or getattr(spec, "decay_per_key", False))
 
 
 def gdn_set_wait_budget(cycles: int) -> None:

@@ -49,6 +49,17 @@ def test_neighbour_bytes():
     assert b == {"x": m, "gate": m, "y": m, "scale": 128 * 2}
 
 
+def test_rule_variant_bytes():
+    """Rules without decay read no a, A_log or dt_bias; rules without the delta term no b;
+    a shared beta is one value per token."""
+    d = bench.io_bytes(workloads.workload("bf16_delta_prefill_t4096"))
+    assert d["a"] == 0 and d["params"] == 0 and d["b"] == 4096 * 16 * 2
+    sb = bench.io_bytes(workloads.workload("bf16_shared_beta_prefill_t4096"))
+    assert sb["b"] == 4096 * 2 and sb["a"] == 4096 * 16 * 2
+    pk = bench.io_bytes(workloads.workload("bf16_perkey_prefill_t4096"))
+    assert pk["a"] == 4096 * 16 * 128 * 2 and pk["params"] == 2 * 16 * 128 * 4
+
+
 def test_prefill_norm_bytes():
     """The prefill's bytes with o replaced by y, plus the gate and the norm scale."""
     inp = workloads.any_workload("varlen_bf16_prefill_norm")

@@ -316,7 +316,10 @@ def test_workload_recipe():
     w = workloads.WORKLOADS
     assert set(w) == {"tiny_f32_prefill", "bf16_prefill_t4096", "bf16_decode_b256",
                       "varlen_bf16_prefill", "gqa_f16_prefill", "bf16_slot_decode_b256",
-                      "bf16_window_b256_t4", "bf16_perkey_decode_b256"}
+                      "bf16_window_b256_t4", "bf16_perkey_decode_b256", "bf16_delta_prefill_t4096",
+                      "bf16_shared_beta_prefill_t4096", "bf16_perkey_prefill_t4096"}
+    assert w["bf16_delta_prefill_t4096"].rule == "delta"
+    assert all(w[n].rule == "gated_delta" for n in w if n != "bf16_delta_prefill_t4096")
     assert set(workloads.CONV_WORKLOADS) == {"bf16_conv_prefill_gqa", "bf16_conv_decode_b256"}
     assert set(workloads.NORM_WORKLOADS) == {"bf16_norm_gqa"}
     cv = workloads.draw_conv(workloads.ConvSpec("t", "bf16", 2, 5, 8, 3, state_std=1.0,

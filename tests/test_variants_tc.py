@@ -99,3 +99,16 @@ def test_per_key_decay_through_the_prefill_entry_point():
                                               d_k=128, d_v=128, state_std=0.05, seed=315,
                                               decay_per_key=True))
     _check(inp, "gated_delta", "per-key decay")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["bf16_delta_prefill_t4096", "bf16_shared_beta_prefill_t4096",
+                                  "bf16_perkey_prefill_t4096"])
+def test_full_size_variant_workloads(name):
+    """The measured prefill-length variants, every element against the oracle: the delta
+    rule and the shared beta on the tensor-core path (time-parallel at this shape),
+    per-key decay on the token-sequential kernel."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    inp = workloads.workload(name)
+    _check(inp, inp.spec.rule, name)

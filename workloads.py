@@ -49,6 +49,7 @@ class Spec:
     window: int = 0              # > 0: emit the states after the last `window` steps
     decay_per_key: bool = False  # a [B,T,h_v,d_k], A_log and dt_bias [h_v,d_k]
     beta_shared: bool = False    # b [B,T,1]: one beta for every head
+    rule: str = "gated_delta"    # the update rule (gated_delta, delta, gated, linear)
 
 
 # The five workloads the method is measured on.
@@ -82,6 +83,18 @@ WORKLOADS = {
     "bf16_perkey_decode_b256": Spec(
         "bf16_perkey_decode_b256", io="bf16", batch=256, seqlen=1, h_qk=32, h_v=32,
         d_k=128, d_v=128, seed=1007, state_std=0.05, decode=True, decay_per_key=True),
+    # The gate-variant row at prefill length, on the 4,096-token shape: the delta rule and
+    # one shared beta run on the chunked tensor-core path, per-key decay on the
+    # token-sequential kernel.
+    "bf16_delta_prefill_t4096": Spec(
+        "bf16_delta_prefill_t4096", io="bf16", batch=1, seqlen=4096, h_qk=16, h_v=16,
+        d_k=128, d_v=128, seed=1008, rule="delta"),
+    "bf16_shared_beta_prefill_t4096": Spec(
+        "bf16_shared_beta_prefill_t4096", io="bf16", batch=1, seqlen=4096, h_qk=16, h_v=16,
+        d_k=128, d_v=128, seed=1009, beta_shared=True),
+    "bf16_perkey_prefill_t4096": Spec(
+        "bf16_perkey_prefill_t4096", io="bf16", batch=1, seqlen=4096, h_qk=16, h_v=16,
+        d_k=128, d_v=128, seed=1015, decay_per_key=True),
 }
 
 
