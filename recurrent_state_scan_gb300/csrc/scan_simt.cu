@@ -103,33 +103,66 @@ __global__ void __launch_bounds__(kThreads, (simt_min_blocks<DKMAX, kThreads>())
     const bool has_decay = (p.rule == GDN_RULE_GATED_DELTA || p.rule == GDN_RULE_GATED);
     const bool has_delta = (p.rule == GDN_RULE_GATED_DELTA || p.rule == GDN_RULE_DELTA);
 
+    // The inputs of token t + 1 are loaded into registers while token t is computed, so a
+    // token's loads are not on the chain: this thread's q and k entries (and per-key decay
+    // logits), its v column, and the scalar gate logits.
+    constexpr int QPT = (DKMAX + kThreads - 1) / kThreads;   // q / k entries a thread loads
+    float nq[QPT], nk[QPT], na[kPerKey ? QPT : 1], nv = 0.f, ng_a = 0.f, ng_b = 0.f;
+    float pA[kPerKey ? QPT : 1], pD[kPerKey ? QPT : 1];     // this thread's per-key A_log, dt_bias
+#pragma unroll
+    for (int u = 0; u < QPT; ++u) {
+        nq[u] = nk[u] = 0.f;
+        if (kPerKey) na[u] = pA[u] = pD[u] = 0.f;
+    }
+    if (kPerKey) {
+        const size_t hk = (size_t)h * p.d_k;
+#pragma unroll
+        for (int u = 0; u < QPT; ++u) {
+            const int i = tid + u * kThreads;
+            if (i < p.d_k) {
+                pA[u] = p.A_log[hk + i];
+                pD[u] = p.dt_bias[hk + i];
+            }
+        }
+    }
+    auto load_token = [&](int64_t t) {
+        const size_t qk_off = ((size_t)t * p.h_qk + hq) * p.d_k;
+#pragma unroll
+        for (int u = 0; u < QPT; ++u) {
+            const int i = tid + u * kThreads;
+            nq[u] = i < p.d_k ? IoType<IO>::ld(q + qk_off + i) : 0.f;
+            nk[u] = i < p.d_k ? IoType<IO>::ld(k + qk_off + i) : 0.f;
+            if (kPerKey)
+                na[u] = (has_decay && i < p.d_k) ? IoType<IO>::ld(ga + ((size_t)t * p.h_v + h) * p.d_k + i) : 0.f;
+        }
+        if (tid < TILE) {
+            const int c = tile * TILE + tid;
+            nv = c < p.d_v ? IoType<IO>::ld(v + ((size_t)t * p.h_v + h) * p.d_v + c) : 0.f;
+        }
+        const size_t gi = (size_t)t * p.h_v + h;
+        if (tid == 0 && has_decay && !kPerKey) ng_a = IoType<IO>::ld(ga + gi);
+        if (tid == kBetaThread && has_delta) ng_b = IoType<IO>::ld(gb + (p.beta_shared ? (size_t)t : gi));
+    };
+    if (t0 < t1) load_token(t0);
+
     for (int64_t t = t0; t < t1; ++t) {
         __syncthreads();   // previous token's shared values are no longer read
-        const size_t qk_off = ((size_t)t * p.h_qk + hq) * p.d_k;
-        for (int i = tid; i < DKMAX; i += kThreads) {
-            sq[i] = i < p.d_k ? IoType<IO>::ld(q + qk_off + i) : 0.f;
-            sk[i] = i < p.d_k ? IoType<IO>::ld(k + qk_off + i) : 0.f;
-        }
         const size_t v_off = ((size_t)t * p.h_v + h) * p.d_v;
-        for (int j = tid; j < TILE; j += kThreads) {
-            const int c = tile * TILE + j;
-            sv[j] = c < p.d_v ? IoType<IO>::ld(v + v_off + c) : 0.f;
+#pragma unroll
+        for (int u = 0; u < QPT; ++u) {
+            const int i = tid + u * kThreads;
+            if (i < DKMAX) {
+                sq[i] = nq[u];
+                sk[i] = nk[u];
+                if (kPerKey)
+                    sa[i] = (has_decay && i < p.d_k) ? expf(decay_f(na[u], pA[u], pD[u])) : 1.f;
+            }
         }
-        // The two scalar gates come from two different warps, so their loads overlap.
-        const size_t gi = (size_t)t * p.h_v + h;
-        if (tid == 0)
-            s_alpha = (has_decay && !kPerKey)
-                          ? expf(decay_f(IoType<IO>::ld(ga + gi), p.A_log[h], p.dt_bias[h]))
-                          : 1.f;
-        if (tid == kBetaThread)
-            s_beta = has_delta ? sigmoid_f(IoType<IO>::ld(gb + (p.beta_shared ? (size_t)t : gi))) : 1.f;
-        if (kPerKey) {
-            const size_t gk = ((size_t)t * p.h_v + h) * p.d_k, hk = (size_t)h * p.d_k;
-            for (int i = tid; i < DKMAX; i += kThreads)
-                sa[i] = (has_decay && i < p.d_k)
-                            ? expf(decay_f(IoType<IO>::ld(ga + gk + i), p.A_log[hk + i], p.dt_bias[hk + i]))
-                            : 1.f;
-        }
+        if (tid < TILE) sv[tid] = nv;
+        // The two scalar gates come from two different warps.
+        if (tid == 0) s_alpha = (has_decay && !kPerKey) ? expf(decay_f(ng_a, p.A_log[h], p.dt_bias[h])) : 1.f;
+        if (tid == kBetaThread) s_beta = has_delta ? sigmoid_f(ng_b) : 1.f;
+        if (t + 1 < t1) load_token(t + 1);
         __syncthreads();
 
         // Partial retrieval S^T k and readout S^T q over this thread's rows.
