@@ -921,8 +921,8 @@ def run_ours(args, rank, world, local, name=None, with_e2e=True):
     window = None
     if s.window:
         window = torch.empty((s.window,) + n_state, dtype=torch.float32, device=dev)
-    ws_need = 0 if (s.decode or s.window) else gdn.gdn_prefill_workspace_bytes(
-        gdn.shape_of_spec(s, inp.n_seq, inp.total_tokens))
+    ws_need = 0 if (s.decode or s.window) else gdn.gdn_prefill_variant_workspace_bytes(
+        gdn.shape_of_spec(s, inp.n_seq, inp.total_tokens), s.rule, s.decay_per_key, s.beta_shared)
     ws = torch.empty(ws_need, dtype=torch.uint8, device=dev) if ws_need else None
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -930,7 +930,7 @@ def run_ours(args, rank, world, local, name=None, with_e2e=True):
 
     def step():
         if variant and not s.decode:
-            # Prefill variants take gdn_prefill's path (per-key decay: token-sequential).
+            # Prefill variants take gdn_prefill's path (per-key decay with its larger workspace).
             gdn_prefill_variant(t["q"], t["k"], t["v"], t["a"], t["b"], t["A_log"], t["dt_bias"],
                                 state0, cu, inp.scale, rule=s.rule, decay_per_key=s.decay_per_key,
                                 beta_shared=s.beta_shared, o=o, state_out=state_out, workspace=ws,
@@ -1173,14 +1173,15 @@ def prefill_kernels(inp) -> str:
         if inp.spec.window:
             return "scan_simt_kernel, one call"
         return "decode_stream_kernel (persistent, prefetching), one call"
-    if inp.spec.decay_per_key:
-        return "scan_simt_kernel (per-key-dim decay), one call"
-    path, _ = gdn.gdn_prefill_plan(gdn.shape_of_spec(inp.spec, inp.n_seq, inp.total_tokens))
+    s = inp.spec
+    prep = "gdn_chunk_prep_pk (per-key-dim decay)" if s.decay_per_key else "gdn_chunk_prep"
+    path, _ = gdn.gdn_prefill_variant_plan(gdn.shape_of_spec(s, inp.n_seq, inp.total_tokens),
+                                           s.rule, s.decay_per_key, s.beta_shared)
     if path == gdn.PATH_TC_TP:
-        return ("gdn_chunk_prep + gdn_chunk_scan (time-parallel segments) + gdn_tp_combine "
+        return (f"{prep} + gdn_chunk_scan (time-parallel segments) + gdn_tp_combine "
                 "+ gdn_tp_correct, one call")
     if path == gdn.PATH_TC:
-        return "gdn_chunk_prep + gdn_chunk_scan, one call"
+        return f"{prep} + gdn_chunk_scan, one call"
     return "scan_simt, one call"
 
 

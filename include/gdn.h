@@ -39,7 +39,8 @@
  * Entry points: gdn_prefill (and gdn_prefill_noalloc, gdn_prefill_plan,
  * gdn_prefill_workspace_bytes), gdn_decode_step, gdn_decode_step_slots (a state
  * pool), gdn_scan_window (the states after each of the last W steps),
- * gdn_scan_variant and gdn_prefill_variant (other update rules and gate layouts),
+ * gdn_scan_variant and gdn_prefill_variant (other update rules and gate layouts; with
+ * gdn_prefill_variant_workspace_bytes and gdn_prefill_variant_plan),
  * the layer ops around the scan: gdn_causal_conv, gdn_causal_conv_slots and
  * gdn_gated_rmsnorm, gdn_prefill_norm (the prefill and the norm in one call) and
  * gdn_decode_layer (conv -> decode step -> norm in one kernel).
@@ -238,16 +239,40 @@ gdn_status gdn_scan_window(const gdn_shape *shape, const void *q, const void *k,
  * the variants and how they shape a, b, A_log and dt_bias), taking the path gdn_prefill
  * takes: for 16-bit I/O at d_k = d_v = 128 the chunked tensor-core prefill, on which the
  * four update rules and the shared beta are switches of the same algebra (no decay:
- * g = 0; no delta term: A = 0, beta = 1 and W = 0, so the chunk update adds K^T V).  A
- * per-key-dim decay runs the token-sequential path, which needs no workspace.  workspace
- * and workspace_bytes are gdn_prefill's (gdn_prefill_workspace_bytes sizes them for the
- * same shape).  Errors are gdn_scan_variant's plus gdn_prefill's workspace rule.
+ * g = 0; no delta term: A = 0, beta = 1 and W = 0, so the chunk update adds K^T V).
+ * A per-key-dim decay (Step 1 scaling row i of the state by e^{g_i}) runs there too, with
+ * the gates inside the operands: the chunk's A and P entries are sums over the key
+ * dimension of k_t k_s e^{G_t - G_s} (G the running decay sum per dimension), formed on
+ * the FP32 cores, and Q and K reach the state scan scaled by e^G and e^{G_C - G}.  That
+ * needs the larger workspace gdn_prefill_variant_workspace_bytes reports (two arrays of
+ * tokens x h_v x 128 16-bit values more); with only gdn_prefill_workspace_bytes, or off
+ * the tensor-core shapes, a per-key decay runs the token-sequential path.  workspace and
+ * workspace_bytes are otherwise gdn_prefill's.  Errors are gdn_scan_variant's plus
+ * gdn_prefill's workspace rule.
  */
 gdn_status gdn_prefill_variant(const gdn_shape *shape, const gdn_variant *variant, const void *q,
                                const void *k, const void *v, const void *a, const void *b,
                                const float *A_log, const float *dt_bias, const float *state_in,
                                const int32_t *cu_seqlens, float scale, void *o, float *state_out,
                                void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * gdn_prefill_variant_workspace_bytes -- the workspace gdn_prefill_variant needs for
+ * `shape` and `variant` to take its fastest path: gdn_prefill_workspace_bytes(shape), plus,
+ * for a per-key-dim decay with a decaying rule, 2 x seqlen x batch x h_v x 128 x 2 bytes
+ * (rounded up to 1 KiB each) for the scaled Q and K.  0 when the shape is off the
+ * tensor-core path; never fails (a NULL variant reads as the default one).
+ */
+size_t gdn_prefill_variant_workspace_bytes(const gdn_shape *shape, const gdn_variant *variant);
+
+/*
+ * gdn_prefill_variant_plan -- gdn_prefill_plan for gdn_prefill_variant with a workspace of
+ * gdn_prefill_variant_workspace_bytes: every rule, the shared beta and the per-key-dim
+ * decay take the same kernel path and launch count as the default rule.  Errors:
+ * GDN_ERR_INVALID_ARG for a NULL variant or an unknown rule, else gdn_prefill_plan's.
+ */
+gdn_status gdn_prefill_variant_plan(const gdn_shape *shape, const gdn_variant *variant, int32_t *path,
+                                    int32_t *launches);
 
 /*
  * gdn_scan_variant -- gdn_prefill with the gate and rule variants of the

@@ -7,5 +7,6 @@ from .gdn import (GdnError, GdnShape, gdn_causal_conv, gdn_causal_conv_slots,  #
                   gdn_decode_layer, gdn_decode_step, gdn_decode_step_slots, gdn_gated_rmsnorm,
                   gdn_last_device_status,
                   gdn_prefill, gdn_prefill_noalloc, gdn_prefill_norm, gdn_prefill_variant,
+                  gdn_prefill_variant_plan, gdn_prefill_variant_workspace_bytes,
                   gdn_prefill_workspace_bytes,
                   gdn_scan_variant, gdn_scan_window, gdn_status_string, load)

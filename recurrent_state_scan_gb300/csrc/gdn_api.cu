@@ -175,6 +175,23 @@ size_t gdn_prefill_workspace_bytes(const gdn_shape *shape) {
     return records + prefill_tc_tp_bytes(false, shape->seqlen, shape->batch, shape->h_v);
 }
 
+size_t gdn_prefill_variant_workspace_bytes(const gdn_shape *shape, const gdn_variant *variant) {
+    const size_t base = gdn_prefill_workspace_bytes(shape);
+    if (base == 0 || variant == nullptr || !variant->decay_per_key) return base;
+    if (variant->rule != GDN_RULE_GATED_DELTA && variant->rule != GDN_RULE_GATED) return base;
+    // Q o e^G and K o e^{G_C - G} per value head, for the packed or batched reading alike.
+    return base + prefill_tc_pk_bytes(shape->seqlen * (int64_t)shape->batch, shape->h_v);
+}
+
+gdn_status gdn_prefill_variant_plan(const gdn_shape *shape, const gdn_variant *variant, int32_t *path,
+                                    int32_t *launches) {
+    if (variant == nullptr) return fail(GDN_ERR_INVALID_ARG, "variant is NULL");
+    if (variant->rule < GDN_RULE_GATED_DELTA || variant->rule > GDN_RULE_LINEAR)
+        return fail(GDN_ERR_INVALID_ARG, "rule %d is not a gdn_rule", variant->rule);
+    // Every variant takes gdn_prefill's path, given gdn_prefill_variant_workspace_bytes.
+    return gdn_prefill_plan(shape, path, launches);
+}
+
 gdn_status gdn_set_wait_budget(int64_t cycles) {
     if (cycles < 0) return fail(GDN_ERR_INVALID_ARG, "wait budget %lld < 0", (long long)cycles);
     __atomic_store_n(&g_wait_budget, (long long)cycles, __ATOMIC_RELAXED);
@@ -274,7 +291,14 @@ gdn_status gdn::prefill_impl(const gdn_shape *shape, const void *q, const void *
     const gdn_dtype io = (gdn_dtype)shape->io_dtype;
     cudaError_t e;
     bool norm_after = norm != nullptr && tokens > 0;   // the norm as its own launch, in place
-    if (!p.decay_per_key && prefill_tc_supported(p, io, tokens)) {
+    // One decay per key dimension (with a decaying rule) takes the tensor-core path when
+    // the workspace also holds its Q~ and K~ arrays, else the token-sequential one.
+    const bool per_key = p.decay_per_key && (p.rule == GDN_RULE_GATED_DELTA || p.rule == GDN_RULE_GATED);
+    const size_t pk_bytes = per_key ? prefill_tc_pk_bytes(tokens, shape->h_v) : 0;
+    const size_t records = prefill_tc_workspace(cu_seqlens != nullptr, shape->seqlen, shape->batch,
+                                                shape->num_seqs, shape->h_v);
+    const bool pk_room = !per_key || (workspace != nullptr && workspace_bytes >= records + pk_bytes);
+    if (pk_room && prefill_tc_supported(p, io, tokens)) {
         if (norm_after && norm->fuse && aligned(norm->gate, 16)) {
             p.norm_scale = norm->scale;
             p.norm_gate = norm->gate;
@@ -282,8 +306,7 @@ gdn_status gdn::prefill_impl(const gdn_shape *shape, const void *q, const void *
             p.norm_silu = norm->activation == GDN_ACT_SILU;
             norm_after = false;
         }
-        const size_t need = prefill_tc_workspace(cu_seqlens != nullptr, shape->seqlen, shape->batch,
-                                                 shape->num_seqs, shape->h_v);
+        const size_t need = records + pk_bytes;
         if (workspace == nullptr || workspace_bytes < need)
             return fail(GDN_ERR_INVALID_ARG, "workspace of %zu bytes is below the %zu this call needs",
                         workspace == nullptr ? (size_t)0 : workspace_bytes, need);

@@ -160,6 +160,9 @@ size_t prefill_records_bytes_for(const gdn_shape *shape, bool varlen);
 // segments it uses (1: none) and the workspace bytes it needs after the records (0: none).
 int prefill_tc_tp_nseg(bool varlen, int64_t seqlen, int64_t batch, int h_v);
 size_t prefill_tc_tp_bytes(bool varlen, int64_t seqlen, int64_t batch, int h_v);
+// One decay per key dimension on the tensor-core path: the bytes of the Q~ and K~ arrays
+// ([tokens][h_v][128] in a 16-bit type, each 1 KiB aligned) that follow the records.
+size_t prefill_tc_pk_bytes(int64_t total_tokens, int h_v);
 // workspace_bytes: the caller's workspace size; the time-parallel scan runs only when the
 // workspace also holds its buffers (and allow_overlap is set).
 cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_tokens,

@@ -107,6 +107,12 @@ struct TcParams {
     const void *norm_gate;          // [tokens][h_v][128] I/O type, 16-byte aligned
     float norm_eps;
     int32_t norm_silu;              // act = silu (1) or sigmoid (0)
+    // One decay per key dimension (gdn_chunk_prep_pk): the prep writes Q o e^G and
+    // K o e^{G_C - G} to qt and kt ([tokens][h_v][128], I/O type), and the scan reads its
+    // Q and K through tm_qt and tm_kt instead of tm_q and tm_k.
+    int32_t per_key;
+    void *qt, *kt;
+    CUtensorMap tm_qt, tm_kt;
 };
 
 // First workspace slot of sequence n.  Batched: n * chunks_per_seq.  Packed: slot
@@ -778,6 +784,576 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
     }
 }
 
+// ===================================================================== chunk prep, per-key decay
+// One decay per key dimension (the CUDA page's decay_per_key_dim: Step 1 scales row i of
+// the state by e^{g_i}).  With G_t = sum_{s<=t} g_s inside the chunk, a vector over d_k,
+//   S_t = diag(e^{G_t}) S_0 + sum_{s<=t} diag(e^{G_t - G_s}) k_s delta_s^T,
+// so the chunk algebra keeps its shape with the gates moved into the operands:
+//   A_ts = beta_t sum_i k_ti k_si e^{G_ti - G_si} (s < t),
+//   P_ts = scale sum_i q_ti k_si e^{G_ti - G_si} (s <= t),
+//   W = T diag(beta) (K o e^G),  U = T diag(beta) V,  Delta = U - W S_c,
+//   o = scale (Q o e^G) S_c + P Delta,  S_{c+1} = diag(e^{G_C}) S_c + (K o e^{G_C - G})^T Delta.
+// The record keeps the scalar layout with the gates folded in: W'_{c+1} = W_{c+1}
+// diag(e^{G_C(c)}) and M_{c+1} = W_{c+1} (K_c o e^{G_C - G})^T, so the scan's lookahead
+// takes no gate (gC = 1), and the gate record holds e^{G_C} per key dimension (gam:
+// dimensions 0-63, kf: 64-127) for the scan's state update.  Q~ = Q o e^G and K~ =
+// K o e^{G_C - G} go to two workspace arrays ([tokens][h_v][128], I/O type), from which
+// the scan loads Q and K.
+// e^{G_t - G_s} depends on the key dimension, so A and P are no scaled Gram matrix: they
+// are formed on the FP32 cores.  Every exponent taken is <= 0 (G never grows along the
+// chunk): a 4 x 4 tile below the diagonal (rows t0 .. t0 + 3, columns s0 .. s0 + 3 < t0)
+// uses e^{G_t - G_t0} e^{G_t0 - G_s}; the 16 tiles on the diagonal take e^{G_t - G_s} per
+// pair.
+constexpr int kGs = 132;                        // row stride (floats) of the G tile
+constexpr int PK_KQ = 0;                        // [K; Q] per d_k half: K -> K o e^G -> W; Q -> V
+constexpr int PK_TT = 2 * kRegP;                // [T diag(beta); T diag(beta)], then U
+constexpr int PK_AS = PK_TT + 16384;            // A, then T (fp32 [64][68]), then K_{c-1} o e^{G_C - G}
+constexpr int PK_G = PK_AS + 64 * kAs * 4;      // G (fp32 [64][132]), then W' staging
+constexpr int kPkSmem = PK_G + 64 * kGs * 4 + 1024;
+
+struct PkCtl {
+    uint64_t full, vfull, d2, d3, kprev, dm;
+    PrepItem nxt;
+    uint32_t tmem;
+    float beta[kC], ones[kC];
+    float tot[2][kDK];     // per key dimension: the decay summed over each half of a chunk
+    float gcp[kDK];        // per key dimension: e^{G_C} of the previous chunk
+};
+
+// Four key dimensions of one row of a [K; Q] region (K rows 0-63, Q rows 64-127), widened.
+template <typename IO>
+__device__ __forceinline__ void pk_ld4(const uint8_t *reg, int row, int st, float (&x)[4]) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(reg + sw128_offset(row, st >> 1) + (st & 1) * 8);
+    const float2 a = Pack<IO>::unpack(u.x), b = Pack<IO>::unpack(u.y);
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+}
+
+// accA[r][c] += sum_i k_{t0+r,i} k_{s0+c,i} e^{G_{t0+r,i} - G_{s0+c,i}} and accP likewise
+// with q_{t0+r}, over the 64 key dimensions of region rg; s0 + 3 < t0, so both factors of
+// e^{G_t - G_t0} e^{G_t0 - G_s} are at most 1.
+template <typename IO>
+__device__ __forceinline__ void pk_tile(const uint8_t *kq, const float *G, int t0, int s0, int rg,
+                                        float (&accA)[4][4], float (&accP)[4][4]) {
+    const uint8_t *reg = kq + rg * kRegP;
+#pragma unroll 1
+    for (int st = 0; st < 16; ++st) {
+        const int i = 64 * rg + 4 * st;
+        const float4 g0 = *reinterpret_cast<const float4 *>(G + t0 * kGs + i);
+        float kc[4][4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float ks[4];
+            pk_ld4<IO>(reg, s0 + c, st, ks);
+            const float4 gs = *reinterpret_cast<const float4 *>(G + (s0 + c) * kGs + i);
+            kc[c][0] = ks[0] * __expf(g0.x - gs.x);
+            kc[c][1] = ks[1] * __expf(g0.y - gs.y);
+            kc[c][2] = ks[2] * __expf(g0.z - gs.z);
+            kc[c][3] = ks[3] * __expf(g0.w - gs.w);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            float kr[4], qr[4];
+            pk_ld4<IO>(reg, t0 + r, st, kr);
+            pk_ld4<IO>(reg, 64 + t0 + r, st, qr);
+            if (r > 0) {
+                const float4 gt = *reinterpret_cast<const float4 *>(G + (t0 + r) * kGs + i);
+                const float f[4] = {__expf(gt.x - g0.x), __expf(gt.y - g0.y), __expf(gt.z - g0.z),
+                                    __expf(gt.w - g0.w)};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    kr[e] *= f[e];
+                    qr[e] *= f[e];
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    accA[r][c] = fmaf(kr[e], kc[c][e], accA[r][c]);
+                    accP[r][c] = fmaf(qr[e], kc[c][e], accP[r][c]);
+                }
+        }
+    }
+}
+
+// P row t, columns s0 .. s0 + 3 (a multiple of 4), into the record's P image.
+template <typename IO>
+__device__ __forceinline__ void pk_put_p(uint8_t *rec, int t, int s0, float x0, float x1, float x2, float x3) {
+    *reinterpret_cast<uint2 *>(rec + REC_PM + sw128_offset(t, s0 >> 3) + (s0 & 7) * 2) =
+        make_uint2(Pack<IO>::two(x0, x1), Pack<IO>::two(x2, x3));
+}
+
+// Persistent CTAs, two to an SM, walk the (chunk slot, value head) items with the grid's
+// stride, as gdn_chunk_prep does, for the rules with decay and one decay per key dimension.
+// Per item: K and Q by TMA while the gates (G per key dimension, beta) are computed; A and
+// P on the FP32 cores; Q~, K~ out and K o e^G in place; T = (I + A)^-1 while V lands over
+// the spent Q rows; D2 = [T'; T''] (K o e^G) -> W; the previous chunk's gates scale its
+// keys (TMA) in place for M; D3 -> U; M = W (K_{c-1} o e^{G_C - G})^T.
+template <typename IO>
+__global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep_pk(const __grid_constant__ TcParams p) {
+    constexpr bool kBf16 = std::is_same<IO, __nv_bfloat16>::value;
+    const bool has_delta = p.has_delta != 0;
+    const bool beta_shared = p.beta_shared != 0;
+    constexpr uint32_t kIdM = idesc_f16(kBf16, 128, 64, false, false);
+    constexpr uint32_t kIdD2 = idesc_f16(kBf16, 128, 128, false, true);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+    __shared__ PkCtl ctl;
+    const int pt = threadIdx.x, warp = pt >> 5, lane = pt & 31;
+    const long long budget = p.wait_budget > 0 ? p.wait_budget : kWaitBudget;
+    const int q = warp & 3, hf = warp >> 2;        // TMEM lane quarter, column half
+    float *const As = reinterpret_cast<float *>(sm + PK_AS);
+    float *const G = reinterpret_cast<float *>(sm + PK_G);
+    const uint32_t aKQ = smem_u32(sm + PK_KQ), aTT = smem_u32(sm + PK_TT);
+    const size_t tstride = (size_t)p.h_v * kDK;   // elements between tokens of a, Q~, K~
+    if (warp == 0) {
+        tmem_alloc(&ctl.tmem, kPrepCols);
+        tmem_relinquish();
+    }
+    if (pt == 0) {
+        mbar_init(&ctl.full, 1);
+        mbar_init(&ctl.vfull, 1);
+        mbar_init(&ctl.d2, 1);
+        mbar_init(&ctl.d3, 1);
+        mbar_init(&ctl.kprev, 1);
+        mbar_init(&ctl.dm, 1);
+        fence_mbar_init();
+        ctl.nxt = prep_item(p, blockIdx.x);
+    }
+    if (pt < kC) ctl.ones[pt] = 1.f;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl.tmem;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    const int row = 32 * q + lane;
+    const int gi = pt & (kDK - 1), gh = pt >> 7;    // gate work: key dimension, half chunk
+    // mbarrier parities: full, vfull, d2 and d3 complete once per item, kprev and dm once
+    // per item that is not a segment's first chunk.
+    uint32_t ph = 0, phk = 0;
+    // thread 0: 1 = V load, 4 = D2, 8 = K_{c-1} load, 16 = M, 32 = D3
+    uint32_t issued = 0;
+    bool ok = true, failed = false;
+    for (int64_t item = blockIdx.x; item < p.prep_items; item += gridDim.x) {
+    const PrepItem it = ctl.nxt;
+    if (!it.valid) {
+        __syncthreads();   // every thread has read ctl.nxt
+        if (pt == 0) ctl.nxt = prep_item(p, item + gridDim.x);
+        __syncthreads();
+        continue;
+    }
+    const int h = it.h, hq = it.hq, Lc = it.Lc;
+    const bool first = it.first != 0;
+    const int64_t tc0 = it.tc0;
+    uint8_t *rec = p.ws + ((size_t)it.slot * p.h_v + h) * kRecord;
+    uint8_t *const rec_prev = rec - (size_t)p.h_v * kRecord;   // chunk c - 1, same head
+    const size_t ahk = (size_t)h * kDK + gi;                  // this thread's A_log / dt_bias
+    issued = 0;
+
+    for (int e = pt; e < 16384 / 16; e += kPrepThreads)
+        *reinterpret_cast<uint4 *>(sm + PK_TT + 16 * e) = make_uint4(0, 0, 0, 0);
+    fence_async_smem();
+    const int tok = (int)tc0;
+    if (pt == 0) {
+        mbar_arrive_expect_tx(&ctl.full, 4 * 8192);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            tma_load_3d(sm + PK_KQ + r * kRegP, &p.tm_k, r * 64, hq, tok, &ctl.full);
+            tma_load_3d(sm + PK_KQ + r * kRegP + 8192, &p.tm_q, r * 64, hq, tok, &ctl.full);
+        }
+    }
+    // G per key dimension while K and Q are in flight: thread (gi, gh) sums tokens
+    // 32 gh .. 32 gh + 31 of dimension gi; the second half adds the first half's sum after
+    // the barrier.  Padded tokens of a ragged chunk decay by nothing and have beta 0.
+    {
+        const float Al = p.A_log[ahk], Db = p.dt_bias[ahk];
+        const IO *ga = static_cast<const IO *>(p.a) + ((size_t)tc0 * p.h_v + h) * kDK + gi;
+        float lg[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            const int t = 32 * gh + r;
+            lg[r] = t < Lc ? IoType<IO>::ld(ga + (size_t)t * tstride) : 0.f;
+        }
+        float run = 0.f;
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            const int t = 32 * gh + r;
+            if (t < Lc) run += decay_f(lg[r], Al, Db);
+            G[t * kGs + gi] = run;
+        }
+        ctl.tot[gh][gi] = run;
+        if (pt < kC) {
+            float be = 0.f;
+            if (pt < Lc)
+                be = has_delta ? sigmoid_f(IoType<IO>::ld(static_cast<const IO *>(p.b) +
+                                                          (beta_shared ? (size_t)(tc0 + pt)
+                                                                       : (size_t)(tc0 + pt) * p.h_v + h)))
+                               : 1.f;
+            ctl.beta[pt] = be;
+        }
+    }
+    named_bar(kBarPrep, kPrepThreads);
+    if (gh == 1) {
+        const float off = ctl.tot[0][gi];
+#pragma unroll 8
+        for (int r = 0; r < 32; ++r) G[(32 + r) * kGs + gi] += off;
+    }
+    ok = mbar_wait(&ctl.full, ph, budget);
+    failed = bar_any(kBarPrep, kPrepThreads, !ok);   // also publishes G and beta
+    if (!failed) {
+        // A (times beta_t, fp32, to As) and P (times scale, to the record) below the
+        // diagonal: thread pairs (2u, 2u + 1), u < 120, take tile u over one d_k half each
+        // and trade partial sums, so that the even thread finishes A and the odd one P.
+        if (pt < 240) {
+            const int u = pt >> 1, dh = pt & 1;
+            int rb = 1;
+            while ((rb + 1) * rb / 2 <= u) ++rb;
+            const int t0 = 4 * rb, s0 = 4 * (u - rb * (rb - 1) / 2);
+            float accA[4][4] = {}, accP[4][4] = {};
+            pk_tile<IO>(sm + PK_KQ, G, t0, s0, dh, accA, accP);
+            const unsigned mask = pt >= 224 ? 0x0000ffffu : 0xffffffffu;
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float got = __shfl_xor_sync(mask, dh ? accA[r][c] : accP[r][c], 1);
+                    if (dh) accP[r][c] += got;
+                    else accA[r][c] += got;
+                }
+            if (dh == 0) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const float b = has_delta ? ctl.beta[t0 + r] : 0.f;
+                    *reinterpret_cast<float4 *>(As + (t0 + r) * kAs + s0) =
+                        make_float4(b * accA[r][0], b * accA[r][1], b * accA[r][2], b * accA[r][3]);
+                }
+            } else {
+                const float sc = p.scale;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    pk_put_p<IO>(rec, t0 + r, s0, sc * accP[r][0], sc * accP[r][1], sc * accP[r][2],
+                                 sc * accP[r][3]);
+                    pk_put_p<IO>(rec, s0 + r, t0, 0.f, 0.f, 0.f, 0.f);   // the mirrored tile is 0
+                }
+            }
+        }
+        named_bar(kBarPrep, kPrepThreads);
+        // The 16 diagonal tiles: tile t0 = 4 (pt / 16), the 16 threads of a tile take 8 key
+        // dimensions each and sum over the tile's threads.
+        {
+            const int t0 = 4 * (pt >> 4), ch = pt & 15;
+            const uint8_t *reg = sm + PK_KQ + (ch >> 3) * kRegP;
+            float a[6] = {}, pp[10] = {};
+#pragma unroll
+            for (int hs = 0; hs < 2; ++hs) {
+                const int st = 2 * (ch & 7) + hs, i = 8 * ch + 4 * hs;
+                float kx[4][4], gx[4][4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    pk_ld4<IO>(reg, t0 + r, st, kx[r]);
+                    const float4 g4 = *reinterpret_cast<const float4 *>(G + (t0 + r) * kGs + i);
+                    gx[r][0] = g4.x; gx[r][1] = g4.y; gx[r][2] = g4.z; gx[r][3] = g4.w;
+                }
+                int n = 0;
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    float qx[4];
+                    pk_ld4<IO>(reg, 64 + t0 + t, st, qx);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) pp[6 + t] = fmaf(qx[e], kx[t][e], pp[6 + t]);
+#pragma unroll
+                    for (int s = 0; s < t; ++s) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float w = kx[s][e] * __expf(gx[t][e] - gx[s][e]);
+                            a[n + s] = fmaf(kx[t][e], w, a[n + s]);
+                            pp[n + s] = fmaf(qx[e], w, pp[n + s]);
+                        }
+                    }
+                    n += t;
+                }
+            }
+#pragma unroll
+            for (int off = 1; off < 16; off <<= 1) {
+#pragma unroll
+                for (int v = 0; v < 6; ++v) a[v] += __shfl_xor_sync(0xffffffffu, a[v], off);
+#pragma unroll
+                for (int v = 0; v < 10; ++v) pp[v] += __shfl_xor_sync(0xffffffffu, pp[v], off);
+            }
+            if (ch == 0) {
+                // Pair (t, s), s < t, is entry t (t - 1) / 2 + s of a and pp.
+                const float sc = p.scale;
+                float b[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) b[t] = has_delta ? ctl.beta[t0 + t] : 0.f;
+                *reinterpret_cast<float4 *>(As + (t0 + 0) * kAs + t0) = make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4 *>(As + (t0 + 1) * kAs + t0) = make_float4(b[1] * a[0], 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4 *>(As + (t0 + 2) * kAs + t0) =
+                    make_float4(b[2] * a[1], b[2] * a[2], 0.f, 0.f);
+                *reinterpret_cast<float4 *>(As + (t0 + 3) * kAs + t0) =
+                    make_float4(b[3] * a[3], b[3] * a[4], b[3] * a[5], 0.f);
+                pk_put_p<IO>(rec, t0 + 0, t0, sc * pp[6], 0.f, 0.f, 0.f);
+                pk_put_p<IO>(rec, t0 + 1, t0, sc * pp[0], sc * pp[7], 0.f, 0.f);
+                pk_put_p<IO>(rec, t0 + 2, t0, sc * pp[1], sc * pp[2], sc * pp[8], 0.f);
+                pk_put_p<IO>(rec, t0 + 3, t0, sc * pp[3], sc * pp[4], sc * pp[5], sc * pp[9]);
+            }
+        }
+        named_bar(kBarPrep, kPrepThreads);
+        // Q~ and K~ to the workspace (real tokens only: the rows past a ragged chunk's end
+        // belong to the next sequence), K o e^G in place for D2, and e^{G_C} per key
+        // dimension to the gate record.  Thread: token row pt / 4, four 8-dimension groups.
+        {
+            const int t = pt >> 2;
+            const float *Gt = G + t * kGs, *GC = G + (kC - 1) * kGs;
+            IO *qdst = static_cast<IO *>(p.qt) + (size_t)(tc0 + t) * tstride + (size_t)h * kDK;
+            IO *kdst = static_cast<IO *>(p.kt) + (size_t)(tc0 + t) * tstride + (size_t)h * kDK;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int cc = (pt & 3) + 4 * j, i = 8 * cc;
+                uint8_t *kp = sm + PK_KQ + (cc >> 3) * kRegP + sw128_offset(t, cc & 7);
+                const uint8_t *qp = sm + PK_KQ + (cc >> 3) * kRegP + sw128_offset(64 + t, cc & 7);
+                float kx[8], qx[8], ko[8];
+                unpack8<IO>(*reinterpret_cast<const uint4 *>(kp), kx);
+                unpack8<IO>(*reinterpret_cast<const uint4 *>(qp), qx);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float g = Gt[i + e];
+                    const float e1 = __expf(g);
+                    ko[e] = kx[e] * __expf(GC[i + e] - g);
+                    qx[e] *= e1;
+                    kx[e] *= e1;
+                }
+                *reinterpret_cast<uint4 *>(kp) = pack8<IO>(kx);
+                if (t < Lc) {
+                    *reinterpret_cast<uint4 *>(qdst + i) = pack8<IO>(qx);
+                    *reinterpret_cast<uint4 *>(kdst + i) = pack8<IO>(ko);
+                }
+            }
+            if (pt < kDK) {
+                GateRec *grec = reinterpret_cast<GateRec *>(rec + REC_G);
+                const float gc = __expf(GC[pt]);
+                if (pt < 64) grec->gam[pt] = gc;
+                else grec->kf[pt - 64] = gc;
+                if (pt == 0) grec->gC = 1.f;
+            }
+        }
+        // Q is spent: V lands over its rows (the generic reads above come first).
+        fence_async_smem();
+        named_bar(kBarPrep, kPrepThreads);
+        if (pt == 0) {
+            mbar_arrive_expect_tx(&ctl.vfull, 2 * 8192);
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+                tma_load_3d(sm + PK_KQ + r * kRegP + 8192, &p.tm_v, r * 64, h, tok, &ctl.vfull);
+            issued |= 1;
+        }
+        auto next_item = [&](int t) {
+            if (t == 0) ctl.nxt = prep_item(p, item + gridDim.x);
+        };
+        invert_chunk<IO>(As, sm + PK_TT, ctl.beta, ctl.ones, has_delta ? 1.f : 0.f, pt, next_item);
+        fence_async_smem();
+        tc_fence_before();
+        named_bar(kBarPrep, kPrepThreads);
+        if (pt == 0) {
+            // The previous chunk's keys into the spent A/T tile.
+            if (!first) {
+                mbar_arrive_expect_tx(&ctl.kprev, 2 * 8192);
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+                    tma_load_3d(sm + PK_AS + r * 8192, &p.tm_k, r * 64, hq, tok - kC, &ctl.kprev);
+                issued |= 8;
+            }
+            // D2 = [T'; T''] (K o e^G): W on lanes 0-63.
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_f16(tmem, sw128_desc(aTT + k * 32, 16, 1024), sw128_desc(aKQ + k * 2048, kRegP, 1024),
+                        kIdD2, k > 0);
+            mma_commit(&ctl.d2);
+            issued |= 4;
+        }
+        if (!first) {
+            // The previous chunk (full: only a sequence's last chunk is ragged): its decay per
+            // key dimension, G', and e^{G'_C - G'} applied to its keys in place, so that
+            // M = W (K_{c-1} o e^{G'_C - G'})^T; e^{G'_C} scales W into W'.
+            const float Al = p.A_log[ahk], Db = p.dt_bias[ahk];
+            const IO *ga = static_cast<const IO *>(p.a) + ((size_t)(tc0 - kC) * p.h_v + h) * kDK + gi;
+            float lg[32];
+#pragma unroll
+            for (int r = 0; r < 32; ++r) lg[r] = IoType<IO>::ld(ga + (size_t)(32 * gh + r) * tstride);
+            float run = 0.f;
+#pragma unroll
+            for (int r = 0; r < 32; ++r) {
+                run += decay_f(lg[r], Al, Db);
+                lg[r] = run;
+            }
+            ctl.tot[gh][gi] = run;
+            named_bar(kBarPrep, kPrepThreads);
+            const float gC = ctl.tot[0][gi] + ctl.tot[1][gi], off = gh ? ctl.tot[0][gi] : 0.f;
+            if (gh == 0) ctl.gcp[gi] = __expf(gC);
+            ok = mbar_wait(&ctl.kprev, phk, budget);
+            if (ok) {
+                uint8_t *kp = sm + PK_AS + (gi >> 6) * 8192 + (gi & 7) * 2;
+#pragma unroll
+                for (int r = 0; r < 32; ++r) {
+                    const int t = 32 * gh + r;
+                    IO *e = reinterpret_cast<IO *>(kp + sw128_offset(t, (gi & 63) >> 3));
+                    IoType<IO>::st(e, IoType<IO>::ld(e) * __expf(gC - (lg[r] + off)));
+                }
+            }
+            fence_async_smem();
+        }
+        if (pt == 0) ok = ok && mbar_wait(&ctl.d2, ph, budget);
+        failed = bar_any(kBarPrep, kPrepThreads, !ok);
+    }
+    if (!failed) {
+        // W (fp32, lanes 0-63) in the I/O type over the spent K rows: the A operand of M and,
+        // for a segment's first chunk, the record's W_0; W' = W diag(e^{G'_C}) for the
+        // previous chunk's record, staged over the spent G tile.
+        tc_fence_after();
+        if (q < 2) {
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + 64 * hf + c0, r);
+                tmem_ld_wait();
+                float x[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8)
+                    *reinterpret_cast<uint4 *>(sm + PK_KQ + hf * kRegP + sw128_offset(row, (c0 >> 3) + q8)) =
+                        pack8<IO>(x + 8 * q8);
+                if (!first) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[e] *= ctl.gcp[64 * hf + c0 + e];
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8)
+                        *reinterpret_cast<uint4 *>(sm + PK_G + hf * 8192 + sw128_offset(row, (c0 >> 3) + q8)) =
+                            pack8<IO>(x + 8 * q8);
+                }
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        named_bar(kBarPrep, kPrepThreads);
+        // D3 = [T'; T''] V (U on lanes 64-127) while W (or W') goes out.
+        if (pt == 0) {
+            if (first) {
+#pragma unroll
+                for (int r = 0; r < 2; ++r) bulk_store(rec + REC_W0 + r * 8192, sm + PK_KQ + r * kRegP, 8192);
+            } else {
+                bulk_store(rec_prev + REC_W, sm + PK_G, 16384);
+            }
+            bulk_commit();
+            ok = mbar_wait(&ctl.vfull, ph, budget);
+            if (ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_f16(tmem, sw128_desc(aTT + k * 32, 16, 1024),
+                            sw128_desc(aKQ + 8192 + k * 2048, kRegP, 1024), kIdD2, k > 0);
+                mma_commit(&ctl.d3);
+                issued |= 32;
+                ok = mbar_wait(&ctl.d3, ph, budget);
+            }
+        }
+        failed = bar_any(kBarPrep, kPrepThreads, !ok);
+    }
+    if (!failed) {
+        // U (lanes 64-127) into the spent [T'; T''] tile, as the record's U image.
+        tc_fence_after();
+        if (q >= 2) {
+            const int j = row - 64;
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + 64 * hf + c0, r);
+                tmem_ld_wait();
+                float x[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8)
+                    *reinterpret_cast<uint4 *>(sm + PK_TT + hf * 8192 + sw128_offset(j, (c0 >> 3) + q8)) =
+                        pack8<IO>(x + 8 * q8);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        named_bar(kBarPrep, kPrepThreads);
+        // U goes out; then M = W (K_{c-1} o e^{G'_C - G'})^T (U has left TMEM).
+        if (pt == 0) {
+            bulk_store(rec + REC_U, sm + PK_TT, 16384);
+            bulk_commit();
+            if (!first) {
+                tc_fence_after();
+                const uint32_t aKp = smem_u32(sm + PK_AS);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mma_f16(tmem, sw128_desc(aKQ + (k >> 2) * kRegP + (k & 3) * 32, 16, 1024),
+                            sw128_desc(aKp + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), kIdM, k > 0);
+                mma_commit(&ctl.dm);
+                issued |= 16;
+                ok = mbar_wait(&ctl.dm, phk, budget);
+            }
+        }
+        if (!first) {
+            failed = bar_any(kBarPrep, kPrepThreads, !ok);
+            if (!failed) {
+                // M rows on lanes 0-63, staged over the spent V rows for the previous
+                // chunk's record.
+                tc_fence_after();
+                if (q < 2) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_base + 32 * hf, r);
+                    tmem_ld_wait();
+                    float x[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8)
+                        *reinterpret_cast<uint4 *>(sm + PK_KQ + 8192 + sw128_offset(row, 4 * hf + q8)) =
+                            pack8<IO>(x + 8 * q8);
+                }
+                fence_async_smem();
+                named_bar(kBarPrep, kPrepThreads);
+                if (pt == 0) {
+                    bulk_store(rec_prev + REC_PM + 8192, sm + PK_KQ + 8192, 8192);
+                    bulk_commit();
+                }
+            }
+        }
+    }
+    if (failed) break;    // the whole CTA, with this item's parities and copies in flight
+    if (pt == 0) bulk_wait_read();
+    ph ^= 1u;
+    if (!first) phk ^= 1u;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    }   // items
+    if (failed && pt == 0) {
+        // Let the copies and MMAs already issued land before the CTA leaves (bounded).
+        atomicOr(p.status, kDevTimeout);
+        mbar_wait(&ctl.full, ph, kWaitBudget);
+        if (issued & 1) mbar_wait(&ctl.vfull, ph, kWaitBudget);
+        if (issued & 4) mbar_wait(&ctl.d2, ph, kWaitBudget);
+        if (issued & 32) mbar_wait(&ctl.d3, ph, kWaitBudget);
+        if (issued & 8) mbar_wait(&ctl.kprev, phk, kWaitBudget);
+        if (issued & 16) mbar_wait(&ctl.dm, phk, kWaitBudget);
+    }
+    if (pt == 0) bulk_wait_read();   // the record stores have read their staging tiles
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kPrepCols);
+    }
+}
+
 // ===================================================================== state scan
 // The chain runs one chunk ahead on W S: with S' = gamma_C S + K^T diag(e^{G_C - G}) Delta
 // the state after chunk c,
@@ -907,7 +1483,10 @@ __device__ __forceinline__ bool wait_peer_or_abort(uint64_t *bar, uint32_t parit
 // squares its 32 rounded o values, the two column groups are summed through shared
 // memory, and each row's sum goes to the other CTA (a store into its shared memory, then
 // an arrival on its barrier), so both halves scale the row by the same 1 / rms.
-template <typename IO, bool kNorm = false>
+// kPK: one decay per key dimension (records of gdn_chunk_prep_pk): Q and K arrive already
+// scaled (Q o e^G, K o e^{G_C - G}), W' carries e^{G_C} (gC = 1), and the state update
+// scales S row i by e^{G_C,i} from the gate record (gam: rows 0-63, kf: rows 64-127).
+template <typename IO, bool kNorm = false, bool kPK = false>
 __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __grid_constant__ TcParams p) {
     constexpr bool kBf16 = std::is_same<IO, __nv_bfloat16>::value;
     constexpr uint32_t kIdNV = idesc_f16(kBf16, 128, kNV, false, true);
@@ -1086,7 +1665,7 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_f16(tmem + TS_DS, sw128_desc(aSt + k * 2048, kRegion, 1024),
-                            sw128_desc(aDB1 + k * 2048, 8192, 1024), kIdDS, k > 0);
+                            sw128_desc((kPK ? aDB0 : aDB1) + k * 2048, 8192, 1024), kIdDS, k > 0);
                 mma_commit(&ctl.ds);
                 // X(c) into block c & 1.  The readout of chunk c - 1 is done, so the readout
                 // warps have seen X phase c, the X block of chunk c - 2 is free, and D4'
@@ -1233,7 +1812,9 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
             // here: part A of the stage is refilled once every thread has arrived on sb_ready.
             ok = ok && warp_wait_or_abort(&ctl.full_a[s], (c >> 1) & 1, abort, budget);
             const float gC = ok ? gr.gC : 0.f;
-            const float fo = (ok && out_warp) ? p.scale * gr.gam[row] : 0.f;   // o row scale
+            const float fo = (ok && out_warp) ? p.scale * (kPK ? 1.f : gr.gam[row]) : 0.f;   // o row scale
+            // Decay of this thread's S row (readout warps): e^{G_C} or, per key, e^{G_C,row}.
+            const float gS = kPK ? ((ok && out_warp) ? gr.gam[row] : 0.f) : gC;
 
             if (!out_warp) {
                 // Delta_c = U_c - W_c S_c on lanes 64-127 (token rows), this thread's 32
@@ -1243,7 +1824,7 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                 if (ok) {
                     tc_fence_after();
                     const int j = row - 64;
-                    const float kfj = gr.kf[j];
+                    const float kfj = kPK ? 1.f : gr.kf[j];
                     const uint32_t wcol = TS_D4 + 64 * ((c + 1) & 1), xcol = TS_X + 64 * ((c + 1) & 1);
 #pragma unroll
                     for (int ps = 0; ps < 2; ++ps) {
@@ -1279,12 +1860,14 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                         for (int q8 = 0; q8 < 2; ++q8)
                             *reinterpret_cast<uint4 *>(sm + SS_DB0 + sw128_offset(j, 4 * g + 2 * ps + q8)) =
                                 pack8<IO>(x + 8 * q8);
+                        if constexpr (!kPK) {   // with per-key decay, K~ carries e^{G_C - G}
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) x[e] *= kfj;
+                            for (int e = 0; e < 16; ++e) x[e] *= kfj;
 #pragma unroll
-                        for (int q8 = 0; q8 < 2; ++q8)
-                            *reinterpret_cast<uint4 *>(sm + SS_DB1 + sw128_offset(j, 4 * g + 2 * ps + q8)) =
-                                pack8<IO>(x + 8 * q8);
+                            for (int q8 = 0; q8 < 2; ++q8)
+                                *reinterpret_cast<uint4 *>(sm + SS_DB1 + sw128_offset(j, 4 * g + 2 * ps + q8)) =
+                                    pack8<IO>(x + 8 * q8);
+                        }
                     }
                 }
                 fence_async_smem();
@@ -1307,7 +1890,7 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
                     tmem_ld16(tmem + lane_base + TS_DS + 32 * g + 16 * ps, r);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) S[16 * ps + e] = fmaf(gC, S[16 * ps + e], __uint_as_float(r[e]));
+                    for (int e = 0; e < 16; ++e) S[16 * ps + e] = fmaf(gS, S[16 * ps + e], __uint_as_float(r[e]));
                 }
             }
             publish_sb(ok);
@@ -1499,7 +2082,7 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
             }
             const GateRec &gr = *reinterpret_cast<const GateRec *>(sm + s * kScanStage + SS_G);
             ok = ok && warp_wait_or_abort(&ctl.full_a[s], (c >> 1) & 1, abort, budget);
-            const float gC = ok ? gr.gC : 0.f;
+            const float gC = ok ? (kPK ? gr.kf[row - 64] : gr.gC) : 0.f;
             ok = ok && warp_wait_or_abort(&ctl.ds, c & 1, abort, budget);
             if (ok) {
                 tc_fence_after();
@@ -1856,6 +2439,7 @@ SideStream *side_stream() {
 // per device and I/O type).
 // Resident prep CTAs per device and I/O type (SMs x CTAs per SM), set by configure().
 int g_prep_slots[64][2] = {};
+int g_prep_pk_slots[64][2] = {};   // the same for the per-key prep
 
 template <typename IO>
 cudaError_t configure() {
@@ -1878,8 +2462,17 @@ cudaError_t configure() {
             e = cudaFuncSetAttribute(gdn_chunk_prep<IO, true>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      (int)cudaSharedmemCarveoutMaxShared);
         if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gdn_chunk_prep_pk<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kPkSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gdn_chunk_prep_pk<IO>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared);
+        if (e == cudaSuccess)
             e = cudaFuncSetAttribute(gdn_chunk_scan<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kScanSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gdn_chunk_scan<IO, false, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(gdn_chunk_scan<IO, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmemNorm);
@@ -1901,6 +2494,13 @@ cudaError_t configure() {
         if (per_sm > 3) per_sm = 3;
         if (sms <= 0 || per_sm <= 0) return cudaErrorInvalidConfiguration;
         g_prep_slots[dev][std::is_same<IO, __nv_bfloat16>::value] = sms * per_sm;
+        e = cudaFuncGetAttributes(&fa, gdn_chunk_prep_pk<IO>);
+        if (e != cudaSuccess) return e;
+        const int per_cta_pk = kPkSmem + (int)fa.sharedSizeBytes + reserved;
+        int per_sm_pk = smem_sm / per_cta_pk;
+        if (per_sm_pk > 2) per_sm_pk = 2;
+        if (per_sm_pk <= 0) return cudaErrorInvalidConfiguration;
+        g_prep_pk_slots[dev][std::is_same<IO, __nv_bfloat16>::value] = sms * per_sm_pk;
         configured[dev] = true;
     }
     return cudaSuccess;
@@ -1913,10 +2513,15 @@ cudaError_t launch_prep(const TcParams &tp, int64_t items, cudaStream_t stream) 
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    const int slots = g_prep_slots[dev][std::is_same<IO, __nv_bfloat16>::value];
+    const int slots = (tp.per_key ? g_prep_pk_slots : g_prep_slots)[dev][std::is_same<IO, __nv_bfloat16>::value];
     if (slots <= 0) return cudaErrorInvalidConfiguration;
     TcParams pk = tp;
     pk.prep_items = items;
+    if (tp.per_key) {
+        const int64_t ctas_pk = items <= 2 * (int64_t)slots ? items : slots;
+        gdn_chunk_prep_pk<IO><<<(unsigned)ctas_pk, kPrepThreads, kPkSmem, stream>>>(pk);
+        return cudaGetLastError();
+    }
     // Persistent CTAs pay off on long item lists; up to three items per resident CTA, one
     // CTA per item leaves a shorter tail.
     const int64_t ctas = items <= 3 * (int64_t)slots ? items : slots;
@@ -1927,10 +2532,26 @@ cudaError_t launch_prep(const TcParams &tp, int64_t items, cudaStream_t stream) 
     return cudaGetLastError();
 }
 
+// The scan's view of a call with one decay per key dimension: Q and K come from the prep's
+// Q~ and K~ arrays, one head per value head.
+TcParams scan_view(const TcParams &tp) {
+    TcParams ts = tp;
+    if (tp.per_key) {
+        ts.tm_q = tp.tm_qt;
+        ts.tm_k = tp.tm_kt;
+        ts.h_qk = tp.h_v;
+    }
+    return ts;
+}
+
 template <typename IO>
 cudaError_t launch_scan(const TcParams &tp, cudaStream_t stream) {
     const int64_t ctas = (int64_t)tp.num_seqs * tp.h_v * (kDK / kNV);
     if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (tp.per_key) {   // never with the norm epilogue
+        gdn_chunk_scan<IO, false, true><<<(unsigned)ctas, kScanAllThreads, kScanSmem, stream>>>(scan_view(tp));
+        return cudaGetLastError();
+    }
     if (tp.norm_gate != nullptr) {
         // The two column halves of a (sequence, head), CTAs 2i and 2i + 1, as a cluster.
         cudaLaunchConfig_t cfg = {};
@@ -2061,7 +2682,11 @@ cudaError_t launch_tp(TcParams tp, int64_t n_slots, int nseg, uint8_t *extra, cu
     e = launch_prep<IO>(tp, n_slots * tp.h_v, stream);
     if (e != cudaSuccess) return e;
     const int64_t units = (int64_t)tp.num_seqs * tp.h_v * (kDK / kNV);
-    gdn_chunk_scan<IO><<<(unsigned)(units * (2 * nseg - 1)), kScanAllThreads, kScanSmem, stream>>>(tp);
+    if (tp.per_key)
+        gdn_chunk_scan<IO, false, true><<<(unsigned)(units * (2 * nseg - 1)), kScanAllThreads, kScanSmem, stream>>>(
+            scan_view(tp));
+    else
+        gdn_chunk_scan<IO><<<(unsigned)(units * (2 * nseg - 1)), kScanAllThreads, kScanSmem, stream>>>(tp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     for (int k = 1; k < nseg; ++k) {
         gdn_tp_combine<IO><<<dim3((unsigned)(tp.num_seqs * tp.h_v), 16), 256, 0, stream>>>(tp, k);
@@ -2090,6 +2715,11 @@ bool encode_map_3d(CUtensorMap *m, const void *base, gdn_dtype io, const uint64_
                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+size_t prefill_tc_pk_bytes(int64_t total_tokens, int h_v) {
+    const size_t each = ((size_t)total_tokens * h_v * kDK * 2 + 1023) & ~(size_t)1023;
+    return 2 * each;
 }
 
 size_t prefill_tc_tp_bytes(bool varlen, int64_t seqlen, int64_t batch, int h_v) {
@@ -2154,7 +2784,19 @@ cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_t
     // The time-parallel scan, when the shape suits it, the caller allows internal
     // resources and the workspace holds its buffers (not with the norm epilogue: the
     // correction adds to o after the scan).
-    const size_t records = prefill_tc_workspace(varlen, p.seqlen, p.num_seqs, p.num_seqs, p.h_v);
+    size_t records = prefill_tc_workspace(varlen, p.seqlen, p.num_seqs, p.num_seqs, p.h_v);
+    if (tp.has_decay && p.decay_per_key) {
+        // Q~ and K~ follow the records; the caller has checked that the workspace holds them.
+        const size_t each = prefill_tc_pk_bytes(total_tokens, p.h_v) / 2;
+        uint8_t *base = static_cast<uint8_t *>(workspace) + records;
+        tp.per_key = 1;
+        tp.qt = base;
+        tp.kt = base + each;
+        if (!make_map(&tp.tm_qt, tp.qt, io, p.h_v, total_tokens) ||
+            !make_map(&tp.tm_kt, tp.kt, io, p.h_v, total_tokens))
+            return cudaErrorInvalidValue;
+        records += 2 * each;
+    }
     const int tps = allow_overlap && p.norm_gate == nullptr
                         ? tp_segments(varlen, p.seqlen, p.num_seqs, p.h_v) : 1;
     if (tps > 1 && workspace_bytes >= records + tp_layout(p.seqlen, p.num_seqs, p.h_v, tps).total) {

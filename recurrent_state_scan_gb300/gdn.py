@@ -27,7 +27,7 @@ EXPORTS = ("gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode_step",
            "gdn_last_error_message", "gdn_prefill_noalloc", "gdn_decode_step_slots",
            "gdn_scan_window", "gdn_scan_variant", "gdn_causal_conv", "gdn_causal_conv_slots",
            "gdn_gated_rmsnorm", "gdn_set_wait_budget", "gdn_decode_layer", "gdn_prefill_variant",
-           "gdn_prefill_norm")
+           "gdn_prefill_norm", "gdn_prefill_variant_workspace_bytes", "gdn_prefill_variant_plan")
 PATH_SIMT, PATH_TC, PATH_TC_TP = 1, 2, 3
 # gdn_rule codes.
 RULES = {"gated_delta": 0, "delta": 1, "gated": 2, "linear": 3}
@@ -125,6 +125,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.gdn_prefill_variant.restype = ctypes.c_int
     lib.gdn_prefill_variant.argtypes = [S, ctypes.POINTER(GdnVariant), P, P, P, P, P, P, P, P, P,
                                         ctypes.c_float, P, P, P, ctypes.c_size_t, P]
+    lib.gdn_prefill_variant_workspace_bytes.restype = ctypes.c_size_t
+    lib.gdn_prefill_variant_workspace_bytes.argtypes = [S, ctypes.POINTER(GdnVariant)]
+    lib.gdn_prefill_variant_plan.restype = ctypes.c_int
+    lib.gdn_prefill_variant_plan.argtypes = [S, ctypes.POINTER(GdnVariant), ctypes.POINTER(ctypes.c_int32),
+                                             ctypes.POINTER(ctypes.c_int32)]
     lib.gdn_prefill_norm.restype = ctypes.c_int
     lib.gdn_prefill_norm.argtypes = [S, P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P,
                                      ctypes.c_float, ctypes.c_int32, ctypes.c_int32, P, P, P,
@@ -352,6 +357,27 @@ def gdn_prefill_plan(shape: GdnShape):
     return path.value, launches.value
 
 
+def gdn_prefill_variant_plan(shape: GdnShape, rule: str = "gated_delta", decay_per_key: bool = False,
+                             beta_shared: bool = False):
+    """(path, launches per call) that gdn_prefill_variant takes for ``shape`` with the
+    workspace gdn_prefill_variant_workspace_bytes reports."""
+    if rule not in RULES:
+        raise GdnError(GDN_ERR_INVALID_ARG, f"unknown rule {rule!r}")
+    var = GdnVariant(RULES[rule], int(bool(decay_per_key)), int(bool(beta_shared)))
+    path, launches = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(load().gdn_prefill_variant_plan(ctypes.byref(shape), ctypes.byref(var), ctypes.byref(path),
+                                           ctypes.byref(launches)))
+    return path.value, launches.value
+
+
+def gdn_prefill_variant_workspace_bytes(shape: GdnShape, rule: str = "gated_delta",
+                                        decay_per_key: bool = False, beta_shared: bool = False) -> int:
+    if rule not in RULES:
+        raise GdnError(GDN_ERR_INVALID_ARG, f"unknown rule {rule!r}")
+    var = GdnVariant(RULES[rule], int(bool(decay_per_key)), int(bool(beta_shared)))
+    return int(load().gdn_prefill_variant_workspace_bytes(ctypes.byref(shape), ctypes.byref(var)))
+
+
 def shape_of_spec(spec, n_seq: int, total_tokens: int) -> GdnShape:
     io = {"f32": GDN_F32, "bf16": GDN_BF16, "f16": GDN_F16}[spec.io]
     if spec.lengths is not None or spec.varlen_range is not None:
@@ -361,10 +387,10 @@ def shape_of_spec(spec, n_seq: int, total_tokens: int) -> GdnShape:
 
 
 def _simt_only(spec) -> bool:
-    """Specs that run the token-sequential kernel alone: decode, state windows and
-    per-key-dim decay (the rules and the shared beta of a prefill take gdn_prefill's path
+    """Specs that run the token-sequential kernel alone: decode and state windows (the
+    rules, the shared beta and the per-key-dim decay of a prefill take gdn_prefill's path
     through gdn_prefill_variant)."""
-    return bool(spec.decode or getattr(spec, "window", 0) or getattr(spec, "decay_per_key", False))
+    return bool(spec.decode or getattr(spec, "window", 0))
 
 
 def gdn_set_wait_budget(cycles: int) -> None:
@@ -530,13 +556,15 @@ def gdn_prefill_variant(q, k, v, a=None, b=None, A_log=None, dt_bias=None, state
                         decay_per_key: bool = False, beta_shared: bool = False, o=None,
                         state_out=None, workspace=None, stream=None):
     """gdn_scan_variant on gdn_prefill's path: the chunked tensor-core prefill for 16-bit
-    I/O at d_k = d_v = 128 (any rule, shared or per-head beta), the token-sequential
-    kernel for per-key-dim decay or other shapes.  ``workspace`` as gdn_prefill's."""
+    I/O at d_k = d_v = 128 (any rule, shared or per-head beta, per-key-dim decay), the
+    token-sequential kernel for other shapes.  ``workspace`` defaults to
+    gdn_prefill_variant_workspace_bytes; a per-key decay given less (down to
+    gdn_prefill_workspace_bytes) runs the token-sequential kernel."""
     lib = load()
     shape, var, o, state_out, gates = _variant_args(q, k, v, a, b, A_log, dt_bias, state_in,
                                                     cu_seqlens, rule, decay_per_key, beta_shared,
                                                     o, state_out)
-    need = int(lib.gdn_prefill_workspace_bytes(ctypes.byref(shape)))
+    need = int(lib.gdn_prefill_variant_workspace_bytes(ctypes.byref(shape), ctypes.byref(var)))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=v.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

@@ -41,3 +41,31 @@ def chunked_unit(q, k, v, g, beta, S0, scale, C=64):
         Ktil = np.exp(G[-1] - G)[:, None] * K
         S = gamma[-1] * S + Ktil.T @ Delta
     return o, S
+
+
+def chunked_unit_per_key(q, k, v, g, beta, S0, scale, C=64):
+    """The same with one log decay per key dimension, g [L, d_k] (Step 1 scales row i of
+    S by e^{g_i}).  G_t = g_1 + ... + g_t per dimension; inside a chunk
+      S_t = diag(e^{G_t}) S0 + sum_{s<=t} diag(e^{G_t - G_s}) k_s delta_s^T,
+    so A_ts = beta_t sum_i k_ti k_si e^{G_ti - G_si} (s < t) and P likewise with q_t
+    (s <= t), W = T diag(beta) (K o e^G), U = T diag(beta) V, and
+      O = scale ((Q o e^G) S0 + P Delta),  S_C = diag(e^{G_C}) S0 + (K o e^{G_C - G})^T Delta."""
+    L = q.shape[0]
+    S = S0.copy()
+    o = np.zeros((L, v.shape[1]))
+    for c0 in range(0, L, C):
+        c1 = min(c0 + C, L)
+        Q, K, V = q[c0:c1], k[c0:c1], v[c0:c1]
+        bc = beta[c0:c1]
+        n = c1 - c0
+        G = np.cumsum(g[c0:c1], axis=0)                              # [n, d_k]
+        E = np.exp(np.minimum(G[:, None, :] - G[None, :, :], 0.0))   # [t, s, i], s <= t used
+        A = np.tril(bc[:, None] * np.einsum("ti,si,tsi->ts", K, K, E), -1)
+        P = np.tril(np.einsum("ti,si,tsi->ts", Q, K, E))
+        Tm = np.linalg.inv(np.eye(n) + A)
+        W = Tm @ (bc[:, None] * (K * np.exp(G)))
+        U = Tm @ (bc[:, None] * V)
+        Delta = U - W @ S
+        o[c0:c1] = scale * ((Q * np.exp(G)) @ S + P @ Delta)
+        S = np.exp(G[-1])[:, None] * S + (K * np.exp(G[-1] - G)).T @ Delta
+    return o, S

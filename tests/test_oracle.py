@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 
 import workloads
-from chunked_ref import chunked_unit
+from chunked_ref import chunked_unit, chunked_unit_per_key
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -306,6 +306,35 @@ def test_chunked_reassociation_matches_sequential(oracle_mod, C, L):
         beta = np.array([oracle_mod.sigmoid(x) for x in f["b"].reshape(L, 2)[:, h]])
         oc, sc = chunked_unit(q[:, 0], k[:, 0], v[:, h], g, beta,
                               f["state_in"].reshape(1, 2, 32, 16)[0, h], inp.scale, C)
+        assert _rel(oc, o[:, h]) < 1e-11
+        assert _rel(sc, s[0, h]) < 1e-11
+
+
+@pytest.mark.parametrize("C,L,bump", [(64, 200, 0.0), (16, 37, 0.0), (64, 64, 3.0), (32, 100, 3.0)])
+def test_chunked_per_key_reassociation_matches_sequential(oracle_mod, C, L, bump):
+    """The per-key-dimension chunked form the GPU prefill uses (gates inside A, P, W, the
+    scaled Q and K and the per-row carry) equals the recurrence in float64; bump raises
+    A_log on every other key dimension so those decay up to ~160 per token."""
+    spec = workloads.small_spec(io="f32", lengths=[L], h_qk=1, h_v=2, d_k=32, d_v=16,
+                                seed=200 + L, state_std=0.05, decay_per_key=True)
+    inp = workloads.draw(spec)
+    f = dict(inp.f64)
+    A_log = f["A_log"].reshape(2, 32).copy()
+    A_log[:, 1::2] += bump
+    f["A_log"] = A_log.reshape(-1)
+    o, s = oracle_mod.scan(inp.cu_seqlens, 1, 2, 32, 16, f["q"], f["k"], f["v"], a=f["a"],
+                           b=f["b"], A_log=f["A_log"], dt_bias=f["dt_bias"],
+                           state_in=f["state_in"], scale=inp.scale, decay_per_key=True)
+    q, k = f["q"].reshape(L, 1, 32), f["k"].reshape(L, 1, 32)
+    v = f["v"].reshape(L, 2, 16)
+    a = f["a"].reshape(L, 2, 32)
+    dtb = f["dt_bias"].reshape(2, 32)
+    for h in range(2):
+        g = np.array([[oracle_mod.decay(a[t, h, i], A_log[h, i], dtb[h, i]) for i in range(32)]
+                      for t in range(L)])
+        beta = np.array([oracle_mod.sigmoid(x) for x in f["b"].reshape(L, 2)[:, h]])
+        oc, sc = chunked_unit_per_key(q[:, 0], k[:, 0], v[:, h], g, beta,
+                                      f["state_in"].reshape(1, 2, 32, 16)[0, h], inp.scale, C)
         assert _rel(oc, o[:, h]) < 1e-11
         assert _rel(sc, s[0, h]) < 1e-11
 

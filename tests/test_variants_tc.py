@@ -1,9 +1,12 @@
-"""GPU parity of gdn_prefill_variant -- the update rules (gated_delta, delta, gated, linear)
-and one beta shared by every head on the chunked tensor-core prefill (16-bit I/O,
-d_k = d_v = 128), and per-key decay through the same entry point on the token-sequential
-kernel -- against the CPU oracle run on the same drawn inputs.  The shapes cover ragged
-chunk tails, packed sequences (one of a single token), GQA, an initial state and the
-time-parallel scan.  Tolerances as in test_parity."""
+"""GPU parity of gdn_prefill_variant -- the update rules (gated_delta, delta, gated, linear),
+one beta shared by every head and one decay per key dimension on the chunked tensor-core
+prefill (16-bit I/O, d_k = d_v = 128) -- against the CPU oracle run on the same drawn
+inputs.  The shapes cover ragged chunk tails, packed sequences (one of a single token),
+GQA, an initial state and the time-parallel scan; per-key decay also runs with decay
+strong enough that most in-chunk factors underflow, and with too small a workspace (the
+token-sequential kernel).  Tolerances as in test_parity."""
+import dataclasses
+
 import pytest
 import torch
 
@@ -12,6 +15,17 @@ import workloads
 from gpu_util import TOL, rel_err, to_device
 
 RULES = ("gated_delta", "delta", "gated", "linear")
+
+
+def _stronger_decay(inp, by=3.0):
+    """The same draw with A_log raised by `by` on every other key dimension, so that those
+    dimensions decay e^by times faster (about -20 to -160 per token)."""
+    bump = torch.zeros_like(inp.A_log)
+    bump[..., 1::2] = by
+    A_log = (inp.A_log + bump).to(torch.float32)
+    f64 = dict(inp.f64)
+    f64["A_log"] = A_log.to(torch.float64).numpy().reshape(-1)
+    return dataclasses.replace(inp, A_log=A_log, f64=f64)
 
 
 def _run(inp, rule, workspace=None):
@@ -39,7 +53,8 @@ def _check(inp, rule, what):
 def _tc_path(inp):
     from recurrent_state_scan_gb300 import gdn
     shape = gdn.shape_of_spec(inp.spec, inp.n_seq, inp.total_tokens)
-    return gdn.gdn_prefill_plan(shape)[0]
+    return gdn.gdn_prefill_variant_plan(shape, inp.spec.rule, inp.spec.decay_per_key,
+                                        inp.spec.beta_shared)[0]
 
 
 @pytest.mark.gpu
@@ -90,24 +105,83 @@ def test_rules_on_the_time_parallel_scan(rule):
 
 
 @pytest.mark.gpu
-def test_per_key_decay_through_the_prefill_entry_point():
-    """Per-key decay is not on the tensor-core path: the same entry point runs it on the
-    token-sequential kernel, with no workspace."""
+@pytest.mark.parametrize("rule", ["gated_delta", "gated"])
+def test_per_key_decay_on_the_tensor_core_prefill_batched(rule):
+    """Two 300-token sequences (a ragged last chunk), GQA 2 -> 4 heads, an initial state."""
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
-    inp = workloads.draw(workloads.small_spec(io="bf16", batch=2, seqlen=70, h_qk=2, h_v=4,
+    from recurrent_state_scan_gb300 import gdn
+    inp = workloads.draw(workloads.small_spec(io="bf16", batch=2, seqlen=300, h_qk=2, h_v=4,
                                               d_k=128, d_v=128, state_std=0.05, seed=315,
                                               decay_per_key=True))
-    _check(inp, "gated_delta", "per-key decay")
+    assert _tc_path(inp) in (gdn.PATH_TC, gdn.PATH_TC_TP)
+    _check(inp, rule, "per-key batched")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("rule", ["gated_delta", "gated"])
+def test_per_key_decay_on_the_tensor_core_prefill_packed(rule):
+    """Packed f16 sequences of 1, 129, 64 and 250 tokens: a ragged chunk's padded rows
+    belong to the next sequence, and its Q~ / K~ rows are not overwritten."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    inp = workloads.draw(workloads.small_spec(io="f16", lengths=(1, 129, 64, 250), h_qk=1, h_v=2,
+                                              d_k=128, d_v=128, state_std=0.05, seed=316,
+                                              decay_per_key=True))
+    _check(inp, rule, "per-key packed")
+
+
+@pytest.mark.gpu
+def test_per_key_decay_on_the_time_parallel_scan():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from recurrent_state_scan_gb300 import gdn
+    inp = workloads.draw(workloads.small_spec(io="bf16", batch=1, seqlen=2048, h_qk=2, h_v=4,
+                                              d_k=128, d_v=128, state_std=0.05, seed=317,
+                                              decay_per_key=True))
+    assert _tc_path(inp) == gdn.PATH_TC_TP
+    _check(inp, "gated_delta", "per-key time-parallel")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("io", ["bf16", "f16"])
+def test_per_key_decay_strong(io):
+    """Half the key dimensions decay by up to ~160 per token: most e^{G_t - G_s} inside a
+    chunk underflow, none may overflow."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    inp = _stronger_decay(workloads.draw(workloads.small_spec(
+        io=io, lengths=(200, 77, 300), h_qk=2, h_v=2, d_k=128, d_v=128, state_std=0.05,
+        seed=318, decay_per_key=True)))
+    _check(inp, "gated_delta", "per-key strong decay")
+
+
+@pytest.mark.gpu
+def test_per_key_decay_with_the_records_only_workspace():
+    """With gdn_prefill_workspace_bytes (no room for Q~ and K~) the call runs the
+    token-sequential kernel: same results."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from recurrent_state_scan_gb300 import gdn
+    inp = workloads.draw(workloads.small_spec(io="bf16", batch=2, seqlen=130, h_qk=2, h_v=2,
+                                              d_k=128, d_v=128, state_std=0.05, seed=319,
+                                              decay_per_key=True))
+    shape = gdn.shape_of_spec(inp.spec, inp.n_seq, inp.total_tokens)
+    small = gdn.gdn_prefill_workspace_bytes(shape)
+    assert gdn.gdn_prefill_variant_workspace_bytes(shape, "gated_delta", True) > small
+    ws = torch.empty(small, dtype=torch.uint8, device="cuda")
+    o, s = _run(inp, "gated_delta", workspace=ws)
+    o_ref, s_ref = oracle.scan_inputs(inp, rule="gated_delta", threads=8)
+    tol = TOL[inp.spec.io]
+    assert rel_err(o, o_ref) <= tol and rel_err(s, s_ref) <= tol
 
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("name", ["bf16_delta_prefill_t4096", "bf16_shared_beta_prefill_t4096",
                                   "bf16_perkey_prefill_t4096"])
 def test_full_size_variant_workloads(name):
-    """The measured prefill-length variants, every element against the oracle: the delta
-    rule and the shared beta on the tensor-core path (time-parallel at this shape),
-    per-key decay on the token-sequential kernel."""
+    """The measured prefill-length variants, every element against the oracle, all on the
+    tensor-core path (time-parallel at this shape)."""
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
     inp = workloads.workload(name)
