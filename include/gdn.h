@@ -245,8 +245,9 @@ gdn_status gdn_scan_window(const gdn_shape *shape, const void *q, const void *k,
  * dimension of k_t k_s e^{G_t - G_s} (G the running decay sum per dimension), formed on
  * the FP32 cores, and Q and K reach the state scan scaled by e^G and e^{G_C - G}.  That
  * needs the larger workspace gdn_prefill_variant_workspace_bytes reports (two arrays of
- * tokens x h_v x 128 16-bit values more); with only gdn_prefill_workspace_bytes, or off
- * the tensor-core shapes, a per-key decay runs the token-sequential path.  workspace and
+ * tokens x h_v x 128 16-bit values more) and `a` 16-byte aligned; with only
+ * gdn_prefill_workspace_bytes, an `a` off 16 bytes, or off the tensor-core shapes, a
+ * per-key decay runs the token-sequential path.  workspace and
  * workspace_bytes are otherwise gdn_prefill's.  Errors are gdn_scan_variant's plus
  * gdn_prefill's workspace rule.
  */

@@ -297,7 +297,9 @@ gdn_status gdn::prefill_impl(const gdn_shape *shape, const void *q, const void *
     const size_t pk_bytes = per_key ? prefill_tc_pk_bytes(tokens, shape->h_v) : 0;
     const size_t records = prefill_tc_workspace(cu_seqlens != nullptr, shape->seqlen, shape->batch,
                                                 shape->num_seqs, shape->h_v);
-    const bool pk_room = !per_key || (workspace != nullptr && workspace_bytes >= records + pk_bytes);
+    // (The per-key path reads a's [64 tokens x 128] tiles by TMA: a must be 16-byte aligned.)
+    const bool pk_room = !per_key || (workspace != nullptr && workspace_bytes >= records + pk_bytes &&
+                                      aligned(a, 16));
     if (pk_room && prefill_tc_supported(p, io, tokens)) {
         if (norm_after && norm->fuse && aligned(norm->gate, 16)) {
             p.norm_scale = norm->scale;

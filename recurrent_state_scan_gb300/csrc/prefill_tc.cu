@@ -113,6 +113,7 @@ struct TcParams {
     int32_t per_key;
     void *qt, *kt;
     CUtensorMap tm_qt, tm_kt;
+    CUtensorMap tm_a;               // the gate logits a [tokens][h_v][128]
 };
 
 // First workspace slot of sequence n.  Batched: n * chunks_per_seq.  Packed: slot
@@ -807,12 +808,13 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
 constexpr int kGs = 132;                        // row stride (floats) of the G tile
 constexpr int PK_KQ = 0;                        // [K; Q] per d_k half: K -> K o e^G -> W; Q -> V
 constexpr int PK_TT = 2 * kRegP;                // [T diag(beta); T diag(beta)], then U
-constexpr int PK_AS = PK_TT + 16384;            // A, then T (fp32 [64][68]), then K_{c-1} o e^{G_C - G}
-constexpr int PK_G = PK_AS + 64 * kAs * 4;      // G (fp32 [64][132]), then W' staging
+constexpr int PK_AS = PK_TT + 16384;            // the chunk's gate logits, A, T (fp32 [64][68]), W' staging
+constexpr int PK_G = PK_AS + 64 * kAs * 4;      // G (fp32 [64][132]); then the previous chunk's
+                                                // logits and keys (o e^{G_C - G}), 16 KB each
 constexpr int kPkSmem = PK_G + 64 * kGs * 4 + 1024;
 
 struct PkCtl {
-    uint64_t full, vfull, d2, d3, kprev, dm;
+    uint64_t full, vfull, d2, d3, kprev, dm;   // kprev: the previous chunk's logits and keys
     PrepItem nxt;
     uint32_t tmem;
     float beta[kC], ones[kC];
@@ -828,67 +830,13 @@ __device__ __forceinline__ void pk_ld4(const uint8_t *reg, int row, int st, floa
     x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
 }
 
-// accA[r][c] += sum_i k_{t0+r,i} k_{s0+c,i} e^{G_{t0+r,i} - G_{s0+c,i}} and accP likewise
-// with q_{t0+r}, over the 64 key dimensions of region rg; s0 + 3 < t0, so both factors of
-// e^{G_t - G_t0} e^{G_t0 - G_s} are at most 1.
-template <typename IO>
-__device__ __forceinline__ void pk_tile(const uint8_t *kq, const float *G, int t0, int s0, int rg,
-                                        float (&accA)[4][4], float (&accP)[4][4]) {
-    const uint8_t *reg = kq + rg * kRegP;
-#pragma unroll 1
-    for (int st = 0; st < 16; ++st) {
-        const int i = 64 * rg + 4 * st;
-        const float4 g0 = *reinterpret_cast<const float4 *>(G + t0 * kGs + i);
-        float kc[4][4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float ks[4];
-            pk_ld4<IO>(reg, s0 + c, st, ks);
-            const float4 gs = *reinterpret_cast<const float4 *>(G + (s0 + c) * kGs + i);
-            kc[c][0] = ks[0] * __expf(g0.x - gs.x);
-            kc[c][1] = ks[1] * __expf(g0.y - gs.y);
-            kc[c][2] = ks[2] * __expf(g0.z - gs.z);
-            kc[c][3] = ks[3] * __expf(g0.w - gs.w);
-        }
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            float kr[4], qr[4];
-            pk_ld4<IO>(reg, t0 + r, st, kr);
-            pk_ld4<IO>(reg, 64 + t0 + r, st, qr);
-            if (r > 0) {
-                const float4 gt = *reinterpret_cast<const float4 *>(G + (t0 + r) * kGs + i);
-                const float f[4] = {__expf(gt.x - g0.x), __expf(gt.y - g0.y), __expf(gt.z - g0.z),
-                                    __expf(gt.w - g0.w)};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    kr[e] *= f[e];
-                    qr[e] *= f[e];
-                }
-            }
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    accA[r][c] = fmaf(kr[e], kc[c][e], accA[r][c]);
-                    accP[r][c] = fmaf(qr[e], kc[c][e], accP[r][c]);
-                }
-        }
-    }
-}
-
-// P row t, columns s0 .. s0 + 3 (a multiple of 4), into the record's P image.
-template <typename IO>
-__device__ __forceinline__ void pk_put_p(uint8_t *rec, int t, int s0, float x0, float x1, float x2, float x3) {
-    *reinterpret_cast<uint2 *>(rec + REC_PM + sw128_offset(t, s0 >> 3) + (s0 & 7) * 2) =
-        make_uint2(Pack<IO>::two(x0, x1), Pack<IO>::two(x2, x3));
-}
-
 // Persistent CTAs, two to an SM, walk the (chunk slot, value head) items with the grid's
 // stride, as gdn_chunk_prep does, for the rules with decay and one decay per key dimension.
-// Per item: K and Q by TMA while the gates (G per key dimension, beta) are computed; A and
-// P on the FP32 cores; Q~, K~ out and K o e^G in place; T = (I + A)^-1 while V lands over
-// the spent Q rows; D2 = [T'; T''] (K o e^G) -> W; the previous chunk's gates scale its
-// keys (TMA) in place for M; D3 -> U; M = W (K_{c-1} o e^{G_C - G})^T.
+// Per item: K, Q and the gate logits by TMA, then G per key dimension (and beta); A and P
+// on the FP32 cores; Q~, K~ out and K o e^G in place; T = (I + A)^-1 while V lands over
+// the spent Q rows and the previous chunk's logits and keys over G; D2 = [T'; T'']
+// (K o e^G) -> W; the previous chunk's gates scale its keys in place for M; D3 -> U;
+// M = W (K_{c-1} o e^{G_C - G})^T.
 template <typename IO>
 __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep_pk(const __grid_constant__ TcParams p) {
     constexpr bool kBf16 = std::is_same<IO, __nv_bfloat16>::value;
@@ -957,147 +905,165 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep_pk(const __gri
     fence_async_smem();
     const int tok = (int)tc0;
     if (pt == 0) {
-        mbar_arrive_expect_tx(&ctl.full, 4 * 8192);
+        mbar_arrive_expect_tx(&ctl.full, 6 * 8192);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             tma_load_3d(sm + PK_KQ + r * kRegP, &p.tm_k, r * 64, hq, tok, &ctl.full);
             tma_load_3d(sm + PK_KQ + r * kRegP + 8192, &p.tm_q, r * 64, hq, tok, &ctl.full);
+            tma_load_3d(sm + PK_AS + r * 8192, &p.tm_a, r * 64, h, tok, &ctl.full);
         }
     }
-    // G per key dimension while K and Q are in flight: thread (gi, gh) sums tokens
-    // 32 gh .. 32 gh + 31 of dimension gi; the second half adds the first half's sum after
-    // the barrier.  Padded tokens of a ragged chunk decay by nothing and have beta 0.
-    {
-        const float Al = p.A_log[ahk], Db = p.dt_bias[ahk];
-        const IO *ga = static_cast<const IO *>(p.a) + ((size_t)tc0 * p.h_v + h) * kDK + gi;
-        float lg[32];
-#pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            const int t = 32 * gh + r;
-            lg[r] = t < Lc ? IoType<IO>::ld(ga + (size_t)t * tstride) : 0.f;
-        }
+    // G per key dimension from the logits tile: thread (gi, gh) sums tokens 32 gh .. 32 gh
+    // + 31 of dimension gi; the second half adds the first half's sum after the barrier.
+    // Padded tokens of a ragged chunk (the next sequence's rows) decay by nothing and have
+    // beta 0.
+    const float Al = p.A_log[ahk], Db = p.dt_bias[ahk];
+    if (pt < kC) {
+        float be = 0.f;
+        if (pt < Lc)
+            be = has_delta ? sigmoid_f(IoType<IO>::ld(static_cast<const IO *>(p.b) +
+                                                      (beta_shared ? (size_t)(tc0 + pt)
+                                                                   : (size_t)(tc0 + pt) * p.h_v + h)))
+                           : 1.f;
+        ctl.beta[pt] = be;
+    }
+    ok = mbar_wait(&ctl.full, ph, budget);
+    if (ok) {
+        const uint8_t *at = sm + PK_AS + (gi >> 6) * 8192 + (gi & 7) * 2;
         float run = 0.f;
-#pragma unroll
+#pragma unroll 8
         for (int r = 0; r < 32; ++r) {
             const int t = 32 * gh + r;
-            if (t < Lc) run += decay_f(lg[r], Al, Db);
+            if (t < Lc)
+                run += decay_f(IoType<IO>::ld(reinterpret_cast<const IO *>(at + sw128_offset(t, (gi & 63) >> 3))),
+                               Al, Db);
             G[t * kGs + gi] = run;
         }
         ctl.tot[gh][gi] = run;
-        if (pt < kC) {
-            float be = 0.f;
-            if (pt < Lc)
-                be = has_delta ? sigmoid_f(IoType<IO>::ld(static_cast<const IO *>(p.b) +
-                                                          (beta_shared ? (size_t)(tc0 + pt)
-                                                                       : (size_t)(tc0 + pt) * p.h_v + h)))
-                               : 1.f;
-            ctl.beta[pt] = be;
-        }
     }
-    named_bar(kBarPrep, kPrepThreads);
-    if (gh == 1) {
+    failed = bar_any(kBarPrep, kPrepThreads, !ok);
+    if (!failed && gh == 1) {
         const float off = ctl.tot[0][gi];
 #pragma unroll 8
         for (int r = 0; r < 32; ++r) G[(32 + r) * kGs + gi] += off;
     }
-    ok = mbar_wait(&ctl.full, ph, budget);
-    failed = bar_any(kBarPrep, kPrepThreads, !ok);   // also publishes G and beta
+    named_bar(kBarPrep, kPrepThreads);   // G and beta complete; the logits tile is spent
     if (!failed) {
-        // A (times beta_t, fp32, to As) and P (times scale, to the record) below the
-        // diagonal: thread pairs (2u, 2u + 1), u < 120, take tile u over one d_k half each
-        // and trade partial sums, so that the even thread finishes A and the odd one P.
-        if (pt < 240) {
-            const int u = pt >> 1, dh = pt & 1;
-            int rb = 1;
-            while ((rb + 1) * rb / 2 <= u) ++rb;
-            const int t0 = 4 * rb, s0 = 4 * (u - rb * (rb - 1) / 2);
-            float accA[4][4] = {}, accP[4][4] = {};
-            pk_tile<IO>(sm + PK_KQ, G, t0, s0, dh, accA, accP);
-            const unsigned mask = pt >= 224 ? 0x0000ffffu : 0xffffffffu;
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float got = __shfl_xor_sync(mask, dh ? accA[r][c] : accP[r][c], 1);
-                    if (dh) accP[r][c] += got;
-                    else accA[r][c] += got;
-                }
-            if (dh == 0) {
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const float b = has_delta ? ctl.beta[t0 + r] : 0.f;
-                    *reinterpret_cast<float4 *>(As + (t0 + r) * kAs + s0) =
-                        make_float4(b * accA[r][0], b * accA[r][1], b * accA[r][2], b * accA[r][3]);
-                }
-            } else {
-                const float sc = p.scale;
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    pk_put_p<IO>(rec, t0 + r, s0, sc * accP[r][0], sc * accP[r][1], sc * accP[r][2],
-                                 sc * accP[r][3]);
-                    pk_put_p<IO>(rec, s0 + r, t0, 0.f, 0.f, 0.f, 0.f);   // the mirrored tile is 0
-                }
-            }
-        }
-        named_bar(kBarPrep, kPrepThreads);
-        // The 16 diagonal tiles: tile t0 = 4 (pt / 16), the 16 threads of a tile take 8 key
-        // dimensions each and sum over the tile's threads.
+        // A (times beta_t, fp32, to As) and P (times scale, to the record) in 4 x 4 tiles
+        // of (t, s) pairs with s <= t (136 tiles): warp w takes tiles w, w + 8, ..., lane l
+        // key dimensions 4l .. 4l + 3 (so a warp reads whole rows), and the tile's 32 sums
+        // (16 of A, then 16 of P) are reduced across the warp, lane l ending with sum l.
         {
-            const int t0 = 4 * (pt >> 4), ch = pt & 15;
-            const uint8_t *reg = sm + PK_KQ + (ch >> 3) * kRegP;
-            float a[6] = {}, pp[10] = {};
+            const int rg = lane >> 4, st = lane & 15, i4 = 4 * lane;
+            const uint8_t *reg = sm + PK_KQ + rg * kRegP;
+            auto ldg = [&](int r, float (&x)[4]) {
+                const float4 g4 = *reinterpret_cast<const float4 *>(G + r * kGs + i4);
+                x[0] = g4.x; x[1] = g4.y; x[2] = g4.z; x[3] = g4.w;
+            };
+#pragma unroll 1
+            for (int u = warp; u < 136; u += 8) {
+                int rb = 0;
+                while ((rb + 1) * (rb + 2) / 2 <= u) ++rb;
+                const int cb = u - rb * (rb + 1) / 2, t0 = 4 * rb, s0 = 4 * cb;
+                float v[32];
+                if (cb < rb) {
+                    // Below the diagonal: e^{G_t - G_s} = e^{G_t - G_t0} e^{G_t0 - G_s}.
+                    float g0[4], kc[4][4];
+                    ldg(t0, g0);
 #pragma unroll
-            for (int hs = 0; hs < 2; ++hs) {
-                const int st = 2 * (ch & 7) + hs, i = 8 * ch + 4 * hs;
-                float kx[4][4], gx[4][4];
+                    for (int c = 0; c < 4; ++c) {
+                        float ks[4], gs[4];
+                        pk_ld4<IO>(reg, s0 + c, st, ks);
+                        ldg(s0 + c, gs);
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    pk_ld4<IO>(reg, t0 + r, st, kx[r]);
-                    const float4 g4 = *reinterpret_cast<const float4 *>(G + (t0 + r) * kGs + i);
-                    gx[r][0] = g4.x; gx[r][1] = g4.y; gx[r][2] = g4.z; gx[r][3] = g4.w;
-                }
-                int n = 0;
+                        for (int e = 0; e < 4; ++e) kc[c][e] = ks[e] * __expf(g0[e] - gs[e]);
+                    }
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    float qx[4];
-                    pk_ld4<IO>(reg, 64 + t0 + t, st, qx);
+                    for (int r = 0; r < 4; ++r) {
+                        float kr[4], qr[4];
+                        pk_ld4<IO>(reg, t0 + r, st, kr);
+                        pk_ld4<IO>(reg, 64 + t0 + r, st, qr);
+                        if (r > 0) {
+                            float gt[4];
+                            ldg(t0 + r, gt);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) pp[6 + t] = fmaf(qx[e], kx[t][e], pp[6 + t]);
+                            for (int e = 0; e < 4; ++e) {
+                                const float f = __expf(gt[e] - g0[e]);
+                                kr[e] *= f;
+                                qr[e] *= f;
+                            }
+                        }
 #pragma unroll
-                    for (int s = 0; s < t; ++s) {
+                        for (int c = 0; c < 4; ++c) {
+                            float a = 0.f, pq = 0.f;
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float w = kx[s][e] * __expf(gx[t][e] - gx[s][e]);
-                            a[n + s] = fmaf(kx[t][e], w, a[n + s]);
-                            pp[n + s] = fmaf(qx[e], w, pp[n + s]);
+                            for (int e = 0; e < 4; ++e) {
+                                a = fmaf(kr[e], kc[c][e], a);
+                                pq = fmaf(qr[e], kc[c][e], pq);
+                            }
+                            v[4 * r + c] = a;
+                            v[16 + 4 * r + c] = pq;
                         }
                     }
-                    n += t;
+                } else {
+                    // On the diagonal: e^{G_t - G_s} per pair s < t; P also takes s = t.
+                    float kx[4][4], gx[4][4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        pk_ld4<IO>(reg, t0 + r, st, kx[r]);
+                        ldg(t0 + r, gx[r]);
+                    }
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        float qx[4];
+                        pk_ld4<IO>(reg, 64 + t0 + t, st, qx);
+#pragma unroll
+                        for (int s = 0; s < 4; ++s) {
+                            float a = 0.f, pq = 0.f;
+                            if (s < t) {
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float w = kx[s][e] * __expf(gx[t][e] - gx[s][e]);
+                                    a = fmaf(kx[t][e], w, a);
+                                    pq = fmaf(qx[e], w, pq);
+                                }
+                            } else if (s == t) {
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) pq = fmaf(qx[e], kx[t][e], pq);
+                            }
+                            v[4 * t + s] = a;
+                            v[16 + 4 * t + s] = pq;
+                        }
+                    }
                 }
-            }
+                // Reduce-scatter over the warp: at each step a lane keeps the half of its
+                // values that its lane bit selects and adds the partner's copy of it.
 #pragma unroll
-            for (int off = 1; off < 16; off <<= 1) {
+                for (int o = 16; o >= 1; o >>= 1) {
+                    const bool up = (lane & o) != 0;
 #pragma unroll
-                for (int v = 0; v < 6; ++v) a[v] += __shfl_xor_sync(0xffffffffu, a[v], off);
-#pragma unroll
-                for (int v = 0; v < 10; ++v) pp[v] += __shfl_xor_sync(0xffffffffu, pp[v], off);
-            }
-            if (ch == 0) {
-                // Pair (t, s), s < t, is entry t (t - 1) / 2 + s of a and pp.
-                const float sc = p.scale;
-                float b[4];
-#pragma unroll
-                for (int t = 0; t < 4; ++t) b[t] = has_delta ? ctl.beta[t0 + t] : 0.f;
-                *reinterpret_cast<float4 *>(As + (t0 + 0) * kAs + t0) = make_float4(0.f, 0.f, 0.f, 0.f);
-                *reinterpret_cast<float4 *>(As + (t0 + 1) * kAs + t0) = make_float4(b[1] * a[0], 0.f, 0.f, 0.f);
-                *reinterpret_cast<float4 *>(As + (t0 + 2) * kAs + t0) =
-                    make_float4(b[2] * a[1], b[2] * a[2], 0.f, 0.f);
-                *reinterpret_cast<float4 *>(As + (t0 + 3) * kAs + t0) =
-                    make_float4(b[3] * a[3], b[3] * a[4], b[3] * a[5], 0.f);
-                pk_put_p<IO>(rec, t0 + 0, t0, sc * pp[6], 0.f, 0.f, 0.f);
-                pk_put_p<IO>(rec, t0 + 1, t0, sc * pp[0], sc * pp[7], 0.f, 0.f);
-                pk_put_p<IO>(rec, t0 + 2, t0, sc * pp[1], sc * pp[2], sc * pp[8], 0.f);
-                pk_put_p<IO>(rec, t0 + 3, t0, sc * pp[3], sc * pp[4], sc * pp[5], sc * pp[9]);
+                    for (int k = 0; k < o; ++k) {
+                        const float send = up ? v[k] : v[k + o];
+                        const float keep = up ? v[k + o] : v[k];
+                        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                    }
+                }
+                const int r = (lane >> 2) & 3, c = lane & 3;
+                if (lane < 16) {
+                    const bool below = cb < rb || c < r;
+                    const float b = has_delta ? ctl.beta[t0 + r] : 0.f;
+                    As[(t0 + r) * kAs + s0 + c] = below ? b * v[0] : 0.f;
+                } else {
+                    const bool on = cb < rb || c <= r;
+                    const int s = s0 + c;
+                    IoType<IO>::st(reinterpret_cast<IO *>(rec + REC_PM + sw128_offset(t0 + r, s >> 3)) + (s & 7),
+                                   on ? p.scale * v[0] : 0.f);
+                    if (cb < rb) {   // the mirrored tile above the diagonal is zero
+                        const int s2 = t0 + c;
+                        IoType<IO>::st(reinterpret_cast<IO *>(rec + REC_PM + sw128_offset(s0 + r, s2 >> 3)) + (s2 & 7),
+                                       0.f);
+                    }
+                }
             }
         }
         named_bar(kBarPrep, kPrepThreads);
@@ -1114,14 +1080,17 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep_pk(const __gri
                 const int cc = (pt & 3) + 4 * j, i = 8 * cc;
                 uint8_t *kp = sm + PK_KQ + (cc >> 3) * kRegP + sw128_offset(t, cc & 7);
                 const uint8_t *qp = sm + PK_KQ + (cc >> 3) * kRegP + sw128_offset(64 + t, cc & 7);
-                float kx[8], qx[8], ko[8];
+                float kx[8], qx[8], ko[8], g[8], gc[8];
                 unpack8<IO>(*reinterpret_cast<const uint4 *>(kp), kx);
                 unpack8<IO>(*reinterpret_cast<const uint4 *>(qp), qx);
+                *reinterpret_cast<float4 *>(g) = *reinterpret_cast<const float4 *>(Gt + i);
+                *reinterpret_cast<float4 *>(g + 4) = *reinterpret_cast<const float4 *>(Gt + i + 4);
+                *reinterpret_cast<float4 *>(gc) = *reinterpret_cast<const float4 *>(GC + i);
+                *reinterpret_cast<float4 *>(gc + 4) = *reinterpret_cast<const float4 *>(GC + i + 4);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float g = Gt[i + e];
-                    const float e1 = __expf(g);
-                    ko[e] = kx[e] * __expf(GC[i + e] - g);
+                    const float e1 = __expf(g[e]);
+                    ko[e] = kx[e] * __expf(gc[e] - g[e]);
                     qx[e] *= e1;
                     kx[e] *= e1;
                 }
@@ -1139,7 +1108,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep_pk(const __gri
                 if (pt == 0) grec->gC = 1.f;
             }
         }
-        // Q is spent: V lands over its rows (the generic reads above come first).
+        // Q and G are spent: V lands over the Q rows and, for M and W', the previous
+        // chunk's logits and keys over G, during the inversion (the generic reads above
+        // come first).
         fence_async_smem();
         named_bar(kBarPrep, kPrepThreads);
         if (pt == 0) {
@@ -1148,6 +1119,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep_pk(const __gri
             for (int r = 0; r < 2; ++r)
                 tma_load_3d(sm + PK_KQ + r * kRegP + 8192, &p.tm_v, r * 64, h, tok, &ctl.vfull);
             issued |= 1;
+            if (!first) {
+                mbar_arrive_expect_tx(&ctl.kprev, 4 * 8192);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    tma_load_3d(sm + PK_G + r * 8192, &p.tm_a, r * 64, h, tok - kC, &ctl.kprev);
+                    tma_load_3d(sm + PK_G + 16384 + r * 8192, &p.tm_k, r * 64, hq, tok - kC, &ctl.kprev);
+                }
+                issued |= 8;
+            }
         }
         auto next_item = [&](int t) {
             if (t == 0) ctl.nxt = prep_item(p, item + gridDim.x);
@@ -1157,14 +1137,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep_pk(const __gri
         tc_fence_before();
         named_bar(kBarPrep, kPrepThreads);
         if (pt == 0) {
-            // The previous chunk's keys into the spent A/T tile.
-            if (!first) {
-                mbar_arrive_expect_tx(&ctl.kprev, 2 * 8192);
-#pragma unroll
-                for (int r = 0; r < 2; ++r)
-                    tma_load_3d(sm + PK_AS + r * 8192, &p.tm_k, r * 64, hq, tok - kC, &ctl.kprev);
-                issued |= 8;
-            }
             // D2 = [T'; T''] (K o e^G): W on lanes 0-63.
             tc_fence_after();
 #pragma unroll
@@ -1178,28 +1150,27 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep_pk(const __gri
             // The previous chunk (full: only a sequence's last chunk is ragged): its decay per
             // key dimension, G', and e^{G'_C - G'} applied to its keys in place, so that
             // M = W (K_{c-1} o e^{G'_C - G'})^T; e^{G'_C} scales W into W'.
-            const float Al = p.A_log[ahk], Db = p.dt_bias[ahk];
-            const IO *ga = static_cast<const IO *>(p.a) + ((size_t)(tc0 - kC) * p.h_v + h) * kDK + gi;
+            ok = mbar_wait(&ctl.kprev, phk, budget);
             float lg[32];
-#pragma unroll
-            for (int r = 0; r < 32; ++r) lg[r] = IoType<IO>::ld(ga + (size_t)(32 * gh + r) * tstride);
             float run = 0.f;
+            const int col = (gi >> 6) * 8192 + (gi & 7) * 2, ch = (gi & 63) >> 3;
 #pragma unroll
             for (int r = 0; r < 32; ++r) {
-                run += decay_f(lg[r], Al, Db);
+                if (ok)
+                    run += decay_f(IoType<IO>::ld(reinterpret_cast<const IO *>(sm + PK_G + col +
+                                                                              sw128_offset(32 * gh + r, ch))),
+                                   Al, Db);
                 lg[r] = run;
             }
             ctl.tot[gh][gi] = run;
             named_bar(kBarPrep, kPrepThreads);
             const float gC = ctl.tot[0][gi] + ctl.tot[1][gi], off = gh ? ctl.tot[0][gi] : 0.f;
             if (gh == 0) ctl.gcp[gi] = __expf(gC);
-            ok = mbar_wait(&ctl.kprev, phk, budget);
             if (ok) {
-                uint8_t *kp = sm + PK_AS + (gi >> 6) * 8192 + (gi & 7) * 2;
+                uint8_t *kp = sm + PK_G + 16384 + col;
 #pragma unroll
                 for (int r = 0; r < 32; ++r) {
-                    const int t = 32 * gh + r;
-                    IO *e = reinterpret_cast<IO *>(kp + sw128_offset(t, (gi & 63) >> 3));
+                    IO *e = reinterpret_cast<IO *>(kp + sw128_offset(32 * gh + r, ch));
                     IoType<IO>::st(e, IoType<IO>::ld(e) * __expf(gC - (lg[r] + off)));
                 }
             }
@@ -1211,7 +1182,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep_pk(const __gri
     if (!failed) {
         // W (fp32, lanes 0-63) in the I/O type over the spent K rows: the A operand of M and,
         // for a segment's first chunk, the record's W_0; W' = W diag(e^{G'_C}) for the
-        // previous chunk's record, staged over the spent G tile.
+        // previous chunk's record, staged over the spent A/T tile.
         tc_fence_after();
         if (q < 2) {
 #pragma unroll
@@ -1231,7 +1202,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep_pk(const __gri
                     for (int e = 0; e < 32; ++e) x[e] *= ctl.gcp[64 * hf + c0 + e];
 #pragma unroll
                     for (int q8 = 0; q8 < 4; ++q8)
-                        *reinterpret_cast<uint4 *>(sm + PK_G + hf * 8192 + sw128_offset(row, (c0 >> 3) + q8)) =
+                        *reinterpret_cast<uint4 *>(sm + PK_AS + hf * 8192 + sw128_offset(row, (c0 >> 3) + q8)) =
                             pack8<IO>(x + 8 * q8);
                 }
             }
@@ -1245,7 +1216,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep_pk(const __gri
 #pragma unroll
                 for (int r = 0; r < 2; ++r) bulk_store(rec + REC_W0 + r * 8192, sm + PK_KQ + r * kRegP, 8192);
             } else {
-                bulk_store(rec_prev + REC_W, sm + PK_G, 16384);
+                bulk_store(rec_prev + REC_W, sm + PK_AS, 16384);
             }
             bulk_commit();
             ok = mbar_wait(&ctl.vfull, ph, budget);
@@ -1290,7 +1261,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep_pk(const __gri
             bulk_commit();
             if (!first) {
                 tc_fence_after();
-                const uint32_t aKp = smem_u32(sm + PK_AS);
+                const uint32_t aKp = smem_u32(sm + PK_G + 16384);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     mma_f16(tmem, sw128_desc(aKQ + (k >> 2) * kRegP + (k & 3) * 32, 16, 1024),
@@ -2793,7 +2764,8 @@ cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_t
         tp.qt = base;
         tp.kt = base + each;
         if (!make_map(&tp.tm_qt, tp.qt, io, p.h_v, total_tokens) ||
-            !make_map(&tp.tm_kt, tp.kt, io, p.h_v, total_tokens))
+            !make_map(&tp.tm_kt, tp.kt, io, p.h_v, total_tokens) ||
+            !make_map(&tp.tm_a, p.a, io, p.h_v, total_tokens))   // a: 16-byte aligned (checked)
             return cudaErrorInvalidValue;
         records += 2 * each;
     }

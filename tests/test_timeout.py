@@ -116,3 +116,34 @@ def test_short_wait_budget_times_out_the_norm_pairs_then_recovers():
     assert gdn_last_device_status() == gdn.GDN_OK
     assert torch.equal(st, st2)
     assert torch.allclose(y.float(), y2.float(), rtol=2.0 ** -7, atol=1e-5)
+
+
+@pytest.mark.gpu
+def test_short_wait_budget_times_out_the_per_key_prep_then_recovers():
+    """The per-key-dim decay prefill (its own prep kernel, the scan's per-key form) under
+    the same 200-cycle budget, then a normal call against the oracle."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from recurrent_state_scan_gb300 import gdn, gdn_last_device_status, gdn_prefill_variant
+    inp = workloads.draw(workloads.small_spec(io="bf16", lengths=[300, 130], h_qk=1, h_v=2,
+                                              seed=19, state_std=0.05, decay_per_key=True))
+    d = to_device(inp)
+    assert gdn_last_device_status() == gdn.GDN_OK
+
+    def call():
+        return gdn_prefill_variant(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
+                                   d["state_in"], d["cu_seqlens"], inp.scale, decay_per_key=True)
+    gdn.gdn_set_wait_budget(200)
+    try:
+        call()
+        torch.cuda.synchronize()
+        assert gdn_last_device_status() == gdn.GDN_ERR_TIMEOUT
+    finally:
+        gdn.gdn_set_wait_budget(0)
+    assert gdn_last_device_status() == gdn.GDN_OK
+    o, s = call()
+    torch.cuda.synchronize()
+    assert gdn_last_device_status() == gdn.GDN_OK
+    o_ref, s_ref = oracle.scan_inputs(inp)
+    check(inp, o.float().cpu().numpy().reshape(-1, 2, 128), s.cpu().numpy(), o_ref, s_ref,
+          what="per-key prefill after a timed-out call")

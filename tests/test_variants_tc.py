@@ -186,3 +186,27 @@ def test_full_size_variant_workloads(name):
         pytest.skip("needs a CUDA GPU")
     inp = workloads.workload(name)
     _check(inp, inp.spec.rule, name)
+
+
+@pytest.mark.gpu
+def test_per_key_decay_with_a_off_16_bytes():
+    """The per-key prep loads a's tiles by TMA; an `a` 2 bytes past a 16-byte boundary takes
+    the token-sequential kernel instead, with the same results."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from recurrent_state_scan_gb300 import gdn_last_device_status, gdn_prefill_variant
+    inp = workloads.draw(workloads.small_spec(io="bf16", batch=2, seqlen=130, h_qk=2, h_v=2,
+                                              d_k=128, d_v=128, state_std=0.05, seed=320,
+                                              decay_per_key=True))
+    d = to_device(inp)
+    buf = torch.empty(d["a"].numel() + 1, dtype=d["a"].dtype, device="cuda")
+    a_off = buf[1:].view(d["a"].shape)
+    a_off.copy_(d["a"])
+    o, st = gdn_prefill_variant(d["q"], d["k"], d["v"], a_off, d["b"], d["A_log"], d["dt_bias"],
+                                d["state_in"], d["cu_seqlens"], inp.scale, decay_per_key=True)
+    torch.cuda.synchronize()
+    assert gdn_last_device_status() == 0
+    o_ref, s_ref = oracle.scan_inputs(inp, threads=8)
+    tol = TOL[inp.spec.io]
+    assert rel_err(o.float().cpu().numpy().reshape(-1, 2, 128), o_ref) <= tol
+    assert rel_err(st.cpu().numpy(), s_ref) <= tol
