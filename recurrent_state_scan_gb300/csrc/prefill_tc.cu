@@ -917,7 +917,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep_pk(const __gri
     // + 31 of dimension gi; the second half adds the first half's sum after the barrier.
     // Padded tokens of a ragged chunk (the next sequence's rows) decay by nothing and have
     // beta 0.
-    const float Al = p.A_log[ahk], Db = p.dt_bias[ahk];
+    // g = -e^{A_log} softplus(a + dt_bias) for this thread's key dimension, in fp32 with the
+    // fast exp / log (absolute error near 1e-7 per token; the scalar gates use the libm
+    // forms, which cost several times more here, where every token has 128 gates).
+    const float nA = -expf(p.A_log[ahk]), Db = p.dt_bias[ahk];
+    auto gate = [&](float x) {
+        const float y = x + Db;
+        return nA * (fmaxf(y, 0.f) + __logf(1.f + __expf(-fabsf(y))));
+    };
     if (pt < kC) {
         float be = 0.f;
         if (pt < Lc)
@@ -934,9 +941,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep_pk(const __gri
 #pragma unroll 8
         for (int r = 0; r < 32; ++r) {
             const int t = 32 * gh + r;
-            if (t < Lc)
-                run += decay_f(IoType<IO>::ld(reinterpret_cast<const IO *>(at + sw128_offset(t, (gi & 63) >> 3))),
-                               Al, Db);
+            if (t < Lc) run += gate(IoType<IO>::ld(reinterpret_cast<const IO *>(at + sw128_offset(t, (gi & 63) >> 3))));
             G[t * kGs + gi] = run;
         }
         ctl.tot[gh][gi] = run;
@@ -949,22 +954,81 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep_pk(const __gri
     }
     named_bar(kBarPrep, kPrepThreads);   // G and beta complete; the logits tile is spent
     if (!failed) {
-        // A (times beta_t, fp32, to As) and P (times scale, to the record) in 4 x 4 tiles
-        // of (t, s) pairs with s <= t (136 tiles): warp w takes tiles w, w + 8, ..., lane l
-        // key dimensions 4l .. 4l + 3 (so a warp reads whole rows), and the tile's 32 sums
-        // (16 of A, then 16 of P) are reduced across the warp, lane l ending with sum l.
+        // A (times beta_t, fp32, to As) and P (times scale, to the record), s <= t.
+        //  - The six 16 x 16 blocks below the diagonal (rows 16b .., columns 16a .., a < b),
+        //    one warp each on tf32 warp MMAs: every term factors through the block's first
+        //    row r = 16b, e^{G_t - G_r} e^{G_r - G_s} with s < r <= t, both factors <= 1, so
+        //    A and P are products of (K, Q) o e^{G - G_r} and K o e^{G_r - G}.
+        //  - The 40 4 x 4 tiles inside the diagonal blocks on the FP32 cores: lane l takes
+        //    key dimensions 4l .. 4l + 3, below a tile's diagonal through its first row as
+        //    above, on it per pair; the tile's 32 sums are reduced across the warp.
         {
+            const uint8_t *kq = sm + PK_KQ;
+            // Element (row, dimension) of the [K; Q] tiles (K rows 0-63, Q rows 64-127).
+            auto el = [&](int r, int i) {
+                return IoType<IO>::ld(reinterpret_cast<const IO *>(
+                    kq + (i >> 6) * kRegP + sw128_offset(r, (i & 63) >> 3) + (i & 7) * 2));
+            };
+            if (warp < 6) {
+                const int b = warp < 1 ? 1 : (warp < 3 ? 2 : 3);
+                const int a = warp - (b * (b - 1)) / 2;
+                const int rt = 16 * b, cs = 16 * a, g = lane >> 2, tq = lane & 3;
+                float accA[2][4] = {}, accP[2][4] = {};
+#pragma unroll 2
+                for (int ks = 0; ks < 16; ++ks) {
+                    const int d0 = 8 * ks + tq, d1 = d0 + 4;
+                    const float r0 = G[rt * kGs + d0], r1 = G[rt * kGs + d1];
+                    const float f00 = __expf(G[(rt + g) * kGs + d0] - r0), f10 = __expf(G[(rt + g + 8) * kGs + d0] - r0);
+                    const float f01 = __expf(G[(rt + g) * kGs + d1] - r1), f11 = __expf(G[(rt + g + 8) * kGs + d1] - r1);
+                    const uint32_t xk[4] = {to_tf32(el(rt + g, d0) * f00), to_tf32(el(rt + g + 8, d0) * f10),
+                                            to_tf32(el(rt + g, d1) * f01), to_tf32(el(rt + g + 8, d1) * f11)};
+                    const uint32_t xq[4] = {to_tf32(el(64 + rt + g, d0) * f00), to_tf32(el(64 + rt + g + 8, d0) * f10),
+                                            to_tf32(el(64 + rt + g, d1) * f01), to_tf32(el(64 + rt + g + 8, d1) * f11)};
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int sc = cs + 8 * nt + g;
+                        const uint32_t y[2] = {to_tf32(el(sc, d0) * __expf(r0 - G[sc * kGs + d0])),
+                                               to_tf32(el(sc, d1) * __expf(r1 - G[sc * kGs + d1]))};
+                        mma_tf32_16x8x8(accA[nt], xk, y);
+                        mma_tf32_16x8x8(accP[nt], xq, y);
+                    }
+                }
+                const float sc = p.scale;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int c = cs + 8 * nt + 2 * tq;
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int t = rt + g + 8 * hh;
+                        const float bt = has_delta ? ctl.beta[t] : 0.f;
+                        *reinterpret_cast<float2 *>(As + t * kAs + c) =
+                            make_float2(bt * accA[nt][2 * hh], bt * accA[nt][2 * hh + 1]);
+                        *reinterpret_cast<uint32_t *>(rec + REC_PM + sw128_offset(t, c >> 3) + (c & 7) * 2) =
+                            Pack<IO>::two(sc * accP[nt][2 * hh], sc * accP[nt][2 * hh + 1]);
+                    }
+                }
+                // The mirrored block above the diagonal is zero: rows 16a .., columns 16b ..
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int idx = lane + 32 * e, t = cs + (idx >> 3), c = rt + 2 * (idx & 7);
+                    *reinterpret_cast<uint32_t *>(rec + REC_PM + sw128_offset(t, c >> 3) + (c & 7) * 2) = 0u;
+                }
+            }
+            // Diagonal blocks: tile j = 10 (block) + (row, column) of the 4 x 4 tiles with
+            // column <= row; warps 0-5 take 4 tiles, warps 6-7 8 (they skipped the MMAs).
             const int rg = lane >> 4, st = lane & 15, i4 = 4 * lane;
-            const uint8_t *reg = sm + PK_KQ + rg * kRegP;
+            const uint8_t *reg = kq + rg * kRegP;
             auto ldg = [&](int r, float (&x)[4]) {
                 const float4 g4 = *reinterpret_cast<const float4 *>(G + r * kGs + i4);
                 x[0] = g4.x; x[1] = g4.y; x[2] = g4.z; x[3] = g4.w;
             };
+            const int j0 = warp < 6 ? 4 * warp : 24 + 8 * (warp - 6), j1 = warp < 6 ? j0 + 4 : j0 + 8;
 #pragma unroll 1
-            for (int u = warp; u < 136; u += 8) {
+            for (int j = j0; j < j1; ++j) {
+                const int blk = j / 10, l = j % 10;
                 int rb = 0;
-                while ((rb + 1) * (rb + 2) / 2 <= u) ++rb;
-                const int cb = u - rb * (rb + 1) / 2, t0 = 4 * rb, s0 = 4 * cb;
+                while ((rb + 1) * (rb + 2) / 2 <= l) ++rb;
+                const int cb = l - rb * (rb + 1) / 2, t0 = 16 * blk + 4 * rb, s0 = 16 * blk + 4 * cb;
                 float v[32];
                 if (cb < rb) {
                     // Below the diagonal: e^{G_t - G_s} = e^{G_t - G_t0} e^{G_t0 - G_s}.
@@ -1156,10 +1220,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep_pk(const __gri
             const int col = (gi >> 6) * 8192 + (gi & 7) * 2, ch = (gi & 63) >> 3;
 #pragma unroll
             for (int r = 0; r < 32; ++r) {
-                if (ok)
-                    run += decay_f(IoType<IO>::ld(reinterpret_cast<const IO *>(sm + PK_G + col +
-                                                                              sw128_offset(32 * gh + r, ch))),
-                                   Al, Db);
+                if (ok) run += gate(IoType<IO>::ld(reinterpret_cast<const IO *>(sm + PK_G + col + sw128_offset(32 * gh + r, ch))));
                 lg[r] = run;
             }
             ctl.tot[gh][gi] = run;
