@@ -959,9 +959,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep_pk(const __gri
         //    one warp each on tf32 warp MMAs: every term factors through the block's first
         //    row r = 16b, e^{G_t - G_r} e^{G_r - G_s} with s < r <= t, both factors <= 1, so
         //    A and P are products of (K, Q) o e^{G - G_r} and K o e^{G_r - G}.
-        //  - The 40 4 x 4 tiles inside the diagonal blocks on the FP32 cores: lane l takes
-        //    key dimensions 4l .. 4l + 3, below a tile's diagonal through its first row as
-        //    above, on it per pair; the tile's 32 sums are reduced across the warp.
+        //  - Inside each diagonal block, its lower-left 8 x 8 part the same way through row
+        //    16b + 8 (warps 6 and 7, the block's 8 K rows stacked over its 8 Q rows).
+        //  - The 24 remaining 4 x 4 tiles on the FP32 cores: lane l takes key dimensions
+        //    4l .. 4l + 3, below a tile's diagonal through its first row as above, on it per
+        //    pair; the tile's 32 sums are reduced across the warp.
         {
             const uint8_t *kq = sm + PK_KQ;
             // Element (row, dimension) of the [K; Q] tiles (K rows 0-63, Q rows 64-127).
@@ -1014,21 +1016,48 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_chunk_prep_pk(const __gri
                     *reinterpret_cast<uint32_t *>(rec + REC_PM + sw128_offset(t, c >> 3) + (c & 7) * 2) = 0u;
                 }
             }
-            // Diagonal blocks: tile j = 10 (block) + (row, column) of the 4 x 4 tiles with
-            // column <= row; warps 0-5 take 4 tiles, warps 6-7 8 (they skipped the MMAs).
+            if (warp >= 6) {
+                const int g = lane >> 2, tq = lane & 3;
+#pragma unroll 1
+                for (int bb = 2 * (warp - 6); bb < 2 * (warp - 6) + 2; ++bb) {
+                    const int rt = 16 * bb + 8, cs = 16 * bb, t = rt + g;
+                    float acc[4] = {};
+#pragma unroll 2
+                    for (int ks = 0; ks < 16; ++ks) {
+                        const int d0 = 8 * ks + tq, d1 = d0 + 4;
+                        const float r0 = G[rt * kGs + d0], r1 = G[rt * kGs + d1];
+                        const float f0 = __expf(G[t * kGs + d0] - r0), f1 = __expf(G[t * kGs + d1] - r1);
+                        const uint32_t x[4] = {to_tf32(el(t, d0) * f0), to_tf32(el(64 + t, d0) * f0),
+                                               to_tf32(el(t, d1) * f1), to_tf32(el(64 + t, d1) * f1)};
+                        const int sc = cs + g;
+                        const uint32_t y[2] = {to_tf32(el(sc, d0) * __expf(r0 - G[sc * kGs + d0])),
+                                               to_tf32(el(sc, d1) * __expf(r1 - G[sc * kGs + d1]))};
+                        mma_tf32_16x8x8(acc, x, y);
+                    }
+                    const int c = cs + 2 * tq;
+                    const float bt = has_delta ? ctl.beta[t] : 0.f;
+                    *reinterpret_cast<float2 *>(As + t * kAs + c) = make_float2(bt * acc[0], bt * acc[1]);
+                    *reinterpret_cast<uint32_t *>(rec + REC_PM + sw128_offset(t, c >> 3) + (c & 7) * 2) =
+                        Pack<IO>::two(p.scale * acc[2], p.scale * acc[3]);
+                    // Its mirror above the diagonal (rows 16b .., columns 16b + 8 ..) is zero.
+                    const int tz = cs + g, cz = rt + 2 * tq;
+                    *reinterpret_cast<uint32_t *>(rec + REC_PM + sw128_offset(tz, cz >> 3) + (cz & 7) * 2) = 0u;
+                }
+            }
+            // The 4 x 4 tiles of the two 8 x 8 diagonal parts of each diagonal block (three
+            // each): tile j = 6 (block) + 3 (part) + (0: upper diagonal, 1: below, 2: lower
+            // diagonal); three tiles a warp.
             const int rg = lane >> 4, st = lane & 15, i4 = 4 * lane;
             const uint8_t *reg = kq + rg * kRegP;
             auto ldg = [&](int r, float (&x)[4]) {
                 const float4 g4 = *reinterpret_cast<const float4 *>(G + r * kGs + i4);
                 x[0] = g4.x; x[1] = g4.y; x[2] = g4.z; x[3] = g4.w;
             };
-            const int j0 = warp < 6 ? 4 * warp : 24 + 8 * (warp - 6), j1 = warp < 6 ? j0 + 4 : j0 + 8;
 #pragma unroll 1
-            for (int j = j0; j < j1; ++j) {
-                const int blk = j / 10, l = j % 10;
-                int rb = 0;
-                while ((rb + 1) * (rb + 2) / 2 <= l) ++rb;
-                const int cb = l - rb * (rb + 1) / 2, t0 = 16 * blk + 4 * rb, s0 = 16 * blk + 4 * cb;
+            for (int j = 3 * warp; j < 3 * warp + 3; ++j) {
+                const int base = 16 * (j / 6) + 8 * ((j % 6) / 3), k3 = j % 3;
+                const int rb = k3 == 0 ? 0 : 1, cb = k3 == 2 ? 1 : 0;
+                const int t0 = base + 4 * rb, s0 = base + 4 * cb;
                 float v[32];
                 if (cb < rb) {
                     // Below the diagonal: e^{G_t - G_s} = e^{G_t - G_t0} e^{G_t0 - G_s}.
