@@ -42,8 +42,10 @@
  * gdn_scan_variant and gdn_prefill_variant (other update rules and gate layouts; with
  * gdn_prefill_variant_workspace_bytes and gdn_prefill_variant_plan),
  * the layer ops around the scan: gdn_causal_conv, gdn_causal_conv_slots and
- * gdn_gated_rmsnorm, gdn_prefill_norm (the prefill and the norm in one call) and
- * gdn_decode_layer (conv -> decode step -> norm in one kernel).
+ * gdn_gated_rmsnorm, gdn_prefill_norm (the prefill and the norm in one call),
+ * gdn_decode_layer (conv -> decode step -> norm in one kernel) and gdn_prefill_layer
+ * (conv -> prefill -> norm, the convolution inside the chunk prep; with
+ * gdn_prefill_layer_workspace_bytes).
  *  - gdn_last_error_message() gives a human-readable detail of the last
  *    non-OK status returned on the calling thread.
  */
@@ -434,6 +436,46 @@ gdn_status gdn_decode_layer(const gdn_shape *shape, const gdn_layer_params *laye
                             const void *b, const float *A_log, const float *dt_bias, float *state,
                             float scale, const void *norm_scale, const void *gate, void *y,
                             void *stream);
+
+/*
+ * gdn_prefill_layer -- the prefill of a whole gated delta-rule layer: gdn_causal_conv
+ * (onnxruntime-ep-mlx ssm.rs `causal_conv_op`) on the layer's mixed input, gdn_prefill
+ * (onnx-runtime-ep-cuda linear_attention.rs `linear_attention_core`, Steps 1-4) on its q,
+ * k and v, then gdn_gated_rmsnorm (ssm.rs `gated_rms_norm_op`) on o, in that order.  The
+ * convolution runs inside the chunked prefill's prep kernel, which convolves each chunk's
+ * q, k and v channels straight into its operand tiles: v never reaches memory, and the
+ * convolved q and k only as the workspace copy the state scan reads.  The norm then runs in
+ * place on y.  Each intermediate is rounded to io_dtype as the separate calls would store
+ * it; the results equal conv -> prefill -> norm up to the order of fp32 sums.
+ *   x            [tokens, C] (packed with cu_seqlens, or [B, T, C]), C = 2 h_qk d_k +
+ *                h_v d_v, read as [q (h_qk x d_k) | k (h_qk x d_k) | v (h_v x d_v)].
+ *   conv_weight  [C, 1, K] with K = layer->conv_kernel in 1..4; conv_bias [C] or NULL;
+ *                dilation 1; layer->conv_activation GDN_ACT_NONE or GDN_ACT_SILU.
+ *   conv_state_in  [sequences, K - 1, C] (oldest position first) or NULL (zeros): the
+ *                inputs before each sequence's first token.
+ *   conv_state_out [sequences, K - 1, C]: each sequence's last K - 1 inputs (state rows
+ *                first when the sequence is shorter).  It must not overlap conv_state_in.
+ *   a, b, A_log, dt_bias, state_in, cu_seqlens, scale, state_out: as gdn_prefill.
+ *   norm_scale [d_v]; gate like y; layer->norm_activation and norm_epsilon as
+ *                gdn_gated_rmsnorm; y [tokens, h_v, d_v], 16-byte aligned, not overlapping
+ *                gate.
+ *   workspace    at least gdn_prefill_layer_workspace_bytes(shape) bytes: gdn_prefill's
+ *                plus the convolved q and k (2 x tokens x h_qk x 128 16-bit values).
+ * Shape: io_dtype bf16 or f16 and d_k = d_v = 128 (GDN_ERR_UNSUPPORTED otherwise); x and
+ * the conv states 16-byte aligned.  Every pointer is device memory owned by the caller.
+ * Errors are gdn_prefill's and gdn_causal_conv's argument rules, checked before anything
+ * is launched.
+ */
+gdn_status gdn_prefill_layer(const gdn_shape *shape, const gdn_layer_params *layer, const void *x,
+                             const void *conv_weight, const void *conv_bias, const void *conv_state_in,
+                             void *conv_state_out, const void *a, const void *b, const float *A_log,
+                             const float *dt_bias, const float *state_in, const int32_t *cu_seqlens,
+                             float scale, const void *norm_scale, const void *gate, void *y,
+                             float *state_out, void *workspace, size_t workspace_bytes, void *stream);
+
+/* gdn_prefill_layer_workspace_bytes -- the workspace gdn_prefill_layer needs for `shape`
+ * (0 off the tensor-core shapes); never fails. */
+size_t gdn_prefill_layer_workspace_bytes(const gdn_shape *shape);
 
 /*
  * gdn_last_device_status -- synchronise `stream`, read the device check word

@@ -218,6 +218,67 @@ gdn_status gdn_prefill_norm(const gdn_shape *shape, const void *q, const void *k
                         state_out, workspace, workspace_bytes, true, stream, nullptr, &norm);
 }
 
+size_t gdn_prefill_layer_workspace_bytes(const gdn_shape *shape) {
+    const size_t base = gdn_prefill_workspace_bytes(shape);
+    if (base == 0) return 0;
+    return base + prefill_tc_conv_bytes(shape->seqlen * (int64_t)shape->batch, shape->h_qk);
+}
+
+gdn_status gdn_prefill_layer(const gdn_shape *shape, const gdn_layer_params *layer, const void *x,
+                             const void *conv_weight, const void *conv_bias, const void *conv_state_in,
+                             void *conv_state_out, const void *a, const void *b, const float *A_log,
+                             const float *dt_bias, const float *state_in, const int32_t *cu_seqlens,
+                             float scale, const void *norm_scale, const void *gate, void *y,
+                             float *state_out, void *workspace, size_t workspace_bytes, void *stream) {
+    gdn_status st = check_shape(shape, cu_seqlens != nullptr);
+    if (st != GDN_OK) return st;
+    if (layer == nullptr) return fail(GDN_ERR_INVALID_ARG, "layer is NULL");
+    if (layer->conv_kernel < 1 || layer->conv_kernel > 4)
+        return fail(GDN_ERR_INVALID_ARG, "conv_kernel %d is not in 1..4", layer->conv_kernel);
+    if (layer->conv_activation != GDN_ACT_NONE && layer->conv_activation != GDN_ACT_SILU)
+        return fail(GDN_ERR_INVALID_ARG, "the convolution's activation is NONE or SILU");
+    if (shape->io_dtype == GDN_F32 || shape->d_k != 128 || shape->d_v != 128)
+        return fail(GDN_ERR_UNSUPPORTED, "the layer prefill runs on the tensor-core path: 16-bit I/O, d_k = d_v = 128");
+    const int64_t tokens = cu_seqlens ? shape->seqlen : shape->seqlen * (int64_t)shape->batch;
+    const size_t es = io_size(shape->io_dtype);
+    const int64_t C = 2LL * shape->h_qk * shape->d_k + (int64_t)shape->h_v * shape->d_v;
+    const int64_t nseq = shape->num_seqs;
+    const size_t state_bytes = (size_t)nseq * (size_t)(layer->conv_kernel - 1) * (size_t)C * es;
+    if (nseq > 0 && tokens > 0) {
+        if (x == nullptr || conv_weight == nullptr) return fail(GDN_ERR_INVALID_ARG, "x or conv_weight is NULL");
+        if (!aligned(x, 16) || !aligned(conv_state_in, 16) || !aligned(conv_state_out, 16))
+            return fail(GDN_ERR_INVALID_ARG, "x and the conv states must be 16-byte aligned");
+        if (!aligned(conv_weight, es) || !aligned(conv_bias, es))
+            return fail(GDN_ERR_INVALID_ARG, "conv_weight / conv_bias is misaligned");
+    }
+    if (state_bytes > 0 && nseq > 0) {
+        if (conv_state_out == nullptr) return fail(GDN_ERR_INVALID_ARG, "conv_state_out is NULL");
+        if (conv_state_in != nullptr) {
+            const uintptr_t i0 = reinterpret_cast<uintptr_t>(conv_state_in), o0 = reinterpret_cast<uintptr_t>(conv_state_out);
+            if (i0 < o0 + state_bytes && o0 < i0 + state_bytes)
+                return fail(GDN_ERR_INVALID_ARG, "conv_state_out overlaps conv_state_in (the update cannot be in place)");
+        }
+    }
+    const NormEpilogue norm{norm_scale, gate, layer->norm_epsilon, layer->norm_activation, false};
+    if (tokens == 0 || nseq == 0) {
+        // No token: the present conv state is the past one, and the prefill copies its state.
+        if (state_bytes > 0 && nseq > 0) {
+            const cudaError_t e = conv_state_in != nullptr
+                                      ? cudaMemcpyAsync(conv_state_out, conv_state_in, state_bytes,
+                                                        cudaMemcpyDeviceToDevice, (cudaStream_t)stream)
+                                      : cudaMemsetAsync(conv_state_out, 0, state_bytes, (cudaStream_t)stream);
+            if (e != cudaSuccess) return cuda_fail(e, "conv state copy");
+        }
+        return prefill_impl(shape, x, x, x, a, b, A_log, dt_bias, state_in, cu_seqlens, scale, y,
+                            state_out, workspace, workspace_bytes, true, stream, nullptr, &norm);
+    }
+    const ConvPrologue conv{x, conv_weight, conv_bias, conv_state_in, conv_state_out, layer->conv_kernel,
+                            layer->conv_activation == GDN_ACT_SILU};
+    // q, k and v are x's channels: x stands in for them in the argument checks.
+    return prefill_impl(shape, x, x, x, a, b, A_log, dt_bias, state_in, cu_seqlens, scale, y,
+                        state_out, workspace, workspace_bytes, true, stream, nullptr, &norm, &conv);
+}
+
 }  // extern "C"
 
 size_t gdn::prefill_records_bytes(const gdn_shape *shape) {
@@ -238,7 +299,7 @@ gdn_status gdn::prefill_impl(const gdn_shape *shape, const void *q, const void *
                              const float *state_in, const int32_t *cu_seqlens, float scale, void *o,
                              float *state_out, void *workspace, size_t workspace_bytes,
                              bool allow_overlap, void *stream, const gdn_variant *variant,
-                             const NormEpilogue *norm) {
+                             const NormEpilogue *norm, const ConvPrologue *conv) {
     gdn_status st = check_shape(shape, cu_seqlens != nullptr);
     if (st != GDN_OK) return st;
     const int64_t tokens = cu_seqlens ? shape->seqlen : shape->seqlen * (int64_t)shape->batch;
@@ -288,6 +349,11 @@ gdn_status gdn::prefill_impl(const gdn_shape *shape, const void *q, const void *
         p.decay_per_key = variant->decay_per_key != 0;
         p.beta_shared = variant->beta_shared != 0;
     }
+    if (conv != nullptr) {
+        p.conv_x = conv->x; p.conv_w = conv->weight; p.conv_b = conv->bias;
+        p.conv_in = conv->state_in; p.conv_out = conv->state_out;
+        p.conv_k = conv->kernel; p.conv_silu = conv->silu;
+    }
     const gdn_dtype io = (gdn_dtype)shape->io_dtype;
     cudaError_t e;
     bool norm_after = norm != nullptr && tokens > 0;   // the norm as its own launch, in place
@@ -300,6 +366,9 @@ gdn_status gdn::prefill_impl(const gdn_shape *shape, const void *q, const void *
     // (The per-key path reads a's [64 tokens x 128] tiles by TMA: a must be 16-byte aligned.)
     const bool pk_room = !per_key || (workspace != nullptr && workspace_bytes >= records + pk_bytes &&
                                       aligned(a, 16));
+    const size_t conv_bytes = conv != nullptr ? prefill_tc_conv_bytes(tokens, shape->h_qk) : 0;
+    if (conv != nullptr && !prefill_tc_supported(p, io, tokens))
+        return fail(GDN_ERR_UNSUPPORTED, "the convolution prologue runs on the tensor-core prefill only");
     if (pk_room && prefill_tc_supported(p, io, tokens)) {
         if (norm_after && norm->fuse && aligned(norm->gate, 16)) {
             p.norm_scale = norm->scale;
@@ -308,7 +377,7 @@ gdn_status gdn::prefill_impl(const gdn_shape *shape, const void *q, const void *
             p.norm_silu = norm->activation == GDN_ACT_SILU;
             norm_after = false;
         }
-        const size_t need = records + pk_bytes;
+        const size_t need = records + pk_bytes + conv_bytes;
         if (workspace == nullptr || workspace_bytes < need)
             return fail(GDN_ERR_INVALID_ARG, "workspace of %zu bytes is below the %zu this call needs",
                         workspace == nullptr ? (size_t)0 : workspace_bytes, need);

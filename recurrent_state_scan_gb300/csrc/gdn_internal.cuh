@@ -44,6 +44,11 @@ struct ScanParams {
     const void *norm_scale, *norm_gate;
     float norm_eps;
     int32_t norm_silu;           // act = silu (1) or sigmoid (0)
+    // The causal convolution of the layer's mixed input before the scan (conv_x set; the
+    // tensor-core path only): q, k and v are then convolved inside the chunk prep.
+    const void *conv_x, *conv_w, *conv_b, *conv_in;
+    void *conv_out;
+    int32_t conv_k, conv_silu;
 };
 
 // ------------------------------------------------------------------ I/O types
@@ -163,6 +168,9 @@ size_t prefill_tc_tp_bytes(bool varlen, int64_t seqlen, int64_t batch, int h_v);
 // One decay per key dimension on the tensor-core path: the bytes of the Q~ and K~ arrays
 // ([tokens][h_v][128] in a 16-bit type, each 1 KiB aligned) that follow the records.
 size_t prefill_tc_pk_bytes(int64_t total_tokens, int h_v);
+// With the convolution before the scan: the bytes of the convolved q and k arrays
+// ([tokens][h_qk][128] in a 16-bit type, each 1 KiB aligned) that follow the records.
+size_t prefill_tc_conv_bytes(int64_t total_tokens, int h_qk);
 // workspace_bytes: the caller's workspace size; the time-parallel scan runs only when the
 // workspace also holds its buffers (and allow_overlap is set).
 cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_tokens,
@@ -180,6 +188,15 @@ bool encode_map_3d(CUtensorMap *m, const void *base, gdn_dtype io, const uint64_
                    const uint64_t strides[2], const uint32_t box[3]);
 
 // The gated RMS norm applied to o after the scan (gdn_prefill_norm).
+// The causal convolution before the prefill (gdn_prefill_layer): x [tokens][C], C =
+// 2 h_qk d_k + h_v d_v, read as [q | k | v]; weight [C][K], bias [C] or NULL, state in /
+// out [sequences][K - 1][C] (in may be NULL: zeros).
+struct ConvPrologue {
+    const void *x, *weight, *bias, *state_in;
+    void *state_out;
+    int32_t kernel, silu;
+};
+
 struct NormEpilogue {
     const void *scale;   // [d_v]
     const void *gate;    // like o
@@ -198,6 +215,6 @@ gdn_status prefill_impl(const gdn_shape *shape, const void *q, const void *k, co
                         const float *state_in, const int32_t *cu_seqlens, float scale, void *o,
                         float *state_out, void *workspace, size_t workspace_bytes,
                         bool allow_overlap, void *stream, const gdn_variant *variant = nullptr,
-                        const NormEpilogue *norm = nullptr);
+                        const NormEpilogue *norm = nullptr, const ConvPrologue *conv = nullptr);
 
 }  // namespace gdn

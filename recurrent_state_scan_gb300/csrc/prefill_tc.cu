@@ -114,6 +114,16 @@ struct TcParams {
     void *qt, *kt;
     CUtensorMap tm_qt, tm_kt;
     CUtensorMap tm_a;               // the gate logits a [tokens][h_v][128]
+    // The causal convolution before the scan (gdn_chunk_prep<IO, false, true>): q, k and v
+    // are channels of the layer's mixed input x [tokens][conv_C] ([q | k | v], heads
+    // outer), each convolved with its conv_k taps (conv_w [conv_C][conv_k], conv_b
+    // [conv_C] or NULL) over the conv state (conv_in [sequences][conv_k - 1][conv_C] or
+    // NULL: zeros) and the sequence's inputs, then silu when conv_silu.  The prep writes the
+    // convolved q and k to cq and ck ([tokens][h_qk][128]; the scan reads them through
+    // tm_q and tm_k) and each sequence's last conv_k - 1 inputs to conv_out.
+    const void *cx, *conv_w, *conv_b, *conv_in;
+    void *conv_out, *cq, *ck;
+    int32_t conv_k, conv_silu, conv_C;
 };
 
 // First workspace slot of sequence n.  Batched: n * chunks_per_seq.  Packed: slot
@@ -347,6 +357,7 @@ constexpr uint32_t kPrepCols = 128;            // TMEM columns of a prep CTA
 // entries are malformed) are not valid.
 struct PrepItem {
     int64_t slot, tc0;
+    int64_t n, ts, te;                 // sequence, its token range [ts, te)
     int32_t h, hq, Lc, first, valid, pad;
 };
 
@@ -379,6 +390,9 @@ __device__ PrepItem prep_item(const TcParams &p, int64_t item) {
     const int64_t c = slot - slot_base(p, n);
     if (c * kC >= t1 - t0 || c < p.seg_begin || c >= p.seg_end) return it;
     it.slot = slot;
+    it.n = n;
+    it.ts = t0;
+    it.te = t1;
     it.tc0 = t0 + c * kC;
     it.Lc = (int32_t)((t1 - it.tc0) < kC ? (t1 - it.tc0) : kC);
     // A segment's first chunk writes W for the scan to start from; every other chunk
@@ -396,6 +410,105 @@ struct PrepCtl {
     float kfp[kC], wsum_p[2];          // previous chunk: e^{G_C - G_j}
 };
 
+// ------------------------------------------------------------------ convolution prologue
+// The causal convolution of eight consecutive channels c0 .. c0 + 7 (one 16-byte group) of
+// the mixed input x, for `count` consecutive tokens from `tok` of the sequence that starts
+// at ts (sequence n), each written by put(j, packed outputs of token tok + j).  Output
+// token t is act(w[c][0] x[t - K + 1][c] + ... + w[c][K - 1] x[t][c] + bias[c]) in fp32,
+// oldest tap first, rounded once, as gdn_causal_conv computes it; positions before ts
+// come from the conv state.  A sliding window of K rows is loaded once per position.
+// Tokens at or past the sequence's end te (a ragged chunk's padded rows) are written as
+// zeros and nothing past te is read: the chunk algebra masks those rows with beta = 0,
+// which needs finite values in them.
+template <typename IO, typename Put>
+__device__ __forceinline__ void conv_group(const TcParams &p, int64_t n, int64_t ts, int64_t te,
+                                           int64_t tok, int count, int c0, Put &&put) {
+    const int K = p.conv_k;
+    const IO *x = static_cast<const IO *>(p.cx);
+    const IO *w = static_cast<const IO *>(p.conv_w);
+    // Window slot j holds position t - 3 + j; tap m (oldest first) sits in slot 4 - K + m,
+    // and the slots before it carry a zero weight (and a zero input), which leaves the
+    // first real product exact, so the sum runs in the convolution kernel's order.  The
+    // taps, the bias and the window stay packed in the I/O type (exact) to spare registers.
+    uint4 wp[4], bp, win[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float t[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            t[i] = j >= 4 - K ? IoType<IO>::ld(w + (size_t)(c0 + i) * K + (j - (4 - K))) : 0.f;
+        wp[j] = pack8<IO>(t);
+    }
+    bp = p.conv_b != nullptr ? *reinterpret_cast<const uint4 *>(static_cast<const IO *>(p.conv_b) + c0)
+                             : make_uint4(0, 0, 0, 0);
+    auto row = [&](int64_t pos) {   // x[pos][c0 ..], or the state before ts
+        uint4 u = make_uint4(0, 0, 0, 0);
+        if (pos >= te) {
+        } else if (pos >= ts) {
+            u = *reinterpret_cast<const uint4 *>(x + (size_t)pos * p.conv_C + c0);
+        } else if (p.conv_in != nullptr) {
+            const int64_t r = (K - 1) + (pos - ts);   // >= 0 for the taps that reach here
+            u = *reinterpret_cast<const uint4 *>(static_cast<const IO *>(p.conv_in) +
+                                                  ((size_t)n * (K - 1) + r) * p.conv_C + c0);
+        }
+        return u;
+    };
+#pragma unroll
+    for (int j = 0; j < 3; ++j) win[j] = j >= 4 - K ? row(tok - 3 + j) : make_uint4(0, 0, 0, 0);
+    auto word = [](const uint4 &u, int k) { return k == 0 ? u.x : k == 1 ? u.y : k == 2 ? u.z : u.w; };
+#pragma unroll 1
+    for (int e = 0; e < count; ++e) {
+        if (tok + e >= te) {
+            put(e, make_uint4(0, 0, 0, 0));
+            continue;
+        }
+        win[3] = row(tok + e);
+        float out[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float2 acc;
+            {
+                const float2 wv = Pack<IO>::unpack(word(wp[0], k)), xv = Pack<IO>::unpack(word(win[0], k));
+                acc = make_float2(wv.x * xv.x, wv.y * xv.y);
+            }
+#pragma unroll
+            for (int j = 1; j < 4; ++j) {
+                const float2 wv = Pack<IO>::unpack(word(wp[j], k)), xv = Pack<IO>::unpack(word(win[j], k));
+                acc.x = fmaf(wv.x, xv.x, acc.x);
+                acc.y = fmaf(wv.y, xv.y, acc.y);
+            }
+            const float2 bv = Pack<IO>::unpack(word(bp, k));
+            acc.x += bv.x;
+            acc.y += bv.y;
+            out[2 * k] = p.conv_silu ? __fdividef(acc.x, 1.0f + __expf(-acc.x)) : acc.x;
+            out[2 * k + 1] = p.conv_silu ? __fdividef(acc.y, 1.0f + __expf(-acc.y)) : acc.y;
+        }
+        put(e, pack8<IO>(out));
+        win[0] = win[1];
+        win[1] = win[2];
+        win[2] = win[3];
+    }
+}
+
+// The present conv state of sequence n for channels c0 .. c0 + 7: its last K - 1 inputs
+// (state rows first when the sequence is shorter than that).
+template <typename IO>
+__device__ __forceinline__ void conv_state_group(const TcParams &p, int64_t n, int64_t ts, int64_t te,
+                                                 int c0) {
+    const int K = p.conv_k;
+    for (int r = 0; r < K - 1; ++r) {
+        const int64_t pos = te - (K - 1) + r;
+        uint4 u = make_uint4(0, 0, 0, 0);
+        if (pos >= ts) {
+            u = *reinterpret_cast<const uint4 *>(static_cast<const IO *>(p.cx) + (size_t)pos * p.conv_C + c0);
+        } else if (p.conv_in != nullptr) {
+            u = *reinterpret_cast<const uint4 *>(static_cast<const IO *>(p.conv_in) +
+                                                  ((size_t)n * (K - 1) + (K - 1) + (pos - ts)) * p.conv_C + c0);
+        }
+        *reinterpret_cast<uint4 *>(static_cast<IO *>(p.conv_out) + ((size_t)n * (K - 1) + r) * p.conv_C + c0) = u;
+    }
+}
+
 // Persistent CTAs, three to an SM, walk the (chunk slot, value head) items with the
 // grid's stride.  TMEM (128 columns) holds one product at a time: D1 = [K; Q] K^T, then
 // D2 = [T'; T''] K (W on lanes 0-63), D3 = [T'; T''] V (U on lanes 64-127) and
@@ -405,7 +518,13 @@ struct PrepCtl {
 // kVariant: the update-rule switches and the shared beta are read from the parameters;
 // without it the gated delta rule with one beta per head is compiled in (the switches
 // cost the default rule about 5% when they were runtime values).
-template <typename IO, bool kVariant>
+// kConv (with the default rule): q, k and v are not loaded but convolved from the layer's
+// mixed input (conv_group) straight into the operand tiles -- K and Q at the item's
+// start, V by the threads the inversion's first step leaves idle, the previous chunk's K
+// while D2 runs -- and thread 0 arrives on the barriers the copies would have completed.
+// The first value head of each q/k head writes the convolved q and k for the scan, and the
+// items of a sequence's last chunk write its present conv state.
+template <typename IO, bool kVariant, bool kConv = false>
 __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_constant__ TcParams p) {
     constexpr bool kBf16 = std::is_same<IO, __nv_bfloat16>::value;
     const bool has_decay = !kVariant || p.has_decay != 0;
@@ -471,7 +590,29 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
         *reinterpret_cast<uint4 *>(sm + PP_TT + 16 * e) = make_uint4(0, 0, 0, 0);
     fence_async_smem();
     const int tok = (int)tc0;
-    if (pt == 0) {
+    // With the convolution: the channel group of q or k (head hq) this thread convolves,
+    // and whether this item writes them out (the first value head of the q/k head) and the
+    // present conv state (a sequence's last chunk).
+    const bool cv_qk_out = kConv && (h % (p.h_v / p.h_qk)) == 0;
+    const bool cv_last = kConv && tc0 + Lc == it.te;
+    if constexpr (kConv) {
+        // K and Q of this chunk: thread (group 0-31 of [q | k] head hq, tokens 8 tb ..).
+        const int grp = pt & 31, tb = pt >> 5;
+        const bool isk = grp >= 16;
+        const int i0 = 8 * (grp & 15);                         // channel within the head
+        const int c0 = (isk ? p.h_qk * kDK : 0) + hq * kDK + i0;
+        uint8_t *dst = sm + PP_KQ + (i0 >> 6) * kRegP + (isk ? 0 : 8192);
+        IO *gout = static_cast<IO *>(isk ? p.ck : p.cq) + (size_t)hq * kDK + i0;
+        conv_group<IO>(p, it.n, it.ts, it.te, tc0 + 8 * tb, 8, c0, [&](int e, const uint4 &u) {
+            const int t = 8 * tb + e;
+            *reinterpret_cast<uint4 *>(dst + sw128_offset(t, (i0 & 63) >> 3)) = u;
+            if (cv_qk_out && t < Lc) *reinterpret_cast<uint4 *>(gout + (size_t)(tc0 + t) * p.h_qk * kDK) = u;
+        });
+        if (cv_qk_out && cv_last && tb == 0) conv_state_group<IO>(p, it.n, it.ts, it.te, c0);
+        fence_async_smem();
+        named_bar(kBarPrep, kPrepThreads);
+        if (pt == 0) mbar_arrive(&ctl.full);
+    } else if (pt == 0) {
         mbar_arrive_expect_tx(&ctl.full, 4 * 8192);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
@@ -550,7 +691,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
             issued |= 2;
             ok = mbar_wait(&ctl.d1, ph, budget);
         }
-        if (ok) {
+        if (ok && !kConv) {
             mbar_arrive_expect_tx(&ctl.vfull, 2 * 8192);
 #pragma unroll
             for (int r = 0; r < 2; ++r)
@@ -614,17 +755,31 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
         named_bar(kBarPrep, kPrepThreads);
 
         // T = (I + A)^-1, written as [T diag(beta gamma); T diag(beta)] (K-major).
-        // Meanwhile one thread of warp 2 looks up the CTA's next item.
+        // Meanwhile one thread of warp 2 looks up the CTA's next item, and with the
+        // convolution 128 of the other threads convolve V over the spent Q rows (D1 has
+        // read them): thread (group of 8 v channels, 8 tokens).
         auto next_item = [&](int t) {
             if (t == 0) ctl.nxt = prep_item(p, item + gridDim.x);
+            if constexpr (kConv) {
+                if (t < 128) {
+                    const int grp = t & 15, tb = t >> 4, i0 = 8 * grp;
+                    const int c0 = 2 * p.h_qk * kDK + h * kDK + i0;
+                    uint8_t *dst = sm + PP_KQ + (i0 >> 6) * kRegP + 8192;
+                    conv_group<IO>(p, it.n, it.ts, it.te, tc0 + 8 * tb, 8, c0, [&](int e, const uint4 &u) {
+                        *reinterpret_cast<uint4 *>(dst + sw128_offset(8 * tb + e, (i0 & 63) >> 3)) = u;
+                    });
+                    if (cv_last && tb == 0) conv_state_group<IO>(p, it.n, it.ts, it.te, c0);
+                }
+            }
         };
         invert_chunk<IO>(As, sm + PP_TT, ctl.beta, ctl.gam, has_delta ? 1.f : 0.f, pt, next_item);
         fence_async_smem();
         tc_fence_before();
         named_bar(kBarPrep, kPrepThreads);
+        if (kConv && pt == 0) mbar_arrive(&ctl.vfull);
         if (pt == 0) {
             // The previous chunk's keys (for M) into the spent A/T tile.
-            if (!first) {
+            if (!first && !kConv) {
                 mbar_arrive_expect_tx(&ctl.kprev, 2 * 8192);
 #pragma unroll
                 for (int r = 0; r < 2; ++r)
@@ -639,8 +794,23 @@ __global__ void __launch_bounds__(kPrepThreads, 3) gdn_chunk_prep(const __grid_c
                         kIdD2, k > 0);
             mma_commit(&ctl.d2);
             issued |= 4;
-            ok = mbar_wait(&ctl.d2, ph, budget);
         }
+        if constexpr (kConv) {
+            // The previous chunk's keys, convolved while D2 runs: thread (group of 8 k
+            // channels, 4 tokens).
+            if (!first) {
+                const int grp = pt & 15, tb = pt >> 4, i0 = 8 * grp;
+                const int c0 = p.h_qk * kDK + hq * kDK + i0;
+                uint8_t *dst = sm + PP_AS + (i0 >> 6) * 8192;
+                conv_group<IO>(p, it.n, it.ts, it.te, tc0 - kC + 4 * tb, 4, c0, [&](int e, const uint4 &u) {
+                    *reinterpret_cast<uint4 *>(dst + sw128_offset(4 * tb + e, (i0 & 63) >> 3)) = u;
+                });
+                fence_async_smem();
+                named_bar(kBarPrep, kPrepThreads);
+                if (pt == 0) mbar_arrive(&ctl.kprev);
+            }
+        }
+        if (pt == 0) ok = mbar_wait(&ctl.d2, ph, budget);
         failed = bar_any(kBarPrep, kPrepThreads, !ok);
     }
     const int row = 32 * q + lane;
@@ -2201,6 +2371,21 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
     }
 }
 
+// ===================================================================== conv state, empty sequences
+// The present conv state of a packed sequence with no tokens is its past state (zeros
+// without one); the prep writes it for every other sequence.  One CTA per sequence.
+template <typename IO>
+__global__ void __launch_bounds__(256) conv_state_empty(const __grid_constant__ TcParams p) {
+    const int64_t n = blockIdx.x;
+    int64_t t0, t1;
+    if (!seq_range(p.cu_seqlens, p.seqlen, p.num_seqs, p.status, n, t0, t1) || t1 > t0) return;
+    const size_t cnt = (size_t)(p.conv_k - 1) * p.conv_C;
+    IO *dst = static_cast<IO *>(p.conv_out) + n * cnt;
+    const IO *src = p.conv_in != nullptr ? static_cast<const IO *>(p.conv_in) + n * cnt : nullptr;
+    for (size_t e = threadIdx.x; e < cnt; e += blockDim.x)
+        IoType<IO>::st(dst + e, src != nullptr ? IoType<IO>::ld(src + e) : 0.f);
+}
+
 // ===================================================================== time-parallel combine
 // The state entering segment k of a sequence: S_1 = Psi_0 (segment 0 ran from state_in),
 // S_{k+1} = Phi_k S_k + Psi_k.  One launch per step k: a CTA owns a 32 x 32 tile of
@@ -2523,6 +2708,12 @@ cudaError_t configure() {
             e = cudaFuncSetAttribute(gdn_chunk_prep<IO, true>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      (int)cudaSharedmemCarveoutMaxShared);
         if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gdn_chunk_prep<IO, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kPrepSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gdn_chunk_prep<IO, false, true>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared);
+        if (e == cudaSuccess)
             e = cudaFuncSetAttribute(gdn_chunk_prep_pk<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kPkSmem);
         if (e == cudaSuccess)
@@ -2578,6 +2769,11 @@ cudaError_t launch_prep(const TcParams &tp, int64_t items, cudaStream_t stream) 
     if (slots <= 0) return cudaErrorInvalidConfiguration;
     TcParams pk = tp;
     pk.prep_items = items;
+    if (tp.cx != nullptr) {   // the convolution prologue, with the default rule
+        const int64_t ctas_cv = items <= 3 * (int64_t)slots ? items : slots;
+        gdn_chunk_prep<IO, false, true><<<(unsigned)ctas_cv, kPrepThreads, kPrepSmem, stream>>>(pk);
+        return cudaGetLastError();
+    }
     if (tp.per_key) {
         const int64_t ctas_pk = items <= 2 * (int64_t)slots ? items : slots;
         gdn_chunk_prep_pk<IO><<<(unsigned)ctas_pk, kPrepThreads, kPkSmem, stream>>>(pk);
@@ -2778,6 +2974,11 @@ bool encode_map_3d(CUtensorMap *m, const void *base, gdn_dtype io, const uint64_
     return r == CUDA_SUCCESS;
 }
 
+size_t prefill_tc_conv_bytes(int64_t total_tokens, int h_qk) {
+    const size_t each = ((size_t)total_tokens * h_qk * kDK * 2 + 1023) & ~(size_t)1023;
+    return 2 * each;
+}
+
 size_t prefill_tc_pk_bytes(int64_t total_tokens, int h_v) {
     const size_t each = ((size_t)total_tokens * h_v * kDK * 2 + 1023) & ~(size_t)1023;
     return 2 * each;
@@ -2859,18 +3060,44 @@ cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_t
             return cudaErrorInvalidValue;
         records += 2 * each;
     }
+    if (p.conv_x != nullptr) {
+        // The convolved q and k follow the records; the caller has checked the room.
+        const size_t each = prefill_tc_conv_bytes(total_tokens, p.h_qk) / 2;
+        uint8_t *base = static_cast<uint8_t *>(workspace) + records;
+        tp.cx = p.conv_x;
+        tp.conv_w = p.conv_w;
+        tp.conv_b = p.conv_b;
+        tp.conv_in = p.conv_in;
+        tp.conv_out = p.conv_out;
+        tp.conv_k = p.conv_k;
+        tp.conv_silu = p.conv_silu;
+        tp.conv_C = 2 * p.h_qk * kDK + p.h_v * kDK;
+        tp.cq = base;
+        tp.ck = base + each;
+        if (!make_map(&tp.tm_q, tp.cq, io, p.h_qk, total_tokens) ||
+            !make_map(&tp.tm_k, tp.ck, io, p.h_qk, total_tokens))
+            return cudaErrorInvalidValue;
+        records += 2 * each;
+    }
     const int tps = allow_overlap && p.norm_gate == nullptr
                         ? tp_segments(varlen, p.seqlen, p.num_seqs, p.h_v) : 1;
     if (tps > 1 && workspace_bytes >= records + tp_layout(p.seqlen, p.num_seqs, p.h_v, tps).total) {
         uint8_t *extra = static_cast<uint8_t *>(workspace) + records;
         if (!make_map(&tp.tm_r, extra + tp_layout(p.seqlen, p.num_seqs, p.h_v, tps).r, io, p.h_v, total_tokens))
             return cudaErrorInvalidValue;
-        if (io == GDN_BF16) return launch_tp<__nv_bfloat16>(tp, n_slots, tps, extra, stream);
-        return launch_tp<__half>(tp, n_slots, tps, extra, stream);
+        cudaError_t e = io == GDN_BF16 ? launch_tp<__nv_bfloat16>(tp, n_slots, tps, extra, stream)
+                                       : launch_tp<__half>(tp, n_slots, tps, extra, stream);
+        return e;   // batched: no sequence is empty
     }
     const int nseg = allow_overlap ? prefill_tc_segments(varlen, p.seqlen, p.num_seqs, p.h_v) : 1;
-    if (io == GDN_BF16) return launch_typed<__nv_bfloat16>(tp, n_slots, nseg, stream);
-    return launch_typed<__half>(tp, n_slots, nseg, stream);
+    cudaError_t e = io == GDN_BF16 ? launch_typed<__nv_bfloat16>(tp, n_slots, nseg, stream)
+                                   : launch_typed<__half>(tp, n_slots, nseg, stream);
+    if (e == cudaSuccess && tp.cx != nullptr && varlen && p.conv_k > 1) {
+        if (io == GDN_BF16) conv_state_empty<__nv_bfloat16><<<(unsigned)p.num_seqs, 256, 0, stream>>>(tp);
+        else conv_state_empty<__half><<<(unsigned)p.num_seqs, 256, 0, stream>>>(tp);
+        e = cudaGetLastError();
+    }
+    return e;
 }
 
 }  // namespace gdn

@@ -27,7 +27,8 @@ EXPORTS = ("gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode_step",
            "gdn_last_error_message", "gdn_prefill_noalloc", "gdn_decode_step_slots",
            "gdn_scan_window", "gdn_scan_variant", "gdn_causal_conv", "gdn_causal_conv_slots",
            "gdn_gated_rmsnorm", "gdn_set_wait_budget", "gdn_decode_layer", "gdn_prefill_variant",
-           "gdn_prefill_norm", "gdn_prefill_variant_workspace_bytes", "gdn_prefill_variant_plan")
+           "gdn_prefill_norm", "gdn_prefill_variant_workspace_bytes", "gdn_prefill_variant_plan",
+           "gdn_prefill_layer", "gdn_prefill_layer_workspace_bytes")
 PATH_SIMT, PATH_TC, PATH_TC_TP = 1, 2, 3
 # gdn_rule codes.
 RULES = {"gated_delta": 0, "delta": 1, "gated": 2, "linear": 3}
@@ -137,6 +138,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.gdn_decode_layer.restype = ctypes.c_int
     lib.gdn_decode_layer.argtypes = [S, ctypes.POINTER(GdnLayerParams), P, P, P, P, P, P, P, P, P,
                                      P, ctypes.c_float, P, P, P, P]
+    lib.gdn_prefill_layer.restype = ctypes.c_int
+    lib.gdn_prefill_layer.argtypes = [S, ctypes.POINTER(GdnLayerParams), P, P, P, P, P, P, P, P, P, P, P,
+                                      ctypes.c_float, P, P, P, P, P, ctypes.c_size_t, P]
+    lib.gdn_prefill_layer_workspace_bytes.restype = ctypes.c_size_t
+    lib.gdn_prefill_layer_workspace_bytes.argtypes = [S]
     _lib = lib
     return lib
 
@@ -724,3 +730,61 @@ def gdn_decode_layer(x, conv_weight, conv_bias, conv_state_in, conv_state_out, a
                                 _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(state), float(scale),
                                 _ptr(norm_scale), _ptr(gate), _ptr(y), _stream(stream)))
     return y
+
+
+def gdn_prefill_layer(x, conv_weight, conv_bias, conv_state_in, a, b, A_log, dt_bias, state_in,
+                      cu_seqlens, norm_scale, gate, *, h_qk: int, h_v: int, scale: float = 0.0,
+                      conv_activation: str = "silu", norm_activation: str = "silu", eps: float = 1e-5,
+                      y=None, state_out=None, conv_state_out=None, workspace=None, stream=None):
+    """The prefill of a layer: causal conv over x (channels [q | k | v], C = 2 h_qk 128 +
+    h_v 128; [B, T, C], or [1, total, C] packed with cu_seqlens), the chunked prefill on its
+    q, k, v, then the gated RMS norm of o.  conv_weight [C, 1, K] (K <= 4); conv_bias [C] or
+    None; conv_state_in [N, K - 1, C] or None (zeros).  Returns (y [.., h_v, 128],
+    state_out [N, h_v, 128, 128], conv_state_out [N, K - 1, C])."""
+    lib = load()
+    dt = x.dtype
+    if dt not in _DTYPE_CODE:
+        raise GdnError(GDN_ERR_INVALID_ARG, f"unsupported io dtype {dt}")
+    for name, t in (("x", x), ("conv_weight", conv_weight), ("a", a), ("b", b),
+                    ("norm_scale", norm_scale), ("gate", gate)):
+        _need_cuda(name, t, dt)
+    for name, t in (("conv_bias", conv_bias), ("conv_state_in", conv_state_in)):
+        if t is not None:
+            _need_cuda(name, t, dt)
+    _need_cuda("A_log", A_log, torch.float32)
+    _need_cuda("dt_bias", dt_bias, torch.float32)
+    if x.dim() != 3:
+        raise GdnError(GDN_ERR_INVALID_ARG, "x must be [B, T, C]")
+    B, T, C = x.shape
+    d = 128
+    if C != 2 * h_qk * d + h_v * d or conv_weight.numel() % C != 0:
+        raise GdnError(GDN_ERR_INVALID_ARG, "x's channels must be 2 h_qk 128 + h_v 128; weight [C, 1, K]")
+    K = conv_weight.numel() // C
+    if cu_seqlens is not None:
+        _need_cuda("cu_seqlens", cu_seqlens, torch.int32)
+        if B != 1:
+            raise GdnError(GDN_ERR_INVALID_ARG, "packed sequences need x [1, total, C]")
+        n_seq = cu_seqlens.numel() - 1
+        shape = make_shape(_DTYPE_CODE[dt], 1, T, n_seq, h_qk, h_v, d, d)
+    else:
+        n_seq = B
+        shape = make_shape(_DTYPE_CODE[dt], B, T, B, h_qk, h_v, d, d)
+    if state_in is not None:
+        _need_cuda("state_in", state_in, torch.float32)
+    if y is None:
+        y = torch.empty((B, T, h_v, d), dtype=dt, device=x.device)
+    if state_out is None:
+        state_out = torch.empty((n_seq, h_v, d, d), dtype=torch.float32, device=x.device)
+    if conv_state_out is None:
+        conv_state_out = torch.empty((n_seq, max(K - 1, 0), C), dtype=dt, device=x.device)
+    need = int(lib.gdn_prefill_layer_workspace_bytes(ctypes.byref(shape)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    layer = GdnLayerParams(K, ACTIVATIONS[conv_activation], ACTIVATIONS[norm_activation], float(eps))
+    _check(lib.gdn_prefill_layer(ctypes.byref(shape), ctypes.byref(layer), _ptr(x), _ptr(conv_weight),
+                                 _ptr(conv_bias), _ptr(conv_state_in), _ptr(conv_state_out), _ptr(a),
+                                 _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(state_in), _ptr(cu_seqlens),
+                                 float(scale), _ptr(norm_scale), _ptr(gate), _ptr(y), _ptr(state_out),
+                                 _ptr(workspace), ws_bytes, _stream(stream)))
+    return y, state_out, conv_state_out

@@ -431,6 +431,118 @@ PREFILL_NORM_WORKLOADS = {
 }
 
 
+@dataclasses.dataclass(frozen=True)
+class PrefillLayerSpec:
+    """The prefill of a whole layer (gdn_prefill_layer): the causal conv over the mixed
+    input x [.., C] (C = 2 h_qk 128 + h_v 128, channels [q | k | v]), the chunked prefill
+    on its q, k, v, then the gated RMS norm of o.
+
+    Recipe (one default_rng(seed), float64 draws in this order, each rounded once to the
+    I/O dtype, A_log / dt_bias / state to fp32): the lengths U[lo, hi] when varlen_range is
+    set; x ~ N(0, x_std^2); the weight ~ U(-1/sqrt(K), 1/sqrt(K)); the bias likewise when
+    asked; the conv state ~ N(0, 1); a, b ~ N(0, 1); A_log ~ U(-1, 1); dt_bias ~
+    N(0, 0.1); the initial state ~ N(0, state_std^2) (0: none); the norm scale ~
+    N(1, 0.1); the gate ~ N(0, 1).  The layer does not normalise q and k, so x_std = 0.3
+    keeps the convolved keys' squared norm near 1 (about 128 x 0.3^2 / 12), where the
+    delta rule's update I - beta k k^T stays contracting over thousands of tokens."""
+    name: str
+    io: str
+    h_qk: int
+    h_v: int
+    seed: int
+    batch: int = 1
+    seqlen: int = 0
+    lengths: Optional[tuple] = None
+    varlen_range: Optional[tuple] = None
+    n_varlen: int = 0
+    kernel: int = 4
+    bias: bool = True
+    silu: bool = True
+    x_std: float = 0.3
+    state_std: float = 0.05
+    eps: float = 1e-6
+    activation: str = "silu"
+
+
+@dataclasses.dataclass
+class PrefillLayerInputs:
+    spec: PrefillLayerSpec
+    cu_seqlens: np.ndarray        # int64 [N + 1]
+    x: torch.Tensor               # [B, T, C] (packed: [1, total, C])
+    w: torch.Tensor               # [C, 1, K]
+    bias: Optional[torch.Tensor]  # [C]
+    conv_state: torch.Tensor      # [N, K - 1, C]
+    a: torch.Tensor               # [B, T, h_v]
+    b: torch.Tensor
+    A_log: torch.Tensor           # [h_v] fp32
+    dt_bias: torch.Tensor
+    state_in: Optional[torch.Tensor]   # [N, h_v, 128, 128] fp32
+    norm_scale: torch.Tensor      # [128]
+    gate: torch.Tensor            # [B, T, h_v, 128]
+    scale: float
+    f64: dict
+
+    @property
+    def n_seq(self) -> int:
+        return len(self.cu_seqlens) - 1
+
+    @property
+    def total_tokens(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+    @property
+    def varlen(self) -> bool:
+        return self.spec.lengths is not None or self.spec.varlen_range is not None
+
+
+def draw_prefill_layer(spec: PrefillLayerSpec) -> PrefillLayerInputs:
+    rng = np.random.default_rng(spec.seed)
+    if spec.varlen_range is not None:
+        lo, hi = spec.varlen_range
+        lengths = rng.integers(lo, hi + 1, spec.n_varlen)
+    elif spec.lengths is not None:
+        lengths = np.asarray(spec.lengths, dtype=np.int64)
+    else:
+        lengths = None
+    if lengths is not None:
+        B, T = 1, int(np.sum(lengths))
+        cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    else:
+        B, T = spec.batch, spec.seqlen
+        cu = np.arange(B + 1, dtype=np.int64) * T
+    N, K = len(cu) - 1, spec.kernel
+    C = 2 * spec.h_qk * 128 + spec.h_v * 128
+    x = rng.normal(0.0, spec.x_std, (B, T, C))
+    lim = 1.0 / math.sqrt(K)
+    w = rng.uniform(-lim, lim, (C, 1, K))
+    bias = rng.uniform(-lim, lim, C) if spec.bias else None
+    conv_state = rng.normal(0.0, 1.0, (N, K - 1, C))
+    a = rng.standard_normal((B, T, spec.h_v))
+    b = rng.standard_normal((B, T, spec.h_v))
+    A_log = rng.uniform(-1.0, 1.0, spec.h_v)
+    dt_bias = rng.normal(0.0, 0.1, spec.h_v)
+    state = rng.normal(0.0, spec.state_std, (N, spec.h_v, 128, 128)) if spec.state_std > 0 else None
+    norm_scale = rng.normal(1.0, 0.1, 128)
+    gate = rng.standard_normal((B, T, spec.h_v, 128))
+    t = {n: (None if v is None else _round(v, spec.io))
+         for n, v in (("x", x), ("w", w), ("bias", bias), ("conv_state", conv_state), ("a", a),
+                      ("b", b), ("norm_scale", norm_scale), ("gate", gate))}
+    t["A_log"] = _round(A_log, "f32")
+    t["dt_bias"] = _round(dt_bias, "f32")
+    t["state_in"] = None if state is None else _round(state, "f32")
+    f64 = {n: (None if v is None else _widen(v).reshape(v.shape)) for n, v in t.items()}
+    return PrefillLayerInputs(spec=spec, cu_seqlens=cu, scale=1.0 / math.sqrt(128), f64=f64, **t)
+
+
+PREFILL_LAYER_WORKLOADS = {
+    # The packed varlen prefill's shape (8 sequences drawn from U[512, 8192], 16 heads,
+    # d = 128) with a 4-tap conv (bias, silu) in front and the gated norm after.
+    "varlen_bf16_prefill_layer": PrefillLayerSpec("varlen_bf16_prefill_layer", io="bf16", h_qk=16,
+                                                  h_v=16, seed=1016, varlen_range=(512, 8192),
+                                                  n_varlen=8),
+}
+
+
 def any_workload(name: str):
     """Draw any named workload: the scan's, the convolution's or the norm's."""
     if name in WORKLOADS:
@@ -441,8 +553,11 @@ def any_workload(name: str):
         return draw_conv(CONV_WORKLOADS[name])
     if name in LAYER_WORKLOADS:
         return draw_layer(LAYER_WORKLOADS[name])
+    if name in PREFILL_LAYER_WORKLOADS:
+        return draw_prefill_layer(PREFILL_LAYER_WORKLOADS[name])
     return draw_norm(NORM_WORKLOADS[name])
 
 
 ALL_WORKLOADS = sorted(list(WORKLOADS) + list(CONV_WORKLOADS) + list(NORM_WORKLOADS) +
-                       list(LAYER_WORKLOADS) + list(PREFILL_NORM_WORKLOADS))
+                       list(LAYER_WORKLOADS) + list(PREFILL_NORM_WORKLOADS) +
+                       list(PREFILL_LAYER_WORKLOADS))
