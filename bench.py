@@ -896,6 +896,229 @@ def main_prefill_norm(args, rank, world, local):
         dist.destroy_process_group()
 
 
+def prefill_layer_io_bytes(inp) -> dict:
+    """One layer prefill: x, the conv's weight, bias and states, a, b, the gate parameters,
+    the recurrent states, the norm's scale and gate, and y, each once."""
+    s = inp.spec
+    es = inp.x.element_size()
+    T, N, K = inp.total_tokens, inp.n_seq, s.kernel
+    C = inp.x.shape[-1]
+    st = N * s.h_v * 128 * 128 * 4
+    y = T * s.h_v * 128 * es
+    return {"x": T * C * es, "conv_weight": C * K * es, "conv_bias": C * es if inp.bias is not None else 0,
+            "conv_state_in": N * (K - 1) * C * es, "conv_state_out": N * (K - 1) * C * es,
+            "a": T * s.h_v * es, "b": T * s.h_v * es, "params": 2 * s.h_v * 4,
+            "state_in": st if inp.state_in is not None else 0, "state_out": st,
+            "norm_scale": 128 * es, "gate": y, "y": y}
+
+
+def prefill_layer_oracle(inp, tokens: int):
+    """The float64 oracle chain over the first sequences that hold `tokens` tokens: the
+    convolution per sequence, its output rounded to the I/O type, the scan, o rounded, the
+    gated RMS norm.  Returns the tokens covered."""
+    import oracle
+    s, cu = inp.spec, [int(c) for c in inp.cu_seqlens]
+    n = 1
+    while n < inp.n_seq and cu[n] < tokens:
+        n += 1
+    T = cu[n]
+    C = inp.x.shape[-1]
+    x = inp.x.reshape(-1, C)[:T].double().numpy()
+    w = inp.w.double().numpy()
+    bias = None if inp.bias is None else inp.bias.double().numpy()
+    cs = inp.conv_state.double().numpy()
+    yc = np.zeros_like(x)
+    for i in range(n):
+        if cu[i + 1] > cu[i]:
+            yc[cu[i]:cu[i + 1]] = oracle.causal_conv(x[cu[i]:cu[i + 1]][None], w, bias, cs[i][None],
+                                                     silu=s.silu)[0][0]
+    yc = torch.from_numpy(yc).to(inp.x.dtype).double().numpy()
+    hk = s.h_qk * 128
+    st = None if inp.state_in is None else inp.state_in[:n].double().numpy()
+    o, _ = oracle.scan(np.asarray(cu[:n + 1]), s.h_qk, s.h_v, 128, 128, yc[:, :hk], yc[:, hk:2 * hk],
+                       yc[:, 2 * hk:], a=inp.a.reshape(-1, s.h_v)[:T].double().numpy(),
+                       b=inp.b.reshape(-1, s.h_v)[:T].double().numpy(), A_log=inp.A_log.double().numpy(),
+                       dt_bias=inp.dt_bias.double().numpy(), state_in=st, scale=inp.scale,
+                       threads=cpu_threads())
+    o_io = torch.from_numpy(np.ascontiguousarray(o)).to(inp.x.dtype).double().numpy()
+    g = inp.gate.reshape(-1, 128)[:T * s.h_v].double().numpy()
+    oracle.gated_rmsnorm(o_io.reshape(-1, 128), inp.norm_scale.double().numpy(), g, s.eps, s.activation)
+    return T
+
+
+def time_prefill_layer_oracle(inp, budget_s: float, min_reps: int = 1, tokens: int = 4096):
+    reps, t0, done = 0, time.perf_counter(), 0
+    while reps < min_reps or time.perf_counter() - t0 < budget_s:
+        done = prefill_layer_oracle(inp, tokens)
+        reps += 1
+    return (time.perf_counter() - t0) / reps, reps, done
+
+
+def main_prefill_layer(args, rank, world, local):
+    inp = workloads.any_workload(args.workload)
+    s = inp.spec
+    nbytes = int(sum(prefill_layer_io_bytes(inp).values()))
+    C = inp.x.shape[-1]
+    config = {"workload": s.name, "io_dtype": s.io, "num_seqs": inp.n_seq, "total_tokens": inp.total_tokens,
+              "h_qk": s.h_qk, "h_v": s.h_v, "d_k": 128, "d_v": 128, "channels": C,
+              "conv": {"kernel": s.kernel, "bias": inp.bias is not None, "activation": "silu" if s.silu else "none"},
+              "norm": {"eps": s.eps, "activation": s.activation},
+              "l2": "flushed before every step (256 MiB write, untimed)",
+              "parallelism": f"replicas: the full workload on each of {world} GPU(s), no collective",
+              "op": "layer prefill: causal conv of the mixed input (fused into the chunk prep), the "
+                    "gated delta-rule prefill, the gated RMS norm of o: gdn_prefill_layer"}
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        for _ in range(args.warmup):
+            time_prefill_layer_oracle(inp, 0.0)
+        per, reps, done = time_prefill_layer_oracle(inp, 0.0, min_reps=args.steps)
+        value = done / per
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config,
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+                             "sample": f"the first {done} of {inp.total_tokens} tokens per step "
+                                       f"(whole sequences), {reps} steps"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}), flush=True)
+        return
+
+    from recurrent_state_scan_gb300 import (gdn, gdn_causal_conv, gdn_gated_rmsnorm, gdn_prefill,
+                                            gdn_prefill_layer, load)
+    load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    names = ("x", "w", "bias", "conv_state", "a", "b", "A_log", "dt_bias", "norm_scale", "gate")
+    t = {n: (None if getattr(inp, n) is None else getattr(inp, n).to(dev)) for n in names}
+    state0 = None if inp.state_in is None else inp.state_in.to(dev)
+    cu = torch.tensor(inp.cu_seqlens, dtype=torch.int32, device=dev) if inp.varlen else None
+    T, N = inp.total_tokens, inp.n_seq
+    y = torch.empty(tuple(inp.x.shape[:2]) + (s.h_v, 128), dtype=inp.x.dtype, device=dev)
+    state_out = torch.empty((N, s.h_v, 128, 128), dtype=torch.float32, device=dev)
+    cs_out = torch.empty((N, s.kernel - 1, C), dtype=inp.x.dtype, device=dev)
+    shape = gdn.make_shape(gdn._DTYPE_CODE[inp.x.dtype], 1 if inp.varlen else inp.x.shape[0],
+                           T if inp.varlen else inp.x.shape[1], N, s.h_qk, s.h_v, 128, 128)
+    ws = torch.empty(max(1, gdn.gdn_prefill_layer_workspace_bytes(shape)), dtype=torch.uint8, device=dev)
+    act = "silu" if s.silu else "none"
+
+    def call(d):
+        gdn_prefill_layer(d["x"], d["w"], d["bias"], d["conv_state"], d["a"], d["b"], d["A_log"],
+                          d["dt_bias"], state0, cu, d["norm_scale"], d["gate"], h_qk=s.h_qk, h_v=s.h_v,
+                          scale=inp.scale, conv_activation=act, norm_activation=s.activation, eps=s.eps,
+                          y=y, state_out=state_out, conv_state_out=cs_out, workspace=ws, stream=stream)
+
+    # The separate calls: the conv per sequence (its kernel has no packed form) into q, k,
+    # v buffers, the prefill, then the norm.
+    hk = s.h_qk * 128
+    qkv = torch.empty((T, C), dtype=inp.x.dtype, device=dev)
+    q, k, v = (torch.empty((1, T, h, 128), dtype=inp.x.dtype, device=dev) for h in (s.h_qk, s.h_qk, s.h_v))
+    o = torch.empty_like(y)
+    ws2 = torch.empty(max(1, gdn.gdn_prefill_workspace_bytes(shape)), dtype=torch.uint8, device=dev)
+    cuh = [int(c) for c in inp.cu_seqlens]
+
+    def separate(d):
+        x2 = d["x"].reshape(-1, C)
+        for i in range(N):
+            if cuh[i + 1] > cuh[i]:
+                gdn_causal_conv(x2[cuh[i]:cuh[i + 1]][None], d["w"], d["bias"], d["conv_state"][i:i + 1],
+                                activation=act, y=qkv[cuh[i]:cuh[i + 1]][None],
+                                state_out=cs_out[i:i + 1], stream=stream)
+        q.view(T, hk).copy_(qkv[:, :hk])
+        k.view(T, hk).copy_(qkv[:, hk:2 * hk])
+        v.view(T, -1).copy_(qkv[:, 2 * hk:])
+        gdn_prefill(q, k, v, d["a"], d["b"], d["A_log"], d["dt_bias"], state0, cu, inp.scale, o=o,
+                    state_out=state_out, workspace=ws2, stream=stream)
+        gdn_gated_rmsnorm(o, d["norm_scale"], d["gate"], s.eps, s.activation, y=y, stream=stream)
+
+    def timed(fn, d):
+        for _ in range(args.warmup):
+            flush.zero_()
+            fn(d)
+        torch.cuda.synchronize(dev)
+        st = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        en = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            flush.zero_()
+            st[i].record(stream)
+            fn(d)
+            en[i].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        return max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in zip(st, en)])), world)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    ms = timed(call, t)
+    clocks = sampler.stop() if sampler else None
+    ms_sep = timed(separate, t)
+
+    e2e = None
+    if not args.no_e2e:
+        # Pinned host inputs (x, a, b, the gate) in; y, the state and the conv state out.
+        host = {n: getattr(inp, n).pin_memory() for n in ("x", "a", "b", "gate")}
+        dbuf = dict(t)
+        for n, hv in host.items():
+            dbuf[n] = torch.empty_like(hv, device=dev)
+        y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        s_host = torch.empty(state_out.shape, dtype=torch.float32).pin_memory()
+        c_host = torch.empty(cs_out.shape, dtype=cs_out.dtype).pin_memory()
+        h2d = sum(hv.numel() * hv.element_size() for hv in host.values())
+        d2h = sum(h.numel() * h.element_size() for h in (y_host, s_host, c_host))
+
+        def e2e_step(d):
+            for n, hv in host.items():
+                d[n].copy_(hv, non_blocking=True)
+            call(d)
+            y_host.copy_(y, non_blocking=True)
+            s_host.copy_(state_out, non_blocking=True)
+            c_host.copy_(cs_out, non_blocking=True)
+
+        ems = timed(e2e_step, dbuf)
+        e2e = {"value": world * T / (ems / 1e3), "unit": "tokens/s", "ms_per_step": ems,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    pk, pk_kind = peaks()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    launches = 3 + (1 if inp.varlen and s.kernel > 1 else 0)
+    line = {
+        "metric": METRIC, "value": world * T / (ms / 1e3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": s.io,
+        "data": "synthetic", "config": config,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm_gbs"], "traffic": profiled_traffic(args.workload, "prefill"),
+                     "peak_source": f"{pk_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+                     if pk_kind == "measured" else "fallback 6.8 TB/s",
+                     "kernels": "gdn_chunk_prep (convolution form) + gdn_chunk_scan + conv_state_empty "
+                                "+ gated_rmsnorm_rows_kernel, one call"},
+        "separate_calls": {"ms_per_step": ms_sep,
+                           "calls": f"gdn_causal_conv per sequence ({N}), q/k/v copies, gdn_prefill "
+                                    "(prep, scan), gdn_gated_rmsnorm"},
+        "gpu_launches": args.steps * launches,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if clocks is not None:
+        line["clocks"] = clocks
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        per, reps, done = time_prefill_layer_oracle(inp, 10.0)
+        line["cpu_baseline"] = {"value": done / per, "unit": "tokens/s", "cores": cpu_threads(),
+                                "kind": "oracle",
+                                "sample": f"the first {done} of {T} tokens (whole sequences) x{reps} "
+                                          f"through the float64 C oracle chain, {per * reps:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, local, name=None, with_e2e=True):
@@ -1058,6 +1281,8 @@ def main():
         return main_layer(args, rank, world, local)
     if inp_name in workloads.PREFILL_NORM_WORKLOADS:
         return main_prefill_norm(args, rank, world, local)
+    if inp_name in workloads.PREFILL_LAYER_WORKLOADS:
+        return main_prefill_layer(args, rank, world, local)
     if inp_name not in workloads.WORKLOADS:
         return main_neighbour(args, rank, world, local)
     if args.impl == "reference":

@@ -376,6 +376,11 @@ def gdn_prefill_variant_plan(shape: GdnShape, rule: str = "gated_delta", decay_p
     return path.value, launches.value
 
 
+def gdn_prefill_layer_workspace_bytes(shape: GdnShape) -> int:
+    """The workspace gdn_prefill_layer needs for ``shape`` (0 off the tensor-core shapes)."""
+    return int(load().gdn_prefill_layer_workspace_bytes(ctypes.byref(shape)))
+
+
 def gdn_prefill_variant_workspace_bytes(shape: GdnShape, rule: str = "gated_delta",
                                         decay_per_key: bool = False, beta_shared: bool = False) -> int:
     if rule not in RULES:

@@ -69,6 +69,23 @@ def test_prefill_norm_bytes():
     assert sum(b.values()) == bench.algorithmic_bytes(inp.prefill) + o + 128 * 2
 
 
+def test_prefill_layer_bytes():
+    """x, the conv's weight, bias and two states, a, b, the gate parameters, the states, the
+    norm's scale and gate, and y."""
+    inp = workloads.any_workload("varlen_bf16_prefill_layer")
+    b = bench.prefill_layer_io_bytes(inp)
+    T, C = inp.total_tokens, 2 * 16 * 128 + 16 * 128
+    assert b["x"] == T * C * 2 and b["y"] == b["gate"] == T * 16 * 128 * 2
+    assert b["conv_state_in"] == b["conv_state_out"] == 8 * 3 * C * 2
+    assert b["state_in"] == b["state_out"] == 8 * 16 * 128 * 128 * 4
+
+
+def test_reference_arm_prefill_layer_workload():
+    d = _reference_line("varlen_bf16_prefill_layer")
+    _check_line(d, "varlen_bf16_prefill_layer")
+    assert d["unit"] == "tokens/s" and f"of {workloads.any_workload('varlen_bf16_prefill_layer').total_tokens} tokens" in d["cpu_baseline"]["sample"]
+
+
 def test_neighbour_sample_is_bounded():
     inp = workloads.any_workload("bf16_conv_prefill_gqa")
     small, what = bench.neighbour_sample(inp)
