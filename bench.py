@@ -965,8 +965,8 @@ def main_prefill_layer(args, rank, world, local):
               "norm": {"eps": s.eps, "activation": s.activation},
               "l2": "flushed before every step (256 MiB write, untimed)",
               "parallelism": f"replicas: the full workload on each of {world} GPU(s), no collective",
-              "op": "layer prefill: causal conv of the mixed input (fused into the chunk prep), the "
-                    "gated delta-rule prefill, the gated RMS norm of o: gdn_prefill_layer"}
+              "op": "layer prefill: causal conv of the mixed input (a streaming pass), the gated "
+                    "delta-rule prefill, the gated RMS norm of o: gdn_prefill_layer"}
     if args.impl == "reference":
         if rank != 0:
             return
@@ -1006,11 +1006,15 @@ def main_prefill_layer(args, rank, world, local):
     ws = torch.empty(max(1, gdn.gdn_prefill_layer_workspace_bytes(shape)), dtype=torch.uint8, device=dev)
     act = "silu" if s.silu else "none"
 
-    def call(d):
+    def call(d, fuse=False):
         gdn_prefill_layer(d["x"], d["w"], d["bias"], d["conv_state"], d["a"], d["b"], d["A_log"],
                           d["dt_bias"], state0, cu, d["norm_scale"], d["gate"], h_qk=s.h_qk, h_v=s.h_v,
                           scale=inp.scale, conv_activation=act, norm_activation=s.activation, eps=s.eps,
-                          y=y, state_out=state_out, conv_state_out=cs_out, workspace=ws, stream=stream)
+                          fuse=fuse, y=y, state_out=state_out, conv_state_out=cs_out, workspace=ws,
+                          stream=stream)
+
+    def fused(d):
+        call(d, fuse=True)
 
     # The separate calls: the conv per sequence (its kernel has no packed form) into q, k,
     # v buffers, the prefill, then the norm.
@@ -1057,6 +1061,7 @@ def main_prefill_layer(args, rank, world, local):
     ms = timed(call, t)
     clocks = sampler.stop() if sampler else None
     ms_sep = timed(separate, t)
+    ms_fused = timed(fused, t)
 
     e2e = None
     if not args.no_e2e:
@@ -1085,7 +1090,7 @@ def main_prefill_layer(args, rank, world, local):
 
     pk, pk_kind = peaks()
     gbs = nbytes / (ms / 1e3) / 1e9
-    launches = 3 + (1 if inp.varlen and s.kernel > 1 else 0)
+    launches = 4 + (1 if inp.varlen and s.kernel > 1 else 0)
     line = {
         "metric": METRIC, "value": world * T / (ms / 1e3), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -1095,8 +1100,11 @@ def main_prefill_layer(args, rank, world, local):
                      "frac": gbs / pk["hbm_gbs"], "traffic": profiled_traffic(args.workload, "prefill"),
                      "peak_source": f"{pk_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"
                      if pk_kind == "measured" else "fallback 6.8 TB/s",
-                     "kernels": "gdn_chunk_prep (convolution form) + gdn_chunk_scan + conv_state_empty "
+                     "kernels": "conv_pass + gdn_chunk_prep + gdn_chunk_scan + conv_state_empty "
                                 "+ gated_rmsnorm_rows_kernel, one call"},
+        "conv_in_prep": {"ms_per_step": ms_fused, "launches": launches - 1,
+                         "kernels": "gdn_chunk_prep (convolution form) + gdn_chunk_scan + conv_state_empty "
+                                    "+ gated_rmsnorm_rows_kernel (fuse = 1)"},
         "separate_calls": {"ms_per_step": ms_sep,
                            "calls": f"gdn_causal_conv per sequence ({N}), q/k/v copies, gdn_prefill "
                                     "(prep, scan), gdn_gated_rmsnorm"},

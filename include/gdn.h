@@ -441,12 +441,14 @@ gdn_status gdn_decode_layer(const gdn_shape *shape, const gdn_layer_params *laye
  * gdn_prefill_layer -- the prefill of a whole gated delta-rule layer: gdn_causal_conv
  * (onnxruntime-ep-mlx ssm.rs `causal_conv_op`) on the layer's mixed input, gdn_prefill
  * (onnx-runtime-ep-cuda linear_attention.rs `linear_attention_core`, Steps 1-4) on its q,
- * k and v, then gdn_gated_rmsnorm (ssm.rs `gated_rms_norm_op`) on o, in that order.  The
- * convolution runs inside the chunked prefill's prep kernel, which convolves each chunk's
- * q, k and v channels straight into its operand tiles: v never reaches memory, and the
- * convolved q and k only as the workspace copy the state scan reads.  The norm then runs in
- * place on y.  Each intermediate is rounded to io_dtype as the separate calls would store
- * it; the results equal conv -> prefill -> norm up to the order of fp32 sums.
+ * k and v, then gdn_gated_rmsnorm (ssm.rs `gated_rms_norm_op`) on o, in that order, with
+ * packed sequences handled by the convolution as by the prefill.  fuse = 0 (the faster
+ * form on GB300): one streaming pass convolves every token of x into q, k and v in the
+ * workspace, then the chunked prefill reads them.  fuse = 1: the prefill's prep kernel
+ * convolves each chunk's q, k and v channels straight into its operand tiles, and v never
+ * reaches memory.  The norm then runs in place on y.  Each intermediate is rounded to
+ * io_dtype as the separate calls would store it, and the convolution sums in their order,
+ * so the results equal conv -> prefill -> norm.
  *   x            [tokens, C] (packed with cu_seqlens, or [B, T, C]), C = 2 h_qk d_k +
  *                h_v d_v, read as [q (h_qk x d_k) | k (h_qk x d_k) | v (h_v x d_v)].
  *   conv_weight  [C, 1, K] with K = layer->conv_kernel in 1..4; conv_bias [C] or NULL;
@@ -460,7 +462,8 @@ gdn_status gdn_decode_layer(const gdn_shape *shape, const gdn_layer_params *laye
  *                gdn_gated_rmsnorm; y [tokens, h_v, d_v], 16-byte aligned, not overlapping
  *                gate.
  *   workspace    at least gdn_prefill_layer_workspace_bytes(shape) bytes: gdn_prefill's
- *                plus the convolved q and k (2 x tokens x h_qk x 128 16-bit values).
+ *                plus the convolved q, k and v (tokens x (2 h_qk + h_v) x 128 16-bit values;
+ *                fuse = 1 needs only q and k).
  * Shape: io_dtype bf16 or f16 and d_k = d_v = 128 (GDN_ERR_UNSUPPORTED otherwise); x and
  * the conv states 16-byte aligned.  Every pointer is device memory owned by the caller.
  * Errors are gdn_prefill's and gdn_causal_conv's argument rules, checked before anything
@@ -471,7 +474,8 @@ gdn_status gdn_prefill_layer(const gdn_shape *shape, const gdn_layer_params *lay
                              void *conv_state_out, const void *a, const void *b, const float *A_log,
                              const float *dt_bias, const float *state_in, const int32_t *cu_seqlens,
                              float scale, const void *norm_scale, const void *gate, void *y,
-                             float *state_out, void *workspace, size_t workspace_bytes, void *stream);
+                             float *state_out, int32_t fuse, void *workspace, size_t workspace_bytes,
+                             void *stream);
 
 /* gdn_prefill_layer_workspace_bytes -- the workspace gdn_prefill_layer needs for `shape`
  * (0 off the tensor-core shapes); never fails. */

@@ -221,7 +221,8 @@ gdn_status gdn_prefill_norm(const gdn_shape *shape, const void *q, const void *k
 size_t gdn_prefill_layer_workspace_bytes(const gdn_shape *shape) {
     const size_t base = gdn_prefill_workspace_bytes(shape);
     if (base == 0) return 0;
-    return base + prefill_tc_conv_bytes(shape->seqlen * (int64_t)shape->batch, shape->h_qk);
+    const int64_t tokens = shape->seqlen * (int64_t)shape->batch;
+    return base + prefill_tc_conv_bytes(tokens, shape->h_qk) + prefill_tc_conv_v_bytes(tokens, shape->h_v);
 }
 
 gdn_status gdn_prefill_layer(const gdn_shape *shape, const gdn_layer_params *layer, const void *x,
@@ -229,7 +230,8 @@ gdn_status gdn_prefill_layer(const gdn_shape *shape, const gdn_layer_params *lay
                              void *conv_state_out, const void *a, const void *b, const float *A_log,
                              const float *dt_bias, const float *state_in, const int32_t *cu_seqlens,
                              float scale, const void *norm_scale, const void *gate, void *y,
-                             float *state_out, void *workspace, size_t workspace_bytes, void *stream) {
+                             float *state_out, int32_t fuse, void *workspace, size_t workspace_bytes,
+                             void *stream) {
     gdn_status st = check_shape(shape, cu_seqlens != nullptr);
     if (st != GDN_OK) return st;
     if (layer == nullptr) return fail(GDN_ERR_INVALID_ARG, "layer is NULL");
@@ -273,7 +275,7 @@ gdn_status gdn_prefill_layer(const gdn_shape *shape, const gdn_layer_params *lay
                             state_out, workspace, workspace_bytes, true, stream, nullptr, &norm);
     }
     const ConvPrologue conv{x, conv_weight, conv_bias, conv_state_in, conv_state_out, layer->conv_kernel,
-                            layer->conv_activation == GDN_ACT_SILU};
+                            layer->conv_activation == GDN_ACT_SILU, fuse != 0};
     // q, k and v are x's channels: x stands in for them in the argument checks.
     return prefill_impl(shape, x, x, x, a, b, A_log, dt_bias, state_in, cu_seqlens, scale, y,
                         state_out, workspace, workspace_bytes, true, stream, nullptr, &norm, &conv);
@@ -353,6 +355,7 @@ gdn_status gdn::prefill_impl(const gdn_shape *shape, const void *q, const void *
         p.conv_x = conv->x; p.conv_w = conv->weight; p.conv_b = conv->bias;
         p.conv_in = conv->state_in; p.conv_out = conv->state_out;
         p.conv_k = conv->kernel; p.conv_silu = conv->silu;
+        p.conv_fuse = conv->fuse;
     }
     const gdn_dtype io = (gdn_dtype)shape->io_dtype;
     cudaError_t e;
@@ -366,7 +369,9 @@ gdn_status gdn::prefill_impl(const gdn_shape *shape, const void *q, const void *
     // (The per-key path reads a's [64 tokens x 128] tiles by TMA: a must be 16-byte aligned.)
     const bool pk_room = !per_key || (workspace != nullptr && workspace_bytes >= records + pk_bytes &&
                                       aligned(a, 16));
-    const size_t conv_bytes = conv != nullptr ? prefill_tc_conv_bytes(tokens, shape->h_qk) : 0;
+    const size_t conv_bytes = conv == nullptr ? 0
+                              : prefill_tc_conv_bytes(tokens, shape->h_qk) +
+                                    (conv->fuse ? 0 : prefill_tc_conv_v_bytes(tokens, shape->h_v));
     if (conv != nullptr && !prefill_tc_supported(p, io, tokens))
         return fail(GDN_ERR_UNSUPPORTED, "the convolution prologue runs on the tensor-core prefill only");
     if (pk_room && prefill_tc_supported(p, io, tokens)) {

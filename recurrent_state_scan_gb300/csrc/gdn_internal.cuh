@@ -49,6 +49,7 @@ struct ScanParams {
     const void *conv_x, *conv_w, *conv_b, *conv_in;
     void *conv_out;
     int32_t conv_k, conv_silu;
+    int32_t conv_fuse;           // 1: in the chunk prep; 0: a streaming pass writes q, k, v first
 };
 
 // ------------------------------------------------------------------ I/O types
@@ -171,6 +172,9 @@ size_t prefill_tc_pk_bytes(int64_t total_tokens, int h_v);
 // With the convolution before the scan: the bytes of the convolved q and k arrays
 // ([tokens][h_qk][128] in a 16-bit type, each 1 KiB aligned) that follow the records.
 size_t prefill_tc_conv_bytes(int64_t total_tokens, int h_qk);
+// The convolved v array ([tokens][h_v][128], 16-bit, 1 KiB aligned) that the streaming
+// convolution pass adds after those.
+size_t prefill_tc_conv_v_bytes(int64_t total_tokens, int h_v);
 // workspace_bytes: the caller's workspace size; the time-parallel scan runs only when the
 // workspace also holds its buffers (and allow_overlap is set).
 cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_tokens,
@@ -195,6 +199,7 @@ struct ConvPrologue {
     const void *x, *weight, *bias, *state_in;
     void *state_out;
     int32_t kernel, silu;
+    bool fuse;   // in the chunk prep (else a streaming pass before the prefill)
 };
 
 struct NormEpilogue {

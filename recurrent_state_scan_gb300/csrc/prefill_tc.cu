@@ -122,7 +122,7 @@ struct TcParams {
     // convolved q and k to cq and ck ([tokens][h_qk][128]; the scan reads them through
     // tm_q and tm_k) and each sequence's last conv_k - 1 inputs to conv_out.
     const void *cx, *conv_w, *conv_b, *conv_in;
-    void *conv_out, *cq, *ck;
+    void *conv_out, *cq, *ck, *cv;   // cv: the convolved v, written by the streaming pass only
     int32_t conv_k, conv_silu, conv_C;
 };
 
@@ -487,6 +487,80 @@ __device__ __forceinline__ void conv_group(const TcParams &p, int64_t n, int64_t
         win[0] = win[1];
         win[1] = win[2];
         win[2] = win[3];
+    }
+}
+
+// The same convolution for the streaming pass (conv_pass), four tokens at a time: the
+// taps are loaded once per thread, and the seven window rows of a call all at once.
+struct ConvTaps {
+    uint4 w[4], b;
+};
+
+template <typename IO>
+__device__ __forceinline__ ConvTaps conv_taps(const TcParams &p, int c0) {
+    const int K = p.conv_k;
+    const IO *w = static_cast<const IO *>(p.conv_w);
+    ConvTaps t;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = j >= 4 - K ? IoType<IO>::ld(w + (size_t)(c0 + i) * K + (j - (4 - K))) : 0.f;
+        t.w[j] = pack8<IO>(v);
+    }
+    t.b = p.conv_b != nullptr ? *reinterpret_cast<const uint4 *>(static_cast<const IO *>(p.conv_b) + c0)
+                              : make_uint4(0, 0, 0, 0);
+    return t;
+}
+
+// x[pos][c0 ..], the conv state before ts, zeros at or past te.
+template <typename IO>
+__device__ __forceinline__ uint4 conv_row(const TcParams &p, int64_t n, int64_t ts, int64_t te, int64_t pos,
+                                          int c0) {
+    if (pos >= te) return make_uint4(0, 0, 0, 0);
+    if (pos >= ts) return *reinterpret_cast<const uint4 *>(static_cast<const IO *>(p.cx) + (size_t)pos * p.conv_C + c0);
+    if (p.conv_in == nullptr) return make_uint4(0, 0, 0, 0);
+    const int64_t r = (p.conv_k - 1) + (pos - ts);
+    if (r < 0) return make_uint4(0, 0, 0, 0);   // a slot the taps do not reach
+    return *reinterpret_cast<const uint4 *>(static_cast<const IO *>(p.conv_in) + ((size_t)n * (p.conv_k - 1) + r) * p.conv_C + c0);
+}
+
+// Tokens tok .. tok + 3: the 7 window rows are loaded at once, then the four outputs are
+// formed and handed to put(e, packed).
+template <typename IO, typename Put>
+__device__ __forceinline__ void conv4(const TcParams &p, const ConvTaps &tp, int64_t n, int64_t ts, int64_t te,
+                                      int64_t tok, int c0, Put &&put) {
+    uint4 win[7];
+#pragma unroll
+    for (int j = 0; j < 7; ++j) win[j] = conv_row<IO>(p, n, ts, te, tok - 3 + j, c0);
+    auto word = [](const uint4 &u, int k) { return k == 0 ? u.x : k == 1 ? u.y : k == 2 ? u.z : u.w; };
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        if (tok + e >= te) {
+            put(e, make_uint4(0, 0, 0, 0));
+            continue;
+        }
+        float out[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float2 acc;
+            {
+                const float2 wv = Pack<IO>::unpack(word(tp.w[0], k)), xv = Pack<IO>::unpack(word(win[e], k));
+                acc = make_float2(wv.x * xv.x, wv.y * xv.y);
+            }
+#pragma unroll
+            for (int j = 1; j < 4; ++j) {
+                const float2 wv = Pack<IO>::unpack(word(tp.w[j], k)), xv = Pack<IO>::unpack(word(win[e + j], k));
+                acc.x = fmaf(wv.x, xv.x, acc.x);
+                acc.y = fmaf(wv.y, xv.y, acc.y);
+            }
+            const float2 bv = Pack<IO>::unpack(word(tp.b, k));
+            acc.x += bv.x;
+            acc.y += bv.y;
+            out[2 * k] = p.conv_silu ? __fdividef(acc.x, 1.0f + __expf(-acc.x)) : acc.x;
+            out[2 * k + 1] = p.conv_silu ? __fdividef(acc.y, 1.0f + __expf(-acc.y)) : acc.y;
+        }
+        put(e, pack8<IO>(out));
     }
 }
 
@@ -2371,6 +2445,66 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
     }
 }
 
+// ===================================================================== convolution pass
+// The streaming form of the convolution before the scan: every (token, 8-channel group) of
+// x once, written to q, k and v ([tokens][heads][128]) for the plain prep, and each
+// sequence's present conv state by the thread that holds its last token.  Thread: a group
+// of 32 along the channels and a run of 32 tokens (8 runs per CTA), the taps loaded once
+// and the window rows four tokens at a time; four tokens that cross a sequence boundary
+// go one by one.
+constexpr int kConvRun = 32;
+template <typename IO>
+__global__ void __launch_bounds__(256, 2) conv_pass(const __grid_constant__ TcParams p) {
+    const int g = blockIdx.x * 32 + (threadIdx.x & 31);
+    const int c0 = 8 * g;
+    if (c0 >= p.conv_C) return;
+    const int64_t T = p.cu_seqlens ? p.seqlen : p.seqlen * p.num_seqs;
+    const int64_t r0 = ((int64_t)blockIdx.y * 8 + (threadIdx.x >> 5)) * kConvRun;
+    if (r0 >= T) return;
+    const int hk = p.h_qk * kDK;
+    IO *dst;
+    int64_t stride;
+    if (c0 < hk) { dst = static_cast<IO *>(p.cq) + c0; stride = hk; }
+    else if (c0 < 2 * hk) { dst = static_cast<IO *>(p.ck) + (c0 - hk); stride = hk; }
+    else { dst = static_cast<IO *>(p.cv) + (c0 - 2 * hk); stride = (int64_t)p.h_v * kDK; }
+    // The sequence of token t: batched, t / seqlen; packed, the last n with cu[n] <= t.
+    auto seq_of = [&](int64_t t, int64_t &n, int64_t &ts, int64_t &te) {
+        if (p.cu_seqlens == nullptr) {
+            n = t / p.seqlen;
+        } else {
+            int64_t lo = 0, hi = p.num_seqs - 1;
+            while (lo < hi) {
+                const int64_t mid = (lo + hi + 1) >> 1;
+                if (p.cu_seqlens[mid] <= t) lo = mid; else hi = mid - 1;
+            }
+            n = lo;
+        }
+        return seq_range(p.cu_seqlens, p.seqlen, p.num_seqs, p.status, n, ts, te);
+    };
+    const ConvTaps taps = conv_taps<IO>(p, c0);
+    int64_t n = -1, ts = 0, te = 0;
+#pragma unroll 1
+    for (int64_t t0 = r0; t0 < r0 + kConvRun && t0 < T; t0 += 4) {
+        if (t0 >= te && !seq_of(t0, n, ts, te)) return;
+        const int64_t tl = t0 + 3 < T ? t0 + 3 : T - 1;   // the last token of these four
+        if (tl < te) {
+            conv4<IO>(p, taps, n, ts, te, t0, c0, [&](int e, const uint4 &u) {
+                if (t0 + e < te) *reinterpret_cast<uint4 *>(dst + (size_t)(t0 + e) * stride) = u;
+            });
+            if (te - 1 >= t0 && te - 1 <= t0 + 3) conv_state_group<IO>(p, n, ts, te, c0);
+            continue;
+        }
+        for (int e = 0; e < 4 && t0 + e < T; ++e) {
+            const int64_t t = t0 + e;
+            if (t >= te && !seq_of(t, n, ts, te)) return;
+            conv4<IO>(p, taps, n, ts, te, t, c0, [&](int e2, const uint4 &u) {
+                if (e2 == 0) *reinterpret_cast<uint4 *>(dst + (size_t)t * stride) = u;
+            });
+            if (t == te - 1) conv_state_group<IO>(p, n, ts, te, c0);
+        }
+    }
+}
+
 // ===================================================================== conv state, empty sequences
 // The present conv state of a packed sequence with no tokens is its past state (zeros
 // without one); the prep writes it for every other sequence.  One CTA per sequence.
@@ -2974,6 +3108,10 @@ bool encode_map_3d(CUtensorMap *m, const void *base, gdn_dtype io, const uint64_
     return r == CUDA_SUCCESS;
 }
 
+size_t prefill_tc_conv_v_bytes(int64_t total_tokens, int h_v) {
+    return ((size_t)total_tokens * h_v * kDK * 2 + 1023) & ~(size_t)1023;
+}
+
 size_t prefill_tc_conv_bytes(int64_t total_tokens, int h_qk) {
     const size_t each = ((size_t)total_tokens * h_qk * kDK * 2 + 1023) & ~(size_t)1023;
     return 2 * each;
@@ -3060,8 +3198,10 @@ cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_t
             return cudaErrorInvalidValue;
         records += 2 * each;
     }
+    bool conv_pass_first = false;
     if (p.conv_x != nullptr) {
-        // The convolved q and k follow the records; the caller has checked the room.
+        // The convolved q and k (and, for the streaming pass, v) follow the records; the
+        // caller has checked the room.
         const size_t each = prefill_tc_conv_bytes(total_tokens, p.h_qk) / 2;
         uint8_t *base = static_cast<uint8_t *>(workspace) + records;
         tp.cx = p.conv_x;
@@ -3078,20 +3218,43 @@ cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_t
             !make_map(&tp.tm_k, tp.ck, io, p.h_qk, total_tokens))
             return cudaErrorInvalidValue;
         records += 2 * each;
+        if (!p.conv_fuse) {
+            // The streaming pass writes v too; the plain prep then reads q, k and v by TMA.
+            tp.cv = static_cast<uint8_t *>(workspace) + records;
+            if (!make_map(&tp.tm_v, tp.cv, io, p.h_v, total_tokens)) return cudaErrorInvalidValue;
+            records += prefill_tc_conv_v_bytes(total_tokens, p.h_v);
+            conv_pass_first = true;
+        }
     }
+    if (conv_pass_first) {
+        const dim3 grid((unsigned)((tp.conv_C / 8 + 31) / 32),
+                        (unsigned)((total_tokens + 8 * kConvRun - 1) / (8 * kConvRun)));
+        if (io == GDN_BF16) conv_pass<__nv_bfloat16><<<grid, 256, 0, stream>>>(tp);
+        else conv_pass<__half><<<grid, 256, 0, stream>>>(tp);
+        cudaError_t ce = cudaGetLastError();
+        if (ce != cudaSuccess) return ce;
+    }
+    // The launches' parameters, taken once every field is set (the time-parallel branch
+    // adds the R map first): the prep's convolution form only when the convolution is
+    // fused into it.
+    auto launch_view = [&]() {
+        TcParams t = tp;
+        if (conv_pass_first) t.cx = nullptr;
+        return t;
+    };
     const int tps = allow_overlap && p.norm_gate == nullptr
                         ? tp_segments(varlen, p.seqlen, p.num_seqs, p.h_v) : 1;
     if (tps > 1 && workspace_bytes >= records + tp_layout(p.seqlen, p.num_seqs, p.h_v, tps).total) {
         uint8_t *extra = static_cast<uint8_t *>(workspace) + records;
         if (!make_map(&tp.tm_r, extra + tp_layout(p.seqlen, p.num_seqs, p.h_v, tps).r, io, p.h_v, total_tokens))
             return cudaErrorInvalidValue;
-        cudaError_t e = io == GDN_BF16 ? launch_tp<__nv_bfloat16>(tp, n_slots, tps, extra, stream)
-                                       : launch_tp<__half>(tp, n_slots, tps, extra, stream);
+        cudaError_t e = io == GDN_BF16 ? launch_tp<__nv_bfloat16>(launch_view(), n_slots, tps, extra, stream)
+                                       : launch_tp<__half>(launch_view(), n_slots, tps, extra, stream);
         return e;   // batched: no sequence is empty
     }
     const int nseg = allow_overlap ? prefill_tc_segments(varlen, p.seqlen, p.num_seqs, p.h_v) : 1;
-    cudaError_t e = io == GDN_BF16 ? launch_typed<__nv_bfloat16>(tp, n_slots, nseg, stream)
-                                   : launch_typed<__half>(tp, n_slots, nseg, stream);
+    cudaError_t e = io == GDN_BF16 ? launch_typed<__nv_bfloat16>(launch_view(), n_slots, nseg, stream)
+                                   : launch_typed<__half>(launch_view(), n_slots, nseg, stream);
     if (e == cudaSuccess && tp.cx != nullptr && varlen && p.conv_k > 1) {
         if (io == GDN_BF16) conv_state_empty<__nv_bfloat16><<<(unsigned)p.num_seqs, 256, 0, stream>>>(tp);
         else conv_state_empty<__half><<<(unsigned)p.num_seqs, 256, 0, stream>>>(tp);

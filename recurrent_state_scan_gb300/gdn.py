@@ -140,7 +140,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                      P, ctypes.c_float, P, P, P, P]
     lib.gdn_prefill_layer.restype = ctypes.c_int
     lib.gdn_prefill_layer.argtypes = [S, ctypes.POINTER(GdnLayerParams), P, P, P, P, P, P, P, P, P, P, P,
-                                      ctypes.c_float, P, P, P, P, P, ctypes.c_size_t, P]
+                                      ctypes.c_float, P, P, P, P, ctypes.c_int32, P, ctypes.c_size_t, P]
     lib.gdn_prefill_layer_workspace_bytes.restype = ctypes.c_size_t
     lib.gdn_prefill_layer_workspace_bytes.argtypes = [S]
     _lib = lib
@@ -740,7 +740,8 @@ def gdn_decode_layer(x, conv_weight, conv_bias, conv_state_in, conv_state_out, a
 def gdn_prefill_layer(x, conv_weight, conv_bias, conv_state_in, a, b, A_log, dt_bias, state_in,
                       cu_seqlens, norm_scale, gate, *, h_qk: int, h_v: int, scale: float = 0.0,
                       conv_activation: str = "silu", norm_activation: str = "silu", eps: float = 1e-5,
-                      y=None, state_out=None, conv_state_out=None, workspace=None, stream=None):
+                      fuse: bool = False, y=None, state_out=None, conv_state_out=None, workspace=None,
+                      stream=None):
     """The prefill of a layer: causal conv over x (channels [q | k | v], C = 2 h_qk 128 +
     h_v 128; [B, T, C], or [1, total, C] packed with cu_seqlens), the chunked prefill on its
     q, k, v, then the gated RMS norm of o.  conv_weight [C, 1, K] (K <= 4); conv_bias [C] or
@@ -791,5 +792,5 @@ def gdn_prefill_layer(x, conv_weight, conv_bias, conv_state_in, a, b, A_log, dt_
                                  _ptr(conv_bias), _ptr(conv_state_in), _ptr(conv_state_out), _ptr(a),
                                  _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(state_in), _ptr(cu_seqlens),
                                  float(scale), _ptr(norm_scale), _ptr(gate), _ptr(y), _ptr(state_out),
-                                 _ptr(workspace), ws_bytes, _stream(stream)))
+                                 int(bool(fuse)), _ptr(workspace), ws_bytes, _stream(stream)))
     return y, state_out, conv_state_out

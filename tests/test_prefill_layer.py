@@ -1,6 +1,7 @@
 """GPU parity of gdn_prefill_layer -- the causal conv (onnxruntime-ep-mlx ssm.rs
-`causal_conv_op`) fused into the chunked prefill's prep, the prefill (the CUDA page's
-`linear_attention_core` Steps 1-4) and the gated RMS norm (ssm.rs `gated_rms_norm_op`).
+`causal_conv_op`), as a streaming pass before the prefill (fuse = 0) or inside the chunked
+prefill's prep (fuse = 1), the prefill (the CUDA page's `linear_attention_core` Steps 1-4)
+and the gated RMS norm (ssm.rs `gated_rms_norm_op`).  Both forms are checked.
 
 References:
   * the float64 oracle chain: the oracle's convolution per sequence, its output rounded
@@ -63,7 +64,7 @@ def _oracle(inp, with_state=True):
     return y.reshape(-1, s.h_v, 128), state, cs
 
 
-def _fused(inp, with_state=True, bias=True):
+def _fused(inp, with_state=True, bias=True, fuse=False):
     from recurrent_state_scan_gb300 import gdn_last_device_status, gdn_prefill_layer
     s = inp.spec
     d = lambda t: None if t is None else t.cuda()
@@ -73,15 +74,15 @@ def _fused(inp, with_state=True, bias=True):
                                   d(inp.A_log), d(inp.dt_bias), d(inp.state_in), cu, d(inp.norm_scale),
                                   d(inp.gate), h_qk=s.h_qk, h_v=s.h_v, scale=inp.scale,
                                   conv_activation="silu" if s.silu else "none",
-                                  norm_activation=s.activation, eps=s.eps)
+                                  norm_activation=s.activation, eps=s.eps, fuse=fuse)
     torch.cuda.synchronize()
     assert gdn_last_device_status() == 0
     return y, st, cs
 
 
-def _against_oracle(inp, with_state=True):
+def _against_oracle(inp, with_state=True, fuse=False):
     s = inp.spec
-    y, st, cs = _fused(inp, with_state, bias=inp.bias is not None)
+    y, st, cs = _fused(inp, with_state, bias=inp.bias is not None, fuse=fuse)
     y_ref, s_ref, cs_ref = _oracle(inp, with_state)
     ey = rel_err(y.float().cpu().numpy().reshape(-1, s.h_v, 128), y_ref)
     es = rel_err(st.cpu().numpy(), s_ref)
@@ -96,26 +97,29 @@ def _spec(**kw):
     return workloads.PrefillLayerSpec(**base)
 
 
-def test_batched_gqa_ragged_against_the_oracle_chain():
+@pytest.mark.parametrize("fuse", [False, True])
+def test_batched_gqa_ragged_against_the_oracle_chain(fuse):
     """Two 300-token sequences (a ragged last chunk), GQA 2 -> 4 heads, a conv bias and
     state, an initial state."""
-    _against_oracle(workloads.draw_prefill_layer(_spec(batch=2, seqlen=300)))
+    _against_oracle(workloads.draw_prefill_layer(_spec(batch=2, seqlen=300)), fuse=fuse)
 
 
-def test_packed_short_and_empty_sequences_against_the_oracle_chain():
+@pytest.mark.parametrize("fuse", [False, True])
+def test_packed_short_and_empty_sequences_against_the_oracle_chain(fuse):
     """Packed sequences of 1, 2, 0, 129, 64 and 250 tokens: the first two are shorter than
     the conv window (their present state mixes the past state and their inputs), one is
     empty (its state passes through), and chunk tails hold the next sequence's rows."""
     _against_oracle(workloads.draw_prefill_layer(_spec(io="f16", lengths=(1, 2, 0, 129, 64, 250),
-                                                       h_qk=1, h_v=2, seed=702)))
+                                                       h_qk=1, h_v=2, seed=702)), fuse=fuse)
 
 
+@pytest.mark.parametrize("fuse", [False, True])
 @pytest.mark.parametrize("K", [1, 2, 3])
-def test_fewer_taps_no_bias_no_state_no_activation(K):
+def test_fewer_taps_no_bias_no_state_no_activation(K, fuse):
     # Without silu the convolved keys are twice as large: x_std 0.12 keeps |k|^2 below 1.
     inp = workloads.draw_prefill_layer(_spec(batch=1, seqlen=200, kernel=K, bias=False, silu=False,
                                              x_std=0.12, h_qk=1, h_v=2, seed=703 + K))
-    _against_oracle(inp, with_state=False)
+    _against_oracle(inp, with_state=False, fuse=fuse)
 
 
 def test_time_parallel_shape_against_the_oracle_chain():
@@ -127,14 +131,15 @@ def test_time_parallel_shape_against_the_oracle_chain():
     _against_oracle(inp)
 
 
+@pytest.mark.parametrize("fuse", [False, True])
 @pytest.mark.parametrize("io", ["bf16", "f16"])
-def test_equals_the_separate_calls(io):
+def test_equals_the_separate_calls(io, fuse):
     """Batched: gdn_causal_conv -> gdn_prefill -> gdn_gated_rmsnorm on the same inputs."""
     from recurrent_state_scan_gb300 import (gdn_causal_conv, gdn_gated_rmsnorm, gdn_last_device_status,
                                             gdn_prefill)
     inp = workloads.draw_prefill_layer(_spec(io=io, batch=3, seqlen=333, seed=708))
     s = inp.spec
-    y, st, cs = _fused(inp)
+    y, st, cs = _fused(inp, fuse=fuse)
     x = inp.x.cuda()
     yc, cs2 = gdn_causal_conv(x, inp.w.cuda(), inp.bias.cuda(), inp.conv_state.cuda(), activation="silu")
     B, T = x.shape[0], x.shape[1]
@@ -153,8 +158,9 @@ def test_equals_the_separate_calls(io):
     assert not (np.abs(a_ - b_) > bound).any()
 
 
-def test_full_size_layer_workload_against_the_oracle_chain():
-    _against_oracle(workloads.any_workload("varlen_bf16_prefill_layer"))
+@pytest.mark.parametrize("fuse", [False, True])
+def test_full_size_layer_workload_against_the_oracle_chain(fuse):
+    _against_oracle(workloads.any_workload("varlen_bf16_prefill_layer"), fuse=fuse)
 
 
 def test_bad_arguments_are_rejected():
