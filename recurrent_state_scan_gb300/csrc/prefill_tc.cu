@@ -493,7 +493,7 @@ __device__ __forceinline__ void conv_group(const TcParams &p, int64_t n, int64_t
 // The same convolution for the streaming pass (conv_pass), four tokens at a time: the
 // taps are loaded once per thread, and the seven window rows of a call all at once.
 struct ConvTaps {
-    uint4 w[4], b;
+    float w[4][8], b[8];   // slot-aligned taps and the bias, widened once
 };
 
 template <typename IO>
@@ -502,14 +502,13 @@ __device__ __forceinline__ ConvTaps conv_taps(const TcParams &p, int c0) {
     const IO *w = static_cast<const IO *>(p.conv_w);
     ConvTaps t;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        float v[8];
+    for (int j = 0; j < 4; ++j)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = j >= 4 - K ? IoType<IO>::ld(w + (size_t)(c0 + i) * K + (j - (4 - K))) : 0.f;
-        t.w[j] = pack8<IO>(v);
-    }
-    t.b = p.conv_b != nullptr ? *reinterpret_cast<const uint4 *>(static_cast<const IO *>(p.conv_b) + c0)
-                              : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < 8; ++i)
+            t.w[j][i] = j >= 4 - K ? IoType<IO>::ld(w + (size_t)(c0 + i) * K + (j - (4 - K))) : 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        t.b[i] = p.conv_b != nullptr ? IoType<IO>::ld(static_cast<const IO *>(p.conv_b) + c0 + i) : 0.f;
     return t;
 }
 
@@ -525,15 +524,17 @@ __device__ __forceinline__ uint4 conv_row(const TcParams &p, int64_t n, int64_t 
     return *reinterpret_cast<const uint4 *>(static_cast<const IO *>(p.conv_in) + ((size_t)n * (p.conv_k - 1) + r) * p.conv_C + c0);
 }
 
-// Tokens tok .. tok + 3: the 7 window rows are loaded at once, then the four outputs are
-// formed and handed to put(e, packed).
+// Tokens tok .. tok + 3: the 7 window rows are loaded at once and widened once, then the
+// four outputs are formed (oldest tap first, then the bias) and handed to put(e, packed).
 template <typename IO, typename Put>
 __device__ __forceinline__ void conv4(const TcParams &p, const ConvTaps &tp, int64_t n, int64_t ts, int64_t te,
                                       int64_t tok, int c0, Put &&put) {
-    uint4 win[7];
+    uint4 raw[7];
 #pragma unroll
-    for (int j = 0; j < 7; ++j) win[j] = conv_row<IO>(p, n, ts, te, tok - 3 + j, c0);
-    auto word = [](const uint4 &u, int k) { return k == 0 ? u.x : k == 1 ? u.y : k == 2 ? u.z : u.w; };
+    for (int j = 0; j < 7; ++j) raw[j] = conv_row<IO>(p, n, ts, te, tok - 3 + j, c0);
+    float win[7][8];
+#pragma unroll
+    for (int j = 0; j < 7; ++j) unpack8<IO>(raw[j], win[j]);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         if (tok + e >= te) {
@@ -542,23 +543,12 @@ __device__ __forceinline__ void conv4(const TcParams &p, const ConvTaps &tp, int
         }
         float out[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            float2 acc;
-            {
-                const float2 wv = Pack<IO>::unpack(word(tp.w[0], k)), xv = Pack<IO>::unpack(word(win[e], k));
-                acc = make_float2(wv.x * xv.x, wv.y * xv.y);
-            }
+        for (int i = 0; i < 8; ++i) {
+            float acc = tp.w[0][i] * win[e][i];
 #pragma unroll
-            for (int j = 1; j < 4; ++j) {
-                const float2 wv = Pack<IO>::unpack(word(tp.w[j], k)), xv = Pack<IO>::unpack(word(win[e + j], k));
-                acc.x = fmaf(wv.x, xv.x, acc.x);
-                acc.y = fmaf(wv.y, xv.y, acc.y);
-            }
-            const float2 bv = Pack<IO>::unpack(word(tp.b, k));
-            acc.x += bv.x;
-            acc.y += bv.y;
-            out[2 * k] = p.conv_silu ? __fdividef(acc.x, 1.0f + __expf(-acc.x)) : acc.x;
-            out[2 * k + 1] = p.conv_silu ? __fdividef(acc.y, 1.0f + __expf(-acc.y)) : acc.y;
+            for (int j = 1; j < 4; ++j) acc = fmaf(tp.w[j][i], win[e + j][i], acc);
+            acc += tp.b[i];
+            out[i] = p.conv_silu ? __fdividef(acc, 1.0f + __expf(-acc)) : acc;
         }
         put(e, pack8<IO>(out));
     }
