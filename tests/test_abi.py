@@ -219,3 +219,60 @@ def test_noalloc_scratch_size_matches_the_header():
     m = re.search(r"#define GDN_PREFILL_NOALLOC_SCRATCH_BYTES \((\d+)u \* 1024u \* 1024u\)",
                   open(os.path.join(ROOT, "include", "gdn.h")).read())
     assert m and int(m.group(1)) * 1024 * 1024 == gdn.PREFILL_NOALLOC_SCRATCH_BYTES
+
+
+def test_variant_and_layer_workspace_sizes():
+    """gdn_prefill_variant_workspace_bytes adds, for a per-key decay with a decaying rule,
+    the scaled Q and K (tokens x h_v x 128 16-bit values each, 1 KiB aligned);
+    gdn_prefill_layer_workspace_bytes adds the convolved q, k (h_qk heads) and v (h_v
+    heads) the same way.  Both are 0 off the tensor-core shapes."""
+    up = lambda x: (x + 1023) // 1024 * 1024
+    sh = gdn.make_shape(gdn.GDN_BF16, 2, 300, 2, 2, 4, 128, 128)
+    base = gdn.gdn_prefill_workspace_bytes(sh)
+    T = 600
+    assert base > 0
+    assert gdn.gdn_prefill_variant_workspace_bytes(sh) == base
+    assert gdn.gdn_prefill_variant_workspace_bytes(sh, "delta", decay_per_key=True) == base
+    assert gdn.gdn_prefill_variant_workspace_bytes(sh, "gated_delta", decay_per_key=True) == \
+        base + 2 * up(T * 4 * 128 * 2)
+    assert gdn.gdn_prefill_variant_workspace_bytes(sh, "gated", decay_per_key=True) == \
+        base + 2 * up(T * 4 * 128 * 2)
+    assert gdn.gdn_prefill_layer_workspace_bytes(sh) == \
+        base + 2 * up(T * 2 * 128 * 2) + up(T * 4 * 128 * 2)
+    off = gdn.make_shape(gdn.GDN_F32, 2, 300, 2, 2, 4, 128, 128)
+    assert gdn.gdn_prefill_layer_workspace_bytes(off) == 0
+    assert gdn.gdn_prefill_variant_workspace_bytes(off, "gated_delta", decay_per_key=True) == 0
+
+
+def test_variant_plan_matches_the_prefill_plan():
+    """Every rule, the shared beta and the per-key decay take gdn_prefill's path."""
+    for sh in (gdn.make_shape(gdn.GDN_BF16, 1, 4096, 1, 16, 16, 128, 128),
+               gdn.make_shape(gdn.GDN_F16, 1, 700, 3, 2, 4, 128, 128),
+               gdn.make_shape(gdn.GDN_F32, 2, 64, 2, 2, 2, 32, 32)):
+        want = gdn.gdn_prefill_plan(sh)
+        for rule in gdn.RULES:
+            for pk in (False, True):
+                assert gdn.gdn_prefill_variant_plan(sh, rule, pk, False) == want
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_prefill_variant_plan(gdn.make_shape(gdn.GDN_BF16, 1, 64, 1, 1, 1, 128, 128), "nope")
+
+
+def test_layer_prefill_rejects_bad_arguments_before_launch():
+    lib = gdn.load()
+    p = ctypes.c_void_p(0x1000)
+    sh = gdn.make_shape(gdn.GDN_BF16, 1, 64, 1, 1, 1, 128, 128)
+
+    def call(shape=sh, K=4, act=1, x=p, cs_in=p, cs_out=ctypes.c_void_p(0x80000)):
+        layer = gdn.GdnLayerParams(K, act, gdn.ACTIVATIONS["silu"], 1e-6)
+        return lib.gdn_prefill_layer(ctypes.byref(shape), ctypes.byref(layer), x, p, None, cs_in, cs_out,
+                                     p, p, p, p, None, None, 0.0, p, p, ctypes.c_void_p(0x90000), p, 0,
+                                     None, 0, None)
+
+    assert call(K=5) == gdn.GDN_ERR_INVALID_ARG                     # more than 4 taps
+    assert call(K=0) == gdn.GDN_ERR_INVALID_ARG
+    assert call(act=2) == gdn.GDN_ERR_INVALID_ARG                   # sigmoid is not a conv activation
+    assert call(x=ctypes.c_void_p(0x1008)) == gdn.GDN_ERR_INVALID_ARG   # x off 16 bytes
+    assert call(cs_out=p) == gdn.GDN_ERR_INVALID_ARG                # the state updated in place
+    assert call(cs_out=None) == gdn.GDN_ERR_INVALID_ARG
+    f32 = gdn.make_shape(gdn.GDN_F32, 1, 64, 1, 1, 1, 128, 128)
+    assert call(shape=f32) == gdn.GDN_ERR_UNSUPPORTED
