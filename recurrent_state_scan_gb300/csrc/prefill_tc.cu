@@ -512,35 +512,16 @@ __device__ __forceinline__ ConvTaps conv_taps(const TcParams &p, int c0) {
     return t;
 }
 
-// x[pos][c0 ..], the conv state before ts, zeros at or past te.
-template <typename IO>
-__device__ __forceinline__ uint4 conv_row(const TcParams &p, int64_t n, int64_t ts, int64_t te, int64_t pos,
-                                          int c0) {
-    if (pos >= te) return make_uint4(0, 0, 0, 0);
-    if (pos >= ts) return *reinterpret_cast<const uint4 *>(static_cast<const IO *>(p.cx) + (size_t)pos * p.conv_C + c0);
-    if (p.conv_in == nullptr) return make_uint4(0, 0, 0, 0);
-    const int64_t r = (p.conv_k - 1) + (pos - ts);
-    if (r < 0) return make_uint4(0, 0, 0, 0);   // a slot the taps do not reach
-    return *reinterpret_cast<const uint4 *>(static_cast<const IO *>(p.conv_in) + ((size_t)n * (p.conv_k - 1) + r) * p.conv_C + c0);
-}
-
-// Tokens tok .. tok + 3: the 7 window rows are loaded at once and widened once, then the
-// four outputs are formed (oldest tap first, then the bias) and handed to put(e, packed).
-template <typename IO, typename Put>
-__device__ __forceinline__ void conv4(const TcParams &p, const ConvTaps &tp, int64_t n, int64_t ts, int64_t te,
-                                      int64_t tok, int c0, Put &&put) {
-    uint4 raw[7];
-#pragma unroll
-    for (int j = 0; j < 7; ++j) raw[j] = conv_row<IO>(p, n, ts, te, tok - 3 + j, c0);
+// Tokens tok .. tok + 3 from the seven window rows row(tok - 3) .. row(tok + 3), widened
+// once: each output is formed oldest tap first, then the bias, rounded once, and handed
+// to put(e, packed).
+template <typename IO, typename Row, typename Put>
+__device__ __forceinline__ void conv4(const TcParams &p, const ConvTaps &tp, int64_t tok, Row &&row, Put &&put) {
     float win[7][8];
 #pragma unroll
-    for (int j = 0; j < 7; ++j) unpack8<IO>(raw[j], win[j]);
+    for (int j = 0; j < 7; ++j) unpack8<IO>(row(tok - 3 + j), win[j]);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        if (tok + e >= te) {
-            put(e, make_uint4(0, 0, 0, 0));
-            continue;
-        }
         float out[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -552,6 +533,24 @@ __device__ __forceinline__ void conv4(const TcParams &p, const ConvTaps &tp, int
         }
         put(e, pack8<IO>(out));
     }
+}
+
+// One token tok from the four rows row(tok - 3) .. row(tok), in the same order.
+template <typename IO, typename Row>
+__device__ __forceinline__ uint4 conv1(const TcParams &p, const ConvTaps &tp, int64_t tok, Row &&row) {
+    float win[4][8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) unpack8<IO>(row(tok - 3 + j), win[j]);
+    float out[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float acc = tp.w[0][i] * win[0][i];
+#pragma unroll
+        for (int j = 1; j < 4; ++j) acc = fmaf(tp.w[j][i], win[j][i], acc);
+        acc += tp.b[i];
+        out[i] = p.conv_silu ? __fdividef(acc, 1.0f + __expf(-acc)) : acc;
+    }
+    return pack8<IO>(out);
 }
 
 // The present conv state of sequence n for channels c0 .. c0 + 7: its last K - 1 inputs
@@ -2438,25 +2437,80 @@ __global__ void __launch_bounds__(kScanAllThreads, 1) gdn_chunk_scan(const __gri
 // ===================================================================== convolution pass
 // The streaming form of the convolution before the scan: every (token, 8-channel group) of
 // x once, written to q, k and v ([tokens][heads][128]) for the plain prep, and each
-// sequence's present conv state by the thread that holds its last token.  Thread: a group
-// of 32 along the channels and a run of 32 tokens (8 runs per CTA), the taps loaded once
-// and the window rows four tokens at a time; four tokens that cross a sequence boundary
-// go one by one.
-constexpr int kConvRun = 32;
+// sequence's present conv state by the thread that holds its last token.
+//  - A CTA owns 256 channels over kPassChunk tokens. x comes in by TMA, a stage at a
+//    time: 32 tokens and the 3 rows before them in one 256 x 35 box (rows outside x read
+//    as zero), kPassDepth stages in flight. Warp 0 issues; each warp computes from a
+//    stage once its `full` barrier completes, then releases it on `empty`.
+//  - Thread (cg, tg) forms 8 channels x 4 tokens from seven shared-memory rows and stores
+//    each token as one 16-byte store, so a warp writes whole 512-byte rows.
+//  - Window rows before a sequence's first token come from its past conv state (zeros
+//    without one). Four tokens that reach back past a sequence start, or run into the
+//    next sequence, are formed one by one.
+//  - Every wait is bounded. A CTA that gives up lets the copies it issued land before it
+//    exits.
+constexpr int kPassWidth = 256;                  // channels of a CTA
+constexpr int kPassTokens = 32;                  // tokens of a stage
+constexpr int kPassRows = kPassTokens + 3;       // rows of a stage
+constexpr int kPassRowB = kPassWidth * 2;        // bytes of a row
+constexpr int kPassBufB = kPassRows * kPassRowB;
+constexpr int kPassDepth = 4;                    // stages in flight
+constexpr int kPassChunk = 256;                  // tokens of a CTA
+constexpr int kPassSmem = kPassDepth * kPassBufB + 128;
 template <typename IO>
-__global__ void __launch_bounds__(256, 2) conv_pass(const __grid_constant__ TcParams p) {
-    const int g = blockIdx.x * 32 + (threadIdx.x & 31);
-    const int c0 = 8 * g;
-    if (c0 >= p.conv_C) return;
+__global__ void __launch_bounds__(256, 2) conv_pass(const __grid_constant__ TcParams p,
+                                                     const __grid_constant__ CUtensorMap tm_x) {
+    extern __shared__ unsigned char pass_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(pass_raw) + 127) & ~static_cast<uintptr_t>(127));
+    __shared__ uint64_t full[kPassDepth], empty[kPassDepth];
+    __shared__ int32_t abort_flag;
+    volatile int32_t *abort = &abort_flag;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t T = p.cu_seqlens ? p.seqlen : p.seqlen * p.num_seqs;
-    const int64_t r0 = ((int64_t)blockIdx.y * 8 + (threadIdx.x >> 5)) * kConvRun;
-    if (r0 >= T) return;
+    const int cbase = blockIdx.x * kPassWidth;
+    const int64_t t_begin = (int64_t)blockIdx.y * kPassChunk;
+    if (t_begin >= T) return;   // the whole CTA, before any barrier
+    const int64_t t_end = t_begin + kPassChunk < T ? t_begin + kPassChunk : T;
+    const int nstage = (int)((t_end - t_begin + kPassTokens - 1) / kPassTokens);
+    const long long budget = p.wait_budget > 0 ? p.wait_budget : kWaitBudget;
+    if (tid == 0) {
+#pragma unroll
+        for (int i = 0; i < kPassDepth; ++i) {
+            mbar_init(&full[i], 1);    // the issuing lane, plus the copy's bytes
+            mbar_init(&empty[i], 8);   // one arrival per warp
+        }
+        fence_mbar_init();
+        abort_flag = 0;
+    }
+    __syncthreads();
+
+    // Warp 0: stage st into its buffer once the stage before it there has been released.
+    auto issue = [&](int st) -> bool {
+        const int i = st % kPassDepth;
+        if (st >= kPassDepth && !warp_wait_or_abort(&empty[i], (uint32_t)(st / kPassDepth - 1) & 1u, abort, budget))
+            return false;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&full[i], kPassBufB);
+            tma_load_3d(smem + i * kPassBufB, &tm_x, cbase, (int)(t_begin + (int64_t)st * kPassTokens - 3), 0,
+                        &full[i]);
+        }
+        return true;
+    };
+
+    const int cg = lane, tg = warp;
+    const int c0 = cbase + 8 * cg;
+    const bool live = c0 < p.conv_C;
     const int hk = p.h_qk * kDK;
-    IO *dst;
-    int64_t stride;
-    if (c0 < hk) { dst = static_cast<IO *>(p.cq) + c0; stride = hk; }
-    else if (c0 < 2 * hk) { dst = static_cast<IO *>(p.ck) + (c0 - hk); stride = hk; }
-    else { dst = static_cast<IO *>(p.cv) + (c0 - 2 * hk); stride = (int64_t)p.h_v * kDK; }
+    IO *dst = nullptr;
+    int64_t stride = 0;
+    ConvTaps taps = {};
+    if (live) {
+        if (c0 < hk) { dst = static_cast<IO *>(p.cq) + c0; stride = hk; }
+        else if (c0 < 2 * hk) { dst = static_cast<IO *>(p.ck) + (c0 - hk); stride = hk; }
+        else { dst = static_cast<IO *>(p.cv) + (c0 - 2 * hk); stride = (int64_t)p.h_v * kDK; }
+        taps = conv_taps<IO>(p, c0);
+    }
     // The sequence of token t: batched, t / seqlen; packed, the last n with cu[n] <= t.
     auto seq_of = [&](int64_t t, int64_t &n, int64_t &ts, int64_t &te) {
         if (p.cu_seqlens == nullptr) {
@@ -2471,26 +2525,69 @@ __global__ void __launch_bounds__(256, 2) conv_pass(const __grid_constant__ TcPa
         }
         return seq_range(p.cu_seqlens, p.seqlen, p.num_seqs, p.status, n, ts, te);
     };
-    const ConvTaps taps = conv_taps<IO>(p, c0);
-    int64_t n = -1, ts = 0, te = 0;
-#pragma unroll 1
-    for (int64_t t0 = r0; t0 < r0 + kConvRun && t0 < T; t0 += 4) {
-        if (t0 >= te && !seq_of(t0, n, ts, te)) return;
-        const int64_t tl = t0 + 3 < T ? t0 + 3 : T - 1;   // the last token of these four
-        if (tl < te) {
-            conv4<IO>(p, taps, n, ts, te, t0, c0, [&](int e, const uint4 &u) {
-                if (t0 + e < te) *reinterpret_cast<uint4 *>(dst + (size_t)(t0 + e) * stride) = u;
-            });
-            if (te - 1 >= t0 && te - 1 <= t0 + 3) conv_state_group<IO>(p, n, ts, te, c0);
-            continue;
+
+    int issued = 0;   // warp 0: stages issued so far
+    bool ok = true, bad = !live;
+    if (warp == 0) {
+        if (lane == 0) tma_prefetch_desc(&tm_x);
+        for (; issued < kPassDepth - 1 && issued < nstage; ++issued) issue(issued);
+    }
+    int64_t n = -1, ts = 0, te = 0;   // the sequence of the tokens at hand
+    for (int st = 0; st < nstage; ++st) {
+        if (warp == 0 && issued < nstage) {
+            if (!issue(issued)) ok = false;
+            else ++issued;
         }
-        for (int e = 0; e < 4 && t0 + e < T; ++e) {
-            const int64_t t = t0 + e;
-            if (t >= te && !seq_of(t, n, ts, te)) return;
-            conv4<IO>(p, taps, n, ts, te, t, c0, [&](int e2, const uint4 &u) {
-                if (e2 == 0) *reinterpret_cast<uint4 *>(dst + (size_t)t * stride) = u;
-            });
-            if (t == te - 1) conv_state_group<IO>(p, n, ts, te, c0);
+        if (ok && !warp_wait_or_abort(&full[st % kPassDepth], (uint32_t)(st / kPassDepth) & 1u, abort, budget))
+            ok = false;
+        if (!ok) break;
+        // Buffer row r holds token s0 - 3 + r.
+        const unsigned char *buf = smem + (st % kPassDepth) * kPassBufB;
+        const int64_t s0 = t_begin + (int64_t)st * kPassTokens;
+        const int64_t t0 = s0 + 4 * tg;
+        auto srow = [&](int64_t pos) {
+            return *reinterpret_cast<const uint4 *>(buf + (int)(pos - s0 + 3) * kPassRowB + cg * 16);
+        };
+        if (!bad && t0 < t_end) {
+            if (t0 >= te && !seq_of(t0, n, ts, te)) bad = true;
+        }
+        if (!bad && t0 < t_end) {
+            if (t0 - 3 >= ts && t0 + 3 < te && t0 + 3 < t_end) {
+                conv4<IO>(p, taps, t0, srow, [&](int e, const uint4 &u) {
+                    *reinterpret_cast<uint4 *>(dst + (size_t)(t0 + e) * stride) = u;
+                });
+                if (te - 1 == t0 + 3) conv_state_group<IO>(p, n, ts, te, c0);
+            } else {
+                for (int e = 0; e < 4 && !bad; ++e) {
+                    const int64_t t = t0 + e;
+                    if (t >= t_end) break;
+                    if (t >= te && !seq_of(t, n, ts, te)) {
+                        bad = true;
+                        break;
+                    }
+                    // Rows before the sequence's first token: its past conv state.
+                    auto row = [&](int64_t pos) -> uint4 {
+                        if (pos >= ts) return srow(pos);
+                        const int64_t r = (p.conv_k - 1) + (pos - ts);
+                        if (p.conv_in == nullptr || r < 0) return make_uint4(0, 0, 0, 0);
+                        return *reinterpret_cast<const uint4 *>(static_cast<const IO *>(p.conv_in) +
+                                                                ((size_t)n * (p.conv_k - 1) + r) * p.conv_C + c0);
+                    };
+                    *reinterpret_cast<uint4 *>(dst + (size_t)t * stride) = conv1<IO>(p, taps, t, row);
+                    if (t == te - 1) conv_state_group<IO>(p, n, ts, te, c0);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st % kPassDepth]);
+    }
+    if (!ok) {
+        if (tid == 0) atomicOr(p.status, kDevTimeout);
+        if (warp == 0) {
+            // Let the copies this CTA issued land before it exits: the latest phase of
+            // each buffer's `full` barrier.
+            for (int s2 = issued - kPassDepth < 0 ? 0 : issued - kPassDepth; s2 < issued; ++s2)
+                mbar_wait(&full[s2 % kPassDepth], (uint32_t)(s2 / kPassDepth) & 1u, kWaitBudget);
         }
     }
 }
@@ -3217,11 +3314,19 @@ cudaError_t launch_prefill_tc(const ScanParams &p, gdn_dtype io, int64_t total_t
         }
     }
     if (conv_pass_first) {
-        const dim3 grid((unsigned)((tp.conv_C / 8 + 31) / 32),
-                        (unsigned)((total_tokens + 8 * kConvRun - 1) / (8 * kConvRun)));
-        if (io == GDN_BF16) conv_pass<__nv_bfloat16><<<grid, 256, 0, stream>>>(tp);
-        else conv_pass<__half><<<grid, 256, 0, stream>>>(tp);
-        cudaError_t ce = cudaGetLastError();
+        // x [tokens][C] as a 3-D map (the third extent 1), one stage box of 256 x 35.
+        CUtensorMap tm_x;
+        const uint64_t dims[3] = {(uint64_t)tp.conv_C, (uint64_t)total_tokens, 1};
+        const uint64_t strides[2] = {(uint64_t)tp.conv_C * 2, (uint64_t)tp.conv_C * 2 * (uint64_t)total_tokens};
+        const uint32_t box[3] = {(uint32_t)kPassWidth, (uint32_t)kPassRows, 1};
+        if (!encode_map_3d(&tm_x, tp.cx, io, dims, strides, box)) return cudaErrorInvalidValue;
+        const dim3 grid((unsigned)((tp.conv_C + kPassWidth - 1) / kPassWidth),
+                        (unsigned)((total_tokens + kPassChunk - 1) / kPassChunk));
+        auto kern = io == GDN_BF16 ? conv_pass<__nv_bfloat16> : conv_pass<__half>;
+        cudaError_t ce = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassSmem);
+        if (ce != cudaSuccess) return ce;
+        kern<<<grid, 256, kPassSmem, stream>>>(tp, tm_x);
+        ce = cudaGetLastError();
         if (ce != cudaSuccess) return ce;
     }
     // The launches' parameters, taken once every field is set (the time-parallel branch
