@@ -147,3 +147,43 @@ def test_short_wait_budget_times_out_the_per_key_prep_then_recovers():
     o_ref, s_ref = oracle.scan_inputs(inp)
     check(inp, o.float().cpu().numpy().reshape(-1, 2, 128), s.cpu().numpy(), o_ref, s_ref,
           what="per-key prefill after a timed-out call")
+
+
+@pytest.mark.gpu
+def test_short_wait_budget_times_out_the_layer_conv_pass_then_recovers():
+    """gdn_prefill_layer in its default form: the conv pass waits for each TMA stage of x
+    under the same budget (a 17.5 KB copy takes longer than 200 cycles even from L2), then
+    the prep and the scan do.  The CTAs give up, let the copies they issued land and
+    report GDN_ERR_TIMEOUT; the next call repeats the one made before the timeout bit for
+    bit, outputs and both states."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from recurrent_state_scan_gb300 import gdn, gdn_last_device_status, gdn_prefill_layer
+    s = workloads.PrefillLayerSpec(name="t", io="bf16", h_qk=2, h_v=4, seed=711,
+                                   lengths=(300, 0, 130, 1))
+    inp = workloads.draw_prefill_layer(s)
+    d = lambda t: None if t is None else t.cuda()
+    cu = torch.tensor(inp.cu_seqlens, dtype=torch.int32, device="cuda")
+
+    def call():
+        out = gdn_prefill_layer(d(inp.x), d(inp.w), d(inp.bias), d(inp.conv_state), d(inp.a),
+                                d(inp.b), d(inp.A_log), d(inp.dt_bias), d(inp.state_in), cu,
+                                d(inp.norm_scale), d(inp.gate), h_qk=s.h_qk, h_v=s.h_v,
+                                scale=inp.scale, conv_activation="silu" if s.silu else "none",
+                                norm_activation=s.activation, eps=s.eps)
+        torch.cuda.synchronize()
+        return out
+
+    before = call()
+    assert gdn_last_device_status() == gdn.GDN_OK
+    gdn.gdn_set_wait_budget(200)
+    try:
+        call()
+        assert gdn_last_device_status() == gdn.GDN_ERR_TIMEOUT
+    finally:
+        gdn.gdn_set_wait_budget(0)
+    assert gdn_last_device_status() == gdn.GDN_OK
+    after = call()
+    assert gdn_last_device_status() == gdn.GDN_OK
+    for b, a in zip(before, after):
+        assert torch.equal(b, a)
